@@ -1,0 +1,187 @@
+"""Float64 CPU oracle for causal kernelized (linear) attention, phi = elu + 1.
+
+TEST INFRASTRUCTURE, NOT PRODUCT CODE.  Only ``tests/``, the smoke check in
+``__graft_entry__`` and the benchmark's CPU-baseline / reference arm may import
+this package.  It shares no code with the CUDA library and never imports it.
+
+The arithmetic lives in ``la_oracle.c`` (plain double-precision loops, one
+(batch, head) sequence at a time, OpenMP across sequences).  This module only
+compiles it with gcc and marshals numpy arrays through ctypes.
+
+Inputs may be float64, float32, or uint16 arrays holding bf16 bit patterns;
+they are widened exactly inside the C code.  Shapes: q, k [..., N, dk],
+v [..., N, dv] with identical leading dims; outputs are float64.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "la_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liblaoracle.so")
+_lock = threading.Lock()
+_lib = None
+
+_TYPE_CODE = {np.dtype(np.float64): 0, np.dtype(np.float32): 1, np.dtype(np.uint16): 2}
+
+
+def build(force: bool = False, out_path: str = _LIB_PATH, defines=()) -> str:
+    """Compile la_oracle.c into a shared library (gcc, -O3, no fast-math).
+
+    ``-ffp-contract=off`` keeps results identical on x86-64 and aarch64 (no
+    fused multiply-add contraction).  ``defines`` is for tests that compile a
+    deliberately wrong variant to show the pins catch it.
+    """
+    if not force and not defines and os.path.exists(out_path) and \
+            os.path.getmtime(out_path) >= os.path.getmtime(_SRC):
+        return out_path
+    cmd = ["gcc", "-O3", "-ffp-contract=off", "-fno-fast-math", "-fopenmp", "-fPIC",
+           "-shared", "-std=c11", "-Wall", "-Wno-unknown-pragmas", _SRC, "-o", out_path, "-lm"]
+    cmd[1:1] = ["-D" + d for d in defines]
+    tmp = out_path + ".tmp%d" % os.getpid()
+    cmd[cmd.index(out_path)] = tmp
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, out_path)
+    return out_path
+
+
+def _declare(lib):
+    P, I, D = ctypes.c_void_p, ctypes.c_int, ctypes.c_double
+    sigs = {
+        "la_oracle_phi": ([D], D),
+        "la_oracle_causal_recurrent": ([P, P, P, I, P, I, I, I, I, D], None),
+        "la_oracle_causal_chunked": ([P, P, P, I, P, I, I, I, I, I, D], None),
+        "la_oracle_causal_quadratic": ([P, P, P, I, P, I, I, I, I, D], None),
+        "la_oracle_prefill_state": ([P, P, I, P, P, I, I, I, I], None),
+        "la_oracle_noncausal": ([P, P, P, I, P, I, I, I, I, D], None),
+        "la_oracle_noncausal_pairwise": ([P, P, P, I, P, I, I, I, I, D], None),
+        "la_oracle_decode_step": ([P, P, P, P, P, I, P, I, I, I, D], None),
+        "la_oracle_num_threads": ([], I),
+    }
+    for name, (args, res) in sigs.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    return lib
+
+
+def load(path: str = None):
+    """Build (if needed) and load the oracle library; returns the ctypes handle."""
+    global _lib
+    if path is not None:
+        return _declare(ctypes.CDLL(path))
+    with _lock:
+        if _lib is None:
+            _lib = _declare(ctypes.CDLL(build()))
+    return _lib
+
+
+def _prep(*arrays):
+    t = None
+    out = []
+    for a in arrays:
+        a = np.ascontiguousarray(a)
+        if a.dtype not in _TYPE_CODE:
+            a = np.ascontiguousarray(a, dtype=np.float64)
+        if t is None:
+            t = a.dtype
+        elif a.dtype != t:
+            raise TypeError("q, k, v must share one element type")
+        out.append(a)
+    return out, _TYPE_CODE[t]
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+class Oracle:
+    """Bound oracle functions; ``lib`` may be a deliberately wrong test build."""
+
+    def __init__(self, lib=None):
+        self.lib = lib if lib is not None else load()
+
+    def phi(self, x: float) -> float:
+        return self.lib.la_oracle_phi(float(x))
+
+    def num_threads(self) -> int:
+        return self.lib.la_oracle_num_threads()
+
+    def _fwd(self, fname, q, k, v, eps, *extra):
+        (q, k, v), t = _prep(q, k, v)
+        N, dk = q.shape[-2], q.shape[-1]
+        dv = v.shape[-1]
+        lead = q.shape[:-2]
+        if k.shape != q.shape or v.shape[:-1] != q.shape[:-1]:
+            raise ValueError("shape mismatch")
+        BH = int(np.prod(lead)) if lead else 1
+        o = np.empty(lead + (N, dv), dtype=np.float64)
+        if BH and N and dv:
+            fn = getattr(self.lib, fname)
+            if extra:
+                fn(_ptr(q), _ptr(k), _ptr(v), t, _ptr(o), BH, N, dk, dv, *extra, float(eps))
+            else:
+                fn(_ptr(q), _ptr(k), _ptr(v), t, _ptr(o), BH, N, dk, dv, float(eps))
+        return o
+
+    def causal_recurrent(self, q, k, v, eps=1e-6):
+        return self._fwd("la_oracle_causal_recurrent", q, k, v, eps)
+
+    def causal_chunked(self, q, k, v, chunk, eps=1e-6):
+        return self._fwd("la_oracle_causal_chunked", q, k, v, eps, int(chunk))
+
+    def causal_quadratic(self, q, k, v, eps=1e-6):
+        return self._fwd("la_oracle_causal_quadratic", q, k, v, eps)
+
+    def noncausal(self, q, k, v, eps=1e-6):
+        return self._fwd("la_oracle_noncausal", q, k, v, eps)
+
+    def noncausal_pairwise(self, q, k, v, eps=1e-6):
+        return self._fwd("la_oracle_noncausal_pairwise", q, k, v, eps)
+
+    def prefill_state(self, k, v):
+        """S [..., dk, dv] and z [..., dk] summed over all N tokens."""
+        (k, v), t = _prep(k, v)
+        N, dk, dv = k.shape[-2], k.shape[-1], v.shape[-1]
+        lead = k.shape[:-2]
+        BH = int(np.prod(lead)) if lead else 1
+        S = np.zeros(lead + (dk, dv), dtype=np.float64)
+        z = np.zeros(lead + (dk,), dtype=np.float64)
+        if BH:
+            self.lib.la_oracle_prefill_state(_ptr(k), _ptr(v), t, _ptr(S), _ptr(z), BH, N, dk, dv)
+        return S, z
+
+    def decode_step(self, S, z, q, k, v, eps=1e-6):
+        """One step for every head: updates float64 S [...,dk,dv], z [...,dk] in place.
+
+        q, k [..., dk], v [..., dv]; returns o [..., dv] float64.
+        """
+        if S.dtype != np.float64 or z.dtype != np.float64 or not S.flags.c_contiguous \
+                or not z.flags.c_contiguous:
+            raise TypeError("S and z must be C-contiguous float64 (updated in place)")
+        (q, k, v), t = _prep(q, k, v)
+        dk, dv = q.shape[-1], v.shape[-1]
+        lead = q.shape[:-1]
+        BH = int(np.prod(lead)) if lead else 1
+        if S.shape != lead + (dk, dv) or z.shape != lead + (dk,):
+            raise ValueError("state shape mismatch")
+        o = np.empty(lead + (dv,), dtype=np.float64)
+        if BH:
+            self.lib.la_oracle_decode_step(_ptr(S), _ptr(z), _ptr(q), _ptr(k), _ptr(v), t,
+                                           _ptr(o), BH, dk, dv, float(eps))
+        return o
+
+
+_default = None
+
+
+def get() -> Oracle:
+    global _default
+    if _default is None:
+        _default = Oracle()
+    return _default

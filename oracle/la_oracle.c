@@ -1,0 +1,372 @@
+/*
+ * Float64 CPU oracle for causal kernelized (linear) attention, phi(x)=elu(x)+1.
+ *
+ * TEST INFRASTRUCTURE, NOT PRODUCT CODE.  Only the tests, the smoke check and
+ * the benchmark's CPU-baseline / reference arm may load or run this library.
+ * It shares no code, header, table or helper with the CUDA path.
+ *
+ * Plain loops in double precision, one (batch, head) sequence at a time; the
+ * only parallelism is OpenMP across independent (b,h) sequences, which does not
+ * change any result.  Every form below follows one passage of the pages:
+ *
+ *   [wiki]     "Linear Attention", aiwiki.thehackersbrain.dev
+ *   [learn]    "Linear attention", learn.pranaymahendrakar.com
+ *   [problems] "26. Linear (Kernelized) Attention: A Softmax-Free Alternative"
+ *   [mlblogg]  "Linear attention: change the order.", mlblogg.com
+ *   [math]     "Linear Attention -- Math + Variants", aicassindra.com
+ *
+ * Readings taken where the pages differ or are silent:
+ *   - normaliser: o = num / max(den, eps) (the clamp of the [wiki] chunked
+ *     listing); the "+1e-6" of [learn]/[problems] and "clip(1e-8)" of [mlblogg]
+ *     agree with it to < 1e-7 relative whenever den >> eps;
+ *   - phi(x) = x + 1 for x > 0, exp(x) otherwise: elu with alpha = 1 plus one,
+ *     written in the overflow-free way of the [mlblogg] implementation section;
+ *   - causality is inclusive (token i sees keys j <= i): update, then read
+ *     ([mlblogg] "The causal recurrence"; [learn] Developer listing);
+ *   - no 1/sqrt(d) scaling of q or k (only softmax scales, [math]);
+ *   - state and all arithmetic in double; inputs are given as float64,
+ *     float32 or bf16 bit patterns and widened exactly.
+ *
+ * Tensor layouts (row-major, contiguous):
+ *   q, k [BH, N, dk];  v, o [BH, N, dv];  S [BH, dk, dv];  z [BH, dk].
+ * Input element type code: 0 = float64, 1 = float32, 2 = bf16 (uint16 bits).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORACLE_F64 0
+#define ORACLE_F32 1
+#define ORACLE_BF16 2
+
+/* Read element i of an input array of the given type as a double. */
+static double load(const void *p, int type, int64_t i)
+{
+    if (type == ORACLE_F64)
+        return ((const double *)p)[i];
+    if (type == ORACLE_F32)
+        return (double)((const float *)p)[i];
+    /* bf16: the upper 16 bits of an IEEE binary32 */
+    uint32_t bits = ((uint32_t)((const uint16_t *)p)[i]) << 16;
+    float f;
+    memcpy(&f, &bits, sizeof f);
+    return (double)f;
+}
+
+/* phi(x) = elu(x) + 1 with alpha = 1 ([math] "Linear Transformer: elu+1";
+ * [wiki] listing applies F.elu then adds one; [mlblogg] writes the same map as
+ * where(x >= 0, x + 1, exp(min(x, 0)))).  Both branches give 1 at x = 0. */
+double la_oracle_phi(double x)
+{
+    return x > 0.0 ? x + 1.0 : exp(x);
+}
+
+static double clamp_den(double den, double eps)
+{
+    return den > eps ? den : eps;
+}
+
+/* phi of row t of a [N, d] slice starting at element `base`. */
+static void phi_row(const void *x, int type, int64_t base, int t, int d, double *out)
+{
+    for (int c = 0; c < d; ++c)
+        out[c] = la_oracle_phi(load(x, type, base + (int64_t)t * d + c));
+}
+
+/* ---------------------------------------------------------------------------
+ * Causal recurrence, token by token: the defining form.
+ * [learn] Researcher "Derivation": S_i = S_{i-1} + phi(k_i) v_i^T,
+ * z_i = z_{i-1} + phi(k_i), o_i = S_i^T phi(q_i) / z_i^T phi(q_i);
+ * [problems] Step-by-Step steps 2-5 (state update before the read).
+ * ------------------------------------------------------------------------- */
+void la_oracle_causal_recurrent(const void *q, const void *k, const void *v, int type,
+                                double *o, int BH, int N, int dk, int dv, double eps)
+{
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int bh = 0; bh < BH; ++bh) {
+        double *S = calloc((size_t)dk * dv, sizeof(double));
+        double *z = calloc((size_t)dk, sizeof(double));
+        double *fq = malloc(sizeof(double) * dk);
+        double *fk = malloc(sizeof(double) * dk);
+        double *vt = malloc(sizeof(double) * dv);
+        const int64_t qb = (int64_t)bh * N * dk, vb = (int64_t)bh * N * dv;
+        for (int t = 0; t < N; ++t) {
+            phi_row(q, type, qb, t, dk, fq);
+            phi_row(k, type, qb, t, dk, fk);
+            for (int c = 0; c < dv; ++c)
+                vt[c] = load(v, type, vb + (int64_t)t * dv + c);
+            /* S += phi(k_t) v_t^T ; z += phi(k_t) */
+            for (int r = 0; r < dk; ++r) {
+                double *Sr = S + (size_t)r * dv;
+                for (int c = 0; c < dv; ++c)
+                    Sr[c] += fk[r] * vt[c];
+                z[r] += fk[r];
+            }
+            /* o_t = phi(q_t)^T S / max(phi(q_t)^T z, eps) */
+            double den = 0.0;
+            for (int r = 0; r < dk; ++r)
+                den += fq[r] * z[r];
+            double *ot = o + vb + (int64_t)t * dv;
+            for (int c = 0; c < dv; ++c)
+                ot[c] = 0.0;
+            for (int r = 0; r < dk; ++r) {
+                const double *Sr = S + (size_t)r * dv;
+                for (int c = 0; c < dv; ++c)
+                    ot[c] += fq[r] * Sr[c];
+            }
+            den = clamp_den(den, eps);
+            for (int c = 0; c < dv; ++c)
+                ot[c] /= den;
+        }
+        free(S); free(z); free(fq); free(fk); free(vt);
+    }
+}
+
+/* ---------------------------------------------------------------------------
+ * Chunked parallel form ([wiki] listing "linear_attention_chunked"): for each
+ * chunk, inter = phi(Q_c) state_before, intra = tril(phi(Q_c) phi(K_c)^T) V_c,
+ * denominator = phi(Q_c) z_before + row sums of the masked scores, then the
+ * state and z absorb the chunk.  The last chunk may be shorter than `chunk`.
+ * ------------------------------------------------------------------------- */
+void la_oracle_causal_chunked(const void *q, const void *k, const void *v, int type,
+                              double *o, int BH, int N, int dk, int dv, int chunk,
+                              double eps)
+{
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int bh = 0; bh < BH; ++bh) {
+        double *state = calloc((size_t)dk * dv, sizeof(double));
+        double *z = calloc((size_t)dk, sizeof(double));
+        double *fq = malloc(sizeof(double) * dk);
+        double *fkj = malloc(sizeof(double) * dk);
+        double *num = malloc(sizeof(double) * dv);
+        const int64_t qb = (int64_t)bh * N * dk, vb = (int64_t)bh * N * dv;
+        for (int i0 = 0; i0 < N; i0 += chunk) {
+            int len = N - i0 < chunk ? N - i0 : chunk;
+            for (int a = 0; a < len; ++a) {
+                phi_row(q, type, qb, i0 + a, dk, fq);
+                /* inter: phi(q) @ state (state holds earlier chunks only) */
+                for (int c = 0; c < dv; ++c) {
+                    double s = 0.0;
+                    for (int r = 0; r < dk; ++r)
+                        s += fq[r] * state[(size_t)r * dv + c];
+                    num[c] = s;
+                }
+                double den = 0.0;
+                for (int r = 0; r < dk; ++r)
+                    den += fq[r] * z[r];
+                /* intra: masked scores, keys b <= a of this chunk */
+                for (int b = 0; b <= a; ++b) {
+                    phi_row(k, type, qb, i0 + b, dk, fkj);
+                    double s = 0.0;
+                    for (int r = 0; r < dk; ++r)
+                        s += fq[r] * fkj[r];
+                    for (int c = 0; c < dv; ++c)
+                        num[c] += s * load(v, type, vb + (int64_t)(i0 + b) * dv + c);
+                    den += s;
+                }
+                den = clamp_den(den, eps);
+                for (int c = 0; c < dv; ++c)
+                    o[vb + (int64_t)(i0 + a) * dv + c] = num[c] / den;
+            }
+            /* state += phi(K_c)^T V_c ; z += column sums of phi(K_c) */
+            for (int b = 0; b < len; ++b) {
+                phi_row(k, type, qb, i0 + b, dk, fkj);
+                for (int r = 0; r < dk; ++r) {
+                    for (int c = 0; c < dv; ++c)
+                        state[(size_t)r * dv + c] +=
+                            fkj[r] * load(v, type, vb + (int64_t)(i0 + b) * dv + c);
+                    z[r] += fkj[r];
+                }
+            }
+        }
+        free(state); free(z); free(fq); free(fkj); free(num);
+    }
+}
+
+/* ---------------------------------------------------------------------------
+ * Masked quadratic form ([learn] Developer listing, part 3; [problems] Key
+ * Functions, the directly-masked score matrix): scores = phi(Q) phi(K)^T kept
+ * for j <= i, o = scores V / row sums.  O(N^2): cross-check only.
+ * ------------------------------------------------------------------------- */
+void la_oracle_causal_quadratic(const void *q, const void *k, const void *v, int type,
+                                double *o, int BH, int N, int dk, int dv, double eps)
+{
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int bh = 0; bh < BH; ++bh) {
+        double *fq = malloc(sizeof(double) * dk);
+        double *fk = malloc(sizeof(double) * dk);
+        const int64_t qb = (int64_t)bh * N * dk, vb = (int64_t)bh * N * dv;
+        for (int i = 0; i < N; ++i) {
+            phi_row(q, type, qb, i, dk, fq);
+            double *oi = o + vb + (int64_t)i * dv;
+            for (int c = 0; c < dv; ++c)
+                oi[c] = 0.0;
+            double rowsum = 0.0;
+            for (int j = 0; j <= i; ++j) {
+                phi_row(k, type, qb, j, dk, fk);
+                double s = 0.0;
+                for (int r = 0; r < dk; ++r)
+                    s += fq[r] * fk[r];
+                rowsum += s;
+                for (int c = 0; c < dv; ++c)
+                    oi[c] += s * load(v, type, vb + (int64_t)j * dv + c);
+            }
+            rowsum = clamp_den(rowsum, eps);
+            for (int c = 0; c < dv; ++c)
+                oi[c] /= rowsum;
+        }
+        free(fq); free(fk);
+    }
+}
+
+/* ---------------------------------------------------------------------------
+ * Final state of a prefix: S = sum_t phi(k_t) v_t^T, z = sum_t phi(k_t) over
+ * all N tokens ([math] "The quadratic wall": S and z; [problems] step 3).
+ * ------------------------------------------------------------------------- */
+void la_oracle_prefill_state(const void *k, const void *v, int type, double *S, double *z,
+                             int BH, int N, int dk, int dv)
+{
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int bh = 0; bh < BH; ++bh) {
+        double *Sb = S + (size_t)bh * dk * dv;
+        double *zb = z + (size_t)bh * dk;
+        double *fk = malloc(sizeof(double) * dk);
+        const int64_t kb = (int64_t)bh * N * dk, vb = (int64_t)bh * N * dv;
+        for (size_t e = 0; e < (size_t)dk * dv; ++e)
+            Sb[e] = 0.0;
+        for (int r = 0; r < dk; ++r)
+            zb[r] = 0.0;
+        for (int t = 0; t < N; ++t) {
+            phi_row(k, type, kb, t, dk, fk);
+            for (int r = 0; r < dk; ++r) {
+                for (int c = 0; c < dv; ++c)
+                    Sb[(size_t)r * dv + c] += fk[r] * load(v, type, vb + (int64_t)t * dv + c);
+                zb[r] += fk[r];
+            }
+        }
+        free(fk);
+    }
+}
+
+/* ---------------------------------------------------------------------------
+ * Non-causal associative form ([mlblogg] "An implementation you can check":
+ * state = phi(K)^T V, normalizer = sum phi(K), o = phi(Q) state / phi(Q) normalizer;
+ * [math] o_i = phi(q_i)^T S / phi(q_i)^T z with S, z summed over all j).
+ * ------------------------------------------------------------------------- */
+void la_oracle_noncausal(const void *q, const void *k, const void *v, int type,
+                         double *o, int BH, int N, int dk, int dv, double eps)
+{
+    double *S = malloc(sizeof(double) * (size_t)BH * dk * dv);
+    double *z = malloc(sizeof(double) * (size_t)BH * dk);
+    la_oracle_prefill_state(k, v, type, S, z, BH, N, dk, dv);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int bh = 0; bh < BH; ++bh) {
+        const double *Sb = S + (size_t)bh * dk * dv;
+        const double *zb = z + (size_t)bh * dk;
+        double *fq = malloc(sizeof(double) * dk);
+        const int64_t qb = (int64_t)bh * N * dk, vb = (int64_t)bh * N * dv;
+        for (int i = 0; i < N; ++i) {
+            phi_row(q, type, qb, i, dk, fq);
+            double den = 0.0;
+            for (int r = 0; r < dk; ++r)
+                den += fq[r] * zb[r];
+            den = clamp_den(den, eps);
+            double *oi = o + vb + (int64_t)i * dv;
+            for (int c = 0; c < dv; ++c) {
+                double s = 0.0;
+                for (int r = 0; r < dk; ++r)
+                    s += fq[r] * Sb[(size_t)r * dv + c];
+                oi[c] = s / den;
+            }
+        }
+        free(fq);
+    }
+    free(S); free(z);
+}
+
+/* ---------------------------------------------------------------------------
+ * Brute-force pairwise non-causal form ([mlblogg] check: pairwise =
+ * phi(q) phi(k)^T, reference = pairwise v / row sums).  O(N^2): cross-check.
+ * ------------------------------------------------------------------------- */
+void la_oracle_noncausal_pairwise(const void *q, const void *k, const void *v, int type,
+                                  double *o, int BH, int N, int dk, int dv, double eps)
+{
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int bh = 0; bh < BH; ++bh) {
+        double *fq = malloc(sizeof(double) * dk);
+        double *fk = malloc(sizeof(double) * dk);
+        const int64_t qb = (int64_t)bh * N * dk, vb = (int64_t)bh * N * dv;
+        for (int i = 0; i < N; ++i) {
+            phi_row(q, type, qb, i, dk, fq);
+            double *oi = o + vb + (int64_t)i * dv;
+            for (int c = 0; c < dv; ++c)
+                oi[c] = 0.0;
+            double rowsum = 0.0;
+            for (int j = 0; j < N; ++j) {
+                phi_row(k, type, qb, j, dk, fk);
+                double s = 0.0;
+                for (int r = 0; r < dk; ++r)
+                    s += fq[r] * fk[r];
+                rowsum += s;
+                for (int c = 0; c < dv; ++c)
+                    oi[c] += s * load(v, type, vb + (int64_t)j * dv + c);
+            }
+            rowsum = clamp_den(rowsum, eps);
+            for (int c = 0; c < dv; ++c)
+                oi[c] /= rowsum;
+        }
+        free(fq); free(fk);
+    }
+}
+
+/* ---------------------------------------------------------------------------
+ * One recurrent decode step for BH independent heads, state in place
+ * ([wiki] "It is a linear RNN": O(d^2) per token; [learn] Developer listing,
+ * part 2, loop body; [problems] steps 3-4).  q, k [BH, dk], v [BH, dv],
+ * S [BH, dk, dv] and z [BH, dk] double, o [BH, dv] double.
+ * ------------------------------------------------------------------------- */
+void la_oracle_decode_step(double *S, double *z, const void *q, const void *k,
+                           const void *v, int type, double *o, int BH, int dk, int dv,
+                           double eps)
+{
+#pragma omp parallel for schedule(static)
+    for (int bh = 0; bh < BH; ++bh) {
+        double *Sb = S + (size_t)bh * dk * dv;
+        double *zb = z + (size_t)bh * dk;
+        double *ob = o + (size_t)bh * dv;
+        double *fq = malloc(sizeof(double) * dk);
+        double *fk = malloc(sizeof(double) * dk);
+        for (int r = 0; r < dk; ++r) {
+            fq[r] = la_oracle_phi(load(q, type, (int64_t)bh * dk + r));
+            fk[r] = la_oracle_phi(load(k, type, (int64_t)bh * dk + r));
+        }
+        for (int r = 0; r < dk; ++r) {
+            for (int c = 0; c < dv; ++c)
+                Sb[(size_t)r * dv + c] += fk[r] * load(v, type, (int64_t)bh * dv + c);
+            zb[r] += fk[r];
+        }
+        double den = 0.0;
+        for (int r = 0; r < dk; ++r)
+            den += fq[r] * zb[r];
+        den = clamp_den(den, eps);
+        for (int c = 0; c < dv; ++c) {
+            double s = 0.0;
+            for (int r = 0; r < dk; ++r)
+                s += fq[r] * Sb[(size_t)r * dv + c];
+            ob[c] = s / den;
+        }
+        free(fq); free(fk);
+    }
+}
+
+/* Threads OpenMP will use (reported beside CPU timings). */
+int la_oracle_num_threads(void)
+{
+#ifdef _OPENMP
+    extern int omp_get_max_threads(void);
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}

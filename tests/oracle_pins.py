@@ -1,0 +1,276 @@
+"""Pins for the float64 oracle: checks against facts the pages and mathematics fix.
+
+Each ``pin_*`` function takes an ``oracle.Oracle`` and raises AssertionError on
+a violation.  ``test_oracle_pins.py`` runs them on the real oracle;
+``test_oracle_mutants.py`` runs them on builds with a planted mistake and
+requires that every such build fails at least one pin.
+
+None of these re-types the oracle's own loop: the references are exact
+rational arithmetic (fractions), a brute-force pairwise form written here with
+numpy, library routines (math.expm1), or identities the method must satisfy.
+"""
+from __future__ import annotations
+
+import math
+from fractions import Fraction
+
+import numpy as np
+
+import workloads
+
+EPS = 1e-6
+
+
+# ----------------------------------------------------------------------------
+# references written independently of the oracle
+# ----------------------------------------------------------------------------
+def elu_plus_one_ref(x: float) -> float:
+    """elu(x) + 1 with alpha = 1 via the library's expm1 (elu(x) = expm1(x) for x <= 0)."""
+    return (x if x > 0 else math.expm1(x)) + 1.0
+
+
+def phi_np(x: np.ndarray) -> np.ndarray:
+    x = np.asarray(x, dtype=np.float64)
+    return np.where(x > 0, x + 1.0, np.exp(np.minimum(x, 0.0)))
+
+
+def pairwise_bruteforce(q, k, v, causal: bool, eps: float = EPS) -> np.ndarray:
+    """Similarity-weighted average, general form sum_j sim(q_i,k_j) v_j / sum_j sim(q_i,k_j)
+    ("Linear attention", learn.pranaymahendrakar.com, Researcher: Derivation), with
+    sim = phi(q).phi(k); for causal, j <= i.  Dense N x N numpy, float64."""
+    fq, fk = phi_np(q), phi_np(k)
+    v = np.asarray(v, dtype=np.float64)
+    scores = fq @ np.swapaxes(fk, -1, -2)
+    if causal:
+        n = scores.shape[-1]
+        scores = scores * np.tril(np.ones((n, n)))
+    den = np.maximum(scores.sum(-1, keepdims=True), eps)
+    return (scores @ v) / den
+
+
+def exact_causal(qf, kf, v, causal=True):
+    """Exact rational o for inputs whose phi values are given as Fractions.
+
+    qf, kf: lists [N][d] of Fraction (already phi-mapped), v: [N][dv] Fraction.
+    """
+    N, dv = len(qf), len(v[0])
+    out = []
+    for i in range(N):
+        js = range(i + 1) if causal else range(N)
+        num = [Fraction(0)] * dv
+        den = Fraction(0)
+        for j in js:
+            s = sum(a * b for a, b in zip(qf[i], kf[j]))
+            den += s
+            for c in range(dv):
+                num[c] += s * v[j][c]
+        out.append([x / den for x in num])
+    return out
+
+
+def _rel_err(a, b):
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    return float(np.max(np.abs(a - b)) / max(np.max(np.abs(b)), 1e-300))
+
+
+def _rand(seed, BH, N, dk, dv, sigma=1.0):
+    q, k, v = workloads.random_inputs(seed, 1, BH, N, dk, dv, "f32", sigma)
+    return q[0].astype(np.float64), k[0].astype(np.float64), v[0].astype(np.float64)
+
+
+# ----------------------------------------------------------------------------
+# pins
+# ----------------------------------------------------------------------------
+def pin_phi_is_elu_plus_one(orc):
+    """phi = elu + 1 (alpha 1): matches expm1-based elu, is continuous at 0 and > 0."""
+    xs = [-50.0, -20.0, -3.5, -1.0, -0.25, -1e-9, 0.0, 1e-9, 0.3, 1.0, 2.5, 40.0]
+    for x in xs:
+        got, ref = orc.phi(x), elu_plus_one_ref(x)
+        assert abs(got - ref) <= 1e-15 * max(1.0, abs(ref)), (x, got, ref)
+        assert got > 0.0
+    assert orc.phi(0.0) == 1.0
+
+
+def pin_output0_equals_v0(orc):
+    """Position 0 returns v_0 for any q_0 ("26. Linear (Kernelized) Attention",
+    Step-by-Step step 6), as long as the denominator is above eps."""
+    rng = np.random.default_rng(123)
+    for scale in (1.0, 10.0, 30.0):
+        for dk, dv in ((3, 2), (8, 5), (32, 32)):
+            q = rng.standard_normal((2, 4, dk)) * scale
+            k = rng.standard_normal((2, 4, dk))
+            v = rng.standard_normal((2, 4, dv))
+            for o in (orc.causal_recurrent(q, k, v, EPS), orc.causal_chunked(q, k, v, 2, EPS),
+                      orc.causal_quadratic(q, k, v, EPS)):
+                den = (phi_np(q[:, 0]) * phi_np(k[:, 0])).sum(-1)
+                ok = den > EPS
+                assert np.all(np.abs(o[ok, 0] - v[ok, 0]) <= 1e-14 * (1 + np.abs(v[ok, 0]))), scale
+
+
+def pin_eps_clamp(orc):
+    """Below eps the denominator is clamped: o_0 = v_0 * den / eps (the clamp of the
+    chunked listing of "Linear Attention", aiwiki.thehackersbrain.dev)."""
+    q = np.full((1, 1, 4), -12.0)
+    k = np.full((1, 1, 4), -12.0)
+    v = np.array([[[0.5, -2.0, 3.0]]])
+    den = 4 * math.exp(-12.0) * math.exp(-12.0)   # ~1.5e-10 < eps
+    assert den < EPS
+    for o in (orc.causal_recurrent(q, k, v, EPS), orc.noncausal(q, k, v, EPS),
+              orc.causal_chunked(q, k, v, 1, EPS)):
+        ref = v[0, 0] * (den / EPS)
+        assert np.allclose(o[0, 0], ref, rtol=1e-12, atol=0), (o, ref)
+
+
+def pin_exact_rational(orc):
+    """Tiny inputs with q, k > 0 (phi = x + 1 is exact) against exact rational
+    arithmetic of the similarity-weighted form; dk != dv so a transposed or
+    mis-indexed operand changes the answer."""
+    rng = np.random.default_rng(5)
+    N, dk, dv = 7, 3, 4
+    qd = rng.integers(1, 9, size=(N, dk)) / 4.0     # positive dyadic values
+    kd = rng.integers(1, 9, size=(N, dk)) / 8.0
+    vd = rng.integers(-6, 7, size=(N, dv)) / 2.0
+    qf = [[Fraction(x) + 1 for x in row] for row in qd]
+    kf = [[Fraction(x) + 1 for x in row] for row in kd]
+    vf = [[Fraction(x) for x in row] for row in vd]
+    for causal in (True, False):
+        ref = np.array([[float(x) for x in row] for row in exact_causal(qf, kf, vf, causal)])
+        if causal:
+            outs = [orc.causal_recurrent(qd, kd, vd, EPS), orc.causal_quadratic(qd, kd, vd, EPS)]
+            outs += [orc.causal_chunked(qd, kd, vd, c, EPS) for c in (1, 2, 3, 7, 9)]
+        else:
+            outs = [orc.noncausal(qd, kd, vd, EPS), orc.noncausal_pairwise(qd, kd, vd, EPS)]
+        for o in outs:
+            assert np.allclose(o, ref, rtol=1e-14, atol=1e-14), (causal, np.max(np.abs(o - ref)))
+
+
+def pin_exact_rational_state(orc):
+    """Prefill state S = sum phi(k) v^T, z = sum phi(k) in exact arithmetic."""
+    rng = np.random.default_rng(6)
+    N, dk, dv = 5, 4, 3
+    kd = rng.integers(1, 9, size=(2, N, dk)) / 4.0
+    vd = rng.integers(-5, 6, size=(2, N, dv)) / 4.0
+    S, z = orc.prefill_state(kd, vd)
+    for b in range(2):
+        for r in range(dk):
+            zr = sum(Fraction(kd[b, t, r]) + 1 for t in range(N))
+            assert float(zr) == z[b, r]
+            for c in range(dv):
+                s = sum((Fraction(kd[b, t, r]) + 1) * Fraction(vd[b, t, c]) for t in range(N))
+                assert float(s) == S[b, r, c], (b, r, c)
+
+
+def pin_noncausal_equals_pairwise(orc):
+    """Non-causal associative form equals the brute-force pairwise form
+    ("Linear attention: change the order.", implementation you can check), both
+    against the numpy brute force here and the oracle's own pairwise form."""
+    for seed, (N, dk, dv) in enumerate(((1, 1, 1), (5, 3, 1), (17, 8, 3), (64, 3, 8), (33, 8, 8))):
+        q, k, v = _rand(100 + seed, 3, N, dk, dv)
+        ref = pairwise_bruteforce(q, k, v, causal=False)
+        assert _rel_err(orc.noncausal(q, k, v, EPS), ref) < 1e-12
+        assert _rel_err(orc.noncausal_pairwise(q, k, v, EPS), ref) < 1e-12
+
+
+def pin_causal_equals_masked_bruteforce(orc):
+    """Causal recurrence equals the masked quadratic form ("Linear attention",
+    Developer listing, part 3: the load-bearing check) on tiny inputs."""
+    for seed, (N, dk, dv) in enumerate(((1, 1, 1), (9, 3, 2), (40, 8, 3), (64, 5, 8))):
+        q, k, v = _rand(200 + seed, 2, N, dk, dv)
+        ref = pairwise_bruteforce(q, k, v, causal=True)
+        assert _rel_err(orc.causal_recurrent(q, k, v, EPS), ref) < 1e-12
+        assert _rel_err(orc.causal_quadratic(q, k, v, EPS), ref) < 1e-12
+
+
+def pin_chunked_equals_recurrent_every_chunk(orc):
+    """Chunked form equals the recurrence for every chunk size 1..N and beyond,
+    including non-divisors of N ("Linear Attention", chunked listing)."""
+    N = 37
+    q, k, v = _rand(300, 2, N, 6, 4)
+    ref = orc.causal_recurrent(q, k, v, EPS)
+    bf = pairwise_bruteforce(q, k, v, causal=True)
+    assert _rel_err(ref, bf) < 1e-12
+    for c in list(range(1, N + 1)) + [N + 5, 128]:
+        assert _rel_err(orc.causal_chunked(q, k, v, c, EPS), ref) < 1e-12, c
+
+
+def pin_convex_hull(orc):
+    """Non-negative weights: every o_i lies within [min_{j<=i} v_j, max_{j<=i} v_j]
+    per component ("Linear Attention": a weighted average with non-negative weights)."""
+    q, k, v = _rand(400, 3, 200, 8, 6, sigma=2.0)
+    o = orc.causal_recurrent(q, k, v, EPS)
+    lo = np.minimum.accumulate(v, axis=1)
+    hi = np.maximum.accumulate(v, axis=1)
+    tol = 1e-12 * (1 + np.abs(v).max())
+    assert np.all(o >= lo - tol) and np.all(o <= hi + tol)
+    on = orc.noncausal(q, k, v, EPS)
+    assert np.all(on >= v.min(axis=1, keepdims=True) - tol)
+    assert np.all(on <= v.max(axis=1, keepdims=True) + tol)
+
+
+def pin_constant_v(orc):
+    """Constant v = c gives o = c everywhere (weights sum to the denominator)."""
+    q, k, _ = _rand(500, 2, 50, 7, 3)
+    v = np.full((2, 50, 3), -1.75)
+    for o in (orc.causal_recurrent(q, k, v, EPS), orc.noncausal(q, k, v, EPS),
+              orc.causal_chunked(q, k, v, 16, EPS)):
+        assert np.allclose(o, -1.75, rtol=1e-13, atol=0)
+
+
+def pin_linear_in_v(orc):
+    """o is linear in v for fixed q, k."""
+    q, k, v1 = _rand(600, 2, 30, 5, 4)
+    _, _, v2 = _rand(601, 2, 30, 5, 4)
+    a, b = 0.75, -2.5
+    for f in (orc.causal_recurrent, orc.noncausal):
+        lhs = f(q, k, a * v1 + b * v2, EPS)
+        rhs = a * f(q, k, v1, EPS) + b * f(q, k, v2, EPS)
+        assert _rel_err(lhs, rhs) < 1e-12
+
+
+def pin_noncausal_permutation_invariant(orc):
+    """Non-causal o does not depend on the order of the (k, v) pairs."""
+    q, k, v = _rand(700, 2, 45, 6, 5)
+    perm = np.random.default_rng(7).permutation(45)
+    assert _rel_err(orc.noncausal(q, k[:, perm], v[:, perm], EPS), orc.noncausal(q, k, v, EPS)) < 1e-13
+
+
+def pin_last_causal_row_is_noncausal(orc):
+    """The last causal row sees every key, so it equals the non-causal row."""
+    q, k, v = _rand(800, 3, 60, 8, 4)
+    oc = orc.causal_recurrent(q, k, v, EPS)
+    on = orc.noncausal(q, k, v, EPS)
+    assert _rel_err(oc[:, -1], on[:, -1]) < 1e-13
+    # and the causal output depends on the sequence order (it is not the non-causal one)
+    assert _rel_err(oc[:, 0], on[:, 0]) > 1e-3
+
+
+def pin_decode_continues_causal(orc):
+    """Prefill state of the first P tokens, then single-token decode steps,
+    reproduces the causal forward of the whole sequence ("Linear Attention
+    -- Math + Variants": parallel form for training, recurrence for decoding)."""
+    BH, N, P, dk, dv = 3, 24, 10, 6, 5
+    q, k, v = _rand(900, BH, N, dk, dv)
+    full = orc.causal_recurrent(q, k, v, EPS)
+    S, z = orc.prefill_state(k[:, :P], v[:, :P])
+    for t in range(P, N):
+        o = orc.decode_step(S, z, q[:, t], k[:, t], v[:, t], EPS)
+        assert _rel_err(o, full[:, t]) < 1e-12, t
+    # after all steps the state is the prefill state of the whole sequence
+    S2, z2 = orc.prefill_state(k, v)
+    assert _rel_err(S, S2) < 1e-13 and _rel_err(z, z2) < 1e-13
+
+
+def pin_bf16_widening(orc):
+    """bf16 inputs are widened exactly: the oracle on bf16 bits equals the oracle
+    on the float64 values those bits denote."""
+    q, k, v = workloads.random_inputs(11, 1, 2, 20, 4, 3, "bf16")
+    qf, kf, vf = (workloads.bf16_bits_to_f32(x).astype(np.float64) for x in (q, k, v))
+    a = orc.causal_recurrent(q, k, v, EPS)
+    b = orc.causal_recurrent(qf, kf, vf, EPS)
+    assert np.array_equal(a, b)
+    ref = pairwise_bruteforce(qf[0], kf[0], vf[0], causal=True)
+    assert _rel_err(a[0], ref) < 1e-12
+
+
+ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

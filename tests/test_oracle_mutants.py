@@ -1,0 +1,66 @@
+"""Plant plausible mistakes in the oracle (on the CPU) and show the pins catch each.
+
+Each mutant is the oracle's C source with one textual edit, compiled to a
+temporary library.  A mutant that passes every pin would mean the pins are too
+weak to trust the oracle.
+"""
+import os
+
+import pytest
+
+import oracle
+from oracle_pins import ALL_PINS
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "la_oracle.c")
+
+MUTANTS = {
+    # phi without the +1 (plain elu: negative weights possible)
+    "phi_drops_plus_one": ("return x > 0.0 ? x + 1.0 : exp(x);", "return x > 0.0 ? x : exp(x) - 1.0;"),
+    # sign error in the exponential branch
+    "phi_wrong_sign": ("return x > 0.0 ? x + 1.0 : exp(x);", "return x > 0.0 ? x + 1.0 : exp(-x);"),
+    # recurrence: state built from phi(q) instead of phi(k)
+    "state_uses_q": ("Sr[c] += fk[r] * vt[c];", "Sr[c] += fq[r] * vt[c];"),
+    # recurrence: denominator from the current key only (dropped accumulation)
+    "den_drops_history": ("            double den = 0.0;\n            for (int r = 0; r < dk; ++r)\n                den += fq[r] * z[r];",
+                          "            double den = 0.0;\n            for (int r = 0; r < dk; ++r)\n                den += fq[r] * fk[r];"),
+    # clamp replaced by a floor of zero
+    "no_eps_clamp": ("return den > eps ? den : eps;", "return den > eps ? den : 0.0 * eps + den;"),
+    # chunked: transposed state read (dk != dv exposes it)
+    "chunked_transposed_state": ("s += fq[r] * state[(size_t)r * dv + c];",
+                                 "s += fq[r] * state[((size_t)c * dk + r) % ((size_t)dk * dv)];"),
+    # chunked: diagonal dropped from the intra-chunk mask (exclusive causality)
+    "chunked_exclusive_mask": ("for (int b = 0; b <= a; ++b) {", "for (int b = 0; b < a; ++b) {"),
+    # non-causal: denominator without the key sums
+    "noncausal_den_no_z": ("den += fq[r] * zb[r];\n            den = clamp_den(den, eps);\n            double *oi",
+                           "den += fq[r];\n            den = clamp_den(den, eps);\n            double *oi"),
+    # decode: normaliser accumulates phi(q)
+    "decode_z_uses_q": ("            zb[r] += fk[r];\n        }\n        double den",
+                        "            zb[r] += fq[r];\n        }\n        double den"),
+    # prefill: v index off by one token
+    "prefill_v_shifted": ("Sb[(size_t)r * dv + c] += fk[r] * load(v, type, vb + (int64_t)t * dv + c);",
+                          "Sb[(size_t)r * dv + c] += fk[r] * load(v, type, vb + (int64_t)((t + 1) % N) * dv + c);"),
+    # bf16 widening with the wrong shift
+    "bf16_wrong_shift": ("<< 16;", "<< 15;"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name, tmp_path):
+    old, new = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) >= 1, "mutation site vanished: " + name
+    mutated = src.replace(old, new, 1)
+    mpath = tmp_path / "la_oracle.c"
+    mpath.write_text(mutated)
+    lib_path = str(tmp_path / "libmutant.so")
+    import subprocess
+    subprocess.run(["gcc", "-O1", "-fopenmp", "-fPIC", "-shared", "-std=c11", "-w", str(mpath),
+                    "-o", lib_path, "-lm"], check=True)
+    orc = oracle.Oracle(oracle.load(lib_path))
+    failed = []
+    for pin in ALL_PINS:
+        try:
+            pin(orc)
+        except AssertionError:
+            failed.append(pin.__name__)
+    assert failed, "no pin caught mutant " + name
