@@ -1,0 +1,536 @@
+#!/usr/bin/env python
+"""Benchmark of the linear-attention library on one GB300 (or N replicas).
+
+Headline (the JSON line's `value`): causal chunked forward, bf16 in / fp32
+accumulate, B=4 H=8 N=2048 dk=dv=64, chunk 128, in tokens/s (B*N sequence
+positions per second; all heads of a position count once).  One step is one
+`la_forward_causal` over one batch.  Steps run from a CUDA graph; 16 input /
+output buffer sets are rotated (537 MB > 4x the 129 MB L2) so every step reads
+q, k, v from HBM.
+
+Also reported ("paths"): the long causal forward (B=1 H=32 N=65536 d=128),
+the non-causal forward (B=8 H=12 N=4096 d=64) and the decode step (128 x 32
+heads, d=128, fp32 state), each with its roofline fraction.
+
+`--impl reference` times the float64 CPU oracle (the only reference this
+method has) on a bounded sample of the same workload, on the host cores.
+
+Multi-GPU: each rank runs its own replica of the workload (independent (b,h)
+sequences: no collective on the data path); `value` is the work of all ranks
+divided by the slowest rank's time ("scaling": "weak").
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import io
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "causal linear-attn fwd tokens/s & TFLOP/s (%roofline); decode tokens/s (%HBM BW)"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_BYTES = 129 * 1024 * 1024
+
+
+# --------------------------------------------------------------------------- accounting
+def causal_flops(BH, N, dk, dv, chunk):
+    """Algorithmic flop (2 per MAC): masked half of each intra-chunk tile only,
+    BH*N*[(C+1)(dk+dv) + 4*dk*dv]."""
+    return float(BH) * N * ((chunk + 1) * (dk + dv) + 4 * dk * dv)
+
+
+def noncausal_flops(BH, N, dk, dv):
+    return float(BH) * N * (4 * dk * dv + 3 * dk + dv)
+
+
+def decode_flops_per_step(BH, dk, dv):
+    return float(BH) * (4 * dk * dv + 6 * dk)
+
+
+def forward_bytes(BH, N, dk, dv, elem):
+    """Read q, k, v once and write o once."""
+    return BH * N * (2 * dk + 2 * dv) * elem
+
+
+def decode_bytes_per_step(BH, dk, dv, elem):
+    """Read + write fp32 S and z, read q, k, v, write o."""
+    return BH * (8 * dk * dv + 8 * dk + (2 * dk + 2 * dv) * elem)
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained")}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def roofline(flops, nbytes, seconds, peaks, source, traffic=None, burst=True):
+    """Bound = the slower of flops at the bf16 dense peak and bytes at HBM bandwidth."""
+    tflops_peak = peaks["bf16_tflops"] if burst else peaks["bf16_tflops_sustained"]
+    t_mem = nbytes / (peaks["hbm_gbs"] * 1e9)
+    t_cmp = flops / (tflops_peak * 1e12)
+    if t_mem >= t_cmp:
+        achieved = nbytes / seconds / 1e9
+        r = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+             "frac": round(achieved / peaks["hbm_gbs"], 4)}
+    else:
+        achieved = flops / seconds / 1e12
+        r = {"bound": "tensor", "achieved": round(achieved, 2), "peak": tflops_peak, "unit": "TFLOP/s",
+             "frac": round(achieved / tflops_peak, 4)}
+    r["traffic"] = traffic
+    r["peak_source"] = "%s (%s)" % (source, "MEASURED_PEAKS.json" if source == "measured" else "recipe fallback")
+    r["algorithmic_bytes"] = int(nbytes)
+    r["algorithmic_flop"] = flops
+    r["tflops"] = round(flops / seconds / 1e12, 3)
+    return r
+
+
+def ncu_traffic(kernel_tag):
+    """DRAM bytes per launch from a committed ncu summary, if it still matches the
+    kernel source (profiles/<tag>.md holds `traffic_bytes_per_launch:` and
+    `source_sha256:` lines); None otherwise."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", kernel_tag + ".md")
+    if not os.path.exists(path):
+        return None
+    fields = {}
+    for line in open(path):
+        if ":" in line and line.strip().startswith(("traffic_bytes_per_launch", "source_file", "source_sha256")):
+            k, v = line.strip().split(":", 1)
+            fields[k.strip()] = v.strip().strip("`")
+    try:
+        src = os.path.join(ROOT, fields["source_file"])
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+        if sha != fields["source_sha256"]:
+            return None
+        return int(fields["traffic_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+# --------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while the GPU works."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index=0, period_ms=100):
+        self.proc = None
+        self.gpu_index = gpu_index
+        self.period_ms = period_ms
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", str(self.period_ms)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = [r for r in csv.reader(io.StringIO(out)) if len(r) >= 9]
+        sm, smax, reasons, loaded = [], None, set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                s, m, pw = float(r[1]), float(r[2]), float(r[3])
+            except ValueError:
+                continue
+            smax = m
+            sm.append(s)
+            if pw > 250.0:  # under load
+                loaded.append(s)
+                for n, val in zip(names, r[5:9]):
+                    if val.strip().lower().startswith("active"):
+                        reasons.add(n)
+        use = loaded if loaded else sm
+        return {"sm_mhz": statistics.median(use) if use else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(rows), "samples_under_load": len(loaded)}
+
+
+# --------------------------------------------------------------------------- distributed
+class Dist:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+
+    def init(self, backend):
+        if self.world > 1:
+            import torch.distributed as dist
+            dist.init_process_group(backend=backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg is not None:
+            self.pg.barrier()
+
+    def max(self, x: float) -> float:
+        if self.pg is None:
+            return x
+        import torch
+        dev = "cuda" if torch.cuda.is_available() and self.pg.get_backend() == "nccl" else "cpu"
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg is not None:
+            self.pg.destroy_process_group()
+
+
+# --------------------------------------------------------------------------- GPU arm
+def _graph_steps(torch, fn, n, stream):
+    """Capture n calls of fn(i) into CUDA graphs of at most 256 steps."""
+    graphs = []
+    i = 0
+    while i < n:
+        m = min(256, n - i)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for j in range(i, i + m):
+                fn(j)
+        graphs.append(g)
+        i += m
+    return graphs
+
+
+def time_graph_steps(torch, la, fn, steps, warmup, dist):
+    """W warm-up steps, then exactly `steps` timed steps, all replayed from CUDA
+    graphs on one side stream; CUDA events on that stream bracket the timed
+    steps, with a barrier and device synchronisation on both sides.  Returns
+    (seconds, kernel launches inside the timed steps)."""
+    stream = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        fn(0)  # plain call first: sets kernel attributes outside capture
+    torch.cuda.synchronize()
+    n0 = la.la_kernel_launches()
+    timed = _graph_steps(torch, fn, steps, stream)
+    launches = la.la_kernel_launches() - n0
+    warm = _graph_steps(torch, fn, warmup, stream) if warmup > 0 else []
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for g in warm:
+            g.replay()
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    dist.barrier()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for g in timed:
+            g.replay()
+        stop.record(stream)
+    torch.cuda.synchronize()
+    dist.barrier()
+    secs = start.elapsed_time(stop) / 1e3
+    del timed, warm
+    return secs, launches
+
+
+def dev_copy(torch, x, dtype):
+    if dtype == "bf16":
+        return torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).cuda().view(torch.bfloat16)
+    return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).cuda()
+
+
+def n_rotations(bytes_per_set):
+    return max(2, math.ceil(4 * L2_BYTES / bytes_per_set))
+
+
+def bench_causal_headline(torch, la, w, steps, warmup, dist, peaks, src):
+    q, k, v = workloads.forward_inputs(w)
+    es = 2 if w.dtype == "bf16" else 4
+    nbytes = forward_bytes(w.BH, w.N, w.dk, w.dv, es)
+    R = n_rotations(nbytes)
+    base = [dev_copy(torch, x, w.dtype) for x in (q, k, v)]
+    sets = [[t.clone() for t in base] + [torch.empty_like(base[2])] for _ in range(R)]
+
+    def step(i):
+        s = sets[i % R]
+        la.la_forward_causal(s[0], s[1], s[2], s[3], chunk=w.chunk, eps=w.eps)
+
+    secs, launches = time_graph_steps(torch, la, step, steps, warmup, dist)
+    return secs, launches, nbytes, R
+
+
+def bench_causal_e2e(torch, la, w, steps, warmup, dist):
+    """The public call with host buffers: pinned host q, k, v -> device copies,
+    la_forward_causal, device -> pinned host o, every step, all on one stream."""
+    q, k, v = workloads.forward_inputs(w)
+    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+
+    def pinned(x):
+        t = torch.from_numpy(np.ascontiguousarray(x).view(np.int16) if w.dtype == "bf16" else x)
+        t = t.view(tdt) if w.dtype == "bf16" else t
+        return t.pin_memory()
+
+    hq, hk, hv = pinned(q), pinned(k), pinned(v)
+    ho = torch.empty(hv.shape, dtype=tdt).pin_memory()
+    dq, dk_, dv_ = (torch.empty(t.shape, dtype=tdt, device="cuda") for t in (hq, hk, hv))
+    do = torch.empty_like(dv_)
+    stream = torch.cuda.Stream()
+
+    def step():
+        dq.copy_(hq, non_blocking=True)
+        dk_.copy_(hk, non_blocking=True)
+        dv_.copy_(hv, non_blocking=True)
+        la.la_forward_causal(dq, dk_, dv_, do, chunk=w.chunk, eps=w.eps)
+        ho.copy_(do, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(warmup, 1)):
+            step()
+    torch.cuda.synchronize()
+    dist.barrier()
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(steps):
+            step()
+        stop.record(stream)
+    torch.cuda.synchronize()
+    dist.barrier()
+    secs = start.elapsed_time(stop) / 1e3
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
+    d2h = ho.numel() * ho.element_size()
+    return secs, h2d, d2h
+
+
+def bench_path_causal_long(torch, la, reps, peaks, src):
+    w = workloads.CAUSAL_BF16_LONG
+    q, k, v = workloads.device_forward_inputs(w)
+    o = torch.empty_like(v)
+
+    def step(i):
+        la.la_forward_causal(q, k, v, o, chunk=w.chunk, eps=w.eps)
+
+    secs, launches = time_graph_steps(torch, la, step, reps, 2, Dist())
+    t = secs / reps
+    nbytes = forward_bytes(w.BH, w.N, w.dk, w.dv, 2)
+    fl = causal_flops(w.BH, w.N, w.dk, w.dv, w.chunk)
+    return {"workload": w.name, "value": round(w.B * w.N / t, 1), "unit": "tokens/s",
+            "ms_per_step": round(t * 1e3, 4), "launches_per_step": launches / reps,
+            "roofline": roofline(fl, nbytes, t, peaks, src, ncu_traffic("causal_long")),
+            "l2": "inputs 2.1 GB > L2"}
+
+
+def bench_path_noncausal(torch, la, reps, peaks, src):
+    w = workloads.NONCAUSAL_BF16
+    q, k, v = workloads.forward_inputs(w)
+    nbytes = forward_bytes(w.BH, w.N, w.dk, w.dv, 2)
+    R = n_rotations(nbytes)
+    base = [dev_copy(torch, x, "bf16") for x in (q, k, v)]
+    sets = [[t.clone() for t in base] + [torch.empty_like(base[2])] for _ in range(R)]
+
+    def step(i):
+        s = sets[i % R]
+        la.la_forward_noncausal(s[0], s[1], s[2], s[3], eps=w.eps)
+
+    secs, launches = time_graph_steps(torch, la, step, reps, 3, Dist())
+    t = secs / reps
+    fl = noncausal_flops(w.BH, w.N, w.dk, w.dv)
+    return {"workload": w.name, "value": round(w.B * w.N / t, 1), "unit": "tokens/s",
+            "ms_per_step": round(t * 1e3, 4), "launches_per_step": launches / reps,
+            "roofline": roofline(fl, nbytes, t, peaks, src, ncu_traffic("noncausal")),
+            "l2": "%d rotating buffer sets" % R}
+
+
+def bench_path_decode(torch, la, steps, peaks, src):
+    w = workloads.DECODE_BF16
+    (qp, kp, vp), (qd, kd, vd) = workloads.device_decode_inputs(w)
+    S, z = la.la_prefill_state(kp, vp)
+    del qp, kp, vp
+    o = torch.empty((w.B, w.H, w.dv), dtype=torch.bfloat16, device="cuda")
+    S0, z0 = S.clone(), z.clone()
+
+    def step(i):
+        la.la_decode_step(S, z, qd[i], kd[i], vd[i], o, eps=w.eps)
+
+    n = min(steps, w.steps)
+    secs, launches = time_graph_steps(torch, la, step, n, 3, Dist())
+    S.copy_(S0)
+    z.copy_(z0)
+    t = secs / n
+    nbytes = decode_bytes_per_step(w.BH, w.dk, w.dv, 2)
+    fl = decode_flops_per_step(w.BH, w.dk, w.dv)
+    return {"workload": w.name, "value": round(w.B / t, 1), "unit": "tokens/s",
+            "head_steps_per_s": round(w.BH / t, 1), "ms_per_step": round(t * 1e3, 5), "steps": n,
+            "launches_per_step": launches / n,
+            "roofline": roofline(fl, nbytes, t, peaks, src, ncu_traffic("decode")),
+            "l2": "state 270 MB > L2"}
+
+
+# --------------------------------------------------------------------------- CPU oracle
+def oracle_causal_sample(w, target_s=10.0, max_reps=50):
+    """The float64 oracle (as it stands) on a bounded sample of workload w:
+    whole (b,h) sequences, repeated until about target_s seconds.  Returns
+    (tokens/s scaled to full positions, threads, description)."""
+    import oracle
+    orc = oracle.get()
+    q, k, v = workloads.forward_inputs(w)
+    qh, kh, vh = (x.reshape((w.BH,) + x.shape[2:]) for x in (q, k, v))
+    nh = w.BH
+    t0 = time.time()
+    reps = 0
+    while True:
+        orc.causal_recurrent(qh[:nh], kh[:nh], vh[:nh], w.eps)
+        reps += 1
+        el = time.time() - t0
+        if el >= target_s or reps >= max_reps:
+            break
+    head_tokens = reps * nh * w.N
+    value = head_tokens / w.H / el
+    desc = "%d pass(es) of all %d (b,h) sequences x %d positions, float64 recurrence, %.1f s" % (
+        reps, nh, w.N, el)
+    return value, orc.num_threads(), desc, el
+
+
+def run_reference(args, dist):
+    """Reference arm: the float64 CPU oracle on the host cores, same metric and
+    config; each step is a bounded sample (8 of the 32 sequences)."""
+    if dist.rank != 0:
+        return 0
+    import oracle
+    w = workloads.CAUSAL_BF16
+    orc = oracle.get()
+    q, k, v = workloads.forward_inputs(w)
+    qh, kh, vh = (x.reshape((w.BH,) + x.shape[2:]) for x in (q, k, v))
+    nh = 8
+    for _ in range(args.warmup):
+        orc.causal_recurrent(qh[:nh], kh[:nh], vh[:nh], w.eps)
+    t0 = time.time()
+    for _ in range(args.steps):
+        orc.causal_recurrent(qh[:nh], kh[:nh], vh[:nh], w.eps)
+    el = time.time() - t0
+    value = args.steps * nh * w.N / w.H / el
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(el / args.steps * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "dk": w.dk, "dv": w.dv,
+                   "chunk": w.chunk, "inputs": "bf16, seed %d" % w.seed},
+        "cpu_baseline": {"value": round(value, 1), "unit": "tokens/s", "cores": orc.num_threads(),
+                         "kind": "oracle",
+                         "sample": "each step: %d of %d (b,h) sequences x %d positions; value scaled per "
+                                   "full position (/H)" % (nh, w.BH, w.N)},
+        "e2e": {"value": round(value, 1), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_gpu(args, dist):
+    import torch
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device (the library has no CPU path)")
+    torch.cuda.set_device(dist.local_rank)
+    dist.init("nccl")
+    from causal_kernelized_attention_gb300 import build as la_build
+    if dist.local_rank == 0:
+        la_build.build()
+    dist.barrier()
+    import causal_kernelized_attention_gb300 as la
+    la.load_library()
+    peaks, src = load_peaks()
+    w = workloads.CAUSAL_BF16
+
+    sampler = ClockSampler(gpu_index=torch.cuda.current_device()).start() if dist.rank == 0 else None
+    secs, launches, nbytes, R = bench_causal_headline(torch, la, w, args.steps, args.warmup, dist, peaks, src)
+    clocks = sampler.stop() if sampler else None
+    secs_max = dist.max(secs)
+    t_step = secs_max / args.steps
+    value = dist.world * w.B * w.N * args.steps / secs_max
+    fl = causal_flops(w.BH, w.N, w.dk, w.dv, w.chunk)
+    roof = roofline(fl, nbytes, secs / args.steps, peaks, src, ncu_traffic("causal_headline"))
+
+    e2e_secs, h2d, d2h = bench_causal_e2e(torch, la, w, max(10, min(args.steps, 200)), args.warmup, dist)
+    e2e_steps = max(10, min(args.steps, 200))
+    e2e_value = dist.world * w.B * w.N * e2e_steps / dist.max(e2e_secs)
+
+    paths = {}
+    if not args.headline_only:
+        s2 = ClockSampler(gpu_index=torch.cuda.current_device()).start() if dist.rank == 0 else None
+        paths["causal_long"] = bench_path_causal_long(torch, la, args.path_reps, peaks, src)
+        paths["noncausal"] = bench_path_noncausal(torch, la, max(args.path_reps, 20), peaks, src)
+        paths["decode"] = bench_path_decode(torch, la, 1024, peaks, src)
+        if s2:
+            paths["clocks"] = s2.stop()
+
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": dist.world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t_step * 1e3, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "dk": w.dk, "dv": w.dv,
+                   "chunk": w.chunk, "accumulate": "fp32", "global_batch": w.B * dist.world,
+                   "seq_len": w.N, "parallelism": "replicas x%d" % dist.world,
+                   "l2": "%d rotating input/output sets (%.0f MB > 4x L2)" % (R, R * nbytes / 1e6),
+                   "timing": "CUDA graph replay, CUDA events on the launch stream"},
+        "tflops": roof["tflops"],
+        "roofline": roof,
+        "gpu_launches": int(launches),
+        "clocks": clocks,
+        "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h), "steps": e2e_steps},
+        "paths": paths,
+    }
+    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
+        val, cores, desc, el = oracle_causal_sample(w, target_s=args.cpu_seconds)
+        line["cpu_baseline"] = {"value": round(val, 1), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                                "sample": desc}
+    if dist.rank == 0:
+        print(json.dumps(line), flush=True)
+    dist.close()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["gpu", "reference"], default="gpu")
+    ap.add_argument("--headline-only", action="store_true", help="skip the secondary paths")
+    ap.add_argument("--path-reps", type=int, default=20, help="timed steps of the long causal path")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps; the line reports the count used
+    dist = Dist()
+    if args.impl == "reference":
+        return run_reference(args, dist)
+    return run_gpu(args, dist)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,24 @@
+"""Causal kernelized (linear) attention, phi = elu + 1, on GB300 (sm_103a).
+
+Thin Python binding over the C ABI of ``liblinattn.so`` (declared in
+``include/la.h``).  Every function below only checks and marshals arguments
+(device pointers, sizes, the current CUDA stream) and calls the C entry point
+of the same name; all arithmetic runs in the library's CUDA kernels.  There is
+no CPU or PyTorch fallback: if the library is missing or fails to load, the
+import of this package's functions raises.
+
+Tensors are PyTorch CUDA tensors (PyTorch supplies device memory and streams):
+  q, k [B, H, N, dk], v, o [B, H, N, dv], fp32 or bf16, contiguous;
+  decode: q, k [B, H, dk], v, o [B, H, dv]; S [B, H, dk, dv] and z [B, H, dk] fp32.
+"""
+from __future__ import annotations
+
+from ._binding import (LA_BF16, LA_F32, LAError, lib_path, la_decode_step, la_forward_causal,
+                       la_forward_noncausal, la_get_device_status, la_kernel_launches, la_last_cuda_error,
+                       la_prefill_state, la_status_string, la_version, load_library)
+
+__all__ = [
+    "LA_BF16", "LA_F32", "LAError", "lib_path", "la_decode_step", "la_forward_causal",
+    "la_forward_noncausal", "la_get_device_status", "la_kernel_launches", "la_last_cuda_error", "la_prefill_state",
+    "la_status_string", "la_version", "load_library",
+]

@@ -1,0 +1,205 @@
+"""ctypes marshalling for liblinattn.so (argument checks and pointers only)."""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from .build import LIB_PATH
+
+LA_F32 = 0
+LA_BF16 = 1
+
+_STATUS_NAMES = {0: "LA_OK", 1: "LA_ERR_INVALID_ARG", 2: "LA_ERR_UNSUPPORTED", 3: "LA_ERR_MISALIGNED",
+                 4: "LA_ERR_CUDA", 5: "LA_ERR_TIMEOUT"}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class LAError(RuntimeError):
+    def __init__(self, fn: str, status: int, cuda_error: int = 0):
+        self.status = status
+        self.cuda_error = cuda_error
+        msg = "%s returned %s" % (fn, _STATUS_NAMES.get(status, status))
+        if cuda_error:
+            msg += " (cudaError %d)" % cuda_error
+        super().__init__(msg)
+
+
+def lib_path() -> str:
+    return LIB_PATH
+
+
+def _declare(lib):
+    P, I, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    sigs = {
+        "la_forward_causal": [P, P, P, P, I, I, I, I, I, I, F, I, P],
+        "la_forward_noncausal": [P, P, P, P, I, I, I, I, I, F, I, P],
+        "la_decode_step": [P, P, P, P, P, P, I, I, I, I, F, I, P],
+        "la_prefill_state": [P, P, P, P, I, I, I, I, I, I, P],
+        "la_get_device_status": [P],
+    }
+    for name, args in sigs.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = ctypes.c_int
+    lib.la_status_string.argtypes = [ctypes.c_int]
+    lib.la_status_string.restype = ctypes.c_char_p
+    lib.la_last_cuda_error.argtypes = []
+    lib.la_last_cuda_error.restype = ctypes.c_int
+    lib.la_version.argtypes = []
+    lib.la_version.restype = ctypes.c_int
+    lib.la_kernel_launches.argtypes = []
+    lib.la_kernel_launches.restype = ctypes.c_ulonglong
+    return lib
+
+
+def load_library(path: str = None):
+    """Load liblinattn.so (built by ``build.py`` / ``__graft_entry__.build()``).
+
+    Raises OSError with a clear message when the library has not been built.
+    """
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise OSError("liblinattn.so not found at %s: build it with "
+                          "`python -m causal_kernelized_attention_gb300.build`" % p)
+        lib = _declare(ctypes.CDLL(p))
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def _check(fn: str, status: int):
+    if status != 0:
+        raise LAError(fn, status, load_library().la_last_cuda_error() if status == 4 else 0)
+
+
+def _stream_ptr(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _dtype_code(t):
+    import torch
+    if t.dtype == torch.float32:
+        return LA_F32
+    if t.dtype == torch.bfloat16:
+        return LA_BF16
+    raise TypeError("q, k, v, o must be float32 or bfloat16, got %s" % t.dtype)
+
+
+def _need_cuda(*ts):
+    for t in ts:
+        if not t.is_cuda:
+            raise ValueError("tensors must be on a CUDA device")
+        if not t.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+
+
+def _same_dtype(*ts):
+    d = ts[0].dtype
+    for t in ts[1:]:
+        if t.dtype != d:
+            raise TypeError("q, k, v, o must share one dtype")
+
+
+def la_forward_causal(q, k, v, o=None, chunk: int = 128, eps: float = 1e-6, stream=None):
+    """Causal forward; q, k [B,H,N,dk], v [B,H,N,dv]; returns o [B,H,N,dv]."""
+    import torch
+    if o is None:
+        o = torch.empty(q.shape[:-1] + (v.shape[-1],), dtype=q.dtype, device=q.device)
+    _need_cuda(q, k, v, o)
+    _same_dtype(q, k, v, o)
+    B, H, N, dk = q.shape
+    dv = v.shape[-1]
+    if tuple(k.shape) != (B, H, N, dk) or tuple(v.shape[:-1]) != (B, H, N) or tuple(o.shape) != (B, H, N, dv):
+        raise ValueError("shape mismatch")
+    st = load_library().la_forward_causal(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                          B, H, N, dk, dv, int(chunk), float(eps), _dtype_code(q),
+                                          _stream_ptr(stream))
+    _check("la_forward_causal", st)
+    return o
+
+
+def la_forward_noncausal(q, k, v, o=None, eps: float = 1e-6, stream=None):
+    """Non-causal forward; q, k [B,H,N,dk], v [B,H,N,dv]; returns o [B,H,N,dv]."""
+    import torch
+    if o is None:
+        o = torch.empty(q.shape[:-1] + (v.shape[-1],), dtype=q.dtype, device=q.device)
+    _need_cuda(q, k, v, o)
+    _same_dtype(q, k, v, o)
+    B, H, N, dk = q.shape
+    dv = v.shape[-1]
+    if tuple(k.shape) != (B, H, N, dk) or tuple(v.shape[:-1]) != (B, H, N) or tuple(o.shape) != (B, H, N, dv):
+        raise ValueError("shape mismatch")
+    st = load_library().la_forward_noncausal(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                             B, H, N, dk, dv, float(eps), _dtype_code(q), _stream_ptr(stream))
+    _check("la_forward_noncausal", st)
+    return o
+
+
+def la_decode_step(S, z, q, k, v, o=None, eps: float = 1e-6, stream=None):
+    """One decode step; S [B,H,dk,dv], z [B,H,dk] fp32 updated in place; returns o [B,H,dv]."""
+    import torch
+    if o is None:
+        o = torch.empty(q.shape[:-1] + (v.shape[-1],), dtype=q.dtype, device=q.device)
+    _need_cuda(S, z, q, k, v, o)
+    _same_dtype(q, k, v, o)
+    if S.dtype != torch.float32 or z.dtype != torch.float32:
+        raise TypeError("S and z must be float32")
+    B, H, dk = q.shape
+    dv = v.shape[-1]
+    if tuple(S.shape) != (B, H, dk, dv) or tuple(z.shape) != (B, H, dk) or tuple(k.shape) != (B, H, dk) \
+            or tuple(v.shape) != (B, H, dv) or tuple(o.shape) != (B, H, dv):
+        raise ValueError("shape mismatch")
+    st = load_library().la_decode_step(S.data_ptr(), z.data_ptr(), q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                       o.data_ptr(), B, H, dk, dv, float(eps), _dtype_code(q),
+                                       _stream_ptr(stream))
+    _check("la_decode_step", st)
+    return o
+
+
+def la_prefill_state(k, v, S=None, z=None, stream=None):
+    """S = sum_t phi(k_t) v_t^T, z = sum_t phi(k_t) over N tokens; returns (S, z) fp32."""
+    import torch
+    B, H, N, dk = k.shape
+    dv = v.shape[-1]
+    if S is None:
+        S = torch.empty((B, H, dk, dv), dtype=torch.float32, device=k.device)
+    if z is None:
+        z = torch.empty((B, H, dk), dtype=torch.float32, device=k.device)
+    _need_cuda(k, v, S, z)
+    _same_dtype(k, v)
+    if tuple(v.shape[:-1]) != (B, H, N) or tuple(S.shape) != (B, H, dk, dv) or tuple(z.shape) != (B, H, dk):
+        raise ValueError("shape mismatch")
+    st = load_library().la_prefill_state(k.data_ptr(), v.data_ptr(), S.data_ptr(), z.data_ptr(),
+                                         B, H, N, dk, dv, _dtype_code(k), _stream_ptr(stream))
+    _check("la_prefill_state", st)
+    return S, z
+
+
+def la_get_device_status(stream=None) -> int:
+    return load_library().la_get_device_status(_stream_ptr(stream))
+
+
+def la_status_string(status: int) -> str:
+    return load_library().la_status_string(int(status)).decode()
+
+
+def la_last_cuda_error() -> int:
+    return load_library().la_last_cuda_error()
+
+
+def la_version() -> int:
+    return load_library().la_version()
+
+
+def la_kernel_launches() -> int:
+    return int(load_library().la_kernel_launches())

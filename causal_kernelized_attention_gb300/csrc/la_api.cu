@@ -1,0 +1,192 @@
+// C ABI entry points: argument validation, dispatch to the kernels, status codes.
+#include <math.h>
+#include <stdint.h>
+
+#include <atomic>
+#include <mutex>
+#include <set>
+#include <tuple>
+
+#include "la_common.cuh"
+#include "la_internal.h"
+
+namespace la {
+
+static thread_local int t_last_cuda_error = 0;
+
+la_status cuda_status(cudaError_t e)
+{
+    if (e == cudaSuccess) return LA_OK;
+    t_last_cuda_error = (int)e;
+    return LA_ERR_CUDA;
+}
+
+la_status Scratch::alloc(size_t bytes, cudaStream_t s)
+{
+    stream = s;
+    return cuda_status(cudaMallocAsync(&ptr, bytes, s));
+}
+
+Scratch::~Scratch()
+{
+    if (ptr) {
+        cudaError_t e = cudaFreeAsync(ptr, stream);
+        if (e != cudaSuccess) t_last_cuda_error = (int)e;
+    }
+}
+
+bool supported_dim(int d) { return d == 32 || d == 64 || d == 128; }
+
+static std::atomic<unsigned long long> g_launches{0};
+
+void count_launches(unsigned n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+la_status ensure_smem(const void *kernel, int bytes)
+{
+    static std::mutex mu;
+    static std::set<std::tuple<const void *, int, int>> done;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_status(e);
+    std::lock_guard<std::mutex> lock(mu);
+    auto key = std::make_tuple(kernel, dev, bytes);
+    if (done.count(key)) return LA_OK;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) return cuda_status(e);
+    done.insert(key);
+    return LA_OK;
+}
+
+static bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+static bool overlaps(const void *a, size_t na, const void *b, size_t nb)
+{
+    const uintptr_t x = (uintptr_t)a, y = (uintptr_t)b;
+    return x < y + nb && y < x + na;
+}
+
+static size_t elem_size(la_dtype t) { return t == LA_F32 ? 4 : 2; }
+
+// Common checks of the forward entry points.  Returns LA_OK and sets *empty when
+// there is nothing to do.
+static la_status check_forward(const void *q, const void *k, const void *v, const void *o, int B, int H,
+                               int N, int dk, int dv, float eps, la_dtype dtype, bool *empty)
+{
+    *empty = false;
+    if (B < 0 || H < 0 || N < 0 || dk < 0 || dv < 0) return LA_ERR_INVALID_ARG;
+    if (!(eps >= 0.f) || !isfinite(eps)) return LA_ERR_INVALID_ARG;
+    if (dtype != LA_F32 && dtype != LA_BF16) return LA_ERR_INVALID_ARG;
+    if ((long long)B * H > 65535) return LA_ERR_UNSUPPORTED;
+    if (B == 0 || H == 0 || N == 0 || dk == 0 || dv == 0) {
+        *empty = true;
+        return LA_OK;
+    }
+    if (!q || !k || !v || !o) return LA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return LA_ERR_MISALIGNED;
+    const size_t es = elem_size(dtype);
+    const size_t nqk = (size_t)B * H * N * dk * es, nvo = (size_t)B * H * N * dv * es;
+    if (overlaps(o, nvo, q, nqk) || overlaps(o, nvo, k, nqk) || overlaps(o, nvo, v, nvo))
+        return LA_ERR_INVALID_ARG;
+    return LA_OK;
+}
+
+}  // namespace la
+
+using namespace la;
+
+extern "C" {
+
+la_status la_forward_causal(const void *q, const void *k, const void *v, void *o, int B, int H, int N,
+                            int dk, int dv, int chunk, float eps, la_dtype dtype, la_stream_t stream)
+{
+    bool empty;
+    la_status st = check_forward(q, k, v, o, B, H, N, dk, dv, eps, dtype, &empty);
+    if (st != LA_OK) return st;
+    if (chunk != 64 && chunk != 128) return LA_ERR_UNSUPPORTED;
+    if (empty) return LA_OK;
+    if (!supported_dim(dk) || !supported_dim(dv)) return LA_ERR_UNSUPPORTED;
+    Problem p{q, k, v, o, B * H, N, dk, dv, chunk, eps, dtype, (cudaStream_t)stream};
+    if (dtype == LA_BF16) {
+        st = causal_tc(p);
+        if (st != LA_ERR_UNSUPPORTED) return st;
+    }
+    return causal_simt(p);
+}
+
+la_status la_forward_noncausal(const void *q, const void *k, const void *v, void *o, int B, int H, int N,
+                               int dk, int dv, float eps, la_dtype dtype, la_stream_t stream)
+{
+    bool empty;
+    la_status st = check_forward(q, k, v, o, B, H, N, dk, dv, eps, dtype, &empty);
+    if (st != LA_OK || empty) return st;
+    if (!supported_dim(dk) || !supported_dim(dv)) return LA_ERR_UNSUPPORTED;
+    Problem p{q, k, v, o, B * H, N, dk, dv, 0, eps, dtype, (cudaStream_t)stream};
+    return noncausal_simt(p);
+}
+
+la_status la_decode_step(float *S, float *z, const void *q, const void *k, const void *v, void *o, int B,
+                         int H, int dk, int dv, float eps, la_dtype dtype, la_stream_t stream)
+{
+    if (B < 0 || H < 0 || dk < 0 || dv < 0) return LA_ERR_INVALID_ARG;
+    if (!(eps >= 0.f) || !isfinite(eps)) return LA_ERR_INVALID_ARG;
+    if (dtype != LA_F32 && dtype != LA_BF16) return LA_ERR_INVALID_ARG;
+    if (B == 0 || H == 0 || dk == 0 || dv == 0) return LA_OK;
+    if (!S || !z || !q || !k || !v || !o) return LA_ERR_INVALID_ARG;
+    if (!aligned16(S) || !aligned16(z) || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o))
+        return LA_ERR_MISALIGNED;
+    if (!supported_dim(dk) || !supported_dim(dv)) return LA_ERR_UNSUPPORTED;
+    const size_t BH = (size_t)B * H, es = elem_size(dtype);
+    if (BH > 0x7fffffff) return LA_ERR_UNSUPPORTED;
+    const size_t nS = BH * dk * dv * 4, nz = BH * dk * 4, nqk = BH * dk * es, nvo = BH * dv * es;
+    if (overlaps(S, nS, z, nz) || overlaps(o, nvo, S, nS) || overlaps(o, nvo, z, nz) ||
+        overlaps(o, nvo, q, nqk) || overlaps(o, nvo, k, nqk) || overlaps(o, nvo, v, nvo))
+        return LA_ERR_INVALID_ARG;
+    return decode_step(S, z, q, k, v, o, (int)BH, dk, dv, eps, dtype, (cudaStream_t)stream);
+}
+
+la_status la_prefill_state(const void *k, const void *v, float *S, float *z, int B, int H, int N, int dk,
+                           int dv, la_dtype dtype, la_stream_t stream)
+{
+    if (B < 0 || H < 0 || N < 0 || dk < 0 || dv < 0) return LA_ERR_INVALID_ARG;
+    if (dtype != LA_F32 && dtype != LA_BF16) return LA_ERR_INVALID_ARG;
+    if ((long long)B * H > 65535) return LA_ERR_UNSUPPORTED;
+    if (B == 0 || H == 0 || dk == 0 || dv == 0) return LA_OK;
+    if (!S || !z || (N > 0 && (!k || !v))) return LA_ERR_INVALID_ARG;
+    if (!aligned16(S) || !aligned16(z) || (N > 0 && (!aligned16(k) || !aligned16(v))))
+        return LA_ERR_MISALIGNED;
+    if (!supported_dim(dk) || !supported_dim(dv)) return LA_ERR_UNSUPPORTED;
+    const size_t BH = (size_t)B * H;
+    if (overlaps(S, BH * dk * dv * 4, z, BH * dk * 4)) return LA_ERR_INVALID_ARG;
+    return state_simt(k, v, S, z, (int)BH, N, dk, dv, dtype, (cudaStream_t)stream);
+}
+
+const char *la_status_string(la_status s)
+{
+    switch (s) {
+    case LA_OK: return "LA_OK";
+    case LA_ERR_INVALID_ARG: return "LA_ERR_INVALID_ARG";
+    case LA_ERR_UNSUPPORTED: return "LA_ERR_UNSUPPORTED";
+    case LA_ERR_MISALIGNED: return "LA_ERR_MISALIGNED";
+    case LA_ERR_CUDA: return "LA_ERR_CUDA";
+    case LA_ERR_TIMEOUT: return "LA_ERR_TIMEOUT";
+    }
+    return "LA_ERR_UNKNOWN";
+}
+
+int la_last_cuda_error(void) { return t_last_cuda_error; }
+
+la_status la_get_device_status(la_stream_t stream)
+{
+    la_status st = cuda_status(cudaStreamSynchronize((cudaStream_t)stream));
+    if (st != LA_OK) return st;
+    unsigned bits = 0;
+    st = tc_causal_read_status((cudaStream_t)stream, &bits);
+    if (st != LA_OK) return st;
+    return (bits & kStatusTimeout) ? LA_ERR_TIMEOUT : LA_OK;
+}
+
+int la_version(void) { return 100; }
+
+unsigned long long la_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
+
+}  // extern "C"

@@ -1,0 +1,57 @@
+// Launchers shared between the library's translation units (not part of the ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "la.h"
+
+namespace la {
+
+// Records a CUDA error for la_last_cuda_error() and returns LA_ERR_CUDA (or LA_OK).
+la_status cuda_status(cudaError_t e);
+
+// Stream-ordered scratch: cudaMallocAsync / cudaFreeAsync on the call's stream.
+struct Scratch {
+    void *ptr = nullptr;
+    cudaStream_t stream = nullptr;
+    la_status alloc(size_t bytes, cudaStream_t s);
+    ~Scratch();
+};
+
+struct Problem {
+    const void *q, *k, *v;
+    void *o;
+    int BH, N, dk, dv, chunk;
+    float eps;
+    la_dtype dtype;
+    cudaStream_t stream;
+};
+
+// SIMT kernels (la_simt.cu): fp32 CUDA-core arithmetic, any supported dtype.
+la_status causal_simt(const Problem &p);
+la_status noncausal_simt(const Problem &p);
+// S, z (fp32, [BH,dk,dv], [BH,dk]) = sums over N tokens; overwrites S and z.
+la_status state_simt(const void *k, const void *v, float *S, float *z, int BH, int N, int dk,
+                     int dv, la_dtype dtype, cudaStream_t stream);
+
+// Decode step (la_decode.cu).
+la_status decode_step(float *S, float *z, const void *q, const void *k, const void *v, void *o,
+                      int BH, int dk, int dv, float eps, la_dtype dtype, cudaStream_t stream);
+
+// Tensor-core (tcgen05) paths (la_tc_causal.cu); return LA_ERR_UNSUPPORTED when
+// the problem is outside the shapes they are built for.
+la_status causal_tc(const Problem &p);
+
+// Device status words of translation units that run bounded waits: read and clear.
+la_status tc_causal_read_status(cudaStream_t s, unsigned *bits);
+
+bool supported_dim(int d);
+
+// Counts every kernel launch / memset the library enqueues (la_kernel_launches).
+void count_launches(unsigned n = 1);
+
+// cudaFuncSetAttribute(MaxDynamicSharedMemorySize) once per kernel and device,
+// so that repeated calls (and stream capture) issue no attribute calls.
+la_status ensure_smem(const void *kernel, int bytes);
+
+}  // namespace la

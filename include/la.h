@@ -1,0 +1,152 @@
+/*
+ * la.h -- C ABI of the GB300 (sm_103a) causal kernelized attention library.
+ *
+ * The library computes linear attention with the feature map
+ * phi(x) = elu(x) + 1 (alpha = 1; equal to x + 1 for x > 0 and exp(x) otherwise):
+ *
+ *   o_i = phi(q_i)^T S_i / max(phi(q_i)^T z_i, eps)
+ *   S_i = sum_{j<=i} phi(k_j) v_j^T   (dk x dv),   z_i = sum_{j<=i} phi(k_j)   (dk)
+ *
+ * Definitions followed ("Linear attention", learn.pranaymahendrakar.com,
+ * Researcher: Derivation, the recurrence S_i = S_{i-1} + phi(k_i) v_i^T and
+ * o_i = S_i^T phi(q_i) / z_i^T phi(q_i); "Linear Attention",
+ * aiwiki.thehackersbrain.dev, the chunked parallel form and its clamp of the
+ * denominator).  No 1/sqrt(d) scaling is applied to q or k.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - All tensor pointers are DEVICE pointers to contiguous row-major memory,
+ *    owned by the caller.  The library keeps no pointer after a call returns
+ *    and never frees caller memory.
+ *  - Each pointer must be 16-byte aligned (LA_ERR_MISALIGNED otherwise).
+ *  - `dtype` is the element type of q, k, v and o (fp32 or bf16).  The states
+ *    S and z are always fp32.  Arithmetic is fp32 (bf16 products on the tensor
+ *    cores accumulate in fp32).
+ *  - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL is the
+ *    legacy default stream).  The return value reports argument validation and
+ *    launch errors only; call la_get_device_status() to learn whether a kernel
+ *    gave up on a bounded wait.
+ *  - Any of B, H, N, dk, dv equal to 0 is a valid empty problem: LA_OK, no work.
+ *    Negative sizes, NULL pointers (for a non-empty problem) and a negative or
+ *    non-finite eps give LA_ERR_INVALID_ARG.  Sizes the kernels are not built
+ *    for give LA_ERR_UNSUPPORTED (see each function).
+ *  - o must not overlap q, k or v.
+ *  - Scratch memory, where a path needs it, is allocated and freed
+ *    stream-ordered (cudaMallocAsync / cudaFreeAsync on `stream`).
+ */
+#ifndef LA_H
+#define LA_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum la_status {
+    LA_OK = 0,
+    LA_ERR_INVALID_ARG = 1,  /* NULL pointer, negative size, bad eps, overlap */
+    LA_ERR_UNSUPPORTED = 2,  /* size/dtype/chunk combination not built */
+    LA_ERR_MISALIGNED = 3,   /* a pointer is not 16-byte aligned */
+    LA_ERR_CUDA = 4,         /* a CUDA runtime call failed (la_last_cuda_error) */
+    LA_ERR_TIMEOUT = 5       /* a kernel's bounded wait expired (device status) */
+} la_status;
+
+typedef enum la_dtype {
+    LA_F32 = 0,   /* IEEE binary32 q, k, v, o */
+    LA_BF16 = 1   /* bfloat16 q, k, v, o */
+} la_dtype;
+
+/* Same type as cudaStream_t, declared here so this header needs no CUDA header. */
+typedef struct CUstream_st *la_stream_t;
+
+/*
+ * Causal forward, chunked parallel form ("Linear Attention",
+ * aiwiki.thehackersbrain.dev: quadratic inside a chunk, recurrent across
+ * chunks; "Linear attention", learn.pranaymahendrakar.com, Implementation
+ * reality: chunks of 64 or 128).
+ *
+ *   q, k : [B, H, N, dk]   v, o : [B, H, N, dv]
+ *
+ * o[b,h,i,:] = phi(q_i)^T S_i / max(phi(q_i)^T z_i, eps) with the sums over
+ * j <= i of the same (b,h) (inclusive of i).  N need not be a multiple of
+ * `chunk`; the last chunk is then shorter.  `chunk` must be 64 or 128.
+ * Supported: dk, dv in {32, 64, 128} for fp32; for bf16 dk == dv in
+ * {64, 128} on the tensor-core path, and dk, dv in {32, 64, 128} otherwise.
+ */
+la_status la_forward_causal(const void *q, const void *k, const void *v, void *o,
+                            int B, int H, int N, int dk, int dv, int chunk, float eps,
+                            la_dtype dtype, la_stream_t stream);
+
+/*
+ * Non-causal forward ("Linear attention: change the order.", implementation
+ * you can check; "Linear Attention -- Math + Variants", o_i = phi(q_i)^T S /
+ * phi(q_i)^T z with S, z summed over the whole sequence).
+ *
+ *   q, k : [B, H, N, dk]   v, o : [B, H, N, dv]
+ *
+ * o_i = phi(q_i)^T S / max(phi(q_i)^T z, eps), S = sum_j phi(k_j) v_j^T,
+ * z = sum_j phi(k_j), j over all N positions of the same (b,h).
+ * Supported: dk, dv in {32, 64, 128}.
+ */
+la_status la_forward_noncausal(const void *q, const void *k, const void *v, void *o,
+                               int B, int H, int N, int dk, int dv, float eps,
+                               la_dtype dtype, la_stream_t stream);
+
+/*
+ * One recurrent decode step for B*H independent heads ("Linear Attention",
+ * "It is a linear RNN": O(d^2) per token with a fixed-size state;
+ * "26. Linear (Kernelized) Attention", Step-by-Step steps 3-4: update the
+ * state, then read it).
+ *
+ *   S : [B, H, dk, dv] fp32, z : [B, H, dk] fp32   (read and updated in place)
+ *   q, k : [B, H, dk]   v, o : [B, H, dv]            (element type `dtype`)
+ *
+ * S += phi(k) v^T;  z += phi(k);  o = phi(q)^T S / max(phi(q)^T z, eps).
+ * S and z are the whole resumable memory of a sequence: passing them back in
+ * continues it.  Supported: dk, dv in {32, 64, 128}.
+ */
+la_status la_decode_step(float *S, float *z, const void *q, const void *k, const void *v,
+                         void *o, int B, int H, int dk, int dv, float eps,
+                         la_dtype dtype, la_stream_t stream);
+
+/*
+ * State of a prefix ("Linear Attention -- Math + Variants": S = sum_j
+ * phi(k_j) v_j^T, z = sum_j phi(k_j)), used to start decoding after a causal
+ * prefill of N tokens.
+ *
+ *   k : [B, H, N, dk]   v : [B, H, N, dv]   S : [B, H, dk, dv] fp32   z : [B, H, dk] fp32
+ *
+ * S and z are OVERWRITTEN (not accumulated).  N = 0 writes zeros.
+ * Supported: dk, dv in {32, 64, 128}.
+ */
+la_status la_prefill_state(const void *k, const void *v, float *S, float *z,
+                           int B, int H, int N, int dk, int dv, la_dtype dtype,
+                           la_stream_t stream);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *la_status_string(la_status s);
+
+/* The cudaError_t of the most recent CUDA failure on this thread (0 if none). */
+int la_last_cuda_error(void);
+
+/*
+ * Synchronises `stream`, then reads and clears the library's device status
+ * word on the current device: LA_ERR_TIMEOUT if a kernel abandoned a bounded
+ * wait since the last call, LA_OK otherwise (LA_ERR_CUDA if the read failed).
+ */
+la_status la_get_device_status(la_stream_t stream);
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+int la_version(void);
+
+/*
+ * Number of kernel launches (and memset nodes) the library has enqueued in this
+ * process since it was loaded, on all streams and devices.  Launches recorded
+ * into a CUDA graph during stream capture are counted once, at capture time.
+ */
+unsigned long long la_kernel_launches(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LA_H */

@@ -1,0 +1,120 @@
+"""The C ABI library loads, exports every declared symbol, and rejects bad
+arguments before touching the GPU (CPU only: no compute call is made)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import causal_kernelized_attention_gb300 as la
+from causal_kernelized_attention_gb300 import build as la_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "la.h")
+
+OK, INVALID, UNSUPPORTED, MISALIGNED = 0, 1, 2, 3
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(la_[a-z_0-9]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    la_build.build()
+    return la.load_library()
+
+
+def test_library_is_in_tree(lib):
+    assert os.path.dirname(la.lib_path()) == os.path.join(ROOT, "causal_kernelized_attention_gb300")
+    assert os.path.exists(la.lib_path())
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert set(names) >= {"la_forward_causal", "la_forward_noncausal", "la_decode_step",
+                          "la_prefill_state", "la_status_string", "la_last_cuda_error",
+                          "la_get_device_status", "la_version"}
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    for code, name in [(0, "LA_OK"), (1, "LA_ERR_INVALID_ARG"), (2, "LA_ERR_UNSUPPORTED"),
+                       (3, "LA_ERR_MISALIGNED"), (4, "LA_ERR_CUDA"), (5, "LA_ERR_TIMEOUT")]:
+        assert lib.la_status_string(code).decode() == name
+    assert lib.la_status_string(99).decode() == "LA_ERR_UNKNOWN"
+    assert lib.la_version() >= 100
+
+
+# Fake pointers are only ever used in calls that must fail validation, so the
+# library never dereferences or launches on them.
+A = 0x100000        # 16-byte aligned
+M = 0x100008        # 8-byte aligned only
+
+
+def causal(lib, q=A, k=A + 0x100000, v=A + 0x200000, o=A + 0x300000, B=1, H=1, N=16, dk=64, dv=64,
+           chunk=128, eps=1e-6, dtype=1):
+    return lib.la_forward_causal(q, k, v, o, B, H, N, dk, dv, chunk, ctypes.c_float(eps), dtype, None)
+
+
+def test_causal_validation(lib):
+    assert causal(lib, q=None) == INVALID
+    assert causal(lib, o=None) == INVALID
+    assert causal(lib, B=-1) == INVALID
+    assert causal(lib, N=-5) == INVALID
+    assert causal(lib, eps=-1.0) == INVALID
+    assert causal(lib, eps=float("nan")) == INVALID
+    assert causal(lib, eps=float("inf")) == INVALID
+    assert causal(lib, dtype=7) == INVALID
+    assert causal(lib, q=M) == MISALIGNED
+    assert causal(lib, o=M) == MISALIGNED
+    assert causal(lib, chunk=96) == UNSUPPORTED
+    assert causal(lib, chunk=0) == UNSUPPORTED
+    assert causal(lib, dk=48) == UNSUPPORTED
+    assert causal(lib, dv=256) == UNSUPPORTED
+    # o overlapping q
+    assert causal(lib, o=A + 64) == INVALID
+    # empty problems are a no-op, even with NULL pointers
+    assert causal(lib, N=0, q=None, k=None, v=None, o=None) == OK
+    assert causal(lib, B=0, q=None, k=None, v=None, o=None) == OK
+
+
+def test_noncausal_validation(lib):
+    f = lib.la_forward_noncausal
+    e = ctypes.c_float(1e-6)
+    assert f(None, A, A, A + 0x300000, 1, 1, 8, 64, 64, e, 1, None) == INVALID
+    assert f(A, A, A, M, 1, 1, 8, 64, 64, e, 1, None) == MISALIGNED
+    assert f(A, A, A, A + 0x300000, 1, 1, 8, 40, 64, e, 1, None) == UNSUPPORTED
+    assert f(None, None, None, None, 1, 1, 0, 64, 64, e, 1, None) == OK
+
+
+def test_decode_validation(lib):
+    f = lib.la_decode_step
+    e = ctypes.c_float(1e-6)
+    S, z, q, k, v, o = A, A + 0x800000, A + 0x900000, A + 0xA00000, A + 0xB00000, A + 0xC00000
+    assert f(None, z, q, k, v, o, 2, 2, 64, 64, e, 1, None) == INVALID
+    assert f(S, z, q, k, v, M, 2, 2, 64, 64, e, 1, None) == MISALIGNED
+    assert f(S, z, q, k, v, o, 2, 2, 64, 96, e, 1, None) == UNSUPPORTED
+    assert f(S, z, q, k, v, o, -2, 2, 64, 64, e, 1, None) == INVALID
+    assert f(S, z, q, k, v, o, 2, 2, 64, 64, ctypes.c_float(-1.0), 1, None) == INVALID
+    # z overlapping S
+    assert f(S, S + 64, q, k, v, o, 2, 2, 64, 64, e, 1, None) == INVALID
+    assert f(None, None, None, None, None, None, 0, 2, 64, 64, e, 1, None) == OK
+
+
+def test_prefill_validation(lib):
+    f = lib.la_prefill_state
+    assert f(A, A, None, A + 0x800000, 1, 1, 8, 64, 64, 1, None) == INVALID
+    assert f(A, A, M, A + 0x800000, 1, 1, 8, 64, 64, 1, None) == MISALIGNED
+    assert f(A, A, A + 0x700000, A + 0x800000, 1, 1, 8, 24, 64, 1, None) == UNSUPPORTED
+    assert f(None, None, None, None, 0, 1, 8, 64, 64, 1, None) == OK
+
+
+def test_binding_raises_without_cuda_tensors():
+    torch = pytest.importorskip("torch")
+    q = torch.zeros(1, 1, 4, 64)
+    with pytest.raises(ValueError):
+        la.la_forward_causal(q, q, q, q.clone())

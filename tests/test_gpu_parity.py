@@ -1,0 +1,258 @@
+"""CUDA path vs the float64 oracle on the same seeded inputs (needs a GB300).
+
+Every call goes through the C ABI (via the thin ctypes binding).  Tolerances:
+fp32 normwise max-abs / max|oracle| <= 1e-5; bf16 max abs <= 2e-2 and mean
+abs <= 2e-3 (see gpu_util).  Full-size workloads are checked completely where
+the oracle finishes in seconds, otherwise on whole sampled heads (heads are
+independent sequences) plus properties that hold for every head.
+"""
+import numpy as np
+import pytest
+
+import workloads
+from gpu_util import assert_parity, errors, from_dev, to_dev
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from causal_kernelized_attention_gb300 import build
+    build.build()
+    import causal_kernelized_attention_gb300 as la
+    la.load_library()
+    return la
+
+
+def la():
+    import causal_kernelized_attention_gb300 as m
+    return m
+
+
+# ----------------------------------------------------------------------------- causal
+def run_causal(q, k, v, dtype, chunk, eps=1e-6):
+    dq, dk_, dv_ = to_dev(q, dtype), to_dev(k, dtype), to_dev(v, dtype)
+    o = la().la_forward_causal(dq, dk_, dv_, chunk=chunk, eps=eps)
+    torch.cuda.synchronize()
+    assert la().la_get_device_status() == 0
+    return from_dev(o)
+
+
+def test_causal_f32_workload(orc):
+    w = workloads.CAUSAL_F32_SMALL
+    q, k, v = workloads.forward_inputs(w)
+    got = run_causal(q, k, v, w.dtype, w.chunk, w.eps)
+    ref = orc.causal_recurrent(q, k, v, w.eps)
+    e = assert_parity(got, ref, "f32", w.name)
+    print(w.name, e)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("N,dk,dv,chunk", [
+    (1, 32, 32, 64), (63, 64, 64, 64), (64, 64, 64, 64), (65, 64, 64, 64), (127, 128, 128, 128),
+    (129, 128, 128, 128), (300, 64, 64, 128), (200, 32, 64, 64), (130, 128, 32, 128),
+    (257, 64, 128, 64), (1000, 128, 128, 128),
+])
+def test_causal_small_cases(orc, dtype, N, dk, dv, chunk):
+    q, k, v = workloads.random_inputs(1000 + N + dk + dv, 2, 3, N, dk, dv, dtype)
+    got = run_causal(q, k, v, dtype, chunk)
+    ref = orc.causal_recurrent(q, k, v)
+    assert_parity(got, ref, dtype, (N, dk, dv, chunk))
+
+
+def test_causal_output0_is_v0(orc):
+    # "26. Linear (Kernelized) Attention", Step-by-Step step 6: o_0 = v_0 for any q_0.
+    q, k, v = workloads.random_inputs(77, 2, 4, 130, 64, 64, "f32")
+    q[..., 0, :] *= 10.0
+    got = run_causal(q, k, v, "f32", 128)
+    np.testing.assert_allclose(got[..., 0, :], v[..., 0, :], rtol=1e-5, atol=1e-6)
+
+
+def test_causal_bf16_workload(orc):
+    w = workloads.CAUSAL_BF16
+    q, k, v = workloads.forward_inputs(w)
+    got = run_causal(q, k, v, w.dtype, w.chunk, w.eps)
+    ref = orc.causal_recurrent(q, k, v, w.eps)
+    e = assert_parity(got, ref, "bf16", w.name)
+    print(w.name, e)
+
+
+def test_causal_bf16_long_workload(orc):
+    """B=1 H=32 N=65536 d=128 (device-drawn inputs): sampled heads fully against
+    the oracle, every head against the prefix convex-hull property."""
+    w = workloads.CAUSAL_BF16_LONG
+    q, k, v = workloads.device_forward_inputs(w)
+    o = la().la_forward_causal(q, k, v, chunk=w.chunk, eps=w.eps)
+    torch.cuda.synchronize()
+    assert la().la_get_device_status() == 0
+    assert bool(torch.isfinite(o.float()).all())
+    # every head: o_i within the per-component hull of v_0..v_i (bf16 output rounding slack)
+    vf = v.float()
+    lo = torch.cummin(vf, dim=2).values
+    hi = torch.cummax(vf, dim=2).values
+    of = o.float()
+    slack = 1e-2
+    assert bool((of >= lo - slack).all()) and bool((of <= hi + slack).all())
+    del vf, lo, hi, of
+    heads = [0, 7, 19, 31]
+    hq, hk, hv = (workloads.to_host_bits(t[:, heads]) for t in (q, k, v))
+    ref = orc.causal_recurrent(hq, hk, hv, w.eps)
+    got = from_dev(o[:, heads])
+    e = assert_parity(got, ref, "bf16", w.name)
+    # the late rows have small magnitude; check they are not a near-zero wrong answer
+    tail = errors(got[:, :, -w.chunk:], ref[:, :, -w.chunk:])
+    assert tail["normwise"] < 2e-2, tail
+    for band in range(0, w.N, 4096):
+        gmax = np.abs(got[:, :, band:band + 4096]).max()
+        rmax = np.abs(ref[:, :, band:band + 4096]).max()
+        assert abs(gmax - rmax) <= 0.1 * rmax, (band, gmax, rmax)
+    print(w.name, e, tail)
+
+
+# ------------------------------------------------------------------------- non-causal
+def run_noncausal(q, k, v, dtype, eps=1e-6):
+    o = la().la_forward_noncausal(to_dev(q, dtype), to_dev(k, dtype), to_dev(v, dtype), eps=eps)
+    torch.cuda.synchronize()
+    return from_dev(o)
+
+
+def test_noncausal_bf16_workload(orc):
+    w = workloads.NONCAUSAL_BF16
+    q, k, v = workloads.forward_inputs(w)
+    got = run_noncausal(q, k, v, w.dtype, w.eps)
+    ref = orc.noncausal(q, k, v, w.eps)
+    e = assert_parity(got, ref, "bf16", w.name)
+    print(w.name, e)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("N,dk,dv", [(1, 32, 32), (65, 64, 64), (257, 128, 64), (1000, 64, 128),
+                                     (4097, 128, 128)])
+def test_noncausal_small_cases(orc, dtype, N, dk, dv):
+    q, k, v = workloads.random_inputs(2000 + N, 2, 2, N, dk, dv, dtype)
+    got = run_noncausal(q, k, v, dtype)
+    assert_parity(got, orc.noncausal(q, k, v), dtype, (N, dk, dv))
+
+
+# ------------------------------------------------------------------------ prefill, decode
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("N,dk,dv", [(0, 64, 64), (1, 32, 64), (200, 64, 64), (512, 128, 128)])
+def test_prefill_state(orc, dtype, N, dk, dv):
+    _, k, v = workloads.random_inputs(3000 + N, 2, 3, N, dk, dv, dtype)
+    S, z = la().la_prefill_state(to_dev(k, dtype), to_dev(v, dtype))
+    torch.cuda.synchronize()
+    Sr, zr = orc.prefill_state(k, v)
+    S, z = from_dev(S), from_dev(z)
+    if N == 0:
+        assert not S.any() and not z.any()
+        return
+    assert errors(S, Sr)["normwise"] < 1e-5 and errors(z, zr)["normwise"] < 1e-6
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("dk,dv", [(32, 32), (64, 128), (128, 64), (128, 128)])
+def test_decode_small(orc, dtype, dk, dv):
+    """Prefill 40 tokens then 24 steps; every step's o against the oracle recurrence."""
+    BH_B, BH_H, P, T = 3, 5, 40, 24
+    q, k, v = workloads.random_inputs(4000 + dk + dv, BH_B, BH_H, P + T, dk, dv, dtype)
+    S, z = la().la_prefill_state(to_dev(k[:, :, :P], dtype), to_dev(v[:, :, :P], dtype))
+    full = orc.causal_recurrent(q, k, v)
+    for t in range(P, P + T):
+        o = la().la_decode_step(S, z, to_dev(q[:, :, t], dtype), to_dev(k[:, :, t], dtype),
+                                to_dev(v[:, :, t], dtype))
+        torch.cuda.synchronize()
+        assert_parity(from_dev(o), full[:, :, t], dtype, ("step", t))
+    Sr, zr = orc.prefill_state(k, v)
+    assert errors(from_dev(S), Sr)["normwise"] < 1e-5
+    assert errors(from_dev(z), zr)["normwise"] < 1e-6
+
+
+def test_decode_workload_sampled(orc):
+    """128 x 32 heads, d=128 (device-drawn inputs): 512-token prefill, then 1024
+    single-token steps.  Sampled heads are checked at every step and in their
+    final state."""
+    w = workloads.DECODE_BF16
+    (qp, kp, vp), (qd, kd, vd) = workloads.device_decode_inputs(w)
+    S, z = la().la_prefill_state(kp, vp)
+    rng = np.random.default_rng(99)
+    flat = np.sort(rng.choice(w.BH, size=48, replace=False))
+    fi = torch.from_numpy(flat).cuda()
+    o = torch.empty((w.B, w.H, w.dv), dtype=torch.bfloat16, device="cuda")
+    outs = torch.empty((w.steps, len(flat), w.dv), dtype=torch.bfloat16, device="cuda")
+    for t in range(w.steps):
+        la().la_decode_step(S, z, qd[t], kd[t], vd[t], o)
+        outs[t] = o.view(w.BH, w.dv).index_select(0, fi)
+    torch.cuda.synchronize()
+    assert la().la_get_device_status() == 0
+    got = from_dev(outs)
+
+    kp_h = workloads.to_host_bits(kp.view(w.BH, w.N, w.dk).index_select(0, fi))
+    vp_h = workloads.to_host_bits(vp.view(w.BH, w.N, w.dv).index_select(0, fi))
+    qd_h = workloads.to_host_bits(qd.view(w.steps, w.BH, w.dk).index_select(1, fi))
+    kd_h = workloads.to_host_bits(kd.view(w.steps, w.BH, w.dk).index_select(1, fi))
+    vd_h = workloads.to_host_bits(vd.view(w.steps, w.BH, w.dv).index_select(1, fi))
+    Sr, zr = orc.prefill_state(kp_h, vp_h)
+    ref = np.empty_like(got)
+    for t in range(w.steps):
+        ref[t] = orc.decode_step(Sr, zr, qd_h[t], kd_h[t], vd_h[t], w.eps)
+    e = assert_parity(got, ref, "bf16", w.name)
+    Sg = from_dev(S.view(w.BH, w.dk, w.dv).index_select(0, fi))
+    zg = from_dev(z.view(w.BH, w.dk).index_select(0, fi))
+    es, ez = errors(Sg, Sr), errors(zg, zr)
+    assert es["normwise"] < 1e-5 and ez["normwise"] < 1e-6, (es, ez)
+    print(w.name, e, es, ez)
+
+
+# ---------------------------------------------------------------------- edges, canaries
+def test_empty_problems_touch_nothing():
+    sentinel = torch.full((64,), 7.0, dtype=torch.float32, device="cuda")
+    q = torch.empty((1, 2, 0, 64), dtype=torch.float32, device="cuda")
+    o = la().la_forward_causal(q, q, q, chunk=64)
+    assert o.numel() == 0
+    S = torch.full((2, 3, 64, 64), 7.0, device="cuda")
+    z = torch.full((2, 3, 64), 7.0, device="cuda")
+    k0 = torch.empty((2, 3, 0, 64), dtype=torch.float32, device="cuda")
+    la().la_prefill_state(k0, k0, S, z)   # N = 0 writes zeros
+    torch.cuda.synchronize()
+    assert not S.any() and not z.any()
+    assert torch.all(sentinel == 7.0)
+
+
+@pytest.mark.parametrize("path", ["causal", "noncausal", "decode"])
+def test_output_guard_canaries(path):
+    """Outputs written into the middle of a sentinel-filled buffer: the padding
+    on both sides stays untouched."""
+    B, H, N, d = 2, 3, 150, 64
+    pad = 256
+    dtype = torch.bfloat16
+    gen = torch.Generator(device="cuda").manual_seed(5)
+    if path == "decode":
+        n_out = B * H * d
+        q = torch.randn((B, H, d), device="cuda", generator=gen).to(dtype)
+        S = torch.zeros((B, H, d, d), device="cuda")
+        z = torch.zeros((B, H, d), device="cuda")
+    else:
+        n_out = B * H * N * d
+        q = torch.randn((B, H, N, d), device="cuda", generator=gen).to(dtype)
+    buf = torch.full((n_out + 2 * pad,), 12345.0, dtype=dtype, device="cuda")
+    o = buf[pad:pad + n_out].view(q.shape)
+    if path == "causal":
+        la().la_forward_causal(q, q, q, o, chunk=128)
+    elif path == "noncausal":
+        la().la_forward_noncausal(q, q, q, o)
+    else:
+        la().la_decode_step(S, z, q, q, q, o)
+    torch.cuda.synchronize()
+    assert torch.all(buf[:pad] == 12345.0) and torch.all(buf[pad + n_out:] == 12345.0)
+    assert torch.all(torch.isfinite(o.float()))
+
+
+def test_unsupported_shape_raises():
+    q = torch.zeros((1, 1, 8, 48), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(la().LAError) as ei:
+        la().la_forward_causal(q, q, q, chunk=128)
+    assert ei.value.status == 2

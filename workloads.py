@@ -4,13 +4,19 @@ This module is shared by the oracle's tests, the CUDA path's parity tests, the
 smoke check and the benchmark.  It holds no arithmetic of the method itself:
 it only draws Gaussian q, k, v with a fixed seed and rounds them to bf16.
 
-Recipe (the same for every workload):
+Host recipe (small workloads and all CPU tests):
   * ``rng = numpy.random.default_rng(seed)``;
   * draw q, then k, then v, each ``rng.standard_normal(shape, float32) * sigma``
     (sigma is 1 or 0.5, both exact powers of two, so scaling is exact);
   * for bf16 workloads round each float32 value to bf16 with
     round-to-nearest-even; the same bf16 bits go to the GPU and, widened, to
     the oracle.
+
+Device recipe (the two large workloads, 0.8e9 and 2.4e9 values, which take
+minutes to draw on the host): the same draw order and scaling from
+``torch.Generator(device).manual_seed(seed)`` (Philox), ``torch.randn`` in
+float32, then ``.to(torch.bfloat16)`` (round-to-nearest-even).  The oracle
+receives host copies of exactly these bf16 values.
 
 The pages ("Linear attention", learn.pranaymahendrakar.com, Developer
 listing; "Linear attention: change the order.", implementation section) use
@@ -67,8 +73,12 @@ def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
     Inputs here are finite Gaussian draws, so NaN/Inf handling is not needed.
     """
     u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
-    rounded = u + np.uint32(0x7FFF) + ((u >> np.uint32(16)) & np.uint32(1))
-    return (rounded >> np.uint32(16)).astype(np.uint16)
+    lsb = u >> np.uint32(16)
+    lsb &= np.uint32(1)
+    lsb += np.uint32(0x7FFF)
+    lsb += u
+    lsb >>= np.uint32(16)
+    return lsb.astype(np.uint16)
 
 
 def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
@@ -160,3 +170,48 @@ class DecodeInputs:
 def iter_heads(BH: int, group: int) -> Iterator[Tuple[int, int]]:
     for s in range(0, BH, group):
         yield s, min(BH, s + group)
+
+
+# ---------------------------------------------------------------------------
+# Device recipe (torch, Philox) for the large workloads.
+# ---------------------------------------------------------------------------
+def _torch_dtype(dtype: str):
+    import torch
+    return torch.bfloat16 if dtype == "bf16" else torch.float32
+
+
+def _device_draw(gen, shape, sigma, dtype, device):
+    import torch
+    x = torch.randn(shape, generator=gen, device=device, dtype=torch.float32)
+    if sigma != 1.0:
+        x.mul_(sigma)
+    return x.to(_torch_dtype(dtype))
+
+
+def device_forward_inputs(w: Workload, device: str = "cuda"):
+    """q, k [B,H,N,dk], v [B,H,N,dv] as torch tensors drawn on ``device``."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(w.seed)
+    q = _device_draw(g, (w.B, w.H, w.N, w.dk), w.sigma, w.dtype, device)
+    k = _device_draw(g, (w.B, w.H, w.N, w.dk), w.sigma, w.dtype, device)
+    v = _device_draw(g, (w.B, w.H, w.N, w.dv), w.sigma, w.dtype, device)
+    return q, k, v
+
+
+def device_decode_inputs(w: Workload, device: str = "cuda"):
+    """Prefill q,k,v [B,H,N,d] then decode q,k,v [steps,B,H,d], drawn on ``device``."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(w.seed)
+    pre = tuple(_device_draw(g, (w.B, w.H, w.N, d), w.sigma, w.dtype, device) for d in (w.dk, w.dk, w.dv))
+    dec = tuple(_device_draw(g, (w.steps, w.B, w.H, d), w.sigma, w.dtype, device) for d in (w.dk, w.dk, w.dv))
+    return pre, dec
+
+
+def to_host_bits(t) -> np.ndarray:
+    """Host copy of a device tensor in the oracle's input form (bf16 bits or float32)."""
+    import torch
+    if t.dtype == torch.bfloat16:
+        return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+    return t.contiguous().cpu().numpy().astype(np.float32)
