@@ -131,10 +131,11 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index=0, period_ms=100):
+    def __init__(self, gpu_index=0, period_ms=100, load_watts=200.0):
         self.proc = None
         self.gpu_index = gpu_index
         self.period_ms = period_ms
+        self.load_watts = load_watts
 
     def start(self):
         try:
@@ -164,11 +165,11 @@ class ClockSampler:
                 continue
             smax = m
             sm.append(s)
-            if pw > 250.0:  # under load
+            if pw > self.load_watts:
                 loaded.append(s)
-                for n, val in zip(names, r[5:9]):
-                    if val.strip().lower().startswith("active"):
-                        reasons.add(n)
+            for n, val in zip(names, r[5:9]):
+                if val.strip().lower().startswith("active"):
+                    reasons.add(n)
         use = loaded if loaded else sm
         return {"sm_mhz": statistics.median(use) if use else None, "sm_max_mhz": smax,
                 "reasons": sorted(reasons), "samples": len(rows), "samples_under_load": len(loaded)}
@@ -222,7 +223,7 @@ def _graph_steps(torch, fn, n, stream):
     return graphs
 
 
-def time_graph_steps(torch, la, fn, steps, warmup, dist):
+def time_graph_steps(torch, la, fn, steps, warmup, dist, sampler=None):
     """W warm-up steps, then exactly `steps` timed steps, all replayed from CUDA
     graphs on one side stream; CUDA events on that stream bracket the timed
     steps, with a barrier and device synchronisation on both sides.  Returns
@@ -244,16 +245,20 @@ def time_graph_steps(torch, la, fn, steps, warmup, dist):
     torch.cuda.synchronize()
     dist.barrier()
     torch.cuda.synchronize()
+    if sampler is not None:
+        sampler.start()
+        time.sleep(0.25)  # let the sampler take its first reading before the timed region
     with torch.cuda.stream(stream):
         start.record(stream)
         for g in timed:
             g.replay()
         stop.record(stream)
     torch.cuda.synchronize()
+    clocks = sampler.stop() if sampler is not None else None
     dist.barrier()
     secs = start.elapsed_time(stop) / 1e3
     del timed, warm
-    return secs, launches
+    return secs, launches, clocks
 
 
 def dev_copy(torch, x, dtype):
@@ -266,7 +271,7 @@ def n_rotations(bytes_per_set):
     return max(2, math.ceil(4 * L2_BYTES / bytes_per_set))
 
 
-def bench_causal_headline(torch, la, w, steps, warmup, dist, peaks, src):
+def bench_causal_headline(torch, la, w, steps, warmup, dist, peaks, src, sampler=None):
     q, k, v = workloads.forward_inputs(w)
     es = 2 if w.dtype == "bf16" else 4
     nbytes = forward_bytes(w.BH, w.N, w.dk, w.dv, es)
@@ -278,8 +283,8 @@ def bench_causal_headline(torch, la, w, steps, warmup, dist, peaks, src):
         s = sets[i % R]
         la.la_forward_causal(s[0], s[1], s[2], s[3], chunk=w.chunk, eps=w.eps)
 
-    secs, launches = time_graph_steps(torch, la, step, steps, warmup, dist)
-    return secs, launches, nbytes, R
+    secs, launches, clocks = time_graph_steps(torch, la, step, steps, warmup, dist, sampler)
+    return secs, launches, nbytes, R, clocks
 
 
 def bench_causal_e2e(torch, la, w, steps, warmup, dist):
@@ -333,7 +338,7 @@ def bench_path_causal_long(torch, la, reps, peaks, src):
     def step(i):
         la.la_forward_causal(q, k, v, o, chunk=w.chunk, eps=w.eps)
 
-    secs, launches = time_graph_steps(torch, la, step, reps, 2, Dist())
+    secs, launches, _ = time_graph_steps(torch, la, step, reps, 3, Dist())
     t = secs / reps
     nbytes = forward_bytes(w.BH, w.N, w.dk, w.dv, 2)
     fl = causal_flops(w.BH, w.N, w.dk, w.dv, w.chunk)
@@ -355,7 +360,7 @@ def bench_path_noncausal(torch, la, reps, peaks, src):
         s = sets[i % R]
         la.la_forward_noncausal(s[0], s[1], s[2], s[3], eps=w.eps)
 
-    secs, launches = time_graph_steps(torch, la, step, reps, 3, Dist())
+    secs, launches, _ = time_graph_steps(torch, la, step, reps, 3, Dist())
     t = secs / reps
     fl = noncausal_flops(w.BH, w.N, w.dk, w.dv)
     return {"workload": w.name, "value": round(w.B * w.N / t, 1), "unit": "tokens/s",
@@ -376,7 +381,7 @@ def bench_path_decode(torch, la, steps, peaks, src):
         la.la_decode_step(S, z, qd[i], kd[i], vd[i], o, eps=w.eps)
 
     n = min(steps, w.steps)
-    secs, launches = time_graph_steps(torch, la, step, n, 3, Dist())
+    secs, launches, _ = time_graph_steps(torch, la, step, n, 3, Dist())
     S.copy_(S0)
     z.copy_(z0)
     t = secs / n
@@ -390,7 +395,7 @@ def bench_path_decode(torch, la, steps, peaks, src):
 
 
 # --------------------------------------------------------------------------- CPU oracle
-def oracle_causal_sample(w, target_s=10.0, max_reps=50):
+def oracle_causal_sample(w, target_s=10.0, max_reps=100000):
     """The float64 oracle (as it stands) on a bounded sample of workload w:
     whole (b,h) sequences, repeated until about target_s seconds.  Returns
     (tokens/s scaled to full positions, threads, description)."""
@@ -464,9 +469,9 @@ def run_gpu(args, dist):
     peaks, src = load_peaks()
     w = workloads.CAUSAL_BF16
 
-    sampler = ClockSampler(gpu_index=torch.cuda.current_device()).start() if dist.rank == 0 else None
-    secs, launches, nbytes, R = bench_causal_headline(torch, la, w, args.steps, args.warmup, dist, peaks, src)
-    clocks = sampler.stop() if sampler else None
+    sampler = ClockSampler(gpu_index=torch.cuda.current_device(), period_ms=50) if dist.rank == 0 else None
+    secs, launches, nbytes, R, clocks = bench_causal_headline(torch, la, w, args.steps, args.warmup, dist, peaks,
+                                                              src, sampler)
     secs_max = dist.max(secs)
     t_step = secs_max / args.steps
     value = dist.world * w.B * w.N * args.steps / secs_max
