@@ -14,11 +14,11 @@ Tensors are PyTorch CUDA tensors (PyTorch supplies device memory and streams):
 from __future__ import annotations
 
 from ._binding import (LA_BF16, LA_F32, LAError, lib_path, la_decode_step, la_forward_causal,
-                       la_forward_noncausal, la_get_device_status, la_kernel_launches, la_last_cuda_error,
+                       la_forward_noncausal, la_forward_noncausal_noalloc, la_get_device_status, la_kernel_launches, la_last_cuda_error,
                        la_prefill_state, la_status_string, la_version, load_library)
 
 __all__ = [
     "LA_BF16", "LA_F32", "LAError", "lib_path", "la_decode_step", "la_forward_causal",
-    "la_forward_noncausal", "la_get_device_status", "la_kernel_launches", "la_last_cuda_error", "la_prefill_state",
+    "la_forward_noncausal", "la_forward_noncausal_noalloc", "la_get_device_status", "la_kernel_launches", "la_last_cuda_error", "la_prefill_state",
     "la_status_string", "la_version", "load_library",
 ]

@@ -36,6 +36,7 @@ def _declare(lib):
     sigs = {
         "la_forward_causal": [P, P, P, P, I, I, I, I, I, I, F, I, P],
         "la_forward_noncausal": [P, P, P, P, I, I, I, I, I, F, I, P],
+        "la_forward_noncausal_noalloc": [P, P, P, P, I, I, I, I, I, F, I, P],
         "la_decode_step": [P, P, P, P, P, P, I, I, I, I, F, I, P],
         "la_prefill_state": [P, P, P, P, I, I, I, I, I, I, P],
         "la_get_device_status": [P],
@@ -142,6 +143,22 @@ def la_forward_noncausal(q, k, v, o=None, eps: float = 1e-6, stream=None):
     st = load_library().la_forward_noncausal(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
                                              B, H, N, dk, dv, float(eps), _dtype_code(q), _stream_ptr(stream))
     _check("la_forward_noncausal", st)
+    return o
+
+
+def la_forward_noncausal_noalloc(q, k, v, o, eps: float = 1e-6, stream=None):
+    """Non-causal forward using the library's fixed scratch array (no device
+    allocation by the library).  `o` must be supplied by the caller."""
+    _need_cuda(q, k, v, o)
+    _same_dtype(q, k, v, o)
+    B, H, N, dk = q.shape
+    dv = v.shape[-1]
+    if tuple(k.shape) != (B, H, N, dk) or tuple(v.shape[:-1]) != (B, H, N) or tuple(o.shape) != (B, H, N, dv):
+        raise ValueError("shape mismatch")
+    st = load_library().la_forward_noncausal_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                                     B, H, N, dk, dv, float(eps), _dtype_code(q),
+                                                     _stream_ptr(stream))
+    _check("la_forward_noncausal_noalloc", st)
     return o
 
 

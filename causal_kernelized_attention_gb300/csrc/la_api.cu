@@ -124,6 +124,17 @@ la_status la_forward_noncausal(const void *q, const void *k, const void *v, void
     return noncausal_simt(p);
 }
 
+la_status la_forward_noncausal_noalloc(const void *q, const void *k, const void *v, void *o, int B, int H,
+                                       int N, int dk, int dv, float eps, la_dtype dtype, la_stream_t stream)
+{
+    bool empty;
+    la_status st = check_forward(q, k, v, o, B, H, N, dk, dv, eps, dtype, &empty);
+    if (st != LA_OK || empty) return st;
+    if (!supported_dim(dk) || !supported_dim(dv)) return LA_ERR_UNSUPPORTED;
+    Problem p{q, k, v, o, B * H, N, dk, dv, 0, eps, dtype, (cudaStream_t)stream};
+    return noncausal_simt_noalloc(p);
+}
+
 la_status la_decode_step(float *S, float *z, const void *q, const void *k, const void *v, void *o, int B,
                          int H, int dk, int dv, float eps, la_dtype dtype, la_stream_t stream)
 {

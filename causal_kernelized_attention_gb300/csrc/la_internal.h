@@ -30,6 +30,8 @@ struct Problem {
 // SIMT kernels (la_simt.cu): fp32 CUDA-core arithmetic, any supported dtype.
 la_status causal_simt(const Problem &p);
 la_status noncausal_simt(const Problem &p);
+// Same computation with the library's fixed scratch array (no allocation).
+la_status noncausal_simt_noalloc(const Problem &p);
 // S, z (fp32, [BH,dk,dv], [BH,dk]) = sums over N tokens; overwrites S and z.
 la_status state_simt(const void *k, const void *v, float *S, float *z, int BH, int N, int dk,
                      int dv, la_dtype dtype, cudaStream_t stream);

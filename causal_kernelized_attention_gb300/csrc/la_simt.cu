@@ -306,3 +306,83 @@ la_status state_simt(const void *k, const void *v, float *S, float *z, int BH, i
 }
 
 }  // namespace la
+
+// ---------------------------------------------------------------------------
+// Allocation-free non-causal forward (la_forward_noncausal_noalloc).
+//
+// Same kernels as the non-causal path above, but the S and z partial sums live
+// in a fixed array compiled into the library instead of stream-ordered scratch.
+// The array is shared by every call on a device and keeps the previous call's
+// contents; launch_state clears the part a call uses before accumulating.
+// Calls whose work overlaps on the GPU (other streams, other host threads) race
+// on it.
+// ---------------------------------------------------------------------------
+#include <mutex>
+#include <unordered_map>
+
+namespace la {
+namespace {
+
+static __device__ __align__(256) float g_noalloc_scratch[LA_NOALLOC_SCRATCH_BYTES / sizeof(float)];
+
+// Device address of g_noalloc_scratch on the current device.  In host code the
+// symbol is only a host-side stand-in, so the address is looked up with
+// cudaGetSymbolAddress once per device (with that device current) and cached.
+la_status noalloc_scratch(float **out)
+{
+    static std::mutex mu;
+    static std::unordered_map<int, float *> addr;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_status(e);
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = addr.find(dev);
+    if (it == addr.end()) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) return cuda_status(e);
+        it = addr.emplace(dev, (float *)p).first;
+    }
+    *out = it->second;
+    return LA_OK;
+}
+
+template <typename T, int DK>
+la_status launch_noncausal_noalloc(const Problem &p, float *scratch)
+{
+    const size_t s_elems = (size_t)p.BH * DK * p.dv;
+    float *S = scratch, *z = scratch + s_elems;  // s_elems is a multiple of 4: z stays 16-byte aligned
+    la_status st = launch_state<T, DK>(p.k, p.v, S, z, p.BH, p.N, p.dv, p.stream);
+    if (st != LA_OK) return st;
+    dim3 grid(ceil_div(p.N, 64), p.BH, ceil_div(p.dv, kDVS));
+    count_launches();
+    apply_simt_kernel<T, DK><<<grid, kThreads, 0, p.stream>>>((const T *)p.q, S, z, (T *)p.o, p.N, p.dv, p.eps);
+    return cuda_status(cudaGetLastError());
+}
+
+template <typename T>
+la_status noncausal_noalloc_by_dk(const Problem &p, float *scratch)
+{
+    switch (p.dk) {
+    case 32: return launch_noncausal_noalloc<T, 32>(p, scratch);
+    case 64: return launch_noncausal_noalloc<T, 64>(p, scratch);
+    case 128: return launch_noncausal_noalloc<T, 128>(p, scratch);
+    }
+    return LA_ERR_UNSUPPORTED;
+}
+
+}  // namespace
+
+la_status noncausal_simt_noalloc(const Problem &p)
+{
+    if (!supported_dim(p.dk) || !supported_dim(p.dv)) return LA_ERR_UNSUPPORTED;
+    const size_t need = sizeof(float) * (size_t)p.BH * p.dk * ((size_t)p.dv + 1);
+    if (need > LA_NOALLOC_SCRATCH_BYTES) return LA_ERR_UNSUPPORTED;
+    float *scratch = nullptr;
+    la_status st = noalloc_scratch(&scratch);
+    if (st != LA_OK) return st;
+    return p.dtype == LA_F32 ? noncausal_noalloc_by_dk<float>(p, scratch)
+                             : noncausal_noalloc_by_dk<__nv_bfloat16>(p, scratch);
+}
+
+}  // namespace la

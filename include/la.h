@@ -91,6 +91,36 @@ la_status la_forward_noncausal(const void *q, const void *k, const void *v, void
                                int B, int H, int N, int dk, int dv, float eps,
                                la_dtype dtype, la_stream_t stream);
 
+/* Size of the scratch array built into the library for la_forward_noncausal_noalloc. */
+#define LA_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+/*
+ * Non-causal forward that allocates no device memory.  The pages have no
+ * counterpart of this entry point: it is the same computation as
+ * la_forward_noncausal (same arguments, layouts and results up to the order
+ * of floating-point additions), offered for callers that cannot call
+ * cudaMalloc or cudaMallocAsync -- for example a host program that has handed
+ * all device memory to its own pool allocator (so a driver allocation would
+ * fail or break its accounting), or a serving loop that forbids allocation
+ * calls once it has started so that its latency and memory use stay fixed.
+ *
+ * Its scratch (the per-head S and z sums, B*H*dk*(dv+1) floats) lives in one
+ * array of LA_NOALLOC_SCRATCH_BYTES bytes compiled into the library; every GPU
+ * that loads the library holds that array until the process exits.  Problems
+ * needing more than LA_NOALLOC_SCRATCH_BYTES bytes of scratch are rejected
+ * with LA_ERR_UNSUPPORTED before any work is enqueued.
+ *
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current) and caches it; make that
+ * first call before any stream capture.  All calls share the one array, and
+ * each call clears the part it uses before accumulating into it, so calls
+ * whose work may overlap on the GPU (different streams, different host
+ * threads) race with each other and must be serialised by the caller.
+ */
+la_status la_forward_noncausal_noalloc(const void *q, const void *k, const void *v, void *o,
+                                       int B, int H, int N, int dk, int dv, float eps,
+                                       la_dtype dtype, la_stream_t stream);
+
 /*
  * One recurrent decode step for B*H independent heads ("Linear Attention",
  * "It is a linear RNN": O(d^2) per token with a fixed-size state;
