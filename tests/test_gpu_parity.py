@@ -64,6 +64,21 @@ def test_causal_small_cases(orc, dtype, N, dk, dv, chunk):
     assert_parity(got, ref, dtype, (N, dk, dv, chunk))
 
 
+@pytest.mark.parametrize("B,H,N,d", [
+    (1, 1, 128, 64), (1, 1, 128, 128), (2, 3, 129, 64), (1, 2, 255, 128), (3, 2, 1000, 64),
+    (2, 3, 5000, 128), (1, 4, 2048, 64), (2, 1, 76800, 128),
+])
+def test_causal_tensor_core_shapes(orc, B, H, N, d):
+    """Shapes of the tensor-core path (bf16, dk = dv in {64, 128}, chunk 128):
+    ragged last chunks, one and many segments per head, long few-head sequences
+    (several chained segments of 8 chunks)."""
+    q, k, v = workloads.random_inputs(5000 + N + d, B, H, N, d, d, "bf16")
+    got = run_causal(q, k, v, "bf16", 128)
+    ref = orc.causal_recurrent(q, k, v)
+    e = assert_parity(got, ref, "bf16", (B, H, N, d))
+    assert e["normwise"] < 2e-2, e
+
+
 def test_causal_output0_is_v0(orc):
     # "26. Linear (Kernelized) Attention", Step-by-Step step 6: o_0 = v_0 for any q_0.
     q, k, v = workloads.random_inputs(77, 2, 4, 130, 64, 64, "f32")
