@@ -23,12 +23,13 @@
 //      S  += phi(K_c)^T V_c,  z += phi(K_c)^T 1          (running state, fp32 TMEM)
 //    o = O / max(rs + qz, eps), written as bf16.
 //
-// Warp roles (512 threads): warps 0-3 apply phi in shared memory; warp 4 issues
-// TMA loads; warp 5 issues MMAs and owns TMEM; warps 8-11 turn T into P; warps
-// 12-15 normalise O, refresh the bf16 copy of S and run phase B.  Every wait
-// is bounded by %globaltimer; on expiry the CTA records LA_ERR_TIMEOUT in its
-// status word, abandons its work, drains its in-flight copies and MMAs, and
-// frees its TMEM.
+// Warp roles (640 threads): warps 0-7 apply phi in shared memory; warp 8 issues
+// TMA loads; warp 9 issues MMAs and owns TMEM; warps 12-15 turn T into P; warps
+// 16-19 normalise O, refresh the bf16 copy of S and run phase B.  Waiting
+// threads sleep on the mbarrier (suspend-time hint) rather than spin, so they
+// leave issue slots to the working warps.  Every wait is bounded by
+// %globaltimer; on expiry the CTA records LA_ERR_TIMEOUT in its status word,
+// abandons its work, drains its in-flight copies and MMAs, and frees its TMEM.
 #include "la_common.cuh"
 #include "la_internal.h"
 #include "la_sm100.cuh"
@@ -45,8 +46,10 @@ using namespace sm100;
 static __device__ unsigned g_tc_status;
 
 constexpr int kC = 128;                  // chunk (tokens per tile)
-constexpr int kThreads = 512;
-constexpr int kTmaWarp = 4, kMmaWarp = 5, kEpiPWarp0 = 8, kEpiOWarp0 = 12;
+constexpr int kThreads = 640;
+constexpr int kPhiThreads = 256;         // warps 0-7
+constexpr int kTmaWarp = 8, kMmaWarp = 9, kEpiPWarp0 = 12, kEpiOWarp0 = 16;
+constexpr uint32_t kSleepHintNs = 200000;  // per try_wait; the total wait stays bounded below
 constexpr uint32_t kBox = kC * 128;      // one [128 rows x 64 bf16] swizzled box: 16 KB
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far beyond any healthy wait
 constexpr uint32_t kFlagReady = 1, kFlagError = 2;
@@ -100,7 +103,7 @@ __device__ __forceinline__ bool wait_bar(int *abort_flag, uint64_t *bar, uint32_
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_sleep(bar, parity, kSleepHintNs)) return true;
         if (aborted(abort_flag)) return false;
         if (globaltimer_ns() - t0 > kWaitLimitNs) {
             *(volatile int *)abort_flag = 1;
@@ -123,27 +126,55 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b)
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
-// phi on one row of a tile (all D/64 boxes), in place; rows >= valid become 0.
-template <int D>
-__device__ __forceinline__ void phi_row(uint8_t *tile, int row, bool valid)
+// phi on a pair of bf16 values: exp(min(x, 0)) + max(x, 0), which is x + 1 for
+// x > 0 and exp(x) otherwise; min, max and the final add in packed bf16 (exact
+// except the single rounding of the sum), exp in fp32.
+__device__ __forceinline__ uint32_t phi2(uint32_t w)
 {
+    const __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162 *>(&w);
+    const __nv_bfloat162 zero = __float2bfloat162_rn(0.f);
+    const float2 nf = __bfloat1622float2(__hmin2(x, zero));
+    const __nv_bfloat162 e = __floats2bfloat162_rn(__expf(nf.x), __expf(nf.y));
+    const __nv_bfloat162 r = __hadd2(e, __hmax2(x, zero));
+    return *reinterpret_cast<const uint32_t *>(&r);
+}
+
+// phi in place on shared-memory tiles, by the 256 phi threads.  A unit is half of
+// one 128-byte row of a 64-column box (4 chunks of 16 bytes); thread t takes units
+// t, t + 256, ...  Units of rows >= `valid` (past the end of the sequence) are
+// zeroed.  All loads of a thread are issued before its arithmetic.  The chunk
+// order is rotated by the row so that the 8 threads of a quarter-warp (8
+// consecutive rows) touch 8 different bank groups.
+template <int D, int NU>
+__device__ __forceinline__ void phi_tiles(uint8_t *kt, uint8_t *qt, int t, int valid)
+{
+    constexpr int kUnitsPerTile = 128 * (D / 32);
+    uint4 buf[NU][4];
+    uint8_t *rowp[NU];
+    int rot[NU];
+    bool ok[NU];
 #pragma unroll
-    for (int b = 0; b < D / 64; ++b) {
-        uint8_t *rp = tile + b * kBox + row * 128;
+    for (int m = 0; m < NU; ++m) {
+        const int u = t + kPhiThreads * m;
+        uint8_t *tile = u < kUnitsPerTile ? kt : qt;
+        const int rem = u % kUnitsPerTile, row = rem & 127, hb = rem >> 7;
+        rowp[m] = tile + (hb >> 1) * kBox + row * 128;
+        rot[m] = row + (hb & 1) * 4;
+        ok[m] = row < valid;
 #pragma unroll
-        for (int p0 = 0; p0 < 8; ++p0) {
-            const int p = (p0 + row) & 7;  // rotate so 8 consecutive rows hit distinct banks
-            uint4 *ptr = reinterpret_cast<uint4 *>(rp + p * 16);
-            uint4 x = *ptr;
-            uint32_t *w = reinterpret_cast<uint32_t *>(&x);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float2 f = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162 *>(&w[e]));
-                w[e] = valid ? pack_bf16(phi_fast(f.x), phi_fast(f.y)) : 0u;
-            }
-            *ptr = x;
-        }
+        for (int k = 0; k < 4; ++k) buf[m][k] = *reinterpret_cast<const uint4 *>(rowp[m] + ((rot[m] + k) & 7) * 16);
     }
+#pragma unroll
+    for (int m = 0; m < NU; ++m)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            uint4 &x = buf[m][k];
+            x = ok[m] ? make_uint4(phi2(x.x), phi2(x.y), phi2(x.z), phi2(x.w)) : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+    for (int m = 0; m < NU; ++m)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) *reinterpret_cast<uint4 *>(rowp[m] + ((rot[m] + k) & 7) * 16) = buf[m][k];
 }
 
 // Descriptor helpers (see la_sm100.cuh for the layouts).
@@ -161,7 +192,7 @@ __device__ __forceinline__ uint64_t wdesc(uint32_t w, int kk)
 }
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(640, 1)
 causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                  const __grid_constant__ CUtensorMap map_v, const Params prm)
 {
@@ -184,7 +215,7 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
     if (tid == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(&sm.full[s], 1);
-            mbar_init(&sm.phi_done[s], 128);
+            mbar_init(&sm.phi_done[s], kPhiThreads);
             mbar_init(&sm.empty[s], 1);
         }
         mbar_init(&sm.t_full, 1);
@@ -221,16 +252,18 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
     const uint32_t tmem = sm.tmem_base;
     int *abort_flag = &sm.abort;
 
-    if (warp < 4) {
+    if (warp < kPhiThreads / 32) {
         // ---------------------------------------------------------------- phi warps
         for (int j = 0; j < total; ++j) {
             const int s = j % S, r = j / S;
             if (!wait_bar(abort_flag, &sm.full[s], r & 1)) break;
             const bool isC = j >= nA;
             const int chunk = c0 + (isC ? j - nA : j);
-            const bool valid = chunk * kC + tid < prm.N;
-            phi_row<D>(sm.k[s], tid, valid);
-            if (isC) phi_row<D>(sm.q[s], tid, valid);
+            const int valid = prm.N - chunk * kC;
+            if (isC)
+                phi_tiles<D, D / 32>(sm.k[s], sm.q[s], tid, valid);
+            else
+                phi_tiles<D, D / 64>(sm.k[s], sm.q[s], tid, valid);
             fence_proxy_async_smem();
             mbar_arrive(&sm.phi_done[s]);
         }
@@ -301,21 +334,20 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
                 for (int kk = 0; kk < D / 16; ++kk)
                     mma_ss(tmem + CF::tT, kmajor(qa, kk), kmajor(ka, kk), id_T, kk > 0 ? 1u : 0u);
                 mma_commit(&sm.t_full);
-                if (!(ok = wait_bar(abort_flag, &sm.p_full, cj & 1))) break;
-                tc_fence_after();
                 if (cj > 0 && !(ok = wait_bar(abort_flag, &sm.o_free, (cj - 1) & 1))) break;
-                tc_fence_after();
-#pragma unroll
-                for (int kk = 0; kk < kC / 16; ++kk) {
-                    mma_ts(tmem + CF::tO, tmem + CF::tP + kk * 8, mnmajor(va, kk, kBox), id_PV, kk > 0 ? 1u : 0u);
-                    mma_ts(tmem + CF::tRS, tmem + CF::tP + kk * 8, wdesc(w_addr, kk), id_W, kk > 0 ? 1u : 0u);
-                }
                 if (!(ok = wait_bar(abort_flag, &sm.s_ready, cj & 1))) break;
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    mma_ss(tmem + CF::tO, kmajor(qa, kk), mnmajor(sb_addr, kk, D * 128), id_QS, 1u);
+                    mma_ss(tmem + CF::tO, kmajor(qa, kk), mnmajor(sb_addr, kk, D * 128), id_QS, kk > 0 ? 1u : 0u);
                     mma_ss(tmem + CF::tQZ, kmajor(qa, kk), wdesc(w_addr, kk), id_W, kk > 0 ? 1u : 0u);
+                }
+                if (!(ok = wait_bar(abort_flag, &sm.p_full, cj & 1))) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < kC / 16; ++kk) {
+                    mma_ts(tmem + CF::tO, tmem + CF::tP + kk * 8, mnmajor(va, kk, kBox), id_PV, 1u);
+                    mma_ts(tmem + CF::tRS, tmem + CF::tP + kk * 8, wdesc(w_addr, kk), id_W, kk > 0 ? 1u : 0u);
                 }
                 mma_commit(&sm.o_full);
                 if (cj < nch - 1) {
@@ -342,23 +374,25 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
             if (!wait_bar_warp(abort_flag, &sm.t_full, cj & 1)) break;
             tc_fence_after();
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
-                uint32_t t[32];
-                tmem_ld32(tl + CF::tT + cc * 32, t);
+            for (int half = 0; half < 2; ++half) {
+                uint32_t t[64];
+                tmem_ld32(tl + CF::tT + half * 64, *reinterpret_cast<uint32_t(*)[32]>(&t[0]));
+                tmem_ld32(tl + CF::tT + half * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&t[32]));
                 tmem_ld_wait();
-                if (cc == 3) {
+                if (half == 1) {
                     tc_fence_before();
                     mbar_arrive(&sm.t_free);
                 }
-                uint32_t p[16];
+                uint32_t p[32];
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const int jk = cc * 32 + 2 * e;  // key index within the chunk
+                for (int e = 0; e < 32; ++e) {
+                    const int jk = half * 64 + 2 * e;  // key index within the chunk
                     const float a = jk <= i ? __uint_as_float(t[2 * e]) : 0.f;
                     const float b = jk + 1 <= i ? __uint_as_float(t[2 * e + 1]) : 0.f;
                     p[e] = pack_bf16(a, b);
                 }
-                tmem_st16(tl + CF::tP + cc * 16, p);
+                tmem_st16(tl + CF::tP + half * 32, *reinterpret_cast<uint32_t(*)[16]>(&p[0]));
+                tmem_st16(tl + CF::tP + half * 32 + 16, *reinterpret_cast<uint32_t(*)[16]>(&p[16]));
             }
             tmem_st_wait();
             tc_fence_before();
@@ -404,7 +438,7 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
                         v = kFlagError;
                         break;
                     }
-                    __nanosleep(64);
+                    __nanosleep(256);
                     v = ld_acquire_gpu(f);
                 }
                 if (v != kFlagReady) *(volatile int *)abort_flag = 1;
@@ -489,14 +523,15 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
             const int row = (c0 + cj) * kC + i;
             uint16_t *orow = prm.o + ((size_t)bh * prm.N + row) * D;
 #pragma unroll 1
-            for (int cc = 0; cc < D / 32; ++cc) {
-                uint32_t a[32];
-                tmem_ld32(tl + CF::tO + cc * 32, a);
+            for (int cc = 0; cc < D / 64; ++cc) {
+                uint32_t a[64];
+                tmem_ld32(tl + CF::tO + cc * 64, *reinterpret_cast<uint32_t(*)[32]>(&a[0]));
+                tmem_ld32(tl + CF::tO + cc * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&a[32]));
                 tmem_ld_wait();
                 if (row < prm.N) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(orow + cc * 32);
+                    uint4 *dst = reinterpret_cast<uint4 *>(orow + cc * 64);
 #pragma unroll
-                    for (int e = 0; e < 4; ++e)
+                    for (int e = 0; e < 8; ++e)
                         dst[e] = make_uint4(
                             pack_bf16(__uint_as_float(a[8 * e]) * inv, __uint_as_float(a[8 * e + 1]) * inv),
                             pack_bf16(__uint_as_float(a[8 * e + 2]) * inv, __uint_as_float(a[8 * e + 3]) * inv),
@@ -510,15 +545,14 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
                 if (!wait_bar_warp(abort_flag, &sm.s_full, cj & 1)) break;
                 tc_fence_after();
 #pragma unroll 1
-                for (int cc = 0; cc < D / 32; ++cc) {
-                    uint32_t a[32];
-                    tmem_ld32(tl + CF::tS + cc * 32, a);
+                for (int cc = 0; cc < D / 64; ++cc) {
+                    uint32_t a[64];
+                    tmem_ld32(tl + CF::tS + cc * 64, *reinterpret_cast<uint32_t(*)[32]>(&a[0]));
+                    tmem_ld32(tl + CF::tS + cc * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&a[32]));
                     tmem_ld_wait();
                     if (row_ok) {
-                        float x[32];
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) x[e] = __uint_as_float(a[e]);
-                        put_sb(cc * 32, x);
+                        put_sb(cc * 64, reinterpret_cast<const float *>(&a[0]));
+                        put_sb(cc * 64 + 32, reinterpret_cast<const float *>(&a[32]));
                     }
                 }
                 const float zv = __uint_as_float(tmem_ld1(tl + CF::tZ));
