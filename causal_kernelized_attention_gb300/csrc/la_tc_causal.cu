@@ -11,10 +11,10 @@
 //  * Phase A (segments with a successor): the segment's aggregate state
 //    A_g = sum_c phi(K_c)^T V_c and a_g = sum_c colsum phi(K_c) accumulate in
 //    tensor memory (TMEM).
-//  * Phase B: wait (bounded) for the inclusive prefix P_{g-1} of the previous
-//    segment of the same head, publish P_g = P_{g-1} + A_g, and load P_{g-1}
-//    as the running state.  This is the exclusive scan of the chunk states,
-//    done across segments, in fp32.
+//  * Phase B: the exclusive scan of the chunk states across segments, in fp32,
+//    by decoupled look-back: publish A_g, sum the predecessors' aggregates back
+//    to the nearest published inclusive prefix (bounded waits), publish
+//    P_g = P_{g-1} + A_g, and load P_{g-1} as the running state.
 //  * Phase C: sweep the segment's chunks.  Per chunk c, on the tensor cores:
 //      T   = phi(Q_c) phi(K_c)^T                         (fp32, TMEM)
 //      P   = bf16(tril(T))                               (TMEM, written by threads)
@@ -23,9 +23,9 @@
 //      S  += phi(K_c)^T V_c,  z += phi(K_c)^T 1          (running state, fp32 TMEM)
 //    o = O / max(rs + qz, eps), written as bf16.
 //
-// Warp roles (640 threads): warps 0-7 apply phi in shared memory; warp 8 issues
-// TMA loads; warp 9 issues MMAs and owns TMEM; warps 12-15 turn T into P; warps
-// 16-19 normalise O, refresh the bf16 copy of S and run phase B.  Waiting
+// Warp roles (576 threads): warps 0-7 apply phi in shared memory; warp 8 issues
+// TMA loads; warp 9 issues MMAs and owns TMEM; warps 10-13 turn T into P; warps
+// 14-17 normalise O and refresh the bf16 copy of S; warps 10-17 run phase B.  Waiting
 // threads sleep on the mbarrier (suspend-time hint) rather than spin, so they
 // leave issue slots to the working warps.  Every wait is bounded by
 // %globaltimer; on expiry the CTA records LA_ERR_TIMEOUT in its status word,
@@ -46,13 +46,18 @@ using namespace sm100;
 static __device__ unsigned g_tc_status;
 
 constexpr int kC = 128;                  // chunk (tokens per tile)
-constexpr int kThreads = 640;
+constexpr int kThreads = 576;
 constexpr int kPhiThreads = 256;         // warps 0-7
-constexpr int kTmaWarp = 8, kMmaWarp = 9, kEpiPWarp0 = 12, kEpiOWarp0 = 16;
+// Epilogue warps access the TMEM lane quadrant warp % 4, so each group of four
+// consecutive warps covers all 128 lanes.
+constexpr int kTmaWarp = 8, kMmaWarp = 9, kEpiPWarp0 = 10, kEpiOWarp0 = 14;
 constexpr uint32_t kSleepHintNs = 200000;  // per try_wait; the total wait stays bounded below
 constexpr uint32_t kBox = kC * 128;      // one [128 rows x 64 bf16] swizzled box: 16 KB
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far beyond any healthy wait
-constexpr uint32_t kFlagReady = 1, kFlagError = 2;
+// Per-segment publish counters: each of the 8 phase-B warps adds 1 (with release
+// semantics) once its part of a state is stored; kPublished means complete, and
+// kPoison or more marks a segment whose CTA gave up.
+constexpr uint32_t kPublished = 8, kPoison = 1u << 20;
 
 template <int D>
 struct Cfg {
@@ -76,10 +81,13 @@ struct alignas(1024) Smem {
     uint8_t w[2048];
     uint8_t sb[Cfg<D>::kSbBytes];
     uint64_t full[Cfg<D>::kStages], phi_done[Cfg<D>::kStages], empty[Cfg<D>::kStages];
+    uint64_t ostore[Cfg<D>::kStages];  // the O tile staged in slot s has been read by its TMA store
     uint64_t t_full, t_free, p_full, o_full, o_free, s_full, s_ready, agg_ready, drain;
+    uint64_t o_staged;  // all 128 rows of the current O tile are staged in shared memory
     uint32_t tmem_base;
     int ticket;
     int abort;
+    int lb_base;  // look-back result
 };
 
 static_assert(sizeof(Smem<128>) <= 232448, "exceeds the 227 KB per-CTA shared memory limit");
@@ -87,8 +95,10 @@ static_assert(sizeof(Smem<64>) <= 232448, "exceeds the 227 KB per-CTA shared mem
 
 struct Params {
     uint16_t *o;            // bf16 output [BH, N, D]
-    float *states;          // [BH, G, D*D + D] inclusive prefixes (S then z)
-    uint32_t *flags;        // [BH, G]
+    float *incl;            // [BH, G, D*D + D] inclusive prefixes (S then z; thread-major, see add_state)
+    float *agg;             // [BH, G, D*D + D] segment aggregates (same layout)
+    uint32_t *incl_cnt;     // [BH, G] publish counters of incl
+    uint32_t *agg_cnt;      // [BH, G] publish counters of agg
     uint32_t *counter;      // work ticket
     int N, BH, G, L, n_chunks;
     float eps;
@@ -139,42 +149,42 @@ __device__ __forceinline__ uint32_t phi2(uint32_t w)
     return *reinterpret_cast<const uint32_t *>(&r);
 }
 
-// phi in place on shared-memory tiles, by the 256 phi threads.  A unit is half of
-// one 128-byte row of a 64-column box (4 chunks of 16 bytes); thread t takes units
-// t, t + 256, ...  Units of rows >= `valid` (past the end of the sequence) are
-// zeroed.  All loads of a thread are issued before its arithmetic.  The chunk
-// order is rotated by the row so that the 8 threads of a quarter-warp (8
+// phi in place on one shared-memory tile, by the 256 phi threads.  A unit is half
+// of one 128-byte row of a 64-column box (4 chunks of 16 bytes); thread t takes
+// units t, t + 256, ...  Units of rows >= `valid` (past the end of the sequence)
+// are zeroed.  All loads of a thread are issued before its arithmetic.  The
+// chunk order is rotated by the row so that the 8 threads of a quarter-warp (8
 // consecutive rows) touch 8 different bank groups.
-template <int D, int NU>
-__device__ __forceinline__ void phi_tiles(uint8_t *kt, uint8_t *qt, int t, int valid)
+template <int D>
+__device__ __forceinline__ void phi_tile(uint8_t *tile, int t, int valid)
 {
-    constexpr int kUnitsPerTile = 128 * (D / 32);
+    constexpr int NU = D / 64;  // units per thread: 128 rows x D/32 units / 256 threads
     uint4 buf[NU][4];
-    uint8_t *rowp[NU];
-    int rot[NU];
-    bool ok[NU];
 #pragma unroll
     for (int m = 0; m < NU; ++m) {
-        const int u = t + kPhiThreads * m;
-        uint8_t *tile = u < kUnitsPerTile ? kt : qt;
-        const int rem = u % kUnitsPerTile, row = rem & 127, hb = rem >> 7;
-        rowp[m] = tile + (hb >> 1) * kBox + row * 128;
-        rot[m] = row + (hb & 1) * 4;
-        ok[m] = row < valid;
+        const int u = t + kPhiThreads * m, row = u & 127, hb = u >> 7;
+        const uint8_t *rp = tile + (hb >> 1) * kBox + row * 128;
+        const int rot = row + (hb & 1) * 4;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) buf[m][k] = *reinterpret_cast<const uint4 *>(rowp[m] + ((rot[m] + k) & 7) * 16);
+        for (int k = 0; k < 4; ++k) buf[m][k] = *reinterpret_cast<const uint4 *>(rp + ((rot + k) & 7) * 16);
     }
 #pragma unroll
-    for (int m = 0; m < NU; ++m)
+    for (int m = 0; m < NU; ++m) {
+        const int row = (t + kPhiThreads * m) & 127;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             uint4 &x = buf[m][k];
-            x = ok[m] ? make_uint4(phi2(x.x), phi2(x.y), phi2(x.z), phi2(x.w)) : make_uint4(0u, 0u, 0u, 0u);
+            x = row < valid ? make_uint4(phi2(x.x), phi2(x.y), phi2(x.z), phi2(x.w)) : make_uint4(0u, 0u, 0u, 0u);
         }
+    }
 #pragma unroll
-    for (int m = 0; m < NU; ++m)
+    for (int m = 0; m < NU; ++m) {
+        const int u = t + kPhiThreads * m, row = u & 127, hb = u >> 7;
+        uint8_t *rp = tile + (hb >> 1) * kBox + row * 128;
+        const int rot = row + (hb & 1) * 4;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) *reinterpret_cast<uint4 *>(rowp[m] + ((rot[m] + k) & 7) * 16) = buf[m][k];
+        for (int k = 0; k < 4; ++k) *reinterpret_cast<uint4 *>(rp + ((rot + k) & 7) * 16) = buf[m][k];
+    }
 }
 
 // Descriptor helpers (see la_sm100.cuh for the layouts).
@@ -191,10 +201,53 @@ __device__ __forceinline__ uint64_t wdesc(uint32_t w, int kk)
     return desc_sw128(w + (kk >> 2) * 1024 + (kk & 3) * 32, 16, 2048);
 }
 
+// Row i of the bf16 state copy (32 columns from col0), MN-major 128-byte swizzled:
+// 64-column blocks of D rows x 128 bytes.
 template <int D>
-__global__ void __launch_bounds__(640, 1)
+__device__ __forceinline__ void put_sb(uint8_t *sb, int i, int col0, const float (&x)[32])
+{
+#pragma unroll
+    for (int c8 = 0; c8 < 32; c8 += 8) {
+        const int col = col0 + c8;
+        const uint32_t off = (col >> 6) * (D * 128) + i * 128 + ((((col & 63) >> 3) ^ (i & 7)) << 4);
+        *reinterpret_cast<uint4 *>(sb + off) =
+            make_uint4(pack_bf16(x[c8], x[c8 + 1]), pack_bf16(x[c8 + 2], x[c8 + 3]),
+                       pack_bf16(x[c8 + 4], x[c8 + 5]), pack_bf16(x[c8 + 6], x[c8 + 7]));
+    }
+}
+// z_i split into a high and a low bf16 part: rows 1 and 2 of W.
+__device__ __forceinline__ void put_z(uint8_t *w, int i, float zv)
+{
+    const __nv_bfloat16 hi = __float2bfloat16_rn(zv);
+    const __nv_bfloat16 lo = __float2bfloat16_rn(zv - __bfloat162float(hi));
+    uint8_t *blk = w + (i >> 6) * 1024;
+    *reinterpret_cast<__nv_bfloat16 *>(blk + sw128_offset(1, i & 63)) = hi;
+    *reinterpret_cast<__nv_bfloat16 *>(blk + sw128_offset(2, i & 63)) = lo;
+}
+// Published scan states use a thread-major layout, so that the 32 rows a warp
+// handles are contiguous: the float4 holding columns 4c..4c+3 of row i is at
+// float4 index c*D + i, and z_i follows at float D*D + i.
+template <int D>
+__device__ __forceinline__ void add_state(float (&acc)[32], const float *state, int cg0, int i)
+{
+    const float4 *s4 = reinterpret_cast<const float4 *>(state);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        const float4 x = __ldcg(s4 + (size_t)(cg0 + e) * D + i);
+        acc[4 * e] += x.x; acc[4 * e + 1] += x.y; acc[4 * e + 2] += x.z; acc[4 * e + 3] += x.w;
+    }
+}
+__device__ __forceinline__ void to_floats(const uint32_t *a, float (&x)[32])
+{
+#pragma unroll
+    for (int e = 0; e < 32; ++e) x[e] = __uint_as_float(a[e]);
+}
+
+template <int D>
+__global__ void __launch_bounds__(576, 1)
 causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
-                 const __grid_constant__ CUtensorMap map_v, const Params prm)
+                 const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_o,
+                 const Params prm)
 {
     using CF = Cfg<D>;
     constexpr int S = CF::kStages;
@@ -217,6 +270,7 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
             mbar_init(&sm.full[s], 1);
             mbar_init(&sm.phi_done[s], kPhiThreads);
             mbar_init(&sm.empty[s], 1);
+            mbar_init(&sm.ostore[s], 1);
         }
         mbar_init(&sm.t_full, 1);
         mbar_init(&sm.t_free, 128);
@@ -227,6 +281,7 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
         mbar_init(&sm.s_ready, 128);
         mbar_init(&sm.agg_ready, 1);
         mbar_init(&sm.drain, 1);
+        mbar_init(&sm.o_staged, 128);
         sm.abort = 0;
         fence_mbar_init();
     }
@@ -260,10 +315,8 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
             const bool isC = j >= nA;
             const int chunk = c0 + (isC ? j - nA : j);
             const int valid = prm.N - chunk * kC;
-            if (isC)
-                phi_tiles<D, D / 32>(sm.k[s], sm.q[s], tid, valid);
-            else
-                phi_tiles<D, D / 64>(sm.k[s], sm.q[s], tid, valid);
+            phi_tile<D>(sm.k[s], tid, valid);
+            if (isC) phi_tile<D>(sm.q[s], tid, valid);
             fence_proxy_async_smem();
             mbar_arrive(&sm.phi_done[s]);
         }
@@ -273,10 +326,16 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
             tma_prefetch_map(&map_q);
             tma_prefetch_map(&map_k);
             tma_prefetch_map(&map_v);
+            tma_prefetch_map(&map_o);
             int issued = 0;
             for (int j = 0; j < total; ++j) {
                 const int s = j % S, r = j / S;
                 if (r > 0 && !wait_bar(abort_flag, &sm.empty[s], (r - 1) & 1)) break;
+                if (j - S >= nA) {  // the previous user of slot s was a C-job: its Q buffer staged O
+                    const int first_c = nA + ((s - nA % S) % S + S) % S;
+                    const int k = (j - S - first_c) / S;  // index of that C-job among slot s's C-jobs
+                    if (!wait_bar(abort_flag, &sm.ostore[s], k & 1)) break;
+                }
                 const bool isC = j >= nA;
                 const int row0 = (c0 + (isC ? j - nA : j)) * kC;
                 mbar_arrive_expect_tx(&sm.full[s], (isC ? 3u : 2u) * CF::kTileBytes);
@@ -366,202 +425,265 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
             while (!mbar_try_wait(&sm.drain, 0) && globaltimer_ns() - t0 < kWaitLimitNs) {
             }
         }
-    } else if (warp >= kEpiPWarp0 && warp < kEpiPWarp0 + 4) {
-        // ---------------------------------------------------------------- T -> P
-        const int quad = warp - kEpiPWarp0, i = quad * 32 + lane;  // query row = TMEM lane
+    } else if (warp >= kEpiPWarp0) {
+        // ---------------------------------------------------------------- epilogue warps 10-17
+        const int quad = warp & 3, i = quad * 32 + lane;  // query row / state row = TMEM lane
+        const bool is_o = warp >= kEpiOWarp0;              // warps 14-17: O and state refresh
+        const int gtid = (warp - kEpiPWarp0) * 32 + lane;  // 0..255
         const uint32_t tl = tmem + ((uint32_t)(quad * 32) << 16);
-        for (int cj = 0; cj < nch; ++cj) {
-            if (!wait_bar_warp(abort_flag, &sm.t_full, cj & 1)) break;
-            tc_fence_after();
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                uint32_t t[64];
-                tmem_ld32(tl + CF::tT + half * 64, *reinterpret_cast<uint32_t(*)[32]>(&t[0]));
-                tmem_ld32(tl + CF::tT + half * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&t[32]));
-                tmem_ld_wait();
-                if (half == 1) {
-                    tc_fence_before();
-                    mbar_arrive(&sm.t_free);
-                }
-                uint32_t p[32];
-#pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const int jk = half * 64 + 2 * e;  // key index within the chunk
-                    const float a = jk <= i ? __uint_as_float(t[2 * e]) : 0.f;
-                    const float b = jk + 1 <= i ? __uint_as_float(t[2 * e + 1]) : 0.f;
-                    p[e] = pack_bf16(a, b);
-                }
-                tmem_st16(tl + CF::tP + half * 32, *reinterpret_cast<uint32_t(*)[16]>(&p[0]));
-                tmem_st16(tl + CF::tP + half * 32 + 16, *reinterpret_cast<uint32_t(*)[16]>(&p[16]));
-            }
-            tmem_st_wait();
-            tc_fence_before();
-            mbar_arrive(&sm.p_full);
-        }
-    } else if (warp >= kEpiOWarp0) {
-        // ---------------------------------------------------------------- phase B, O, S refresh
-        const int quad = warp - kEpiOWarp0, i = quad * 32 + lane;  // query row / state row = TMEM lane
-        const uint32_t tl = tmem + ((uint32_t)(quad * 32) << 16);
-        const size_t seg_floats = (size_t)D * D + D;
         const bool row_ok = i < D;
 
-        // Writes row i of the bf16 state copy (32 columns starting at c0) and the z split.
-        auto put_sb = [&](int col0, const float *x) {
-#pragma unroll
-            for (int c8 = 0; c8 < 32; c8 += 8) {
-                const int col = col0 + c8;
-                const uint32_t off = (col >> 6) * (D * 128) + i * 128 + ((((col & 63) >> 3) ^ (i & 7)) << 4);
-                *reinterpret_cast<uint4 *>(sm.sb + off) =
-                    make_uint4(pack_bf16(x[c8], x[c8 + 1]), pack_bf16(x[c8 + 2], x[c8 + 3]),
-                               pack_bf16(x[c8 + 4], x[c8 + 5]), pack_bf16(x[c8 + 6], x[c8 + 7]));
-            }
-        };
-        auto put_z = [&](float zv) {
-            const __nv_bfloat16 hi = __float2bfloat16_rn(zv);
-            const __nv_bfloat16 lo = __float2bfloat16_rn(zv - __bfloat162float(hi));
-            uint8_t *blk = sm.w + (i >> 6) * 1024;
-            *reinterpret_cast<__nv_bfloat16 *>(blk + sw128_offset(1, i & 63)) = hi;
-            *reinterpret_cast<__nv_bfloat16 *>(blk + sw128_offset(2, i & 63)) = lo;
-        };
-
-        // ---- phase B: prefix of the earlier segments of this head
-        const float *prev = nullptr;
-        bool failed = false;
-        if (g > 0) {
-            if (i == 0) {
-                const uint32_t *f = prm.flags + (size_t)bh * prm.G + (g - 1);
-                const uint64_t t0 = globaltimer_ns();
-                uint32_t v = ld_acquire_gpu(f);
-                while (v == 0) {
-                    if (globaltimer_ns() - t0 > kWaitLimitNs) {
-                        atomicOr(&g_tc_status, kStatusTimeout);
-                        v = kFlagError;
-                        break;
-                    }
-                    __nanosleep(256);
-                    v = ld_acquire_gpu(f);
-                }
-                if (v != kFlagReady) *(volatile int *)abort_flag = 1;
-            }
-            named_bar_sync(1, 128);
-            failed = aborted(abort_flag);
-            if (!failed) prev = prm.states + ((size_t)bh * prm.G + (g - 1)) * seg_floats;
-        }
-        float *mine = has_next ? prm.states + ((size_t)bh * prm.G + g) * seg_floats : nullptr;
+        // ---- phase B: exclusive prefix of this segment by decoupled look-back.
+        // A segment with a successor publishes its aggregate as soon as phase A
+        // is done (segment 0 publishes its inclusive prefix directly), and its
+        // inclusive prefix after this CTA has set up its own running state.  A
+        // CTA sums the aggregates of its predecessors back to the nearest
+        // published inclusive prefix.  Each thread owns state row i and the
+        // columns [col0, col0 + D/2).
+        constexpr int kHalf = D / 2;
+        const int col0 = is_o ? kHalf : 0;
+        const size_t seg_floats = (size_t)D * D + D;
+        const size_t head0 = (size_t)bh * prm.G, my = head0 + g;
         bool have_agg = false;
         if (nA > 0) have_agg = wait_bar_warp(abort_flag, &sm.agg_ready, 0);
         tc_fence_after();
-#pragma unroll 1
-        for (int cc = 0; cc < D / 32; ++cc) {
-            float pv[32];
-            if (prev != nullptr && row_ok) {
-                const float4 *src = reinterpret_cast<const float4 *>(prev + (size_t)i * D + cc * 32);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const float4 x = __ldcg(src + e);
-                    pv[4 * e] = x.x; pv[4 * e + 1] = x.y; pv[4 * e + 2] = x.z; pv[4 * e + 3] = x.w;
-                }
-            } else {
-#pragma unroll
-                for (int e = 0; e < 32; ++e) pv[e] = 0.f;
-            }
+        if (has_next && g > 0) {
+            float *dst = prm.agg + my * seg_floats;
             if (have_agg) {
+#pragma unroll 1
+                for (int cc = 0; cc < kHalf; cc += 32) {
+                    uint32_t a[32];
+                    tmem_ld32(tl + CF::tS + col0 + cc, a);
+                    tmem_ld_wait();
+                    if (row_ok) {
+                        float4 *d4 = reinterpret_cast<float4 *>(dst);
+                        const int cg0 = (col0 + cc) >> 2;
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            d4[(size_t)(cg0 + e) * D + i] =
+                                make_float4(__uint_as_float(a[4 * e]), __uint_as_float(a[4 * e + 1]),
+                                            __uint_as_float(a[4 * e + 2]), __uint_as_float(a[4 * e + 3]));
+                    }
+                }
+                if (!is_o) {
+                    const float za = __uint_as_float(tmem_ld1(tl + CF::tZ));
+                    tmem_ld_wait();
+                    if (row_ok) dst[(size_t)D * D + i] = za;
+                }
+            }
+            __syncwarp();
+            if (lane == 0) red_release_add_gpu(prm.agg_cnt + my, have_agg ? 1u : kPoison);
+        }
+        if (gtid < 32) {
+            // One warp reads the counters of up to 32 predecessors per round.
+            int base = -1;
+            bool bad = false;
+            if (g > 0) {
+                const uint64_t t0 = globaltimer_ns();
+                while (true) {
+                    const int j = g - 1 - lane;
+                    uint32_t ci = 0, ca = 0;
+                    if (j >= 0) {
+                        ci = ld_acquire_gpu(prm.incl_cnt + head0 + j);
+                        ca = ld_acquire_gpu(prm.agg_cnt + head0 + j);
+                    }
+                    const unsigned inc = __ballot_sync(0xffffffffu, ci == kPublished);
+                    const unsigned avail = __ballot_sync(0xffffffffu, ci == kPublished || ca == kPublished);
+                    const unsigned poison = __ballot_sync(0xffffffffu, ci >= kPoison || ca >= kPoison);
+                    const int first = inc ? __ffs(inc) - 1 : 32;  // nearest inclusive prefix
+                    const unsigned need = first >= 32 ? 0xffffffffu : ((1u << first) - 1u);
+                    if ((poison & (need | (first < 32 ? (1u << first) : 0u))) != 0u) {
+                        bad = true;
+                        break;
+                    }
+                    if (first < 32 && (avail & need) == need) {
+                        base = g - 1 - first;
+                        break;
+                    }
+                    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                        if (lane == 0) atomicOr(&g_tc_status, kStatusTimeout);
+                        bad = true;
+                        break;
+                    }
+                    __nanosleep(128);
+                }
+            }
+            if (lane == 0) {
+                sm.lb_base = base;
+                if (bad) *(volatile int *)abort_flag = 1;
+            }
+        }
+        named_bar_sync(1, 256);
+        const int base = sm.lb_base;
+        const bool use_prev = g > 0 && !aborted(abort_flag);
+        float *incl_out = has_next ? prm.incl + my * seg_floats : nullptr;
+#pragma unroll 1
+        for (int cc = 0; cc < kHalf; cc += 32) {
+            float acc[32];
+#pragma unroll
+            for (int e = 0; e < 32; ++e) acc[e] = 0.f;
+            const int cg0 = (col0 + cc) >> 2;
+            if (use_prev && row_ok) {
+                if (base >= 0) add_state<D>(acc, prm.incl + (head0 + base) * seg_floats, cg0, i);
+                int j = base + 1;
+                for (; j + 1 < g; j += 2) {  // two states per round trip
+                    add_state<D>(acc, prm.agg + (head0 + j) * seg_floats, cg0, i);
+                    add_state<D>(acc, prm.agg + (head0 + j + 1) * seg_floats, cg0, i);
+                }
+                if (j < g) add_state<D>(acc, prm.agg + (head0 + j) * seg_floats, cg0, i);
+            }
+            if (has_next) {
                 uint32_t a[32];
-                tmem_ld32(tl + CF::tS + cc * 32, a);
-                tmem_ld_wait();
+                if (have_agg) {
+                    tmem_ld32(tl + CF::tS + col0 + cc, a);
+                    tmem_ld_wait();
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) a[e] = 0u;
+                }
                 if (row_ok) {
-                    float4 *dst = reinterpret_cast<float4 *>(mine + (size_t)i * D + cc * 32);
+                    float4 *d4 = reinterpret_cast<float4 *>(incl_out);
 #pragma unroll
                     for (int e = 0; e < 8; ++e)
-                        dst[e] = make_float4(pv[4 * e] + __uint_as_float(a[4 * e]),
-                                             pv[4 * e + 1] + __uint_as_float(a[4 * e + 1]),
-                                             pv[4 * e + 2] + __uint_as_float(a[4 * e + 2]),
-                                             pv[4 * e + 3] + __uint_as_float(a[4 * e + 3]));
+                        d4[(size_t)(cg0 + e) * D + i] = make_float4(acc[4 * e] + __uint_as_float(a[4 * e]),
+                                            acc[4 * e + 1] + __uint_as_float(a[4 * e + 1]),
+                                            acc[4 * e + 2] + __uint_as_float(a[4 * e + 2]),
+                                            acc[4 * e + 3] + __uint_as_float(a[4 * e + 3]));
                 }
             }
-            uint32_t w0[16], w1[16];
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-                w0[e] = __float_as_uint(pv[e]);
-                w1[e] = __float_as_uint(pv[16 + e]);
-            }
-            tmem_st16(tl + CF::tS + cc * 32, w0);
-            tmem_st16(tl + CF::tS + cc * 32 + 16, w1);
-            if (row_ok) put_sb(cc * 32, pv);
+            tmem_st16(tl + CF::tS + col0 + cc, *reinterpret_cast<const uint32_t(*)[16]>(&acc[0]));
+            tmem_st16(tl + CF::tS + col0 + cc + 16, *reinterpret_cast<const uint32_t(*)[16]>(&acc[16]));
+            if (row_ok) put_sb<D>(sm.sb, i, col0 + cc, acc);
         }
-        {
-            const float zp = (prev != nullptr && row_ok) ? __ldcg(prev + (size_t)D * D + i) : 0.f;
-            if (have_agg) {
-                const float za = __uint_as_float(tmem_ld1(tl + CF::tZ));
-                tmem_ld_wait();
-                if (row_ok) mine[(size_t)D * D + i] = zp + za;
+        if (!is_o) {  // z, by the warps of the first column half
+            float zacc = 0.f;
+            if (use_prev && row_ok) {
+                const size_t off = (size_t)D * D + i;
+                if (base >= 0) zacc += __ldcg(prm.incl + (head0 + base) * seg_floats + off);
+                for (int j = base + 1; j < g; ++j) zacc += __ldcg(prm.agg + (head0 + j) * seg_floats + off);
             }
-            tmem_st1(tl + CF::tZ, __float_as_uint(zp));
-            if (row_ok) put_z(zp);
+            if (has_next) {
+                float za = 0.f;
+                if (have_agg) {
+                    za = __uint_as_float(tmem_ld1(tl + CF::tZ));
+                    tmem_ld_wait();
+                }
+                if (row_ok) incl_out[(size_t)D * D + i] = zacc + za;
+            }
+            tmem_st1(tl + CF::tZ, __float_as_uint(zacc));
+            if (row_ok) put_z(sm.w, i, zacc);
         }
         tmem_st_wait();
-        if (has_next) {
-            __threadfence();
-            named_bar_sync(1, 128);
-            if (i == 0)
-                st_release_gpu(prm.flags + (size_t)bh * prm.G + g,
-                               (have_agg && !aborted(abort_flag)) ? kFlagReady : kFlagError);
-        }
         fence_proxy_async_smem();
+        named_bar_sync(1, 256);
         tc_fence_before();
-        mbar_arrive(&sm.s_ready);
+        if (is_o) mbar_arrive(&sm.s_ready);  // sb and S_acc of both halves are in place
+        if (has_next) {  // publish the inclusive prefix (its stores were issued above)
+            __syncwarp();
+            if (lane == 0)
+                red_release_add_gpu(prm.incl_cnt + my, (have_agg && !aborted(abort_flag)) ? 1u : kPoison);
+        }
 
-        // ---- phase C: normalise and store O; refresh the bf16 state copy
-        for (int cj = 0; cj < nch; ++cj) {
-            if (!wait_bar_warp(abort_flag, &sm.o_full, cj & 1)) break;
-            tc_fence_after();
-            uint32_t dn[32];
-            tmem_ld32(tl + CF::tRS, dn);  // columns: rs[0..15], qz[0..15]
-            tmem_ld_wait();
-            const float den = __uint_as_float(dn[0]) + __uint_as_float(dn[17]) + __uint_as_float(dn[18]);
-            const float inv = 1.f / fmaxf(den, prm.eps);
-            const int row = (c0 + cj) * kC + i;
-            uint16_t *orow = prm.o + ((size_t)bh * prm.N + row) * D;
-#pragma unroll 1
-            for (int cc = 0; cc < D / 64; ++cc) {
-                uint32_t a[64];
-                tmem_ld32(tl + CF::tO + cc * 64, *reinterpret_cast<uint32_t(*)[32]>(&a[0]));
-                tmem_ld32(tl + CF::tO + cc * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&a[32]));
-                tmem_ld_wait();
-                if (row < prm.N) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(orow + cc * 64);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        dst[e] = make_uint4(
-                            pack_bf16(__uint_as_float(a[8 * e]) * inv, __uint_as_float(a[8 * e + 1]) * inv),
-                            pack_bf16(__uint_as_float(a[8 * e + 2]) * inv, __uint_as_float(a[8 * e + 3]) * inv),
-                            pack_bf16(__uint_as_float(a[8 * e + 4]) * inv, __uint_as_float(a[8 * e + 5]) * inv),
-                            pack_bf16(__uint_as_float(a[8 * e + 6]) * inv, __uint_as_float(a[8 * e + 7]) * inv));
-                }
-            }
-            tc_fence_before();
-            mbar_arrive(&sm.o_free);
-            if (cj < nch - 1) {
-                if (!wait_bar_warp(abort_flag, &sm.s_full, cj & 1)) break;
+        if (!is_o) {
+            // ------------------------------------------------------------ T -> P
+            for (int cj = 0; cj < nch; ++cj) {
+                if (!wait_bar_warp(abort_flag, &sm.t_full, cj & 1)) break;
                 tc_fence_after();
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    uint32_t t[64];
+                    tmem_ld32(tl + CF::tT + hh * 64, *reinterpret_cast<uint32_t(*)[32]>(&t[0]));
+                    tmem_ld32(tl + CF::tT + hh * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&t[32]));
+                    tmem_ld_wait();
+                    if (hh == 1) {
+                        tc_fence_before();
+                        mbar_arrive(&sm.t_free);
+                    }
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        const int jk = hh * 64 + 2 * e;  // key index within the chunk
+                        const float a = jk <= i ? __uint_as_float(t[2 * e]) : 0.f;
+                        const float b = jk + 1 <= i ? __uint_as_float(t[2 * e + 1]) : 0.f;
+                        pk[e] = pack_bf16(a, b);
+                    }
+                    tmem_st16(tl + CF::tP + hh * 32, *reinterpret_cast<uint32_t(*)[16]>(&pk[0]));
+                    tmem_st16(tl + CF::tP + hh * 32 + 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[16]));
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(&sm.p_full);
+            }
+        } else {
+            // ------------------------------------------------------------ O out, state refresh
+            // O is staged (bf16, 128-byte swizzled boxes) in the Q buffer of its own
+            // slot -- Q is no longer read once O is final -- and written by a TMA
+            // store, which clips rows past the end of the sequence.
+            const bool leader = (warp == kEpiOWarp0 && lane == 0);
+            for (int cj = 0; cj < nch; ++cj) {
+                const int s = (nA + cj) % S;
+                if (!wait_bar_warp(abort_flag, &sm.o_full, cj & 1)) break;
+                tc_fence_after();
+                uint32_t dn[32];
+                tmem_ld32(tl + CF::tRS, dn);  // columns: rs[0..15], qz[0..15]
+                tmem_ld_wait();
+                const float den = __uint_as_float(dn[0]) + __uint_as_float(dn[17]) + __uint_as_float(dn[18]);
+                const float inv = 1.f / fmaxf(den, prm.eps);
 #pragma unroll 1
                 for (int cc = 0; cc < D / 64; ++cc) {
                     uint32_t a[64];
-                    tmem_ld32(tl + CF::tS + cc * 64, *reinterpret_cast<uint32_t(*)[32]>(&a[0]));
-                    tmem_ld32(tl + CF::tS + cc * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&a[32]));
+                    tmem_ld32(tl + CF::tO + cc * 64, *reinterpret_cast<uint32_t(*)[32]>(&a[0]));
+                    tmem_ld32(tl + CF::tO + cc * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&a[32]));
                     tmem_ld_wait();
-                    if (row_ok) {
-                        put_sb(cc * 64, reinterpret_cast<const float *>(&a[0]));
-                        put_sb(cc * 64 + 32, reinterpret_cast<const float *>(&a[32]));
-                    }
+                    uint8_t *rowp = sm.q[s] + cc * kBox + i * 128;
+#pragma unroll
+                    for (int c = 0; c < 8; ++c)
+                        *reinterpret_cast<uint4 *>(rowp + ((c ^ (i & 7)) << 4)) = make_uint4(
+                            pack_bf16(__uint_as_float(a[8 * c]) * inv, __uint_as_float(a[8 * c + 1]) * inv),
+                            pack_bf16(__uint_as_float(a[8 * c + 2]) * inv, __uint_as_float(a[8 * c + 3]) * inv),
+                            pack_bf16(__uint_as_float(a[8 * c + 4]) * inv, __uint_as_float(a[8 * c + 5]) * inv),
+                            pack_bf16(__uint_as_float(a[8 * c + 6]) * inv, __uint_as_float(a[8 * c + 7]) * inv));
                 }
-                const float zv = __uint_as_float(tmem_ld1(tl + CF::tZ));
-                tmem_ld_wait();
-                if (row_ok) put_z(zv);
-                fence_proxy_async_smem();
                 tc_fence_before();
-                mbar_arrive(&sm.s_ready);
+                mbar_arrive(&sm.o_free);
+                fence_proxy_async_smem();
+                mbar_arrive(&sm.o_staged);
+                if (leader && wait_bar(abort_flag, &sm.o_staged, cj & 1)) {
+#pragma unroll
+                    for (int cc = 0; cc < D / 64; ++cc)
+                        tma_store_3d(&map_o, sm.q[s] + cc * kBox, 64 * cc, (c0 + cj) * kC, bh);
+                    tma_store_commit();
+                }
+                if (cj < nch - 1) {
+                    if (!wait_bar_warp(abort_flag, &sm.s_full, cj & 1)) break;
+                    tc_fence_after();
+#pragma unroll 1
+                    for (int cc = 0; cc < D / 64; ++cc) {
+                        uint32_t a[64];
+                        tmem_ld32(tl + CF::tS + cc * 64, *reinterpret_cast<uint32_t(*)[32]>(&a[0]));
+                        tmem_ld32(tl + CF::tS + cc * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&a[32]));
+                        tmem_ld_wait();
+                        if (row_ok) {
+                            float x[32];
+                            to_floats(&a[0], x);
+                            put_sb<D>(sm.sb, i, cc * 64, x);
+                            to_floats(&a[32], x);
+                            put_sb<D>(sm.sb, i, cc * 64 + 32, x);
+                        }
+                    }
+                    const float zv = __uint_as_float(tmem_ld1(tl + CF::tZ));
+                    tmem_ld_wait();
+                    if (row_ok) put_z(sm.w, i, zv);
+                    fence_proxy_async_smem();
+                    tc_fence_before();
+                    mbar_arrive(&sm.s_ready);
+                }
+                if (leader) {  // slot s may be refilled once the store has read the staged O
+                    tma_store_wait_read_all();
+                    mbar_arrive(&sm.ostore[s]);
+                }
             }
+            if (leader) tma_store_wait_all();  // all output stores complete before the CTA exits
         }
     }
 
@@ -630,10 +752,11 @@ int sm_count()
 template <int D>
 la_status launch(const Problem &p)
 {
-    CUtensorMap mq, mk, mv;
+    CUtensorMap mq, mk, mv, mo;
     la_status st = make_map(&mq, p.q, p.BH, p.N, D);
     if (st == LA_OK) st = make_map(&mk, p.k, p.BH, p.N, D);
     if (st == LA_OK) st = make_map(&mv, p.v, p.BH, p.N, D);
+    if (st == LA_OK) st = make_map(&mo, p.o, p.BH, p.N, D);
     if (st != LA_OK) return st;
 
     const int n_chunks = ceil_div(p.N, kC);
@@ -641,8 +764,8 @@ la_status launch(const Problem &p)
     const int L = (int)std::min<long long>(8, std::max<long long>(1, (work + sm_count() - 1) / sm_count()));
     const int G = ceil_div(n_chunks, L);
     const size_t items = (size_t)p.BH * G;
-    const size_t flag_bytes = ((items * 4 + 16) + 255) / 256 * 256;
-    const size_t state_bytes = G > 1 ? items * ((size_t)D * D + D) * 4 : 0;
+    const size_t flag_bytes = ((items * 8 + 16) + 255) / 256 * 256;
+    const size_t state_bytes = G > 1 ? 2 * items * ((size_t)D * D + D) * 4 : 0;
 
     Scratch scratch;
     st = scratch.alloc(flag_bytes + state_bytes, p.stream);
@@ -655,8 +778,10 @@ la_status launch(const Problem &p)
     Params prm;
     prm.o = (uint16_t *)p.o;
     prm.counter = (uint32_t *)base;
-    prm.flags = (uint32_t *)(base + 16);
-    prm.states = (float *)(base + flag_bytes);
+    prm.incl_cnt = (uint32_t *)(base + 16);
+    prm.agg_cnt = prm.incl_cnt + items;
+    prm.incl = (float *)(base + flag_bytes);
+    prm.agg = prm.incl + (G > 1 ? items * ((size_t)D * D + D) : 0);
     prm.N = p.N;
     prm.BH = p.BH;
     prm.G = G;
@@ -669,7 +794,7 @@ la_status launch(const Problem &p)
     st = ensure_smem((const void *)kern, smem);
     if (st != LA_OK) return st;
     count_launches();
-    kern<<<(unsigned)items, kThreads, smem, p.stream>>>(mq, mk, mv, prm);
+    kern<<<(unsigned)items, kThreads, smem, p.stream>>>(mq, mk, mv, mo, prm);
     return cuda_status(cudaGetLastError());
 }
 
