@@ -137,15 +137,29 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b)
 }
 
 // phi on a pair of bf16 values: exp(min(x, 0)) + max(x, 0), which is x + 1 for
-// x > 0 and exp(x) otherwise; min, max and the final add in packed bf16 (exact
-// except the single rounding of the sum), exp in fp32.
+// x > 0 and exp(x) otherwise, all in packed bf16x2: y = min(x, 0) * log2(e) with
+// one rounding (log2(e) split into a bf16 head and tail, fused multiply-add),
+// then the packed bf16 exp2 of the special-function unit (two values per
+// operation), then the exact add of max(x, 0).  The result is a bf16 tensor-core
+// operand either way; rounding y to bf16 perturbs exp(x) by about |x| * 2^-9
+// relative, which stays far inside the bf16 tolerances.
+__device__ __forceinline__ uint32_t ex2_bf16x2(uint32_t y)
+{
+    uint32_t r;
+    asm("ex2.approx.ftz.bf16x2 %0, %1;" : "=r"(r) : "r"(y));
+    return r;
+}
 __device__ __forceinline__ uint32_t phi2(uint32_t w)
 {
     const __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162 *>(&w);
     const __nv_bfloat162 zero = __float2bfloat162_rn(0.f);
-    const float2 nf = __bfloat1622float2(__hmin2(x, zero));
-    const __nv_bfloat162 e = __floats2bfloat162_rn(__expf(nf.x), __expf(nf.y));
-    const __nv_bfloat162 r = __hadd2(e, __hmax2(x, zero));
+    const __nv_bfloat162 log2e_hi = __float2bfloat162_rn(1.4453125f);          // bf16(log2 e)
+    const __nv_bfloat162 log2e_lo = __float2bfloat162_rn(-0.0026174591f);      // log2 e - head
+    const __nv_bfloat162 neg = __hmin2(x, zero);
+    const __nv_bfloat162 y = __hfma2(neg, log2e_hi, __hmul2(neg, log2e_lo));
+    const uint32_t yb = *reinterpret_cast<const uint32_t *>(&y);
+    const uint32_t eb = ex2_bf16x2(yb);
+    const __nv_bfloat162 r = __hadd2(*reinterpret_cast<const __nv_bfloat162 *>(&eb), __hmax2(x, zero));
     return *reinterpret_cast<const uint32_t *>(&r);
 }
 
