@@ -163,28 +163,31 @@ __device__ __forceinline__ uint32_t phi2(uint32_t w)
     return *reinterpret_cast<const uint32_t *>(&r);
 }
 
-// phi in place on one shared-memory tile, by the 256 phi threads.  A unit is half
-// of one 128-byte row of a 64-column box (4 chunks of 16 bytes); thread t takes
-// units t, t + 256, ...  Units of rows >= `valid` (past the end of the sequence)
-// are zeroed.  All loads of a thread are issued before its arithmetic.  The
-// chunk order is rotated by the row so that the 8 threads of a quarter-warp (8
+// phi in place on one shared-memory tile, by NT threads.  A unit is half of one
+// 128-byte row of a 64-column box (4 chunks of 16 bytes); thread t takes units
+// t, t + NT, ...  Units of rows >= `valid` (past the end of the sequence) are
+// zeroed.  All loads of a thread are issued before its arithmetic.  The chunk
+// order is rotated by the row so that the 8 threads of a quarter-warp (8
 // consecutive rows) touch 8 different bank groups.
-template <int D>
+template <int D, int NT>
 __device__ __forceinline__ void phi_tile(uint8_t *tile, int t, int valid)
 {
-    constexpr int NU = D / 64;  // units per thread: 128 rows x D/32 units / 256 threads
+    constexpr int kUnits = 128 * (D / 32);
+    constexpr int NU = (kUnits + NT - 1) / NT;
     uint4 buf[NU][4];
 #pragma unroll
     for (int m = 0; m < NU; ++m) {
-        const int u = t + kPhiThreads * m, row = u & 127, hb = u >> 7;
-        const uint8_t *rp = tile + (hb >> 1) * kBox + row * 128;
-        const int rot = row + (hb & 1) * 4;
+        const int u = t + NT * m, row = u & 127, hb = u >> 7;
+        if (u < kUnits) {
+            const uint8_t *rp = tile + (hb >> 1) * kBox + row * 128;
+            const int rot = row + (hb & 1) * 4;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) buf[m][k] = *reinterpret_cast<const uint4 *>(rp + ((rot + k) & 7) * 16);
+            for (int k = 0; k < 4; ++k) buf[m][k] = *reinterpret_cast<const uint4 *>(rp + ((rot + k) & 7) * 16);
+        }
     }
 #pragma unroll
     for (int m = 0; m < NU; ++m) {
-        const int row = (t + kPhiThreads * m) & 127;
+        const int u = t + NT * m, row = u & 127;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             uint4 &x = buf[m][k];
@@ -193,11 +196,13 @@ __device__ __forceinline__ void phi_tile(uint8_t *tile, int t, int valid)
     }
 #pragma unroll
     for (int m = 0; m < NU; ++m) {
-        const int u = t + kPhiThreads * m, row = u & 127, hb = u >> 7;
-        uint8_t *rp = tile + (hb >> 1) * kBox + row * 128;
-        const int rot = row + (hb & 1) * 4;
+        const int u = t + NT * m, row = u & 127, hb = u >> 7;
+        if (u < kUnits) {
+            uint8_t *rp = tile + (hb >> 1) * kBox + row * 128;
+            const int rot = row + (hb & 1) * 4;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) *reinterpret_cast<uint4 *>(rp + ((rot + k) & 7) * 16) = buf[m][k];
+            for (int k = 0; k < 4; ++k) *reinterpret_cast<uint4 *>(rp + ((rot + k) & 7) * 16) = buf[m][k];
+        }
     }
 }
 
@@ -282,7 +287,9 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
     if (tid == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(&sm.full[s], 1);
-            mbar_init(&sm.phi_done[s], kPhiThreads);
+            // 512 arrivals: phi threads and epilogue threads share the K tiles of
+            // phase A; for phase-C jobs each phi thread arrives with a count of 2.
+            mbar_init(&sm.phi_done[s], 2 * kPhiThreads);
             mbar_init(&sm.empty[s], 1);
             mbar_init(&sm.ostore[s], 1);
         }
@@ -329,10 +336,17 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
             const bool isC = j >= nA;
             const int chunk = c0 + (isC ? j - nA : j);
             const int valid = prm.N - chunk * kC;
-            phi_tile<D>(sm.k[s], tid, valid);
-            if (isC) phi_tile<D>(sm.q[s], tid, valid);
+            if (isC) {
+                phi_tile<D, kPhiThreads>(sm.k[s], tid, valid);
+                phi_tile<D, kPhiThreads>(sm.q[s], tid, valid);
+            } else {
+                phi_tile<D, 2 * kPhiThreads>(sm.k[s], tid, valid);  // the other half: epilogue warps
+            }
             fence_proxy_async_smem();
-            mbar_arrive(&sm.phi_done[s]);
+            if (isC)
+                mbar_arrive_cnt(&sm.phi_done[s], 2);
+            else
+                mbar_arrive(&sm.phi_done[s]);
         }
     } else if (warp == kTmaWarp) {
         // ---------------------------------------------------------------- TMA producer
@@ -454,6 +468,16 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
         // CTA sums the aggregates of its predecessors back to the nearest
         // published inclusive prefix.  Each thread owns state row i and the
         // columns [col0, col0 + D/2).
+        // Phase A: the epilogue warps are otherwise idle, so they apply phi to the
+        // second half of each K tile (units 256..511).
+        for (int j = 0; j < nA; ++j) {
+            const int s = j % S, r = j / S;
+            if (!wait_bar(abort_flag, &sm.full[s], r & 1)) break;
+            phi_tile<D, 2 * kPhiThreads>(sm.k[s], kPhiThreads + gtid, prm.N - (c0 + j) * kC);
+            fence_proxy_async_smem();
+            mbar_arrive(&sm.phi_done[s]);
+        }
+
         constexpr int kHalf = D / 2;
         const int col0 = is_o ? kHalf : 0;
         const size_t seg_floats = (size_t)D * D + D;
@@ -603,26 +627,39 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
             for (int cj = 0; cj < nch; ++cj) {
                 if (!wait_bar_warp(abort_flag, &sm.t_full, cj & 1)) break;
                 tc_fence_after();
+                // This warp's rows are 32*quad .. 32*quad+31, so key block b (32 keys)
+                // is entirely visible for b < quad, masked on the diagonal for b ==
+                // quad, and entirely masked (zeros, no TMEM read) for b > quad.
+                {
+                    uint32_t t[32];
+                    uint32_t pk[16];
 #pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    uint32_t t[64];
-                    tmem_ld32(tl + CF::tT + hh * 64, *reinterpret_cast<uint32_t(*)[32]>(&t[0]));
-                    tmem_ld32(tl + CF::tT + hh * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&t[32]));
-                    tmem_ld_wait();
-                    if (hh == 1) {
-                        tc_fence_before();
-                        mbar_arrive(&sm.t_free);
-                    }
-                    uint32_t pk[32];
+                    for (int b = 0; b < 4; ++b) {
+                        if (b <= quad) {
+                            tmem_ld32(tl + CF::tT + b * 32, t);
+                            tmem_ld_wait();
+                            if (b == quad) {
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        const int jk = hh * 64 + 2 * e;  // key index within the chunk
-                        const float a = jk <= i ? __uint_as_float(t[2 * e]) : 0.f;
-                        const float b = jk + 1 <= i ? __uint_as_float(t[2 * e + 1]) : 0.f;
-                        pk[e] = pack_bf16(a, b);
+                                for (int e = 0; e < 16; ++e) {
+                                    const int jk = 2 * e;  // key offset within the diagonal block
+                                    pk[e] = pack_bf16(jk <= lane ? __uint_as_float(t[2 * e]) : 0.f,
+                                                      jk + 1 <= lane ? __uint_as_float(t[2 * e + 1]) : 0.f);
+                                }
+                            } else {
+#pragma unroll
+                                for (int e = 0; e < 16; ++e)
+                                    pk[e] = pack_bf16(__uint_as_float(t[2 * e]), __uint_as_float(t[2 * e + 1]));
+                            }
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) pk[e] = 0u;
+                        }
+                        if (b == 3) {  // all of T that this warp reads has been read
+                            tc_fence_before();
+                            mbar_arrive(&sm.t_free);
+                        }
+                        tmem_st16(tl + CF::tP + b * 16, pk);
                     }
-                    tmem_st16(tl + CF::tP + hh * 32, *reinterpret_cast<uint32_t(*)[16]>(&pk[0]));
-                    tmem_st16(tl + CF::tP + hh * 32 + 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[16]));
                 }
                 tmem_st_wait();
                 tc_fence_before();
@@ -775,7 +812,9 @@ la_status launch(const Problem &p)
 
     const int n_chunks = ceil_div(p.N, kC);
     const long long work = (long long)p.BH * n_chunks;
-    const int L = (int)std::min<long long>(8, std::max<long long>(1, (work + sm_count() - 1) / sm_count()));
+    // Chunks per segment: enough items to fill the GPU, at most 16 (longer segments
+    // mean fewer scan steps; the K, V re-read of phase C should still hit L2).
+    const int L = (int)std::min<long long>(16, std::max<long long>(1, (work + sm_count() - 1) / sm_count()));
     const int G = ceil_div(n_chunks, L);
     const size_t items = (size_t)p.BH * G;
     const size_t flag_bytes = ((items * 8 + 16) + 255) / 256 * 256;
