@@ -519,6 +519,47 @@ def run_gpu(args, dist):
     return 0
 
 
+PROFILE_CASES = ("headline", "causal_long", "causal_long_quarter", "noncausal", "decode")
+
+
+def run_profile_case(name: str, launches: int) -> int:
+    """A few plain launches of one workload (no graphs, no timing), for ncu.
+
+    causal_long_quarter is the long causal workload at N = 16384 (537 MB of
+    q, k, v, o: above L2, small enough for multi-pass profiling)."""
+    import torch
+    import causal_kernelized_attention_gb300 as la
+    from causal_kernelized_attention_gb300 import build as la_build
+    la_build.build()
+    la.load_library()
+    if name in ("headline", "causal_long", "causal_long_quarter"):
+        w = workloads.CAUSAL_BF16 if name == "headline" else workloads.CAUSAL_BF16_LONG
+        if name == "causal_long_quarter":
+            import dataclasses
+            w = dataclasses.replace(w, N=16384)
+        q, k, v = workloads.device_forward_inputs(w)
+        o = torch.empty_like(v)
+        for _ in range(launches):
+            la.la_forward_causal(q, k, v, o, chunk=w.chunk, eps=w.eps)
+    elif name == "noncausal":
+        w = workloads.NONCAUSAL_BF16
+        q, k, v = workloads.device_forward_inputs(w)
+        o = torch.empty_like(v)
+        for _ in range(launches):
+            la.la_forward_noncausal(q, k, v, o, eps=w.eps)
+    else:
+        import dataclasses
+        w = dataclasses.replace(workloads.DECODE_BF16, steps=launches)
+        (qp, kp, vp), (qd, kd, vd) = workloads.device_decode_inputs(w)
+        S, z = la.la_prefill_state(kp, vp)
+        o = torch.empty((w.B, w.H, w.dv), dtype=torch.bfloat16, device="cuda")
+        for t in range(launches):
+            la.la_decode_step(S, z, qd[t], kd[t], vd[t], o, eps=w.eps)
+    torch.cuda.synchronize()
+    print("profile case %s: %d launches ok" % (name, launches))
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -529,7 +570,12 @@ def main():
     ap.add_argument("--path-reps", type=int, default=20, help="timed steps of the long causal path")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--profile-case", choices=PROFILE_CASES, default=None,
+                    help="run a few plain launches of one workload (for ncu) instead of the benchmark")
+    ap.add_argument("--profile-launches", type=int, default=3)
     args = ap.parse_args()
+    if args.profile_case:
+        return run_profile_case(args.profile_case, args.profile_launches)
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps; the line reports the count used
     dist = Dist()
     if args.impl == "reference":
