@@ -123,6 +123,12 @@ def ncu_traffic(kernel_tag):
         return None
 
 
+def whole_job_throughput(world: int, units_per_rank: float, steps: int, slowest_secs: float) -> float:
+    """Units per second of the whole job: every rank processes `units_per_rank`
+    per step (weak scaling), and the job takes as long as its slowest rank."""
+    return world * units_per_rank * steps / slowest_secs
+
+
 # --------------------------------------------------------------------------- clocks
 class ClockSampler:
     """nvidia-smi sampling of SM clocks and throttle reasons while the GPU works."""
@@ -474,13 +480,13 @@ def run_gpu(args, dist):
                                                               src, sampler)
     secs_max = dist.max(secs)
     t_step = secs_max / args.steps
-    value = dist.world * w.B * w.N * args.steps / secs_max
+    value = whole_job_throughput(dist.world, w.B * w.N, args.steps, secs_max)
     fl = causal_flops(w.BH, w.N, w.dk, w.dv, w.chunk)
     roof = roofline(fl, nbytes, secs / args.steps, peaks, src, ncu_traffic("causal_headline"))
 
     e2e_secs, h2d, d2h = bench_causal_e2e(torch, la, w, max(10, min(args.steps, 200)), args.warmup, dist)
     e2e_steps = max(10, min(args.steps, 200))
-    e2e_value = dist.world * w.B * w.N * e2e_steps / dist.max(e2e_secs)
+    e2e_value = whole_job_throughput(dist.world, w.B * w.N, e2e_steps, dist.max(e2e_secs))
 
     paths = {}
     if not args.headline_only:
