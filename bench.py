@@ -102,8 +102,10 @@ def roofline(flops, nbytes, seconds, peaks, source, traffic=None, burst=True):
 
 def ncu_traffic(kernel_tag):
     """DRAM bytes per launch from a committed ncu summary, if it still matches the
-    kernel source (profiles/<tag>.md holds `traffic_bytes_per_launch:` and
-    `source_sha256:` lines); None otherwise."""
+    kernel source (profiles/<tag>.md holds `traffic_bytes_per_launch:`,
+    `source_file:` -- one path, or several separated by commas -- and
+    `source_sha256:`, the SHA-256 of those files' bytes concatenated in that
+    order); None otherwise."""
     import hashlib
     path = os.path.join(ROOT, "profiles", kernel_tag + ".md")
     if not os.path.exists(path):
@@ -114,8 +116,10 @@ def ncu_traffic(kernel_tag):
             k, v = line.strip().split(":", 1)
             fields[k.strip()] = v.strip().strip("`")
     try:
-        src = os.path.join(ROOT, fields["source_file"])
-        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+        h = hashlib.sha256()
+        for f in fields["source_file"].split(","):
+            h.update(open(os.path.join(ROOT, f.strip()), "rb").read())
+        sha = h.hexdigest()
         if sha != fields["source_sha256"]:
             return None
         return int(fields["traffic_bytes_per_launch"])

@@ -121,6 +121,10 @@ la_status la_forward_noncausal(const void *q, const void *k, const void *v, void
     if (st != LA_OK || empty) return st;
     if (!supported_dim(dk) || !supported_dim(dv)) return LA_ERR_UNSUPPORTED;
     Problem p{q, k, v, o, B * H, N, dk, dv, 0, eps, dtype, (cudaStream_t)stream};
+    if (dtype == LA_BF16) {
+        st = noncausal_tc(p);
+        if (st != LA_ERR_UNSUPPORTED) return st;
+    }
     return noncausal_simt(p);
 }
 
@@ -190,10 +194,12 @@ la_status la_get_device_status(la_stream_t stream)
 {
     la_status st = cuda_status(cudaStreamSynchronize((cudaStream_t)stream));
     if (st != LA_OK) return st;
-    unsigned bits = 0;
+    unsigned bits = 0, nc_bits = 0;
     st = tc_causal_read_status((cudaStream_t)stream, &bits);
     if (st != LA_OK) return st;
-    return (bits & kStatusTimeout) ? LA_ERR_TIMEOUT : LA_OK;
+    st = tc_noncausal_read_status((cudaStream_t)stream, &nc_bits);
+    if (st != LA_OK) return st;
+    return ((bits | nc_bits) & kStatusTimeout) ? LA_ERR_TIMEOUT : LA_OK;
 }
 
 int la_version(void) { return 100; }

@@ -43,9 +43,12 @@ la_status decode_step(float *S, float *z, const void *q, const void *k, const vo
 // Tensor-core (tcgen05) paths (la_tc_causal.cu); return LA_ERR_UNSUPPORTED when
 // the problem is outside the shapes they are built for.
 la_status causal_tc(const Problem &p);
+// (la_tc_noncausal.cu)
+la_status noncausal_tc(const Problem &p);
 
 // Device status words of translation units that run bounded waits: read and clear.
 la_status tc_causal_read_status(cudaStream_t s, unsigned *bits);
+la_status tc_noncausal_read_status(cudaStream_t s, unsigned *bits);
 
 bool supported_dim(int d);
 

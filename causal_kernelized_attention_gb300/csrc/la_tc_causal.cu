@@ -33,6 +33,7 @@
 #include "la_common.cuh"
 #include "la_internal.h"
 #include "la_sm100.cuh"
+#include "la_tc_common.cuh"
 
 #include <algorithm>
 #include <mutex>
@@ -42,18 +43,15 @@ namespace la {
 namespace {
 
 using namespace sm100;
+using namespace tc;
 
 static __device__ unsigned g_tc_status;
 
-constexpr int kC = 128;                  // chunk (tokens per tile)
 constexpr int kThreads = 576;
 constexpr int kPhiThreads = 256;         // warps 0-7
 // Epilogue warps access the TMEM lane quadrant warp % 4, so each group of four
 // consecutive warps covers all 128 lanes.
 constexpr int kTmaWarp = 8, kMmaWarp = 9, kEpiPWarp0 = 10, kEpiOWarp0 = 14;
-constexpr uint32_t kSleepHintNs = 200000;  // per try_wait; the total wait stays bounded below
-constexpr uint32_t kBox = kC * 128;      // one [128 rows x 64 bf16] swizzled box: 16 KB
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far beyond any healthy wait
 // Per-segment publish counters: each of the 8 phase-B warps adds 1 (with release
 // semantics) once its part of a state is stored; kPublished means complete, and
 // kPoison or more marks a segment whose CTA gave up.
@@ -104,162 +102,13 @@ struct Params {
     float eps;
 };
 
-__device__ __forceinline__ bool aborted(const volatile int *a) { return *a != 0; }
-
-// Bounded wait on an mbarrier phase; sets the CTA abort flag and the device
-// status word on expiry.
 __device__ __forceinline__ bool wait_bar(int *abort_flag, uint64_t *bar, uint32_t parity)
 {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
-    while (true) {
-        if (mbar_try_wait_sleep(bar, parity, kSleepHintNs)) return true;
-        if (aborted(abort_flag)) return false;
-        if (globaltimer_ns() - t0 > kWaitLimitNs) {
-            *(volatile int *)abort_flag = 1;
-            atomicOr(&g_tc_status, kStatusTimeout);
-            return false;
-        }
-    }
+    return tc::wait_bar(&g_tc_status, abort_flag, bar, parity);
 }
-
-// Same, with one result for the whole warp (for roles that issue warp-collective
-// tcgen05.ld / tcgen05.st after the wait).
 __device__ __forceinline__ bool wait_bar_warp(int *abort_flag, uint64_t *bar, uint32_t parity)
 {
-    return __all_sync(0xffffffffu, wait_bar(abort_flag, bar, parity));
-}
-
-__device__ __forceinline__ uint32_t pack_bf16(float a, float b)
-{
-    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-    return *reinterpret_cast<uint32_t *>(&h);
-}
-
-// phi on a pair of bf16 values: exp(min(x, 0)) + max(x, 0), which is x + 1 for
-// x > 0 and exp(x) otherwise, all in packed bf16x2: y = min(x, 0) * log2(e) with
-// one rounding (log2(e) split into a bf16 head and tail, fused multiply-add),
-// then the packed bf16 exp2 of the special-function unit (two values per
-// operation), then the exact add of max(x, 0).  The result is a bf16 tensor-core
-// operand either way; rounding y to bf16 perturbs exp(x) by about |x| * 2^-9
-// relative, which stays far inside the bf16 tolerances.
-__device__ __forceinline__ uint32_t ex2_bf16x2(uint32_t y)
-{
-    uint32_t r;
-    asm("ex2.approx.ftz.bf16x2 %0, %1;" : "=r"(r) : "r"(y));
-    return r;
-}
-__device__ __forceinline__ uint32_t phi2(uint32_t w)
-{
-    const __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162 *>(&w);
-    const __nv_bfloat162 zero = __float2bfloat162_rn(0.f);
-    const __nv_bfloat162 log2e_hi = __float2bfloat162_rn(1.4453125f);          // bf16(log2 e)
-    const __nv_bfloat162 log2e_lo = __float2bfloat162_rn(-0.0026174591f);      // log2 e - head
-    const __nv_bfloat162 neg = __hmin2(x, zero);
-    const __nv_bfloat162 y = __hfma2(neg, log2e_hi, __hmul2(neg, log2e_lo));
-    const uint32_t yb = *reinterpret_cast<const uint32_t *>(&y);
-    const uint32_t eb = ex2_bf16x2(yb);
-    const __nv_bfloat162 r = __hadd2(*reinterpret_cast<const __nv_bfloat162 *>(&eb), __hmax2(x, zero));
-    return *reinterpret_cast<const uint32_t *>(&r);
-}
-
-// phi in place on one shared-memory tile, by NT threads.  A unit is half of one
-// 128-byte row of a 64-column box (4 chunks of 16 bytes); thread t takes units
-// t, t + NT, ...  Units of rows >= `valid` (past the end of the sequence) are
-// zeroed.  All loads of a thread are issued before its arithmetic.  The chunk
-// order is rotated by the row so that the 8 threads of a quarter-warp (8
-// consecutive rows) touch 8 different bank groups.
-template <int D, int NT>
-__device__ __forceinline__ void phi_tile(uint8_t *tile, int t, int valid)
-{
-    constexpr int kUnits = 128 * (D / 32);
-    constexpr int NU = (kUnits + NT - 1) / NT;
-    uint4 buf[NU][4];
-#pragma unroll
-    for (int m = 0; m < NU; ++m) {
-        const int u = t + NT * m, row = u & 127, hb = u >> 7;
-        if (u < kUnits) {
-            const uint8_t *rp = tile + (hb >> 1) * kBox + row * 128;
-            const int rot = row + (hb & 1) * 4;
-#pragma unroll
-            for (int k = 0; k < 4; ++k) buf[m][k] = *reinterpret_cast<const uint4 *>(rp + ((rot + k) & 7) * 16);
-        }
-    }
-#pragma unroll
-    for (int m = 0; m < NU; ++m) {
-        const int u = t + NT * m, row = u & 127;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            uint4 &x = buf[m][k];
-            x = row < valid ? make_uint4(phi2(x.x), phi2(x.y), phi2(x.z), phi2(x.w)) : make_uint4(0u, 0u, 0u, 0u);
-        }
-    }
-#pragma unroll
-    for (int m = 0; m < NU; ++m) {
-        const int u = t + NT * m, row = u & 127, hb = u >> 7;
-        if (u < kUnits) {
-            uint8_t *rp = tile + (hb >> 1) * kBox + row * 128;
-            const int rot = row + (hb & 1) * 4;
-#pragma unroll
-            for (int k = 0; k < 4; ++k) *reinterpret_cast<uint4 *>(rp + ((rot + k) & 7) * 16) = buf[m][k];
-        }
-    }
-}
-
-// Descriptor helpers (see la_sm100.cuh for the layouts).
-__device__ __forceinline__ uint64_t kmajor(uint32_t tile, int kk)
-{
-    return desc_sw128(tile + (kk >> 2) * kBox + (kk & 3) * 32, 16, 1024);
-}
-__device__ __forceinline__ uint64_t mnmajor(uint32_t tile, int kk, uint32_t lbo)
-{
-    return desc_sw128(tile + kk * 2048, lbo, 1024);
-}
-__device__ __forceinline__ uint64_t wdesc(uint32_t w, int kk)
-{
-    return desc_sw128(w + (kk >> 2) * 1024 + (kk & 3) * 32, 16, 2048);
-}
-
-// Row i of the bf16 state copy (32 columns from col0), MN-major 128-byte swizzled:
-// 64-column blocks of D rows x 128 bytes.
-template <int D>
-__device__ __forceinline__ void put_sb(uint8_t *sb, int i, int col0, const float (&x)[32])
-{
-#pragma unroll
-    for (int c8 = 0; c8 < 32; c8 += 8) {
-        const int col = col0 + c8;
-        const uint32_t off = (col >> 6) * (D * 128) + i * 128 + ((((col & 63) >> 3) ^ (i & 7)) << 4);
-        *reinterpret_cast<uint4 *>(sb + off) =
-            make_uint4(pack_bf16(x[c8], x[c8 + 1]), pack_bf16(x[c8 + 2], x[c8 + 3]),
-                       pack_bf16(x[c8 + 4], x[c8 + 5]), pack_bf16(x[c8 + 6], x[c8 + 7]));
-    }
-}
-// z_i split into a high and a low bf16 part: rows 1 and 2 of W.
-__device__ __forceinline__ void put_z(uint8_t *w, int i, float zv)
-{
-    const __nv_bfloat16 hi = __float2bfloat16_rn(zv);
-    const __nv_bfloat16 lo = __float2bfloat16_rn(zv - __bfloat162float(hi));
-    uint8_t *blk = w + (i >> 6) * 1024;
-    *reinterpret_cast<__nv_bfloat16 *>(blk + sw128_offset(1, i & 63)) = hi;
-    *reinterpret_cast<__nv_bfloat16 *>(blk + sw128_offset(2, i & 63)) = lo;
-}
-// Published scan states use a thread-major layout, so that the 32 rows a warp
-// handles are contiguous: the float4 holding columns 4c..4c+3 of row i is at
-// float4 index c*D + i, and z_i follows at float D*D + i.
-template <int D>
-__device__ __forceinline__ void add_state(float (&acc)[32], const float *state, int cg0, int i)
-{
-    const float4 *s4 = reinterpret_cast<const float4 *>(state);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-        const float4 x = __ldcg(s4 + (size_t)(cg0 + e) * D + i);
-        acc[4 * e] += x.x; acc[4 * e + 1] += x.y; acc[4 * e + 2] += x.z; acc[4 * e + 3] += x.w;
-    }
-}
-__device__ __forceinline__ void to_floats(const uint32_t *a, float (&x)[32])
-{
-#pragma unroll
-    for (int e = 0; e < 32; ++e) x[e] = __uint_as_float(a[e]);
+    return tc::wait_bar_warp(&g_tc_status, abort_flag, bar, parity);
 }
 
 template <int D>
@@ -695,10 +544,13 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
                             pack_bf16(__uint_as_float(a[8 * c + 4]) * inv, __uint_as_float(a[8 * c + 5]) * inv),
                             pack_bf16(__uint_as_float(a[8 * c + 6]) * inv, __uint_as_float(a[8 * c + 7]) * inv));
                 }
-                tc_fence_before();
-                mbar_arrive(&sm.o_free);
+                // o_staged before o_free: the next chunk's o_full needs every thread's
+                // o_free, so no thread can arrive on o_staged for the next chunk while
+                // another has yet to arrive for this one.
                 fence_proxy_async_smem();
                 mbar_arrive(&sm.o_staged);
+                tc_fence_before();
+                mbar_arrive(&sm.o_free);
                 if (leader && wait_bar(abort_flag, &sm.o_staged, cj & 1)) {
 #pragma unroll
                     for (int cc = 0; cc < D / 64; ++cc)
@@ -745,61 +597,6 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
 }
 
 // ------------------------------------------------------------------ host side
-typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
-                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
-                                  CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
-                                  CUtensorMapFloatOOBfill);
-
-la_status encode_fn(EncodeTiledFn *out)
-{
-    static std::mutex mu;
-    static EncodeTiledFn fn = nullptr;
-    std::lock_guard<std::mutex> lock(mu);
-    if (!fn) {
-        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
-        cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", (void **)&fn, 12000,
-                                                         cudaEnableDefault, &q);
-        if (e != cudaSuccess) return cuda_status(e);
-        if (q != cudaDriverEntryPointSuccess || !fn) {
-            fn = nullptr;
-            return cuda_status(cudaErrorNotSupported);
-        }
-    }
-    *out = fn;
-    return LA_OK;
-}
-
-// [BH, N, D] bf16 as a 3-D tensor (D, N, BH); box = 64 columns x 128 rows, 128-byte swizzle.
-la_status make_map(CUtensorMap *m, const void *ptr, int BH, int N, int D)
-{
-    EncodeTiledFn enc;
-    la_status st = encode_fn(&enc);
-    if (st != LA_OK) return st;
-    const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)N, (cuuint64_t)BH};
-    const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)N * D * 2};
-    const cuuint32_t box[3] = {64, (cuuint32_t)kC, 1};
-    const cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, estr,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? LA_OK : cuda_status(cudaErrorInvalidValue);
-}
-
-int sm_count()
-{
-    static std::mutex mu;
-    static std::unordered_map<int, int> cache;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return 148;
-    std::lock_guard<std::mutex> lock(mu);
-    auto it = cache.find(dev);
-    if (it != cache.end()) return it->second;
-    int n = 148;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) n = 148;
-    cache[dev] = n;
-    return n;
-}
-
 template <int D>
 la_status launch(const Problem &p)
 {

@@ -1,0 +1,635 @@
+// Tensor-core (tcgen05 + TMA) non-causal forward, bf16 in / fp32 accumulate,
+// dk = dv = D in {64, 128}.
+//
+// The non-causal form ("Linear attention: change the order.", mlblogg.com,
+// associative trick and its NumPy implementation; "Linear Attention -- Math +
+// Variants", aicassindra.com, the quadratic wall): the key-value summary of a
+// head is built once, S = sum_n phi(k_n)^T v_n and z = sum_n phi(k_n), and every
+// output row reads it, o_n = phi(q_n) S / max(phi(q_n) z, eps).
+//
+//  * One persistent CTA per SM takes work items by ticket.  Tickets first name
+//    (head, split of its key chunks) items, which build the summary, then
+//    (head, group of query chunks) items, which write outputs.  A CTA takes its
+//    tickets in increasing order, so an output item only waits on summary items
+//    whose tickets were taken before, by CTAs that are running.
+//  * Summary item: per key/value chunk, S_p += phi(K_c)^T V_c and
+//    z_p += phi(K_c)^T 1 in tensor memory; the split's partial (fp32) goes to
+//    global memory.  The CTA that completes the last split of a head sums the
+//    head's partials in split order (so the result does not depend on which CTA
+//    comes last) and writes the head's state image -- the bf16 copy of S in the
+//    MN-major swizzled layout of the output MMA and z as a bf16 high + low pair,
+//    byte for byte as shared memory holds them -- then sets the head's ready flag.
+//  * Output item: one bulk copy brings the image into shared memory (only when
+//    the head changes); per query chunk O = phi(Q_c) S_bf16 and
+//    qz = phi(Q_c)(z_hi + z_lo) on the tensor cores; o = O / max(qz, eps),
+//    rounded to bf16 in shared memory and written by a TMA store.
+//
+// Warp roles (512 threads): warps 0-3 epilogue (TMEM lane quadrant = warp),
+// warp 4 scheduler and TMA producer, warp 5 MMA issuer and TMEM owner, warp 6
+// state-image loader, warp 7 idle, warps 8-15 apply phi in shared memory.  Each
+// item is published to the other roles through a small ring in shared memory.
+// Every wait is bounded (mbarriers and the ready flag alike); on expiry the CTA
+// records LA_ERR_TIMEOUT in this file's status word and winds down.
+#include "la_common.cuh"
+#include "la_internal.h"
+#include "la_sm100.cuh"
+#include "la_tc_common.cuh"
+
+#include <algorithm>
+
+namespace la {
+namespace {
+
+using namespace sm100;
+using namespace tc;
+
+static __device__ unsigned g_nc_status;
+
+constexpr int kThreads = 512;
+constexpr int kEpiThreads = 128;  // warps 0-3
+constexpr int kTmaWarp = 4, kMmaWarp = 5, kImgWarp = 6, kPhiWarp0 = 8;
+constexpr int kPhiThreads = 256;  // warps 8-15
+constexpr int kRing = 4;          // item ring entries
+// Readers of each ring entry: 8 phi warps, the MMA thread, the loader, 4 epilogue warps.
+constexpr uint32_t kRingReaders = 8 + 1 + 1 + 4;
+
+enum : int { kEnd = 0, kSum = 1, kOut = 2 };
+
+struct Item {
+    int kind, bh, c0, nch, split;
+};
+
+template <int D>
+struct Cfg {
+    static constexpr uint32_t kTileBytes = kC * D * 2;
+    static constexpr int kStages = D == 128 ? 2 : 6;        // a stage holds K and V, or Q and the staged O
+    static constexpr int kImgs = D == 128 ? 1 : 2;          // state images held at once
+    static constexpr uint32_t kSbBytes = D * D * 2;
+    static constexpr uint32_t kImgBytes = 2048 + kSbBytes;  // W (z rows) then the bf16 copy of S
+    // Accumulator buffers in TMEM: [S or O: D columns][z or qz: 16 columns].
+    static constexpr uint32_t kAccStride = D == 128 ? 256 : 128;
+    static constexpr int kAcc = 512 / kAccStride;
+};
+
+template <int D>
+struct alignas(1024) Smem {
+    uint8_t stage[Cfg<D>::kStages][2 * Cfg<D>::kTileBytes];
+    // Summary W: row 0 ones (column sums of phi(K)); rows 8..15 of its descriptor
+    // alias into img[0], which only feeds result columns that are never read.
+    uint8_t w1[2048];
+    uint8_t img[Cfg<D>::kImgs][Cfg<D>::kImgBytes];
+    uint64_t full[Cfg<D>::kStages], phi_done[Cfg<D>::kStages], empty[Cfg<D>::kStages];
+    uint64_t item_full[kRing], item_empty[kRing];
+    uint64_t acc_full[Cfg<D>::kAcc], acc_free[Cfg<D>::kAcc], o_staged[Cfg<D>::kAcc];
+    uint64_t img_full[Cfg<D>::kImgs], img_empty[Cfg<D>::kImgs];
+    uint64_t epi_sync, drain;
+    Item items[kRing];
+    uint32_t tmem_base;
+    int abort;
+    int last;  // the epilogue's CTA completed the last split of its head
+};
+
+static_assert(sizeof(Smem<128>) <= 232448, "exceeds the 227 KB per-CTA shared memory limit");
+static_assert(sizeof(Smem<64>) <= 232448, "exceeds the 227 KB per-CTA shared memory limit");
+
+struct Params {
+    float *part;         // [BH, P, D*D + D] split partials (S then z; thread-major, see add_state)
+    uint8_t *img;        // [BH, kImgBytes] state images
+    uint32_t *ticket;    // work ticket
+    uint32_t *arrived;   // [BH] completed splits per head
+    uint32_t *ready;     // [BH] 1 once the head's state image is written
+    int N, BH, n_chunks;
+    int P, L1;           // splits per head, key chunks per split
+    int T, L2;           // output items per head, query chunks per item
+    float eps;
+};
+
+__device__ __forceinline__ bool wait_bar(int *abort_flag, uint64_t *bar, uint32_t parity)
+{
+    return tc::wait_bar(&g_nc_status, abort_flag, bar, parity);
+}
+__device__ __forceinline__ bool wait_bar_warp(int *abort_flag, uint64_t *bar, uint32_t parity)
+{
+    return tc::wait_bar_warp(&g_nc_status, abort_flag, bar, parity);
+}
+
+__device__ __forceinline__ Item decode_ticket(const Params &prm, int t)
+{
+    Item it{kEnd, 0, 0, 0, 0};
+    const int n1 = prm.BH * prm.P, n2 = prm.BH * prm.T;
+    if (t < n1) {
+        it.kind = kSum;
+        it.bh = t / prm.P;
+        it.split = t % prm.P;
+        it.c0 = it.split * prm.L1;
+        it.nch = min(prm.L1, prm.n_chunks - it.c0);
+    } else if (t < n1 + n2) {
+        const int u = t - n1;
+        it.kind = kOut;
+        it.bh = u / prm.T;
+        it.c0 = (u % prm.T) * prm.L2;
+        it.nch = min(prm.L2, prm.n_chunks - it.c0);
+    }
+    return it;
+}
+
+// Sums the head's P partials (in split order) and writes its state image:
+// bytes [0, 2048) are W (row 1 = z_hi, row 2 = z_lo, other rows zero) and bytes
+// [2048, 2048 + 2 D^2) the bf16 copy of S, MN-major, 128-byte swizzled.  Run by
+// the 128 epilogue threads; thread t takes state row t % D and a column range.
+template <int D>
+__device__ __forceinline__ void build_image(const Params &prm, int bh, int t)
+{
+    constexpr int kGroups = 128 / D, kCols = D / kGroups;
+    const size_t seg = (size_t)D * D + D;
+    const float *part = prm.part + (size_t)bh * prm.P * seg;
+    uint8_t *img = prm.img + (size_t)bh * Cfg<D>::kImgBytes;
+    const int i = t % D, grp = t / D;
+#pragma unroll 1
+    for (int cc = 0; cc < kCols; cc += 32) {
+        float acc[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) acc[e] = 0.f;
+        const int col0 = grp * kCols + cc;
+        for (int p = 0; p < prm.P; ++p) add_state<D>(acc, part + p * seg, col0 >> 2, i);
+        put_sb<D>(img + 2048, i, col0, acc);
+    }
+    // W: thread t writes one 16-byte chunk (block t / 64, row (t / 8) % 8,
+    // physical chunk t % 8, which holds logical chunk (t % 8) ^ row).
+    const int blk = t >> 6, row = (t >> 3) & 7, lc = (t & 7) ^ row;
+    uint32_t wv[4] = {0u, 0u, 0u, 0u};
+    if (row == 1 || row == 2) {
+#pragma unroll
+        for (int e = 0; e < 8; e += 2) {
+            float hl[2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int kidx = 64 * blk + 8 * lc + e + h;
+                float zk = 0.f;
+                if (kidx < D)
+                    for (int p = 0; p < prm.P; ++p) zk += __ldcg(part + p * seg + (size_t)D * D + kidx);
+                const float hi = __bfloat162float(__float2bfloat16_rn(zk));
+                hl[h] = row == 1 ? hi : zk - hi;
+            }
+            wv[e >> 1] = pack_bf16(hl[0], hl[1]);
+        }
+    }
+    *reinterpret_cast<uint4 *>(img + blk * 1024 + row * 128 + (t & 7) * 16) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+}
+
+// The epilogue threads' barrier: an mbarrier of 128 arrivals, waited on with a
+// bound (a thread can arrive for the next use only after the current use has
+// completed, so the phases never mix).
+__device__ __forceinline__ bool epi_barrier(int *abort_flag, uint64_t *bar, uint32_t &uses)
+{
+    mbar_arrive(bar);
+    const bool ok = wait_bar_warp(abort_flag, bar, uses & 1);
+    ++uses;
+    return ok;
+}
+
+template <int D>
+__global__ void __launch_bounds__(512, 1)
+noncausal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
+                    const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_o,
+                    const Params prm)
+{
+    using CF = Cfg<D>;
+    constexpr int S = CF::kStages;
+    constexpr uint32_t kTile = CF::kTileBytes;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    if (smem_u32(smem_raw) & 1023u) {  // layout assumption of the swizzled tiles
+        if (threadIdx.x == 0) atomicOr(&g_nc_status, kStatusTimeout);
+        return;
+    }
+    Smem<D> &sm = *reinterpret_cast<Smem<D> *>(smem_raw);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    if (tid < 128) {  // w1: row 0 ones, everything else zero
+        const int blk = tid >> 6, within = tid & 63;
+        const uint32_t val = (within < 8) ? 0x3F803F80u : 0u;
+        *reinterpret_cast<uint4 *>(sm.w1 + blk * 1024 + within * 16) = make_uint4(val, val, val, val);
+        fence_proxy_async_smem();
+    }
+    if (tid == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&sm.full[s], 1);
+            mbar_init(&sm.phi_done[s], kPhiThreads);
+            mbar_init(&sm.empty[s], 1);
+        }
+        for (int r = 0; r < kRing; ++r) {
+            mbar_init(&sm.item_full[r], 1);
+            mbar_init(&sm.item_empty[r], kRingReaders);
+        }
+        for (int a = 0; a < CF::kAcc; ++a) {
+            mbar_init(&sm.acc_full[a], 1);
+            mbar_init(&sm.acc_free[a], kEpiThreads);
+            mbar_init(&sm.o_staged[a], kEpiThreads);
+        }
+        for (int m = 0; m < CF::kImgs; ++m) {
+            mbar_init(&sm.img_full[m], 1);
+            mbar_init(&sm.img_empty[m], 1);
+        }
+        mbar_init(&sm.epi_sync, kEpiThreads);
+        mbar_init(&sm.drain, 1);
+        sm.abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(&sm.tmem_base, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sm.tmem_base;
+    int *abort_flag = &sm.abort;
+
+    if (warp >= kPhiWarp0) {
+        // ---------------------------------------------------------------- phi warps
+        const int t = tid - kPhiWarp0 * 32;
+        int j = 0;
+        for (int it = 0;; ++it) {
+            const int r = it % kRing;
+            if (!wait_bar_warp(abort_flag, &sm.item_full[r], (it / kRing) & 1)) break;
+            const Item item = sm.items[r];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.item_empty[r]);
+            if (item.kind == kEnd) break;
+            bool ok = true;
+            for (int c = 0; c < item.nch; ++c, ++j) {
+                const int s = j % S;
+                if (!(ok = wait_bar_warp(abort_flag, &sm.full[s], (j / S) & 1))) break;
+                // K (summary) or Q (output) is the first tile of the stage.
+                phi_tile<D, kPhiThreads>(sm.stage[s], t, prm.N - (item.c0 + c) * kC);
+                fence_proxy_async_smem();
+                mbar_arrive(&sm.phi_done[s]);
+            }
+            if (!ok) break;
+        }
+    } else if (warp == kTmaWarp) {
+        // ---------------------------------------------------------------- scheduler + TMA producer
+        if (lane == 0) {
+            tma_prefetch_map(&map_q);
+            tma_prefetch_map(&map_k);
+            tma_prefetch_map(&map_v);
+            tma_prefetch_map(&map_o);
+            int j = 0;
+            bool ok = true;
+            for (int it = 0; ok; ++it) {
+                const int r = it % kRing;
+                if (it >= kRing && !(ok = wait_bar(abort_flag, &sm.item_empty[r], ((it / kRing) - 1) & 1))) break;
+                const Item item = decode_ticket(prm, (int)atomicAdd(prm.ticket, 1u));
+                sm.items[r] = item;
+                mbar_arrive(&sm.item_full[r]);
+                if (item.kind == kEnd) break;
+                for (int c = 0; c < item.nch; ++c, ++j) {
+                    const int s = j % S, rr = j / S;
+                    if (rr > 0 && !(ok = wait_bar(abort_flag, &sm.empty[s], (rr - 1) & 1))) break;
+                    const int row0 = (item.c0 + c) * kC;
+                    uint8_t *st = sm.stage[s];
+                    if (item.kind == kSum) {
+                        mbar_arrive_expect_tx(&sm.full[s], 2 * kTile);
+#pragma unroll
+                        for (int b = 0; b < D / 64; ++b) {
+                            tma_load_3d(st + b * kBox, &map_k, &sm.full[s], 64 * b, row0, item.bh);
+                            tma_load_3d(st + kTile + b * kBox, &map_v, &sm.full[s], 64 * b, row0, item.bh);
+                        }
+                    } else {
+                        mbar_arrive_expect_tx(&sm.full[s], kTile);
+#pragma unroll
+                        for (int b = 0; b < D / 64; ++b)
+                            tma_load_3d(st + b * kBox, &map_q, &sm.full[s], 64 * b, row0, item.bh);
+                    }
+                }
+            }
+            // No copy may still be writing shared memory when the CTA exits.
+            for (int jj = max(0, j - S); jj < j; ++jj) {
+                const uint64_t t0 = globaltimer_ns();
+                while (!mbar_try_wait(&sm.full[jj % S], (jj / S) & 1) && globaltimer_ns() - t0 < kWaitLimitNs) {
+                }
+            }
+        }
+    } else if (warp == kMmaWarp) {
+        // ---------------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            const uint32_t id_KV = idesc_bf16_f32(128, D, true, true);    // phi(K)^T V
+            const uint32_t id_KW = idesc_bf16_f32(128, 16, true, false);  // phi(K)^T W^T
+            const uint32_t id_QS = idesc_bf16_f32(128, D, false, true);   // phi(Q) S_bf16
+            const uint32_t id_QW = idesc_bf16_f32(128, 16, false, false); // phi(Q) W^T
+            const uint32_t w1 = smem_u32(sm.w1);
+            int j = 0, q = 0, n_img = 0, cur_bh = -1, cur_m = 0;
+            bool ok = true;
+            for (int it = 0; ok; ++it) {
+                const int r = it % kRing;
+                if (!(ok = wait_bar(abort_flag, &sm.item_full[r], (it / kRing) & 1))) break;
+                const Item item = sm.items[r];
+                mbar_arrive(&sm.item_empty[r]);
+                if (item.kind == kEnd) break;
+                if (item.kind == kSum) {
+                    const int a = q % CF::kAcc;
+                    if (q >= CF::kAcc && !(ok = wait_bar(abort_flag, &sm.acc_free[a], ((q / CF::kAcc) - 1) & 1)))
+                        break;
+                    tc_fence_after();
+                    const uint32_t dS = tmem + a * CF::kAccStride, dZ = dS + D;
+                    for (int c = 0; c < item.nch; ++c, ++j) {
+                        const int s = j % S;
+                        if (!(ok = wait_bar(abort_flag, &sm.phi_done[s], (j / S) & 1))) break;
+                        tc_fence_after();
+                        // phi(K)^T is MN-major with its second 64-row block one box on
+                        // (for D = 64 that is the V tile: rows 64..127 are never read).
+                        const uint32_t ka = smem_u32(sm.stage[s]), va = ka + kTile;
+#pragma unroll
+                        for (int kk = 0; kk < kC / 16; ++kk) {
+                            const uint32_t acc = (c > 0 || kk > 0) ? 1u : 0u;
+                            mma_ss(dS, mnmajor(ka, kk, kBox), mnmajor(va, kk, kBox), id_KV, acc);
+                            mma_ss(dZ, mnmajor(ka, kk, kBox), wdesc(w1, kk), id_KW, acc);
+                        }
+                        mma_commit(&sm.empty[s]);
+                    }
+                    if (!ok) break;
+                    mma_commit(&sm.acc_full[a]);
+                    ++q;
+                } else {
+                    if (item.bh != cur_bh) {  // next state image; the one before it is free once
+                        const int m = n_img % CF::kImgs;  // every MMA issued so far completes
+                        if (n_img > 0) mma_commit(&sm.img_empty[(n_img - 1) % CF::kImgs]);
+                        if (!(ok = wait_bar(abort_flag, &sm.img_full[m], (n_img / CF::kImgs) & 1))) break;
+                        cur_bh = item.bh;
+                        cur_m = m;
+                        ++n_img;
+                    }
+                    const uint32_t w2 = smem_u32(sm.img[cur_m]), sb = w2 + 2048;
+                    for (int c = 0; c < item.nch; ++c, ++j, ++q) {
+                        const int s = j % S, a = q % CF::kAcc;
+                        if (!(ok = wait_bar(abort_flag, &sm.phi_done[s], (j / S) & 1))) break;
+                        if (q >= CF::kAcc && !(ok = wait_bar(abort_flag, &sm.acc_free[a], ((q / CF::kAcc) - 1) & 1)))
+                            break;
+                        tc_fence_after();
+                        const uint32_t qa = smem_u32(sm.stage[s]);
+                        const uint32_t dO = tmem + a * CF::kAccStride, dQZ = dO + D;
+#pragma unroll
+                        for (int kk = 0; kk < D / 16; ++kk) {
+                            mma_ss(dO, kmajor(qa, kk), mnmajor(sb, kk, D * 128), id_QS, kk > 0 ? 1u : 0u);
+                            mma_ss(dQZ, kmajor(qa, kk), wdesc(w2, kk), id_QW, kk > 0 ? 1u : 0u);
+                        }
+                        mma_commit(&sm.acc_full[a]);
+                    }
+                }
+            }
+            // all issued MMAs complete before TMEM is freed
+            mma_commit(&sm.drain);
+            const uint64_t t0 = globaltimer_ns();
+            while (!mbar_try_wait(&sm.drain, 0) && globaltimer_ns() - t0 < kWaitLimitNs) {
+            }
+        }
+    } else if (warp == kImgWarp) {
+        // ---------------------------------------------------------------- state-image loader
+        if (lane == 0) {
+            int n_img = 0, cur_bh = -1;
+            bool ok = true;
+            for (int it = 0; ok; ++it) {
+                const int r = it % kRing;
+                if (!(ok = wait_bar(abort_flag, &sm.item_full[r], (it / kRing) & 1))) break;
+                const Item item = sm.items[r];
+                mbar_arrive(&sm.item_empty[r]);
+                if (item.kind == kEnd) break;
+                if (item.kind != kOut || item.bh == cur_bh) continue;
+                const int m = n_img % CF::kImgs;
+                if (n_img >= CF::kImgs && !(ok = wait_bar(abort_flag, &sm.img_empty[m], ((n_img / CF::kImgs) - 1) & 1)))
+                    break;
+                // The head's summary is complete once its ready flag is set (bounded wait).
+                const uint64_t t0 = globaltimer_ns();
+                while (ld_acquire_gpu(prm.ready + item.bh) == 0u) {
+                    if (aborted(abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                        *(volatile int *)abort_flag = 1;
+                        atomicOr(&g_nc_status, kStatusTimeout);
+                        ok = false;
+                        break;
+                    }
+                    __nanosleep(256);
+                }
+                if (!ok) break;
+                fence_proxy_async_global();
+                mbar_arrive_expect_tx(&sm.img_full[m], CF::kImgBytes);
+                bulk_load(sm.img[m], prm.img + (size_t)item.bh * CF::kImgBytes, CF::kImgBytes, &sm.img_full[m]);
+                cur_bh = item.bh;
+                ++n_img;
+            }
+            // No copy may still be writing shared memory when the CTA exits.
+            for (int n = max(0, n_img - CF::kImgs); n < n_img; ++n) {
+                const uint64_t t0 = globaltimer_ns();
+                while (!mbar_try_wait(&sm.img_full[n % CF::kImgs], (n / CF::kImgs) & 1) &&
+                       globaltimer_ns() - t0 < kWaitLimitNs) {
+                }
+            }
+        }
+    } else if (warp < kEpiThreads / 32) {
+        // ---------------------------------------------------------------- epilogue warps 0-3
+        const int i = tid;  // TMEM lane = state row (summary) or query row (output)
+        const uint32_t tl = tmem + ((uint32_t)(warp * 32) << 16);
+        const bool leader = tid == 0;
+        const size_t seg = (size_t)D * D + D;
+        int j = 0, q = 0, prev_stage = -1;
+        uint32_t syncs = 0;
+        // Phase bit of each o_staged[a]: those barriers advance only on output
+        // jobs, while q also counts summary jobs.
+        uint32_t ostaged_phase = 0;
+        for (int it = 0;; ++it) {
+            const int r = it % kRing;
+            if (!wait_bar_warp(abort_flag, &sm.item_full[r], (it / kRing) & 1)) break;
+            const Item item = sm.items[r];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.item_empty[r]);
+            if (item.kind == kEnd) break;
+            if (item.kind == kSum) {
+                const int a = q % CF::kAcc;
+                if (!wait_bar_warp(abort_flag, &sm.acc_full[a], (q / CF::kAcc) & 1)) break;
+                tc_fence_after();
+                const uint32_t ta = tl + a * CF::kAccStride;
+                float *dst = prm.part + ((size_t)item.bh * prm.P + item.split) * seg;
+#pragma unroll 1
+                for (int cc = 0; cc < D; cc += 32) {
+                    uint32_t v[32];
+                    tmem_ld32(ta + cc, v);
+                    tmem_ld_wait();
+                    if (i < D) {
+                        float4 *d4 = reinterpret_cast<float4 *>(dst);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            d4[(size_t)((cc >> 2) + e) * D + i] =
+                                make_float4(__uint_as_float(v[4 * e]), __uint_as_float(v[4 * e + 1]),
+                                            __uint_as_float(v[4 * e + 2]), __uint_as_float(v[4 * e + 3]));
+                    }
+                }
+                const float zs = __uint_as_float(tmem_ld1(ta + D));
+                tmem_ld_wait();
+                if (i < D) dst[(size_t)D * D + i] = zs;
+                tc_fence_before();
+                mbar_arrive(&sm.acc_free[a]);
+                ++q;
+                j += item.nch;
+                // Count the split; the CTA that completes the head's last split builds its image.
+                __threadfence();
+                if (!epi_barrier(abort_flag, &sm.epi_sync, syncs)) break;
+                if (leader) sm.last = atom_add_acq_rel_gpu(prm.arrived + item.bh, 1u) == (uint32_t)(prm.P - 1);
+                if (!epi_barrier(abort_flag, &sm.epi_sync, syncs)) break;
+                if (sm.last) {
+                    __threadfence();
+                    build_image<D>(prm, item.bh, tid);
+                    __threadfence();
+                    fence_proxy_async_global();
+                    if (!epi_barrier(abort_flag, &sm.epi_sync, syncs)) break;
+                    if (leader) st_release_gpu(prm.ready + item.bh, 1u);
+                }
+            } else {
+                bool ok = true;
+                for (int c = 0; c < item.nch; ++c, ++j, ++q) {
+                    const int s = j % S, a = q % CF::kAcc;
+                    if (!(ok = wait_bar_warp(abort_flag, &sm.acc_full[a], (q / CF::kAcc) & 1))) break;
+                    tc_fence_after();
+                    const uint32_t ta = tl + a * CF::kAccStride;
+                    float inv;
+                    {
+                        uint32_t qz[32];  // columns D + 1 and D + 2: phi(q) z_hi, phi(q) z_lo
+                        tmem_ld32(ta + D, qz);
+                        tmem_ld_wait();
+                        inv = 1.f / fmaxf(__uint_as_float(qz[1]) + __uint_as_float(qz[2]), prm.eps);
+                    }
+                    uint8_t *ost = sm.stage[s] + kTile;  // the second tile of the stage stages O
+#pragma unroll 1
+                    for (int cc = 0; cc < D / 64; ++cc) {
+                        uint32_t v[64];
+                        tmem_ld32(ta + cc * 64, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+                        tmem_ld32(ta + cc * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+                        tmem_ld_wait();
+                        uint8_t *rowp = ost + cc * kBox + i * 128;
+#pragma unroll
+                        for (int u = 0; u < 8; ++u)
+                            *reinterpret_cast<uint4 *>(rowp + ((u ^ (i & 7)) << 4)) = make_uint4(
+                                pack_bf16(__uint_as_float(v[8 * u]) * inv, __uint_as_float(v[8 * u + 1]) * inv),
+                                pack_bf16(__uint_as_float(v[8 * u + 2]) * inv, __uint_as_float(v[8 * u + 3]) * inv),
+                                pack_bf16(__uint_as_float(v[8 * u + 4]) * inv, __uint_as_float(v[8 * u + 5]) * inv),
+                                pack_bf16(__uint_as_float(v[8 * u + 6]) * inv, __uint_as_float(v[8 * u + 7]) * inv));
+                    }
+                    // o_staged before acc_free: buffer a is refilled only after every
+                    // thread has arrived on acc_free[a], hence on o_staged[a] as well.
+                    fence_proxy_async_smem();
+                    mbar_arrive(&sm.o_staged[a]);
+                    tc_fence_before();
+                    mbar_arrive(&sm.acc_free[a]);
+                    if (leader && (ok = wait_bar(abort_flag, &sm.o_staged[a], (ostaged_phase >> a) & 1u))) {
+#pragma unroll
+                        for (int cc = 0; cc < D / 64; ++cc)
+                            tma_store_3d(&map_o, ost + cc * kBox, 64 * cc, (item.c0 + c) * kC, item.bh);
+                        tma_store_commit();
+                        // The previous tile's store has read its staged O: that stage may be refilled.
+                        tma_store_wait_read<1>();
+                        if (prev_stage >= 0) mbar_arrive(&sm.empty[prev_stage]);
+                        prev_stage = s;
+                    }
+                    ostaged_phase ^= 1u << a;
+                    if (!(ok = __all_sync(0xffffffffu, ok))) break;  // the whole warp leaves together
+                }
+                if (!ok) break;
+            }
+        }
+        if (leader) {
+            tma_store_wait_read_all();
+            if (prev_stage >= 0) mbar_arrive(&sm.empty[prev_stage]);
+            tma_store_wait_all();  // all output stores complete before the CTA exits
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == kMmaWarp) tmem_dealloc(tmem, 512);
+}
+
+// ------------------------------------------------------------------ host side
+template <int D>
+la_status launch(const Problem &p)
+{
+    using CF = Cfg<D>;
+    CUtensorMap mq, mk, mv, mo;
+    la_status st = make_map(&mq, p.q, p.BH, p.N, D);
+    if (st == LA_OK) st = make_map(&mk, p.k, p.BH, p.N, D);
+    if (st == LA_OK) st = make_map(&mv, p.v, p.BH, p.N, D);
+    if (st == LA_OK) st = make_map(&mo, p.o, p.BH, p.N, D);
+    if (st != LA_OK) return st;
+
+    const int n_chunks = ceil_div(p.N, kC);
+    const int n_sm = sm_count();
+    // About two summary items and four output items per SM: enough to balance
+    // the persistent CTAs; at most 32 partials per head for its last CTA to sum.
+    int P = std::min(std::min(32, n_chunks), std::max(1, ceil_div(2 * n_sm, p.BH)));
+    const int L1 = ceil_div(n_chunks, P);
+    P = ceil_div(n_chunks, L1);
+    int T = std::min(n_chunks, std::max(1, ceil_div(4 * n_sm, p.BH)));
+    const int L2 = ceil_div(n_chunks, T);
+    T = ceil_div(n_chunks, L2);
+    const long long items = (long long)p.BH * (P + T);
+    if (items > 0x7fffffffLL) return LA_ERR_UNSUPPORTED;
+
+    const size_t seg = (size_t)D * D + D;
+    const size_t flag_bytes = ((16 + (size_t)p.BH * 8) + 255) / 256 * 256;
+    const size_t part_bytes = ((size_t)p.BH * P * seg * 4 + 255) / 256 * 256;
+    const size_t img_bytes = (size_t)p.BH * CF::kImgBytes;
+
+    Scratch scratch;
+    st = scratch.alloc(flag_bytes + part_bytes + img_bytes, p.stream);
+    if (st != LA_OK) return st;
+    uint8_t *base = (uint8_t *)scratch.ptr;
+    cudaError_t e = cudaMemsetAsync(base, 0, flag_bytes, p.stream);
+    count_launches();
+    if (e != cudaSuccess) return cuda_status(e);
+
+    Params prm;
+    prm.ticket = (uint32_t *)base;
+    prm.arrived = (uint32_t *)(base + 16);
+    prm.ready = prm.arrived + p.BH;
+    prm.part = (float *)(base + flag_bytes);
+    prm.img = base + flag_bytes + part_bytes;
+    prm.N = p.N;
+    prm.BH = p.BH;
+    prm.n_chunks = n_chunks;
+    prm.P = P;
+    prm.L1 = L1;
+    prm.T = T;
+    prm.L2 = L2;
+    prm.eps = p.eps;
+
+    const int smem = (int)sizeof(Smem<D>);
+    auto kern = noncausal_tc_kernel<D>;
+    st = ensure_smem((const void *)kern, smem);
+    if (st != LA_OK) return st;
+    const unsigned grid = (unsigned)std::min<long long>(items, n_sm);
+    count_launches();
+    kern<<<grid, kThreads, smem, p.stream>>>(mq, mk, mv, mo, prm);
+    return cuda_status(cudaGetLastError());
+}
+
+}  // namespace
+
+la_status noncausal_tc(const Problem &p)
+{
+    if (p.dtype != LA_BF16 || p.dk != p.dv || (p.dk != 64 && p.dk != 128) || p.N < kC)
+        return LA_ERR_UNSUPPORTED;
+    return p.dk == 128 ? launch<128>(p) : launch<64>(p);
+}
+
+la_status tc_noncausal_read_status(cudaStream_t s, unsigned *bits)
+{
+    unsigned zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbolAsync(bits, g_nc_status, sizeof(unsigned), 0, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaMemcpyToSymbolAsync(g_nc_status, &zero, sizeof(unsigned), 0, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    return cuda_status(e);
+}
+
+}  // namespace la
