@@ -3,9 +3,11 @@
 #include <stdint.h>
 
 #include <atomic>
+#include <map>
 #include <mutex>
 #include <set>
 #include <tuple>
+#include <utility>
 
 #include "la_common.cuh"
 #include "la_internal.h"
@@ -54,6 +56,40 @@ la_status ensure_smem(const void *kernel, int bytes)
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (e != cudaSuccess) return cuda_status(e);
     done.insert(key);
+    return LA_OK;
+}
+
+la_status flag_workspace(cudaStream_t s, size_t bytes, void **out)
+{
+    *out = nullptr;
+    if (bytes > kFlagWorkspaceBytes) return LA_ERR_UNSUPPORTED;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_status(e);
+    static std::mutex mu;
+    static std::map<std::pair<int, cudaStream_t>, void *> spaces;  // kept until the process exits
+    std::lock_guard<std::mutex> lock(mu);
+    const auto key = std::make_pair(dev, s);
+    auto it = spaces.find(key);
+    if (it != spaces.end()) {
+        *out = it->second;
+        return LA_OK;
+    }
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    e = cudaStreamIsCapturing(s, &cs);
+    if (e != cudaSuccess) return cuda_status(e);
+    if (cs != cudaStreamCaptureStatusNone) return LA_ERR_UNSUPPORTED;
+    void *p = nullptr;
+    e = cudaMalloc(&p, kFlagWorkspaceBytes);
+    if (e != cudaSuccess) return cuda_status(e);
+    e = cudaMemsetAsync(p, 0, kFlagWorkspaceBytes, s);
+    count_launches();
+    if (e != cudaSuccess) {
+        cudaFree(p);
+        return cuda_status(e);
+    }
+    spaces[key] = p;
+    *out = p;
     return LA_OK;
 }
 

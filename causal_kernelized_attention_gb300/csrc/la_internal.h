@@ -55,6 +55,18 @@ bool supported_dim(int d);
 // Counts every kernel launch / memset the library enqueues (la_kernel_launches).
 void count_launches(unsigned n = 1);
 
+// Flag workspace of the ticketed kernels: kFlagWorkspaceBytes per (device,
+// stream), zeroed once when it is created, and left zeroed by every kernel that
+// uses it (the last CTA to finish clears what the launch used).  Layout: [0]
+// work ticket, [1] CTAs done, flags from byte 16.  Returns LA_ERR_UNSUPPORTED
+// when it cannot serve the call -- more bytes than it holds, or a stream under
+// capture that has none yet (it is created only outside capture) -- and the
+// caller then uses per-call scratch cleared by a memset.  Calls on one stream
+// are ordered, so they never share the flags at the same time; a captured graph
+// keeps the workspace of the stream it was captured on.
+constexpr size_t kFlagWorkspaceBytes = 64 << 10;
+la_status flag_workspace(cudaStream_t s, size_t bytes, void **out);
+
 // cudaFuncSetAttribute(MaxDynamicSharedMemorySize) once per kernel and device,
 // so that repeated calls (and stream capture) issue no attribute calls.
 la_status ensure_smem(const void *kernel, int bytes);

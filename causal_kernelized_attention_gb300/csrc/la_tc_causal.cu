@@ -57,27 +57,41 @@ constexpr int kTmaWarp = 8, kMmaWarp = 9, kEpiPWarp0 = 10, kEpiOWarp0 = 14;
 // kPoison or more marks a segment whose CTA gave up.
 constexpr uint32_t kPublished = 8, kPoison = 1u << 20;
 
+// Row sums and z ride on the tensor cores in one of two ways:
+//  * fused (D = 64): the B operand of P V and of the state update is [V | 1] and
+//    that of phi(Q) S is [S_bf16 | z]: one N = D + 16 MMA whose second 64-wide
+//    block (an LBO away) is the ones block (column 0 = 1) or the z block (columns
+//    0 and 1 = z_hi, z_lo), so result column D holds the row sum or z;
+//  * separate (D = 128, no room for those blocks): N = 16 MMAs against W, a
+//    [16 rows x 128] bf16 K-major operand (two 1 KB blocks of 8 rows; rows 8..15 of
+//    its descriptor alias into the next 2 KB, the S copy, and feed only unread
+//    columns).  Row 0 = ones, rows 1 and 2 = the high and low bf16 parts of z.
 template <int D>
 struct Cfg {
+    static constexpr bool kFused = D == 64;
     static constexpr int kStages = D == 128 ? 2 : 4;
     static constexpr uint32_t kTileBytes = kC * D * 2;
     static constexpr uint32_t kSbBytes = D * D * 2;   // bf16 copy of S, MN-major for the phi(Q) S MMA
-    // TMEM columns
-    static constexpr uint32_t tT = 0, tP = 128, tRS = 192, tQZ = 208, tZ = 224, tO = 256, tS = 256 + D;
+    // aux: fused = ones block (128 rows), S copy, z block (D rows); separate = W, S copy
+    static constexpr uint32_t kOnes = 0, kW = 0;
+    static constexpr uint32_t kSb = kFused ? kC * 128 : 2048;
+    static constexpr uint32_t kZb = kSb + kSbBytes;
+    static constexpr uint32_t kAuxBytes = kFused ? kZb + D * 128 : kSb + kSbBytes;
+    // TMEM columns (fused: O and S are D + 16 wide, z in column D of S)
+    static constexpr uint32_t tT = 0, tP = 128, tRS = 192, tQZ = 208, tO = 256;
+    static constexpr uint32_t tS = kFused ? 384 : 256 + D;
+    static constexpr uint32_t tZ = kFused ? tS + D : 224;
     static constexpr uint32_t kTmemCols = 512;
+    static_assert(tP + 64 <= tRS && tRS + 16 <= tQZ && tQZ + 16 <= tO && tS + (kFused ? D + 16 : D) <= kTmemCols,
+                  "TMEM column groups overlap");
 };
 
-// W: [16 rows x 128] bf16, K-major, two 1 KB blocks of 8 rows (rows 8..15 of the
-// descriptor alias into the next 2 KB, which is the S copy: only columns 0..2 of
-// results that use W are read).  Row 0 = ones (row and column sums), rows 1 and 2 =
-// the high and low bf16 parts of the running z.
 template <int D>
 struct alignas(1024) Smem {
     uint8_t q[Cfg<D>::kStages][Cfg<D>::kTileBytes];
     uint8_t k[Cfg<D>::kStages][Cfg<D>::kTileBytes];
     uint8_t v[Cfg<D>::kStages][Cfg<D>::kTileBytes];
-    uint8_t w[2048];
-    uint8_t sb[Cfg<D>::kSbBytes];
+    uint8_t aux[Cfg<D>::kAuxBytes];
     uint64_t full[Cfg<D>::kStages], phi_done[Cfg<D>::kStages], empty[Cfg<D>::kStages];
     uint64_t ostore[Cfg<D>::kStages];  // the O tile staged in slot s has been read by its TMA store
     uint64_t t_full, t_free, p_full, o_full, o_free, s_full, s_ready, agg_ready, drain;
@@ -86,6 +100,7 @@ struct alignas(1024) Smem {
     int ticket;
     int abort;
     int lb_base;  // look-back result
+    int last;     // this CTA finished last: it clears the flags for the next launch
 };
 
 static_assert(sizeof(Smem<128>) <= 232448, "exceeds the 227 KB per-CTA shared memory limit");
@@ -97,7 +112,7 @@ struct Params {
     float *agg;             // [BH, G, D*D + D] segment aggregates (same layout)
     uint32_t *incl_cnt;     // [BH, G] publish counters of incl
     uint32_t *agg_cnt;      // [BH, G] publish counters of agg
-    uint32_t *counter;      // work ticket
+    uint32_t *counter;      // work ticket; counter[1] counts finished CTAs
     int N, BH, G, L, n_chunks;
     float eps;
 };
@@ -109,6 +124,68 @@ __device__ __forceinline__ bool wait_bar(int *abort_flag, uint64_t *bar, uint32_
 __device__ __forceinline__ bool wait_bar_warp(int *abort_flag, uint64_t *bar, uint32_t parity)
 {
     return tc::wait_bar_warp(&g_tc_status, abort_flag, bar, parity);
+}
+
+// z_i as a bf16 high + low pair in columns 0 and 1 of row i of the z block.
+__device__ __forceinline__ void put_zb(uint8_t *zb, int i, float zv)
+{
+    const __nv_bfloat16 hi = __float2bfloat16_rn(zv);
+    const __nv_bfloat16 lo = __float2bfloat16_rn(zv - __bfloat162float(hi));
+    *reinterpret_cast<__nv_bfloat162 *>(zb + sw128_offset(i, 0)) = __halves2bfloat162(hi, lo);
+}
+template <int D>
+__device__ __forceinline__ void set_z(uint8_t *aux, int i, float zv)
+{
+    if constexpr (Cfg<D>::kFused)
+        put_zb(aux + Cfg<D>::kZb, i, zv);
+    else
+        put_z(aux + Cfg<D>::kW, i, zv);
+}
+
+// S += phi(K_c)^T [V_c | 1] (fused) or S += phi(K_c)^T V_c and z += phi(K_c)^T 1.
+// phi(K_c)^T is MN-major with its second dk block one box on (D = 64: the next
+// tile, whose rows 64..127 of the result are never read).
+template <int D>
+__device__ __forceinline__ void issue_state_update(uint32_t tmem, uint32_t ka, uint32_t va, uint32_t lbo_v,
+                                                   uint32_t w_addr, uint32_t id_KV, uint32_t id_KW, bool first)
+{
+#pragma unroll
+    for (int kk = 0; kk < kC / 16; ++kk) {
+        const uint32_t acc = (!first || kk > 0) ? 1u : 0u;
+        mma_ss(tmem + Cfg<D>::tS, mnmajor(ka, kk, kBox), mnmajor(va, kk, lbo_v), id_KV, acc);
+        if constexpr (!Cfg<D>::kFused)
+            mma_ss(tmem + Cfg<D>::tZ, mnmajor(ka, kk, kBox), wdesc(w_addr, kk), id_KW, acc);
+    }
+}
+
+// The bf16 copy of S (and z) for the next chunk, from S_acc, once s_full completes.
+template <int D>
+__device__ __forceinline__ bool refresh_state(Smem<D> &sm, int *abort_flag, uint32_t tl, int i, bool row_ok, int cj)
+{
+    using CF = Cfg<D>;
+    if (!wait_bar_warp(abort_flag, &sm.s_full, cj & 1)) return false;
+    tc_fence_after();
+#pragma unroll 1
+    for (int cc = 0; cc < D / 64; ++cc) {
+        uint32_t a[64];
+        tmem_ld32(tl + CF::tS + cc * 64, *reinterpret_cast<uint32_t(*)[32]>(&a[0]));
+        tmem_ld32(tl + CF::tS + cc * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&a[32]));
+        tmem_ld_wait();
+        if (row_ok) {
+            float x[32];
+            to_floats(&a[0], x);
+            put_sb<D>(sm.aux + CF::kSb, i, cc * 64, x);
+            to_floats(&a[32], x);
+            put_sb<D>(sm.aux + CF::kSb, i, cc * 64 + 32, x);
+        }
+    }
+    const float zv = __uint_as_float(tmem_ld1(tl + CF::tZ));
+    tmem_ld_wait();
+    if (row_ok) set_z<D>(sm.aux, i, zv);
+    fence_proxy_async_smem();
+    tc_fence_before();
+    mbar_arrive(&sm.s_ready);
+    return true;
 }
 
 template <int D>
@@ -126,11 +203,29 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
     }
     Smem<D> &sm = *reinterpret_cast<Smem<D> *>(smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    uint8_t *const sb = sm.aux + CF::kSb;
 
-    if (tid < 128) {  // W: row 0 ones, everything else zero (rows 1, 2 get z in phase B)
-        const int blk = tid >> 6, within = tid & 63;
-        const uint32_t val = (within < 8) ? 0x3F803F80u : 0u;  // first 128 bytes of a block = row 0
-        *reinterpret_cast<uint4 *>(sm.w + blk * 1024 + within * 16) = make_uint4(val, val, val, val);
+    // The work ticket is taken first, its latency hidden behind the set-up.  A CTA
+    // that waits on an earlier ticket waits on a running CTA: no other CTA of this
+    // library fits on an SM beside one of this kernel (shared memory), so the TMEM
+    // allocation below can only wait on other kernels' CTAs, which never wait on it.
+    int my_ticket = 0;
+    if (tid == 0) my_ticket = (int)atomicAdd(prm.counter, 1u);
+
+    if (tid < 128) {
+        if constexpr (CF::kFused) {
+            // ones block: row r holds 1 in column 0 (physical 16-byte chunk r % 8); z block zero
+            for (int c = tid; c < kC * 8; c += 128) {
+                const uint32_t x = (c & 7) == ((c >> 3) & 7) ? 0x3F80u : 0u;
+                *reinterpret_cast<uint4 *>(sm.aux + CF::kOnes + c * 16) = make_uint4(x, 0u, 0u, 0u);
+            }
+            for (int c = tid; c < D * 8; c += 128)
+                *reinterpret_cast<uint4 *>(sm.aux + CF::kZb + c * 16) = make_uint4(0u, 0u, 0u, 0u);
+        } else {  // W: row 0 ones, everything else zero (rows 1, 2 get z in phase B)
+            const int blk = tid >> 6, within = tid & 63;
+            const uint32_t val = (within < 8) ? 0x3F803F80u : 0u;  // first 128 bytes of a block = row 0
+            *reinterpret_cast<uint4 *>(sm.aux + CF::kW + blk * 1024 + within * 16) = make_uint4(val, val, val, val);
+        }
         fence_proxy_async_smem();
     }
     if (tid == 0) {
@@ -159,13 +254,10 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
         tmem_alloc(&sm.tmem_base, CF::kTmemCols);
         tmem_relinquish();
     }
+    if (tid == 0) sm.ticket = my_ticket;
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    // The ticket is taken only once this CTA holds its TMEM, so a CTA that waits
-    // on an earlier ticket waits on a CTA that is already running.
-    if (tid == 0) sm.ticket = (int)atomicAdd(prm.counter, 1u);
-    __syncthreads();
 
     const int ticket = sm.ticket;
     const int g = ticket / prm.BH, bh = ticket % prm.BH;
@@ -234,14 +326,18 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
     } else if (warp == kMmaWarp) {
         // ---------------------------------------------------------------- MMA issuer
         if (lane == 0) {
+            constexpr int NE = CF::kFused ? D + 16 : D;  // N of the MMAs against V or S
             const uint32_t id_T = idesc_bf16_f32(128, 128, false, false);   // phi(Q) phi(K)^T
-            const uint32_t id_PV = idesc_bf16_f32(128, D, false, true);     // P V (P in TMEM)
-            const uint32_t id_QS = idesc_bf16_f32(128, D, false, true);     // phi(Q) S_bf16
-            const uint32_t id_KV = idesc_bf16_f32(128, D, true, true);      // phi(K)^T V
+            const uint32_t id_PV = idesc_bf16_f32(128, NE, false, true);    // P [V | 1] (P in TMEM)
+            const uint32_t id_QS = idesc_bf16_f32(128, NE, false, true);    // phi(Q) [S_bf16 | z]
+            const uint32_t id_KV = idesc_bf16_f32(128, NE, true, true);     // phi(K)^T [V | 1]
             const uint32_t id_W = idesc_bf16_f32(128, 16, false, false);    // x W^T (A K-major or TMEM)
             const uint32_t id_KW = idesc_bf16_f32(128, 16, true, false);    // phi(K)^T W^T
-            const uint32_t lbo_kt = kBox;  // second dk block of phi(K)^T (D = 64: rows 64..127 unused)
-            const uint32_t w_addr = smem_u32(sm.w), sb_addr = smem_u32(sm.sb);
+            const uint32_t aux = smem_u32(sm.aux);
+            const uint32_t w_addr = aux + CF::kW, sb_addr = aux + CF::kSb, ones_addr = aux + CF::kOnes;
+            // Second 64-wide block of the B operands: the z block after the S copy
+            // (fused) or the S copy's own second block (D = 128).
+            const uint32_t lbo_sb = CF::kFused ? CF::kZb - CF::kSb : D * 128;
             bool ok = true;
             // phase A: aggregate state of the segment
             for (int ja = 0; ja < nA && ok; ++ja) {
@@ -249,12 +345,8 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
                 if (!(ok = wait_bar(abort_flag, &sm.phi_done[s], r & 1))) break;
                 tc_fence_after();
                 const uint32_t ka = smem_u32(sm.k[s]), va = smem_u32(sm.v[s]);
-#pragma unroll
-                for (int kk = 0; kk < kC / 16; ++kk) {
-                    const uint32_t acc = (ja > 0 || kk > 0) ? 1u : 0u;
-                    mma_ss(tmem + CF::tS, mnmajor(ka, kk, lbo_kt), mnmajor(va, kk, kBox), id_KV, acc);
-                    mma_ss(tmem + CF::tZ, mnmajor(ka, kk, lbo_kt), wdesc(w_addr, kk), id_KW, acc);
-                }
+                const uint32_t lbo_v = CF::kFused ? ones_addr - va : kBox;  // [V | 1] or V's second box
+                issue_state_update<D>(tmem, ka, va, lbo_v, w_addr, id_KV, id_KW, ja == 0);
                 mma_commit(&sm.empty[s]);
             }
             if (ok && nA > 0) mma_commit(&sm.agg_ready);
@@ -266,6 +358,7 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
                 if (cj > 0 && !(ok = wait_bar(abort_flag, &sm.t_free, (cj - 1) & 1))) break;
                 tc_fence_after();
                 const uint32_t qa = smem_u32(sm.q[s]), ka = smem_u32(sm.k[s]), va = smem_u32(sm.v[s]);
+                const uint32_t lbo_v = CF::kFused ? ones_addr - va : kBox;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
                     mma_ss(tmem + CF::tT, kmajor(qa, kk), kmajor(ka, kk), id_T, kk > 0 ? 1u : 0u);
@@ -275,23 +368,30 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    mma_ss(tmem + CF::tO, kmajor(qa, kk), mnmajor(sb_addr, kk, D * 128), id_QS, kk > 0 ? 1u : 0u);
-                    mma_ss(tmem + CF::tQZ, kmajor(qa, kk), wdesc(w_addr, kk), id_W, kk > 0 ? 1u : 0u);
+                    mma_ss(tmem + CF::tO, kmajor(qa, kk), mnmajor(sb_addr, kk, lbo_sb), id_QS, kk > 0 ? 1u : 0u);
+                    if constexpr (!CF::kFused)
+                        mma_ss(tmem + CF::tQZ, kmajor(qa, kk), wdesc(w_addr, kk), id_W, kk > 0 ? 1u : 0u);
+                }
+                // Fused layout (4 stages): the state update reads phi(K), V and S_acc, whose
+                // bf16 copy for this chunk is in place, so it runs while T becomes P (its
+                // commit also covers the MMAs above that read the S copy and z).  D = 128
+                // (2 stages): P V first, so that O -- whose store frees the stage -- is
+                // out sooner.
+                if (CF::kFused && cj < nch - 1) {
+                    issue_state_update<D>(tmem, ka, va, lbo_v, w_addr, id_KV, id_KW, false);
+                    mma_commit(&sm.s_full);
                 }
                 if (!(ok = wait_bar(abort_flag, &sm.p_full, cj & 1))) break;
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < kC / 16; ++kk) {
-                    mma_ts(tmem + CF::tO, tmem + CF::tP + kk * 8, mnmajor(va, kk, kBox), id_PV, 1u);
-                    mma_ts(tmem + CF::tRS, tmem + CF::tP + kk * 8, wdesc(w_addr, kk), id_W, kk > 0 ? 1u : 0u);
+                    mma_ts(tmem + CF::tO, tmem + CF::tP + kk * 8, mnmajor(va, kk, lbo_v), id_PV, 1u);
+                    if constexpr (!CF::kFused)
+                        mma_ts(tmem + CF::tRS, tmem + CF::tP + kk * 8, wdesc(w_addr, kk), id_W, kk > 0 ? 1u : 0u);
                 }
                 mma_commit(&sm.o_full);
-                if (cj < nch - 1) {
-#pragma unroll
-                    for (int kk = 0; kk < kC / 16; ++kk) {
-                        mma_ss(tmem + CF::tS, mnmajor(ka, kk, lbo_kt), mnmajor(va, kk, kBox), id_KV, 1u);
-                        mma_ss(tmem + CF::tZ, mnmajor(ka, kk, lbo_kt), wdesc(w_addr, kk), id_KW, 1u);
-                    }
+                if (!CF::kFused && cj < nch - 1) {
+                    issue_state_update<D>(tmem, ka, va, lbo_v, w_addr, id_KV, id_KW, false);
                     mma_commit(&sm.s_full);
                 }
                 mma_commit(&sm.empty[s]);
@@ -440,7 +540,7 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
             }
             tmem_st16(tl + CF::tS + col0 + cc, *reinterpret_cast<const uint32_t(*)[16]>(&acc[0]));
             tmem_st16(tl + CF::tS + col0 + cc + 16, *reinterpret_cast<const uint32_t(*)[16]>(&acc[16]));
-            if (row_ok) put_sb<D>(sm.sb, i, col0 + cc, acc);
+            if (row_ok) put_sb<D>(sb, i, col0 + cc, acc);
         }
         if (!is_o) {  // z, by the warps of the first column half
             float zacc = 0.f;
@@ -458,7 +558,7 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
                 if (row_ok) incl_out[(size_t)D * D + i] = zacc + za;
             }
             tmem_st1(tl + CF::tZ, __float_as_uint(zacc));
-            if (row_ok) put_z(sm.w, i, zacc);
+            if (row_ok) set_z<D>(sm.aux, i, zacc);
         }
         tmem_st_wait();
         fence_proxy_async_smem();
@@ -515,19 +615,32 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
                 mbar_arrive(&sm.p_full);
             }
         } else {
-            // ------------------------------------------------------------ O out, state refresh
-            // O is staged (bf16, 128-byte swizzled boxes) in the Q buffer of its own
-            // slot -- Q is no longer read once O is final -- and written by a TMA
-            // store, which clips rows past the end of the sequence.
+            // ------------------------------------------------------------ state refresh, O out
+            // The bf16 copy of the next chunk's state gates that chunk's MMAs: with
+            // the fused layout it is made first (its s_full comes before o_full);
+            // with D = 128 after O, whose store frees the stage.  O is staged (bf16,
+            // 128-byte swizzled boxes) in the Q buffer of its own slot -- Q is no
+            // longer read once O is final -- and written by a TMA store, which clips
+            // rows past the end of the sequence.
             const bool leader = (warp == kEpiOWarp0 && lane == 0);
             for (int cj = 0; cj < nch; ++cj) {
                 const int s = (nA + cj) % S;
+                if (CF::kFused && cj < nch - 1 && !refresh_state<D>(sm, abort_flag, tl, i, row_ok, cj)) break;
                 if (!wait_bar_warp(abort_flag, &sm.o_full, cj & 1)) break;
                 tc_fence_after();
-                uint32_t dn[32];
-                tmem_ld32(tl + CF::tRS, dn);  // columns: rs[0..15], qz[0..15]
-                tmem_ld_wait();
-                const float den = __uint_as_float(dn[0]) + __uint_as_float(dn[17]) + __uint_as_float(dn[18]);
+                float den;
+                {
+                    uint32_t dn[32];
+                    if constexpr (CF::kFused) {
+                        tmem_ld32(tl + CF::tO + D, dn);  // column D: rs + phi(q) z_hi; D + 1: phi(q) z_lo
+                        tmem_ld_wait();
+                        den = __uint_as_float(dn[0]) + __uint_as_float(dn[1]);
+                    } else {
+                        tmem_ld32(tl + CF::tRS, dn);  // columns: rs[0..15], qz[0..15]
+                        tmem_ld_wait();
+                        den = __uint_as_float(dn[0]) + __uint_as_float(dn[17]) + __uint_as_float(dn[18]);
+                    }
+                }
                 const float inv = 1.f / fmaxf(den, prm.eps);
 #pragma unroll 1
                 for (int cc = 0; cc < D / 64; ++cc) {
@@ -557,30 +670,7 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
                         tma_store_3d(&map_o, sm.q[s] + cc * kBox, 64 * cc, (c0 + cj) * kC, bh);
                     tma_store_commit();
                 }
-                if (cj < nch - 1) {
-                    if (!wait_bar_warp(abort_flag, &sm.s_full, cj & 1)) break;
-                    tc_fence_after();
-#pragma unroll 1
-                    for (int cc = 0; cc < D / 64; ++cc) {
-                        uint32_t a[64];
-                        tmem_ld32(tl + CF::tS + cc * 64, *reinterpret_cast<uint32_t(*)[32]>(&a[0]));
-                        tmem_ld32(tl + CF::tS + cc * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&a[32]));
-                        tmem_ld_wait();
-                        if (row_ok) {
-                            float x[32];
-                            to_floats(&a[0], x);
-                            put_sb<D>(sm.sb, i, cc * 64, x);
-                            to_floats(&a[32], x);
-                            put_sb<D>(sm.sb, i, cc * 64 + 32, x);
-                        }
-                    }
-                    const float zv = __uint_as_float(tmem_ld1(tl + CF::tZ));
-                    tmem_ld_wait();
-                    if (row_ok) put_z(sm.w, i, zv);
-                    fence_proxy_async_smem();
-                    tc_fence_before();
-                    mbar_arrive(&sm.s_ready);
-                }
+                if (!CF::kFused && cj < nch - 1 && !refresh_state<D>(sm, abort_flag, tl, i, row_ok, cj)) break;
                 if (leader) {  // slot s may be refilled once the store has read the staged O
                     tma_store_wait_read_all();
                     mbar_arrive(&sm.ostore[s]);
@@ -591,9 +681,22 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
     }
 
     tc_fence_before();
+    __threadfence();  // this CTA's flag traffic is done before it counts itself finished
     __syncthreads();
     tc_fence_after();
     if (warp == kMmaWarp) tmem_dealloc(tmem, CF::kTmemCols);
+    // The last CTA to finish leaves the ticket, the counter and every publish flag
+    // of this launch at zero, ready for the next launch on the same flags.
+    if (tid == 0) sm.last = atom_add_acq_rel_gpu(prm.counter + 1, 1u) == gridDim.x - 1;
+    __syncthreads();
+    if (sm.last) {
+        const int n = 2 * prm.BH * prm.G;  // incl_cnt then agg_cnt
+        for (int x = tid; x < n; x += kThreads) prm.incl_cnt[x] = 0u;
+        if (tid == 0) {
+            prm.counter[0] = 0u;
+            prm.counter[1] = 0u;
+        }
+    }
 }
 
 // ------------------------------------------------------------------ host side
@@ -617,20 +720,31 @@ la_status launch(const Problem &p)
     const size_t flag_bytes = ((items * 8 + 16) + 255) / 256 * 256;
     const size_t state_bytes = G > 1 ? 2 * items * ((size_t)D * D + D) * 4 : 0;
 
+    // Flags from the stream's workspace (already zero) when it can hold them, else
+    // from per-call scratch cleared by a memset.
+    void *ws = nullptr;
+    st = flag_workspace(p.stream, flag_bytes, &ws);
+    if (st != LA_OK && st != LA_ERR_UNSUPPORTED) return st;
+    const size_t own_flags = ws ? 0 : flag_bytes;
     Scratch scratch;
-    st = scratch.alloc(flag_bytes + state_bytes, p.stream);
-    if (st != LA_OK) return st;
+    if (own_flags + state_bytes > 0) {
+        st = scratch.alloc(own_flags + state_bytes, p.stream);
+        if (st != LA_OK) return st;
+    }
     uint8_t *base = (uint8_t *)scratch.ptr;
-    cudaError_t e = cudaMemsetAsync(base, 0, flag_bytes, p.stream);
-    count_launches();
-    if (e != cudaSuccess) return cuda_status(e);
+    uint8_t *flags = ws ? (uint8_t *)ws : base;
+    if (!ws) {
+        cudaError_t e = cudaMemsetAsync(flags, 0, flag_bytes, p.stream);
+        count_launches();
+        if (e != cudaSuccess) return cuda_status(e);
+    }
 
     Params prm;
     prm.o = (uint16_t *)p.o;
-    prm.counter = (uint32_t *)base;
-    prm.incl_cnt = (uint32_t *)(base + 16);
+    prm.counter = (uint32_t *)flags;
+    prm.incl_cnt = (uint32_t *)(flags + 16);
     prm.agg_cnt = prm.incl_cnt + items;
-    prm.incl = (float *)(base + flag_bytes);
+    prm.incl = (float *)(base + own_flags);
     prm.agg = prm.incl + (G > 1 ? items * ((size_t)D * D + D) : 0);
     prm.N = p.N;
     prm.BH = p.BH;

@@ -86,7 +86,8 @@ struct alignas(1024) Smem {
     Item items[kRing];
     uint32_t tmem_base;
     int abort;
-    int last;  // the epilogue's CTA completed the last split of its head
+    int last;      // the epilogue's CTA completed the last split of its head
+    int last_cta;  // this CTA finished last: it clears the flags for the next launch
 };
 
 static_assert(sizeof(Smem<128>) <= 232448, "exceeds the 227 KB per-CTA shared memory limit");
@@ -95,7 +96,7 @@ static_assert(sizeof(Smem<64>) <= 232448, "exceeds the 227 KB per-CTA shared mem
 struct Params {
     float *part;         // [BH, P, D*D + D] split partials (S then z; thread-major, see add_state)
     uint8_t *img;        // [BH, kImgBytes] state images
-    uint32_t *ticket;    // work ticket
+    uint32_t *ticket;    // work ticket; ticket[1] counts finished CTAs
     uint32_t *arrived;   // [BH] completed splits per head
     uint32_t *ready;     // [BH] 1 once the head's state image is written
     int N, BH, n_chunks;
@@ -546,9 +547,21 @@ noncausal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
     }
 
     tc_fence_before();
+    __threadfence();  // this CTA's flag traffic is done before it counts itself finished
     __syncthreads();
     tc_fence_after();
     if (warp == kMmaWarp) tmem_dealloc(tmem, 512);
+    // The last CTA to finish leaves the ticket, the counter and the per-head flags
+    // at zero, ready for the next launch on the same flags.
+    if (tid == 0) sm.last_cta = atom_add_acq_rel_gpu(prm.ticket + 1, 1u) == gridDim.x - 1;
+    __syncthreads();
+    if (sm.last_cta) {
+        for (int x = tid; x < 2 * prm.BH; x += kThreads) prm.arrived[x] = 0u;  // arrived then ready
+        if (tid == 0) {
+            prm.ticket[0] = 0u;
+            prm.ticket[1] = 0u;
+        }
+    }
 }
 
 // ------------------------------------------------------------------ host side
@@ -581,20 +594,29 @@ la_status launch(const Problem &p)
     const size_t part_bytes = ((size_t)p.BH * P * seg * 4 + 255) / 256 * 256;
     const size_t img_bytes = (size_t)p.BH * CF::kImgBytes;
 
+    // Flags from the stream's workspace (already zero) when it can hold them, else
+    // from per-call scratch cleared by a memset.
+    void *ws = nullptr;
+    st = flag_workspace(p.stream, flag_bytes, &ws);
+    if (st != LA_OK && st != LA_ERR_UNSUPPORTED) return st;
+    const size_t own_flags = ws ? 0 : flag_bytes;
     Scratch scratch;
-    st = scratch.alloc(flag_bytes + part_bytes + img_bytes, p.stream);
+    st = scratch.alloc(own_flags + part_bytes + img_bytes, p.stream);
     if (st != LA_OK) return st;
     uint8_t *base = (uint8_t *)scratch.ptr;
-    cudaError_t e = cudaMemsetAsync(base, 0, flag_bytes, p.stream);
-    count_launches();
-    if (e != cudaSuccess) return cuda_status(e);
+    uint8_t *flags = ws ? (uint8_t *)ws : base;
+    if (!ws) {
+        cudaError_t e = cudaMemsetAsync(flags, 0, flag_bytes, p.stream);
+        count_launches();
+        if (e != cudaSuccess) return cuda_status(e);
+    }
 
     Params prm;
-    prm.ticket = (uint32_t *)base;
-    prm.arrived = (uint32_t *)(base + 16);
+    prm.ticket = (uint32_t *)flags;
+    prm.arrived = (uint32_t *)(flags + 16);
     prm.ready = prm.arrived + p.BH;
-    prm.part = (float *)(base + flag_bytes);
-    prm.img = base + flag_bytes + part_bytes;
+    prm.part = (float *)(base + own_flags);
+    prm.img = base + own_flags + part_bytes;
     prm.N = p.N;
     prm.BH = p.BH;
     prm.n_chunks = n_chunks;

@@ -313,3 +313,57 @@ def test_unsupported_shape_raises():
     with pytest.raises(la().LAError) as ei:
         la().la_forward_causal(q, q, q, chunk=128)
     assert ei.value.status == 2
+
+
+# ------------------------------------------------------------------ flag workspace
+def test_flag_workspace_reused_across_shapes_and_paths(orc):
+    """Both ticketed kernels take their tickets and publish flags from one
+    workspace per stream, which every launch leaves cleared for the next: calls
+    of different shapes and paths in a row all match the oracle, twice over."""
+    cases = [("causal", 2, 3, 1000, 64), ("noncausal", 4, 40, 4173, 64), ("causal", 1, 4, 8192, 128),
+             ("noncausal", 1, 1, 128, 128), ("causal", 3, 5, 300, 64), ("noncausal", 2, 3, 9000, 128)]
+    refs = {}
+    for rep in range(2):
+        for kind, B, H, N, d in cases:
+            q, k, v = workloads.random_inputs(9000 + N + d, B, H, N, d, d, "bf16")
+            key = (kind, B, H, N, d)
+            if key not in refs:
+                refs[key] = orc.causal_recurrent(q, k, v) if kind == "causal" else orc.noncausal(q, k, v)
+            got = run_causal(q, k, v, "bf16", 128) if kind == "causal" else run_noncausal(q, k, v, "bf16")
+            assert_parity(got, refs[key], "bf16", (rep,) + key)
+
+
+@pytest.mark.parametrize("warm", [False, True])
+def test_ticketed_kernels_under_graph_capture(orc, warm):
+    """Captured and replayed calls on a fresh stream.  warm: the stream's flag
+    workspace exists before capture (the graph reuses it, and each launch clears
+    it for the next); cold: capture falls back to per-call flags and a memset."""
+    q, k, v = workloads.random_inputs(4242, 2, 4, 1500, 64, 64, "bf16")
+    qn, kn, vn = workloads.random_inputs(4343, 3, 4, 2048, 64, 64, "bf16")
+    ref_c, ref_n = orc.causal_recurrent(q, k, v), orc.noncausal(qn, kn, vn)
+    dev = [to_dev(x, "bf16") for x in (q, k, v, qn, kn, vn)]
+    s = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    if warm:
+        with torch.cuda.stream(s):
+            la().la_forward_causal(dev[0], dev[1], dev[2])
+        torch.cuda.synchronize()
+    outs_c = [torch.empty_like(dev[2]) for _ in range(2)]
+    outs_n = [torch.empty_like(dev[5]) for _ in range(2)]
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for oc, on in zip(outs_c, outs_n):
+            la().la_forward_causal(dev[0], dev[1], dev[2], oc)
+            la().la_forward_noncausal(dev[3], dev[4], dev[5], on)
+    for rep in range(2):
+        for x in outs_c + outs_n:
+            x.fill_(float("nan"))
+        torch.cuda.synchronize()
+        with torch.cuda.stream(s):
+            g.replay()
+        torch.cuda.synchronize()
+        assert la().la_get_device_status() == 0
+        for x in outs_c:
+            assert_parity(from_dev(x), ref_c, "bf16", ("graph causal", warm, rep))
+        for x in outs_n:
+            assert_noncausal_parity(from_dev(x), ref_n, "bf16", ("graph noncausal", warm, rep))
