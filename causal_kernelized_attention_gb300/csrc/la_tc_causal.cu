@@ -77,12 +77,17 @@ struct Cfg {
     static constexpr uint32_t kSb = kFused ? kC * 128 : 2048;
     static constexpr uint32_t kZb = kSb + kSbBytes;
     static constexpr uint32_t kAuxBytes = kFused ? kZb + D * 128 : kSb + kSbBytes;
-    // TMEM columns (fused: O and S are D + 16 wide, z in column D of S)
-    static constexpr uint32_t tT = 0, tP = 128, tRS = 192, tQZ = 208, tO = 256;
+    // TMEM columns.  Fused: O (two buffers, kOStride apart) and S are D + 16 wide,
+    // z in column D of S.  Separate: one O buffer, row sums and phi(q) z in their
+    // own 16-column groups, z at tZ.
+    static constexpr uint32_t tT = 0, tP = 128, tRS = 192, tQZ = 208;
+    static constexpr uint32_t tO = kFused ? 192 : 256, kOStride = kFused ? 96 : 0;
     static constexpr uint32_t tS = kFused ? 384 : 256 + D;
     static constexpr uint32_t tZ = kFused ? tS + D : 224;
     static constexpr uint32_t kTmemCols = 512;
-    static_assert(tP + 64 <= tRS && tRS + 16 <= tQZ && tQZ + 16 <= tO && tS + (kFused ? D + 16 : D) <= kTmemCols,
+    static_assert(kFused ? (tP + 64 <= tO && tO + kOStride + D + 16 <= tS && tS + D + 16 <= kTmemCols)
+                         : (tP + 64 <= tRS && tRS + 16 <= tQZ && tQZ + 16 <= tO && tO + D <= tS &&
+                            tS + D <= kTmemCols),
                   "TMEM column groups overlap");
 };
 
@@ -94,8 +99,9 @@ struct alignas(1024) Smem {
     uint8_t aux[Cfg<D>::kAuxBytes];
     uint64_t full[Cfg<D>::kStages], phi_done[Cfg<D>::kStages], empty[Cfg<D>::kStages];
     uint64_t ostore[Cfg<D>::kStages];  // the O tile staged in slot s has been read by its TMA store
-    uint64_t t_full, t_free, p_full, o_full, o_free, s_full, s_ready, agg_ready, drain;
-    uint64_t o_staged;  // all 128 rows of the current O tile are staged in shared memory
+    uint64_t t_full, t_free, p_full, s_full, s_ready, agg_ready, drain;
+    uint64_t o_full[2], o_free[2];  // per O buffer (the separate layout uses buffer 0)
+    uint64_t o_staged[2];           // all 128 rows of the buffer's O tile are staged in shared memory
     uint32_t tmem_base;
     int ticket;
     int abort;
@@ -188,6 +194,16 @@ __device__ __forceinline__ bool refresh_state(Smem<D> &sm, int *abort_flag, uint
     return true;
 }
 
+// add_state, plus z_i of the same state (issued with it) when want_z.
+template <int D>
+__device__ __forceinline__ void add_state_z(float (&acc)[32], float &zacc, const float *state, int cg0, int i,
+                                            bool want_z)
+{
+    const float zv = want_z ? __ldcg(state + (size_t)D * D + i) : 0.f;
+    add_state<D>(acc, state, cg0, i);
+    zacc += zv;
+}
+
 template <int D>
 __global__ void __launch_bounds__(576, 1)
 causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
@@ -240,13 +256,15 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
         mbar_init(&sm.t_full, 1);
         mbar_init(&sm.t_free, 128);
         mbar_init(&sm.p_full, 128);
-        mbar_init(&sm.o_full, 1);
-        mbar_init(&sm.o_free, 128);
+        for (int ob = 0; ob < 2; ++ob) {
+            mbar_init(&sm.o_full[ob], 1);
+            mbar_init(&sm.o_free[ob], 128);
+            mbar_init(&sm.o_staged[ob], 128);
+        }
         mbar_init(&sm.s_full, 1);
         mbar_init(&sm.s_ready, 128);
         mbar_init(&sm.agg_ready, 1);
         mbar_init(&sm.drain, 1);
-        mbar_init(&sm.o_staged, 128);
         sm.abort = 0;
         fence_mbar_init();
     }
@@ -351,50 +369,94 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
             }
             if (ok && nA > 0) mma_commit(&sm.agg_ready);
             // phase C: outputs
-            for (int cj = 0; cj < nch && ok; ++cj) {
-                const int j = nA + cj, s = j % S, r = j / S;
-                if (!(ok = wait_bar(abort_flag, &sm.phi_done[s], r & 1))) break;
-                tc_fence_after();
-                if (cj > 0 && !(ok = wait_bar(abort_flag, &sm.t_free, (cj - 1) & 1))) break;
-                tc_fence_after();
-                const uint32_t qa = smem_u32(sm.q[s]), ka = smem_u32(sm.k[s]), va = smem_u32(sm.v[s]);
-                const uint32_t lbo_v = CF::kFused ? ones_addr - va : kBox;
+            if constexpr (CF::kFused) {
+                // Software-pipelined over chunks: P V of chunk c (its within-chunk term,
+                // into O buffer c % 2), then T of chunk c + 1 -- so that P(c+1) is formed
+                // while the rest of chunk c runs -- then phi(Q_c)[S | z], completing O(c),
+                // then the state update.  The state update's commit also covers the MMAs
+                // that read the S copy and z, which the refresh overwrites next.
+                if (nch > 0) {
+                    const int s0 = nA % S;
+                    if ((ok = wait_bar(abort_flag, &sm.phi_done[s0], (nA / S) & 1))) {
+                        tc_fence_after();
+                        const uint32_t qa = smem_u32(sm.q[s0]), ka = smem_u32(sm.k[s0]);
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk)
-                    mma_ss(tmem + CF::tT, kmajor(qa, kk), kmajor(ka, kk), id_T, kk > 0 ? 1u : 0u);
-                mma_commit(&sm.t_full);
-                if (cj > 0 && !(ok = wait_bar(abort_flag, &sm.o_free, (cj - 1) & 1))) break;
-                if (!(ok = wait_bar(abort_flag, &sm.s_ready, cj & 1))) break;
-                tc_fence_after();
+                        for (int kk = 0; kk < D / 16; ++kk)
+                            mma_ss(tmem + CF::tT, kmajor(qa, kk), kmajor(ka, kk), id_T, kk > 0 ? 1u : 0u);
+                        mma_commit(&sm.t_full);
+                    }
+                }
+                for (int cj = 0; cj < nch && ok; ++cj) {
+                    const int j = nA + cj, s = j % S, ob = cj & 1;
+                    const uint32_t dO = tmem + CF::tO + ob * CF::kOStride;
+                    const uint32_t qa = smem_u32(sm.q[s]), ka = smem_u32(sm.k[s]), va = smem_u32(sm.v[s]);
+                    const uint32_t lbo_v = ones_addr - va;
+                    if (cj >= 2 && !(ok = wait_bar(abort_flag, &sm.o_free[ob], ((cj >> 1) - 1) & 1))) break;
+                    if (!(ok = wait_bar(abort_flag, &sm.p_full, cj & 1))) break;
+                    tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    mma_ss(tmem + CF::tO, kmajor(qa, kk), mnmajor(sb_addr, kk, lbo_sb), id_QS, kk > 0 ? 1u : 0u);
-                    if constexpr (!CF::kFused)
+                    for (int kk = 0; kk < kC / 16; ++kk)
+                        mma_ts(dO, tmem + CF::tP + kk * 8, mnmajor(va, kk, lbo_v), id_PV, kk > 0 ? 1u : 0u);
+                    if (cj + 1 < nch) {
+                        const int s1 = (j + 1) % S;
+                        if (!(ok = wait_bar(abort_flag, &sm.phi_done[s1], ((j + 1) / S) & 1))) break;
+                        if (!(ok = wait_bar(abort_flag, &sm.t_free, cj & 1))) break;
+                        tc_fence_after();
+                        const uint32_t qa1 = smem_u32(sm.q[s1]), ka1 = smem_u32(sm.k[s1]);
+#pragma unroll
+                        for (int kk = 0; kk < D / 16; ++kk)
+                            mma_ss(tmem + CF::tT, kmajor(qa1, kk), kmajor(ka1, kk), id_T, kk > 0 ? 1u : 0u);
+                        mma_commit(&sm.t_full);
+                    }
+                    if (!(ok = wait_bar(abort_flag, &sm.s_ready, cj & 1))) break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk)
+                        mma_ss(dO, kmajor(qa, kk), mnmajor(sb_addr, kk, lbo_sb), id_QS, 1u);
+                    mma_commit(&sm.o_full[ob]);
+                    if (cj < nch - 1) {
+                        issue_state_update<D>(tmem, ka, va, lbo_v, w_addr, id_KV, id_KW, false);
+                        mma_commit(&sm.s_full);
+                    }
+                    mma_commit(&sm.empty[s]);
+                }
+            } else {
+                // D = 128: per chunk T, phi(Q) S and its z term, P V and the row sums, then
+                // the state update -- O first, since its store frees the stage.
+                for (int cj = 0; cj < nch && ok; ++cj) {
+                    const int j = nA + cj, s = j % S, r = j / S;
+                    if (!(ok = wait_bar(abort_flag, &sm.phi_done[s], r & 1))) break;
+                    tc_fence_after();
+                    if (cj > 0 && !(ok = wait_bar(abort_flag, &sm.t_free, (cj - 1) & 1))) break;
+                    tc_fence_after();
+                    const uint32_t qa = smem_u32(sm.q[s]), ka = smem_u32(sm.k[s]), va = smem_u32(sm.v[s]);
+                    const uint32_t lbo_v = kBox;
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk)
+                        mma_ss(tmem + CF::tT, kmajor(qa, kk), kmajor(ka, kk), id_T, kk > 0 ? 1u : 0u);
+                    mma_commit(&sm.t_full);
+                    if (cj > 0 && !(ok = wait_bar(abort_flag, &sm.o_free[0], (cj - 1) & 1))) break;
+                    if (!(ok = wait_bar(abort_flag, &sm.s_ready, cj & 1))) break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        mma_ss(tmem + CF::tO, kmajor(qa, kk), mnmajor(sb_addr, kk, lbo_sb), id_QS, kk > 0 ? 1u : 0u);
                         mma_ss(tmem + CF::tQZ, kmajor(qa, kk), wdesc(w_addr, kk), id_W, kk > 0 ? 1u : 0u);
-                }
-                // Fused layout (4 stages): the state update reads phi(K), V and S_acc, whose
-                // bf16 copy for this chunk is in place, so it runs while T becomes P (its
-                // commit also covers the MMAs above that read the S copy and z).  D = 128
-                // (2 stages): P V first, so that O -- whose store frees the stage -- is
-                // out sooner.
-                if (CF::kFused && cj < nch - 1) {
-                    issue_state_update<D>(tmem, ka, va, lbo_v, w_addr, id_KV, id_KW, false);
-                    mma_commit(&sm.s_full);
-                }
-                if (!(ok = wait_bar(abort_flag, &sm.p_full, cj & 1))) break;
-                tc_fence_after();
+                    }
+                    if (!(ok = wait_bar(abort_flag, &sm.p_full, cj & 1))) break;
+                    tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < kC / 16; ++kk) {
-                    mma_ts(tmem + CF::tO, tmem + CF::tP + kk * 8, mnmajor(va, kk, lbo_v), id_PV, 1u);
-                    if constexpr (!CF::kFused)
+                    for (int kk = 0; kk < kC / 16; ++kk) {
+                        mma_ts(tmem + CF::tO, tmem + CF::tP + kk * 8, mnmajor(va, kk, lbo_v), id_PV, 1u);
                         mma_ts(tmem + CF::tRS, tmem + CF::tP + kk * 8, wdesc(w_addr, kk), id_W, kk > 0 ? 1u : 0u);
+                    }
+                    mma_commit(&sm.o_full[0]);
+                    if (cj < nch - 1) {
+                        issue_state_update<D>(tmem, ka, va, lbo_v, w_addr, id_KV, id_KW, false);
+                        mma_commit(&sm.s_full);
+                    }
+                    mma_commit(&sm.empty[s]);
                 }
-                mma_commit(&sm.o_full);
-                if (!CF::kFused && cj < nch - 1) {
-                    issue_state_update<D>(tmem, ka, va, lbo_v, w_addr, id_KV, id_KW, false);
-                    mma_commit(&sm.s_full);
-                }
-                mma_commit(&sm.empty[s]);
             }
             // all issued MMAs complete before TMEM is freed
             mma_commit(&sm.drain);
@@ -412,10 +474,10 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
 
         // ---- phase B: exclusive prefix of this segment by decoupled look-back.
         // A segment with a successor publishes its aggregate as soon as phase A
-        // is done (segment 0 publishes its inclusive prefix directly), and its
-        // inclusive prefix after this CTA has set up its own running state.  A
-        // CTA sums the aggregates of its predecessors back to the nearest
-        // published inclusive prefix.  Each thread owns state row i and the
+        // is done -- segment 0's aggregate is its inclusive prefix and is published
+        // as such -- and its inclusive prefix after this CTA has set up its own
+        // running state.  A CTA sums the aggregates of its predecessors back to the
+        // nearest published inclusive prefix.  Each thread owns state row i and the
         // columns [col0, col0 + D/2).
         // Phase A: the epilogue warps are otherwise idle, so they apply phi to the
         // second half of each K tile (units 256..511).
@@ -434,8 +496,8 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
         bool have_agg = false;
         if (nA > 0) have_agg = wait_bar_warp(abort_flag, &sm.agg_ready, 0);
         tc_fence_after();
-        if (has_next && g > 0) {
-            float *dst = prm.agg + my * seg_floats;
+        if (has_next) {
+            float *dst = (g == 0 ? prm.incl : prm.agg) + my * seg_floats;
             if (have_agg) {
 #pragma unroll 1
                 for (int cc = 0; cc < kHalf; cc += 32) {
@@ -459,7 +521,7 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
                 }
             }
             __syncwarp();
-            if (lane == 0) red_release_add_gpu(prm.agg_cnt + my, have_agg ? 1u : kPoison);
+            if (lane == 0) red_release_add_gpu((g == 0 ? prm.incl_cnt : prm.agg_cnt) + my, have_agg ? 1u : kPoison);
         }
         if (gtid < 32) {
             // One warp reads the counters of up to 32 predecessors per round.
@@ -503,23 +565,25 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
         named_bar_sync(1, 256);
         const int base = sm.lb_base;
         const bool use_prev = g > 0 && !aborted(abort_flag);
-        float *incl_out = has_next ? prm.incl + my * seg_floats : nullptr;
+        float *incl_out = (has_next && g > 0) ? prm.incl + my * seg_floats : nullptr;
+        float zacc = 0.f;  // z prefix, summed by the warps of the first column half with their first block
 #pragma unroll 1
         for (int cc = 0; cc < kHalf; cc += 32) {
             float acc[32];
 #pragma unroll
             for (int e = 0; e < 32; ++e) acc[e] = 0.f;
             const int cg0 = (col0 + cc) >> 2;
+            const bool want_z = !is_o && cc == 0;
             if (use_prev && row_ok) {
-                if (base >= 0) add_state<D>(acc, prm.incl + (head0 + base) * seg_floats, cg0, i);
+                if (base >= 0) add_state_z<D>(acc, zacc, prm.incl + (head0 + base) * seg_floats, cg0, i, want_z);
                 int j = base + 1;
                 for (; j + 1 < g; j += 2) {  // two states per round trip
-                    add_state<D>(acc, prm.agg + (head0 + j) * seg_floats, cg0, i);
-                    add_state<D>(acc, prm.agg + (head0 + j + 1) * seg_floats, cg0, i);
+                    add_state_z<D>(acc, zacc, prm.agg + (head0 + j) * seg_floats, cg0, i, want_z);
+                    add_state_z<D>(acc, zacc, prm.agg + (head0 + j + 1) * seg_floats, cg0, i, want_z);
                 }
-                if (j < g) add_state<D>(acc, prm.agg + (head0 + j) * seg_floats, cg0, i);
+                if (j < g) add_state_z<D>(acc, zacc, prm.agg + (head0 + j) * seg_floats, cg0, i, want_z);
             }
-            if (has_next) {
+            if (incl_out) {
                 uint32_t a[32];
                 if (have_agg) {
                     tmem_ld32(tl + CF::tS + col0 + cc, a);
@@ -543,13 +607,7 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
             if (row_ok) put_sb<D>(sb, i, col0 + cc, acc);
         }
         if (!is_o) {  // z, by the warps of the first column half
-            float zacc = 0.f;
-            if (use_prev && row_ok) {
-                const size_t off = (size_t)D * D + i;
-                if (base >= 0) zacc += __ldcg(prm.incl + (head0 + base) * seg_floats + off);
-                for (int j = base + 1; j < g; ++j) zacc += __ldcg(prm.agg + (head0 + j) * seg_floats + off);
-            }
-            if (has_next) {
+            if (incl_out) {
                 float za = 0.f;
                 if (have_agg) {
                     za = __uint_as_float(tmem_ld1(tl + CF::tZ));
@@ -565,7 +623,7 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
         named_bar_sync(1, 256);
         tc_fence_before();
         if (is_o) mbar_arrive(&sm.s_ready);  // sb and S_acc of both halves are in place
-        if (has_next) {  // publish the inclusive prefix (its stores were issued above)
+        if (incl_out) {  // publish the inclusive prefix (its stores were issued above)
             __syncwarp();
             if (lane == 0)
                 red_release_add_gpu(prm.incl_cnt + my, (have_agg && !aborted(abort_flag)) ? 1u : kPoison);
@@ -613,26 +671,30 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
                 tmem_st_wait();
                 tc_fence_before();
                 mbar_arrive(&sm.p_full);
+                // Fused layout: these warps also make the bf16 copy of the state for
+                // this chunk, from the update that chunk cj - 1's MMAs issued.
+                if (CF::kFused && cj >= 1 && !refresh_state<D>(sm, abort_flag, tl, i, row_ok, cj - 1)) break;
             }
         } else {
-            // ------------------------------------------------------------ state refresh, O out
-            // The bf16 copy of the next chunk's state gates that chunk's MMAs: with
-            // the fused layout it is made first (its s_full comes before o_full);
-            // with D = 128 after O, whose store frees the stage.  O is staged (bf16,
-            // 128-byte swizzled boxes) in the Q buffer of its own slot -- Q is no
-            // longer read once O is final -- and written by a TMA store, which clips
-            // rows past the end of the sequence.
+            // ------------------------------------------------------------ O out (, state refresh)
+            // O is staged (bf16, 128-byte swizzled boxes) in the Q buffer of its own
+            // slot -- Q is no longer read once O is final -- and written by a TMA
+            // store, which clips rows past the end of the sequence.  With D = 128 these
+            // warps then make the bf16 copy of the next chunk's state (after O, whose
+            // store frees the stage); the fused layout has the T -> P warps do it.
             const bool leader = (warp == kEpiOWarp0 && lane == 0);
             for (int cj = 0; cj < nch; ++cj) {
                 const int s = (nA + cj) % S;
-                if (CF::kFused && cj < nch - 1 && !refresh_state<D>(sm, abort_flag, tl, i, row_ok, cj)) break;
-                if (!wait_bar_warp(abort_flag, &sm.o_full, cj & 1)) break;
+                const int ob = CF::kFused ? (cj & 1) : 0;                       // O buffer
+                const uint32_t opar = CF::kFused ? ((cj >> 1) & 1) : (cj & 1);  // its phase
+                const uint32_t tOb = CF::tO + ob * CF::kOStride;
+                if (!wait_bar_warp(abort_flag, &sm.o_full[ob], opar)) break;
                 tc_fence_after();
                 float den;
                 {
                     uint32_t dn[32];
                     if constexpr (CF::kFused) {
-                        tmem_ld32(tl + CF::tO + D, dn);  // column D: rs + phi(q) z_hi; D + 1: phi(q) z_lo
+                        tmem_ld32(tl + tOb + D, dn);  // column D: rs + phi(q) z_hi; D + 1: phi(q) z_lo
                         tmem_ld_wait();
                         den = __uint_as_float(dn[0]) + __uint_as_float(dn[1]);
                     } else {
@@ -645,8 +707,8 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
 #pragma unroll 1
                 for (int cc = 0; cc < D / 64; ++cc) {
                     uint32_t a[64];
-                    tmem_ld32(tl + CF::tO + cc * 64, *reinterpret_cast<uint32_t(*)[32]>(&a[0]));
-                    tmem_ld32(tl + CF::tO + cc * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&a[32]));
+                    tmem_ld32(tl + tOb + cc * 64, *reinterpret_cast<uint32_t(*)[32]>(&a[0]));
+                    tmem_ld32(tl + tOb + cc * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&a[32]));
                     tmem_ld_wait();
                     uint8_t *rowp = sm.q[s] + cc * kBox + i * 128;
 #pragma unroll
@@ -657,14 +719,14 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
                             pack_bf16(__uint_as_float(a[8 * c + 4]) * inv, __uint_as_float(a[8 * c + 5]) * inv),
                             pack_bf16(__uint_as_float(a[8 * c + 6]) * inv, __uint_as_float(a[8 * c + 7]) * inv));
                 }
-                // o_staged before o_free: the next chunk's o_full needs every thread's
-                // o_free, so no thread can arrive on o_staged for the next chunk while
-                // another has yet to arrive for this one.
+                // o_staged before o_free: the next o_full of this buffer needs every
+                // thread's o_free, so no thread can arrive on o_staged[ob] for that
+                // chunk while another has yet to arrive for this one.
                 fence_proxy_async_smem();
-                mbar_arrive(&sm.o_staged);
+                mbar_arrive(&sm.o_staged[ob]);
                 tc_fence_before();
-                mbar_arrive(&sm.o_free);
-                if (leader && wait_bar(abort_flag, &sm.o_staged, cj & 1)) {
+                mbar_arrive(&sm.o_free[ob]);
+                if (leader && wait_bar(abort_flag, &sm.o_staged[ob], opar)) {
 #pragma unroll
                     for (int cc = 0; cc < D / 64; ++cc)
                         tma_store_3d(&map_o, sm.q[s] + cc * kBox, 64 * cc, (c0 + cj) * kC, bh);
