@@ -60,8 +60,10 @@ constexpr uint32_t kPublished = 8, kPoison = 1u << 20;
 // Row sums and z ride on the tensor cores in one of two ways:
 //  * fused (D = 64): the B operand of P V and of the state update is [V | 1] and
 //    that of phi(Q) S is [S_bf16 | z]: one N = D + 16 MMA whose second 64-wide
-//    block (an LBO away) is the ones block (column 0 = 1) or the z block (columns
-//    0 and 1 = z_hi, z_lo), so result column D holds the row sum or z;
+//    block (an LBO away) is the ones block (column 0 = 1) or a z block (columns
+//    0 and 1 = z_hi, z_lo), so result column D holds the row sum or z.  The ones
+//    block's rows use only column 0, so the two z blocks (one per bf16 S copy) live
+//    in its columns 16.. and 32..: a start address 32 or 64 bytes on;
 //  * separate (D = 128, no room for those blocks): N = 16 MMAs against W, a
 //    [16 rows x 128] bf16 K-major operand (two 1 KB blocks of 8 rows; rows 8..15 of
 //    its descriptor alias into the next 2 KB, the S copy, and feed only unread
@@ -72,20 +74,23 @@ struct Cfg {
     static constexpr int kStages = D == 128 ? 2 : 4;
     static constexpr uint32_t kTileBytes = kC * D * 2;
     static constexpr uint32_t kSbBytes = D * D * 2;   // bf16 copy of S, MN-major for the phi(Q) S MMA
-    // aux: fused = ones block (128 rows), S copy, z block (D rows); separate = W, S copy
-    static constexpr uint32_t kOnes = 0, kW = 0;
-    static constexpr uint32_t kSb = kFused ? kC * 128 : 2048;
-    static constexpr uint32_t kZb = kSb + kSbBytes;
-    static constexpr uint32_t kAuxBytes = kFused ? kZb + D * 128 : kSb + kSbBytes;
-    // TMEM columns.  Fused: O (two buffers, kOStride apart) and S are D + 16 wide,
-    // z in column D of S.  Separate: one O buffer, row sums and phi(q) z in their
-    // own 16-column groups, z at tZ.
+    // aux: fused = two bf16 S copies, then the ones block (128 rows) holding the two z
+    // blocks; separate = W, then the S copy
+    static constexpr uint32_t kW = 0;
+    static constexpr uint32_t kSb = kFused ? 0 : 2048;
+    static constexpr uint32_t kOnes = 2 * kSbBytes;
+    static constexpr uint32_t kAuxBytes = kFused ? kOnes + kC * 128 : kSb + kSbBytes;
+    // TMEM columns.  Fused: P and O have two buffers each (kPStride, kOStride
+    // apart), O and S are D + 16 wide, z in column D of S.  Separate: one P and one
+    // O buffer, row sums and phi(q) z in their own 16-column groups, z at tZ.
     static constexpr uint32_t tT = 0, tP = 128, tRS = 192, tQZ = 208;
-    static constexpr uint32_t tO = kFused ? 192 : 256, kOStride = kFused ? 96 : 0;
-    static constexpr uint32_t tS = kFused ? 384 : 256 + D;
+    static constexpr uint32_t kPStride = kFused ? 64 : 0;
+    static constexpr uint32_t tO = 256, kOStride = kFused ? D + 16 : 0;
+    static constexpr uint32_t tS = kFused ? 416 : 256 + D;
     static constexpr uint32_t tZ = kFused ? tS + D : 224;
     static constexpr uint32_t kTmemCols = 512;
-    static_assert(kFused ? (tP + 64 <= tO && tO + kOStride + D + 16 <= tS && tS + D + 16 <= kTmemCols)
+    static_assert(kFused ? (tP + 2 * kPStride <= tO && tO + 2 * kOStride <= tS && tS + D + 16 <= kTmemCols &&
+                            tS % 32 == 0 && kOStride % 16 == 0)
                          : (tP + 64 <= tRS && tRS + 16 <= tQZ && tQZ + 16 <= tO && tO + D <= tS &&
                             tS + D <= kTmemCols),
                   "TMEM column groups overlap");
@@ -132,20 +137,25 @@ __device__ __forceinline__ bool wait_bar_warp(int *abort_flag, uint64_t *bar, ui
     return tc::wait_bar_warp(&g_tc_status, abort_flag, bar, parity);
 }
 
-// z_i as a bf16 high + low pair in columns 0 and 1 of row i of the z block.
-__device__ __forceinline__ void put_zb(uint8_t *zb, int i, float zv)
-{
-    const __nv_bfloat16 hi = __float2bfloat16_rn(zv);
-    const __nv_bfloat16 lo = __float2bfloat16_rn(zv - __bfloat162float(hi));
-    *reinterpret_cast<__nv_bfloat162 *>(zb + sw128_offset(i, 0)) = __halves2bfloat162(hi, lo);
-}
+// z_i as a bf16 high + low pair: fused, in columns 16(b+1) and 16(b+1)+1 of row i
+// of the ones block (z block b); separate, in rows 1 and 2 of W.
 template <int D>
-__device__ __forceinline__ void set_z(uint8_t *aux, int i, float zv)
+__device__ __forceinline__ void set_z(uint8_t *aux, int i, float zv, int b)
 {
-    if constexpr (Cfg<D>::kFused)
-        put_zb(aux + Cfg<D>::kZb, i, zv);
-    else
+    if constexpr (Cfg<D>::kFused) {
+        const __nv_bfloat16 hi = __float2bfloat16_rn(zv);
+        const __nv_bfloat16 lo = __float2bfloat16_rn(zv - __bfloat162float(hi));
+        *reinterpret_cast<__nv_bfloat162 *>(aux + Cfg<D>::kOnes + sw128_offset(i, 16 * (b + 1))) =
+            __halves2bfloat162(hi, lo);
+    } else {
         put_z(aux + Cfg<D>::kW, i, zv);
+    }
+}
+// bf16 S copy b (fused: b = target chunk % 2; separate: the single copy).
+template <int D>
+__device__ __forceinline__ uint8_t *sb_copy(uint8_t *aux, int b)
+{
+    return aux + Cfg<D>::kSb + (Cfg<D>::kFused ? b * Cfg<D>::kSbBytes : 0);
 }
 
 // S += phi(K_c)^T [V_c | 1] (fused) or S += phi(K_c)^T V_c and z += phi(K_c)^T 1.
@@ -165,6 +175,9 @@ __device__ __forceinline__ void issue_state_update(uint32_t tmem, uint32_t ka, u
 }
 
 // The bf16 copy of S (and z) for the next chunk, from S_acc, once s_full completes.
+// The bf16 copy (and z) of the state for chunk cj + 1, from S_acc once chunk cj's
+// state update is done (s_full).  Fused: into copy (cj + 1) % 2, the caller signals
+// through p_full; separate: the single copy, then s_ready.
 template <int D>
 __device__ __forceinline__ bool refresh_state(Smem<D> &sm, int *abort_flag, uint32_t tl, int i, bool row_ok, int cj)
 {
@@ -180,17 +193,19 @@ __device__ __forceinline__ bool refresh_state(Smem<D> &sm, int *abort_flag, uint
         if (row_ok) {
             float x[32];
             to_floats(&a[0], x);
-            put_sb<D>(sm.aux + CF::kSb, i, cc * 64, x);
+            put_sb<D>(sb_copy<D>(sm.aux, (cj + 1) & 1), i, cc * 64, x);
             to_floats(&a[32], x);
-            put_sb<D>(sm.aux + CF::kSb, i, cc * 64 + 32, x);
+            put_sb<D>(sb_copy<D>(sm.aux, (cj + 1) & 1), i, cc * 64 + 32, x);
         }
     }
     const float zv = __uint_as_float(tmem_ld1(tl + CF::tZ));
     tmem_ld_wait();
-    if (row_ok) set_z<D>(sm.aux, i, zv);
+    if (row_ok) set_z<D>(sm.aux, i, zv, (cj + 1) & 1);
     fence_proxy_async_smem();
-    tc_fence_before();
-    mbar_arrive(&sm.s_ready);
+    if constexpr (!CF::kFused) {
+        tc_fence_before();
+        mbar_arrive(&sm.s_ready);
+    }
     return true;
 }
 
@@ -219,7 +234,7 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
     }
     Smem<D> &sm = *reinterpret_cast<Smem<D> *>(smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    uint8_t *const sb = sm.aux + CF::kSb;
+    uint8_t *const sb = sb_copy<D>(sm.aux, 0);  // phase B writes the state for the first chunk here
 
     // The work ticket is taken first, its latency hidden behind the set-up.  A CTA
     // that waits on an earlier ticket waits on a running CTA: no other CTA of this
@@ -235,8 +250,6 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
                 const uint32_t x = (c & 7) == ((c >> 3) & 7) ? 0x3F80u : 0u;
                 *reinterpret_cast<uint4 *>(sm.aux + CF::kOnes + c * 16) = make_uint4(x, 0u, 0u, 0u);
             }
-            for (int c = tid; c < D * 8; c += 128)
-                *reinterpret_cast<uint4 *>(sm.aux + CF::kZb + c * 16) = make_uint4(0u, 0u, 0u, 0u);
         } else {  // W: row 0 ones, everything else zero (rows 1, 2 get z in phase B)
             const int blk = tid >> 6, within = tid & 63;
             const uint32_t val = (within < 8) ? 0x3F803F80u : 0u;  // first 128 bytes of a block = row 0
@@ -353,9 +366,9 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
             const uint32_t id_KW = idesc_bf16_f32(128, 16, true, false);    // phi(K)^T W^T
             const uint32_t aux = smem_u32(sm.aux);
             const uint32_t w_addr = aux + CF::kW, sb_addr = aux + CF::kSb, ones_addr = aux + CF::kOnes;
-            // Second 64-wide block of the B operands: the z block after the S copy
-            // (fused) or the S copy's own second block (D = 128).
-            const uint32_t lbo_sb = CF::kFused ? CF::kZb - CF::kSb : D * 128;
+            // Second 64-wide block of [S_bf16 | z] (fused: z block b, in the ones block
+            // 32(b+1) bytes on) or of the S copy itself (D = 128).
+            const uint32_t lbo_sb = D * 128;
             bool ok = true;
             // phase A: aggregate state of the segment
             for (int ja = 0; ja < nA && ok; ++ja) {
@@ -370,55 +383,63 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
             if (ok && nA > 0) mma_commit(&sm.agg_ready);
             // phase C: outputs
             if constexpr (CF::kFused) {
-                // Software-pipelined over chunks: P V of chunk c (its within-chunk term,
-                // into O buffer c % 2), then T of chunk c + 1 -- so that P(c+1) is formed
-                // while the rest of chunk c runs -- then phi(Q_c)[S | z], completing O(c),
-                // then the state update.  The state update's commit also covers the MMAs
-                // that read the S copy and z, which the refresh overwrites next.
+                // Software-pipelined over chunks.  Every mbarrier operation of this
+                // thread costs about as much as an MMA while the tensor pipe idles, so a
+                // chunk takes two waits and up to four commits.  Chunk c: wait p_full(c)
+                // -- which also stands for "T(c) read, the bf16 state for chunk c in
+                // place, phi of chunk c + 1 done" (the T -> P warps wait for those) --
+                // then T(c + 1) first, so that P(c + 1) is formed (into the other P
+                // buffer) while the rest of chunk c runs; the state update (S_acc to the
+                // state for chunk c + 1, from which the T -> P warps refresh the other bf16
+                // copy); P V of chunk c (its within-chunk term, into O buffer c % 2); and
+                // phi(Q_c)[S | z] with copy c % 2, completing O(c).  The descriptors of
+                // one chunk differ by constant steps of the start address.
                 if (nch > 0) {
                     const int s0 = nA % S;
                     if ((ok = wait_bar(abort_flag, &sm.phi_done[s0], (nA / S) & 1))) {
                         tc_fence_after();
-                        const uint32_t qa = smem_u32(sm.q[s0]), ka = smem_u32(sm.k[s0]);
+                        const uint64_t dq = kmajor(smem_u32(sm.q[s0]), 0), dk = kmajor(smem_u32(sm.k[s0]), 0);
 #pragma unroll
                         for (int kk = 0; kk < D / 16; ++kk)
-                            mma_ss(tmem + CF::tT, kmajor(qa, kk), kmajor(ka, kk), id_T, kk > 0 ? 1u : 0u);
+                            mma_ss(tmem + CF::tT, dq + 2 * kk, dk + 2 * kk, id_T, kk > 0 ? 1u : 0u);
                         mma_commit(&sm.t_full);
                     }
                 }
                 for (int cj = 0; cj < nch && ok; ++cj) {
                     const int j = nA + cj, s = j % S, ob = cj & 1;
                     const uint32_t dO = tmem + CF::tO + ob * CF::kOStride;
-                    const uint32_t qa = smem_u32(sm.q[s]), ka = smem_u32(sm.k[s]), va = smem_u32(sm.v[s]);
-                    const uint32_t lbo_v = ones_addr - va;
+                    const uint32_t dP = tmem + CF::tP + ob * CF::kPStride;
+                    const uint32_t va = smem_u32(sm.v[s]);
+                    const uint64_t dv = mnmajor(va, 0, ones_addr - va);           // [V | 1], + 128 per kk
+                    const uint32_t sbc = sb_addr + ob * CF::kSbBytes;
+                    const uint64_t dsb = mnmajor(sbc, 0, ones_addr + 32 * (ob + 1) - sbc);  // [S | z]
+                    const uint64_t dqc = kmajor(smem_u32(sm.q[s]), 0);          // + 2 per kk
                     if (cj >= 2 && !(ok = wait_bar(abort_flag, &sm.o_free[ob], ((cj >> 1) - 1) & 1))) break;
                     if (!(ok = wait_bar(abort_flag, &sm.p_full, cj & 1))) break;
                     tc_fence_after();
-#pragma unroll
-                    for (int kk = 0; kk < kC / 16; ++kk)
-                        mma_ts(dO, tmem + CF::tP + kk * 8, mnmajor(va, kk, lbo_v), id_PV, kk > 0 ? 1u : 0u);
                     if (cj + 1 < nch) {
                         const int s1 = (j + 1) % S;
-                        if (!(ok = wait_bar(abort_flag, &sm.phi_done[s1], ((j + 1) / S) & 1))) break;
-                        if (!(ok = wait_bar(abort_flag, &sm.t_free, cj & 1))) break;
-                        tc_fence_after();
-                        const uint32_t qa1 = smem_u32(sm.q[s1]), ka1 = smem_u32(sm.k[s1]);
+                        const uint64_t dq1 = kmajor(smem_u32(sm.q[s1]), 0), dk1 = kmajor(smem_u32(sm.k[s1]), 0);
 #pragma unroll
                         for (int kk = 0; kk < D / 16; ++kk)
-                            mma_ss(tmem + CF::tT, kmajor(qa1, kk), kmajor(ka1, kk), id_T, kk > 0 ? 1u : 0u);
+                            mma_ss(tmem + CF::tT, dq1 + 2 * kk, dk1 + 2 * kk, id_T, kk > 0 ? 1u : 0u);
                         mma_commit(&sm.t_full);
                     }
-                    if (!(ok = wait_bar(abort_flag, &sm.s_ready, cj & 1))) break;
-                    tc_fence_after();
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk)
-                        mma_ss(dO, kmajor(qa, kk), mnmajor(sb_addr, kk, lbo_sb), id_QS, 1u);
-                    mma_commit(&sm.o_full[ob]);
                     if (cj < nch - 1) {
-                        issue_state_update<D>(tmem, ka, va, lbo_v, w_addr, id_KV, id_KW, false);
+                        const uint64_t dkt = mnmajor(smem_u32(sm.k[s]), 0, kBox);  // phi(K)^T, + 128 per kk
+#pragma unroll
+                        for (int kk = 0; kk < kC / 16; ++kk)
+                            mma_ss(tmem + CF::tS, dkt + 128 * kk, dv + 128 * kk, id_KV, 1u);
                         mma_commit(&sm.s_full);
                     }
-                    mma_commit(&sm.empty[s]);
+#pragma unroll
+                    for (int kk = 0; kk < kC / 16; ++kk)
+                        mma_ts(dO, dP + kk * 8, dv + 128 * kk, id_PV, kk > 0 ? 1u : 0u);
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk)
+                        mma_ss(dO, dqc + 2 * kk, dsb + 128 * kk, id_QS, 1u);
+                    mma_commit(&sm.o_full[ob]);
+                    if (j + S < total) mma_commit(&sm.empty[s]);  // only a stage that is refilled
                 }
             } else {
                 // D = 128: per chunk T, phi(Q) S and its z term, P V and the row sums, then
@@ -616,7 +637,7 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
                 if (row_ok) incl_out[(size_t)D * D + i] = zacc + za;
             }
             tmem_st1(tl + CF::tZ, __float_as_uint(zacc));
-            if (row_ok) set_z<D>(sm.aux, i, zacc);
+            if (row_ok) set_z<D>(sm.aux, i, zacc, 0);
         }
         tmem_st_wait();
         fence_proxy_async_smem();
@@ -633,6 +654,7 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
             // ------------------------------------------------------------ T -> P
             for (int cj = 0; cj < nch; ++cj) {
                 if (!wait_bar_warp(abort_flag, &sm.t_full, cj & 1)) break;
+                const uint32_t tPb = CF::tP + (cj & 1) * CF::kPStride;
                 tc_fence_after();
                 // This warp's rows are 32*quad .. 32*quad+31, so key block b (32 keys)
                 // is entirely visible for b < quad, masked on the diagonal for b ==
@@ -661,19 +683,25 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
 #pragma unroll
                             for (int e = 0; e < 16; ++e) pk[e] = 0u;
                         }
-                        if (b == 3) {  // all of T that this warp reads has been read
+                        if (!CF::kFused && b == 3) {  // all of T that this warp reads has been read
                             tc_fence_before();
                             mbar_arrive(&sm.t_free);
                         }
-                        tmem_st16(tl + CF::tP + b * 16, pk);
+                        tmem_st16(tl + tPb + b * 16, pk);
                     }
                 }
                 tmem_st_wait();
+                if constexpr (CF::kFused) {
+                    // p_full(cj) also stands for the bf16 state for chunk cj (copy cj % 2,
+                    // made here once chunk cj - 1's state update is done; the first chunk's
+                    // came from phase B) and for phi of chunk cj + 1.
+                    if (cj >= 1 && !refresh_state<D>(sm, abort_flag, tl, i, row_ok, cj - 1)) break;
+                    if (cj + 1 < nch && !wait_bar_warp(abort_flag, &sm.phi_done[(nA + cj + 1) % S],
+                                                       ((nA + cj + 1) / S) & 1))
+                        break;
+                }
                 tc_fence_before();
                 mbar_arrive(&sm.p_full);
-                // Fused layout: these warps also make the bf16 copy of the state for
-                // this chunk, from the update that chunk cj - 1's MMAs issued.
-                if (CF::kFused && cj >= 1 && !refresh_state<D>(sm, abort_flag, tl, i, row_ok, cj - 1)) break;
             }
         } else {
             // ------------------------------------------------------------ O out (, state refresh)
@@ -694,7 +722,9 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
                 {
                     uint32_t dn[32];
                     if constexpr (CF::kFused) {
-                        tmem_ld32(tl + tOb + D, dn);  // column D: rs + phi(q) z_hi; D + 1: phi(q) z_lo
+                        // column D: rs + phi(q) z_hi; D + 1: phi(q) z_lo (16-column loads: O
+                        // buffer 1 starts on a 16-column boundary)
+                        tmem_ld16(tl + tOb + D, *reinterpret_cast<uint32_t(*)[16]>(&dn[0]));
                         tmem_ld_wait();
                         den = __uint_as_float(dn[0]) + __uint_as_float(dn[1]);
                     } else {
@@ -707,8 +737,14 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
 #pragma unroll 1
                 for (int cc = 0; cc < D / 64; ++cc) {
                     uint32_t a[64];
-                    tmem_ld32(tl + tOb + cc * 64, *reinterpret_cast<uint32_t(*)[32]>(&a[0]));
-                    tmem_ld32(tl + tOb + cc * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&a[32]));
+                    if constexpr (CF::kFused) {
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4)
+                            tmem_ld16(tl + tOb + cc * 64 + 16 * q4, *reinterpret_cast<uint32_t(*)[16]>(&a[16 * q4]));
+                    } else {
+                        tmem_ld32(tl + tOb + cc * 64, *reinterpret_cast<uint32_t(*)[32]>(&a[0]));
+                        tmem_ld32(tl + tOb + cc * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&a[32]));
+                    }
                     tmem_ld_wait();
                     uint8_t *rowp = sm.q[s] + cc * kBox + i * 128;
 #pragma unroll
