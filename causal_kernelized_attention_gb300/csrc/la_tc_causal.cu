@@ -158,6 +158,14 @@ __device__ __forceinline__ uint8_t *sb_copy(uint8_t *aux, int b)
     return aux + Cfg<D>::kSb + (Cfg<D>::kFused ? b * Cfg<D>::kSbBytes : 0);
 }
 
+// Chunk of job j: phase-A jobs walk the segment backwards, so that phase C, which
+// walks it forwards, starts with the K and V tiles read most recently (the likeliest
+// still in L2); the aggregate is a sum, so its order is free.
+__device__ __forceinline__ int job_chunk(int j, int nA, int c0)
+{
+    return j < nA ? c0 + (nA - 1 - j) : c0 + (j - nA);
+}
+
 // S += phi(K_c)^T [V_c | 1] (fused) or S += phi(K_c)^T V_c and z += phi(K_c)^T 1.
 // phi(K_c)^T is MN-major with its second dk block one box on (D = 64: the next
 // tile, whose rows 64..127 of the result are never read).
@@ -306,7 +314,7 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
             const int s = j % S, r = j / S;
             if (!wait_bar(abort_flag, &sm.full[s], r & 1)) break;
             const bool isC = j >= nA;
-            const int chunk = c0 + (isC ? j - nA : j);
+            const int chunk = job_chunk(j, nA, c0);
             const int valid = prm.N - chunk * kC;
             if (isC) {
                 phi_tile<D, kPhiThreads>(sm.k[s], tid, valid);
@@ -327,6 +335,10 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
             tma_prefetch_map(&map_k);
             tma_prefetch_map(&map_v);
             tma_prefetch_map(&map_o);
+            // All tiles are loaded evict-first.  (Keeping phase A's K and V with
+            // evict-last for their second read in phase C measured slower on long
+            // sequences: 1 MB of them per CTA outgrows L2 across the GPU anyway.)
+            const uint64_t pol_first = l2_policy_evict_first();
             int issued = 0;
             for (int j = 0; j < total; ++j) {
                 const int s = j % S, r = j / S;
@@ -337,13 +349,13 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
                     if (!wait_bar(abort_flag, &sm.ostore[s], k & 1)) break;
                 }
                 const bool isC = j >= nA;
-                const int row0 = (c0 + (isC ? j - nA : j)) * kC;
+                const int row0 = job_chunk(j, nA, c0) * kC;
                 mbar_arrive_expect_tx(&sm.full[s], (isC ? 3u : 2u) * CF::kTileBytes);
 #pragma unroll
                 for (int b = 0; b < D / 64; ++b) {
-                    if (isC) tma_load_3d(sm.q[s] + b * kBox, &map_q, &sm.full[s], 64 * b, row0, bh);
-                    tma_load_3d(sm.k[s] + b * kBox, &map_k, &sm.full[s], 64 * b, row0, bh);
-                    tma_load_3d(sm.v[s] + b * kBox, &map_v, &sm.full[s], 64 * b, row0, bh);
+                    if (isC) tma_load_3d_hint(sm.q[s] + b * kBox, &map_q, &sm.full[s], 64 * b, row0, bh, pol_first);
+                    tma_load_3d_hint(sm.k[s] + b * kBox, &map_k, &sm.full[s], 64 * b, row0, bh, pol_first);
+                    tma_load_3d_hint(sm.v[s] + b * kBox, &map_v, &sm.full[s], 64 * b, row0, bh, pol_first);
                 }
                 issued = j + 1;
             }
@@ -505,7 +517,7 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
         for (int j = 0; j < nA; ++j) {
             const int s = j % S, r = j / S;
             if (!wait_bar(abort_flag, &sm.full[s], r & 1)) break;
-            phi_tile<D, 2 * kPhiThreads>(sm.k[s], kPhiThreads + gtid, prm.N - (c0 + j) * kC);
+            phi_tile<D, 2 * kPhiThreads>(sm.k[s], kPhiThreads + gtid, prm.N - job_chunk(j, nA, c0) * kC);
             fence_proxy_async_smem();
             mbar_arrive(&sm.phi_done[s]);
         }
@@ -763,9 +775,10 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
                 tc_fence_before();
                 mbar_arrive(&sm.o_free[ob]);
                 if (leader && wait_bar(abort_flag, &sm.o_staged[ob], opar)) {
+                    const uint64_t pol_once = l2_policy_evict_first();
 #pragma unroll
                     for (int cc = 0; cc < D / 64; ++cc)
-                        tma_store_3d(&map_o, sm.q[s] + cc * kBox, 64 * cc, (c0 + cj) * kC, bh);
+                        tma_store_3d_hint(&map_o, sm.q[s] + cc * kBox, 64 * cc, (c0 + cj) * kC, bh, pol_once);
                     tma_store_commit();
                 }
                 if (!CF::kFused && cj < nch - 1 && !refresh_state<D>(sm, abort_flag, tl, i, row_ok, cj)) break;

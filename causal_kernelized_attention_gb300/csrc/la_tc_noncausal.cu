@@ -275,6 +275,9 @@ noncausal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
             tma_prefetch_map(&map_k);
             tma_prefetch_map(&map_v);
             tma_prefetch_map(&map_o);
+            // Every tile is read once: let it leave L2 first, ahead of the partials and
+            // state images that other CTAs read back.
+            const uint64_t pol_once = l2_policy_evict_first();
             int j = 0;
             bool ok = true;
             for (int it = 0; ok; ++it) {
@@ -293,14 +296,14 @@ noncausal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
                         mbar_arrive_expect_tx(&sm.full[s], 2 * kTile);
 #pragma unroll
                         for (int b = 0; b < D / 64; ++b) {
-                            tma_load_3d(st + b * kBox, &map_k, &sm.full[s], 64 * b, row0, item.bh);
-                            tma_load_3d(st + kTile + b * kBox, &map_v, &sm.full[s], 64 * b, row0, item.bh);
+                            tma_load_3d_hint(st + b * kBox, &map_k, &sm.full[s], 64 * b, row0, item.bh, pol_once);
+                            tma_load_3d_hint(st + kTile + b * kBox, &map_v, &sm.full[s], 64 * b, row0, item.bh, pol_once);
                         }
                     } else {
                         mbar_arrive_expect_tx(&sm.full[s], kTile);
 #pragma unroll
                         for (int b = 0; b < D / 64; ++b)
-                            tma_load_3d(st + b * kBox, &map_q, &sm.full[s], 64 * b, row0, item.bh);
+                            tma_load_3d_hint(st + b * kBox, &map_q, &sm.full[s], 64 * b, row0, item.bh, pol_once);
                     }
                 }
             }
@@ -524,9 +527,10 @@ noncausal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
                     tc_fence_before();
                     mbar_arrive(&sm.acc_free[a]);
                     if (leader && (ok = wait_bar(abort_flag, &sm.o_staged[a], (ostaged_phase >> a) & 1u))) {
+                        const uint64_t pol_once = l2_policy_evict_first();
 #pragma unroll
                         for (int cc = 0; cc < D / 64; ++cc)
-                            tma_store_3d(&map_o, ost + cc * kBox, 64 * cc, (item.c0 + c) * kC, item.bh);
+                            tma_store_3d_hint(&map_o, ost + cc * kBox, 64 * cc, (item.c0 + c) * kC, item.bh, pol_once);
                         tma_store_commit();
                         // The previous tile's store has read its staged O: that stage may be refilled.
                         tma_store_wait_read<1>();
