@@ -135,17 +135,20 @@ def whole_job_throughput(world: int, units_per_rank: float, steps: int, slowest_
 
 # --------------------------------------------------------------------------- clocks
 class ClockSampler:
-    """nvidia-smi sampling of SM clocks and throttle reasons while the GPU works."""
+    """nvidia-smi sampling of SM clocks and throttle reasons while the GPU works.
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    Each sample carries nvidia-smi's own timestamp; stop(window=(t0, t1)) reports
+    the samples taken inside that host-time window (the timed region) as the ones
+    under load, and the throttle reasons seen anywhere in the run."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index=0, period_ms=100, load_watts=200.0):
+    def __init__(self, gpu_index=0, period_ms=20):
         self.proc = None
         self.gpu_index = gpu_index
         self.period_ms = period_ms
-        self.load_watts = load_watts
 
     def start(self):
         try:
@@ -156,7 +159,15 @@ class ClockSampler:
             self.proc = None
         return self
 
-    def stop(self):
+    @staticmethod
+    def _epoch(stamp: str):
+        import datetime
+        try:
+            return datetime.datetime.strptime(stamp.strip(), "%Y/%m/%d %H:%M:%S.%f").timestamp()
+        except ValueError:
+            return None
+
+    def stop(self, window=None):
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
         self.proc.terminate()
@@ -165,24 +176,32 @@ class ClockSampler:
         except Exception:
             self.proc.kill()
             out, _ = self.proc.communicate()
-        rows = [r for r in csv.reader(io.StringIO(out)) if len(r) >= 9]
-        sm, smax, reasons, loaded = [], None, set(), []
+        return self.summarise(out, window, self.period_ms)
+
+    @classmethod
+    def summarise(cls, text, window, period_ms):
+        """Median SM clock of the samples inside `window` (all samples if none is),
+        the maximum clock, and every throttle reason seen."""
+        rows = [r for r in csv.reader(io.StringIO(text)) if len(r) >= 10]
+        sm, smax, reasons, inside = [], None, set(), []
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for r in rows:
             try:
-                s, m, pw = float(r[1]), float(r[2]), float(r[3])
+                s, m = float(r[2]), float(r[3])
             except ValueError:
                 continue
             smax = m
             sm.append(s)
-            if pw > self.load_watts:
-                loaded.append(s)
-            for n, val in zip(names, r[5:9]):
+            t = cls._epoch(r[0])
+            if window is not None and t is not None and window[0] <= t <= window[1]:
+                inside.append(s)
+            for n, val in zip(names, r[6:10]):
                 if val.strip().lower().startswith("active"):
                     reasons.add(n)
-        use = loaded if loaded else sm
+        use = inside if inside else sm
         return {"sm_mhz": statistics.median(use) if use else None, "sm_max_mhz": smax,
-                "reasons": sorted(reasons), "samples": len(rows), "samples_under_load": len(loaded)}
+                "reasons": sorted(reasons), "samples": len(sm), "samples_in_timed_region": len(inside),
+                "sampling_ms": period_ms}
 
 
 # --------------------------------------------------------------------------- distributed
@@ -258,13 +277,17 @@ def time_graph_steps(torch, la, fn, steps, warmup, dist, sampler=None):
     if sampler is not None:
         sampler.start()
         time.sleep(0.25)  # let the sampler take its first reading before the timed region
+    t_begin = time.time()
     with torch.cuda.stream(stream):
         start.record(stream)
         for g in timed:
             g.replay()
         stop.record(stream)
     torch.cuda.synchronize()
-    clocks = sampler.stop() if sampler is not None else None
+    t_end = time.time()
+    if sampler is not None:
+        time.sleep(2.5 * sampler.period_ms / 1e3)  # one more reading after the timed region
+    clocks = sampler.stop(window=(t_begin, t_end)) if sampler is not None else None
     dist.barrier()
     secs = start.elapsed_time(stop) / 1e3
     del timed, warm
@@ -479,7 +502,7 @@ def run_gpu(args, dist):
     peaks, src = load_peaks()
     w = workloads.CAUSAL_BF16
 
-    sampler = ClockSampler(gpu_index=torch.cuda.current_device(), period_ms=50) if dist.rank == 0 else None
+    sampler = ClockSampler(gpu_index=torch.cuda.current_device()) if dist.rank == 0 else None
     secs, launches, nbytes, R, clocks = bench_causal_headline(torch, la, w, args.steps, args.warmup, dist, peaks,
                                                               src, sampler)
     secs_max = dist.max(secs)
@@ -494,12 +517,13 @@ def run_gpu(args, dist):
 
     paths = {}
     if not args.headline_only:
-        s2 = ClockSampler(gpu_index=torch.cuda.current_device()).start() if dist.rank == 0 else None
+        s2 = ClockSampler(gpu_index=torch.cuda.current_device(), period_ms=100).start() if dist.rank == 0 else None
+        t_paths = time.time()
         paths["causal_long"] = bench_path_causal_long(torch, la, args.path_reps, peaks, src)
         paths["noncausal"] = bench_path_noncausal(torch, la, max(args.path_reps, 20), peaks, src)
         paths["decode"] = bench_path_decode(torch, la, 1024, peaks, src)
         if s2:
-            paths["clocks"] = s2.stop()
+            paths["clocks"] = s2.stop(window=(t_paths, time.time()))
 
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": dist.world,

@@ -1,6 +1,6 @@
-"""Multi-rank host logic of bench.py on CPU (gloo, world size 2): the timed
-region's max-over-ranks reduction and barrier, the whole-job throughput, and the
-reference arm printing on rank 0 only."""
+"""Host logic of bench.py on CPU: the multi-rank timed region (gloo, world size
+2: max-over-ranks reduction and barrier), the whole-job throughput, the
+reference arm printing on rank 0 only, and the clock record's sample selection."""
 import os
 import socket
 import subprocess
@@ -60,3 +60,26 @@ def test_reference_arm_prints_on_rank_zero_only():
                         "--warmup", "3"], env=env, capture_output=True, text=True, timeout=300)
     assert r.returncode == 0
     assert r.stdout.strip() == ""
+
+
+def test_clock_sampler_uses_samples_inside_the_timed_window():
+    import datetime
+    sys.path.insert(0, ROOT)
+    import bench
+    t0 = datetime.datetime(2026, 1, 2, 3, 4, 5)
+
+    def row(dt_ms, sm, reasons=("Not Active",) * 4):
+        stamp = (t0 + datetime.timedelta(milliseconds=dt_ms)).strftime("%Y/%m/%d %H:%M:%S.%f")[:-3]
+        return ", ".join([stamp, "0", str(sm), "2070", "300.0", "0x0"] + list(reasons))
+
+    text = "\n".join([row(0, 1200), row(20, 2070), row(40, 2055),
+                      row(60, 1800, ("Not Active", "Not Active", "Not Active", "Active"))])
+    window = ((t0 + datetime.timedelta(milliseconds=10)).timestamp(),
+              (t0 + datetime.timedelta(milliseconds=45)).timestamp())
+    c = bench.ClockSampler.summarise(text, window, 20)
+    assert c["samples"] == 4 and c["samples_in_timed_region"] == 2
+    assert c["sm_mhz"] == (2070 + 2055) / 2 and c["sm_max_mhz"] == 2070
+    assert c["reasons"] == ["sw_power_cap"]
+    # no sample inside the window: the median of all samples
+    c = bench.ClockSampler.summarise(text, (0.0, 1.0), 20)
+    assert c["samples_in_timed_region"] == 0 and c["sm_mhz"] == (1800 + 2055) / 2
