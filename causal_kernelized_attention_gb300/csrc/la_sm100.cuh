@@ -110,6 +110,14 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, const void 
                  : "memory");
 }
 
+// Prefetch a tile into L2 (no shared-memory destination, no completion to wait for).
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap *map, int x, int y, int z)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(map), "r"(x), "r"(y),
+                 "r"(z)
+                 : "memory");
+}
+
 // L2 cache policies for the hinted copies: keep (evict_last) data that is read
 // again soon, let single-use streams go first (evict_first).
 __device__ __forceinline__ uint64_t l2_policy_evict_last()

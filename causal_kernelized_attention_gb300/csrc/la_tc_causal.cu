@@ -104,7 +104,8 @@ struct alignas(1024) Smem {
     uint8_t aux[Cfg<D>::kAuxBytes];
     uint64_t full[Cfg<D>::kStages], phi_done[Cfg<D>::kStages], empty[Cfg<D>::kStages];
     uint64_t ostore[Cfg<D>::kStages];  // the O tile staged in slot s has been read by its TMA store
-    uint64_t t_full, t_free, p_full, s_full, s_ready, agg_ready, drain;
+    uint64_t t_full, t_free, s_full, s_ready, agg_ready, drain;
+    uint64_t p_full[2];  // per P buffer (the separate layout uses buffer 0)
     uint64_t o_full[2], o_free[2];  // per O buffer (the separate layout uses buffer 0)
     uint64_t o_staged[2];           // all 128 rows of the buffer's O tile are staged in shared memory
     uint32_t tmem_base;
@@ -217,6 +218,46 @@ __device__ __forceinline__ bool refresh_state(Smem<D> &sm, int *abort_flag, uint
     return true;
 }
 
+// T -> P for the key blocks in `blocks` (bit b = keys 32b..32b+31) of this warp's
+// 32 query rows (32*quad .. 32*quad+31): block b is entirely visible for b < quad,
+// masked on the diagonal for b == quad, and entirely masked (zeros, no TMEM read)
+// for b > quad.  When t_free is given, it is arrived on once T has been read.
+template <int D>
+__device__ __forceinline__ void convert_tp(uint32_t tl, uint32_t tPb, int quad, int lane, unsigned blocks,
+                                           uint64_t *t_free)
+{
+    uint32_t t[32];
+    uint32_t pk[16];
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+        if (!((blocks >> b) & 1u)) continue;
+        if (b <= quad) {
+            tmem_ld32(tl + Cfg<D>::tT + b * 32, t);
+            tmem_ld_wait();
+            if (b == quad) {
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const int jk = 2 * e;  // key offset within the diagonal block
+                    pk[e] = pack_bf16(jk <= lane ? __uint_as_float(t[2 * e]) : 0.f,
+                                      jk + 1 <= lane ? __uint_as_float(t[2 * e + 1]) : 0.f);
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < 16; ++e) pk[e] = pack_bf16(__uint_as_float(t[2 * e]), __uint_as_float(t[2 * e + 1]));
+            }
+        } else {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) pk[e] = 0u;
+        }
+        if (t_free && b == 3) {  // all of T that this warp reads has been read
+            tc_fence_before();
+            mbar_arrive(t_free);
+        }
+        tmem_st16(tl + tPb + b * 16, pk);
+    }
+    tmem_st_wait();
+}
+
 // add_state, plus z_i of the same state (issued with it) when want_z.
 template <int D>
 __device__ __forceinline__ void add_state_z(float (&acc)[32], float &zacc, const float *state, int cg0, int i,
@@ -250,6 +291,24 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
     // allocation below can only wait on other kernels' CTAs, which never wait on it.
     int my_ticket = 0;
     if (tid == 0) my_ticket = (int)atomicAdd(prm.counter, 1u);
+    if (warp == kTmaWarp && lane == 0) {
+        // While the ticket is out: warm L2 with the first tiles of segment blockIdx.x.
+        // Every segment belongs to exactly one CTA, which reads these tiles first
+        // (phase A's last chunks, or the first chunk when there is no phase A),
+        // whichever CTA draws that ticket.
+        const int pg = (int)blockIdx.x / prm.BH, pbh = (int)blockIdx.x % prm.BH;
+        const int pc0 = pg * prm.L, pn = min(prm.L, prm.n_chunks - pc0);
+        const bool pa = pg < prm.G - 1;
+        for (int x = 0; x < min(pn, S); ++x) {
+            const int row0 = (pa ? pc0 + pn - 1 - x : pc0 + x) * kC;
+#pragma unroll
+            for (int b = 0; b < D / 64; ++b) {
+                if (!pa) tma_prefetch_3d(&map_q, 64 * b, row0, pbh);
+                tma_prefetch_3d(&map_k, 64 * b, row0, pbh);
+                tma_prefetch_3d(&map_v, 64 * b, row0, pbh);
+            }
+        }
+    }
 
     if (tid < 128) {
         if constexpr (CF::kFused) {
@@ -276,7 +335,8 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
         }
         mbar_init(&sm.t_full, 1);
         mbar_init(&sm.t_free, 128);
-        mbar_init(&sm.p_full, 128);
+        for (int b = 0; b < 2; ++b)
+            mbar_init(&sm.p_full[b], CF::kFused ? 256 : 128);  // fused: the T->P and the O warps convert
         for (int ob = 0; ob < 2; ++ob) {
             mbar_init(&sm.o_full[ob], 1);
             mbar_init(&sm.o_free[ob], 128);
@@ -395,17 +455,15 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
             if (ok && nA > 0) mma_commit(&sm.agg_ready);
             // phase C: outputs
             if constexpr (CF::kFused) {
-                // Software-pipelined over chunks.  Every mbarrier operation of this
-                // thread costs about as much as an MMA while the tensor pipe idles, so a
-                // chunk takes two waits and up to four commits.  Chunk c: wait p_full(c)
-                // -- which also stands for "T(c) read, the bf16 state for chunk c in
-                // place, phi of chunk c + 1 done" (the T -> P warps wait for those) --
-                // then T(c + 1) first, so that P(c + 1) is formed (into the other P
-                // buffer) while the rest of chunk c runs; the state update (S_acc to the
-                // state for chunk c + 1, from which the T -> P warps refresh the other bf16
-                // copy); P V of chunk c (its within-chunk term, into O buffer c % 2); and
-                // phi(Q_c)[S | z] with copy c % 2, completing O(c).  The descriptors of
-                // one chunk differ by constant steps of the start address.
+                // Software-pipelined over chunks.  Chunk c waits for p_full(c), which also
+                // stands for "T(c) read, the bf16 state for chunk c in place, phi of
+                // chunk c + 1 done" (the T -> P warps wait for those), then issues:
+                //   S_acc += phi(K_c)^T [V_c | 1]  (the state for chunk c + 1: first, so
+                //            that the T -> P warps can make its bf16 copy at once),
+                //   T(c + 1) (into the T buffer they convert next, into the other P buffer),
+                //   O(c) = P(c) [V_c | 1] + phi(Q_c)[S | z]  (O buffer c % 2, copy c % 2).
+                // p_full(c + 1) can then complete while O(c) is still in the tensor pipe.
+                // The descriptors of one chunk differ by constant steps of the start address.
                 if (nch > 0) {
                     const int s0 = nA % S;
                     if ((ok = wait_bar(abort_flag, &sm.phi_done[s0], (nA / S) & 1))) {
@@ -427,8 +485,15 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
                     const uint64_t dsb = mnmajor(sbc, 0, ones_addr + 32 * (ob + 1) - sbc);  // [S | z]
                     const uint64_t dqc = kmajor(smem_u32(sm.q[s]), 0);          // + 2 per kk
                     if (cj >= 2 && !(ok = wait_bar(abort_flag, &sm.o_free[ob], ((cj >> 1) - 1) & 1))) break;
-                    if (!(ok = wait_bar(abort_flag, &sm.p_full, cj & 1))) break;
+                    if (!(ok = wait_bar(abort_flag, &sm.p_full[ob], (cj >> 1) & 1))) break;
                     tc_fence_after();
+                    if (cj < nch - 1) {
+                        const uint64_t dkt = mnmajor(smem_u32(sm.k[s]), 0, kBox);  // phi(K)^T, + 128 per kk
+#pragma unroll
+                        for (int kk = 0; kk < kC / 16; ++kk)
+                            mma_ss(tmem + CF::tS, dkt + 128 * kk, dv + 128 * kk, id_KV, 1u);
+                        mma_commit(&sm.s_full);
+                    }
                     if (cj + 1 < nch) {
                         const int s1 = (j + 1) % S;
                         const uint64_t dq1 = kmajor(smem_u32(sm.q[s1]), 0), dk1 = kmajor(smem_u32(sm.k[s1]), 0);
@@ -436,13 +501,6 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
                         for (int kk = 0; kk < D / 16; ++kk)
                             mma_ss(tmem + CF::tT, dq1 + 2 * kk, dk1 + 2 * kk, id_T, kk > 0 ? 1u : 0u);
                         mma_commit(&sm.t_full);
-                    }
-                    if (cj < nch - 1) {
-                        const uint64_t dkt = mnmajor(smem_u32(sm.k[s]), 0, kBox);  // phi(K)^T, + 128 per kk
-#pragma unroll
-                        for (int kk = 0; kk < kC / 16; ++kk)
-                            mma_ss(tmem + CF::tS, dkt + 128 * kk, dv + 128 * kk, id_KV, 1u);
-                        mma_commit(&sm.s_full);
                     }
 #pragma unroll
                     for (int kk = 0; kk < kC / 16; ++kk)
@@ -476,7 +534,7 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
                         mma_ss(tmem + CF::tO, kmajor(qa, kk), mnmajor(sb_addr, kk, lbo_sb), id_QS, kk > 0 ? 1u : 0u);
                         mma_ss(tmem + CF::tQZ, kmajor(qa, kk), wdesc(w_addr, kk), id_W, kk > 0 ? 1u : 0u);
                     }
-                    if (!(ok = wait_bar(abort_flag, &sm.p_full, cj & 1))) break;
+                    if (!(ok = wait_bar(abort_flag, &sm.p_full[0], cj & 1))) break;
                     tc_fence_after();
 #pragma unroll
                     for (int kk = 0; kk < kC / 16; ++kk) {
@@ -587,7 +645,6 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
                         bad = true;
                         break;
                     }
-                    __nanosleep(128);
                 }
             }
             if (lane == 0) {
@@ -665,55 +722,30 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
         if (!is_o) {
             // ------------------------------------------------------------ T -> P
             for (int cj = 0; cj < nch; ++cj) {
+                if constexpr (CF::kFused) {
+                    // P buffer cj % 2 and bf16 copy cj % 2 were last read by chunk cj - 2's
+                    // MMAs (o_full of that chunk); then the bf16 state for chunk cj (made
+                    // once chunk cj - 1's state update is done, which the MMA thread issues
+                    // before T(cj); the first chunk's came from phase B).
+                    if (cj >= 2 && !wait_bar_warp(abort_flag, &sm.o_full[cj & 1], ((cj >> 1) - 1) & 1)) break;
+                    if (cj >= 1 && !refresh_state<D>(sm, abort_flag, tl, i, row_ok, cj - 1)) break;
+                }
                 if (!wait_bar_warp(abort_flag, &sm.t_full, cj & 1)) break;
                 const uint32_t tPb = CF::tP + (cj & 1) * CF::kPStride;
                 tc_fence_after();
-                // This warp's rows are 32*quad .. 32*quad+31, so key block b (32 keys)
-                // is entirely visible for b < quad, masked on the diagonal for b ==
-                // quad, and entirely masked (zeros, no TMEM read) for b > quad.
-                {
-                    uint32_t t[32];
-                    uint32_t pk[16];
-#pragma unroll
-                    for (int b = 0; b < 4; ++b) {
-                        if (b <= quad) {
-                            tmem_ld32(tl + CF::tT + b * 32, t);
-                            tmem_ld_wait();
-                            if (b == quad) {
-#pragma unroll
-                                for (int e = 0; e < 16; ++e) {
-                                    const int jk = 2 * e;  // key offset within the diagonal block
-                                    pk[e] = pack_bf16(jk <= lane ? __uint_as_float(t[2 * e]) : 0.f,
-                                                      jk + 1 <= lane ? __uint_as_float(t[2 * e + 1]) : 0.f);
-                                }
-                            } else {
-#pragma unroll
-                                for (int e = 0; e < 16; ++e)
-                                    pk[e] = pack_bf16(__uint_as_float(t[2 * e]), __uint_as_float(t[2 * e + 1]));
-                            }
-                        } else {
-#pragma unroll
-                            for (int e = 0; e < 16; ++e) pk[e] = 0u;
-                        }
-                        if (!CF::kFused && b == 3) {  // all of T that this warp reads has been read
-                            tc_fence_before();
-                            mbar_arrive(&sm.t_free);
-                        }
-                        tmem_st16(tl + tPb + b * 16, pk);
-                    }
-                }
-                tmem_st_wait();
-                if constexpr (CF::kFused) {
-                    // p_full(cj) also stands for the bf16 state for chunk cj (copy cj % 2,
-                    // made here once chunk cj - 1's state update is done; the first chunk's
-                    // came from phase B) and for phi of chunk cj + 1.
-                    if (cj >= 1 && !refresh_state<D>(sm, abort_flag, tl, i, row_ok, cj - 1)) break;
+                // Fused layout: key blocks 0 and 3 here, 1 and 2 by the O warp of the same
+                // lane quadrant (no warp reads more than two blocks); D = 128: all four.
+                if constexpr (CF::kFused)
+                    convert_tp<D>(tl, tPb, quad, lane, 0x9u, nullptr);
+                else
+                    convert_tp<D>(tl, tPb, quad, lane, 0xFu, &sm.t_free);
+                if constexpr (CF::kFused) {  // p_full(cj) also stands for phi of chunk cj + 1
                     if (cj + 1 < nch && !wait_bar_warp(abort_flag, &sm.phi_done[(nA + cj + 1) % S],
                                                        ((nA + cj + 1) / S) & 1))
                         break;
                 }
                 tc_fence_before();
-                mbar_arrive(&sm.p_full);
+                mbar_arrive(&sm.p_full[CF::kFused ? (cj & 1) : 0]);
             }
         } else {
             // ------------------------------------------------------------ O out (, state refresh)
@@ -721,9 +753,24 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
             // slot -- Q is no longer read once O is final -- and written by a TMA
             // store, which clips rows past the end of the sequence.  With D = 128 these
             // warps then make the bf16 copy of the next chunk's state (after O, whose
-            // store frees the stage); the fused layout has the T -> P warps do it.
+            // store frees the stage); the fused layout has the T -> P warps do it, and
+            // these warps convert key blocks 1 and 2 of each T, which is ready (t_full
+            // of chunk it) before O of the chunk before it (o_full of chunk it - 1).
             const bool leader = (warp == kEpiOWarp0 && lane == 0);
-            for (int cj = 0; cj < nch; ++cj) {
+            for (int it = 0; it < nch + (CF::kFused ? 1 : 0); ++it) {
+                if constexpr (CF::kFused) {
+                    if (it < nch) {
+                        if (!wait_bar_warp(abort_flag, &sm.t_full, it & 1)) break;
+                        tc_fence_after();
+                        // (P buffer it % 2 is free: these warps saw o_full of chunk it - 2
+                        // in the previous iteration)
+                        convert_tp<D>(tl, CF::tP + (it & 1) * CF::kPStride, quad, lane, 0x6u, nullptr);
+                        tc_fence_before();
+                        mbar_arrive(&sm.p_full[it & 1]);
+                    }
+                    if (it == 0) continue;
+                }
+                const int cj = CF::kFused ? it - 1 : it;
                 const int s = (nA + cj) % S;
                 const int ob = CF::kFused ? (cj & 1) : 0;                       // O buffer
                 const uint32_t opar = CF::kFused ? ((cj >> 1) & 1) : (cj & 1);  // its phase
