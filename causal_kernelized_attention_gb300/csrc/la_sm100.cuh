@@ -169,6 +169,10 @@ __device__ __forceinline__ void fence_proxy_async_smem()
 {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
+// Release/acquire fence at GPU scope (lighter than the sequentially consistent
+// __threadfence, and all a release-acquire chain needs).
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
 // Orders generic-proxy accesses of global memory with later async-proxy (bulk copy) ones.
 __device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
 

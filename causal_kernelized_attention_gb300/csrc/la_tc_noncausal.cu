@@ -59,13 +59,33 @@ struct Item {
     int kind, bh, c0, nch, split;
 };
 
+// Column sums and z ride on the tensor cores in one of two ways (as in the
+// causal kernel):
+//  * fused (D = 64): the summary MMA's B operand is [V | 1] and the output MMA's
+//    is [S_bf16 | z], one N = D + 16 MMA whose second 64-wide block (an LBO away)
+//    is the ones block (column 0 = 1) or, for image slot m, the ones block's
+//    columns 16(m+1) and 16(m+1)+1 holding z_hi and z_lo;
+//  * separate (D = 128): N = 16 MMAs against W (summary: row 0 ones; output: the
+//    image's W, rows 1 and 2 = z_hi, z_lo).
 template <int D>
 struct Cfg {
+    static constexpr bool kFused = D == 64;
     static constexpr uint32_t kTileBytes = kC * D * 2;
-    static constexpr int kStages = D == 128 ? 2 : 6;        // a stage holds K and V, or Q and the staged O
+    static constexpr int kStages = D == 128 ? 2 : 5;        // a stage holds K and V, or Q and the staged O
     static constexpr int kImgs = D == 128 ? 1 : 2;          // state images held at once
     static constexpr uint32_t kSbBytes = D * D * 2;
-    static constexpr uint32_t kImgBytes = 2048 + kSbBytes;  // W (z rows) then the bf16 copy of S
+    // State image in global memory: fused = the bf16 copy of S, then z as D (hi, lo)
+    // bf16 pairs; separate = W (z rows) then the bf16 copy of S.  In shared memory a
+    // slot holds the S copy (fused; z goes to the ones block) or the whole image.
+    static constexpr uint32_t kImgBytes = kFused ? kSbBytes + 4 * D : 2048 + kSbBytes;
+    static constexpr uint32_t kSlotBytes = kFused ? kSbBytes : kImgBytes;
+    // aux: fused = image slots, then the ones block (after every tile it pairs with,
+    // so that LBOs are positive); separate = W (whose descriptor rows 8..15 alias into
+    // the image slot after it, feeding only unread columns), then the image slot.
+    static constexpr uint32_t kW = 0;
+    static constexpr uint32_t kImg0 = kFused ? 0 : 2048;
+    static constexpr uint32_t kOnes = kImg0 + kImgs * kSlotBytes;
+    static constexpr uint32_t kAuxBytes = kFused ? kOnes + kC * 128 : kOnes;
     // Accumulator buffers in TMEM: [S or O: D columns][z or qz: 16 columns].
     static constexpr uint32_t kAccStride = D == 128 ? 256 : 128;
     static constexpr int kAcc = 512 / kAccStride;
@@ -74,10 +94,7 @@ struct Cfg {
 template <int D>
 struct alignas(1024) Smem {
     uint8_t stage[Cfg<D>::kStages][2 * Cfg<D>::kTileBytes];
-    // Summary W: row 0 ones (column sums of phi(K)); rows 8..15 of its descriptor
-    // alias into img[0], which only feeds result columns that are never read.
-    uint8_t w1[2048];
-    uint8_t img[Cfg<D>::kImgs][Cfg<D>::kImgBytes];
+    uint8_t aux[Cfg<D>::kAuxBytes];
     uint64_t full[Cfg<D>::kStages], phi_done[Cfg<D>::kStages], empty[Cfg<D>::kStages];
     uint64_t item_full[kRing], item_empty[kRing];
     uint64_t acc_full[Cfg<D>::kAcc], acc_free[Cfg<D>::kAcc], o_staged[Cfg<D>::kAcc];
@@ -134,17 +151,19 @@ __device__ __forceinline__ Item decode_ticket(const Params &prm, int t)
     return it;
 }
 
-// Sums the head's P partials (in split order) and writes its state image:
-// bytes [0, 2048) are W (row 1 = z_hi, row 2 = z_lo, other rows zero) and bytes
-// [2048, 2048 + 2 D^2) the bf16 copy of S, MN-major, 128-byte swizzled.  Run by
-// the 128 epilogue threads; thread t takes state row t % D and a column range.
+// Sums the head's P partials (in split order) and writes its state image: the
+// bf16 copy of S (MN-major, 128-byte swizzled) and z -- fused: S copy at byte 0,
+// then (z_hi, z_lo) bf16 pairs; separate: W at byte 0 (row 1 = z_hi, row 2 = z_lo,
+// other rows zero), then the S copy.  Run by the 128 epilogue threads; thread t
+// takes state row t % D and a column range.  Two partials per round of loads.
 template <int D>
 __device__ __forceinline__ void build_image(const Params &prm, int bh, int t)
 {
+    using CF = Cfg<D>;
     constexpr int kGroups = 128 / D, kCols = D / kGroups;
     const size_t seg = (size_t)D * D + D;
     const float *part = prm.part + (size_t)bh * prm.P * seg;
-    uint8_t *img = prm.img + (size_t)bh * Cfg<D>::kImgBytes;
+    uint8_t *img = prm.img + (size_t)bh * CF::kImgBytes;
     const int i = t % D, grp = t / D;
 #pragma unroll 1
     for (int cc = 0; cc < kCols; cc += 32) {
@@ -152,8 +171,23 @@ __device__ __forceinline__ void build_image(const Params &prm, int bh, int t)
 #pragma unroll
         for (int e = 0; e < 32; ++e) acc[e] = 0.f;
         const int col0 = grp * kCols + cc;
-        for (int p = 0; p < prm.P; ++p) add_state<D>(acc, part + p * seg, col0 >> 2, i);
-        put_sb<D>(img + 2048, i, col0, acc);
+        int p = 0;
+        for (; p + 1 < prm.P; p += 2) {
+            add_state<D>(acc, part + p * seg, col0 >> 2, i);
+            add_state<D>(acc, part + (p + 1) * seg, col0 >> 2, i);
+        }
+        if (p < prm.P) add_state<D>(acc, part + p * seg, col0 >> 2, i);
+        put_sb<D>(img + (CF::kFused ? 0 : 2048), i, col0, acc);
+    }
+    if constexpr (CF::kFused) {
+        if (t < D) {
+            float zk = 0.f;
+            for (int q = 0; q < prm.P; ++q) zk += __ldcg(part + q * seg + (size_t)D * D + t);
+            const __nv_bfloat16 hi = __float2bfloat16_rn(zk);
+            const __nv_bfloat16 lo = __float2bfloat16_rn(zk - __bfloat162float(hi));
+            *reinterpret_cast<__nv_bfloat162 *>(img + CF::kSbBytes + 4 * t) = __halves2bfloat162(hi, lo);
+        }
+        return;
     }
     // W: thread t writes one 16-byte chunk (block t / 64, row (t / 8) % 8,
     // physical chunk t % 8, which holds logical chunk (t % 8) ^ row).
@@ -206,10 +240,19 @@ noncausal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
     Smem<D> &sm = *reinterpret_cast<Smem<D> *>(smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-    if (tid < 128) {  // w1: row 0 ones, everything else zero
-        const int blk = tid >> 6, within = tid & 63;
-        const uint32_t val = (within < 8) ? 0x3F803F80u : 0u;
-        *reinterpret_cast<uint4 *>(sm.w1 + blk * 1024 + within * 16) = make_uint4(val, val, val, val);
+    if (tid < 128) {
+        if constexpr (CF::kFused) {
+            // ones block: row r holds 1 in column 0 (physical 16-byte chunk r % 8), the
+            // rest zero (the z columns are written with each image)
+            for (int c = tid; c < kC * 8; c += 128) {
+                const uint32_t x = (c & 7) == ((c >> 3) & 7) ? 0x3F80u : 0u;
+                *reinterpret_cast<uint4 *>(sm.aux + CF::kOnes + c * 16) = make_uint4(x, 0u, 0u, 0u);
+            }
+        } else {  // W: row 0 ones, everything else zero
+            const int blk = tid >> 6, within = tid & 63;
+            const uint32_t val = (within < 8) ? 0x3F803F80u : 0u;
+            *reinterpret_cast<uint4 *>(sm.aux + CF::kW + blk * 1024 + within * 16) = make_uint4(val, val, val, val);
+        }
         fence_proxy_async_smem();
     }
     if (tid == 0) {
@@ -317,11 +360,13 @@ noncausal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
     } else if (warp == kMmaWarp) {
         // ---------------------------------------------------------------- MMA issuer
         if (lane == 0) {
-            const uint32_t id_KV = idesc_bf16_f32(128, D, true, true);    // phi(K)^T V
+            constexpr int NE = CF::kFused ? D + 16 : D;  // N of the MMAs against V or S
+            const uint32_t id_KV = idesc_bf16_f32(128, NE, true, true);   // phi(K)^T [V | 1]
             const uint32_t id_KW = idesc_bf16_f32(128, 16, true, false);  // phi(K)^T W^T
-            const uint32_t id_QS = idesc_bf16_f32(128, D, false, true);   // phi(Q) S_bf16
+            const uint32_t id_QS = idesc_bf16_f32(128, NE, false, true);  // phi(Q) [S_bf16 | z]
             const uint32_t id_QW = idesc_bf16_f32(128, 16, false, false); // phi(Q) W^T
-            const uint32_t w1 = smem_u32(sm.w1);
+            const uint32_t aux = smem_u32(sm.aux);
+            const uint32_t w1 = aux + CF::kW, ones = aux + CF::kOnes;
             int j = 0, q = 0, n_img = 0, cur_bh = -1, cur_m = 0;
             bool ok = true;
             for (int it = 0; ok; ++it) {
@@ -343,11 +388,13 @@ noncausal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
                         // phi(K)^T is MN-major with its second 64-row block one box on
                         // (for D = 64 that is the V tile: rows 64..127 are never read).
                         const uint32_t ka = smem_u32(sm.stage[s]), va = ka + kTile;
+                        const uint32_t lbo_v = CF::kFused ? ones - va : kBox;  // [V | 1] or V's second box
 #pragma unroll
                         for (int kk = 0; kk < kC / 16; ++kk) {
                             const uint32_t acc = (c > 0 || kk > 0) ? 1u : 0u;
-                            mma_ss(dS, mnmajor(ka, kk, kBox), mnmajor(va, kk, kBox), id_KV, acc);
-                            mma_ss(dZ, mnmajor(ka, kk, kBox), wdesc(w1, kk), id_KW, acc);
+                            mma_ss(dS, mnmajor(ka, kk, kBox), mnmajor(va, kk, lbo_v), id_KV, acc);
+                            if constexpr (!CF::kFused)
+                                mma_ss(dZ, mnmajor(ka, kk, kBox), wdesc(w1, kk), id_KW, acc);
                         }
                         mma_commit(&sm.empty[s]);
                     }
@@ -363,7 +410,11 @@ noncausal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
                         cur_m = m;
                         ++n_img;
                     }
-                    const uint32_t w2 = smem_u32(sm.img[cur_m]), sb = w2 + 2048;
+                    // separate: W then the S copy in the slot; fused: the S copy, its z in
+                    // the ones block's columns 16(m+1), 16(m+1)+1 (32(m+1) bytes on)
+                    const uint32_t slot = aux + CF::kImg0 + cur_m * CF::kSlotBytes;
+                    const uint32_t w2 = slot, sb = CF::kFused ? slot : slot + 2048;
+                    const uint32_t lbo_sb = CF::kFused ? ones + 32 * (cur_m + 1) - sb : D * 128;
                     for (int c = 0; c < item.nch; ++c, ++j, ++q) {
                         const int s = j % S, a = q % CF::kAcc;
                         if (!(ok = wait_bar(abort_flag, &sm.phi_done[s], (j / S) & 1))) break;
@@ -374,8 +425,9 @@ noncausal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
                         const uint32_t dO = tmem + a * CF::kAccStride, dQZ = dO + D;
 #pragma unroll
                         for (int kk = 0; kk < D / 16; ++kk) {
-                            mma_ss(dO, kmajor(qa, kk), mnmajor(sb, kk, D * 128), id_QS, kk > 0 ? 1u : 0u);
-                            mma_ss(dQZ, kmajor(qa, kk), wdesc(w2, kk), id_QW, kk > 0 ? 1u : 0u);
+                            mma_ss(dO, kmajor(qa, kk), mnmajor(sb, kk, lbo_sb), id_QS, kk > 0 ? 1u : 0u);
+                            if constexpr (!CF::kFused)
+                                mma_ss(dQZ, kmajor(qa, kk), wdesc(w2, kk), id_QW, kk > 0 ? 1u : 0u);
                         }
                         mma_commit(&sm.acc_full[a]);
                     }
@@ -419,8 +471,23 @@ noncausal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
                 }
                 if (!ok) break;
                 fence_proxy_async_global();
-                mbar_arrive_expect_tx(&sm.img_full[m], CF::kImgBytes);
-                bulk_load(sm.img[m], prm.img + (size_t)item.bh * CF::kImgBytes, CF::kImgBytes, &sm.img_full[m]);
+                const uint8_t *src = prm.img + (size_t)item.bh * CF::kImgBytes;
+                uint8_t *slot = sm.aux + CF::kImg0 + m * CF::kSlotBytes;
+                if constexpr (CF::kFused) {
+                    // z (hi, lo) pairs into the ones block's columns 16(m+1), 16(m+1)+1
+                    const uint4 *zs = reinterpret_cast<const uint4 *>(src + CF::kSbBytes);
+                    for (int x = 0; x < D / 4; ++x) {
+                        const uint4 z4 = __ldcg(zs + x);
+                        const uint32_t zz[4] = {z4.x, z4.y, z4.z, z4.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            *reinterpret_cast<uint32_t *>(sm.aux + CF::kOnes + sw128_offset(4 * x + e, 16 * (m + 1))) =
+                                zz[e];
+                    }
+                    fence_proxy_async_smem();
+                }
+                mbar_arrive_expect_tx(&sm.img_full[m], CF::kSlotBytes);
+                bulk_load(slot, src, CF::kSlotBytes, &sm.img_full[m]);
                 cur_bh = item.bh;
                 ++n_img;
             }
@@ -478,14 +545,14 @@ noncausal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
                 ++q;
                 j += item.nch;
                 // Count the split; the CTA that completes the head's last split builds its image.
-                __threadfence();
+                fence_acq_rel_gpu();
                 if (!epi_barrier(abort_flag, &sm.epi_sync, syncs)) break;
                 if (leader) sm.last = atom_add_acq_rel_gpu(prm.arrived + item.bh, 1u) == (uint32_t)(prm.P - 1);
                 if (!epi_barrier(abort_flag, &sm.epi_sync, syncs)) break;
                 if (sm.last) {
-                    __threadfence();
+                    fence_acq_rel_gpu();
                     build_image<D>(prm, item.bh, tid);
-                    __threadfence();
+                    fence_acq_rel_gpu();
                     fence_proxy_async_global();
                     if (!epi_barrier(abort_flag, &sm.epi_sync, syncs)) break;
                     if (leader) st_release_gpu(prm.ready + item.bh, 1u);
@@ -499,10 +566,13 @@ noncausal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
                     const uint32_t ta = tl + a * CF::kAccStride;
                     float inv;
                     {
-                        uint32_t qz[32];  // columns D + 1 and D + 2: phi(q) z_hi, phi(q) z_lo
+                        // phi(q) z_hi and phi(q) z_lo: fused in columns D, D + 1; separate
+                        // in columns D + 1, D + 2 (W rows 1 and 2)
+                        uint32_t qz[32];
                         tmem_ld32(ta + D, qz);
                         tmem_ld_wait();
-                        inv = 1.f / fmaxf(__uint_as_float(qz[1]) + __uint_as_float(qz[2]), prm.eps);
+                        constexpr int zc = CF::kFused ? 0 : 1;
+                        inv = 1.f / fmaxf(__uint_as_float(qz[zc]) + __uint_as_float(qz[zc + 1]), prm.eps);
                     }
                     uint8_t *ost = sm.stage[s] + kTile;  // the second tile of the stage stages O
 #pragma unroll 1
