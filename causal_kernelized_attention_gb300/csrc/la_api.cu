@@ -2,6 +2,7 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <algorithm>
 #include <atomic>
 #include <map>
 #include <mutex>
@@ -89,6 +90,38 @@ la_status flag_workspace(cudaStream_t s, size_t bytes, void **out)
         return cuda_status(e);
     }
     spaces[key] = p;
+    *out = p;
+    return LA_OK;
+}
+
+la_status data_workspace(cudaStream_t s, size_t bytes, void **out)
+{
+    *out = nullptr;
+    if (bytes == 0) return LA_OK;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_status(e);
+    static std::mutex mu;
+    static std::map<std::pair<int, cudaStream_t>, std::pair<void *, size_t>> spaces;
+    std::lock_guard<std::mutex> lock(mu);
+    const auto key = std::make_pair(dev, s);
+    auto it = spaces.find(key);
+    if (it != spaces.end() && it->second.second >= bytes) {
+        *out = it->second.first;
+        return LA_OK;
+    }
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    e = cudaStreamIsCapturing(s, &cs);
+    if (e != cudaSuccess) return cuda_status(e);
+    if (cs != cudaStreamCaptureStatusNone) return LA_ERR_UNSUPPORTED;
+    size_t size = it != spaces.end() ? std::max(bytes, 2 * it->second.second) : bytes;
+    size = (size + (2u << 20) - 1) / (2u << 20) * (2u << 20);
+    void *p = nullptr;
+    if (cudaMalloc(&p, size) != cudaSuccess) {
+        (void)cudaGetLastError();  // not sticky: the caller's per-call scratch may still fit
+        return LA_ERR_UNSUPPORTED;
+    }
+    spaces[key] = std::make_pair(p, size);  // an outgrown buffer stays allocated (see above)
     *out = p;
     return LA_OK;
 }

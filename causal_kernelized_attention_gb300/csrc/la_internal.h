@@ -67,6 +67,15 @@ void count_launches(unsigned n = 1);
 constexpr size_t kFlagWorkspaceBytes = 64 << 10;
 la_status flag_workspace(cudaStream_t s, size_t bytes, void **out);
 
+// Data workspace of the ticketed kernels (split partials, published states,
+// state images; contents need no clearing): one buffer per (device, stream),
+// grown outside capture to the largest request seen (at least doubling).  A
+// buffer it outgrows is kept, not freed, until the process exits, so a graph
+// captured against it stays valid.  Returns LA_ERR_UNSUPPORTED when it cannot
+// serve the call (a stream under capture whose buffer is too small, or the
+// allocation failed); the caller then uses per-call scratch.
+la_status data_workspace(cudaStream_t s, size_t bytes, void **out);
+
 // cudaFuncSetAttribute(MaxDynamicSharedMemorySize) once per kernel and device,
 // so that repeated calls (and stream capture) issue no attribute calls.
 la_status ensure_smem(const void *kernel, int bytes);

@@ -173,6 +173,17 @@ __device__ __forceinline__ void fence_proxy_async_smem()
 // __threadfence, and all a release-acquire chain needs).
 __device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 
+// Programmatic dependent launch.  launch_dependents: the next grid on the stream
+// (launched with programmatic stream serialization) may be scheduled once every
+// CTA of this grid has executed it or exited.  wait: blocks the thread until the
+// grids this one depends on have completed and their memory operations are
+// visible to this grid; it returns at once when there are none.
+__device__ __forceinline__ void griddep_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Orders generic-proxy accesses of global memory with later async-proxy (bulk copy) ones.
 __device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
 

@@ -284,18 +284,28 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
     Smem<D> &sm = *reinterpret_cast<Smem<D> *>(smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     uint8_t *const sb = sb_copy<D>(sm.aux, 0);  // phase B writes the state for the first chunk here
+    // The next launch on the stream may start its set-up now; it waits for this
+    // grid to complete before it touches global memory.
+    griddep_launch_dependents();
 
-    // The work ticket is taken first, its latency hidden behind the set-up.  A CTA
-    // that waits on an earlier ticket waits on a running CTA: no other CTA of this
-    // library fits on an SM beside one of this kernel (shared memory), so the TMEM
-    // allocation below can only wait on other kernels' CTAs, which never wait on it.
+    // The work ticket is taken first (once the grids this one depends on are done:
+    // the launch before may still be clearing the flags), its latency hidden behind
+    // the set-up.  A CTA that waits on an earlier ticket waits on a running CTA: no
+    // other CTA of this library fits on an SM beside one of this kernel (shared
+    // memory), so the TMEM allocation below can only wait on other kernels' CTAs,
+    // which never wait on it.  Every other thread reaches global memory after the
+    // set-up barrier, hence after this thread's griddep_wait.
     int my_ticket = 0;
-    if (tid == 0) my_ticket = (int)atomicAdd(prm.counter, 1u);
+    if (tid == 0) {
+        griddep_wait();
+        my_ticket = (int)atomicAdd(prm.counter, 1u);
+    }
     if (warp == kTmaWarp && lane == 0) {
         // While the ticket is out: warm L2 with the first tiles of segment blockIdx.x.
         // Every segment belongs to exactly one CTA, which reads these tiles first
         // (phase A's last chunks, or the first chunk when there is no phase A),
-        // whichever CTA draws that ticket.
+        // whichever CTA draws that ticket.  A prefetch is only a hint to L2 (the point
+        // of coherence), so it may run before the grid dependency is resolved.
         const int pg = (int)blockIdx.x / prm.BH, pbh = (int)blockIdx.x % prm.BH;
         const int pc0 = pg * prm.L, pn = min(prm.L, prm.n_chunks - pc0);
         const bool pa = pg < prm.G - 1;
@@ -878,19 +888,25 @@ la_status launch(const Problem &p)
     const size_t flag_bytes = ((items * 8 + 16) + 255) / 256 * 256;
     const size_t state_bytes = G > 1 ? 2 * items * ((size_t)D * D + D) * 4 : 0;
 
-    // Flags from the stream's workspace (already zero) when it can hold them, else
-    // from per-call scratch cleared by a memset.
-    void *ws = nullptr;
+    // Flags and published states from the stream's workspaces (flags already zero)
+    // when they can serve the call, else from per-call scratch (flags cleared by a
+    // memset).  With both workspaces, consecutive calls on the stream are kernel
+    // after kernel, which lets a launch overlap the tail of the one before it.
+    void *ws = nullptr, *data = nullptr;
     st = flag_workspace(p.stream, flag_bytes, &ws);
     if (st != LA_OK && st != LA_ERR_UNSUPPORTED) return st;
+    st = data_workspace(p.stream, state_bytes, &data);
+    if (st != LA_OK && st != LA_ERR_UNSUPPORTED) return st;
     const size_t own_flags = ws ? 0 : flag_bytes;
+    const size_t own_state = data ? 0 : state_bytes;
     Scratch scratch;
-    if (own_flags + state_bytes > 0) {
-        st = scratch.alloc(own_flags + state_bytes, p.stream);
+    if (own_flags + own_state > 0) {
+        st = scratch.alloc(own_flags + own_state, p.stream);
         if (st != LA_OK) return st;
     }
     uint8_t *base = (uint8_t *)scratch.ptr;
     uint8_t *flags = ws ? (uint8_t *)ws : base;
+    uint8_t *states = data ? (uint8_t *)data : base + own_flags;
     if (!ws) {
         cudaError_t e = cudaMemsetAsync(flags, 0, flag_bytes, p.stream);
         count_launches();
@@ -902,7 +918,7 @@ la_status launch(const Problem &p)
     prm.counter = (uint32_t *)flags;
     prm.incl_cnt = (uint32_t *)(flags + 16);
     prm.agg_cnt = prm.incl_cnt + items;
-    prm.incl = (float *)(base + own_flags);
+    prm.incl = (float *)states;
     prm.agg = prm.incl + (G > 1 ? items * ((size_t)D * D + D) : 0);
     prm.N = p.N;
     prm.BH = p.BH;
@@ -916,8 +932,7 @@ la_status launch(const Problem &p)
     st = ensure_smem((const void *)kern, smem);
     if (st != LA_OK) return st;
     count_launches();
-    kern<<<(unsigned)items, kThreads, smem, p.stream>>>(mq, mk, mv, mo, prm);
-    return cuda_status(cudaGetLastError());
+    return launch_dependent(kern, (unsigned)items, kThreads, smem, p.stream, mq, mk, mv, mo, prm);
 }
 
 }  // namespace

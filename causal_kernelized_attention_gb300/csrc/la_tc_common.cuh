@@ -222,6 +222,27 @@ inline la_status make_map(CUtensorMap *m, const void *ptr, int BH, int N, int D)
     return r == CUDA_SUCCESS ? LA_OK : cuda_status(cudaErrorInvalidValue);
 }
 
+// Launches a tensor-core kernel with programmatic stream serialization: its CTAs
+// may start (set-up, TMEM allocation) while the previous kernel on the stream
+// finishes; the kernel executes griddep_wait() before its first access to global
+// memory that an earlier launch may still write (inputs, flags, workspace).
+template <typename... Params, typename... Args>
+inline la_status launch_dependent(void (*kern)(Params...), unsigned grid, int threads, int smem, cudaStream_t s,
+                                  Args... args)
+{
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3(grid);
+    lc.blockDim = dim3((unsigned)threads);
+    lc.dynamicSmemBytes = (size_t)smem;
+    lc.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    lc.attrs = at;
+    lc.numAttrs = 1;
+    return cuda_status(cudaLaunchKernelEx(&lc, kern, args...));
+}
+
 inline int sm_count()
 {
     static std::mutex mu;

@@ -239,6 +239,9 @@ noncausal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
     }
     Smem<D> &sm = *reinterpret_cast<Smem<D> *>(smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // The next launch on the stream may start its set-up now; it waits for this
+    // grid to complete before it touches global memory.
+    griddep_launch_dependents();
 
     if (tid < 128) {
         if constexpr (CF::kFused) {
@@ -283,6 +286,9 @@ noncausal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
         tmem_alloc(&sm.tmem_base, 512);
         tmem_relinquish();
     }
+    // Global memory only after the grids this one depends on are done (the launch
+    // before may still be clearing the flags or reading the workspace).
+    griddep_wait();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -544,8 +550,10 @@ noncausal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
                 mbar_arrive(&sm.acc_free[a]);
                 ++q;
                 j += item.nch;
-                // Count the split; the CTA that completes the head's last split builds its image.
-                fence_acq_rel_gpu();
+                // Count the split; the CTA that completes the head's last split builds its
+                // image.  The barrier (mbarrier arrive/wait: release/acquire at CTA scope)
+                // orders every thread's partial writes before the leader's acq_rel atomic,
+                // whose release is cumulative: no fence per thread is needed.
                 if (!epi_barrier(abort_flag, &sm.epi_sync, syncs)) break;
                 if (leader) sm.last = atom_add_acq_rel_gpu(prm.arrived + item.bh, 1u) == (uint32_t)(prm.P - 1);
                 if (!epi_barrier(abort_flag, &sm.epi_sync, syncs)) break;
@@ -668,17 +676,25 @@ la_status launch(const Problem &p)
     const size_t part_bytes = ((size_t)p.BH * P * seg * 4 + 255) / 256 * 256;
     const size_t img_bytes = (size_t)p.BH * CF::kImgBytes;
 
-    // Flags from the stream's workspace (already zero) when it can hold them, else
-    // from per-call scratch cleared by a memset.
-    void *ws = nullptr;
+    // Flags, partials and images from the stream's workspaces (flags already zero)
+    // when they can serve the call, else from per-call scratch (flags cleared by a
+    // memset).  With both workspaces, consecutive calls on the stream are kernel
+    // after kernel, which lets a launch overlap the tail of the one before it.
+    void *ws = nullptr, *data = nullptr;
     st = flag_workspace(p.stream, flag_bytes, &ws);
     if (st != LA_OK && st != LA_ERR_UNSUPPORTED) return st;
+    st = data_workspace(p.stream, part_bytes + img_bytes, &data);
+    if (st != LA_OK && st != LA_ERR_UNSUPPORTED) return st;
     const size_t own_flags = ws ? 0 : flag_bytes;
+    const size_t own_data = data ? 0 : part_bytes + img_bytes;
     Scratch scratch;
-    st = scratch.alloc(own_flags + part_bytes + img_bytes, p.stream);
-    if (st != LA_OK) return st;
+    if (own_flags + own_data > 0) {
+        st = scratch.alloc(own_flags + own_data, p.stream);
+        if (st != LA_OK) return st;
+    }
     uint8_t *base = (uint8_t *)scratch.ptr;
     uint8_t *flags = ws ? (uint8_t *)ws : base;
+    uint8_t *work = data ? (uint8_t *)data : base + own_flags;
     if (!ws) {
         cudaError_t e = cudaMemsetAsync(flags, 0, flag_bytes, p.stream);
         count_launches();
@@ -689,8 +705,8 @@ la_status launch(const Problem &p)
     prm.ticket = (uint32_t *)flags;
     prm.arrived = (uint32_t *)(flags + 16);
     prm.ready = prm.arrived + p.BH;
-    prm.part = (float *)(base + own_flags);
-    prm.img = base + own_flags + part_bytes;
+    prm.part = (float *)work;
+    prm.img = work + part_bytes;
     prm.N = p.N;
     prm.BH = p.BH;
     prm.n_chunks = n_chunks;
@@ -706,8 +722,7 @@ la_status launch(const Problem &p)
     if (st != LA_OK) return st;
     const unsigned grid = (unsigned)std::min<long long>(items, n_sm);
     count_launches();
-    kern<<<grid, kThreads, smem, p.stream>>>(mq, mk, mv, mo, prm);
-    return cuda_status(cudaGetLastError());
+    return launch_dependent(kern, grid, kThreads, smem, p.stream, mq, mk, mv, mo, prm);
 }
 
 }  // namespace

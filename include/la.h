@@ -31,8 +31,24 @@
  *    non-finite eps give LA_ERR_INVALID_ARG.  Sizes the kernels are not built
  *    for give LA_ERR_UNSUPPORTED (see each function).
  *  - o must not overlap q, k or v.
- *  - Scratch memory, where a path needs it, is allocated and freed
- *    stream-ordered (cudaMallocAsync / cudaFreeAsync on `stream`).
+ *  - Scratch memory.  The bf16 tensor-core forward paths keep two workspaces
+ *    per (device, stream): 64 KB of work tickets and flags, zeroed once and
+ *    left zeroed by every launch, and a data buffer (split partials,
+ *    published states) grown to the largest problem seen on that stream.
+ *    Both are created or grown only outside stream capture, with cudaMalloc,
+ *    and are kept until the process exits (a grown-out buffer too, so that a
+ *    graph captured against it stays valid).  When a workspace cannot serve a
+ *    call (first call during capture, or a larger problem during capture),
+ *    that call allocates and frees its scratch stream-ordered
+ *    (cudaMallocAsync / cudaFreeAsync on `stream`) instead, as every other
+ *    path does.  Calls on one stream are ordered, so they never use a
+ *    workspace at the same time; a graph replays with the workspaces of the
+ *    stream it was captured on, so do not replay it while other work of this
+ *    library runs on that stream, nor replay two of its instances at once.
+ *  - The tensor-core forward kernels are launched with programmatic stream
+ *    serialization: a launch may begin its set-up while the kernel before it
+ *    on the stream finishes, and waits for that kernel to complete before it
+ *    reads any global memory.
  */
 #ifndef LA_H
 #define LA_H

@@ -367,3 +367,50 @@ def test_ticketed_kernels_under_graph_capture(orc, warm):
             assert_parity(from_dev(x), ref_c, "bf16", ("graph causal", warm, rep))
         for x in outs_n:
             assert_noncausal_parity(from_dev(x), ref_n, "bf16", ("graph noncausal", warm, rep))
+
+
+def test_data_workspace_growth_and_capture_fallback(orc):
+    """The per-stream data workspace (partials, published states) is sized by the
+    first small problem.  A capture that needs more uses per-call scratch (with
+    the flags still from the workspace); an eager call of that size grows the
+    workspace; a graph captured against the outgrown buffer still replays."""
+    cases = {"small": workloads.random_inputs(5151, 1, 2, 1024, 64, 64, "bf16"),
+             "big": workloads.random_inputs(5252, 4, 8, 4096, 64, 64, "bf16")}
+    ref = {n: (orc.causal_recurrent(*x), orc.noncausal(*x)) for n, x in cases.items()}
+    dev = {n: [to_dev(t, "bf16") for t in x] for n, x in cases.items()}
+    outs = {n: [torch.empty_like(dev[n][2]) for _ in range(2)] for n in cases}
+    s = torch.cuda.Stream()
+
+    def calls(n):
+        q, k, v = dev[n]
+        la().la_forward_causal(q, k, v, outs[n][0])
+        la().la_forward_noncausal(q, k, v, outs[n][1])
+
+    def check(n, tag):
+        torch.cuda.synchronize()
+        assert la().la_get_device_status() == 0
+        assert_parity(from_dev(outs[n][0]), ref[n][0], "bf16", (tag, n, "causal"))
+        assert_noncausal_parity(from_dev(outs[n][1]), ref[n][1], "bf16", (tag, n, "noncausal"))
+        for x in outs[n]:
+            x.fill_(float("nan"))
+
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        calls("small")
+    check("small", "eager")
+    graphs = {n: torch.cuda.CUDAGraph() for n in cases}
+    for n in ("small", "big"):
+        with torch.cuda.graph(graphs[n], stream=s):
+            calls(n)
+    for n in ("big", "small"):
+        with torch.cuda.stream(s):
+            graphs[n].replay()
+        check(n, "replay before growth")
+    with torch.cuda.stream(s):
+        calls("big")
+    check("big", "eager growth")
+    for rep in range(2):
+        for n in ("small", "big"):
+            with torch.cuda.stream(s):
+                graphs[n].replay()
+            check(n, ("replay after growth", rep))
