@@ -241,6 +241,12 @@ la_status la_prefill_state(const void *k, const void *v, float *S, float *z, int
     if (!supported_dim(dk) || !supported_dim(dv)) return LA_ERR_UNSUPPORTED;
     const size_t BH = (size_t)B * H;
     if (overlaps(S, BH * dk * dv * 4, z, BH * dk * 4)) return LA_ERR_INVALID_ARG;
+    // bf16 with dk = dv in {64, 128}: the summary phase of the tensor-core non-causal
+    // kernel (the final causal state is the non-causal state of the prefix).
+    if (dtype == LA_BF16 && dk == dv && (dk == 64 || dk == 128) && N >= 128) {
+        const la_status st = noncausal_tc_state(k, v, S, z, (int)BH, N, dk, (cudaStream_t)stream);
+        if (st != LA_ERR_UNSUPPORTED) return st;
+    }
     return state_simt(k, v, S, z, (int)BH, N, dk, dv, dtype, (cudaStream_t)stream);
 }
 

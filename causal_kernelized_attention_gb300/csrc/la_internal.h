@@ -45,6 +45,10 @@ la_status decode_step(float *S, float *z, const void *q, const void *k, const vo
 la_status causal_tc(const Problem &p);
 // (la_tc_noncausal.cu)
 la_status noncausal_tc(const Problem &p);
+// S, z (fp32, [BH,D,D], [BH,D]) = sums over N tokens on the tensor cores (bf16
+// k, v; D in {64, 128}, N >= 128); overwrites S and z.
+la_status noncausal_tc_state(const void *k, const void *v, float *S, float *z, int BH, int N, int D,
+                             cudaStream_t stream);
 
 // Device status words of translation units that run bounded waits: read and clear.
 la_status tc_causal_read_status(cudaStream_t s, unsigned *bits);

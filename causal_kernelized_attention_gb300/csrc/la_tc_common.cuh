@@ -125,6 +125,51 @@ __device__ __forceinline__ void phi_tile(uint8_t *tile, int t, int valid)
     }
 }
 
+// phi of two bf16 values in fp32, split into bf16 high parts (returned) and the
+// bf16 rounding of the remainders (*lo): hi + lo carries phi to about 2^-17.
+__device__ __forceinline__ uint32_t phi2_split(uint32_t w, uint32_t *lo)
+{
+    const __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162 *>(&w);
+    const float a = __bfloat162float(x.x), b = __bfloat162float(x.y);
+    const float pa = a > 0.f ? a + 1.f : __expf(a), pb = b > 0.f ? b + 1.f : __expf(b);
+    const __nv_bfloat16 ha = __float2bfloat16_rn(pa), hb = __float2bfloat16_rn(pb);
+    const __nv_bfloat162 l = __floats2bfloat162_rn(pa - __bfloat162float(ha), pb - __bfloat162float(hb));
+    *lo = *reinterpret_cast<const uint32_t *>(&l);
+    const __nv_bfloat162 h = __halves2bfloat162(ha, hb);
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+// As phi_tile, with phi split: the high parts in place, the low parts at the
+// same offsets of `lo` (a tile of the same layout).
+template <int D, int NT>
+__device__ __forceinline__ void phi_tile_split(uint8_t *tile, uint8_t *lo, int t, int valid)
+{
+    constexpr int kUnits = 128 * (D / 32);
+    constexpr int NU = (kUnits + NT - 1) / NT;
+#pragma unroll 1
+    for (int m = 0; m < NU; ++m) {
+        const int u = t + NT * m, row = u & 127, hb = u >> 7;
+        if (u >= kUnits) break;
+        const uint32_t off = (hb >> 1) * kBox + row * 128;
+        const int rot = row + (hb & 1) * 4;
+        uint4 x[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) x[k] = *reinterpret_cast<const uint4 *>(tile + off + ((rot + k) & 7) * 16);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            uint4 h = make_uint4(0u, 0u, 0u, 0u), l = make_uint4(0u, 0u, 0u, 0u);
+            if (row < valid) {
+                h.x = phi2_split(x[k].x, &l.x);
+                h.y = phi2_split(x[k].y, &l.y);
+                h.z = phi2_split(x[k].z, &l.z);
+                h.w = phi2_split(x[k].w, &l.w);
+            }
+            *reinterpret_cast<uint4 *>(tile + off + ((rot + k) & 7) * 16) = h;
+            *reinterpret_cast<uint4 *>(lo + off + ((rot + k) & 7) * 16) = l;
+        }
+    }
+}
+
 // Descriptor helpers (see la_sm100.cuh for the layouts).
 __device__ __forceinline__ uint64_t kmajor(uint32_t tile, int kk)
 {

@@ -23,6 +23,12 @@
 //    the head changes); per query chunk O = phi(Q_c) S_bf16 and
 //    qz = phi(Q_c)(z_hi + z_lo) on the tensor cores; o = O / max(qz, eps),
 //    rounded to bf16 in shared memory and written by a TMA store.
+//  * State mode (the prefill state of a prefix; no output items): the sums are
+//    written as fp32 S and z -- by the split's own epilogue when a head has one
+//    split, else by the CTA that completes the head's last split.  phi(K) is
+//    evaluated in fp32 and split into bf16 high and low parts, each multiplied
+//    by [V | 1] (or V and W), so the state is accurate to about 2^-17 relative
+//    to fp32 phi rather than to bf16 rounding.
 //
 // Warp roles (512 threads): warps 0-3 epilogue (TMEM lane quadrant = warp),
 // warp 4 scheduler and TMA producer, warp 5 MMA issuer and TMEM owner, warp 6
@@ -100,6 +106,7 @@ struct alignas(1024) Smem {
     uint64_t acc_full[Cfg<D>::kAcc], acc_free[Cfg<D>::kAcc], o_staged[Cfg<D>::kAcc];
     uint64_t img_full[Cfg<D>::kImgs], img_empty[Cfg<D>::kImgs];
     uint64_t epi_sync, drain;
+    uint64_t lo_free;  // state mode: the MMAs of a tile's low phi parts have read them
     Item items[kRing];
     uint32_t tmem_base;
     int abort;
@@ -108,6 +115,9 @@ struct alignas(1024) Smem {
 };
 
 static_assert(sizeof(Smem<128>) <= 232448, "exceeds the 227 KB per-CTA shared memory limit");
+// State mode keeps the low phi parts of a key tile in the image slots.
+static_assert(Cfg<64>::kImgs * Cfg<64>::kSlotBytes >= Cfg<64>::kTileBytes, "no room for the low phi parts");
+static_assert(Cfg<128>::kImgs * Cfg<128>::kSlotBytes >= Cfg<128>::kTileBytes, "no room for the low phi parts");
 static_assert(sizeof(Smem<64>) <= 232448, "exceeds the 227 KB per-CTA shared memory limit");
 
 struct Params {
@@ -120,6 +130,9 @@ struct Params {
     int P, L1;           // splits per head, key chunks per split
     int T, L2;           // output items per head, query chunks per item
     float eps;
+    // State mode (T = 0, no output items): the sums are written to S_out [BH, D, D]
+    // (row = key feature) and z_out [BH, D], fp32, row-major; null otherwise.
+    float *S_out, *z_out;
 };
 
 __device__ __forceinline__ bool wait_bar(int *abort_flag, uint64_t *bar, uint32_t parity)
@@ -212,6 +225,39 @@ __device__ __forceinline__ void build_image(const Params &prm, int bh, int t)
     *reinterpret_cast<uint4 *>(img + blk * 1024 + row * 128 + (t & 7) * 16) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
 }
 
+// State mode: sums the head's P partials in split order and writes S (fp32,
+// [D, D] row-major, row = key feature) and z (fp32, [D]).  Run by the 128
+// epilogue threads; thread t takes row t % D and a column range.
+template <int D>
+__device__ __forceinline__ void write_state(const Params &prm, int bh, int t)
+{
+    constexpr int kGroups = 128 / D, kCols = D / kGroups;
+    const size_t seg = (size_t)D * D + D;
+    const float *part = prm.part + (size_t)bh * prm.P * seg;
+    const int i = t % D, grp = t / D;
+#pragma unroll 1
+    for (int cc = 0; cc < kCols; cc += 32) {
+        float acc[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) acc[e] = 0.f;
+        const int col0 = grp * kCols + cc;
+        int p = 0;
+        for (; p + 1 < prm.P; p += 2) {
+            add_state<D>(acc, part + p * seg, col0 >> 2, i);
+            add_state<D>(acc, part + (p + 1) * seg, col0 >> 2, i);
+        }
+        if (p < prm.P) add_state<D>(acc, part + p * seg, col0 >> 2, i);
+        float4 *dst = reinterpret_cast<float4 *>(prm.S_out + ((size_t)bh * D + i) * D + col0);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) dst[e] = make_float4(acc[4 * e], acc[4 * e + 1], acc[4 * e + 2], acc[4 * e + 3]);
+    }
+    if (t < D) {
+        float zk = 0.f;
+        for (int q = 0; q < prm.P; ++q) zk += __ldcg(part + q * seg + (size_t)D * D + t);
+        prm.z_out[(size_t)bh * D + t] = zk;
+    }
+}
+
 // The epilogue threads' barrier: an mbarrier of 128 arrivals, waited on with a
 // bound (a thread can arrive for the next use only after the current use has
 // completed, so the phases never mix).
@@ -278,6 +324,7 @@ noncausal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
             mbar_init(&sm.img_empty[m], 1);
         }
         mbar_init(&sm.epi_sync, kEpiThreads);
+        mbar_init(&sm.lo_free, 1);
         mbar_init(&sm.drain, 1);
         sm.abort = 0;
         fence_mbar_init();
@@ -311,7 +358,16 @@ noncausal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
                 const int s = j % S;
                 if (!(ok = wait_bar_warp(abort_flag, &sm.full[s], (j / S) & 1))) break;
                 // K (summary) or Q (output) is the first tile of the stage.
-                phi_tile<D, kPhiThreads>(sm.stage[s], t, prm.N - (item.c0 + c) * kC);
+                const int valid = prm.N - (item.c0 + c) * kC;
+                if (prm.S_out) {
+                    // State mode: phi in fp32, split into bf16 high parts (in place) and
+                    // low parts (in the unused image slots), once the previous tile's
+                    // MMAs have read the low parts.
+                    if (j > 0 && !(ok = wait_bar_warp(abort_flag, &sm.lo_free, (j - 1) & 1))) break;
+                    phi_tile_split<D, kPhiThreads>(sm.stage[s], sm.aux + CF::kImg0, t, valid);
+                } else {
+                    phi_tile<D, kPhiThreads>(sm.stage[s], t, valid);
+                }
                 fence_proxy_async_smem();
                 mbar_arrive(&sm.phi_done[s]);
             }
@@ -401,6 +457,16 @@ noncausal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
                             mma_ss(dS, mnmajor(ka, kk, kBox), mnmajor(va, kk, lbo_v), id_KV, acc);
                             if constexpr (!CF::kFused)
                                 mma_ss(dZ, mnmajor(ka, kk, kBox), wdesc(w1, kk), id_KW, acc);
+                        }
+                        if (prm.S_out) {  // state mode: the low phi parts against the same V (and 1)
+                            const uint32_t la = aux + CF::kImg0;
+#pragma unroll
+                            for (int kk = 0; kk < kC / 16; ++kk) {
+                                mma_ss(dS, mnmajor(la, kk, kBox), mnmajor(va, kk, lbo_v), id_KV, 1u);
+                                if constexpr (!CF::kFused)
+                                    mma_ss(dZ, mnmajor(la, kk, kBox), wdesc(w1, kk), id_KW, 1u);
+                            }
+                            mma_commit(&sm.lo_free);
                         }
                         mma_commit(&sm.empty[s]);
                     }
@@ -528,13 +594,21 @@ noncausal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
                 if (!wait_bar_warp(abort_flag, &sm.acc_full[a], (q / CF::kAcc) & 1)) break;
                 tc_fence_after();
                 const uint32_t ta = tl + a * CF::kAccStride;
+                // State mode with one split per head: the sums go straight to S_out, z_out.
+                const bool state_now = prm.S_out != nullptr && prm.P == 1;
                 float *dst = prm.part + ((size_t)item.bh * prm.P + item.split) * seg;
 #pragma unroll 1
                 for (int cc = 0; cc < D; cc += 32) {
                     uint32_t v[32];
                     tmem_ld32(ta + cc, v);
                     tmem_ld_wait();
-                    if (i < D) {
+                    if (i < D && state_now) {
+                        float4 *d4 = reinterpret_cast<float4 *>(prm.S_out + ((size_t)item.bh * D + i) * D + cc);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            d4[e] = make_float4(__uint_as_float(v[4 * e]), __uint_as_float(v[4 * e + 1]),
+                                                __uint_as_float(v[4 * e + 2]), __uint_as_float(v[4 * e + 3]));
+                    } else if (i < D) {
                         float4 *d4 = reinterpret_cast<float4 *>(dst);
 #pragma unroll
                         for (int e = 0; e < 8; ++e)
@@ -545,11 +619,17 @@ noncausal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
                 }
                 const float zs = __uint_as_float(tmem_ld1(ta + D));
                 tmem_ld_wait();
-                if (i < D) dst[(size_t)D * D + i] = zs;
+                if (i < D) {
+                    if (state_now)
+                        prm.z_out[(size_t)item.bh * D + i] = zs;
+                    else
+                        dst[(size_t)D * D + i] = zs;
+                }
                 tc_fence_before();
                 mbar_arrive(&sm.acc_free[a]);
                 ++q;
                 j += item.nch;
+                if (state_now) continue;
                 // Count the split; the CTA that completes the head's last split builds its
                 // image.  The barrier (mbarrier arrive/wait: release/acquire at CTA scope)
                 // orders every thread's partial writes before the leader's acq_rel atomic,
@@ -557,7 +637,10 @@ noncausal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
                 if (!epi_barrier(abort_flag, &sm.epi_sync, syncs)) break;
                 if (leader) sm.last = atom_add_acq_rel_gpu(prm.arrived + item.bh, 1u) == (uint32_t)(prm.P - 1);
                 if (!epi_barrier(abort_flag, &sm.epi_sync, syncs)) break;
-                if (sm.last) {
+                if (sm.last && prm.S_out) {  // state mode: the sums are the result
+                    fence_acq_rel_gpu();
+                    write_state<D>(prm, item.bh, tid);
+                } else if (sm.last) {
                     fence_acq_rel_gpu();
                     build_image<D>(prm, item.bh, tid);
                     fence_acq_rel_gpu();
@@ -648,14 +731,17 @@ noncausal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
 
 // ------------------------------------------------------------------ host side
 template <int D>
-la_status launch(const Problem &p)
+la_status launch(const Problem &p, float *S_out = nullptr, float *z_out = nullptr)
 {
     using CF = Cfg<D>;
+    // State mode (S_out given): summary items only; the q and o maps are never used
+    // and are built on k.
+    const bool state = S_out != nullptr;
     CUtensorMap mq, mk, mv, mo;
-    la_status st = make_map(&mq, p.q, p.BH, p.N, D);
+    la_status st = make_map(&mq, state ? p.k : p.q, p.BH, p.N, D);
     if (st == LA_OK) st = make_map(&mk, p.k, p.BH, p.N, D);
     if (st == LA_OK) st = make_map(&mv, p.v, p.BH, p.N, D);
-    if (st == LA_OK) st = make_map(&mo, p.o, p.BH, p.N, D);
+    if (st == LA_OK) st = make_map(&mo, state ? p.k : p.o, p.BH, p.N, D);
     if (st != LA_OK) return st;
 
     const int n_chunks = ceil_div(p.N, kC);
@@ -665,16 +751,20 @@ la_status launch(const Problem &p)
     int P = std::min(std::min(32, n_chunks), std::max(1, ceil_div(2 * n_sm, p.BH)));
     const int L1 = ceil_div(n_chunks, P);
     P = ceil_div(n_chunks, L1);
-    int T = std::min(n_chunks, std::max(1, ceil_div(4 * n_sm, p.BH)));
-    const int L2 = ceil_div(n_chunks, T);
-    T = ceil_div(n_chunks, L2);
+    int T = 0, L2 = 1;
+    if (!state) {
+        T = std::min(n_chunks, std::max(1, ceil_div(4 * n_sm, p.BH)));
+        L2 = ceil_div(n_chunks, T);
+        T = ceil_div(n_chunks, L2);
+    }
     const long long items = (long long)p.BH * (P + T);
     if (items > 0x7fffffffLL) return LA_ERR_UNSUPPORTED;
 
     const size_t seg = (size_t)D * D + D;
     const size_t flag_bytes = ((16 + (size_t)p.BH * 8) + 255) / 256 * 256;
-    const size_t part_bytes = ((size_t)p.BH * P * seg * 4 + 255) / 256 * 256;
-    const size_t img_bytes = (size_t)p.BH * CF::kImgBytes;
+    // (state mode with one split per head writes the sums directly: no partials)
+    const size_t part_bytes = state && P == 1 ? 0 : ((size_t)p.BH * P * seg * 4 + 255) / 256 * 256;
+    const size_t img_bytes = state ? 0 : (size_t)p.BH * CF::kImgBytes;
 
     // Flags, partials and images from the stream's workspaces (flags already zero)
     // when they can serve the call, else from per-call scratch (flags cleared by a
@@ -715,6 +805,8 @@ la_status launch(const Problem &p)
     prm.T = T;
     prm.L2 = L2;
     prm.eps = p.eps;
+    prm.S_out = S_out;
+    prm.z_out = z_out;
 
     const int smem = (int)sizeof(Smem<D>);
     auto kern = noncausal_tc_kernel<D>;
@@ -732,6 +824,25 @@ la_status noncausal_tc(const Problem &p)
     if (p.dtype != LA_BF16 || p.dk != p.dv || (p.dk != 64 && p.dk != 128) || p.N < kC)
         return LA_ERR_UNSUPPORTED;
     return p.dk == 128 ? launch<128>(p) : launch<64>(p);
+}
+
+la_status noncausal_tc_state(const void *k, const void *v, float *S, float *z, int BH, int N, int D,
+                             cudaStream_t stream)
+{
+    if ((D != 64 && D != 128) || N < kC) return LA_ERR_UNSUPPORTED;
+    Problem p{};
+    p.q = k;
+    p.k = k;
+    p.v = v;
+    p.o = nullptr;
+    p.BH = BH;
+    p.N = N;
+    p.dk = p.dv = D;
+    p.chunk = kC;
+    p.eps = 0.f;
+    p.dtype = LA_BF16;
+    p.stream = stream;
+    return D == 128 ? launch<128>(p, S, z) : launch<64>(p, S, z);
 }
 
 la_status tc_noncausal_read_status(cudaStream_t s, unsigned *bits)

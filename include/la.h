@@ -162,7 +162,11 @@ la_status la_decode_step(float *S, float *z, const void *q, const void *k, const
  *   k : [B, H, N, dk]   v : [B, H, N, dv]   S : [B, H, dk, dv] fp32   z : [B, H, dk] fp32
  *
  * S and z are OVERWRITTEN (not accumulated).  N = 0 writes zeros.
- * Supported: dk, dv in {32, 64, 128}.
+ * Supported: dk, dv in {32, 64, 128}.  bf16 with dk = dv in {64, 128} and
+ * N >= 128 runs on the tensor cores: phi(k) is evaluated in fp32 and split into
+ * a bf16 high part and a bf16 low part (together accurate to about 2^-17), both
+ * multiplied by v with fp32 accumulation; other shapes use fp32 CUDA-core
+ * arithmetic.
  */
 la_status la_prefill_state(const void *k, const void *v, float *S, float *z,
                            int B, int H, int N, int dk, int dv, la_dtype dtype,

@@ -213,6 +213,22 @@ def test_prefill_state(orc, dtype, N, dk, dv):
     assert errors(S, Sr)["normwise"] < 1e-5 and errors(z, zr)["normwise"] < 1e-5
 
 
+# bf16 prefill states on the tensor cores (phi split into bf16 high and low
+# parts): one key split per head, written by the split itself (320 heads), and
+# many splits per head summed by the last one (2 heads x 2000 tokens); ragged
+# last chunks.  Held to the fp32 bar, like the CUDA-core path.
+@pytest.mark.parametrize("B,H,N,d", [(16, 20, 130, 64), (16, 20, 256, 128), (1, 2, 2000, 64), (1, 2, 1500, 128),
+                                     (3, 5, 700, 64)])
+def test_prefill_state_tensor_core(orc, B, H, N, d):
+    _, k, v = workloads.random_inputs(3300 + N + d, B, H, N, d, d, "bf16")
+    S, z = la().la_prefill_state(to_dev(k, "bf16"), to_dev(v, "bf16"))
+    torch.cuda.synchronize()
+    assert la().la_get_device_status() == 0
+    Sr, zr = orc.prefill_state(k, v)
+    eS, ez = errors(from_dev(S), Sr), errors(from_dev(z), zr)
+    assert eS["normwise"] < 1e-5 and ez["normwise"] < 1e-5, (B, H, N, d, eS, ez)
+
+
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("dk,dv", [(32, 32), (64, 128), (128, 64), (128, 128)])
 def test_decode_small(orc, dtype, dk, dv):
