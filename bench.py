@@ -427,6 +427,29 @@ def bench_path_decode(torch, la, steps, peaks, src):
             "l2": "state 270 MB > L2"}
 
 
+def bench_path_prefill(torch, la, reps, peaks, src):
+    """la_prefill_state on the decode workload's prefill (k, v 1.07 GB > L2): S, z
+    fp32 sums over 512 tokens of 4096 heads at d = 128."""
+    w = workloads.DECODE_BF16
+    (qp, kp, vp), (qd, kd, vd) = workloads.device_decode_inputs(w)
+    del qp, qd, kd, vd
+    S = torch.empty((w.B, w.H, w.dk, w.dv), dtype=torch.float32, device="cuda")
+    z = torch.empty((w.B, w.H, w.dk), dtype=torch.float32, device="cuda")
+
+    def step(i):
+        la.la_prefill_state(kp, vp, S, z)
+
+    secs, launches, _ = time_graph_steps(torch, la, step, reps, 3, Dist())
+    t = secs / reps
+    nbytes = w.BH * w.N * (w.dk + w.dv) * 2 + w.BH * w.dk * (w.dv + 1) * 4
+    fl = 2.0 * w.BH * w.N * w.dk * (w.dv + 1)
+    return {"workload": "prefill_state_bf16_b%d_h%d_n%d_d%d" % (w.B, w.H, w.N, w.dk),
+            "value": round(w.B * w.N / t, 1), "unit": "tokens/s", "ms_per_step": round(t * 1e3, 4),
+            "launches_per_step": launches / reps,
+            "roofline": roofline(fl, nbytes, t, peaks, src, ncu_traffic("prefill_state")),
+            "l2": "k, v 1.07 GB > L2"}
+
+
 # --------------------------------------------------------------------------- CPU oracle
 def oracle_causal_sample(w, target_s=10.0, max_reps=100000):
     """The float64 oracle (as it stands) on a bounded sample of workload w:
@@ -522,6 +545,7 @@ def run_gpu(args, dist):
         paths["causal_long"] = bench_path_causal_long(torch, la, args.path_reps, peaks, src)
         paths["noncausal"] = bench_path_noncausal(torch, la, max(args.path_reps, 20), peaks, src)
         paths["decode"] = bench_path_decode(torch, la, 1024, peaks, src)
+        paths["prefill_state"] = bench_path_prefill(torch, la, max(args.path_reps, 20), peaks, src)
         if s2:
             paths["clocks"] = s2.stop(window=(t_paths, time.time()))
 
@@ -553,14 +577,16 @@ def run_gpu(args, dist):
     return 0
 
 
-PROFILE_CASES = ("headline", "causal_long", "causal_long_quarter", "noncausal", "decode")
+PROFILE_CASES = ("headline", "causal_long", "causal_long_quarter", "noncausal", "decode", "prefill_state_quarter")
 
 
 def run_profile_case(name: str, launches: int) -> int:
     """A few plain launches of one workload (no graphs, no timing), for ncu.
 
     causal_long_quarter is the long causal workload at N = 16384 (537 MB of
-    q, k, v, o: above L2, small enough for multi-pass profiling)."""
+    q, k, v, o: above L2, small enough for multi-pass profiling);
+    prefill_state_quarter is the decode workload's prefill state with a quarter
+    of its heads (B = 32: 268 MB of k, v)."""
     import torch
     import causal_kernelized_attention_gb300 as la
     from causal_kernelized_attention_gb300 import build as la_build
@@ -581,6 +607,13 @@ def run_profile_case(name: str, launches: int) -> int:
         o = torch.empty_like(v)
         for _ in range(launches):
             la.la_forward_noncausal(q, k, v, o, eps=w.eps)
+    elif name == "prefill_state_quarter":
+        import dataclasses
+        w = dataclasses.replace(workloads.DECODE_BF16, B=workloads.DECODE_BF16.B // 4, steps=1)
+        (qp, kp, vp), _ = workloads.device_decode_inputs(w)
+        S, z = la.la_prefill_state(kp, vp)
+        for _ in range(launches - 1):
+            la.la_prefill_state(kp, vp, S, z)
     else:
         import dataclasses
         w = dataclasses.replace(workloads.DECODE_BF16, steps=launches)

@@ -100,13 +100,17 @@ struct Cfg {
 template <int D>
 struct alignas(1024) Smem {
     uint8_t stage[Cfg<D>::kStages][2 * Cfg<D>::kTileBytes];
+    // State mode: the second buffer of low phi parts (the first is the image slots).
+    // It precedes aux, so that the MMA's second 64-row block of it (16 KB on) stays
+    // inside shared memory.
+    uint8_t lo1[Cfg<D>::kTileBytes];
     uint8_t aux[Cfg<D>::kAuxBytes];
     uint64_t full[Cfg<D>::kStages], phi_done[Cfg<D>::kStages], empty[Cfg<D>::kStages];
     uint64_t item_full[kRing], item_empty[kRing];
     uint64_t acc_full[Cfg<D>::kAcc], acc_free[Cfg<D>::kAcc], o_staged[Cfg<D>::kAcc];
     uint64_t img_full[Cfg<D>::kImgs], img_empty[Cfg<D>::kImgs];
     uint64_t epi_sync, drain;
-    uint64_t lo_free;  // state mode: the MMAs of a tile's low phi parts have read them
+    uint64_t lo_free[2];  // state mode: the MMAs have read low-part buffer b
     Item items[kRing];
     uint32_t tmem_base;
     int abort;
@@ -115,7 +119,7 @@ struct alignas(1024) Smem {
 };
 
 static_assert(sizeof(Smem<128>) <= 232448, "exceeds the 227 KB per-CTA shared memory limit");
-// State mode keeps the low phi parts of a key tile in the image slots.
+// State mode keeps the low phi parts of a key tile in the image slots or in lo1.
 static_assert(Cfg<64>::kImgs * Cfg<64>::kSlotBytes >= Cfg<64>::kTileBytes, "no room for the low phi parts");
 static_assert(Cfg<128>::kImgs * Cfg<128>::kSlotBytes >= Cfg<128>::kTileBytes, "no room for the low phi parts");
 static_assert(sizeof(Smem<64>) <= 232448, "exceeds the 227 KB per-CTA shared memory limit");
@@ -324,7 +328,8 @@ noncausal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
             mbar_init(&sm.img_empty[m], 1);
         }
         mbar_init(&sm.epi_sync, kEpiThreads);
-        mbar_init(&sm.lo_free, 1);
+        mbar_init(&sm.lo_free[0], 1);
+        mbar_init(&sm.lo_free[1], 1);
         mbar_init(&sm.drain, 1);
         sm.abort = 0;
         fence_mbar_init();
@@ -361,10 +366,11 @@ noncausal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
                 const int valid = prm.N - (item.c0 + c) * kC;
                 if (prm.S_out) {
                     // State mode: phi in fp32, split into bf16 high parts (in place) and
-                    // low parts (in the unused image slots), once the previous tile's
-                    // MMAs have read the low parts.
-                    if (j > 0 && !(ok = wait_bar_warp(abort_flag, &sm.lo_free, (j - 1) & 1))) break;
-                    phi_tile_split<D, kPhiThreads>(sm.stage[s], sm.aux + CF::kImg0, t, valid);
+                    // low parts (buffer j % 2: the unused image slots or lo1), once the
+                    // MMAs of the tile two before have read that buffer.
+                    const int b = j & 1, n = j >> 1;
+                    if (n > 0 && !(ok = wait_bar_warp(abort_flag, &sm.lo_free[b], (n - 1) & 1))) break;
+                    phi_tile_split<D, kPhiThreads>(sm.stage[s], b ? sm.lo1 : sm.aux + CF::kImg0, t, valid);
                 } else {
                     phi_tile<D, kPhiThreads>(sm.stage[s], t, valid);
                 }
@@ -459,14 +465,14 @@ noncausal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
                                 mma_ss(dZ, mnmajor(ka, kk, kBox), wdesc(w1, kk), id_KW, acc);
                         }
                         if (prm.S_out) {  // state mode: the low phi parts against the same V (and 1)
-                            const uint32_t la = aux + CF::kImg0;
+                            const uint32_t la = (j & 1) ? smem_u32(sm.lo1) : aux + CF::kImg0;
 #pragma unroll
                             for (int kk = 0; kk < kC / 16; ++kk) {
                                 mma_ss(dS, mnmajor(la, kk, kBox), mnmajor(va, kk, lbo_v), id_KV, 1u);
                                 if constexpr (!CF::kFused)
                                     mma_ss(dZ, mnmajor(la, kk, kBox), wdesc(w1, kk), id_KW, 1u);
                             }
-                            mma_commit(&sm.lo_free);
+                            mma_commit(&sm.lo_free[j & 1]);
                         }
                         mma_commit(&sm.empty[s]);
                     }
