@@ -56,6 +56,7 @@ constexpr int kTmaWarp = 8, kMmaWarp = 9, kEpiPWarp0 = 10, kEpiOWarp0 = 14;
 // semantics) once its part of a state is stored; kPublished means complete, and
 // kPoison or more marks a segment whose CTA gave up.
 constexpr uint32_t kPublished = 8, kPoison = 1u << 20;
+constexpr int kMaxShortSegs = 32;  // segments per head in short-sequence mode
 
 // Row sums and z ride on the tensor cores in one of two ways:
 //  * fused (D = 64): the B operand of P V and of the state update is [V | 1] and
@@ -127,6 +128,11 @@ struct Params {
     uint32_t *counter;      // work ticket; counter[1] counts finished CTAs
     int N, BH, G, L, n_chunks;
     float eps;
+    // Short sequences: segment g of every head is chunks [bounds[g], bounds[g + 1]);
+    // it sums its own prefix (chunks before bounds[g]) in phase A, so no segment
+    // waits on another (no ticket, scan or flags).  0: the scan over L-chunk segments.
+    int short_mode;
+    int bounds[kMaxShortSegs + 1];
 };
 
 __device__ __forceinline__ bool wait_bar(int *abort_flag, uint64_t *bar, uint32_t parity)
@@ -159,12 +165,41 @@ __device__ __forceinline__ uint8_t *sb_copy(uint8_t *aux, int b)
     return aux + Cfg<D>::kSb + (Cfg<D>::kFused ? b * Cfg<D>::kSbBytes : 0);
 }
 
-// Chunk of job j: phase-A jobs walk the segment backwards, so that phase C, which
-// walks it forwards, starts with the K and V tiles read most recently (the likeliest
-// still in L2); the aggregate is a sum, so its order is free.
-__device__ __forceinline__ int job_chunk(int j, int nA, int c0)
+// Chunk of job j: phase-A jobs walk chunks [a0, a0 + nA) backwards -- the segment
+// itself (scan: a0 = c0), so that phase C, which walks it forwards, starts with the
+// K and V tiles read most recently (the likeliest still in L2), or the chunks
+// before it (short sequences: a0 = 0); a sum, so its order is free.
+__device__ __forceinline__ int job_chunk(int j, int nA, int a0, int c0)
 {
-    return j < nA ? c0 + (nA - 1 - j) : c0 + (j - nA);
+    return j < nA ? a0 + (nA - 1 - j) : c0 + (j - nA);
+}
+
+// The work of ticket t: segment g of head bh is chunks [c0, c0 + nch); phase A sums
+// the nA chunks from a0 (scan: the segment itself when it has a successor;
+// short sequences: the chunks before it, its exclusive prefix).
+struct Seg {
+    int g, bh, c0, nch, a0, nA;
+    bool has_next;  // scan mode: a later segment reads this one's aggregate
+};
+__device__ __forceinline__ Seg segment_of(const Params &prm, int t)
+{
+    Seg r;
+    r.g = t / prm.BH;
+    r.bh = t % prm.BH;
+    if (prm.short_mode) {
+        r.c0 = prm.bounds[r.g];
+        r.nch = prm.bounds[r.g + 1] - r.c0;
+        r.a0 = 0;
+        r.nA = r.c0;
+        r.has_next = false;
+    } else {
+        r.c0 = r.g * prm.L;
+        r.nch = min(prm.L, prm.n_chunks - r.c0);
+        r.has_next = r.g < prm.G - 1;
+        r.a0 = r.c0;
+        r.nA = r.has_next ? r.nch : 0;
+    }
+    return r;
 }
 
 // S += phi(K_c)^T [V_c | 1] (fused) or S += phi(K_c)^T V_c and z += phi(K_c)^T 1.
@@ -295,27 +330,26 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
     // memory), so the TMEM allocation below can only wait on other kernels' CTAs,
     // which never wait on it.  Every other thread reaches global memory after the
     // set-up barrier, hence after this thread's griddep_wait.
+    // (Short sequences: no segment waits on another, so the segment is blockIdx.x
+    // and no ticket is taken.)
     int my_ticket = 0;
     if (tid == 0) {
         griddep_wait();
-        my_ticket = (int)atomicAdd(prm.counter, 1u);
+        my_ticket = prm.short_mode ? (int)blockIdx.x : (int)atomicAdd(prm.counter, 1u);
     }
     if (warp == kTmaWarp && lane == 0) {
         // While the ticket is out: warm L2 with the first tiles of segment blockIdx.x.
-        // Every segment belongs to exactly one CTA, which reads these tiles first
-        // (phase A's last chunks, or the first chunk when there is no phase A),
+        // Every segment belongs to exactly one CTA, which reads these tiles first,
         // whichever CTA draws that ticket.  A prefetch is only a hint to L2 (the point
         // of coherence), so it may run before the grid dependency is resolved.
-        const int pg = (int)blockIdx.x / prm.BH, pbh = (int)blockIdx.x % prm.BH;
-        const int pc0 = pg * prm.L, pn = min(prm.L, prm.n_chunks - pc0);
-        const bool pa = pg < prm.G - 1;
-        for (int x = 0; x < min(pn, S); ++x) {
-            const int row0 = (pa ? pc0 + pn - 1 - x : pc0 + x) * kC;
+        const Seg ps = segment_of(prm, (int)blockIdx.x);
+        for (int x = 0; x < min(ps.nA + ps.nch, S); ++x) {
+            const int row0 = job_chunk(x, ps.nA, ps.a0, ps.c0) * kC;
 #pragma unroll
             for (int b = 0; b < D / 64; ++b) {
-                if (!pa) tma_prefetch_3d(&map_q, 64 * b, row0, pbh);
-                tma_prefetch_3d(&map_k, 64 * b, row0, pbh);
-                tma_prefetch_3d(&map_v, 64 * b, row0, pbh);
+                if (x >= ps.nA) tma_prefetch_3d(&map_q, 64 * b, row0, ps.bh);
+                tma_prefetch_3d(&map_k, 64 * b, row0, ps.bh);
+                tma_prefetch_3d(&map_v, 64 * b, row0, ps.bh);
             }
         }
     }
@@ -368,12 +402,9 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
     __syncthreads();
     tc_fence_after();
 
-    const int ticket = sm.ticket;
-    const int g = ticket / prm.BH, bh = ticket % prm.BH;
-    const int c0 = g * prm.L;
-    const int nch = min(prm.L, prm.n_chunks - c0);
-    const bool has_next = g < prm.G - 1;  // phase A and publishing only when a successor exists
-    const int nA = has_next ? nch : 0;
+    const Seg seg = segment_of(prm, sm.ticket);
+    const int g = seg.g, bh = seg.bh, c0 = seg.c0, nch = seg.nch, a0 = seg.a0, nA = seg.nA;
+    const bool has_next = seg.has_next;  // scan: publishing only when a successor exists
     const int total = nA + nch;
     const uint32_t tmem = sm.tmem_base;
     int *abort_flag = &sm.abort;
@@ -384,7 +415,7 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
             const int s = j % S, r = j / S;
             if (!wait_bar(abort_flag, &sm.full[s], r & 1)) break;
             const bool isC = j >= nA;
-            const int chunk = job_chunk(j, nA, c0);
+            const int chunk = job_chunk(j, nA, a0, c0);
             const int valid = prm.N - chunk * kC;
             if (isC) {
                 phi_tile<D, kPhiThreads>(sm.k[s], tid, valid);
@@ -419,7 +450,7 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
                     if (!wait_bar(abort_flag, &sm.ostore[s], k & 1)) break;
                 }
                 const bool isC = j >= nA;
-                const int row0 = job_chunk(j, nA, c0) * kC;
+                const int row0 = job_chunk(j, nA, a0, c0) * kC;
                 mbar_arrive_expect_tx(&sm.full[s], (isC ? 3u : 2u) * CF::kTileBytes);
 #pragma unroll
                 for (int b = 0; b < D / 64; ++b) {
@@ -585,7 +616,7 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
         for (int j = 0; j < nA; ++j) {
             const int s = j % S, r = j / S;
             if (!wait_bar(abort_flag, &sm.full[s], r & 1)) break;
-            phi_tile<D, 2 * kPhiThreads>(sm.k[s], kPhiThreads + gtid, prm.N - job_chunk(j, nA, c0) * kC);
+            phi_tile<D, 2 * kPhiThreads>(sm.k[s], kPhiThreads + gtid, prm.N - job_chunk(j, nA, a0, c0) * kC);
             fence_proxy_async_smem();
             mbar_arrive(&sm.phi_done[s]);
         }
@@ -597,136 +628,174 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
         bool have_agg = false;
         if (nA > 0) have_agg = wait_bar_warp(abort_flag, &sm.agg_ready, 0);
         tc_fence_after();
-        if (has_next) {
-            float *dst = (g == 0 ? prm.incl : prm.agg) + my * seg_floats;
-            if (have_agg) {
+        if (prm.short_mode) {
+            // Short sequences: phase A left the exclusive prefix in S_acc (zero-filled
+            // here when the segment starts the sequence); its bf16 copy and z for the
+            // first chunk.
 #pragma unroll 1
-                for (int cc = 0; cc < kHalf; cc += 32) {
+            for (int cc = 0; cc < kHalf; cc += 32) {
+                float acc[32];
+                if (have_agg) {
                     uint32_t a[32];
                     tmem_ld32(tl + CF::tS + col0 + cc, a);
                     tmem_ld_wait();
-                    if (row_ok) {
-                        float4 *d4 = reinterpret_cast<float4 *>(dst);
-                        const int cg0 = (col0 + cc) >> 2;
-#pragma unroll
-                        for (int e = 0; e < 8; ++e)
-                            d4[(size_t)(cg0 + e) * D + i] =
-                                make_float4(__uint_as_float(a[4 * e]), __uint_as_float(a[4 * e + 1]),
-                                            __uint_as_float(a[4 * e + 2]), __uint_as_float(a[4 * e + 3]));
-                    }
-                }
-                if (!is_o) {
-                    const float za = __uint_as_float(tmem_ld1(tl + CF::tZ));
-                    tmem_ld_wait();
-                    if (row_ok) dst[(size_t)D * D + i] = za;
-                }
-            }
-            __syncwarp();
-            if (lane == 0) red_release_add_gpu((g == 0 ? prm.incl_cnt : prm.agg_cnt) + my, have_agg ? 1u : kPoison);
-        }
-        if (gtid < 32) {
-            // One warp reads the counters of up to 32 predecessors per round.
-            int base = -1;
-            bool bad = false;
-            if (g > 0) {
-                const uint64_t t0 = globaltimer_ns();
-                while (true) {
-                    const int j = g - 1 - lane;
-                    uint32_t ci = 0, ca = 0;
-                    if (j >= 0) {
-                        ci = ld_acquire_gpu(prm.incl_cnt + head0 + j);
-                        ca = ld_acquire_gpu(prm.agg_cnt + head0 + j);
-                    }
-                    const unsigned inc = __ballot_sync(0xffffffffu, ci == kPublished);
-                    const unsigned avail = __ballot_sync(0xffffffffu, ci == kPublished || ca == kPublished);
-                    const unsigned poison = __ballot_sync(0xffffffffu, ci >= kPoison || ca >= kPoison);
-                    const int first = inc ? __ffs(inc) - 1 : 32;  // nearest inclusive prefix
-                    const unsigned need = first >= 32 ? 0xffffffffu : ((1u << first) - 1u);
-                    if ((poison & (need | (first < 32 ? (1u << first) : 0u))) != 0u) {
-                        bad = true;
-                        break;
-                    }
-                    if (first < 32 && (avail & need) == need) {
-                        base = g - 1 - first;
-                        break;
-                    }
-                    if (globaltimer_ns() - t0 > kWaitLimitNs) {
-                        if (lane == 0) atomicOr(&g_tc_status, kStatusTimeout);
-                        bad = true;
-                        break;
-                    }
-                }
-            }
-            if (lane == 0) {
-                sm.lb_base = base;
-                if (bad) *(volatile int *)abort_flag = 1;
-            }
-        }
-        named_bar_sync(1, 256);
-        const int base = sm.lb_base;
-        const bool use_prev = g > 0 && !aborted(abort_flag);
-        float *incl_out = (has_next && g > 0) ? prm.incl + my * seg_floats : nullptr;
-        float zacc = 0.f;  // z prefix, summed by the warps of the first column half with their first block
-#pragma unroll 1
-        for (int cc = 0; cc < kHalf; cc += 32) {
-            float acc[32];
-#pragma unroll
-            for (int e = 0; e < 32; ++e) acc[e] = 0.f;
-            const int cg0 = (col0 + cc) >> 2;
-            const bool want_z = !is_o && cc == 0;
-            if (use_prev && row_ok) {
-                if (base >= 0) add_state_z<D>(acc, zacc, prm.incl + (head0 + base) * seg_floats, cg0, i, want_z);
-                int j = base + 1;
-                for (; j + 1 < g; j += 2) {  // two states per round trip
-                    add_state_z<D>(acc, zacc, prm.agg + (head0 + j) * seg_floats, cg0, i, want_z);
-                    add_state_z<D>(acc, zacc, prm.agg + (head0 + j + 1) * seg_floats, cg0, i, want_z);
-                }
-                if (j < g) add_state_z<D>(acc, zacc, prm.agg + (head0 + j) * seg_floats, cg0, i, want_z);
-            }
-            if (incl_out) {
-                uint32_t a[32];
-                if (have_agg) {
-                    tmem_ld32(tl + CF::tS + col0 + cc, a);
-                    tmem_ld_wait();
+                    to_floats(a, acc);
                 } else {
+                    const uint32_t zero16[16] = {};
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) a[e] = 0u;
+                    for (int e = 0; e < 32; ++e) acc[e] = 0.f;
+                    tmem_st16(tl + CF::tS + col0 + cc, zero16);
+                    tmem_st16(tl + CF::tS + col0 + cc + 16, zero16);
                 }
-                if (row_ok) {
-                    float4 *d4 = reinterpret_cast<float4 *>(incl_out);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        d4[(size_t)(cg0 + e) * D + i] = make_float4(acc[4 * e] + __uint_as_float(a[4 * e]),
-                                            acc[4 * e + 1] + __uint_as_float(a[4 * e + 1]),
-                                            acc[4 * e + 2] + __uint_as_float(a[4 * e + 2]),
-                                            acc[4 * e + 3] + __uint_as_float(a[4 * e + 3]));
-                }
+                if (row_ok) put_sb<D>(sb, i, col0 + cc, acc);
             }
-            tmem_st16(tl + CF::tS + col0 + cc, *reinterpret_cast<const uint32_t(*)[16]>(&acc[0]));
-            tmem_st16(tl + CF::tS + col0 + cc + 16, *reinterpret_cast<const uint32_t(*)[16]>(&acc[16]));
-            if (row_ok) put_sb<D>(sb, i, col0 + cc, acc);
-        }
-        if (!is_o) {  // z, by the warps of the first column half
-            if (incl_out) {
+            if (!is_o) {  // z, by the warps of the first column half
                 float za = 0.f;
                 if (have_agg) {
                     za = __uint_as_float(tmem_ld1(tl + CF::tZ));
                     tmem_ld_wait();
+                } else {
+                    tmem_st1(tl + CF::tZ, 0u);
                 }
-                if (row_ok) incl_out[(size_t)D * D + i] = zacc + za;
+                if (row_ok) set_z<D>(sm.aux, i, za, 0);
             }
-            tmem_st1(tl + CF::tZ, __float_as_uint(zacc));
-            if (row_ok) set_z<D>(sm.aux, i, zacc, 0);
-        }
-        tmem_st_wait();
-        fence_proxy_async_smem();
-        named_bar_sync(1, 256);
-        tc_fence_before();
-        if (is_o) mbar_arrive(&sm.s_ready);  // sb and S_acc of both halves are in place
-        if (incl_out) {  // publish the inclusive prefix (its stores were issued above)
-            __syncwarp();
-            if (lane == 0)
-                red_release_add_gpu(prm.incl_cnt + my, (have_agg && !aborted(abort_flag)) ? 1u : kPoison);
+            tmem_st_wait();
+            fence_proxy_async_smem();
+            named_bar_sync(1, 256);
+            tc_fence_before();
+            if (is_o) mbar_arrive(&sm.s_ready);  // sb and S_acc of both halves are in place
+        } else {
+            if (has_next) {
+                float *dst = (g == 0 ? prm.incl : prm.agg) + my * seg_floats;
+                if (have_agg) {
+    #pragma unroll 1
+                    for (int cc = 0; cc < kHalf; cc += 32) {
+                        uint32_t a[32];
+                        tmem_ld32(tl + CF::tS + col0 + cc, a);
+                        tmem_ld_wait();
+                        if (row_ok) {
+                            float4 *d4 = reinterpret_cast<float4 *>(dst);
+                            const int cg0 = (col0 + cc) >> 2;
+    #pragma unroll
+                            for (int e = 0; e < 8; ++e)
+                                d4[(size_t)(cg0 + e) * D + i] =
+                                    make_float4(__uint_as_float(a[4 * e]), __uint_as_float(a[4 * e + 1]),
+                                                __uint_as_float(a[4 * e + 2]), __uint_as_float(a[4 * e + 3]));
+                        }
+                    }
+                    if (!is_o) {
+                        const float za = __uint_as_float(tmem_ld1(tl + CF::tZ));
+                        tmem_ld_wait();
+                        if (row_ok) dst[(size_t)D * D + i] = za;
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) red_release_add_gpu((g == 0 ? prm.incl_cnt : prm.agg_cnt) + my, have_agg ? 1u : kPoison);
+            }
+            if (gtid < 32) {
+                // One warp reads the counters of up to 32 predecessors per round.
+                int base = -1;
+                bool bad = false;
+                if (g > 0) {
+                    const uint64_t t0 = globaltimer_ns();
+                    while (true) {
+                        const int j = g - 1 - lane;
+                        uint32_t ci = 0, ca = 0;
+                        if (j >= 0) {
+                            ci = ld_acquire_gpu(prm.incl_cnt + head0 + j);
+                            ca = ld_acquire_gpu(prm.agg_cnt + head0 + j);
+                        }
+                        const unsigned inc = __ballot_sync(0xffffffffu, ci == kPublished);
+                        const unsigned avail = __ballot_sync(0xffffffffu, ci == kPublished || ca == kPublished);
+                        const unsigned poison = __ballot_sync(0xffffffffu, ci >= kPoison || ca >= kPoison);
+                        const int first = inc ? __ffs(inc) - 1 : 32;  // nearest inclusive prefix
+                        const unsigned need = first >= 32 ? 0xffffffffu : ((1u << first) - 1u);
+                        if ((poison & (need | (first < 32 ? (1u << first) : 0u))) != 0u) {
+                            bad = true;
+                            break;
+                        }
+                        if (first < 32 && (avail & need) == need) {
+                            base = g - 1 - first;
+                            break;
+                        }
+                        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                            if (lane == 0) atomicOr(&g_tc_status, kStatusTimeout);
+                            bad = true;
+                            break;
+                        }
+                    }
+                }
+                if (lane == 0) {
+                    sm.lb_base = base;
+                    if (bad) *(volatile int *)abort_flag = 1;
+                }
+            }
+            named_bar_sync(1, 256);
+            const int base = sm.lb_base;
+            const bool use_prev = g > 0 && !aborted(abort_flag);
+            float *incl_out = (has_next && g > 0) ? prm.incl + my * seg_floats : nullptr;
+            float zacc = 0.f;  // z prefix, summed by the warps of the first column half with their first block
+    #pragma unroll 1
+            for (int cc = 0; cc < kHalf; cc += 32) {
+                float acc[32];
+    #pragma unroll
+                for (int e = 0; e < 32; ++e) acc[e] = 0.f;
+                const int cg0 = (col0 + cc) >> 2;
+                const bool want_z = !is_o && cc == 0;
+                if (use_prev && row_ok) {
+                    if (base >= 0) add_state_z<D>(acc, zacc, prm.incl + (head0 + base) * seg_floats, cg0, i, want_z);
+                    int j = base + 1;
+                    for (; j + 1 < g; j += 2) {  // two states per round trip
+                        add_state_z<D>(acc, zacc, prm.agg + (head0 + j) * seg_floats, cg0, i, want_z);
+                        add_state_z<D>(acc, zacc, prm.agg + (head0 + j + 1) * seg_floats, cg0, i, want_z);
+                    }
+                    if (j < g) add_state_z<D>(acc, zacc, prm.agg + (head0 + j) * seg_floats, cg0, i, want_z);
+                }
+                if (incl_out) {
+                    uint32_t a[32];
+                    if (have_agg) {
+                        tmem_ld32(tl + CF::tS + col0 + cc, a);
+                        tmem_ld_wait();
+                    } else {
+    #pragma unroll
+                        for (int e = 0; e < 32; ++e) a[e] = 0u;
+                    }
+                    if (row_ok) {
+                        float4 *d4 = reinterpret_cast<float4 *>(incl_out);
+    #pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            d4[(size_t)(cg0 + e) * D + i] = make_float4(acc[4 * e] + __uint_as_float(a[4 * e]),
+                                                acc[4 * e + 1] + __uint_as_float(a[4 * e + 1]),
+                                                acc[4 * e + 2] + __uint_as_float(a[4 * e + 2]),
+                                                acc[4 * e + 3] + __uint_as_float(a[4 * e + 3]));
+                    }
+                }
+                tmem_st16(tl + CF::tS + col0 + cc, *reinterpret_cast<const uint32_t(*)[16]>(&acc[0]));
+                tmem_st16(tl + CF::tS + col0 + cc + 16, *reinterpret_cast<const uint32_t(*)[16]>(&acc[16]));
+                if (row_ok) put_sb<D>(sb, i, col0 + cc, acc);
+            }
+            if (!is_o) {  // z, by the warps of the first column half
+                if (incl_out) {
+                    float za = 0.f;
+                    if (have_agg) {
+                        za = __uint_as_float(tmem_ld1(tl + CF::tZ));
+                        tmem_ld_wait();
+                    }
+                    if (row_ok) incl_out[(size_t)D * D + i] = zacc + za;
+                }
+                tmem_st1(tl + CF::tZ, __float_as_uint(zacc));
+                if (row_ok) set_z<D>(sm.aux, i, zacc, 0);
+            }
+            tmem_st_wait();
+            fence_proxy_async_smem();
+            named_bar_sync(1, 256);
+            tc_fence_before();
+            if (is_o) mbar_arrive(&sm.s_ready);  // sb and S_acc of both halves are in place
+            if (incl_out) {  // publish the inclusive prefix (its stores were issued above)
+                __syncwarp();
+                if (lane == 0)
+                    red_release_add_gpu(prm.incl_cnt + my, (have_agg && !aborted(abort_flag)) ? 1u : kPoison);
+            }
         }
 
         if (!is_o) {
@@ -854,7 +923,9 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
     tc_fence_after();
     if (warp == kMmaWarp) tmem_dealloc(tmem, CF::kTmemCols);
     // The last CTA to finish leaves the ticket, the counter and every publish flag
-    // of this launch at zero, ready for the next launch on the same flags.
+    // of this launch at zero, ready for the next launch on the same flags.  (Short
+    // sequences touch no flag.)
+    if (prm.short_mode) return;
     if (tid == 0) sm.last = atom_add_acq_rel_gpu(prm.counter + 1, 1u) == gridDim.x - 1;
     __syncthreads();
     if (sm.last) {
@@ -880,13 +951,43 @@ la_status launch(const Problem &p)
 
     const int n_chunks = ceil_div(p.N, kC);
     const long long work = (long long)p.BH * n_chunks;
-    // Chunks per segment: enough items to fill the GPU, at most 16 (longer segments
+    const int n_sm = sm_count();
+    // Scan: chunks per segment enough to fill the GPU, at most 16 (longer segments
     // mean fewer scan steps; the K, V re-read of phase C should still hit L2).
-    const int L = (int)std::min<long long>(16, std::max<long long>(1, (work + sm_count() - 1) / sm_count()));
-    const int G = ceil_div(n_chunks, L);
+    int L = (int)std::min<long long>(16, std::max<long long>(1, (work + n_sm - 1) / n_sm));
+    int G = ceil_div(n_chunks, L);
+    // Short sequences: segments that sum their own prefix instead (no scan), with
+    // boundaries that balance a segment's cost -- a prefix chunk counts 1 (8 MMAs),
+    // an output chunk 3 (24 MMAs and the T -> P hand-off) -- over at most one wave.
+    // Taken when that balanced cost is below the scan's: 4 per chunk of its
+    // segments plus about 8 for the publish / look-back / state set-up round trips.
+    int bounds[kMaxShortSegs + 1] = {};
+    int short_G = 0, short_T = 0;
+    if (n_chunks <= kMaxShortSegs) {
+        const int gmax = std::max(1, std::min(n_chunks, n_sm / std::max(1, p.BH)));
+        for (int T = 3;; ++T) {
+            int c = 0, gg = 0;
+            while (c < n_chunks && gg < gmax) {
+                const int len = (T - c) / 3;  // output chunks this segment affords
+                if (len < 1) break;           // T too small
+                c = std::min(n_chunks, c + len);
+                bounds[++gg] = c;
+            }
+            if (c >= n_chunks) {
+                short_G = gg;
+                short_T = T;
+                break;
+            }
+        }
+    }
+    const bool short_mode = short_G > 0 && short_T <= 4 * L + 8;
+    if (short_mode) {
+        G = short_G;
+        L = 0;
+    }
     const size_t items = (size_t)p.BH * G;
     const size_t flag_bytes = ((items * 8 + 16) + 255) / 256 * 256;
-    const size_t state_bytes = G > 1 ? 2 * items * ((size_t)D * D + D) * 4 : 0;
+    const size_t state_bytes = !short_mode && G > 1 ? 2 * items * ((size_t)D * D + D) * 4 : 0;
 
     // Flags and published states from the stream's workspaces (flags already zero)
     // when they can serve the call, else from per-call scratch (flags cleared by a
@@ -913,7 +1014,7 @@ la_status launch(const Problem &p)
         if (e != cudaSuccess) return cuda_status(e);
     }
 
-    Params prm;
+    Params prm{};
     prm.o = (uint16_t *)p.o;
     prm.counter = (uint32_t *)flags;
     prm.incl_cnt = (uint32_t *)(flags + 16);
@@ -926,6 +1027,8 @@ la_status launch(const Problem &p)
     prm.L = L;
     prm.n_chunks = n_chunks;
     prm.eps = p.eps;
+    prm.short_mode = short_mode ? 1 : 0;
+    for (int x = 0; x <= G && short_mode; ++x) prm.bounds[x] = bounds[x];
 
     const int smem = (int)sizeof(Smem<D>);
     auto kern = causal_tc_kernel<D>;
