@@ -525,7 +525,10 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
                     const uint32_t sbc = sb_addr + ob * CF::kSbBytes;
                     const uint64_t dsb = mnmajor(sbc, 0, ones_addr + 32 * (ob + 1) - sbc);  // [S | z]
                     const uint64_t dqc = kmajor(smem_u32(sm.q[s]), 0);          // + 2 per kk
-                    if (cj >= 2 && !(ok = wait_bar(abort_flag, &sm.o_free[ob], ((cj >> 1) - 1) & 1))) break;
+                    // p_full(cj) also stands for "O buffer ob free": every O warp finishes
+                    // reading O of chunk cj - 2 (load wait, fence, its o_free arrival) before
+                    // it converts T(cj) and arrives on p_full(cj), so no o_free wait here
+                    // (a completed mbarrier wait still costs the issuer ~250 cycles).
                     if (!(ok = wait_bar(abort_flag, &sm.p_full[ob], (cj >> 1) & 1))) break;
                     tc_fence_after();
                     if (cj < nch - 1) {
@@ -894,8 +897,9 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
                             pack_bf16(__uint_as_float(a[8 * c + 6]) * inv, __uint_as_float(a[8 * c + 7]) * inv));
                 }
                 // o_staged before o_free: the next o_full of this buffer needs every
-                // thread's o_free, so no thread can arrive on o_staged[ob] for that
-                // chunk while another has yet to arrive for this one.
+                // thread's o_free (D = 128) or every thread's p_full arrival for that
+                // chunk, which follows this iteration (fused), so no thread can arrive on
+                // o_staged[ob] for that chunk while another has yet to arrive for this one.
                 fence_proxy_async_smem();
                 mbar_arrive(&sm.o_staged[ob]);
                 tc_fence_before();
