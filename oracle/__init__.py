@@ -61,6 +61,9 @@ def _declare(lib):
         "la_oracle_noncausal": ([P, P, P, I, P, I, I, I, I, D], None),
         "la_oracle_noncausal_pairwise": ([P, P, P, I, P, I, I, I, I, D], None),
         "la_oracle_decode_step": ([P, P, P, P, P, I, P, I, I, I, D], None),
+        "la_oracle_causal_decay_recurrent": ([P, P, P, I, P, P, I, I, I, I, D], None),
+        "la_oracle_causal_decay_quadratic": ([P, P, P, I, P, P, I, I, I, I, D], None),
+        "la_oracle_decode_step_decay": ([P, P, P, P, P, I, P, P, I, I, I, D], None),
         "la_oracle_num_threads": ([], I),
     }
     for name, (args, res) in sigs.items():
@@ -174,6 +177,54 @@ class Oracle:
         if BH:
             self.lib.la_oracle_decode_step(_ptr(S), _ptr(z), _ptr(q), _ptr(k), _ptr(v), t,
                                            _ptr(o), BH, dk, dv, float(eps))
+        return o
+
+
+    # ---------------------------------------------------------------- decayed state
+    @staticmethod
+    def _gamma(gamma, lead):
+        g = np.ascontiguousarray(np.broadcast_to(np.asarray(gamma, dtype=np.float64), lead)).reshape(-1)
+        if np.any(g < 0) or np.any(g > 1) or not np.all(np.isfinite(g)):
+            raise ValueError("gamma must lie in [0, 1]")
+        return np.ascontiguousarray(g)
+
+    def _fwd_decay(self, fname, q, k, v, gamma, eps):
+        (q, k, v), t = _prep(q, k, v)
+        N, dk = q.shape[-2], q.shape[-1]
+        dv = v.shape[-1]
+        lead = q.shape[:-2]
+        if k.shape != q.shape or v.shape[:-1] != q.shape[:-1]:
+            raise ValueError("shape mismatch")
+        g = self._gamma(gamma, lead)
+        BH = int(np.prod(lead)) if lead else 1
+        o = np.empty(lead + (N, dv), dtype=np.float64)
+        if BH and N and dv:
+            getattr(self.lib, fname)(_ptr(q), _ptr(k), _ptr(v), t, _ptr(g), _ptr(o), BH, N, dk, dv, float(eps))
+        return o
+
+    def causal_decay_recurrent(self, q, k, v, gamma, eps=1e-6):
+        """Decayed causal form; gamma broadcasts to the leading dims ([H] per head)."""
+        return self._fwd_decay("la_oracle_causal_decay_recurrent", q, k, v, gamma, eps)
+
+    def causal_decay_quadratic(self, q, k, v, gamma, eps=1e-6):
+        return self._fwd_decay("la_oracle_causal_decay_quadratic", q, k, v, gamma, eps)
+
+    def decode_step_decay(self, S, z, q, k, v, gamma, eps=1e-6):
+        """One decayed step for every head, S and z (float64) updated in place."""
+        if S.dtype != np.float64 or z.dtype != np.float64 or not S.flags.c_contiguous \
+                or not z.flags.c_contiguous:
+            raise TypeError("S and z must be C-contiguous float64 (updated in place)")
+        (q, k, v), t = _prep(q, k, v)
+        dk, dv = q.shape[-1], v.shape[-1]
+        lead = q.shape[:-1]
+        BH = int(np.prod(lead)) if lead else 1
+        if S.shape != lead + (dk, dv) or z.shape != lead + (dk,):
+            raise ValueError("state shape mismatch")
+        g = self._gamma(gamma, lead)
+        o = np.empty(lead + (dv,), dtype=np.float64)
+        if BH:
+            self.lib.la_oracle_decode_step_decay(_ptr(S), _ptr(z), _ptr(q), _ptr(k), _ptr(v), t, _ptr(g),
+                                                 _ptr(o), BH, dk, dv, float(eps))
         return o
 
 

@@ -360,6 +360,136 @@ void la_oracle_decode_step(double *S, double *z, const void *q, const void *k,
     }
 }
 
+/* ---------------------------------------------------------------------------
+ * Decayed state (scalar decay per sequence).  [math] "RetNet and gated linear
+ * attention: decay in the state": S_i = gamma S_{i-1} + k_i v_i^T with a fixed
+ * per-head gamma; [wiki] "What is actually lost": S_t = G_t (.) S_{t-1} +
+ * phi(k_t) v_t^T; [learn] "Try it yourself": S = 0.9 * S + outer(k_t, v_t).
+ * Reading: phi as above, and the normaliser z decays with the same gamma, so
+ * gamma = 1 is the undecayed form above:
+ *   S_t = g S_{t-1} + phi(k_t) v_t^T,  z_t = g z_{t-1} + phi(k_t),
+ *   o_t = phi(q_t)^T S_t / max(phi(q_t)^T z_t, eps).
+ * gamma: one value per (b,h) sequence, [BH] double.
+ * ------------------------------------------------------------------------- */
+void la_oracle_causal_decay_recurrent(const void *q, const void *k, const void *v, int type,
+                                      const double *gamma, double *o, int BH, int N, int dk,
+                                      int dv, double eps)
+{
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int bh = 0; bh < BH; ++bh) {
+        const double g = gamma[bh];
+        double *S = calloc((size_t)dk * dv, sizeof(double));
+        double *z = calloc((size_t)dk, sizeof(double));
+        double *fq = malloc(sizeof(double) * dk);
+        double *fk = malloc(sizeof(double) * dk);
+        double *vt = malloc(sizeof(double) * dv);
+        const int64_t qb = (int64_t)bh * N * dk, vb = (int64_t)bh * N * dv;
+        for (int t = 0; t < N; ++t) {
+            phi_row(q, type, qb, t, dk, fq);
+            phi_row(k, type, qb, t, dk, fk);
+            for (int c = 0; c < dv; ++c)
+                vt[c] = load(v, type, vb + (int64_t)t * dv + c);
+            /* S = g S + phi(k_t) v_t^T ; z = g z + phi(k_t) */
+            for (int r = 0; r < dk; ++r) {
+                double *Sr = S + (size_t)r * dv;
+                for (int c = 0; c < dv; ++c)
+                    Sr[c] = g * Sr[c] + fk[r] * vt[c];
+                z[r] = g * z[r] + fk[r];
+            }
+            double den = 0.0;
+            for (int r = 0; r < dk; ++r)
+                den += fq[r] * z[r];
+            double *ot = o + vb + (int64_t)t * dv;
+            for (int c = 0; c < dv; ++c)
+                ot[c] = 0.0;
+            for (int r = 0; r < dk; ++r) {
+                const double *Sr = S + (size_t)r * dv;
+                for (int c = 0; c < dv; ++c)
+                    ot[c] += fq[r] * Sr[c];
+            }
+            den = clamp_den(den, eps);
+            for (int c = 0; c < dv; ++c)
+                ot[c] /= den;
+        }
+        free(S); free(z); free(fq); free(fk); free(vt);
+    }
+}
+
+/* The weighted quadratic form the decayed recurrence equals ([learn] "Try it
+ * yourself": the weighted quadratic form it does match): scores
+ * g^(i-j) phi(q_i).phi(k_j) kept for j <= i, o = scores V / row sums.  O(N^2):
+ * cross-check only.  0^0 = 1 (the token itself). */
+void la_oracle_causal_decay_quadratic(const void *q, const void *k, const void *v, int type,
+                                      const double *gamma, double *o, int BH, int N, int dk,
+                                      int dv, double eps)
+{
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int bh = 0; bh < BH; ++bh) {
+        const double g = gamma[bh];
+        double *fq = malloc(sizeof(double) * dk);
+        double *fk = malloc(sizeof(double) * dk);
+        const int64_t qb = (int64_t)bh * N * dk, vb = (int64_t)bh * N * dv;
+        for (int i = 0; i < N; ++i) {
+            phi_row(q, type, qb, i, dk, fq);
+            double *oi = o + vb + (int64_t)i * dv;
+            for (int c = 0; c < dv; ++c)
+                oi[c] = 0.0;
+            double rowsum = 0.0;
+            for (int j = 0; j <= i; ++j) {
+                phi_row(k, type, qb, j, dk, fk);
+                double s = 0.0;
+                for (int r = 0; r < dk; ++r)
+                    s += fq[r] * fk[r];
+                s *= (i == j) ? 1.0 : pow(g, (double)(i - j));
+                rowsum += s;
+                for (int c = 0; c < dv; ++c)
+                    oi[c] += s * load(v, type, vb + (int64_t)j * dv + c);
+            }
+            rowsum = clamp_den(rowsum, eps);
+            for (int c = 0; c < dv; ++c)
+                oi[c] /= rowsum;
+        }
+        free(fq); free(fk);
+    }
+}
+
+/* One decayed decode step, state in place: S = g S + phi(k) v^T, z = g z +
+ * phi(k), then o = phi(q)^T S / max(phi(q)^T z, eps).  gamma [BH]. */
+void la_oracle_decode_step_decay(double *S, double *z, const void *q, const void *k,
+                                 const void *v, int type, const double *gamma, double *o, int BH,
+                                 int dk, int dv, double eps)
+{
+#pragma omp parallel for schedule(static)
+    for (int bh = 0; bh < BH; ++bh) {
+        const double g = gamma[bh];
+        double *Sb = S + (size_t)bh * dk * dv;
+        double *zb = z + (size_t)bh * dk;
+        double *ob = o + (size_t)bh * dv;
+        double *fq = malloc(sizeof(double) * dk);
+        double *fk = malloc(sizeof(double) * dk);
+        for (int r = 0; r < dk; ++r) {
+            fq[r] = la_oracle_phi(load(q, type, (int64_t)bh * dk + r));
+            fk[r] = la_oracle_phi(load(k, type, (int64_t)bh * dk + r));
+        }
+        for (int r = 0; r < dk; ++r) {
+            for (int c = 0; c < dv; ++c)
+                Sb[(size_t)r * dv + c] = g * Sb[(size_t)r * dv + c] + fk[r] * load(v, type, (int64_t)bh * dv + c);
+            zb[r] = g * zb[r] + fk[r];
+        }
+        double den = 0.0;
+        for (int r = 0; r < dk; ++r)
+            den += fq[r] * zb[r];
+        den = clamp_den(den, eps);
+        for (int c = 0; c < dv; ++c) {
+            double s = 0.0;
+            for (int r = 0; r < dk; ++r)
+                s += fq[r] * Sb[(size_t)r * dv + c];
+            ob[c] = s / den;
+        }
+        free(fq); free(fk);
+    }
+}
+
 /* Threads OpenMP will use (reported beside CPU timings). */
 int la_oracle_num_threads(void)
 {

@@ -273,4 +273,96 @@ def pin_bf16_widening(orc):
     assert _rel_err(a[0], ref) < 1e-12
 
 
+# ----------------------------------------------------------------------------
+# decayed state: S_t = g S_{t-1} + phi(k_t) v_t^T, z likewise ("Linear Attention --
+# Math + Variants", RetNet and gated linear attention: a fixed per-head decay;
+# "Linear attention", learn.pranaymahendrakar.com, Try it yourself)
+# ----------------------------------------------------------------------------
+def weighted_pairwise(q, k, v, g, eps=EPS):
+    """sum_{j<=i} g^(i-j) phi(q_i).phi(k_j) v_j / sum_{j<=i} g^(i-j) phi(q_i).phi(k_j),
+    dense numpy per sequence (leading dim = sequences, g one value per sequence)."""
+    out = []
+    for s in range(q.shape[0]):
+        fq, fk = phi_np(q[s]), phi_np(k[s])
+        n = fq.shape[0]
+        i, j = np.meshgrid(np.arange(n), np.arange(n), indexing="ij")
+        w = np.where(j <= i, float(g[s]) ** np.maximum(i - j, 0), 0.0)
+        scores = (fq @ fk.T) * w
+        den = np.maximum(scores.sum(-1, keepdims=True), eps)
+        out.append((scores @ np.asarray(v[s], dtype=np.float64)) / den)
+    return np.stack(out)
+
+
+def pin_decay_equals_weighted_pairwise(orc):
+    """The decayed recurrence (and the oracle's own weighted quadratic form) equals the
+    weighted pairwise form written above, for decays 1, 0.9, 0.5 and 0."""
+    q, k, v = _rand(1000, 4, 50, 6, 5)
+    g = np.array([1.0, 0.9, 0.5, 0.0])
+    ref = weighted_pairwise(q, k, v, g)
+    assert _rel_err(orc.causal_decay_recurrent(q, k, v, g, EPS), ref) < 1e-12
+    assert _rel_err(orc.causal_decay_quadratic(q, k, v, g, EPS), ref) < 1e-12
+
+
+def pin_decay_one_is_undecayed(orc):
+    """gamma = 1 gives the undecayed causal form, for every head."""
+    q, k, v = _rand(1010, 3, 40, 5, 7)
+    assert _rel_err(orc.causal_decay_recurrent(q, k, v, np.ones(3), EPS), orc.causal_recurrent(q, k, v, EPS)) < 1e-13
+
+
+def pin_decay_zero_returns_v(orc):
+    """gamma = 0 keeps only the current token: o_t = v_t (phi > 0, so the weight is
+    positive and cancels)."""
+    q, k, v = _rand(1020, 2, 30, 4, 3)
+    assert _rel_err(orc.causal_decay_recurrent(q, k, v, np.zeros(2), EPS), v) < 1e-14
+
+
+def pin_decay_exact_rational(orc):
+    """Tiny inputs with q, k > 0 (phi = x + 1 exact) and gamma = 1/2, against exact
+    rational arithmetic of the weighted form."""
+    rng = np.random.default_rng(1030)
+    N, dk, dv = 6, 3, 2
+    qv = rng.integers(1, 8, size=(N, dk)) / 8.0
+    kv = rng.integers(1, 8, size=(N, dk)) / 8.0
+    vv = rng.integers(-8, 9, size=(N, dv)) / 4.0
+    got = orc.causal_decay_recurrent(qv[None], kv[None], vv[None], [0.5], 0.0)[0]
+    fq = [[Fraction(x).limit_denominator(64) + 1 for x in row] for row in qv]
+    fk = [[Fraction(x).limit_denominator(64) + 1 for x in row] for row in kv]
+    vf = [[Fraction(x).limit_denominator(64) for x in row] for row in vv]
+    for i in range(N):
+        num = [Fraction(0)] * dv
+        den = Fraction(0)
+        for j in range(i + 1):
+            s = sum(a * b for a, b in zip(fq[i], fk[j])) * Fraction(1, 2) ** (i - j)
+            den += s
+            for c in range(dv):
+                num[c] += s * vf[j][c]
+        for c in range(dv):
+            assert abs(got[i, c] - float(num[c] / den)) <= 1e-14 * max(1.0, abs(float(num[c] / den)))
+
+
+def pin_decay_differs_from_unweighted(orc):
+    """With decay the causal output no longer matches the unweighted quadratic form
+    ("Linear attention", Try it yourself), except at the first position."""
+    q, k, v = _rand(1040, 2, 30, 4, 3)
+    dec = orc.causal_decay_recurrent(q, k, v, np.full(2, 0.9), EPS)
+    plain = pairwise_bruteforce(q, k, v, causal=True)
+    assert _rel_err(dec[:, 0], plain[:, 0]) < 1e-13
+    assert _rel_err(dec[:, 1:], plain[:, 1:]) > 1e-2
+
+
+def pin_decode_decay_continues_causal(orc):
+    """Decayed decode steps from a zero state reproduce the decayed causal forward at
+    every position (the step is the recurrence's body)."""
+    BH, N, dk, dv = 3, 20, 5, 4
+    q, k, v = _rand(1050, BH, N, dk, dv)
+    g = np.array([0.95, 0.7, 1.0])
+    full = orc.causal_decay_recurrent(q, k, v, g, EPS)
+    S = np.zeros((BH, dk, dv))
+    z = np.zeros((BH, dk))
+    for t in range(N):
+        o = orc.decode_step_decay(S, z, q[:, t], k[:, t], v[:, t], g, EPS)
+        assert _rel_err(o, full[:, t]) < 1e-12, t
+    assert _rel_err(o, weighted_pairwise(q, k, v, g)[:, -1]) < 1e-12
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -41,6 +41,17 @@ MUTANTS = {
                           "Sb[(size_t)r * dv + c] += fk[r] * load(v, type, vb + (int64_t)((t + 1) % N) * dv + c);"),
     # bf16 widening with the wrong shift
     "bf16_wrong_shift": ("<< 16;", "<< 15;"),
+    # decay: the normaliser not decayed
+    "decay_z_undecayed": ("z[r] = g * z[r] + fk[r];", "z[r] = z[r] + fk[r];"),
+    # decay: the current token decayed too (exponent off by one)
+    "decay_current_token_decayed": ("Sr[c] = g * Sr[c] + fk[r] * vt[c];", "Sr[c] = g * (Sr[c] + fk[r] * vt[c]);"),
+    # decay, weighted quadratic form: exponent with the wrong sign
+    "decay_quadratic_sign": ("pow(g, (double)(i - j))", "pow(g, (double)(j - i))"),
+    # decayed decode: normaliser accumulates phi(q)
+    "decode_decay_z_uses_q": ("zb[r] = g * zb[r] + fk[r];", "zb[r] = g * zb[r] + fq[r];"),
+    # decayed decode: state not decayed
+    "decode_decay_state_undecayed": ("Sb[(size_t)r * dv + c] = g * Sb[(size_t)r * dv + c] + fk[r]",
+                                     "Sb[(size_t)r * dv + c] = Sb[(size_t)r * dv + c] + fk[r]"),
 }
 
 
