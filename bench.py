@@ -472,6 +472,53 @@ def bench_path_prefill(torch, la, reps, peaks, src):
             "l2": "k, v 1.07 GB > L2"}
 
 
+def bench_path_causal_decay(torch, la, reps, peaks, src):
+    """la_forward_causal_decay on the headline causal shape (B=4 H=8 N=2048 d=64,
+    chunk 128, bf16) with per-head decays from 0.9 to 0.999; CUDA cores, fp32."""
+    w = workloads.CAUSAL_BF16
+    q, k, v = workloads.forward_inputs(w)
+    nbytes = forward_bytes(w.BH, w.N, w.dk, w.dv, 2)
+    R = n_rotations(nbytes)
+    base = [dev_copy(torch, x, "bf16") for x in (q, k, v)]
+    sets = [[t.clone() for t in base] + [torch.empty_like(base[2])] for _ in range(R)]
+    g = torch.from_numpy(workloads.decay_gammas(w.H)).cuda()
+
+    def step(i):
+        s = sets[i % R]
+        la.la_forward_causal_decay(s[0], s[1], s[2], g, s[3], chunk=w.chunk, eps=w.eps)
+
+    secs, launches, _ = time_graph_steps(torch, la, step, reps, 3, Dist())
+    t = secs / reps
+    fl = causal_flops(w.BH, w.N, w.dk, w.dv, w.chunk)
+    return {"workload": w.name + "_decay", "value": round(w.B * w.N / t, 1), "unit": "tokens/s",
+            "ms_per_step": round(t * 1e3, 4), "launches_per_step": launches / reps,
+            "roofline": roofline(fl, nbytes, t, peaks, src, None),
+            "l2": "%d rotating buffer sets" % R}
+
+
+def bench_path_decode_decay(torch, la, steps, peaks, src):
+    """la_decode_step_decay on the decode workload (4096 heads, d = 128, fp32 state)."""
+    w = workloads.DECODE_BF16
+    (qp, kp, vp), (qd, kd, vd) = workloads.device_decode_inputs(w)
+    g = torch.from_numpy(workloads.decay_gammas(w.H)).cuda()
+    S, z = la.la_prefill_state_decay(kp, vp, g)
+    del qp, kp, vp
+    o = torch.empty((w.B, w.H, w.dv), dtype=torch.bfloat16, device="cuda")
+
+    def step(i):
+        la.la_decode_step_decay(S, z, qd[i], kd[i], vd[i], g, o, eps=w.eps)
+
+    n = min(steps, w.steps)
+    secs, launches, _ = time_graph_steps(torch, la, step, n, 3, Dist())
+    t = secs / n
+    nbytes = decode_bytes_per_step(w.BH, w.dk, w.dv, 2)
+    fl = decode_flops_per_step(w.BH, w.dk, w.dv)
+    return {"workload": w.name + "_decay", "value": round(w.B / t, 1), "unit": "tokens/s",
+            "ms_per_step": round(t * 1e3, 5), "steps": n, "launches_per_step": launches / n,
+            "roofline": roofline(fl, nbytes, t, peaks, src, None),
+            "l2": "state 270 MB > L2"}
+
+
 # --------------------------------------------------------------------------- CPU oracle
 def oracle_causal_sample(w, target_s=10.0, max_reps=100000):
     """The float64 oracle (as it stands) on a bounded sample of workload w:
@@ -568,6 +615,8 @@ def run_gpu(args, dist):
         paths["noncausal"] = bench_path_noncausal(torch, la, max(args.path_reps, 20), peaks, src)
         paths["decode"] = bench_path_decode(torch, la, 1024, peaks, src)
         paths["prefill_state"] = bench_path_prefill(torch, la, max(args.path_reps, 20), peaks, src)
+        paths["causal_decay"] = bench_path_causal_decay(torch, la, max(args.path_reps, 20), peaks, src)
+        paths["decode_decay"] = bench_path_decode_decay(torch, la, 1024, peaks, src)
         if s2:
             paths["clocks"] = s2.stop(window=(t_paths, time.time()))
 

@@ -9,16 +9,19 @@ import of this package's functions raises.
 
 Tensors are PyTorch CUDA tensors (PyTorch supplies device memory and streams):
   q, k [B, H, N, dk], v, o [B, H, N, dv], fp32 or bf16, contiguous;
-  decode: q, k [B, H, dk], v, o [B, H, dv]; S [B, H, dk, dv] and z [B, H, dk] fp32.
+  decode: q, k [B, H, dk], v, o [B, H, dv]; S [B, H, dk, dv] and z [B, H, dk] fp32;
+  decayed forms: gamma [H] fp32, one decay per head.
 """
 from __future__ import annotations
 
-from ._binding import (LA_BF16, LA_F32, LAError, lib_path, la_decode_step, la_forward_causal,
-                       la_forward_noncausal, la_forward_noncausal_noalloc, la_get_device_status, la_kernel_launches, la_last_cuda_error,
-                       la_prefill_state, la_status_string, la_version, load_library)
+from ._binding import (LA_BF16, LA_F32, LAError, lib_path, la_decode_step, la_decode_step_decay,
+                       la_forward_causal, la_forward_causal_decay, la_forward_noncausal, la_forward_noncausal_noalloc, la_get_device_status, la_kernel_launches, la_last_cuda_error,
+                       la_prefill_state, la_prefill_state_decay, la_status_string, la_version, load_library)
 
 __all__ = [
-    "LA_BF16", "LA_F32", "LAError", "lib_path", "la_decode_step", "la_forward_causal",
+    "LA_BF16", "LA_F32", "LAError", "lib_path", "la_decode_step", "la_decode_step_decay",
+    "la_forward_causal", "la_forward_causal_decay",
     "la_forward_noncausal", "la_forward_noncausal_noalloc", "la_get_device_status", "la_kernel_launches", "la_last_cuda_error", "la_prefill_state",
+    "la_prefill_state_decay",
     "la_status_string", "la_version", "load_library",
 ]

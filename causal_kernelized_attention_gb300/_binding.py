@@ -39,6 +39,9 @@ def _declare(lib):
         "la_forward_noncausal_noalloc": [P, P, P, P, I, I, I, I, I, F, I, P],
         "la_decode_step": [P, P, P, P, P, P, I, I, I, I, F, I, P],
         "la_prefill_state": [P, P, P, P, I, I, I, I, I, I, P],
+        "la_forward_causal_decay": [P, P, P, P, P, I, I, I, I, I, I, F, I, P],
+        "la_decode_step_decay": [P, P, P, P, P, P, P, I, I, I, I, F, I, P],
+        "la_prefill_state_decay": [P, P, P, P, P, I, I, I, I, I, I, P],
         "la_get_device_status": [P],
     }
     for name, args in sigs.items():
@@ -183,6 +186,56 @@ def la_decode_step(S, z, q, k, v, o=None, eps: float = 1e-6, stream=None):
     return o
 
 
+def _gamma_tensor(gamma, H: int):
+    import torch
+    _need_cuda(gamma)
+    if gamma.dtype != torch.float32 or tuple(gamma.shape) != (H,):
+        raise ValueError("gamma must be a float32 tensor of shape [H]")
+
+
+def la_forward_causal_decay(q, k, v, gamma, o=None, chunk: int = 128, eps: float = 1e-6, stream=None):
+    """Causal forward with a decayed state, gamma [H] fp32 (one decay per head);
+    q, k [B,H,N,dk], v [B,H,N,dv]; returns o [B,H,N,dv]."""
+    import torch
+    if o is None:
+        o = torch.empty(q.shape[:-1] + (v.shape[-1],), dtype=q.dtype, device=q.device)
+    _need_cuda(q, k, v, o)
+    _same_dtype(q, k, v, o)
+    B, H, N, dk = q.shape
+    dv = v.shape[-1]
+    if tuple(k.shape) != (B, H, N, dk) or tuple(v.shape[:-1]) != (B, H, N) or tuple(o.shape) != (B, H, N, dv):
+        raise ValueError("shape mismatch")
+    _gamma_tensor(gamma, H)
+    st = load_library().la_forward_causal_decay(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                                gamma.data_ptr(), B, H, N, dk, dv, int(chunk), float(eps),
+                                                _dtype_code(q), _stream_ptr(stream))
+    _check("la_forward_causal_decay", st)
+    return o
+
+
+def la_decode_step_decay(S, z, q, k, v, gamma, o=None, eps: float = 1e-6, stream=None):
+    """One decayed decode step (S = g S + phi(k) v^T, z = g z + phi(k), g = gamma[h]);
+    S, z updated in place; returns o [B,H,dv]."""
+    import torch
+    if o is None:
+        o = torch.empty(q.shape[:-1] + (v.shape[-1],), dtype=q.dtype, device=q.device)
+    _need_cuda(S, z, q, k, v, o)
+    _same_dtype(q, k, v, o)
+    if S.dtype != torch.float32 or z.dtype != torch.float32:
+        raise TypeError("S and z must be float32")
+    B, H, dk = q.shape
+    dv = v.shape[-1]
+    if tuple(S.shape) != (B, H, dk, dv) or tuple(z.shape) != (B, H, dk) or tuple(k.shape) != (B, H, dk) \
+            or tuple(v.shape) != (B, H, dv) or tuple(o.shape) != (B, H, dv):
+        raise ValueError("shape mismatch")
+    _gamma_tensor(gamma, H)
+    st = load_library().la_decode_step_decay(S.data_ptr(), z.data_ptr(), q.data_ptr(), k.data_ptr(),
+                                             v.data_ptr(), o.data_ptr(), gamma.data_ptr(), B, H, dk, dv,
+                                             float(eps), _dtype_code(q), _stream_ptr(stream))
+    _check("la_decode_step_decay", st)
+    return o
+
+
 def la_prefill_state(k, v, S=None, z=None, stream=None):
     """S = sum_t phi(k_t) v_t^T, z = sum_t phi(k_t) over N tokens; returns (S, z) fp32."""
     import torch
@@ -199,6 +252,27 @@ def la_prefill_state(k, v, S=None, z=None, stream=None):
     st = load_library().la_prefill_state(k.data_ptr(), v.data_ptr(), S.data_ptr(), z.data_ptr(),
                                          B, H, N, dk, dv, _dtype_code(k), _stream_ptr(stream))
     _check("la_prefill_state", st)
+    return S, z
+
+
+def la_prefill_state_decay(k, v, gamma, S=None, z=None, stream=None):
+    """Decayed prefix state: S = sum_t g^(N-1-t) phi(k_t) v_t^T, z likewise, g = gamma[h];
+    returns (S, z) fp32."""
+    import torch
+    B, H, N, dk = k.shape
+    dv = v.shape[-1]
+    if S is None:
+        S = torch.empty((B, H, dk, dv), dtype=torch.float32, device=k.device)
+    if z is None:
+        z = torch.empty((B, H, dk), dtype=torch.float32, device=k.device)
+    _need_cuda(k, v, S, z)
+    _same_dtype(k, v)
+    if tuple(v.shape[:-1]) != (B, H, N) or tuple(S.shape) != (B, H, dk, dv) or tuple(z.shape) != (B, H, dk):
+        raise ValueError("shape mismatch")
+    _gamma_tensor(gamma, H)
+    st = load_library().la_prefill_state_decay(k.data_ptr(), v.data_ptr(), gamma.data_ptr(), S.data_ptr(),
+                                               z.data_ptr(), B, H, N, dk, dv, _dtype_code(k), _stream_ptr(stream))
+    _check("la_prefill_state_decay", st)
     return S, z
 
 

@@ -159,6 +159,28 @@ static la_status check_forward(const void *q, const void *k, const void *v, cons
     return LA_OK;
 }
 
+// Checks of the decode entry points; gamma null for the undecayed step.
+static la_status decode_checked(float *S, float *z, const void *q, const void *k, const void *v, void *o,
+                                const float *gamma, int B, int H, int dk, int dv, float eps, la_dtype dtype,
+                                cudaStream_t stream)
+{
+    if (B < 0 || H < 0 || dk < 0 || dv < 0) return LA_ERR_INVALID_ARG;
+    if (!(eps >= 0.f) || !isfinite(eps)) return LA_ERR_INVALID_ARG;
+    if (dtype != LA_F32 && dtype != LA_BF16) return LA_ERR_INVALID_ARG;
+    if (B == 0 || H == 0 || dk == 0 || dv == 0) return LA_OK;
+    if (!S || !z || !q || !k || !v || !o) return LA_ERR_INVALID_ARG;
+    if (!aligned16(S) || !aligned16(z) || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o))
+        return LA_ERR_MISALIGNED;
+    if (!supported_dim(dk) || !supported_dim(dv)) return LA_ERR_UNSUPPORTED;
+    const size_t BH = (size_t)B * H, es = elem_size(dtype);
+    if (BH > 0x7fffffff) return LA_ERR_UNSUPPORTED;
+    const size_t nS = BH * dk * dv * 4, nz = BH * dk * 4, nqk = BH * dk * es, nvo = BH * dv * es;
+    if (overlaps(S, nS, z, nz) || overlaps(o, nvo, S, nS) || overlaps(o, nvo, z, nz) ||
+        overlaps(o, nvo, q, nqk) || overlaps(o, nvo, k, nqk) || overlaps(o, nvo, v, nvo))
+        return LA_ERR_INVALID_ARG;
+    return decode_step(S, z, q, k, v, o, (int)BH, dk, dv, eps, dtype, stream, gamma, H);
+}
+
 }  // namespace la
 
 using namespace la;
@@ -211,21 +233,39 @@ la_status la_forward_noncausal_noalloc(const void *q, const void *k, const void 
 la_status la_decode_step(float *S, float *z, const void *q, const void *k, const void *v, void *o, int B,
                          int H, int dk, int dv, float eps, la_dtype dtype, la_stream_t stream)
 {
-    if (B < 0 || H < 0 || dk < 0 || dv < 0) return LA_ERR_INVALID_ARG;
-    if (!(eps >= 0.f) || !isfinite(eps)) return LA_ERR_INVALID_ARG;
-    if (dtype != LA_F32 && dtype != LA_BF16) return LA_ERR_INVALID_ARG;
-    if (B == 0 || H == 0 || dk == 0 || dv == 0) return LA_OK;
-    if (!S || !z || !q || !k || !v || !o) return LA_ERR_INVALID_ARG;
-    if (!aligned16(S) || !aligned16(z) || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o))
-        return LA_ERR_MISALIGNED;
+    return decode_checked(S, z, q, k, v, o, nullptr, B, H, dk, dv, eps, dtype, (cudaStream_t)stream);
+}
+
+la_status la_forward_causal_decay(const void *q, const void *k, const void *v, void *o, const float *gamma,
+                                  int B, int H, int N, int dk, int dv, int chunk, float eps, la_dtype dtype,
+                                  la_stream_t stream)
+{
+    bool empty;
+    la_status st = check_forward(q, k, v, o, B, H, N, dk, dv, eps, dtype, &empty);
+    if (st != LA_OK) return st;
+    if (chunk != 64 && chunk != 128) return LA_ERR_UNSUPPORTED;
+    if (empty) return LA_OK;
+    if (!gamma) return LA_ERR_INVALID_ARG;
+    if (((uintptr_t)gamma & 3u) != 0) return LA_ERR_MISALIGNED;
     if (!supported_dim(dk) || !supported_dim(dv)) return LA_ERR_UNSUPPORTED;
-    const size_t BH = (size_t)B * H, es = elem_size(dtype);
-    if (BH > 0x7fffffff) return LA_ERR_UNSUPPORTED;
-    const size_t nS = BH * dk * dv * 4, nz = BH * dk * 4, nqk = BH * dk * es, nvo = BH * dv * es;
-    if (overlaps(S, nS, z, nz) || overlaps(o, nvo, S, nS) || overlaps(o, nvo, z, nz) ||
-        overlaps(o, nvo, q, nqk) || overlaps(o, nvo, k, nqk) || overlaps(o, nvo, v, nvo))
-        return LA_ERR_INVALID_ARG;
-    return decode_step(S, z, q, k, v, o, (int)BH, dk, dv, eps, dtype, (cudaStream_t)stream);
+    if (overlaps(o, (size_t)B * H * N * dv * elem_size(dtype), gamma, (size_t)H * 4)) return LA_ERR_INVALID_ARG;
+    Problem p{q, k, v, o, B * H, N, dk, dv, chunk, eps, dtype, (cudaStream_t)stream, gamma, H};
+    return causal_simt(p);
+}
+
+la_status la_decode_step_decay(float *S, float *z, const void *q, const void *k, const void *v, void *o,
+                               const float *gamma, int B, int H, int dk, int dv, float eps, la_dtype dtype,
+                               la_stream_t stream)
+{
+    if (B > 0 && H > 0 && dk > 0 && dv > 0) {
+        if (!gamma) return LA_ERR_INVALID_ARG;
+        if (((uintptr_t)gamma & 3u) != 0) return LA_ERR_MISALIGNED;
+        const size_t BH = (size_t)B * H;
+        if (overlaps(gamma, (size_t)H * 4, S, BH * dk * dv * 4) || overlaps(gamma, (size_t)H * 4, z, BH * dk * 4))
+            return LA_ERR_INVALID_ARG;
+        if (o && overlaps(gamma, (size_t)H * 4, o, BH * dv * elem_size(dtype))) return LA_ERR_INVALID_ARG;
+    }
+    return decode_checked(S, z, q, k, v, o, gamma, B, H, dk, dv, eps, dtype, (cudaStream_t)stream);
 }
 
 la_status la_prefill_state(const void *k, const void *v, float *S, float *z, int B, int H, int N, int dk,
@@ -248,6 +288,25 @@ la_status la_prefill_state(const void *k, const void *v, float *S, float *z, int
         if (st != LA_ERR_UNSUPPORTED) return st;
     }
     return state_simt(k, v, S, z, (int)BH, N, dk, dv, dtype, (cudaStream_t)stream);
+}
+
+la_status la_prefill_state_decay(const void *k, const void *v, const float *gamma, float *S, float *z, int B,
+                                 int H, int N, int dk, int dv, la_dtype dtype, la_stream_t stream)
+{
+    if (B < 0 || H < 0 || N < 0 || dk < 0 || dv < 0) return LA_ERR_INVALID_ARG;
+    if (dtype != LA_F32 && dtype != LA_BF16) return LA_ERR_INVALID_ARG;
+    if ((long long)B * H > 65535) return LA_ERR_UNSUPPORTED;
+    if (B == 0 || H == 0 || dk == 0 || dv == 0) return LA_OK;
+    if (!S || !z || (N > 0 && (!k || !v || !gamma))) return LA_ERR_INVALID_ARG;
+    if (!aligned16(S) || !aligned16(z) || (N > 0 && (!aligned16(k) || !aligned16(v))))
+        return LA_ERR_MISALIGNED;
+    if (N > 0 && ((uintptr_t)gamma & 3u) != 0) return LA_ERR_MISALIGNED;
+    if (!supported_dim(dk) || !supported_dim(dv)) return LA_ERR_UNSUPPORTED;
+    const size_t BH = (size_t)B * H;
+    if (overlaps(S, BH * dk * dv * 4, z, BH * dk * 4)) return LA_ERR_INVALID_ARG;
+    if (N > 0 && (overlaps(gamma, (size_t)H * 4, S, BH * dk * dv * 4) || overlaps(gamma, (size_t)H * 4, z, BH * dk * 4)))
+        return LA_ERR_INVALID_ARG;
+    return state_simt(k, v, S, z, (int)BH, N, dk, dv, dtype, (cudaStream_t)stream, N > 0 ? gamma : nullptr, H);
 }
 
 const char *la_status_string(la_status s)

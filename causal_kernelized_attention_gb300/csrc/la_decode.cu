@@ -4,6 +4,10 @@
 //
 //   S += phi(k) v^T,  z += phi(k),  o = phi(q)^T S / max(phi(q)^T z, eps)
 //
+// The decayed step ("Linear Attention -- Math + Variants", RetNet and gated
+// linear attention: a scalar decay per head on the recurrent state) scales the
+// old state and normaliser first: S = g S + phi(k) v^T, z = g z + phi(k).
+//
 // The step is bound by HBM traffic on S (fp32 read + write, 2*4*dk*dv bytes per
 // head).  One CTA per head: each thread owns 16-byte column groups (float4) of a
 // few rows of S, issues all of its loads before any arithmetic (so a CTA keeps
@@ -49,11 +53,13 @@ __device__ __forceinline__ void st_stream(float4 *p, float4 v)
                  "f"(v.w) : "memory");
 }
 
-// Grid: one CTA per head (blockIdx.x = b*H + h).
-template <typename T, int DK, int DV>
+// Grid: one CTA per head (blockIdx.x = b*H + h).  kDecay: gamma[(b*H + h) % H]
+// scales the old S and z.
+template <typename T, int DK, int DV, bool kDecay>
 __global__ void __launch_bounds__(kDecodeThreads)
 decode_kernel(float *__restrict__ S, float *__restrict__ z, const T *__restrict__ q,
-              const T *__restrict__ k, const T *__restrict__ v, T *__restrict__ o, float eps)
+              const T *__restrict__ k, const T *__restrict__ v, T *__restrict__ o, float eps,
+              const float *__restrict__ gamma, int H)
 {
     constexpr int kCols4 = DV / 4;                       // float4 groups per row
     constexpr int kRowGroups = kDecodeThreads / kCols4;  // threads stacked over rows
@@ -72,6 +78,7 @@ decode_kernel(float *__restrict__ S, float *__restrict__ z, const T *__restrict_
     float4 s[kRows];
 #pragma unroll
     for (int m = 0; m < kRows; ++m) s[m] = ld_stream(Sh + (size_t)(rg + m * kRowGroups) * kCols4 + cg);
+    const float g = kDecay ? gamma[head % H] : 1.f;
 
     for (int r = tid; r < DK; r += kDecodeThreads) {
         fq[r] = Elem<T>::phi(Elem<T>::to_f32(q[head * DK + r]));
@@ -87,6 +94,9 @@ decode_kernel(float *__restrict__ S, float *__restrict__ z, const T *__restrict_
         const int r = rg + m * kRowGroups;
         const float a = fk[r], b = fq[r];
         float4 x = s[m];
+        if (kDecay) {
+            x.x *= g; x.y *= g; x.z *= g; x.w *= g;
+        }
         x.x += a * vc[0]; x.y += a * vc[1]; x.z += a * vc[2]; x.w += a * vc[3];
         st_stream(Sh + (size_t)r * kCols4 + cg, x);
         acc.x += b * x.x; acc.y += b * x.y; acc.z += b * x.z; acc.w += b * x.w;
@@ -96,7 +106,7 @@ decode_kernel(float *__restrict__ S, float *__restrict__ z, const T *__restrict_
     // z update and denominator phi(q) . z_new.
     float d = 0.f;
     for (int r = tid; r < DK; r += kDecodeThreads) {
-        const float zn = z[head * DK + r] + fk[r];
+        const float zn = (kDecay ? g * z[head * DK + r] : z[head * DK + r]) + fk[r];
         z[head * DK + r] = zn;
         d += fq[r] * zn;
     }
@@ -122,36 +132,48 @@ decode_kernel(float *__restrict__ S, float *__restrict__ z, const T *__restrict_
     }
 }
 
+struct DecodeArgs {
+    float *S, *z;
+    const void *q, *k, *v;
+    void *o;
+    int BH;
+    float eps;
+    const float *gamma;
+    int H;
+    cudaStream_t stream;
+};
+
 template <typename T, int DK, int DV>
-la_status launch(float *S, float *z, const void *q, const void *k, const void *v, void *o, int BH,
-                 float eps, cudaStream_t stream)
+la_status launch(const DecodeArgs &a)
 {
     count_launches();
-    decode_kernel<T, DK, DV><<<BH, kDecodeThreads, 0, stream>>>(S, z, (const T *)q, (const T *)k,
-                                                                (const T *)v, (T *)o, eps);
+    if (a.gamma)
+        decode_kernel<T, DK, DV, true><<<a.BH, kDecodeThreads, 0, a.stream>>>(
+            a.S, a.z, (const T *)a.q, (const T *)a.k, (const T *)a.v, (T *)a.o, a.eps, a.gamma, a.H);
+    else
+        decode_kernel<T, DK, DV, false><<<a.BH, kDecodeThreads, 0, a.stream>>>(
+            a.S, a.z, (const T *)a.q, (const T *)a.k, (const T *)a.v, (T *)a.o, a.eps, nullptr, 1);
     return cuda_status(cudaGetLastError());
 }
 
 template <typename T, int DK>
-la_status by_dv(float *S, float *z, const void *q, const void *k, const void *v, void *o, int BH,
-                int dv, float eps, cudaStream_t s)
+la_status by_dv(const DecodeArgs &a, int dv)
 {
     switch (dv) {
-    case 32: return launch<T, DK, 32>(S, z, q, k, v, o, BH, eps, s);
-    case 64: return launch<T, DK, 64>(S, z, q, k, v, o, BH, eps, s);
-    case 128: return launch<T, DK, 128>(S, z, q, k, v, o, BH, eps, s);
+    case 32: return launch<T, DK, 32>(a);
+    case 64: return launch<T, DK, 64>(a);
+    case 128: return launch<T, DK, 128>(a);
     }
     return LA_ERR_UNSUPPORTED;
 }
 
 template <typename T>
-la_status by_dk(float *S, float *z, const void *q, const void *k, const void *v, void *o, int BH, int dk,
-                int dv, float eps, cudaStream_t s)
+la_status by_dk(const DecodeArgs &a, int dk, int dv)
 {
     switch (dk) {
-    case 32: return by_dv<T, 32>(S, z, q, k, v, o, BH, dv, eps, s);
-    case 64: return by_dv<T, 64>(S, z, q, k, v, o, BH, dv, eps, s);
-    case 128: return by_dv<T, 128>(S, z, q, k, v, o, BH, dv, eps, s);
+    case 32: return by_dv<T, 32>(a, dv);
+    case 64: return by_dv<T, 64>(a, dv);
+    case 128: return by_dv<T, 128>(a, dv);
     }
     return LA_ERR_UNSUPPORTED;
 }
@@ -159,11 +181,12 @@ la_status by_dk(float *S, float *z, const void *q, const void *k, const void *v,
 }  // namespace
 
 la_status decode_step(float *S, float *z, const void *q, const void *k, const void *v, void *o, int BH,
-                      int dk, int dv, float eps, la_dtype dtype, cudaStream_t stream)
+                      int dk, int dv, float eps, la_dtype dtype, cudaStream_t stream,
+                      const float *gamma, int H)
 {
     if (!supported_dim(dk) || !supported_dim(dv)) return LA_ERR_UNSUPPORTED;
-    return dtype == LA_F32 ? by_dk<float>(S, z, q, k, v, o, BH, dk, dv, eps, stream)
-                           : by_dk<__nv_bfloat16>(S, z, q, k, v, o, BH, dk, dv, eps, stream);
+    const DecodeArgs a{S, z, q, k, v, o, BH, eps, gamma, H, stream};
+    return dtype == LA_F32 ? by_dk<float>(a, dk, dv) : by_dk<__nv_bfloat16>(a, dk, dv);
 }
 
 }  // namespace la

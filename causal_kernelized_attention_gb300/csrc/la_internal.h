@@ -25,6 +25,10 @@ struct Problem {
     float eps;
     la_dtype dtype;
     cudaStream_t stream;
+    // Decayed state (la_forward_causal_decay): gamma [H] on the device, head of
+    // sequence bh = bh % H; null for the undecayed forms.
+    const float *gamma = nullptr;
+    int H = 1;
 };
 
 // SIMT kernels (la_simt.cu): fp32 CUDA-core arithmetic, any supported dtype.
@@ -33,12 +37,17 @@ la_status noncausal_simt(const Problem &p);
 // Same computation with the library's fixed scratch array (no allocation).
 la_status noncausal_simt_noalloc(const Problem &p);
 // S, z (fp32, [BH,dk,dv], [BH,dk]) = sums over N tokens; overwrites S and z.
+// gamma (device, [H]): token t weighted by gamma[bh % H]^(N-1-t); null: unweighted.
 la_status state_simt(const void *k, const void *v, float *S, float *z, int BH, int N, int dk,
-                     int dv, la_dtype dtype, cudaStream_t stream);
+                     int dv, la_dtype dtype, cudaStream_t stream, const float *gamma = nullptr,
+                     int H = 1);
 
 // Decode step (la_decode.cu).
+// gamma (device, [H], head = bh % H): the decayed step S = g S + phi(k) v^T,
+// z = g z + phi(k); null for the undecayed step.
 la_status decode_step(float *S, float *z, const void *q, const void *k, const void *v, void *o,
-                      int BH, int dk, int dv, float eps, la_dtype dtype, cudaStream_t stream);
+                      int BH, int dk, int dv, float eps, la_dtype dtype, cudaStream_t stream,
+                      const float *gamma = nullptr, int H = 1);
 
 // Tensor-core (tcgen05) paths (la_tc_causal.cu); return LA_ERR_UNSUPPORTED when
 // the problem is outside the shapes they are built for.

@@ -6,6 +6,14 @@
 // the running state S (dk x 32) and z in shared memory ("Linear Attention",
 // aiwiki.thehackersbrain.dev, chunked form: quadratic and masked inside a chunk,
 // recurrent across chunks).
+//
+// The same kernel, instantiated with kDecay, computes the decayed state
+// ("Linear Attention -- Math + Variants", RetNet and gated linear attention:
+// S_t = g S_{t-1} + phi(k_t) v_t^T, z likewise, g a scalar per head).  In
+// chunked form, with powers gp[d] = g^d of the per-head g:
+//   intra-chunk score (a, b <= a)   * gp[a - b]
+//   inter-chunk terms phi(q_a).S, phi(q_a).z   * gp[a + 1]
+//   state after the chunk: gp[len] S + sum_j gp[len - 1 - j] phi(k_j) v_j^T, z likewise.
 #include "la_common.cuh"
 #include "la_internal.h"
 
@@ -23,13 +31,21 @@ struct CausalSmem {
     float S[DK][kDVS];     // running state slice, sum over earlier chunks
     float z[DK];           // running normaliser
     float qrow[kWarps][DK];
+    float gp[C + 1];       // decay powers g^0 .. g^C (decayed form only)
 };
 
-// Grid: (BH, dv / 32).  Block: 256 threads.
-template <typename T, int DK, int C>
+// g^d, evaluated in double and rounded once to fp32 (g^0 = 1 for any g).  It is
+// evaluated at most once per token or chunk offset, so the fp64 rate is immaterial.
+__device__ __forceinline__ float decay_pow(float g, int d)
+{
+    return d == 0 ? 1.f : (float)pow((double)g, (double)d);
+}
+
+// Grid: (BH, dv / 32).  Block: 256 threads.  kDecay: g = gamma[bh % H].
+template <typename T, int DK, int C, bool kDecay>
 __global__ void __launch_bounds__(kThreads)
 causal_simt_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
-                   T *__restrict__ o, int N, int DV, float eps)
+                   T *__restrict__ o, int N, int DV, float eps, const float *__restrict__ gamma, int H)
 {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     auto &sm = *reinterpret_cast<CausalSmem<T, DK, C> *>(smem_raw);
@@ -43,6 +59,10 @@ causal_simt_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__
 
     for (int e = tid; e < DK * kDVS; e += kThreads) (&sm.S[0][0])[e] = 0.f;
     for (int e = tid; e < DK; e += kThreads) sm.z[e] = 0.f;
+    if (kDecay) {
+        const float g = gamma[bh % H];
+        for (int d = tid; d <= C; d += kThreads) sm.gp[d] = decay_pow(g, d);
+    }
 
     for (int i0 = 0; i0 < N; i0 += C) {
         const int len = min(C, N - i0);
@@ -67,6 +87,10 @@ causal_simt_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__
 #pragma unroll 8
             for (int r = 0; r < DK; ++r) num += sm.qrow[warp][r] * sm.S[r][lane];
             for (int r = lane; r < DK; r += 32) den += sm.qrow[warp][r] * sm.z[r];
+            if (kDecay) {
+                num *= sm.gp[a + 1];
+                den *= sm.gp[a + 1];
+            }
             // intra-chunk part: scores s_ab = phi(q_a) . phi(k_b), b <= a (inclusive)
             float s[C / 32];
 #pragma unroll
@@ -75,7 +99,7 @@ causal_simt_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__
                 float acc = 0.f;
 #pragma unroll 8
                 for (int r = 0; r < DK; ++r) acc += sm.qrow[warp][r] * sm.fk[b][r];
-                s[m] = (b <= a) ? acc : 0.f;
+                s[m] = (b <= a) ? (kDecay ? acc * sm.gp[a - b] : acc) : 0.f;
                 den += s[m];
             }
 #pragma unroll
@@ -92,16 +116,18 @@ causal_simt_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__
         }
         __syncthreads();
 
-        // State update: S += phi(K_c)^T V_c, z += column sums of phi(K_c).
+        // State update: S += phi(K_c)^T V_c, z += column sums of phi(K_c)
+        // (decayed: the old state scaled by g^len, token j by g^(len-1-j)).
         for (int e = tid; e < DK * kDVS; e += kThreads) {
             const int r = e / kDVS, c = e % kDVS;
-            float acc = sm.S[r][c];
-            for (int j = 0; j < len; ++j) acc += sm.fk[j][r] * sm.vs[j][c];
+            float acc = kDecay ? sm.S[r][c] * sm.gp[len] : sm.S[r][c];
+            for (int j = 0; j < len; ++j)
+                acc += (kDecay ? sm.fk[j][r] * sm.gp[len - 1 - j] : sm.fk[j][r]) * sm.vs[j][c];
             sm.S[r][c] = acc;
         }
         for (int r = tid; r < DK; r += kThreads) {
-            float acc = sm.z[r];
-            for (int j = 0; j < len; ++j) acc += sm.fk[j][r];
+            float acc = kDecay ? sm.z[r] * sm.gp[len] : sm.z[r];
+            for (int j = 0; j < len; ++j) acc += kDecay ? sm.fk[j][r] * sm.gp[len - 1 - j] : sm.fk[j][r];
             sm.z[r] = acc;
         }
     }
@@ -109,16 +135,19 @@ causal_simt_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__
 
 // Partial prefix states: grid (BH, dv/32, splits).  Each CTA sums phi(k_t) v_t^T over
 // its token range and adds the result into S (and z, from the first column slice)
-// with atomics; S and z must be zero on entry.
+// with atomics; S and z must be zero on entry.  kDecay: token t is weighted by
+// g^(N-1-t), g = gamma[bh % H] (the decayed recurrence unrolled over the prefix).
 constexpr int kStateTile = 64;
 
-template <typename T, int DK>
+template <typename T, int DK, bool kDecay>
 __global__ void __launch_bounds__(kThreads)
 state_simt_kernel(const T *__restrict__ k, const T *__restrict__ v, float *__restrict__ S,
-                  float *__restrict__ z, int N, int DV, int tokens_per_split)
+                  float *__restrict__ z, int N, int DV, int tokens_per_split,
+                  const float *__restrict__ gamma, int H)
 {
     __shared__ float fk[kStateTile][DK];
     __shared__ float vs[kStateTile][kDVS];
+    __shared__ float wt[kStateTile];
     const int bh = blockIdx.x, c0 = blockIdx.y * kDVS;
     const int t0 = blockIdx.z * tokens_per_split;
     const int t1 = min(N, t0 + tokens_per_split);
@@ -133,9 +162,15 @@ state_simt_kernel(const T *__restrict__ k, const T *__restrict__ v, float *__res
     for (int b0 = t0; b0 < t1; b0 += kStateTile) {
         const int len = min(kStateTile, t1 - b0);
         __syncthreads();
+        if (kDecay) {
+            if (tid < kStateTile) wt[tid] = tid < len ? decay_pow(gamma[bh % H], N - 1 - (b0 + tid)) : 0.f;
+            __syncthreads();
+        }
         for (int e = tid; e < kStateTile * DK; e += kThreads) {
             const int j = e / DK, r = e % DK;
-            fk[j][r] = j < len ? Elem<T>::phi(Elem<T>::to_f32(kh[(size_t)(b0 + j) * DK + r])) : 0.f;
+            float f = j < len ? Elem<T>::phi(Elem<T>::to_f32(kh[(size_t)(b0 + j) * DK + r])) : 0.f;
+            if (kDecay) f *= wt[j];
+            fk[j][r] = f;
         }
         for (int e = tid; e < kStateTile * kDVS; e += kThreads) {
             const int j = e / kDVS, c = e % kDVS;
@@ -200,19 +235,19 @@ template <typename T, int DK, int C>
 la_status launch_causal(const Problem &p)
 {
     const size_t smem = sizeof(CausalSmem<T, DK, C>);
-    auto kern = causal_simt_kernel<T, DK, C>;
+    auto kern = p.gamma ? causal_simt_kernel<T, DK, C, true> : causal_simt_kernel<T, DK, C, false>;
     la_status st = ensure_smem((const void *)kern, (int)smem);
     if (st != LA_OK) return st;
     dim3 grid(p.BH, ceil_div(p.dv, kDVS));
     count_launches();
     kern<<<grid, kThreads, smem, p.stream>>>((const T *)p.q, (const T *)p.k, (const T *)p.v, (T *)p.o,
-                                             p.N, p.dv, p.eps);
+                                             p.N, p.dv, p.eps, p.gamma, p.H);
     return cuda_status(cudaGetLastError());
 }
 
 template <typename T, int DK>
 la_status launch_state(const void *k, const void *v, float *S, float *z, int BH, int N, int dv,
-                       cudaStream_t stream)
+                       cudaStream_t stream, const float *gamma = nullptr, int H = 1)
 {
     cudaError_t e = cudaMemsetAsync(S, 0, sizeof(float) * (size_t)BH * DK * dv, stream);
     if (e == cudaSuccess) e = cudaMemsetAsync(z, 0, sizeof(float) * (size_t)BH * DK, stream);
@@ -226,8 +261,12 @@ la_status launch_state(const void *k, const void *v, float *S, float *z, int BH,
     const int per = ceil_div(ceil_div(N, splits), kStateTile) * kStateTile;
     splits = ceil_div(N, per);
     count_launches();
-    state_simt_kernel<T, DK><<<dim3(BH, slices, splits), kThreads, 0, stream>>>(
-        (const T *)k, (const T *)v, S, z, N, dv, per);
+    if (gamma)
+        state_simt_kernel<T, DK, true><<<dim3(BH, slices, splits), kThreads, 0, stream>>>(
+            (const T *)k, (const T *)v, S, z, N, dv, per, gamma, H);
+    else
+        state_simt_kernel<T, DK, false><<<dim3(BH, slices, splits), kThreads, 0, stream>>>(
+            (const T *)k, (const T *)v, S, z, N, dv, per, nullptr, 1);
     return cuda_status(cudaGetLastError());
 }
 
@@ -261,12 +300,12 @@ la_status causal_by_dk(const Problem &p)
 
 template <typename T>
 la_status state_by_dk(const void *k, const void *v, float *S, float *z, int BH, int N, int dk, int dv,
-                      cudaStream_t s)
+                      cudaStream_t s, const float *gamma, int H)
 {
     switch (dk) {
-    case 32: return launch_state<T, 32>(k, v, S, z, BH, N, dv, s);
-    case 64: return launch_state<T, 64>(k, v, S, z, BH, N, dv, s);
-    case 128: return launch_state<T, 128>(k, v, S, z, BH, N, dv, s);
+    case 32: return launch_state<T, 32>(k, v, S, z, BH, N, dv, s, gamma, H);
+    case 64: return launch_state<T, 64>(k, v, S, z, BH, N, dv, s, gamma, H);
+    case 128: return launch_state<T, 128>(k, v, S, z, BH, N, dv, s, gamma, H);
     }
     return LA_ERR_UNSUPPORTED;
 }
@@ -298,11 +337,11 @@ la_status noncausal_simt(const Problem &p)
 }
 
 la_status state_simt(const void *k, const void *v, float *S, float *z, int BH, int N, int dk, int dv,
-                     la_dtype dtype, cudaStream_t stream)
+                     la_dtype dtype, cudaStream_t stream, const float *gamma, int H)
 {
     if (!supported_dim(dk) || !supported_dim(dv)) return LA_ERR_UNSUPPORTED;
-    return dtype == LA_F32 ? state_by_dk<float>(k, v, S, z, BH, N, dk, dv, stream)
-                           : state_by_dk<__nv_bfloat16>(k, v, S, z, BH, N, dk, dv, stream);
+    return dtype == LA_F32 ? state_by_dk<float>(k, v, S, z, BH, N, dk, dv, stream, gamma, H)
+                           : state_by_dk<__nv_bfloat16>(k, v, S, z, BH, N, dk, dv, stream, gamma, H);
 }
 
 }  // namespace la

@@ -155,6 +155,42 @@ la_status la_decode_step(float *S, float *z, const void *q, const void *k, const
                          la_dtype dtype, la_stream_t stream);
 
 /*
+ * Causal forward with a decayed state ("Linear Attention -- Math + Variants",
+ * RetNet and gated linear attention: the recurrent state is multiplied by a
+ * decay before each update, so old tokens fade).  One scalar decay per head:
+ *
+ *   S_i = g S_{i-1} + phi(k_i) v_i^T,   z_i = g z_{i-1} + phi(k_i),
+ *   o_i = phi(q_i)^T S_i / max(phi(q_i)^T z_i, eps)
+ *
+ * i.e. o_i weights key j <= i by g^(i-j) in both the numerator and the
+ * normaliser.  g = 1 gives la_forward_causal; g = 0 gives o_i = v_i wherever
+ * phi(q_i).phi(k_i) >= eps.
+ *
+ *   q, k : [B, H, N, dk]   v, o : [B, H, N, dv]   gamma : [H] fp32, DEVICE memory
+ *
+ * Head h of every batch entry uses gamma[h].  gamma must be 4-byte aligned and
+ * must not overlap o; its values are read by the kernel and not checked (the
+ * method takes them in [0, 1]).  `chunk` (64 or 128) is the length of the
+ * intra-chunk quadratic blocks.  Runs on the CUDA cores in fp32 for both
+ * element types.  Supported: dk, dv in {32, 64, 128}.
+ */
+la_status la_forward_causal_decay(const void *q, const void *k, const void *v, void *o,
+                                  const float *gamma, int B, int H, int N, int dk, int dv,
+                                  int chunk, float eps, la_dtype dtype, la_stream_t stream);
+
+/*
+ * One decode step with a decayed state (same source as la_forward_causal_decay):
+ *
+ *   S = g S + phi(k) v^T;  z = g z + phi(k);  o = phi(q)^T S / max(phi(q)^T z, eps)
+ *
+ * with g = gamma[h] (DEVICE memory, [H] fp32, 4-byte aligned, overlapping none
+ * of S, z, o).  Arguments, layouts and in-place update as la_decode_step.
+ */
+la_status la_decode_step_decay(float *S, float *z, const void *q, const void *k, const void *v,
+                               void *o, const float *gamma, int B, int H, int dk, int dv,
+                               float eps, la_dtype dtype, la_stream_t stream);
+
+/*
  * State of a prefix ("Linear Attention -- Math + Variants": S = sum_j
  * phi(k_j) v_j^T, z = sum_j phi(k_j)), used to start decoding after a causal
  * prefill of N tokens.
@@ -171,6 +207,21 @@ la_status la_decode_step(float *S, float *z, const void *q, const void *k, const
 la_status la_prefill_state(const void *k, const void *v, float *S, float *z,
                            int B, int H, int N, int dk, int dv, la_dtype dtype,
                            la_stream_t stream);
+
+/*
+ * State of a prefix under the decayed recurrence of la_forward_causal_decay
+ * (the recurrence unrolled over N tokens from a zero state):
+ *
+ *   S = sum_t g^(N-1-t) phi(k_t) v_t^T,   z = sum_t g^(N-1-t) phi(k_t),   g = gamma[h]
+ *
+ * so that la_decode_step_decay continues the sequence.  Layouts as
+ * la_prefill_state; gamma as la_forward_causal_decay (DEVICE memory, [H] fp32,
+ * 4-byte aligned, not overlapping S or z; may be NULL when N = 0).  S and z are
+ * OVERWRITTEN; N = 0 writes zeros.  Runs on the CUDA cores in fp32.
+ */
+la_status la_prefill_state_decay(const void *k, const void *v, const float *gamma, float *S,
+                                 float *z, int B, int H, int N, int dk, int dv, la_dtype dtype,
+                                 la_stream_t stream);
 
 /* Human-readable name of a status code (static string, never NULL). */
 const char *la_status_string(la_status s);

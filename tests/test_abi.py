@@ -35,7 +35,9 @@ def test_library_is_in_tree(lib):
 def test_exports_every_declared_symbol(lib):
     names = declared_functions()
     assert set(names) >= {"la_forward_causal", "la_forward_noncausal", "la_decode_step",
-                          "la_prefill_state", "la_status_string", "la_last_cuda_error",
+                          "la_prefill_state", "la_forward_causal_decay", "la_decode_step_decay",
+                          "la_prefill_state_decay",
+                          "la_status_string", "la_last_cuda_error",
                           "la_get_device_status", "la_version"}
     for n in names:
         assert hasattr(lib, n), n
@@ -111,6 +113,53 @@ def test_prefill_validation(lib):
     assert f(A, A, M, A + 0x800000, 1, 1, 8, 64, 64, 1, None) == MISALIGNED
     assert f(A, A, A + 0x700000, A + 0x800000, 1, 1, 8, 24, 64, 1, None) == UNSUPPORTED
     assert f(None, None, None, None, 0, 1, 8, 64, 64, 1, None) == OK
+
+
+def test_causal_decay_validation(lib):
+    f = lib.la_forward_causal_decay
+    e = ctypes.c_float(1e-6)
+    q, k, v, o, g = A, A + 0x100000, A + 0x200000, A + 0x300000, A + 0x400000
+
+    def call(q=q, k=k, v=v, o=o, g=g, B=1, H=2, N=16, dk=64, dv=64, chunk=128, eps=e, dtype=1):
+        return f(q, k, v, o, g, B, H, N, dk, dv, chunk, eps, dtype, None)
+
+    assert call(g=None) == INVALID
+    assert call(g=g + 2) == MISALIGNED
+    assert call(q=None) == INVALID
+    assert call(o=M) == MISALIGNED
+    assert call(chunk=32) == UNSUPPORTED
+    assert call(dk=40) == UNSUPPORTED
+    assert call(eps=ctypes.c_float(-1.0)) == INVALID
+    # gamma inside o
+    assert call(g=o + 16) == INVALID
+    # empty problems are a no-op, even with NULL pointers and NULL gamma
+    assert call(N=0, q=None, k=None, v=None, o=None, g=None) == OK
+
+
+def test_decode_decay_validation(lib):
+    f = lib.la_decode_step_decay
+    e = ctypes.c_float(1e-6)
+    S, z, q, k, v, o, g = (A, A + 0x800000, A + 0x900000, A + 0xA00000, A + 0xB00000, A + 0xC00000,
+                           A + 0xD00000)
+    assert f(S, z, q, k, v, o, None, 2, 2, 64, 64, e, 1, None) == INVALID
+    assert f(S, z, q, k, v, o, g + 1, 2, 2, 64, 64, e, 1, None) == MISALIGNED
+    assert f(S, z, q, k, v, o, S + 64, 2, 2, 64, 64, e, 1, None) == INVALID  # gamma inside S
+    assert f(S, z, q, k, v, o, z + 4, 2, 2, 64, 64, e, 1, None) == INVALID   # gamma inside z
+    assert f(S, z, q, k, v, o, o, 2, 2, 64, 64, e, 1, None) == INVALID       # gamma inside o
+    assert f(None, z, q, k, v, o, g, 2, 2, 64, 64, e, 1, None) == INVALID
+    assert f(S, z, q, k, v, o, g, 2, 2, 64, 96, e, 1, None) == UNSUPPORTED
+    assert f(None, None, None, None, None, None, None, 0, 2, 64, 64, e, 1, None) == OK
+
+
+def test_prefill_decay_validation(lib):
+    f = lib.la_prefill_state_decay
+    S, z, g = A + 0x700000, A + 0x800000, A + 0x900000
+    assert f(A, A, None, S, z, 1, 1, 8, 64, 64, 1, None) == INVALID
+    assert f(A, A, g + 2, S, z, 1, 1, 8, 64, 64, 1, None) == MISALIGNED
+    assert f(A, A, S + 4, S, z, 1, 1, 8, 64, 64, 1, None) == INVALID   # gamma inside S
+    assert f(A, A, g, M, z, 1, 1, 8, 64, 64, 1, None) == MISALIGNED
+    assert f(A, A, g, S, z, 1, 1, 8, 24, 64, 1, None) == UNSUPPORTED
+    assert f(None, None, None, None, None, 0, 1, 8, 64, 64, 1, None) == OK
 
 
 def test_binding_raises_without_cuda_tensors():

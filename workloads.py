@@ -116,6 +116,17 @@ def forward_inputs(w: Workload, N: Optional[int] = None):
     return draw_qkv(w.seed, (w.B, w.H, n, w.dk), (w.B, w.H, n, w.dv), w.sigma, w.dtype)
 
 
+def decay_gammas(H: int, lo: float = 1e-1, hi: float = 1e-3) -> np.ndarray:
+    """Per-head decays for the decayed-state forms: one scalar per head so that
+    heads span several timescales, 1 - gamma log-spaced from `lo` (memory of about
+    10 tokens, the 0.9 of the fixed-decay exercise) down to `hi` (about 1000
+    tokens).  float32 [H]; both the CUDA path and the oracle take these exact values.
+    """
+    if H == 1:
+        return np.array([1.0 - lo], dtype=np.float32)
+    return (1.0 - np.logspace(np.log10(lo), np.log10(hi), H)).astype(np.float32)
+
+
 def random_inputs(seed: int, B: int, H: int, N: int, dk: int, dv: int,
                   dtype: str = "f32", sigma: float = 1.0):
     """Same recipe for arbitrary (test) shapes."""
