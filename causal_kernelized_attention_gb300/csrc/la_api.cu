@@ -250,6 +250,10 @@ la_status la_forward_causal_decay(const void *q, const void *k, const void *v, v
     if (!supported_dim(dk) || !supported_dim(dv)) return LA_ERR_UNSUPPORTED;
     if (overlaps(o, (size_t)B * H * N * dv * elem_size(dtype), gamma, (size_t)H * 4)) return LA_ERR_INVALID_ARG;
     Problem p{q, k, v, o, B * H, N, dk, dv, chunk, eps, dtype, (cudaStream_t)stream, gamma, H};
+    if (dtype == LA_BF16) {
+        st = causal_tc(p);
+        if (st != LA_ERR_UNSUPPORTED) return st;
+    }
     return causal_simt(p);
 }
 

@@ -109,6 +109,7 @@ struct alignas(1024) Smem {
     uint64_t p_full[2];  // per P buffer (the separate layout uses buffer 0)
     uint64_t o_full[2], o_free[2];  // per O buffer (the separate layout uses buffer 0)
     uint64_t o_staged[2];           // all 128 rows of the buffer's O tile are staged in shared memory
+    float gp[32 + kC];              // decayed state: gp[32 + d] = gamma^d for d in [0, C), 0 for d < 0
     uint32_t tmem_base;
     int ticket;
     int abort;
@@ -133,6 +134,9 @@ struct Params {
     // waits on another (no ticket, scan or flags).  0: the scan over L-chunk segments.
     int short_mode;
     int bounds[kMaxShortSegs + 1];
+    // Decayed state: gamma[bh % H] per head (device memory); unused otherwise.
+    const float *gamma;
+    int H;
 };
 
 __device__ __forceinline__ bool wait_bar(int *abort_flag, uint64_t *bar, uint32_t parity)
@@ -222,8 +226,11 @@ __device__ __forceinline__ void issue_state_update(uint32_t tmem, uint32_t ka, u
 // The bf16 copy (and z) of the state for chunk cj + 1, from S_acc once chunk cj's
 // state update is done (s_full).  Fused: into copy (cj + 1) % 2, the caller signals
 // through p_full; separate: the single copy, then s_ready.
-template <int D>
-__device__ __forceinline__ bool refresh_state(Smem<D> &sm, int *abort_flag, uint32_t tl, int i, bool row_ok, int cj)
+// Decayed state: S_acc and z are also scaled in place by gC = gamma^C, ready for the
+// next chunk's update S = gamma^C S + sum_j gamma^(C-1-j) phi(k_j) [v_j | 1]^T.
+template <int D, bool kDecay>
+__device__ __forceinline__ bool refresh_state(Smem<D> &sm, int *abort_flag, uint32_t tl, int i, bool row_ok, int cj,
+                                              float gC)
 {
     using CF = Cfg<D>;
     if (!wait_bar_warp(abort_flag, &sm.s_full, cj & 1)) return false;
@@ -241,10 +248,21 @@ __device__ __forceinline__ bool refresh_state(Smem<D> &sm, int *abort_flag, uint
             to_floats(&a[32], x);
             put_sb<D>(sb_copy<D>(sm.aux, (cj + 1) & 1), i, cc * 64 + 32, x);
         }
+        if constexpr (kDecay) {
+#pragma unroll
+            for (int e = 0; e < 64; ++e) a[e] = __float_as_uint(__uint_as_float(a[e]) * gC);
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4)
+                tmem_st16(tl + CF::tS + cc * 64 + 16 * q4, *reinterpret_cast<const uint32_t(*)[16]>(&a[16 * q4]));
+        }
     }
     const float zv = __uint_as_float(tmem_ld1(tl + CF::tZ));
     tmem_ld_wait();
     if (row_ok) set_z<D>(sm.aux, i, zv, (cj + 1) & 1);
+    if constexpr (kDecay) {
+        tmem_st1(tl + CF::tZ, __float_as_uint(zv * gC));
+        tmem_st_wait();
+    }
     fence_proxy_async_smem();
     if constexpr (!CF::kFused) {
         tc_fence_before();
@@ -257,9 +275,11 @@ __device__ __forceinline__ bool refresh_state(Smem<D> &sm, int *abort_flag, uint
 // 32 query rows (32*quad .. 32*quad+31): block b is entirely visible for b < quad,
 // masked on the diagonal for b == quad, and entirely masked (zeros, no TMEM read)
 // for b > quad.  When t_free is given, it is arrived on once T has been read.
-template <int D>
+// Decayed state: key b of query row a is also weighted by gp[32 + a - b] = gamma^(a - b)
+// (0 for b > a: the table's first 32 entries).
+template <int D, bool kDecay>
 __device__ __forceinline__ void convert_tp(uint32_t tl, uint32_t tPb, int quad, int lane, unsigned blocks,
-                                           uint64_t *t_free)
+                                           uint64_t *t_free, const float *gp)
 {
     uint32_t t[32];
     uint32_t pk[16];
@@ -269,6 +289,11 @@ __device__ __forceinline__ void convert_tp(uint32_t tl, uint32_t tPb, int quad, 
         if (b <= quad) {
             tmem_ld32(tl + Cfg<D>::tT + b * 32, t);
             tmem_ld_wait();
+            if constexpr (kDecay) {
+                const float *w = gp + 32 + 32 * (quad - b) + lane;  // at a - (first key of the block)
+#pragma unroll
+                for (int e = 0; e < 32; ++e) t[e] = __float_as_uint(__uint_as_float(t[e]) * w[-e]);
+            }
             if (b == quad) {
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
@@ -302,8 +327,22 @@ __device__ __forceinline__ void add_state_z(float (&acc)[32], float &zacc, const
     add_state<D>(acc, state, cg0, i);
     zacc += zv;
 }
-
+// add_state_z with the state weighted by w (decayed state: gamma^(tokens since it ended)).
 template <int D>
+__device__ __forceinline__ void add_state_zw(float (&acc)[32], float &zacc, const float *state, int cg0, int i,
+                                             bool want_z, float w)
+{
+    const float zv = want_z ? __ldcg(state + (size_t)D * D + i) : 0.f;
+    const float4 *s4 = reinterpret_cast<const float4 *>(state);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        const float4 x = __ldcg(s4 + (size_t)(cg0 + e) * D + i);
+        acc[4 * e] += w * x.x; acc[4 * e + 1] += w * x.y; acc[4 * e + 2] += w * x.z; acc[4 * e + 3] += w * x.w;
+    }
+    zacc += w * zv;
+}
+
+template <int D, bool kDecay>
 __global__ void __launch_bounds__(576, 1)
 causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                  const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_o,
@@ -408,6 +447,10 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
     const int total = nA + nch;
     const uint32_t tmem = sm.tmem_base;
     int *abort_flag = &sm.abort;
+    // Decayed state: lg = log2(gamma) of this head; phase A weights token t of its
+    // range by gamma^(eA - t), eA = the range's last token.
+    const float lg = kDecay ? log2f(__ldg(prm.gamma + bh % prm.H)) : 0.f;
+    const int eA = (a0 + nA) * kC - 1;
 
     if (warp < kPhiThreads / 32) {
         // ---------------------------------------------------------------- phi warps
@@ -420,8 +463,8 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
             if (isC) {
                 phi_tile<D, kPhiThreads>(sm.k[s], tid, valid);
                 phi_tile<D, kPhiThreads>(sm.q[s], tid, valid);
-            } else {
-                phi_tile<D, 2 * kPhiThreads>(sm.k[s], tid, valid);  // the other half: epilogue warps
+            } else {  // the other half: epilogue warps
+                phi_tile<D, 2 * kPhiThreads, kDecay>(sm.k[s], tid, valid, lg, eA - chunk * kC);
             }
             fence_proxy_async_smem();
             if (isC)
@@ -573,13 +616,19 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
                     if (cj > 0 && !(ok = wait_bar(abort_flag, &sm.o_free[0], (cj - 1) & 1))) break;
                     if (!(ok = wait_bar(abort_flag, &sm.s_ready, cj & 1))) break;
                     tc_fence_after();
+                    if constexpr (kDecay) {  // phi(Q) of the chunk is scaled before p_full
+                        if (!(ok = wait_bar(abort_flag, &sm.p_full[0], cj & 1))) break;
+                        tc_fence_after();
+                    }
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
                         mma_ss(tmem + CF::tO, kmajor(qa, kk), mnmajor(sb_addr, kk, lbo_sb), id_QS, kk > 0 ? 1u : 0u);
                         mma_ss(tmem + CF::tQZ, kmajor(qa, kk), wdesc(w_addr, kk), id_W, kk > 0 ? 1u : 0u);
                     }
-                    if (!(ok = wait_bar(abort_flag, &sm.p_full[0], cj & 1))) break;
-                    tc_fence_after();
+                    if constexpr (!kDecay) {
+                        if (!(ok = wait_bar(abort_flag, &sm.p_full[0], cj & 1))) break;
+                        tc_fence_after();
+                    }
 #pragma unroll
                     for (int kk = 0; kk < kC / 16; ++kk) {
                         mma_ts(tmem + CF::tO, tmem + CF::tP + kk * 8, mnmajor(va, kk, lbo_v), id_PV, 1u);
@@ -616,10 +665,13 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
         // columns [col0, col0 + D/2).
         // Phase A: the epilogue warps are otherwise idle, so they apply phi to the
         // second half of each K tile (units 256..511).
+        if (kDecay && gtid < 32 + kC) sm.gp[gtid] = gtid < 32 ? 0.f : pow_decay(lg, gtid - 32);  // read after phase B's barrier
+        const float gC = pow_decay(lg, kC);
         for (int j = 0; j < nA; ++j) {
             const int s = j % S, r = j / S;
             if (!wait_bar(abort_flag, &sm.full[s], r & 1)) break;
-            phi_tile<D, 2 * kPhiThreads>(sm.k[s], kPhiThreads + gtid, prm.N - job_chunk(j, nA, a0, c0) * kC);
+            const int chunk = job_chunk(j, nA, a0, c0);
+            phi_tile<D, 2 * kPhiThreads, kDecay>(sm.k[s], kPhiThreads + gtid, prm.N - chunk * kC, lg, eA - chunk * kC);
             fence_proxy_async_smem();
             mbar_arrive(&sm.phi_done[s]);
         }
@@ -643,6 +695,12 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
                     tmem_ld32(tl + CF::tS + col0 + cc, a);
                     tmem_ld_wait();
                     to_floats(a, acc);
+                    if constexpr (kDecay) {  // S_acc = gamma^C S for the first chunk's update
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) a[e] = __float_as_uint(acc[e] * gC);
+                        tmem_st16(tl + CF::tS + col0 + cc, *reinterpret_cast<const uint32_t(*)[16]>(&a[0]));
+                        tmem_st16(tl + CF::tS + col0 + cc + 16, *reinterpret_cast<const uint32_t(*)[16]>(&a[16]));
+                    }
                 } else {
                     const uint32_t zero16[16] = {};
 #pragma unroll
@@ -657,6 +715,7 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
                 if (have_agg) {
                     za = __uint_as_float(tmem_ld1(tl + CF::tZ));
                     tmem_ld_wait();
+                    if constexpr (kDecay) tmem_st1(tl + CF::tZ, __float_as_uint(za * gC));
                 } else {
                     tmem_st1(tl + CF::tZ, 0u);
                 }
@@ -746,14 +805,27 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
                 const int cg0 = (col0 + cc) >> 2;
                 const bool want_z = !is_o && cc == 0;
                 if (use_prev && row_ok) {
-                    if (base >= 0) add_state_z<D>(acc, zacc, prm.incl + (head0 + base) * seg_floats, cg0, i, want_z);
-                    int j = base + 1;
-                    for (; j + 1 < g; j += 2) {  // two states per round trip
-                        add_state_z<D>(acc, zacc, prm.agg + (head0 + j) * seg_floats, cg0, i, want_z);
-                        add_state_z<D>(acc, zacc, prm.agg + (head0 + j + 1) * seg_floats, cg0, i, want_z);
+                    if constexpr (kDecay) {
+                        // the state that ended with segment j is weighted by gamma^((g-1-j) L C)
+                        const int seg_tokens = prm.L * kC;
+                        if (base >= 0)
+                            add_state_zw<D>(acc, zacc, prm.incl + (head0 + base) * seg_floats, cg0, i, want_z,
+                                            pow_decay(lg, (g - 1 - base) * seg_tokens));
+                        for (int j = base + 1; j < g; ++j)
+                            add_state_zw<D>(acc, zacc, prm.agg + (head0 + j) * seg_floats, cg0, i, want_z,
+                                            pow_decay(lg, (g - 1 - j) * seg_tokens));
+                    } else {
+                        if (base >= 0) add_state_z<D>(acc, zacc, prm.incl + (head0 + base) * seg_floats, cg0, i, want_z);
+                        int j = base + 1;
+                        for (; j + 1 < g; j += 2) {  // two states per round trip
+                            add_state_z<D>(acc, zacc, prm.agg + (head0 + j) * seg_floats, cg0, i, want_z);
+                            add_state_z<D>(acc, zacc, prm.agg + (head0 + j + 1) * seg_floats, cg0, i, want_z);
+                        }
+                        if (j < g) add_state_z<D>(acc, zacc, prm.agg + (head0 + j) * seg_floats, cg0, i, want_z);
                     }
-                    if (j < g) add_state_z<D>(acc, zacc, prm.agg + (head0 + j) * seg_floats, cg0, i, want_z);
                 }
+                // decayed state: this segment's own aggregate ends L C tokens after acc's state
+                const float gL = kDecay ? pow_decay(lg, prm.L * kC) : 1.f;
                 if (incl_out) {
                     uint32_t a[32];
                     if (have_agg) {
@@ -767,15 +839,23 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
                         float4 *d4 = reinterpret_cast<float4 *>(incl_out);
     #pragma unroll
                         for (int e = 0; e < 8; ++e)
-                            d4[(size_t)(cg0 + e) * D + i] = make_float4(acc[4 * e] + __uint_as_float(a[4 * e]),
-                                                acc[4 * e + 1] + __uint_as_float(a[4 * e + 1]),
-                                                acc[4 * e + 2] + __uint_as_float(a[4 * e + 2]),
-                                                acc[4 * e + 3] + __uint_as_float(a[4 * e + 3]));
+                            d4[(size_t)(cg0 + e) * D + i] = make_float4(gL * acc[4 * e] + __uint_as_float(a[4 * e]),
+                                                gL * acc[4 * e + 1] + __uint_as_float(a[4 * e + 1]),
+                                                gL * acc[4 * e + 2] + __uint_as_float(a[4 * e + 2]),
+                                                gL * acc[4 * e + 3] + __uint_as_float(a[4 * e + 3]));
                     }
                 }
-                tmem_st16(tl + CF::tS + col0 + cc, *reinterpret_cast<const uint32_t(*)[16]>(&acc[0]));
-                tmem_st16(tl + CF::tS + col0 + cc + 16, *reinterpret_cast<const uint32_t(*)[16]>(&acc[16]));
-                if (row_ok) put_sb<D>(sb, i, col0 + cc, acc);
+                if constexpr (kDecay) {  // S_acc = gamma^C S for the first chunk's update
+                    if (row_ok) put_sb<D>(sb, i, col0 + cc, acc);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) acc[e] *= gC;
+                    tmem_st16(tl + CF::tS + col0 + cc, *reinterpret_cast<const uint32_t(*)[16]>(&acc[0]));
+                    tmem_st16(tl + CF::tS + col0 + cc + 16, *reinterpret_cast<const uint32_t(*)[16]>(&acc[16]));
+                } else {
+                    tmem_st16(tl + CF::tS + col0 + cc, *reinterpret_cast<const uint32_t(*)[16]>(&acc[0]));
+                    tmem_st16(tl + CF::tS + col0 + cc + 16, *reinterpret_cast<const uint32_t(*)[16]>(&acc[16]));
+                    if (row_ok) put_sb<D>(sb, i, col0 + cc, acc);
+                }
             }
             if (!is_o) {  // z, by the warps of the first column half
                 if (incl_out) {
@@ -784,9 +864,9 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
                         za = __uint_as_float(tmem_ld1(tl + CF::tZ));
                         tmem_ld_wait();
                     }
-                    if (row_ok) incl_out[(size_t)D * D + i] = zacc + za;
+                    if (row_ok) incl_out[(size_t)D * D + i] = (kDecay ? pow_decay(lg, prm.L * kC) : 1.f) * zacc + za;
                 }
-                tmem_st1(tl + CF::tZ, __float_as_uint(zacc));
+                tmem_st1(tl + CF::tZ, __float_as_uint(kDecay ? zacc * gC : zacc));
                 if (row_ok) set_z<D>(sm.aux, i, zacc, 0);
             }
             tmem_st_wait();
@@ -810,17 +890,26 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
                     // once chunk cj - 1's state update is done, which the MMA thread issues
                     // before T(cj); the first chunk's came from phase B).
                     if (cj >= 2 && !wait_bar_warp(abort_flag, &sm.o_full[cj & 1], ((cj >> 1) - 1) & 1)) break;
-                    if (cj >= 1 && !refresh_state<D>(sm, abort_flag, tl, i, row_ok, cj - 1)) break;
+                    if (cj >= 1 && !refresh_state<D, kDecay>(sm, abort_flag, tl, i, row_ok, cj - 1, gC)) break;
                 }
                 if (!wait_bar_warp(abort_flag, &sm.t_full, cj & 1)) break;
                 const uint32_t tPb = CF::tP + (cj & 1) * CF::kPStride;
                 tc_fence_after();
+                if constexpr (kDecay) {
+                    // T(cj) is done with phi(Q), phi(K) of this chunk: row a of phi(Q) takes
+                    // gamma^(a+1) for phi(Q)[S | z], row j of phi(K) gamma^(C-1-j) for the
+                    // state update (D = 64: the O warps scale phi(K)).
+                    const int s = (nA + cj) % S;
+                    scale_row<D>(sm.q[s], i, pow_decay(lg, i + 1));
+                    if constexpr (!CF::kFused) scale_row<D>(sm.k[s], i, pow_decay(lg, kC - 1 - i));
+                    fence_proxy_async_smem();
+                }
                 // Fused layout: key blocks 0 and 3 here, 1 and 2 by the O warp of the same
                 // lane quadrant (no warp reads more than two blocks); D = 128: all four.
                 if constexpr (CF::kFused)
-                    convert_tp<D>(tl, tPb, quad, lane, 0x9u, nullptr);
+                    convert_tp<D, kDecay>(tl, tPb, quad, lane, 0x9u, nullptr, sm.gp);
                 else
-                    convert_tp<D>(tl, tPb, quad, lane, 0xFu, &sm.t_free);
+                    convert_tp<D, kDecay>(tl, tPb, quad, lane, 0xFu, &sm.t_free, sm.gp);
                 if constexpr (CF::kFused) {  // p_full(cj) also stands for phi of chunk cj + 1
                     if (cj + 1 < nch && !wait_bar_warp(abort_flag, &sm.phi_done[(nA + cj + 1) % S],
                                                        ((nA + cj + 1) / S) & 1))
@@ -844,9 +933,13 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
                     if (it < nch) {
                         if (!wait_bar_warp(abort_flag, &sm.t_full, it & 1)) break;
                         tc_fence_after();
+                        if constexpr (kDecay) {  // phi(K) row j of this chunk: gamma^(C-1-j)
+                            scale_row<D>(sm.k[(nA + it) % S], i, pow_decay(lg, kC - 1 - i));
+                            fence_proxy_async_smem();
+                        }
                         // (P buffer it % 2 is free: these warps saw o_full of chunk it - 2
                         // in the previous iteration)
-                        convert_tp<D>(tl, CF::tP + (it & 1) * CF::kPStride, quad, lane, 0x6u, nullptr);
+                        convert_tp<D, kDecay>(tl, CF::tP + (it & 1) * CF::kPStride, quad, lane, 0x6u, nullptr, sm.gp);
                         tc_fence_before();
                         mbar_arrive(&sm.p_full[it & 1]);
                     }
@@ -911,7 +1004,8 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
                         tma_store_3d_hint(&map_o, sm.q[s] + cc * kBox, 64 * cc, (c0 + cj) * kC, bh, pol_once);
                     tma_store_commit();
                 }
-                if (!CF::kFused && cj < nch - 1 && !refresh_state<D>(sm, abort_flag, tl, i, row_ok, cj)) break;
+                if (!CF::kFused && cj < nch - 1 && !refresh_state<D, kDecay>(sm, abort_flag, tl, i, row_ok, cj, gC))
+                    break;
                 if (leader) {  // slot s may be refilled once the store has read the staged O
                     tma_store_wait_read_all();
                     mbar_arrive(&sm.ostore[s]);
@@ -943,7 +1037,7 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
 }
 
 // ------------------------------------------------------------------ host side
-template <int D>
+template <int D, bool kDecay>
 la_status launch(const Problem &p)
 {
     CUtensorMap mq, mk, mv, mo;
@@ -1033,9 +1127,11 @@ la_status launch(const Problem &p)
     prm.eps = p.eps;
     prm.short_mode = short_mode ? 1 : 0;
     for (int x = 0; x <= G && short_mode; ++x) prm.bounds[x] = bounds[x];
+    prm.gamma = p.gamma;
+    prm.H = p.H;
 
     const int smem = (int)sizeof(Smem<D>);
-    auto kern = causal_tc_kernel<D>;
+    auto kern = causal_tc_kernel<D, kDecay>;
     st = ensure_smem((const void *)kern, smem);
     if (st != LA_OK) return st;
     count_launches();
@@ -1048,7 +1144,8 @@ la_status causal_tc(const Problem &p)
 {
     if (p.dtype != LA_BF16 || p.dk != p.dv || (p.dk != 64 && p.dk != 128) || p.chunk != kC || p.N < kC)
         return LA_ERR_UNSUPPORTED;
-    return p.dk == 128 ? launch<128>(p) : launch<64>(p);
+    if (p.gamma) return p.dk == 128 ? launch<128, true>(p) : launch<64, true>(p);
+    return p.dk == 128 ? launch<128, false>(p) : launch<64, false>(p);
 }
 
 la_status tc_causal_read_status(cudaStream_t s, unsigned *bits)

@@ -82,14 +82,46 @@ __device__ __forceinline__ uint32_t phi2(uint32_t w)
     return *reinterpret_cast<const uint32_t *>(&r);
 }
 
+// Decayed state: gamma^e for an integer e >= 0 from lg = log2(gamma) (gamma^0 = 1
+// for any gamma, including 0, whose lg is -inf).
+__device__ __forceinline__ float pow_decay(float lg, int e)
+{
+    return e == 0 ? 1.f : exp2f((float)e * lg);
+}
+// w times a pair of bf16 values, in fp32 with one rounding back to bf16.
+__device__ __forceinline__ uint32_t scale_bf16x2(uint32_t v, float w)
+{
+    const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&v));
+    return pack_bf16(f.x * w, f.y * w);
+}
+// Row `row` of a 128-row, 128-byte-swizzled bf16 tile of D columns (D / 64 boxes)
+// multiplied by w in place (the swizzle permutes 16-byte chunks within the row, so
+// any chunk order will do: rotated by the row, 8 consecutive rows hit 8 bank groups).
+template <int D>
+__device__ __forceinline__ void scale_row(uint8_t *tile, int row, float w)
+{
+#pragma unroll
+    for (int b = 0; b < D / 64; ++b) {
+        uint4 *rp = reinterpret_cast<uint4 *>(tile + b * kBox + row * 128);
+        uint4 x[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) x[c] = rp[(c + row) & 7];
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+            rp[(c + row) & 7] = make_uint4(scale_bf16x2(x[c].x, w), scale_bf16x2(x[c].y, w),
+                                           scale_bf16x2(x[c].z, w), scale_bf16x2(x[c].w, w));
+    }
+}
+
 // phi in place on one shared-memory tile, by NT threads.  A unit is half of one
 // 128-byte row of a 64-column box (4 chunks of 16 bytes); thread t takes units
 // t, t + NT, ...  Units of rows >= `valid` (past the end of the sequence) are
 // zeroed.  All loads of a thread are issued before its arithmetic.  The chunk
 // order is rotated by the row so that the 8 threads of a quarter-warp (8
 // consecutive rows) touch 8 different bank groups.
-template <int D, int NT>
-__device__ __forceinline__ void phi_tile(uint8_t *tile, int t, int valid)
+// kScale (decayed state): row r is also multiplied by gamma^(ebase - r), lg = log2(gamma).
+template <int D, int NT, bool kScale = false>
+__device__ __forceinline__ void phi_tile(uint8_t *tile, int t, int valid, float lg = 0.f, int ebase = 0)
 {
     constexpr int kUnits = 128 * (D / 32);
     constexpr int NU = (kUnits + NT - 1) / NT;
@@ -107,10 +139,13 @@ __device__ __forceinline__ void phi_tile(uint8_t *tile, int t, int valid)
 #pragma unroll
     for (int m = 0; m < NU; ++m) {
         const int u = t + NT * m, row = u & 127;
+        const float w = kScale ? pow_decay(lg, ebase - row) : 1.f;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             uint4 &x = buf[m][k];
             x = row < valid ? make_uint4(phi2(x.x), phi2(x.y), phi2(x.z), phi2(x.w)) : make_uint4(0u, 0u, 0u, 0u);
+            if (kScale)
+                x = make_uint4(scale_bf16x2(x.x, w), scale_bf16x2(x.y, w), scale_bf16x2(x.z, w), scale_bf16x2(x.w, w));
         }
     }
 #pragma unroll

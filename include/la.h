@@ -171,8 +171,11 @@ la_status la_decode_step(float *S, float *z, const void *q, const void *k, const
  * Head h of every batch entry uses gamma[h].  gamma must be 4-byte aligned and
  * must not overlap o; its values are read by the kernel and not checked (the
  * method takes them in [0, 1]).  `chunk` (64 or 128) is the length of the
- * intra-chunk quadratic blocks.  Runs on the CUDA cores in fp32 for both
- * element types.  Supported: dk, dv in {32, 64, 128}.
+ * intra-chunk quadratic blocks.  bf16 with dk = dv in {64, 128}, chunk 128 and
+ * N >= 128 runs on the tensor cores (the kernel of la_forward_causal with the
+ * decay weights in the intra-chunk mask, on the rows of phi(Q) and phi(K), on
+ * the running state and in the scan across segments); other shapes run on the
+ * CUDA cores in fp32.  Supported: dk, dv in {32, 64, 128}.
  */
 la_status la_forward_causal_decay(const void *q, const void *k, const void *v, void *o,
                                   const float *gamma, int B, int H, int N, int dk, int dv,

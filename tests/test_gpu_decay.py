@@ -69,6 +69,52 @@ def test_causal_decay_special_gammas(orc, chunk):
     np.testing.assert_allclose(got[:, 1], v[:, 1].astype(np.float64), rtol=1e-5, atol=1e-6)
 
 
+@pytest.mark.parametrize("B,H,N,d", [
+    (1, 1, 128, 64), (1, 1, 128, 128), (2, 3, 129, 64), (1, 2, 255, 128), (3, 2, 1000, 64),
+    (2, 3, 2000, 128), (4, 8, 2048, 64), (1, 3, 20000, 64), (1, 2, 20000, 128),
+])
+def test_causal_decay_tensor_core_shapes(orc, B, H, N, d):
+    """Shapes of the tensor-core path (bf16, dk = dv in {64, 128}, chunk 128):
+    ragged last chunks, short sequences split into segments that sum their own
+    decayed prefix, and long sequences whose segments combine decayed
+    aggregates by look-back."""
+    q, k, v = workloads.random_inputs(12000 + N + d, B, H, N, d, d, "bf16")
+    gamma = workloads.decay_gammas(H)
+    got = run_decay(q, k, v, gamma, "bf16", 128)
+    ref = orc.causal_decay_recurrent(q, k, v, gamma.astype(np.float64))
+    e = assert_parity(got, ref, "bf16", (B, H, N, d))
+    assert e["normwise"] < 2e-2, e
+
+
+@pytest.mark.parametrize("B,N,d", [(2, 1000, 64), (1, 3000, 128), (1, 20000, 64)])
+def test_causal_decay_tensor_core_special_gammas(orc, B, N, d):
+    """g = 0 (o_i = v_i), 1/2, 1 (the undecayed form) and 0.999 on the tensor-core path."""
+    H = 4
+    q, k, v = workloads.random_inputs(13000 + N + d, B, H, N, d, d, "bf16")
+    gamma = np.array([0.0, 0.5, 1.0, 0.999], dtype=np.float32)
+    got = run_decay(q, k, v, gamma, "bf16", 128)
+    ref = orc.causal_decay_recurrent(q, k, v, gamma.astype(np.float64))
+    assert_parity(got, ref, "bf16", (B, N, d))
+    assert_parity(got[:, 2], orc.causal_recurrent(q, k, v)[:, 2], "bf16", "g = 1")
+    vv = workloads.bf16_bits_to_f32(v[:, 0]).astype(np.float64)
+    assert np.max(np.abs(got[:, 0] - vv)) <= 2e-2
+
+
+def test_causal_decay_gamma_one_matches_undecayed_tensor_core():
+    """g = 1 on the tensor-core path gives the undecayed kernel's result (every
+    weight is exactly 1; D = 128 accumulates O in another order)."""
+    for d in (64, 128):
+        gen = torch.Generator(device="cuda").manual_seed(21 + d)
+        q, k, v = ((torch.randn((2, 4, 3000, d), device="cuda", generator=gen) * 0.5).to(torch.bfloat16)
+                   for _ in range(3))
+        o1 = la().la_forward_causal(q, k, v)
+        o2 = la().la_forward_causal_decay(q, k, v, torch.ones(4, device="cuda"))
+        torch.cuda.synchronize()
+        assert la().la_get_device_status() == 0
+        diff = (o1.float() - o2.float()).abs().max().item()
+        assert diff <= (0.0 if d == 64 else 1.6e-2), (d, diff)
+
+
 def test_causal_decay_differs_from_undecayed(orc):
     """With g < 1 the output no longer matches the undecayed causal form."""
     q, k, v = workloads.random_inputs(8555, 1, 2, 512, 64, 64, "f32")
