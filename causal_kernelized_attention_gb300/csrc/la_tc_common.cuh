@@ -88,18 +88,22 @@ __device__ __forceinline__ float pow_decay(float lg, int e)
 {
     return e == 0 ? 1.f : exp2f((float)e * lg);
 }
-// w times a pair of bf16 values, in fp32 with one rounding back to bf16.
-__device__ __forceinline__ uint32_t scale_bf16x2(uint32_t v, float w)
+// w times a pair of bf16 values: one packed bf16 multiply by w rounded to bf16
+// (the weight's own rounding, 2^-9 relative, is the size of the operand's).
+__device__ __forceinline__ uint32_t scale_bf16x2(uint32_t v, uint32_t w2)
 {
-    const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&v));
-    return pack_bf16(f.x * w, f.y * w);
+    const __nv_bfloat162 r = __hmul2(*reinterpret_cast<const __nv_bfloat162 *>(&v),
+                                     *reinterpret_cast<const __nv_bfloat162 *>(&w2));
+    return *reinterpret_cast<const uint32_t *>(&r);
 }
+__device__ __forceinline__ uint32_t bf16x2_splat(float w) { return pack_bf16(w, w); }
 // Row `row` of a 128-row, 128-byte-swizzled bf16 tile of D columns (D / 64 boxes)
 // multiplied by w in place (the swizzle permutes 16-byte chunks within the row, so
 // any chunk order will do: rotated by the row, 8 consecutive rows hit 8 bank groups).
 template <int D>
-__device__ __forceinline__ void scale_row(uint8_t *tile, int row, float w)
+__device__ __forceinline__ void scale_row(uint8_t *tile, int row, float wf)
 {
+    const uint32_t w = bf16x2_splat(wf);
 #pragma unroll
     for (int b = 0; b < D / 64; ++b) {
         uint4 *rp = reinterpret_cast<uint4 *>(tile + b * kBox + row * 128);
@@ -139,7 +143,7 @@ __device__ __forceinline__ void phi_tile(uint8_t *tile, int t, int valid, float 
 #pragma unroll
     for (int m = 0; m < NU; ++m) {
         const int u = t + NT * m, row = u & 127;
-        const float w = kScale ? pow_decay(lg, ebase - row) : 1.f;
+        const uint32_t w = kScale ? bf16x2_splat(pow_decay(lg, ebase - row)) : 0u;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             uint4 &x = buf[m][k];
