@@ -492,7 +492,7 @@ def bench_path_causal_decay(torch, la, reps, peaks, src):
     fl = causal_flops(w.BH, w.N, w.dk, w.dv, w.chunk)
     return {"workload": w.name + "_decay", "value": round(w.B * w.N / t, 1), "unit": "tokens/s",
             "ms_per_step": round(t * 1e3, 4), "launches_per_step": launches / reps,
-            "roofline": roofline(fl, nbytes, t, peaks, src, None),
+            "roofline": roofline(fl, nbytes, t, peaks, src, ncu_traffic("causal_decay")),
             "l2": "%d rotating buffer sets" % R}
 
 
@@ -515,7 +515,7 @@ def bench_path_decode_decay(torch, la, steps, peaks, src):
     fl = decode_flops_per_step(w.BH, w.dk, w.dv)
     return {"workload": w.name + "_decay", "value": round(w.B / t, 1), "unit": "tokens/s",
             "ms_per_step": round(t * 1e3, 5), "steps": n, "launches_per_step": launches / n,
-            "roofline": roofline(fl, nbytes, t, peaks, src, None),
+            "roofline": roofline(fl, nbytes, t, peaks, src, ncu_traffic("decode_decay")),
             "l2": "state 270 MB > L2"}
 
 
@@ -650,7 +650,8 @@ def run_gpu(args, dist):
     return 0
 
 
-PROFILE_CASES = ("headline", "causal_long", "causal_long_quarter", "noncausal", "decode", "prefill_state_quarter")
+PROFILE_CASES = ("headline", "causal_long", "causal_long_quarter", "noncausal", "decode", "prefill_state_quarter",
+                 "causal_decay", "decode_decay")
 
 
 def run_profile_case(name: str, launches: int) -> int:
@@ -665,7 +666,23 @@ def run_profile_case(name: str, launches: int) -> int:
     from causal_kernelized_attention_gb300 import build as la_build
     la_build.build()
     la.load_library()
-    if name in ("headline", "causal_long", "causal_long_quarter"):
+    if name == "causal_decay":
+        w = workloads.CAUSAL_BF16
+        q, k, v = workloads.device_forward_inputs(w)
+        o = torch.empty_like(v)
+        g = torch.from_numpy(workloads.decay_gammas(w.H)).cuda()
+        for _ in range(launches):
+            la.la_forward_causal_decay(q, k, v, g, o, chunk=w.chunk, eps=w.eps)
+    elif name == "decode_decay":
+        import dataclasses
+        w = dataclasses.replace(workloads.DECODE_BF16, steps=launches)
+        (qp, kp, vp), (qd, kd, vd) = workloads.device_decode_inputs(w)
+        g = torch.from_numpy(workloads.decay_gammas(w.H)).cuda()
+        S, z = la.la_prefill_state_decay(kp, vp, g)
+        o = torch.empty((w.B, w.H, w.dv), dtype=torch.bfloat16, device="cuda")
+        for t in range(launches):
+            la.la_decode_step_decay(S, z, qd[t], kd[t], vd[t], g, o, eps=w.eps)
+    elif name in ("headline", "causal_long", "causal_long_quarter"):
         w = workloads.CAUSAL_BF16 if name == "headline" else workloads.CAUSAL_BF16_LONG
         if name == "causal_long_quarter":
             import dataclasses
