@@ -496,6 +496,30 @@ def bench_path_causal_decay(torch, la, reps, peaks, src):
             "l2": "%d rotating buffer sets" % R}
 
 
+def bench_path_prefill_decay(torch, la, reps, peaks, src):
+    """la_prefill_state_decay on the decode workload's prefill (4096 heads x 512
+    tokens, d = 128, per-head decays 0.9 .. 0.999)."""
+    w = workloads.DECODE_BF16
+    (qp, kp, vp), (qd, kd, vd) = workloads.device_decode_inputs(w)
+    del qp, qd, kd, vd
+    g = torch.from_numpy(workloads.decay_gammas(w.H)).cuda()
+    S = torch.empty((w.B, w.H, w.dk, w.dv), dtype=torch.float32, device="cuda")
+    z = torch.empty((w.B, w.H, w.dk), dtype=torch.float32, device="cuda")
+
+    def step(i):
+        la.la_prefill_state_decay(kp, vp, g, S, z)
+
+    secs, launches, _ = time_graph_steps(torch, la, step, reps, 3, Dist())
+    t = secs / reps
+    nbytes = w.BH * w.N * (w.dk + w.dv) * 2 + w.BH * w.dk * (w.dv + 1) * 4
+    fl = 2.0 * w.BH * w.N * w.dk * (w.dv + 1)
+    return {"workload": "prefill_state_decay_bf16_b%d_h%d_n%d_d%d" % (w.B, w.H, w.N, w.dk),
+            "value": round(w.B * w.N / t, 1), "unit": "tokens/s", "ms_per_step": round(t * 1e3, 4),
+            "launches_per_step": launches / reps,
+            "roofline": roofline(fl, nbytes, t, peaks, src, ncu_traffic("prefill_state_decay")),
+            "l2": "k, v 1.07 GB > L2"}
+
+
 def bench_path_decode_decay(torch, la, steps, peaks, src):
     """la_decode_step_decay on the decode workload (4096 heads, d = 128, fp32 state)."""
     w = workloads.DECODE_BF16
@@ -617,6 +641,7 @@ def run_gpu(args, dist):
         paths["prefill_state"] = bench_path_prefill(torch, la, max(args.path_reps, 20), peaks, src)
         paths["causal_decay"] = bench_path_causal_decay(torch, la, max(args.path_reps, 20), peaks, src)
         paths["decode_decay"] = bench_path_decode_decay(torch, la, 1024, peaks, src)
+        paths["prefill_state_decay"] = bench_path_prefill_decay(torch, la, max(args.path_reps, 20), peaks, src)
         if s2:
             paths["clocks"] = s2.stop(window=(t_paths, time.time()))
 
@@ -651,7 +676,7 @@ def run_gpu(args, dist):
 
 
 PROFILE_CASES = ("headline", "causal_long", "causal_long_quarter", "noncausal", "decode", "prefill_state_quarter",
-                 "causal_decay", "decode_decay")
+                 "causal_decay", "decode_decay", "prefill_state_decay_quarter")
 
 
 def run_profile_case(name: str, launches: int) -> int:
@@ -697,6 +722,14 @@ def run_profile_case(name: str, launches: int) -> int:
         o = torch.empty_like(v)
         for _ in range(launches):
             la.la_forward_noncausal(q, k, v, o, eps=w.eps)
+    elif name == "prefill_state_decay_quarter":
+        import dataclasses
+        w = dataclasses.replace(workloads.DECODE_BF16, B=workloads.DECODE_BF16.B // 4, steps=1)
+        (qp, kp, vp), _ = workloads.device_decode_inputs(w)
+        g = torch.from_numpy(workloads.decay_gammas(w.H)).cuda()
+        S, z = la.la_prefill_state_decay(kp, vp, g)
+        for _ in range(launches - 1):
+            la.la_prefill_state_decay(kp, vp, g, S, z)
     elif name == "prefill_state_quarter":
         import dataclasses
         w = dataclasses.replace(workloads.DECODE_BF16, B=workloads.DECODE_BF16.B // 4, steps=1)

@@ -310,6 +310,10 @@ la_status la_prefill_state_decay(const void *k, const void *v, const float *gamm
     if (overlaps(S, BH * dk * dv * 4, z, BH * dk * 4)) return LA_ERR_INVALID_ARG;
     if (N > 0 && (overlaps(gamma, (size_t)H * 4, S, BH * dk * dv * 4) || overlaps(gamma, (size_t)H * 4, z, BH * dk * 4)))
         return LA_ERR_INVALID_ARG;
+    if (dtype == LA_BF16 && dk == dv && (dk == 64 || dk == 128) && N >= 128) {
+        const la_status st = noncausal_tc_state(k, v, S, z, (int)BH, N, dk, (cudaStream_t)stream, gamma, H);
+        if (st != LA_ERR_UNSUPPORTED) return st;
+    }
     return state_simt(k, v, S, z, (int)BH, N, dk, dv, dtype, (cudaStream_t)stream, N > 0 ? gamma : nullptr, H);
 }
 

@@ -55,9 +55,10 @@ la_status causal_tc(const Problem &p);
 // (la_tc_noncausal.cu)
 la_status noncausal_tc(const Problem &p);
 // S, z (fp32, [BH,D,D], [BH,D]) = sums over N tokens on the tensor cores (bf16
-// k, v; D in {64, 128}, N >= 128); overwrites S and z.
+// k, v; D in {64, 128}, N >= 128); overwrites S and z.  gamma (device, [H]): token
+// t weighted by gamma[bh % H]^(N-1-t); null: unweighted.
 la_status noncausal_tc_state(const void *k, const void *v, float *S, float *z, int BH, int N, int D,
-                             cudaStream_t stream);
+                             cudaStream_t stream, const float *gamma = nullptr, int H = 1);
 
 // Device status words of translation units that run bounded waits: read and clear.
 la_status tc_causal_read_status(cudaStream_t s, unsigned *bits);

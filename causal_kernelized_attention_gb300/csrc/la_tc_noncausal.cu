@@ -137,7 +137,54 @@ struct Params {
     // State mode (T = 0, no output items): the sums are written to S_out [BH, D, D]
     // (row = key feature) and z_out [BH, D], fp32, row-major; null otherwise.
     float *S_out, *z_out;
+    // State mode, decayed state: token t of head bh weighted by gamma[bh % H]^(N-1-t)
+    // (the decayed recurrence unrolled over the prefix); null otherwise.
+    const float *gamma;
+    int H;
 };
+
+// State mode, decayed state: phi in fp32, times the row's weight gamma^(ebase - row)
+// (lg = log2 gamma), split into bf16 high parts (in place) and low parts (in `lo`).
+__device__ __forceinline__ uint32_t phi2_split_w(uint32_t w, float wt, uint32_t *lo)
+{
+    const __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162 *>(&w);
+    const float a = __bfloat162float(x.x), b = __bfloat162float(x.y);
+    const float pa = (a > 0.f ? a + 1.f : __expf(a)) * wt, pb = (b > 0.f ? b + 1.f : __expf(b)) * wt;
+    const __nv_bfloat16 ha = __float2bfloat16_rn(pa), hb = __float2bfloat16_rn(pb);
+    const __nv_bfloat162 l = __floats2bfloat162_rn(pa - __bfloat162float(ha), pb - __bfloat162float(hb));
+    *lo = *reinterpret_cast<const uint32_t *>(&l);
+    const __nv_bfloat162 h = __halves2bfloat162(ha, hb);
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+template <int D, int NT>
+__device__ __forceinline__ void phi_tile_split_w(uint8_t *tile, uint8_t *lo, int t, int valid, float lg, int ebase)
+{
+    constexpr int kUnits = 128 * (D / 32);
+    constexpr int NU = (kUnits + NT - 1) / NT;
+#pragma unroll 1
+    for (int m = 0; m < NU; ++m) {
+        const int u = t + NT * m, row = u & 127, hb = u >> 7;
+        if (u >= kUnits) break;
+        const uint32_t off = (hb >> 1) * kBox + row * 128;
+        const int rot = row + (hb & 1) * 4;
+        uint4 x[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) x[k] = *reinterpret_cast<const uint4 *>(tile + off + ((rot + k) & 7) * 16);
+        const float wt = row < valid ? pow_decay(lg, ebase - row) : 0.f;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            uint4 h = make_uint4(0u, 0u, 0u, 0u), l = make_uint4(0u, 0u, 0u, 0u);
+            if (row < valid) {
+                h.x = phi2_split_w(x[k].x, wt, &l.x);
+                h.y = phi2_split_w(x[k].y, wt, &l.y);
+                h.z = phi2_split_w(x[k].z, wt, &l.z);
+                h.w = phi2_split_w(x[k].w, wt, &l.w);
+            }
+            *reinterpret_cast<uint4 *>(tile + off + ((rot + k) & 7) * 16) = h;
+            *reinterpret_cast<uint4 *>(lo + off + ((rot + k) & 7) * 16) = l;
+        }
+    }
+}
 
 __device__ __forceinline__ bool wait_bar(int *abort_flag, uint64_t *bar, uint32_t parity)
 {
@@ -370,7 +417,12 @@ noncausal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
                     // MMAs of the tile two before have read that buffer.
                     const int b = j & 1, n = j >> 1;
                     if (n > 0 && !(ok = wait_bar_warp(abort_flag, &sm.lo_free[b], (n - 1) & 1))) break;
-                    phi_tile_split<D, kPhiThreads>(sm.stage[s], b ? sm.lo1 : sm.aux + CF::kImg0, t, valid);
+                    if (prm.gamma)
+                        phi_tile_split_w<D, kPhiThreads>(sm.stage[s], b ? sm.lo1 : sm.aux + CF::kImg0, t, valid,
+                                                         log2f(__ldg(prm.gamma + item.bh % prm.H)),
+                                                         prm.N - 1 - (item.c0 + c) * kC);
+                    else
+                        phi_tile_split<D, kPhiThreads>(sm.stage[s], b ? sm.lo1 : sm.aux + CF::kImg0, t, valid);
                 } else {
                     phi_tile<D, kPhiThreads>(sm.stage[s], t, valid);
                 }
@@ -813,6 +865,8 @@ la_status launch(const Problem &p, float *S_out = nullptr, float *z_out = nullpt
     prm.eps = p.eps;
     prm.S_out = S_out;
     prm.z_out = z_out;
+    prm.gamma = state ? p.gamma : nullptr;
+    prm.H = p.H;
 
     const int smem = (int)sizeof(Smem<D>);
     auto kern = noncausal_tc_kernel<D>;
@@ -833,7 +887,7 @@ la_status noncausal_tc(const Problem &p)
 }
 
 la_status noncausal_tc_state(const void *k, const void *v, float *S, float *z, int BH, int N, int D,
-                             cudaStream_t stream)
+                             cudaStream_t stream, const float *gamma, int H)
 {
     if ((D != 64 && D != 128) || N < kC) return LA_ERR_UNSUPPORTED;
     Problem p{};
@@ -848,6 +902,8 @@ la_status noncausal_tc_state(const void *k, const void *v, float *S, float *z, i
     p.eps = 0.f;
     p.dtype = LA_BF16;
     p.stream = stream;
+    p.gamma = gamma;
+    p.H = H;
     return D == 128 ? launch<128>(p, S, z) : launch<64>(p, S, z);
 }
 

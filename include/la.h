@@ -220,7 +220,9 @@ la_status la_prefill_state(const void *k, const void *v, float *S, float *z,
  * so that la_decode_step_decay continues the sequence.  Layouts as
  * la_prefill_state; gamma as la_forward_causal_decay (DEVICE memory, [H] fp32,
  * 4-byte aligned, not overlapping S or z; may be NULL when N = 0).  S and z are
- * OVERWRITTEN; N = 0 writes zeros.  Runs on the CUDA cores in fp32.
+ * OVERWRITTEN; N = 0 writes zeros.  bf16 with dk = dv in {64, 128} and N >= 128
+ * runs on the tensor cores as la_prefill_state does (phi(k) times its weight in
+ * fp32, split into bf16 high and low parts); other shapes on the CUDA cores in fp32.
  */
 la_status la_prefill_state_decay(const void *k, const void *v, const float *gamma, float *S,
                                  float *z, int B, int H, int N, int dk, int dv, la_dtype dtype,

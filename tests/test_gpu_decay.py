@@ -167,6 +167,40 @@ def test_prefill_state_decay(orc, dtype, N, dk, dv):
     assert es["normwise"] < 1e-5 and ez["normwise"] < 1e-5, (es, ez)
 
 
+@pytest.mark.parametrize("B,H,N,d", [(1, 1, 128, 64), (2, 3, 130, 128), (2, 3, 700, 64), (1, 4, 2000, 128),
+                                     (3, 5, 1025, 64)])
+def test_prefill_state_decay_tensor_core(orc, B, H, N, d):
+    """bf16, dk = dv in {64, 128}, N >= 128: the tensor-core state mode with
+    phi(k) times its weight in fp32, split into bf16 high and low parts."""
+    q, k, v = workloads.random_inputs(9300 + N + d, B, H, N, d, d, "bf16")
+    gamma = workloads.decay_gammas(H)
+    g = torch.from_numpy(gamma).cuda()
+    S, z = la().la_prefill_state_decay(to_dev(k, "bf16"), to_dev(v, "bf16"), g)
+    torch.cuda.synchronize()
+    assert la().la_get_device_status() == 0
+    Sr, zr = oracle_state(orc, k, v, gamma.astype(np.float64), d, d)
+    es, ez = errors(from_dev(S), Sr), errors(from_dev(z), zr)
+    assert es["normwise"] < 1e-5 and ez["normwise"] < 1e-5, (es, ez)
+
+
+def test_decode_decay_after_tensor_core_prefill(orc):
+    """Tensor-core decayed prefill of 300 tokens (d = 128), then 16 decayed steps."""
+    B, H, P, T, d = 2, 4, 300, 16, 128
+    q, k, v = workloads.random_inputs(9700, B, H, P + T, d, d, "bf16")
+    gamma = np.array([0.0, 0.5, 0.99, 1.0], dtype=np.float32)
+    g = torch.from_numpy(gamma).cuda()
+    S, z = la().la_prefill_state_decay(to_dev(k[:, :, :P], "bf16"), to_dev(v[:, :, :P], "bf16"), g)
+    full = orc.causal_decay_recurrent(q, k, v, gamma.astype(np.float64))
+    for t in range(P, P + T):
+        o = la().la_decode_step_decay(S, z, to_dev(q[:, :, t], "bf16"), to_dev(k[:, :, t], "bf16"),
+                                      to_dev(v[:, :, t], "bf16"), g)
+        torch.cuda.synchronize()
+        assert_parity(from_dev(o), full[:, :, t], "bf16", ("step", t))
+    Sr, zr = oracle_state(orc, k, v, gamma.astype(np.float64), d, d)
+    assert errors(from_dev(S), Sr)["normwise"] < 1e-5
+    assert errors(from_dev(z), zr)["normwise"] < 1e-5
+
+
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("dk,dv", [(32, 32), (64, 128), (128, 64), (128, 128)])
 def test_decode_decay_continues_prefill(orc, dtype, dk, dv):
