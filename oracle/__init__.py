@@ -64,6 +64,11 @@ def _declare(lib):
         "la_oracle_causal_decay_recurrent": ([P, P, P, I, P, P, I, I, I, I, D], None),
         "la_oracle_causal_decay_quadratic": ([P, P, P, I, P, P, I, I, I, I, D], None),
         "la_oracle_decode_step_decay": ([P, P, P, P, P, I, P, P, I, I, I, D], None),
+        "la_oracle_causal_general": ([P, P, P, I, P, I, D, I, P, I, I, I, I, D], None),
+        "la_oracle_causal_general_quadratic": ([P, P, P, I, P, I, D, I, P, I, I, I, I, D], None),
+        "la_oracle_prefill_state_general": ([P, P, I, P, I, D, P, P, I, I, I, I], None),
+        "la_oracle_noncausal_general": ([P, P, P, I, I, D, I, P, I, I, I, I, D], None),
+        "la_oracle_decode_step_general": ([P, P, P, P, P, I, P, I, D, I, P, I, I, I, D], None),
         "la_oracle_num_threads": ([], I),
     }
     for name, (args, res) in sigs.items():
@@ -225,6 +230,85 @@ class Oracle:
         if BH:
             self.lib.la_oracle_decode_step_decay(_ptr(S), _ptr(z), _ptr(q), _ptr(k), _ptr(v), t, _ptr(g),
                                                  _ptr(o), BH, dk, dv, float(eps))
+        return o
+
+    # ------------------------------------------------ feature maps and the normaliser
+    # fmap: 0 = elu + 1, 1 = max(x, 0) + shift, 2 = x + shift; normalize: divide by
+    # max(phi(q)^T z, eps) or not; gamma: None (no decay) or broadcast to the heads.
+    FMAPS = {"elu1": 0, "relu": 1, "identity": 2}
+
+    def _gptr(self, gamma, lead):
+        if gamma is None:
+            return None, None
+        g = self._gamma(gamma, lead)
+        return g, _ptr(g)
+
+    def _fwd_general(self, fname, q, k, v, gamma, fmap, shift, normalize, eps):
+        (q, k, v), t = _prep(q, k, v)
+        N, dk = q.shape[-2], q.shape[-1]
+        dv = v.shape[-1]
+        lead = q.shape[:-2]
+        if k.shape != q.shape or v.shape[:-1] != q.shape[:-1]:
+            raise ValueError("shape mismatch")
+        g, gp = self._gptr(gamma, lead)
+        BH = int(np.prod(lead)) if lead else 1
+        o = np.empty(lead + (N, dv), dtype=np.float64)
+        if BH and N and dv:
+            getattr(self.lib, fname)(_ptr(q), _ptr(k), _ptr(v), t, gp, self.FMAPS[fmap], float(shift),
+                                     int(bool(normalize)), _ptr(o), BH, N, dk, dv, float(eps))
+        return o
+
+    def causal_general(self, q, k, v, gamma=None, fmap="elu1", shift=0.0, normalize=True, eps=1e-6):
+        """The causal recurrence with a feature map, an optional decay and an optional normaliser."""
+        return self._fwd_general("la_oracle_causal_general", q, k, v, gamma, fmap, shift, normalize, eps)
+
+    def causal_general_quadratic(self, q, k, v, gamma=None, fmap="elu1", shift=0.0, normalize=True,
+                                 eps=1e-6):
+        return self._fwd_general("la_oracle_causal_general_quadratic", q, k, v, gamma, fmap, shift,
+                                 normalize, eps)
+
+    def noncausal_general(self, q, k, v, fmap="elu1", shift=0.0, normalize=True, eps=1e-6):
+        (q, k, v), t = _prep(q, k, v)
+        N, dk = q.shape[-2], q.shape[-1]
+        dv = v.shape[-1]
+        lead = q.shape[:-2]
+        BH = int(np.prod(lead)) if lead else 1
+        o = np.empty(lead + (N, dv), dtype=np.float64)
+        if BH and N and dv:
+            self.lib.la_oracle_noncausal_general(_ptr(q), _ptr(k), _ptr(v), t, self.FMAPS[fmap], float(shift),
+                                                 int(bool(normalize)), _ptr(o), BH, N, dk, dv, float(eps))
+        return o
+
+    def prefill_state_general(self, k, v, gamma=None, fmap="elu1", shift=0.0):
+        (k, v), t = _prep(k, v)
+        N, dk, dv = k.shape[-2], k.shape[-1], v.shape[-1]
+        lead = k.shape[:-2]
+        g, gp = self._gptr(gamma, lead)
+        BH = int(np.prod(lead)) if lead else 1
+        S = np.zeros(lead + (dk, dv), dtype=np.float64)
+        z = np.zeros(lead + (dk,), dtype=np.float64)
+        if BH:
+            self.lib.la_oracle_prefill_state_general(_ptr(k), _ptr(v), t, gp, self.FMAPS[fmap], float(shift),
+                                                     _ptr(S), _ptr(z), BH, N, dk, dv)
+        return S, z
+
+    def decode_step_general(self, S, z, q, k, v, gamma=None, fmap="elu1", shift=0.0, normalize=True,
+                            eps=1e-6):
+        if S.dtype != np.float64 or z.dtype != np.float64 or not S.flags.c_contiguous \
+                or not z.flags.c_contiguous:
+            raise TypeError("S and z must be C-contiguous float64 (updated in place)")
+        (q, k, v), t = _prep(q, k, v)
+        dk, dv = q.shape[-1], v.shape[-1]
+        lead = q.shape[:-1]
+        BH = int(np.prod(lead)) if lead else 1
+        if S.shape != lead + (dk, dv) or z.shape != lead + (dk,):
+            raise ValueError("state shape mismatch")
+        g, gp = self._gptr(gamma, lead)
+        o = np.empty(lead + (dv,), dtype=np.float64)
+        if BH:
+            self.lib.la_oracle_decode_step_general(_ptr(S), _ptr(z), _ptr(q), _ptr(k), _ptr(v), t, gp,
+                                                   self.FMAPS[fmap], float(shift), int(bool(normalize)),
+                                                   _ptr(o), BH, dk, dv, float(eps))
         return o
 
 

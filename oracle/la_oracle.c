@@ -25,7 +25,10 @@
  *     ([mlblogg] "The causal recurrence"; [learn] Developer listing);
  *   - no 1/sqrt(d) scaling of q or k (only softmax scales, [math]);
  *   - state and all arithmetic in double; inputs are given as float64,
- *     float32 or bf16 bit patterns and widened exactly.
+ *     float32 or bf16 bit patterns and widened exactly;
+ *   - variants (the *_general forms): the decay, the ReLU and identity-plus-
+ *     shift feature maps and the normaliser-free output compose freely; the
+ *     decayed normaliser z decays with the same gamma as S.
  *
  * Tensor layouts (row-major, contiguous):
  *   q, k [BH, N, dk];  v, o [BH, N, dv];  S [BH, dk, dv];  z [BH, dk].
@@ -485,6 +488,226 @@ void la_oracle_decode_step_decay(double *S, double *z, const void *q, const void
             for (int r = 0; r < dk; ++r)
                 s += fq[r] * Sb[(size_t)r * dv + c];
             ob[c] = s / den;
+        }
+        free(fq); free(fk);
+    }
+}
+
+/* ---------------------------------------------------------------------------
+ * Variants of the feature map and of the normaliser, for every form above.
+ *
+ * Feature maps ([learn] "What the pieces are for": ReLU among the other
+ * choices; [math] "Feature-map families": ReLU and identity-plus-shift;
+ * [problems] "Key Functions & Tricks": relu(x) + eps):
+ *   map 0: elu(x) + 1 (the default; the shift is ignored),
+ *   map 1: max(x, 0) + c,
+ *   map 2: x + c.
+ * Normaliser ([math] "Implementation reality": most variants drop phi(q)^T z
+ * and normalise the output with a layer after attention): normalize = 1 gives
+ * o = phi(q)^T S / max(phi(q)^T z, eps); normalize = 0 gives o = phi(q)^T S.
+ * gamma: NULL for no decay, else [BH] (the decayed state above).
+ * ------------------------------------------------------------------------- */
+static double phi_map(double x, int map, double c)
+{
+    if (map == 1)
+        return (x > 0.0 ? x : 0.0) + c;
+    if (map == 2)
+        return x + c;
+    return la_oracle_phi(x);
+}
+
+static void phi_row_map(const void *x, int type, int64_t base, int t, int d, int map, double c, double *out)
+{
+    for (int i = 0; i < d; ++i)
+        out[i] = phi_map(load(x, type, base + (int64_t)t * d + i), map, c);
+}
+
+/* The recurrence with a feature map, an optional decay and an optional normaliser. */
+void la_oracle_causal_general(const void *q, const void *k, const void *v, int type,
+                              const double *gamma, int map, double shift, int normalize,
+                              double *o, int BH, int N, int dk, int dv, double eps)
+{
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int bh = 0; bh < BH; ++bh) {
+        const double g = gamma ? gamma[bh] : 1.0;
+        double *S = calloc((size_t)dk * dv, sizeof(double));
+        double *z = calloc((size_t)dk, sizeof(double));
+        double *fq = malloc(sizeof(double) * dk);
+        double *fk = malloc(sizeof(double) * dk);
+        double *vt = malloc(sizeof(double) * dv);
+        const int64_t qb = (int64_t)bh * N * dk, vb = (int64_t)bh * N * dv;
+        for (int t = 0; t < N; ++t) {
+            phi_row_map(q, type, qb, t, dk, map, shift, fq);
+            phi_row_map(k, type, qb, t, dk, map, shift, fk);
+            for (int c = 0; c < dv; ++c)
+                vt[c] = load(v, type, vb + (int64_t)t * dv + c);
+            for (int r = 0; r < dk; ++r) {
+                double *Sr = S + (size_t)r * dv;
+                for (int c = 0; c < dv; ++c)
+                    Sr[c] = g * Sr[c] + fk[r] * vt[c];
+                z[r] = g * z[r] + fk[r];
+            }
+            double *ot = o + vb + (int64_t)t * dv;
+            for (int c = 0; c < dv; ++c)
+                ot[c] = 0.0;
+            for (int r = 0; r < dk; ++r) {
+                const double *Sr = S + (size_t)r * dv;
+                for (int c = 0; c < dv; ++c)
+                    ot[c] += fq[r] * Sr[c];
+            }
+            if (normalize) {
+                double den = 0.0;
+                for (int r = 0; r < dk; ++r)
+                    den += fq[r] * z[r];
+                den = clamp_den(den, eps);
+                for (int c = 0; c < dv; ++c)
+                    ot[c] /= den;
+            }
+        }
+        free(S); free(z); free(fq); free(fk); free(vt);
+    }
+}
+
+/* The same function as masked (and weighted) scores: s_ij = g^(i-j)
+ * phi(q_i).phi(k_j) for j <= i; o = s V, divided by the row sums when
+ * normalize.  O(N^2): cross-check only. */
+void la_oracle_causal_general_quadratic(const void *q, const void *k, const void *v, int type,
+                                        const double *gamma, int map, double shift, int normalize,
+                                        double *o, int BH, int N, int dk, int dv, double eps)
+{
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int bh = 0; bh < BH; ++bh) {
+        const double g = gamma ? gamma[bh] : 1.0;
+        double *fq = malloc(sizeof(double) * dk);
+        double *fk = malloc(sizeof(double) * dk);
+        const int64_t qb = (int64_t)bh * N * dk, vb = (int64_t)bh * N * dv;
+        for (int i = 0; i < N; ++i) {
+            phi_row_map(q, type, qb, i, dk, map, shift, fq);
+            double *oi = o + vb + (int64_t)i * dv;
+            for (int c = 0; c < dv; ++c)
+                oi[c] = 0.0;
+            double rowsum = 0.0;
+            for (int j = 0; j <= i; ++j) {
+                phi_row_map(k, type, qb, j, dk, map, shift, fk);
+                double s = 0.0;
+                for (int r = 0; r < dk; ++r)
+                    s += fq[r] * fk[r];
+                s *= (i == j) ? 1.0 : pow(g, (double)(i - j));
+                rowsum += s;
+                for (int c = 0; c < dv; ++c)
+                    oi[c] += s * load(v, type, vb + (int64_t)j * dv + c);
+            }
+            if (normalize) {
+                rowsum = clamp_den(rowsum, eps);
+                for (int c = 0; c < dv; ++c)
+                    oi[c] /= rowsum;
+            }
+        }
+        free(fq); free(fk);
+    }
+}
+
+/* Prefix state under a feature map and an optional decay: S = sum_t
+ * g^(N-1-t) phi(k_t) v_t^T, z likewise (the recurrence from a zero state). */
+void la_oracle_prefill_state_general(const void *k, const void *v, int type, const double *gamma,
+                                     int map, double shift, double *S, double *z, int BH, int N,
+                                     int dk, int dv)
+{
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int bh = 0; bh < BH; ++bh) {
+        const double g = gamma ? gamma[bh] : 1.0;
+        double *Sb = S + (size_t)bh * dk * dv;
+        double *zb = z + (size_t)bh * dk;
+        double *fk = malloc(sizeof(double) * dk);
+        const int64_t kb = (int64_t)bh * N * dk, vb = (int64_t)bh * N * dv;
+        for (size_t e = 0; e < (size_t)dk * dv; ++e)
+            Sb[e] = 0.0;
+        for (int r = 0; r < dk; ++r)
+            zb[r] = 0.0;
+        for (int t = 0; t < N; ++t) {
+            phi_row_map(k, type, kb, t, dk, map, shift, fk);
+            for (int r = 0; r < dk; ++r) {
+                for (int c = 0; c < dv; ++c)
+                    Sb[(size_t)r * dv + c] = g * Sb[(size_t)r * dv + c] +
+                                             fk[r] * load(v, type, vb + (int64_t)t * dv + c);
+                zb[r] = g * zb[r] + fk[r];
+            }
+        }
+        free(fk);
+    }
+}
+
+/* Non-causal form under a feature map, with or without the normaliser. */
+void la_oracle_noncausal_general(const void *q, const void *k, const void *v, int type, int map,
+                                 double shift, int normalize, double *o, int BH, int N, int dk,
+                                 int dv, double eps)
+{
+    double *S = malloc(sizeof(double) * (size_t)BH * dk * dv);
+    double *z = malloc(sizeof(double) * (size_t)BH * dk);
+    la_oracle_prefill_state_general(k, v, type, NULL, map, shift, S, z, BH, N, dk, dv);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int bh = 0; bh < BH; ++bh) {
+        const double *Sb = S + (size_t)bh * dk * dv;
+        const double *zb = z + (size_t)bh * dk;
+        double *fq = malloc(sizeof(double) * dk);
+        const int64_t qb = (int64_t)bh * N * dk, vb = (int64_t)bh * N * dv;
+        for (int i = 0; i < N; ++i) {
+            phi_row_map(q, type, qb, i, dk, map, shift, fq);
+            double den = 1.0;
+            if (normalize) {
+                den = 0.0;
+                for (int r = 0; r < dk; ++r)
+                    den += fq[r] * zb[r];
+                den = clamp_den(den, eps);
+            }
+            double *oi = o + vb + (int64_t)i * dv;
+            for (int c = 0; c < dv; ++c) {
+                double s = 0.0;
+                for (int r = 0; r < dk; ++r)
+                    s += fq[r] * Sb[(size_t)r * dv + c];
+                oi[c] = normalize ? s / den : s;
+            }
+        }
+        free(fq);
+    }
+    free(S); free(z);
+}
+
+/* One decode step under a feature map, an optional decay and an optional
+ * normaliser: S = g S + phi(k) v^T, z = g z + phi(k), then the read. */
+void la_oracle_decode_step_general(double *S, double *z, const void *q, const void *k, const void *v,
+                                   int type, const double *gamma, int map, double shift, int normalize,
+                                   double *o, int BH, int dk, int dv, double eps)
+{
+#pragma omp parallel for schedule(static)
+    for (int bh = 0; bh < BH; ++bh) {
+        const double g = gamma ? gamma[bh] : 1.0;
+        double *Sb = S + (size_t)bh * dk * dv;
+        double *zb = z + (size_t)bh * dk;
+        double *ob = o + (size_t)bh * dv;
+        double *fq = malloc(sizeof(double) * dk);
+        double *fk = malloc(sizeof(double) * dk);
+        for (int r = 0; r < dk; ++r) {
+            fq[r] = phi_map(load(q, type, (int64_t)bh * dk + r), map, shift);
+            fk[r] = phi_map(load(k, type, (int64_t)bh * dk + r), map, shift);
+        }
+        for (int r = 0; r < dk; ++r) {
+            for (int c = 0; c < dv; ++c)
+                Sb[(size_t)r * dv + c] = g * Sb[(size_t)r * dv + c] + fk[r] * load(v, type, (int64_t)bh * dv + c);
+            zb[r] = g * zb[r] + fk[r];
+        }
+        double den = 1.0;
+        if (normalize) {
+            den = 0.0;
+            for (int r = 0; r < dk; ++r)
+                den += fq[r] * zb[r];
+            den = clamp_den(den, eps);
+        }
+        for (int c = 0; c < dv; ++c) {
+            double s = 0.0;
+            for (int r = 0; r < dk; ++r)
+                s += fq[r] * Sb[(size_t)r * dv + c];
+            ob[c] = normalize ? s / den : s;
         }
         free(fq); free(fk);
     }

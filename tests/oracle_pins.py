@@ -365,4 +365,156 @@ def pin_decode_decay_continues_causal(orc):
     assert _rel_err(o, weighted_pairwise(q, k, v, g)[:, -1]) < 1e-12
 
 
+# ----------------------------------------------------------------------------
+# feature maps and the normaliser ("Linear attention", What the pieces are for:
+# ReLU; "Linear Attention -- Math + Variants", Feature-map families: ReLU and
+# identity-plus-shift, Implementation reality: dropping the normaliser;
+# "26. Linear (Kernelized) Attention", Key Functions & Tricks: relu(x) + eps)
+# ----------------------------------------------------------------------------
+def feature_np(x, fmap, shift):
+    x = np.asarray(x, dtype=np.float64)
+    if fmap == "relu":
+        return np.maximum(x, 0.0) + shift
+    if fmap == "identity":
+        return x + shift
+    return phi_np(x)
+
+
+def general_pairwise(q, k, v, g, fmap, shift, normalize, causal=True, eps=EPS):
+    """Dense numpy per sequence: scores g^(i-j) f(q_i).f(k_j) (j <= i when causal;
+    g = None: no decay), o = scores v, divided by max(row sums, eps) when normalize."""
+    out = []
+    for s in range(q.shape[0]):
+        fq, fk = feature_np(q[s], fmap, shift), feature_np(k[s], fmap, shift)
+        n = fq.shape[0]
+        i, j = np.meshgrid(np.arange(n), np.arange(n), indexing="ij")
+        w = np.ones((n, n)) if g is None else float(g[s]) ** np.maximum(i - j, 0)
+        if causal:
+            w = np.where(j <= i, w, 0.0)
+        scores = (fq @ fk.T) * w
+        o = scores @ np.asarray(v[s], dtype=np.float64)
+        if normalize:
+            o = o / np.maximum(scores.sum(-1, keepdims=True), eps)
+        out.append(o)
+    return np.stack(out)
+
+
+def pin_general_default_is_the_pinned_forms(orc):
+    """The general recurrence with elu + 1 and the normaliser is the pinned causal
+    form, with a decay the pinned decayed form (bit for bit: same arithmetic)."""
+    q, k, v = _rand(2000, 3, 25, 5, 4)
+    assert np.array_equal(orc.causal_general(q, k, v), orc.causal_recurrent(q, k, v, EPS))
+    g = np.array([0.9, 0.5, 1.0])
+    assert np.array_equal(orc.causal_general(q, k, v, gamma=g), orc.causal_decay_recurrent(q, k, v, g, EPS))
+
+
+def pin_general_equals_numpy_pairwise(orc):
+    """Every map x normaliser x decay against the dense numpy form above (and the
+    oracle's own quadratic form against it too)."""
+    q, k, v = _rand(2010, 3, 40, 6, 5)
+    for fmap, shift in (("relu", 0.0), ("relu", 0.25), ("identity", 0.5), ("elu1", 0.0)):
+        for normalize in (True, False):
+            for g in (None, np.array([0.9, 0.6, 1.0])):
+                ref = general_pairwise(q, k, v, g, fmap, shift, normalize)
+                got = orc.causal_general(q, k, v, gamma=g, fmap=fmap, shift=shift, normalize=normalize)
+                assert _rel_err(got, ref) < 1e-12, (fmap, shift, normalize, g is None)
+                got = orc.causal_general_quadratic(q, k, v, gamma=g, fmap=fmap, shift=shift, normalize=normalize)
+                assert _rel_err(got, ref) < 1e-12, (fmap, shift, normalize, g is None)
+
+
+def pin_general_exact_integers(orc):
+    """Identity map without shift, no normaliser, small integers: every value is an
+    integer below 2^53, so the float64 result equals exact integer arithmetic."""
+    rng = np.random.default_rng(2020)
+    N, dk, dv = 9, 4, 3
+    q = rng.integers(-5, 6, size=(1, N, dk)).astype(np.float64)
+    k = rng.integers(-5, 6, size=(1, N, dk)).astype(np.float64)
+    v = rng.integers(-7, 8, size=(1, N, dv)).astype(np.float64)
+    got = orc.causal_general(q, k, v, fmap="identity", shift=0.0, normalize=False)[0]
+    qi, ki, vi = q[0].astype(int).tolist(), k[0].astype(int).tolist(), v[0].astype(int).tolist()
+    for i in range(N):
+        for c in range(dv):
+            exact = sum(sum(a * b for a, b in zip(qi[i], ki[j])) * vi[j][c] for j in range(i + 1))
+            assert got[i, c] == exact
+    # relu + 1 of integers: max(x, 0) + 1, again all integers
+    got = orc.causal_general(q, k, v, fmap="relu", shift=1.0, normalize=False)[0]
+    fq = [[max(a, 0) + 1 for a in row] for row in qi]
+    fk = [[max(a, 0) + 1 for a in row] for row in ki]
+    for i in range(N):
+        for c in range(dv):
+            exact = sum(sum(a * b for a, b in zip(fq[i], fk[j])) * vi[j][c] for j in range(i + 1))
+            assert got[i, c] == exact
+
+
+def pin_unnormalized_ones_is_the_denominator(orc):
+    """Without the normaliser, v = 1 gives the denominator sum_j w_ij f(q_i).f(k_j); the
+    normalised output is the unnormalised one divided by max(that, eps)."""
+    q, k, v = _rand(2030, 2, 30, 5, 4)
+    g = np.array([0.8, 1.0])
+    ones = np.ones((2, 30, 1))
+    for fmap, shift in (("relu", 0.1), ("elu1", 0.0), ("identity", 3.0)):
+        den = orc.causal_general(q, k, ones, gamma=g, fmap=fmap, shift=shift, normalize=False)
+        raw = orc.causal_general(q, k, v, gamma=g, fmap=fmap, shift=shift, normalize=False)
+        nrm = orc.causal_general(q, k, v, gamma=g, fmap=fmap, shift=shift, normalize=True)
+        assert _rel_err(nrm, raw / np.maximum(den, EPS)) < 1e-13, fmap
+
+
+def pin_relu_dead_queries_give_zero(orc):
+    """ReLU without shift: a query with no positive component has f(q) = 0, so the
+    numerator is 0 and the clamped denominator eps gives o = 0 (normalised or not)."""
+    q, k, v = _rand(2040, 2, 20, 4, 3)
+    q = -np.abs(q)
+    for normalize in (True, False):
+        o = orc.causal_general(q, k, v, fmap="relu", shift=0.0, normalize=normalize)
+        assert np.all(o == 0.0)
+
+
+def pin_relu_on_nonnegative_is_identity(orc):
+    """For q, k >= 0, max(x, 0) + c = x + c: the two maps agree exactly."""
+    q, k, v = _rand(2050, 2, 20, 4, 3)
+    q, k = np.abs(q), np.abs(k)
+    for normalize in (True, False):
+        a = orc.causal_general(q, k, v, fmap="relu", shift=0.3, normalize=normalize)
+        b = orc.causal_general(q, k, v, fmap="identity", shift=0.3, normalize=normalize)
+        assert np.array_equal(a, b)
+
+
+def pin_general_noncausal_equals_pairwise(orc):
+    q, k, v = _rand(2060, 3, 30, 5, 4)
+    for fmap, shift in (("relu", 0.0), ("relu", 0.5), ("identity", 2.0), ("elu1", 0.0)):
+        for normalize in (True, False):
+            ref = general_pairwise(q, k, v, None, fmap, shift, normalize, causal=False)
+            got = orc.noncausal_general(q, k, v, fmap=fmap, shift=shift, normalize=normalize)
+            assert _rel_err(got, ref) < 1e-12, (fmap, normalize)
+
+
+def pin_general_prefill_state(orc):
+    """S = sum_t g^(N-1-t) f(k_t) v_t^T, z = sum_t g^(N-1-t) f(k_t), as numpy sums."""
+    BH, N, dk, dv = 3, 25, 5, 4
+    q, k, v = _rand(2070, BH, N, dk, dv)
+    g = np.array([0.9, 0.0, 1.0])
+    for fmap, shift in (("relu", 0.2), ("identity", 0.0), ("elu1", 0.0)):
+        S, z = orc.prefill_state_general(k, v, gamma=g, fmap=fmap, shift=shift)
+        fk = feature_np(k, fmap, shift)
+        w = g[:, None] ** (N - 1 - np.arange(N))[None, :]
+        Sr = np.einsum("bt,btr,btc->brc", w, fk, v)
+        zr = np.einsum("bt,btr->br", w, fk)
+        assert _rel_err(S, Sr) < 1e-12 and _rel_err(z, zr) < 1e-12, fmap
+
+
+def pin_general_decode_continues_causal(orc):
+    """General decode steps from a zero state reproduce the general causal forward."""
+    BH, N, dk, dv = 3, 16, 5, 4
+    q, k, v = _rand(2080, BH, N, dk, dv)
+    g = np.array([0.95, 0.5, 1.0])
+    for fmap, shift, normalize in (("relu", 0.1, True), ("identity", 0.0, False), ("relu", 0.0, False)):
+        full = orc.causal_general(q, k, v, gamma=g, fmap=fmap, shift=shift, normalize=normalize)
+        S = np.zeros((BH, dk, dv))
+        z = np.zeros((BH, dk))
+        for t in range(N):
+            o = orc.decode_step_general(S, z, q[:, t], k[:, t], v[:, t], gamma=g, fmap=fmap, shift=shift,
+                                        normalize=normalize)
+            assert _rel_err(o, full[:, t]) < 1e-12, (fmap, t)
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -52,6 +52,14 @@ MUTANTS = {
     # decayed decode: state not decayed
     "decode_decay_state_undecayed": ("Sb[(size_t)r * dv + c] = g * Sb[(size_t)r * dv + c] + fk[r]",
                                      "Sb[(size_t)r * dv + c] = Sb[(size_t)r * dv + c] + fk[r]"),
+    # feature maps and the normaliser
+    "relu_keeps_negative_part": ("return (x > 0.0 ? x : 0.0) + c;", "return (x > 0.0 ? 0.0 : x) + c;"),
+    "identity_drops_shift": ("        return x + c;\n    return la_oracle_phi(x);", "        return x;\n    return la_oracle_phi(x);"),
+    "general_always_normalizes": ("            if (normalize) {\n                double den = 0.0;", "            if (1) {\n                double den = 0.0;"),
+    "general_ignores_decay": ("        const double g = gamma ? gamma[bh] : 1.0;\n        double *S = calloc", "        const double g = 1.0;\n        double *S = calloc"),
+    "prefill_general_undecayed": ("Sb[(size_t)r * dv + c] = g * Sb[(size_t)r * dv + c] +\n", "Sb[(size_t)r * dv + c] = Sb[(size_t)r * dv + c] +\n"),
+    "noncausal_general_default_map": ("la_oracle_prefill_state_general(k, v, type, NULL, map, shift, S, z, BH, N, dk, dv);", "la_oracle_prefill_state_general(k, v, type, NULL, 0, shift, S, z, BH, N, dk, dv);"),
+    "decode_general_key_from_query": ("fk[r] = phi_map(load(k, type, (int64_t)bh * dk + r), map, shift);", "fk[r] = phi_map(load(q, type, (int64_t)bh * dk + r), map, shift);"),
 }
 
 
