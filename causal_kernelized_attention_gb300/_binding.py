@@ -27,6 +27,24 @@ class LAError(RuntimeError):
         super().__init__(msg)
 
 
+class Variant(ctypes.Structure):
+    """la_variant: feature map (LA_PHI_ELU1 / LA_PHI_RELU / LA_PHI_IDENTITY), its shift,
+    and whether the output is divided by max(phi(q)^T z, eps)."""
+    _fields_ = [("feature_map", ctypes.c_int), ("shift", ctypes.c_float), ("normalize", ctypes.c_int)]
+
+
+LA_PHI_ELU1, LA_PHI_RELU, LA_PHI_IDENTITY = 0, 1, 2
+_FMAPS = {"elu1": LA_PHI_ELU1, "relu": LA_PHI_RELU, "identity": LA_PHI_IDENTITY}
+
+
+def _variant(feature_map, shift, normalize):
+    """A la_variant by reference, or None for the default (elu + 1, normalised)."""
+    fm = _FMAPS[feature_map] if isinstance(feature_map, str) else int(feature_map)
+    if fm == LA_PHI_ELU1 and normalize:
+        return None
+    return ctypes.byref(Variant(fm, float(shift), 1 if normalize else 0))
+
+
 def lib_path() -> str:
     return LIB_PATH
 
@@ -42,6 +60,10 @@ def _declare(lib):
         "la_forward_causal_decay": [P, P, P, P, P, I, I, I, I, I, I, F, I, P],
         "la_decode_step_decay": [P, P, P, P, P, P, P, I, I, I, I, F, I, P],
         "la_prefill_state_decay": [P, P, P, P, P, I, I, I, I, I, I, P],
+        "la_forward_causal_ex": [P, P, P, P, P, P, I, I, I, I, I, I, F, I, P],
+        "la_forward_noncausal_ex": [P, P, P, P, P, I, I, I, I, I, F, I, P],
+        "la_decode_step_ex": [P, P, P, P, P, P, P, P, I, I, I, I, F, I, P],
+        "la_prefill_state_ex": [P, P, P, P, P, P, I, I, I, I, I, I, P],
         "la_get_device_status": [P],
     }
     for name, args in sigs.items():
@@ -273,6 +295,95 @@ def la_prefill_state_decay(k, v, gamma, S=None, z=None, stream=None):
     st = load_library().la_prefill_state_decay(k.data_ptr(), v.data_ptr(), gamma.data_ptr(), S.data_ptr(),
                                                z.data_ptr(), B, H, N, dk, dv, _dtype_code(k), _stream_ptr(stream))
     _check("la_prefill_state_decay", st)
+    return S, z
+
+
+def _gamma_ptr(gamma, H):
+    if gamma is None:
+        return None
+    _gamma_tensor(gamma, H)
+    return gamma.data_ptr()
+
+
+def la_forward_causal_ex(q, k, v, o=None, gamma=None, feature_map="elu1", shift=0.0, normalize=True,
+                         chunk: int = 128, eps: float = 1e-6, stream=None):
+    """Causal forward with a feature map ("elu1", "relu": max(x, 0) + shift, "identity":
+    x + shift), with or without the normaliser, with or without a per-head decay gamma [H]."""
+    import torch
+    if o is None:
+        o = torch.empty(q.shape[:-1] + (v.shape[-1],), dtype=q.dtype, device=q.device)
+    _need_cuda(q, k, v, o)
+    _same_dtype(q, k, v, o)
+    B, H, N, dk = q.shape
+    dv = v.shape[-1]
+    if tuple(k.shape) != (B, H, N, dk) or tuple(v.shape[:-1]) != (B, H, N) or tuple(o.shape) != (B, H, N, dv):
+        raise ValueError("shape mismatch")
+    st = load_library().la_forward_causal_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                             _gamma_ptr(gamma, H), _variant(feature_map, shift, normalize),
+                                             B, H, N, dk, dv, int(chunk), float(eps), _dtype_code(q),
+                                             _stream_ptr(stream))
+    _check("la_forward_causal_ex", st)
+    return o
+
+
+def la_forward_noncausal_ex(q, k, v, o=None, feature_map="elu1", shift=0.0, normalize=True, eps: float = 1e-6,
+                            stream=None):
+    """Non-causal forward with a feature map, with or without the normaliser."""
+    import torch
+    if o is None:
+        o = torch.empty(q.shape[:-1] + (v.shape[-1],), dtype=q.dtype, device=q.device)
+    _need_cuda(q, k, v, o)
+    _same_dtype(q, k, v, o)
+    B, H, N, dk = q.shape
+    dv = v.shape[-1]
+    if tuple(k.shape) != (B, H, N, dk) or tuple(v.shape[:-1]) != (B, H, N) or tuple(o.shape) != (B, H, N, dv):
+        raise ValueError("shape mismatch")
+    st = load_library().la_forward_noncausal_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                                _variant(feature_map, shift, normalize), B, H, N, dk, dv,
+                                                float(eps), _dtype_code(q), _stream_ptr(stream))
+    _check("la_forward_noncausal_ex", st)
+    return o
+
+
+def la_decode_step_ex(S, z, q, k, v, o=None, gamma=None, feature_map="elu1", shift=0.0, normalize=True,
+                      eps: float = 1e-6, stream=None):
+    """One decode step with a feature map, normaliser choice and optional decay; S, z in place."""
+    import torch
+    if o is None:
+        o = torch.empty(q.shape[:-1] + (v.shape[-1],), dtype=q.dtype, device=q.device)
+    _need_cuda(S, z, q, k, v, o)
+    _same_dtype(q, k, v, o)
+    if S.dtype != torch.float32 or z.dtype != torch.float32:
+        raise TypeError("S and z must be float32")
+    B, H, dk = q.shape
+    dv = v.shape[-1]
+    if tuple(S.shape) != (B, H, dk, dv) or tuple(z.shape) != (B, H, dk) or tuple(k.shape) != (B, H, dk) \
+            or tuple(v.shape) != (B, H, dv) or tuple(o.shape) != (B, H, dv):
+        raise ValueError("shape mismatch")
+    st = load_library().la_decode_step_ex(S.data_ptr(), z.data_ptr(), q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                          o.data_ptr(), _gamma_ptr(gamma, H), _variant(feature_map, shift, normalize),
+                                          B, H, dk, dv, float(eps), _dtype_code(q), _stream_ptr(stream))
+    _check("la_decode_step_ex", st)
+    return o
+
+
+def la_prefill_state_ex(k, v, S=None, z=None, gamma=None, feature_map="elu1", shift=0.0, stream=None):
+    """Prefix state under a feature map and an optional decay; returns (S, z) fp32."""
+    import torch
+    B, H, N, dk = k.shape
+    dv = v.shape[-1]
+    if S is None:
+        S = torch.empty((B, H, dk, dv), dtype=torch.float32, device=k.device)
+    if z is None:
+        z = torch.empty((B, H, dk), dtype=torch.float32, device=k.device)
+    _need_cuda(k, v, S, z)
+    _same_dtype(k, v)
+    if tuple(v.shape[:-1]) != (B, H, N) or tuple(S.shape) != (B, H, dk, dv) or tuple(z.shape) != (B, H, dk):
+        raise ValueError("shape mismatch")
+    st = load_library().la_prefill_state_ex(k.data_ptr(), v.data_ptr(), _gamma_ptr(gamma, H),
+                                            _variant(feature_map, shift, True), S.data_ptr(), z.data_ptr(),
+                                            B, H, N, dk, dv, _dtype_code(k), _stream_ptr(stream))
+    _check("la_prefill_state_ex", st)
     return S, z
 
 

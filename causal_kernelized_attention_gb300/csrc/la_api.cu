@@ -159,10 +159,25 @@ static la_status check_forward(const void *q, const void *k, const void *v, cons
     return LA_OK;
 }
 
+// A variant of the feature map / normaliser (NULL: elu + 1 with the normaliser).
+static la_status check_variant(const la_variant *v, Variant *out)
+{
+    *out = Variant();
+    if (!v) return LA_OK;
+    if (v->feature_map != LA_PHI_ELU1 && v->feature_map != LA_PHI_RELU && v->feature_map != LA_PHI_IDENTITY)
+        return LA_ERR_INVALID_ARG;
+    if (!isfinite(v->shift)) return LA_ERR_INVALID_ARG;
+    if (v->normalize != 0 && v->normalize != 1) return LA_ERR_INVALID_ARG;
+    out->map = v->feature_map;
+    out->shift = v->feature_map == LA_PHI_ELU1 ? 0.f : v->shift;
+    out->normalize = v->normalize;
+    return LA_OK;
+}
+
 // Checks of the decode entry points; gamma null for the undecayed step.
 static la_status decode_checked(float *S, float *z, const void *q, const void *k, const void *v, void *o,
                                 const float *gamma, int B, int H, int dk, int dv, float eps, la_dtype dtype,
-                                cudaStream_t stream)
+                                cudaStream_t stream, const Variant &var)
 {
     if (B < 0 || H < 0 || dk < 0 || dv < 0) return LA_ERR_INVALID_ARG;
     if (!(eps >= 0.f) || !isfinite(eps)) return LA_ERR_INVALID_ARG;
@@ -178,7 +193,7 @@ static la_status decode_checked(float *S, float *z, const void *q, const void *k
     if (overlaps(S, nS, z, nz) || overlaps(o, nvo, S, nS) || overlaps(o, nvo, z, nz) ||
         overlaps(o, nvo, q, nqk) || overlaps(o, nvo, k, nqk) || overlaps(o, nvo, v, nvo))
         return LA_ERR_INVALID_ARG;
-    return decode_step(S, z, q, k, v, o, (int)BH, dk, dv, eps, dtype, stream, gamma, H);
+    return decode_step(S, z, q, k, v, o, (int)BH, dk, dv, eps, dtype, stream, gamma, H, var);
 }
 
 }  // namespace la
@@ -187,16 +202,22 @@ using namespace la;
 
 extern "C" {
 
-la_status la_forward_causal(const void *q, const void *k, const void *v, void *o, int B, int H, int N,
-                            int dk, int dv, int chunk, float eps, la_dtype dtype, la_stream_t stream)
+la_status la_forward_causal_ex(const void *q, const void *k, const void *v, void *o, const float *gamma,
+                               const la_variant *variant, int B, int H, int N, int dk, int dv, int chunk,
+                               float eps, la_dtype dtype, la_stream_t stream)
 {
     bool empty;
     la_status st = check_forward(q, k, v, o, B, H, N, dk, dv, eps, dtype, &empty);
     if (st != LA_OK) return st;
+    Variant var;
+    if ((st = check_variant(variant, &var)) != LA_OK) return st;
     if (chunk != 64 && chunk != 128) return LA_ERR_UNSUPPORTED;
     if (empty) return LA_OK;
+    if (gamma && ((uintptr_t)gamma & 3u) != 0) return LA_ERR_MISALIGNED;
     if (!supported_dim(dk) || !supported_dim(dv)) return LA_ERR_UNSUPPORTED;
-    Problem p{q, k, v, o, B * H, N, dk, dv, chunk, eps, dtype, (cudaStream_t)stream};
+    if (gamma && overlaps(o, (size_t)B * H * N * dv * elem_size(dtype), gamma, (size_t)H * 4))
+        return LA_ERR_INVALID_ARG;
+    Problem p{q, k, v, o, B * H, N, dk, dv, chunk, eps, dtype, (cudaStream_t)stream, gamma, H, var};
     if (dtype == LA_BF16) {
         st = causal_tc(p);
         if (st != LA_ERR_UNSUPPORTED) return st;
@@ -204,19 +225,48 @@ la_status la_forward_causal(const void *q, const void *k, const void *v, void *o
     return causal_simt(p);
 }
 
-la_status la_forward_noncausal(const void *q, const void *k, const void *v, void *o, int B, int H, int N,
-                               int dk, int dv, float eps, la_dtype dtype, la_stream_t stream)
+la_status la_forward_causal(const void *q, const void *k, const void *v, void *o, int B, int H, int N,
+                            int dk, int dv, int chunk, float eps, la_dtype dtype, la_stream_t stream)
+{
+    return la_forward_causal_ex(q, k, v, o, nullptr, nullptr, B, H, N, dk, dv, chunk, eps, dtype, stream);
+}
+
+la_status la_forward_causal_decay(const void *q, const void *k, const void *v, void *o, const float *gamma,
+                                  int B, int H, int N, int dk, int dv, int chunk, float eps, la_dtype dtype,
+                                  la_stream_t stream)
+{
+    if (!gamma) {  // required unless there is nothing to do
+        bool empty;
+        la_status st = check_forward(q, k, v, o, B, H, N, dk, dv, eps, dtype, &empty);
+        if (st != LA_OK) return st;
+        if (chunk != 64 && chunk != 128) return LA_ERR_UNSUPPORTED;
+        return empty ? LA_OK : LA_ERR_INVALID_ARG;
+    }
+    return la_forward_causal_ex(q, k, v, o, gamma, nullptr, B, H, N, dk, dv, chunk, eps, dtype, stream);
+}
+
+la_status la_forward_noncausal_ex(const void *q, const void *k, const void *v, void *o, const la_variant *variant,
+                                  int B, int H, int N, int dk, int dv, float eps, la_dtype dtype,
+                                  la_stream_t stream)
 {
     bool empty;
     la_status st = check_forward(q, k, v, o, B, H, N, dk, dv, eps, dtype, &empty);
-    if (st != LA_OK || empty) return st;
+    if (st != LA_OK) return st;
+    Variant var;
+    if ((st = check_variant(variant, &var)) != LA_OK || empty) return st;
     if (!supported_dim(dk) || !supported_dim(dv)) return LA_ERR_UNSUPPORTED;
-    Problem p{q, k, v, o, B * H, N, dk, dv, 0, eps, dtype, (cudaStream_t)stream};
+    Problem p{q, k, v, o, B * H, N, dk, dv, 0, eps, dtype, (cudaStream_t)stream, nullptr, H, var};
     if (dtype == LA_BF16) {
         st = noncausal_tc(p);
         if (st != LA_ERR_UNSUPPORTED) return st;
     }
     return noncausal_simt(p);
+}
+
+la_status la_forward_noncausal(const void *q, const void *k, const void *v, void *o, int B, int H, int N,
+                               int dk, int dv, float eps, la_dtype dtype, la_stream_t stream)
+{
+    return la_forward_noncausal_ex(q, k, v, o, nullptr, B, H, N, dk, dv, eps, dtype, stream);
 }
 
 la_status la_forward_noncausal_noalloc(const void *q, const void *k, const void *v, void *o, int B, int H,
@@ -230,91 +280,78 @@ la_status la_forward_noncausal_noalloc(const void *q, const void *k, const void 
     return noncausal_simt_noalloc(p);
 }
 
-la_status la_decode_step(float *S, float *z, const void *q, const void *k, const void *v, void *o, int B,
-                         int H, int dk, int dv, float eps, la_dtype dtype, la_stream_t stream)
+la_status la_decode_step_ex(float *S, float *z, const void *q, const void *k, const void *v, void *o,
+                            const float *gamma, const la_variant *variant, int B, int H, int dk, int dv, float eps,
+                            la_dtype dtype, la_stream_t stream)
 {
-    return decode_checked(S, z, q, k, v, o, nullptr, B, H, dk, dv, eps, dtype, (cudaStream_t)stream);
-}
-
-la_status la_forward_causal_decay(const void *q, const void *k, const void *v, void *o, const float *gamma,
-                                  int B, int H, int N, int dk, int dv, int chunk, float eps, la_dtype dtype,
-                                  la_stream_t stream)
-{
-    bool empty;
-    la_status st = check_forward(q, k, v, o, B, H, N, dk, dv, eps, dtype, &empty);
+    Variant var;
+    la_status st = check_variant(variant, &var);
     if (st != LA_OK) return st;
-    if (chunk != 64 && chunk != 128) return LA_ERR_UNSUPPORTED;
-    if (empty) return LA_OK;
-    if (!gamma) return LA_ERR_INVALID_ARG;
-    if (((uintptr_t)gamma & 3u) != 0) return LA_ERR_MISALIGNED;
-    if (!supported_dim(dk) || !supported_dim(dv)) return LA_ERR_UNSUPPORTED;
-    if (overlaps(o, (size_t)B * H * N * dv * elem_size(dtype), gamma, (size_t)H * 4)) return LA_ERR_INVALID_ARG;
-    Problem p{q, k, v, o, B * H, N, dk, dv, chunk, eps, dtype, (cudaStream_t)stream, gamma, H};
-    if (dtype == LA_BF16) {
-        st = causal_tc(p);
-        if (st != LA_ERR_UNSUPPORTED) return st;
-    }
-    return causal_simt(p);
-}
-
-la_status la_decode_step_decay(float *S, float *z, const void *q, const void *k, const void *v, void *o,
-                               const float *gamma, int B, int H, int dk, int dv, float eps, la_dtype dtype,
-                               la_stream_t stream)
-{
-    if (B > 0 && H > 0 && dk > 0 && dv > 0) {
-        if (!gamma) return LA_ERR_INVALID_ARG;
+    if (gamma && B > 0 && H > 0 && dk > 0 && dv > 0) {
         if (((uintptr_t)gamma & 3u) != 0) return LA_ERR_MISALIGNED;
         const size_t BH = (size_t)B * H;
         if (overlaps(gamma, (size_t)H * 4, S, BH * dk * dv * 4) || overlaps(gamma, (size_t)H * 4, z, BH * dk * 4))
             return LA_ERR_INVALID_ARG;
         if (o && overlaps(gamma, (size_t)H * 4, o, BH * dv * elem_size(dtype))) return LA_ERR_INVALID_ARG;
     }
-    return decode_checked(S, z, q, k, v, o, gamma, B, H, dk, dv, eps, dtype, (cudaStream_t)stream);
+    return decode_checked(S, z, q, k, v, o, gamma, B, H, dk, dv, eps, dtype, (cudaStream_t)stream, var);
 }
 
-la_status la_prefill_state(const void *k, const void *v, float *S, float *z, int B, int H, int N, int dk,
-                           int dv, la_dtype dtype, la_stream_t stream)
+la_status la_decode_step(float *S, float *z, const void *q, const void *k, const void *v, void *o, int B,
+                         int H, int dk, int dv, float eps, la_dtype dtype, la_stream_t stream)
+{
+    return la_decode_step_ex(S, z, q, k, v, o, nullptr, nullptr, B, H, dk, dv, eps, dtype, stream);
+}
+
+la_status la_decode_step_decay(float *S, float *z, const void *q, const void *k, const void *v, void *o,
+                               const float *gamma, int B, int H, int dk, int dv, float eps, la_dtype dtype,
+                               la_stream_t stream)
+{
+    if (!gamma && B > 0 && H > 0 && dk > 0 && dv > 0) return LA_ERR_INVALID_ARG;
+    return la_decode_step_ex(S, z, q, k, v, o, gamma, nullptr, B, H, dk, dv, eps, dtype, stream);
+}
+
+la_status la_prefill_state_ex(const void *k, const void *v, const float *gamma, const la_variant *variant, float *S,
+                              float *z, int B, int H, int N, int dk, int dv, la_dtype dtype, la_stream_t stream)
 {
     if (B < 0 || H < 0 || N < 0 || dk < 0 || dv < 0) return LA_ERR_INVALID_ARG;
     if (dtype != LA_F32 && dtype != LA_BF16) return LA_ERR_INVALID_ARG;
+    Variant var;
+    la_status st = check_variant(variant, &var);
+    if (st != LA_OK) return st;
     if ((long long)B * H > 65535) return LA_ERR_UNSUPPORTED;
     if (B == 0 || H == 0 || dk == 0 || dv == 0) return LA_OK;
     if (!S || !z || (N > 0 && (!k || !v))) return LA_ERR_INVALID_ARG;
     if (!aligned16(S) || !aligned16(z) || (N > 0 && (!aligned16(k) || !aligned16(v))))
         return LA_ERR_MISALIGNED;
+    if (N > 0 && gamma && ((uintptr_t)gamma & 3u) != 0) return LA_ERR_MISALIGNED;
     if (!supported_dim(dk) || !supported_dim(dv)) return LA_ERR_UNSUPPORTED;
     const size_t BH = (size_t)B * H;
     if (overlaps(S, BH * dk * dv * 4, z, BH * dk * 4)) return LA_ERR_INVALID_ARG;
+    if (N > 0 && gamma &&
+        (overlaps(gamma, (size_t)H * 4, S, BH * dk * dv * 4) || overlaps(gamma, (size_t)H * 4, z, BH * dk * 4)))
+        return LA_ERR_INVALID_ARG;
+    if (N == 0) gamma = nullptr;
     // bf16 with dk = dv in {64, 128}: the summary phase of the tensor-core non-causal
     // kernel (the final causal state is the non-causal state of the prefix).
     if (dtype == LA_BF16 && dk == dv && (dk == 64 || dk == 128) && N >= 128) {
-        const la_status st = noncausal_tc_state(k, v, S, z, (int)BH, N, dk, (cudaStream_t)stream);
+        st = noncausal_tc_state(k, v, S, z, (int)BH, N, dk, (cudaStream_t)stream, gamma, H, var);
         if (st != LA_ERR_UNSUPPORTED) return st;
     }
-    return state_simt(k, v, S, z, (int)BH, N, dk, dv, dtype, (cudaStream_t)stream);
+    return state_simt(k, v, S, z, (int)BH, N, dk, dv, dtype, (cudaStream_t)stream, gamma, H, var);
+}
+
+la_status la_prefill_state(const void *k, const void *v, float *S, float *z, int B, int H, int N, int dk,
+                           int dv, la_dtype dtype, la_stream_t stream)
+{
+    return la_prefill_state_ex(k, v, nullptr, nullptr, S, z, B, H, N, dk, dv, dtype, stream);
 }
 
 la_status la_prefill_state_decay(const void *k, const void *v, const float *gamma, float *S, float *z, int B,
                                  int H, int N, int dk, int dv, la_dtype dtype, la_stream_t stream)
 {
-    if (B < 0 || H < 0 || N < 0 || dk < 0 || dv < 0) return LA_ERR_INVALID_ARG;
-    if (dtype != LA_F32 && dtype != LA_BF16) return LA_ERR_INVALID_ARG;
-    if ((long long)B * H > 65535) return LA_ERR_UNSUPPORTED;
-    if (B == 0 || H == 0 || dk == 0 || dv == 0) return LA_OK;
-    if (!S || !z || (N > 0 && (!k || !v || !gamma))) return LA_ERR_INVALID_ARG;
-    if (!aligned16(S) || !aligned16(z) || (N > 0 && (!aligned16(k) || !aligned16(v))))
-        return LA_ERR_MISALIGNED;
-    if (N > 0 && ((uintptr_t)gamma & 3u) != 0) return LA_ERR_MISALIGNED;
-    if (!supported_dim(dk) || !supported_dim(dv)) return LA_ERR_UNSUPPORTED;
-    const size_t BH = (size_t)B * H;
-    if (overlaps(S, BH * dk * dv * 4, z, BH * dk * 4)) return LA_ERR_INVALID_ARG;
-    if (N > 0 && (overlaps(gamma, (size_t)H * 4, S, BH * dk * dv * 4) || overlaps(gamma, (size_t)H * 4, z, BH * dk * 4)))
-        return LA_ERR_INVALID_ARG;
-    if (dtype == LA_BF16 && dk == dv && (dk == 64 || dk == 128) && N >= 128) {
-        const la_status st = noncausal_tc_state(k, v, S, z, (int)BH, N, dk, (cudaStream_t)stream, gamma, H);
-        if (st != LA_ERR_UNSUPPORTED) return st;
-    }
-    return state_simt(k, v, S, z, (int)BH, N, dk, dv, dtype, (cudaStream_t)stream, N > 0 ? gamma : nullptr, H);
+    if (!gamma && N > 0 && B > 0 && H > 0 && dk > 0 && dv > 0) return LA_ERR_INVALID_ARG;  // required
+    return la_prefill_state_ex(k, v, gamma, nullptr, S, z, B, H, N, dk, dv, dtype, stream);
 }
 
 const char *la_status_string(la_status s)

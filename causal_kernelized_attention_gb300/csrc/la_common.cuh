@@ -6,6 +6,7 @@
 #include <stdint.h>
 
 #include "la.h"
+#include "la_internal.h"
 
 namespace la {
 
@@ -31,6 +32,18 @@ template <> struct Elem<__nv_bfloat16> {
     static __device__ __forceinline__ __nv_bfloat16 from_f32(float x) { return __float2bfloat16_rn(x); }
     static __device__ __forceinline__ float phi(float x) { return phi_fast(x); }
 };
+
+// Feature-map variants (struct Variant, la_internal.h).
+template <typename T>
+__device__ __forceinline__ float phi_variant(float x, const Variant &v)
+{
+    return v.map == LA_PHI_RELU ? fmaxf(x, 0.f) + v.shift : v.map == LA_PHI_IDENTITY ? x + v.shift : Elem<T>::phi(x);
+}
+// The output scale: 1 / max(den, eps), or 1 without the normaliser.
+__device__ __forceinline__ float out_scale(float den, float eps, const Variant &v)
+{
+    return v.normalize ? 1.f / fmaxf(den, eps) : 1.f;
+}
 
 __host__ __device__ constexpr int ceil_div(int a, int b) { return (a + b - 1) / b; }
 

@@ -59,7 +59,7 @@ template <typename T, int DK, int DV, bool kDecay>
 __global__ void __launch_bounds__(kDecodeThreads)
 decode_kernel(float *__restrict__ S, float *__restrict__ z, const T *__restrict__ q,
               const T *__restrict__ k, const T *__restrict__ v, T *__restrict__ o, float eps,
-              const float *__restrict__ gamma, int H)
+              const float *__restrict__ gamma, int H, const Variant var)
 {
     constexpr int kCols4 = DV / 4;                       // float4 groups per row
     constexpr int kRowGroups = kDecodeThreads / kCols4;  // threads stacked over rows
@@ -81,8 +81,8 @@ decode_kernel(float *__restrict__ S, float *__restrict__ z, const T *__restrict_
     const float g = kDecay ? gamma[head % H] : 1.f;
 
     for (int r = tid; r < DK; r += kDecodeThreads) {
-        fq[r] = Elem<T>::phi(Elem<T>::to_f32(q[head * DK + r]));
-        fk[r] = Elem<T>::phi(Elem<T>::to_f32(k[head * DK + r]));
+        fq[r] = phi_variant<T>(Elem<T>::to_f32(q[head * DK + r]), var);
+        fk[r] = phi_variant<T>(Elem<T>::to_f32(k[head * DK + r]), var);
     }
     float vc[4];
     load4<T>(v + head * DV + 4 * cg, vc);
@@ -117,7 +117,7 @@ decode_kernel(float *__restrict__ S, float *__restrict__ z, const T *__restrict_
     float den = 0.f;
 #pragma unroll
     for (int w = 0; w < kDecodeThreads / 32; ++w) den += red[w];
-    const float inv = 1.f / fmaxf(den, eps);
+    const float inv = var.normalize ? 1.f / fmaxf(den, eps) : 1.f;
 
     // Column sums of the row-group partials: thread t < DV produces o[t].
     if (tid < DV) {
@@ -141,6 +141,7 @@ struct DecodeArgs {
     const float *gamma;
     int H;
     cudaStream_t stream;
+    Variant var;
 };
 
 template <typename T, int DK, int DV>
@@ -149,10 +150,10 @@ la_status launch(const DecodeArgs &a)
     count_launches();
     if (a.gamma)
         decode_kernel<T, DK, DV, true><<<a.BH, kDecodeThreads, 0, a.stream>>>(
-            a.S, a.z, (const T *)a.q, (const T *)a.k, (const T *)a.v, (T *)a.o, a.eps, a.gamma, a.H);
+            a.S, a.z, (const T *)a.q, (const T *)a.k, (const T *)a.v, (T *)a.o, a.eps, a.gamma, a.H, a.var);
     else
         decode_kernel<T, DK, DV, false><<<a.BH, kDecodeThreads, 0, a.stream>>>(
-            a.S, a.z, (const T *)a.q, (const T *)a.k, (const T *)a.v, (T *)a.o, a.eps, nullptr, 1);
+            a.S, a.z, (const T *)a.q, (const T *)a.k, (const T *)a.v, (T *)a.o, a.eps, nullptr, 1, a.var);
     return cuda_status(cudaGetLastError());
 }
 
@@ -182,10 +183,10 @@ la_status by_dk(const DecodeArgs &a, int dk, int dv)
 
 la_status decode_step(float *S, float *z, const void *q, const void *k, const void *v, void *o, int BH,
                       int dk, int dv, float eps, la_dtype dtype, cudaStream_t stream,
-                      const float *gamma, int H)
+                      const float *gamma, int H, const Variant &var)
 {
     if (!supported_dim(dk) || !supported_dim(dv)) return LA_ERR_UNSUPPORTED;
-    const DecodeArgs a{S, z, q, k, v, o, BH, eps, gamma, H, stream};
+    const DecodeArgs a{S, z, q, k, v, o, BH, eps, gamma, H, stream, var};
     return dtype == LA_F32 ? by_dk<float>(a, dk, dv) : by_dk<__nv_bfloat16>(a, dk, dv);
 }
 

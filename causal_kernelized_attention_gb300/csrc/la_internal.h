@@ -18,6 +18,18 @@ struct Scratch {
     ~Scratch();
 };
 
+// Feature-map and normaliser variant ("Linear attention", What the pieces are
+// for: ReLU; "Linear Attention -- Math + Variants", Feature-map families: ReLU
+// and identity-plus-shift, Implementation reality: dropping the normaliser):
+// map LA_PHI_ELU1 (elu + 1), LA_PHI_RELU (max(x, 0) + shift), LA_PHI_IDENTITY
+// (x + shift); normalize 0: o = phi(q)^T S.
+struct Variant {
+    int map = LA_PHI_ELU1;
+    float shift = 0.f;
+    int normalize = 1;
+    bool is_default() const { return map == LA_PHI_ELU1 && normalize == 1; }
+};
+
 struct Problem {
     const void *q, *k, *v;
     void *o;
@@ -29,6 +41,7 @@ struct Problem {
     // sequence bh = bh % H; null for the undecayed forms.
     const float *gamma = nullptr;
     int H = 1;
+    Variant var;
 };
 
 // SIMT kernels (la_simt.cu): fp32 CUDA-core arithmetic, any supported dtype.
@@ -40,14 +53,14 @@ la_status noncausal_simt_noalloc(const Problem &p);
 // gamma (device, [H]): token t weighted by gamma[bh % H]^(N-1-t); null: unweighted.
 la_status state_simt(const void *k, const void *v, float *S, float *z, int BH, int N, int dk,
                      int dv, la_dtype dtype, cudaStream_t stream, const float *gamma = nullptr,
-                     int H = 1);
+                     int H = 1, const Variant &var = Variant());
 
 // Decode step (la_decode.cu).
 // gamma (device, [H], head = bh % H): the decayed step S = g S + phi(k) v^T,
 // z = g z + phi(k); null for the undecayed step.
 la_status decode_step(float *S, float *z, const void *q, const void *k, const void *v, void *o,
                       int BH, int dk, int dv, float eps, la_dtype dtype, cudaStream_t stream,
-                      const float *gamma = nullptr, int H = 1);
+                      const float *gamma = nullptr, int H = 1, const Variant &var = Variant());
 
 // Tensor-core (tcgen05) paths (la_tc_causal.cu); return LA_ERR_UNSUPPORTED when
 // the problem is outside the shapes they are built for.
@@ -58,7 +71,8 @@ la_status noncausal_tc(const Problem &p);
 // k, v; D in {64, 128}, N >= 128); overwrites S and z.  gamma (device, [H]): token
 // t weighted by gamma[bh % H]^(N-1-t); null: unweighted.
 la_status noncausal_tc_state(const void *k, const void *v, float *S, float *z, int BH, int N, int D,
-                             cudaStream_t stream, const float *gamma = nullptr, int H = 1);
+                             cudaStream_t stream, const float *gamma = nullptr, int H = 1,
+                             const Variant &var = Variant());
 
 // Device status words of translation units that run bounded waits: read and clear.
 la_status tc_causal_read_status(cudaStream_t s, unsigned *bits);

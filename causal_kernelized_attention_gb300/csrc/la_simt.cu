@@ -45,7 +45,8 @@ __device__ __forceinline__ float decay_pow(float g, int d)
 template <typename T, int DK, int C, bool kDecay>
 __global__ void __launch_bounds__(kThreads)
 causal_simt_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
-                   T *__restrict__ o, int N, int DV, float eps, const float *__restrict__ gamma, int H)
+                   T *__restrict__ o, int N, int DV, float eps, const float *__restrict__ gamma, int H,
+                   const Variant var)
 {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     auto &sm = *reinterpret_cast<CausalSmem<T, DK, C> *>(smem_raw);
@@ -69,7 +70,7 @@ causal_simt_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__
         __syncthreads();  // previous chunk's state update is complete
         for (int e = tid; e < C * DK; e += kThreads) {
             const int j = e / DK, r = e % DK;
-            sm.fk[j][r] = j < len ? Elem<T>::phi(Elem<T>::to_f32(kh[(size_t)(i0 + j) * DK + r])) : 0.f;
+            sm.fk[j][r] = j < len ? phi_variant<T>(Elem<T>::to_f32(kh[(size_t)(i0 + j) * DK + r]), var) : 0.f;
         }
         for (int e = tid; e < C * kDVS; e += kThreads) {
             const int j = e / kDVS, c = e % kDVS;
@@ -80,7 +81,7 @@ causal_simt_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__
         // Outputs: one warp per query row, lanes over key positions then over columns.
         for (int a = warp; a < len; a += kWarps) {
             for (int r = lane; r < DK; r += 32)
-                sm.qrow[warp][r] = Elem<T>::phi(Elem<T>::to_f32(qh[(size_t)(i0 + a) * DK + r]));
+                sm.qrow[warp][r] = phi_variant<T>(Elem<T>::to_f32(qh[(size_t)(i0 + a) * DK + r]), var);
             __syncwarp();
             // inter-chunk part: phi(q) . S (state of earlier chunks), phi(q) . z
             float num = 0.f, den = 0.f;
@@ -111,7 +112,7 @@ causal_simt_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__
                     num += __shfl_sync(0xffffffffu, s[m], bb) * sm.vs[32 * m + bb][lane];
             }
             if (c0 + lane < DV)
-                oh[(size_t)(i0 + a) * DV + c0 + lane] = Elem<T>::from_f32(num / fmaxf(den, eps));
+                oh[(size_t)(i0 + a) * DV + c0 + lane] = Elem<T>::from_f32(var.normalize ? num / fmaxf(den, eps) : num);
             __syncwarp();
         }
         __syncthreads();
@@ -143,7 +144,7 @@ template <typename T, int DK, bool kDecay>
 __global__ void __launch_bounds__(kThreads)
 state_simt_kernel(const T *__restrict__ k, const T *__restrict__ v, float *__restrict__ S,
                   float *__restrict__ z, int N, int DV, int tokens_per_split,
-                  const float *__restrict__ gamma, int H)
+                  const float *__restrict__ gamma, int H, const Variant var)
 {
     __shared__ float fk[kStateTile][DK];
     __shared__ float vs[kStateTile][kDVS];
@@ -168,7 +169,7 @@ state_simt_kernel(const T *__restrict__ k, const T *__restrict__ v, float *__res
         }
         for (int e = tid; e < kStateTile * DK; e += kThreads) {
             const int j = e / DK, r = e % DK;
-            float f = j < len ? Elem<T>::phi(Elem<T>::to_f32(kh[(size_t)(b0 + j) * DK + r])) : 0.f;
+            float f = j < len ? phi_variant<T>(Elem<T>::to_f32(kh[(size_t)(b0 + j) * DK + r]), var) : 0.f;
             if (kDecay) f *= wt[j];
             fk[j][r] = f;
         }
@@ -200,7 +201,7 @@ state_simt_kernel(const T *__restrict__ k, const T *__restrict__ v, float *__res
 template <typename T, int DK>
 __global__ void __launch_bounds__(kThreads)
 apply_simt_kernel(const T *__restrict__ q, const float *__restrict__ S, const float *__restrict__ z,
-                  T *__restrict__ o, int N, int DV, float eps)
+                  T *__restrict__ o, int N, int DV, float eps, const Variant var)
 {
     __shared__ float Ss[DK][kDVS];
     __shared__ float zs[DK];
@@ -218,7 +219,7 @@ apply_simt_kernel(const T *__restrict__ q, const float *__restrict__ S, const fl
     T *oh = o + (size_t)bh * N * DV;
     const int row_end = min(N, (int)(blockIdx.x + 1) * 64);
     for (int i = blockIdx.x * 64 + warp; i < row_end; i += kWarps) {
-        for (int r = lane; r < DK; r += 32) qrow[warp][r] = Elem<T>::phi(Elem<T>::to_f32(qh[(size_t)i * DK + r]));
+        for (int r = lane; r < DK; r += 32) qrow[warp][r] = phi_variant<T>(Elem<T>::to_f32(qh[(size_t)i * DK + r]), var);
         __syncwarp();
         float num = 0.f, den = 0.f;
 #pragma unroll 8
@@ -226,7 +227,7 @@ apply_simt_kernel(const T *__restrict__ q, const float *__restrict__ S, const fl
         for (int r = lane; r < DK; r += 32) den += qrow[warp][r] * zs[r];
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
-        if (c0 + lane < DV) oh[(size_t)i * DV + c0 + lane] = Elem<T>::from_f32(num / fmaxf(den, eps));
+        if (c0 + lane < DV) oh[(size_t)i * DV + c0 + lane] = Elem<T>::from_f32(var.normalize ? num / fmaxf(den, eps) : num);
         __syncwarp();
     }
 }
@@ -241,13 +242,13 @@ la_status launch_causal(const Problem &p)
     dim3 grid(p.BH, ceil_div(p.dv, kDVS));
     count_launches();
     kern<<<grid, kThreads, smem, p.stream>>>((const T *)p.q, (const T *)p.k, (const T *)p.v, (T *)p.o,
-                                             p.N, p.dv, p.eps, p.gamma, p.H);
+                                             p.N, p.dv, p.eps, p.gamma, p.H, p.var);
     return cuda_status(cudaGetLastError());
 }
 
 template <typename T, int DK>
 la_status launch_state(const void *k, const void *v, float *S, float *z, int BH, int N, int dv,
-                       cudaStream_t stream, const float *gamma = nullptr, int H = 1)
+                       cudaStream_t stream, const float *gamma = nullptr, int H = 1, Variant var = Variant())
 {
     cudaError_t e = cudaMemsetAsync(S, 0, sizeof(float) * (size_t)BH * DK * dv, stream);
     if (e == cudaSuccess) e = cudaMemsetAsync(z, 0, sizeof(float) * (size_t)BH * DK, stream);
@@ -263,10 +264,10 @@ la_status launch_state(const void *k, const void *v, float *S, float *z, int BH,
     count_launches();
     if (gamma)
         state_simt_kernel<T, DK, true><<<dim3(BH, slices, splits), kThreads, 0, stream>>>(
-            (const T *)k, (const T *)v, S, z, N, dv, per, gamma, H);
+            (const T *)k, (const T *)v, S, z, N, dv, per, gamma, H, var);
     else
         state_simt_kernel<T, DK, false><<<dim3(BH, slices, splits), kThreads, 0, stream>>>(
-            (const T *)k, (const T *)v, S, z, N, dv, per, nullptr, 1);
+            (const T *)k, (const T *)v, S, z, N, dv, per, nullptr, 1, var);
     return cuda_status(cudaGetLastError());
 }
 
@@ -278,11 +279,12 @@ la_status launch_noncausal(const Problem &p)
     la_status st = scratch.alloc(sizeof(float) * (s_elems + z_elems), p.stream);
     if (st != LA_OK) return st;
     float *S = (float *)scratch.ptr, *z = S + s_elems;
-    st = launch_state<T, DK>(p.k, p.v, S, z, p.BH, p.N, p.dv, p.stream);
+    st = launch_state<T, DK>(p.k, p.v, S, z, p.BH, p.N, p.dv, p.stream, nullptr, 1, p.var);
     if (st != LA_OK) return st;
     dim3 grid(ceil_div(p.N, 64), p.BH, ceil_div(p.dv, kDVS));
     count_launches();
-    apply_simt_kernel<T, DK><<<grid, kThreads, 0, p.stream>>>((const T *)p.q, S, z, (T *)p.o, p.N, p.dv, p.eps);
+    apply_simt_kernel<T, DK><<<grid, kThreads, 0, p.stream>>>((const T *)p.q, S, z, (T *)p.o, p.N, p.dv, p.eps,
+                                                              p.var);
     return cuda_status(cudaGetLastError());
 }
 
@@ -300,12 +302,12 @@ la_status causal_by_dk(const Problem &p)
 
 template <typename T>
 la_status state_by_dk(const void *k, const void *v, float *S, float *z, int BH, int N, int dk, int dv,
-                      cudaStream_t s, const float *gamma, int H)
+                      cudaStream_t s, const float *gamma, int H, const Variant &var)
 {
     switch (dk) {
-    case 32: return launch_state<T, 32>(k, v, S, z, BH, N, dv, s, gamma, H);
-    case 64: return launch_state<T, 64>(k, v, S, z, BH, N, dv, s, gamma, H);
-    case 128: return launch_state<T, 128>(k, v, S, z, BH, N, dv, s, gamma, H);
+    case 32: return launch_state<T, 32>(k, v, S, z, BH, N, dv, s, gamma, H, var);
+    case 64: return launch_state<T, 64>(k, v, S, z, BH, N, dv, s, gamma, H, var);
+    case 128: return launch_state<T, 128>(k, v, S, z, BH, N, dv, s, gamma, H, var);
     }
     return LA_ERR_UNSUPPORTED;
 }
@@ -337,11 +339,11 @@ la_status noncausal_simt(const Problem &p)
 }
 
 la_status state_simt(const void *k, const void *v, float *S, float *z, int BH, int N, int dk, int dv,
-                     la_dtype dtype, cudaStream_t stream, const float *gamma, int H)
+                     la_dtype dtype, cudaStream_t stream, const float *gamma, int H, const Variant &var)
 {
     if (!supported_dim(dk) || !supported_dim(dv)) return LA_ERR_UNSUPPORTED;
-    return dtype == LA_F32 ? state_by_dk<float>(k, v, S, z, BH, N, dk, dv, stream, gamma, H)
-                           : state_by_dk<__nv_bfloat16>(k, v, S, z, BH, N, dk, dv, stream, gamma, H);
+    return dtype == LA_F32 ? state_by_dk<float>(k, v, S, z, BH, N, dk, dv, stream, gamma, H, var)
+                           : state_by_dk<__nv_bfloat16>(k, v, S, z, BH, N, dk, dv, stream, gamma, H, var);
 }
 
 }  // namespace la
@@ -391,11 +393,12 @@ la_status launch_noncausal_noalloc(const Problem &p, float *scratch)
 {
     const size_t s_elems = (size_t)p.BH * DK * p.dv;
     float *S = scratch, *z = scratch + s_elems;  // s_elems is a multiple of 4: z stays 16-byte aligned
-    la_status st = launch_state<T, DK>(p.k, p.v, S, z, p.BH, p.N, p.dv, p.stream);
+    la_status st = launch_state<T, DK>(p.k, p.v, S, z, p.BH, p.N, p.dv, p.stream, nullptr, 1, p.var);
     if (st != LA_OK) return st;
     dim3 grid(ceil_div(p.N, 64), p.BH, ceil_div(p.dv, kDVS));
     count_launches();
-    apply_simt_kernel<T, DK><<<grid, kThreads, 0, p.stream>>>((const T *)p.q, S, z, (T *)p.o, p.N, p.dv, p.eps);
+    apply_simt_kernel<T, DK><<<grid, kThreads, 0, p.stream>>>((const T *)p.q, S, z, (T *)p.o, p.N, p.dv, p.eps,
+                                                              p.var);
     return cuda_status(cudaGetLastError());
 }
 

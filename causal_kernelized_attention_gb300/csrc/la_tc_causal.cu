@@ -137,6 +137,10 @@ struct Params {
     // Decayed state: gamma[bh % H] per head (device memory); unused otherwise.
     const float *gamma;
     int H;
+    // Feature-map variant (kVar): LA_PHI_* map with shift; normalize 0: o = phi(q)^T S.
+    int map;
+    float shift;
+    int normalize;
 };
 
 __device__ __forceinline__ bool wait_bar(int *abort_flag, uint64_t *bar, uint32_t parity)
@@ -342,7 +346,7 @@ __device__ __forceinline__ void add_state_zw(float (&acc)[32], float &zacc, cons
     zacc += w * zv;
 }
 
-template <int D, bool kDecay>
+template <int D, bool kDecay, bool kVar>
 __global__ void __launch_bounds__(576, 1)
 causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                  const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_o,
@@ -461,10 +465,10 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
             const int chunk = job_chunk(j, nA, a0, c0);
             const int valid = prm.N - chunk * kC;
             if (isC) {
-                phi_tile<D, kPhiThreads>(sm.k[s], tid, valid);
-                phi_tile<D, kPhiThreads>(sm.q[s], tid, valid);
+                phi_tile<D, kPhiThreads, false, kVar>(sm.k[s], tid, valid, 0.f, 0, prm.map, prm.shift);
+                phi_tile<D, kPhiThreads, false, kVar>(sm.q[s], tid, valid, 0.f, 0, prm.map, prm.shift);
             } else {  // the other half: epilogue warps
-                phi_tile<D, 2 * kPhiThreads, kDecay>(sm.k[s], tid, valid, lg, eA - chunk * kC);
+                phi_tile<D, 2 * kPhiThreads, kDecay, kVar>(sm.k[s], tid, valid, lg, eA - chunk * kC, prm.map, prm.shift);
             }
             fence_proxy_async_smem();
             if (isC)
@@ -671,7 +675,8 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
             const int s = j % S, r = j / S;
             if (!wait_bar(abort_flag, &sm.full[s], r & 1)) break;
             const int chunk = job_chunk(j, nA, a0, c0);
-            phi_tile<D, 2 * kPhiThreads, kDecay>(sm.k[s], kPhiThreads + gtid, prm.N - chunk * kC, lg, eA - chunk * kC);
+            phi_tile<D, 2 * kPhiThreads, kDecay, kVar>(sm.k[s], kPhiThreads + gtid, prm.N - chunk * kC, lg,
+                                                      eA - chunk * kC, prm.map, prm.shift);
             fence_proxy_async_smem();
             mbar_arrive(&sm.phi_done[s]);
         }
@@ -967,7 +972,7 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
                         den = __uint_as_float(dn[0]) + __uint_as_float(dn[17]) + __uint_as_float(dn[18]);
                     }
                 }
-                const float inv = 1.f / fmaxf(den, prm.eps);
+                const float inv = (kVar && !prm.normalize) ? 1.f : 1.f / fmaxf(den, prm.eps);
 #pragma unroll 1
                 for (int cc = 0; cc < D / 64; ++cc) {
                     uint32_t a[64];
@@ -1037,7 +1042,7 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
 }
 
 // ------------------------------------------------------------------ host side
-template <int D, bool kDecay>
+template <int D, bool kDecay, bool kVar>
 la_status launch(const Problem &p)
 {
     CUtensorMap mq, mk, mv, mo;
@@ -1129,9 +1134,12 @@ la_status launch(const Problem &p)
     for (int x = 0; x <= G && short_mode; ++x) prm.bounds[x] = bounds[x];
     prm.gamma = p.gamma;
     prm.H = p.H;
+    prm.map = p.var.map;
+    prm.shift = p.var.shift;
+    prm.normalize = p.var.normalize;
 
     const int smem = (int)sizeof(Smem<D>);
-    auto kern = causal_tc_kernel<D, kDecay>;
+    auto kern = causal_tc_kernel<D, kDecay, kVar>;
     st = ensure_smem((const void *)kern, smem);
     if (st != LA_OK) return st;
     count_launches();
@@ -1144,8 +1152,13 @@ la_status causal_tc(const Problem &p)
 {
     if (p.dtype != LA_BF16 || p.dk != p.dv || (p.dk != 64 && p.dk != 128) || p.chunk != kC || p.N < kC)
         return LA_ERR_UNSUPPORTED;
-    if (p.gamma) return p.dk == 128 ? launch<128, true>(p) : launch<64, true>(p);
-    return p.dk == 128 ? launch<128, false>(p) : launch<64, false>(p);
+    const bool var = !p.var.is_default();
+    if (p.gamma) {
+        if (var) return p.dk == 128 ? launch<128, true, true>(p) : launch<64, true, true>(p);
+        return p.dk == 128 ? launch<128, true, false>(p) : launch<64, true, false>(p);
+    }
+    if (var) return p.dk == 128 ? launch<128, false, true>(p) : launch<64, false, true>(p);
+    return p.dk == 128 ? launch<128, false, false>(p) : launch<64, false, false>(p);
 }
 
 la_status tc_causal_read_status(cudaStream_t s, unsigned *bits)

@@ -82,6 +82,19 @@ __device__ __forceinline__ uint32_t phi2(uint32_t w)
     return *reinterpret_cast<const uint32_t *>(&r);
 }
 
+// Feature-map variants on a pair of bf16 values (map LA_PHI_RELU: max(x, 0) + c,
+// LA_PHI_IDENTITY: x + c; LA_PHI_ELU1: phi2), in fp32 with one rounding to bf16.
+__device__ __forceinline__ uint32_t phi2_variant(uint32_t w, int map, float c)
+{
+    if (map == LA_PHI_ELU1) return phi2(w);
+    float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w));
+    if (map == LA_PHI_RELU) {
+        f.x = fmaxf(f.x, 0.f);
+        f.y = fmaxf(f.y, 0.f);
+    }
+    return pack_bf16(f.x + c, f.y + c);
+}
+
 // Decayed state: gamma^e for an integer e >= 0 from lg = log2(gamma) (gamma^0 = 1
 // for any gamma, including 0, whose lg is -inf).
 __device__ __forceinline__ float pow_decay(float lg, int e)
@@ -124,8 +137,10 @@ __device__ __forceinline__ void scale_row(uint8_t *tile, int row, float wf)
 // order is rotated by the row so that the 8 threads of a quarter-warp (8
 // consecutive rows) touch 8 different bank groups.
 // kScale (decayed state): row r is also multiplied by gamma^(ebase - r), lg = log2(gamma).
-template <int D, int NT, bool kScale = false>
-__device__ __forceinline__ void phi_tile(uint8_t *tile, int t, int valid, float lg = 0.f, int ebase = 0)
+// kVar: the feature map `map` with shift c (phi2_variant) instead of elu + 1.
+template <int D, int NT, bool kScale = false, bool kVar = false>
+__device__ __forceinline__ void phi_tile(uint8_t *tile, int t, int valid, float lg = 0.f, int ebase = 0,
+                                         int map = LA_PHI_ELU1, float c = 0.f)
 {
     constexpr int kUnits = 128 * (D / 32);
     constexpr int NU = (kUnits + NT - 1) / NT;
@@ -147,7 +162,12 @@ __device__ __forceinline__ void phi_tile(uint8_t *tile, int t, int valid, float 
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             uint4 &x = buf[m][k];
-            x = row < valid ? make_uint4(phi2(x.x), phi2(x.y), phi2(x.z), phi2(x.w)) : make_uint4(0u, 0u, 0u, 0u);
+            if (kVar)
+                x = row < valid ? make_uint4(phi2_variant(x.x, map, c), phi2_variant(x.y, map, c),
+                                             phi2_variant(x.z, map, c), phi2_variant(x.w, map, c))
+                                : make_uint4(0u, 0u, 0u, 0u);
+            else
+                x = row < valid ? make_uint4(phi2(x.x), phi2(x.y), phi2(x.z), phi2(x.w)) : make_uint4(0u, 0u, 0u, 0u);
             if (kScale)
                 x = make_uint4(scale_bf16x2(x.x, w), scale_bf16x2(x.y, w), scale_bf16x2(x.z, w), scale_bf16x2(x.w, w));
         }

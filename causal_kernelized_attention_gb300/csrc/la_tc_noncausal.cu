@@ -141,15 +141,24 @@ struct Params {
     // (the decayed recurrence unrolled over the prefix); null otherwise.
     const float *gamma;
     int H;
+    // Feature-map variant (kVar): LA_PHI_* map with shift; normalize 0: o = phi(q)^T S.
+    int map;
+    float shift;
+    int normalize;
 };
 
-// State mode, decayed state: phi in fp32, times the row's weight gamma^(ebase - row)
-// (lg = log2 gamma), split into bf16 high parts (in place) and low parts (in `lo`).
-__device__ __forceinline__ uint32_t phi2_split_w(uint32_t w, float wt, uint32_t *lo)
+// State mode, decayed state or another feature map: the map (elu + 1, max(x, 0) + c
+// or x + c) in fp32, times the row's weight gamma^(ebase - row) (lg = log2 gamma; 0
+// without decay), split into bf16 high parts (in place) and low parts (in `lo`).
+__device__ __forceinline__ float phi_map_f32(float x, int map, float c)
+{
+    return map == LA_PHI_RELU ? fmaxf(x, 0.f) + c : map == LA_PHI_IDENTITY ? x + c : (x > 0.f ? x + 1.f : __expf(x));
+}
+__device__ __forceinline__ uint32_t phi2_split_w(uint32_t w, float wt, uint32_t *lo, int map, float c)
 {
     const __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162 *>(&w);
     const float a = __bfloat162float(x.x), b = __bfloat162float(x.y);
-    const float pa = (a > 0.f ? a + 1.f : __expf(a)) * wt, pb = (b > 0.f ? b + 1.f : __expf(b)) * wt;
+    const float pa = phi_map_f32(a, map, c) * wt, pb = phi_map_f32(b, map, c) * wt;
     const __nv_bfloat16 ha = __float2bfloat16_rn(pa), hb = __float2bfloat16_rn(pb);
     const __nv_bfloat162 l = __floats2bfloat162_rn(pa - __bfloat162float(ha), pb - __bfloat162float(hb));
     *lo = *reinterpret_cast<const uint32_t *>(&l);
@@ -157,7 +166,8 @@ __device__ __forceinline__ uint32_t phi2_split_w(uint32_t w, float wt, uint32_t 
     return *reinterpret_cast<const uint32_t *>(&h);
 }
 template <int D, int NT>
-__device__ __forceinline__ void phi_tile_split_w(uint8_t *tile, uint8_t *lo, int t, int valid, float lg, int ebase)
+__device__ __forceinline__ void phi_tile_split_w(uint8_t *tile, uint8_t *lo, int t, int valid, float lg, int ebase,
+                                                 int map, float c)
 {
     constexpr int kUnits = 128 * (D / 32);
     constexpr int NU = (kUnits + NT - 1) / NT;
@@ -175,10 +185,10 @@ __device__ __forceinline__ void phi_tile_split_w(uint8_t *tile, uint8_t *lo, int
         for (int k = 0; k < 4; ++k) {
             uint4 h = make_uint4(0u, 0u, 0u, 0u), l = make_uint4(0u, 0u, 0u, 0u);
             if (row < valid) {
-                h.x = phi2_split_w(x[k].x, wt, &l.x);
-                h.y = phi2_split_w(x[k].y, wt, &l.y);
-                h.z = phi2_split_w(x[k].z, wt, &l.z);
-                h.w = phi2_split_w(x[k].w, wt, &l.w);
+                h.x = phi2_split_w(x[k].x, wt, &l.x, map, c);
+                h.y = phi2_split_w(x[k].y, wt, &l.y, map, c);
+                h.z = phi2_split_w(x[k].z, wt, &l.z, map, c);
+                h.w = phi2_split_w(x[k].w, wt, &l.w, map, c);
             }
             *reinterpret_cast<uint4 *>(tile + off + ((rot + k) & 7) * 16) = h;
             *reinterpret_cast<uint4 *>(lo + off + ((rot + k) & 7) * 16) = l;
@@ -320,7 +330,7 @@ __device__ __forceinline__ bool epi_barrier(int *abort_flag, uint64_t *bar, uint
     return ok;
 }
 
-template <int D>
+template <int D, bool kVar>
 __global__ void __launch_bounds__(512, 1)
 noncausal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                     const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_o,
@@ -417,14 +427,14 @@ noncausal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
                     // MMAs of the tile two before have read that buffer.
                     const int b = j & 1, n = j >> 1;
                     if (n > 0 && !(ok = wait_bar_warp(abort_flag, &sm.lo_free[b], (n - 1) & 1))) break;
-                    if (prm.gamma)
+                    if (kVar || prm.gamma)
                         phi_tile_split_w<D, kPhiThreads>(sm.stage[s], b ? sm.lo1 : sm.aux + CF::kImg0, t, valid,
-                                                         log2f(__ldg(prm.gamma + item.bh % prm.H)),
-                                                         prm.N - 1 - (item.c0 + c) * kC);
+                                                         prm.gamma ? log2f(__ldg(prm.gamma + item.bh % prm.H)) : 0.f,
+                                                         prm.N - 1 - (item.c0 + c) * kC, prm.map, prm.shift);
                     else
                         phi_tile_split<D, kPhiThreads>(sm.stage[s], b ? sm.lo1 : sm.aux + CF::kImg0, t, valid);
                 } else {
-                    phi_tile<D, kPhiThreads>(sm.stage[s], t, valid);
+                    phi_tile<D, kPhiThreads, false, kVar>(sm.stage[s], t, valid, 0.f, 0, prm.map, prm.shift);
                 }
                 fence_proxy_async_smem();
                 mbar_arrive(&sm.phi_done[s]);
@@ -721,7 +731,9 @@ noncausal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
                         tmem_ld32(ta + D, qz);
                         tmem_ld_wait();
                         constexpr int zc = CF::kFused ? 0 : 1;
-                        inv = 1.f / fmaxf(__uint_as_float(qz[zc]) + __uint_as_float(qz[zc + 1]), prm.eps);
+                        inv = (kVar && !prm.normalize)
+                                  ? 1.f
+                                  : 1.f / fmaxf(__uint_as_float(qz[zc]) + __uint_as_float(qz[zc + 1]), prm.eps);
                     }
                     uint8_t *ost = sm.stage[s] + kTile;  // the second tile of the stage stages O
 #pragma unroll 1
@@ -788,7 +800,7 @@ noncausal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
 }
 
 // ------------------------------------------------------------------ host side
-template <int D>
+template <int D, bool kVar>
 la_status launch(const Problem &p, float *S_out = nullptr, float *z_out = nullptr)
 {
     using CF = Cfg<D>;
@@ -867,9 +879,12 @@ la_status launch(const Problem &p, float *S_out = nullptr, float *z_out = nullpt
     prm.z_out = z_out;
     prm.gamma = state ? p.gamma : nullptr;
     prm.H = p.H;
+    prm.map = p.var.map;
+    prm.shift = p.var.shift;
+    prm.normalize = p.var.normalize;
 
     const int smem = (int)sizeof(Smem<D>);
-    auto kern = noncausal_tc_kernel<D>;
+    auto kern = noncausal_tc_kernel<D, kVar>;
     st = ensure_smem((const void *)kern, smem);
     if (st != LA_OK) return st;
     const unsigned grid = (unsigned)std::min<long long>(items, n_sm);
@@ -883,11 +898,12 @@ la_status noncausal_tc(const Problem &p)
 {
     if (p.dtype != LA_BF16 || p.dk != p.dv || (p.dk != 64 && p.dk != 128) || p.N < kC)
         return LA_ERR_UNSUPPORTED;
-    return p.dk == 128 ? launch<128>(p) : launch<64>(p);
+    if (!p.var.is_default()) return p.dk == 128 ? launch<128, true>(p) : launch<64, true>(p);
+    return p.dk == 128 ? launch<128, false>(p) : launch<64, false>(p);
 }
 
 la_status noncausal_tc_state(const void *k, const void *v, float *S, float *z, int BH, int N, int D,
-                             cudaStream_t stream, const float *gamma, int H)
+                             cudaStream_t stream, const float *gamma, int H, const Variant &var)
 {
     if ((D != 64 && D != 128) || N < kC) return LA_ERR_UNSUPPORTED;
     Problem p{};
@@ -904,7 +920,11 @@ la_status noncausal_tc_state(const void *k, const void *v, float *S, float *z, i
     p.stream = stream;
     p.gamma = gamma;
     p.H = H;
-    return D == 128 ? launch<128>(p, S, z) : launch<64>(p, S, z);
+    // the state does not depend on the normaliser: only a map other than elu + 1 is a variant
+    p.var.map = var.map;
+    p.var.shift = var.shift;
+    if (var.map != LA_PHI_ELU1) return D == 128 ? launch<128, true>(p, S, z) : launch<64, true>(p, S, z);
+    return D == 128 ? launch<128, false>(p, S, z) : launch<64, false>(p, S, z);
 }
 
 la_status tc_noncausal_read_status(cudaStream_t s, unsigned *bits)

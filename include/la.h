@@ -228,6 +228,59 @@ la_status la_prefill_state_decay(const void *k, const void *v, const float *gamm
                                  float *z, int B, int H, int N, int dk, int dv, la_dtype dtype,
                                  la_stream_t stream);
 
+/*
+ * Variants of the feature map and of the normaliser.
+ *
+ * Feature maps ("Linear attention", learn.pranaymahendrakar.com, What the
+ * pieces are for: ReLU among the alternatives to elu + 1; "Linear Attention --
+ * Math + Variants", Feature-map families: ReLU and identity-plus-shift; "26.
+ * Linear (Kernelized) Attention", Key Functions & Tricks: relu(x) + eps):
+ *   LA_PHI_ELU1      phi(x) = elu(x) + 1          (the default; shift ignored)
+ *   LA_PHI_RELU      phi(x) = max(x, 0) + shift   (shift >= 0 keeps phi >= 0)
+ *   LA_PHI_IDENTITY  phi(x) = x + shift
+ * normalize = 1: o = phi(q)^T S / max(phi(q)^T z, eps) (the default);
+ * normalize = 0: o = phi(q)^T S, the normaliser-free output that "Linear
+ * Attention -- Math + Variants", Implementation reality, describes (a
+ * normalisation layer after attention, which needs trained weights, is the
+ * caller's).  A NULL variant pointer means the default.
+ */
+typedef enum { LA_PHI_ELU1 = 0, LA_PHI_RELU = 1, LA_PHI_IDENTITY = 2 } la_feature_map;
+
+typedef struct {
+    int feature_map; /* la_feature_map */
+    float shift;     /* finite */
+    int normalize;   /* 0 or 1 */
+} la_variant;
+
+/*
+ * The general forms: any feature map, with or without the normaliser, with or
+ * without the decayed state (gamma: DEVICE pointer to H fp32 values, one per
+ * head, as la_forward_causal_decay; NULL = no decay).  Same layouts, checks
+ * and results as the specialised entry points, which they reduce to:
+ *   la_forward_causal_ex(..., NULL, NULL, ...)   = la_forward_causal
+ *   la_forward_causal_ex(..., gamma, NULL, ...)  = la_forward_causal_decay
+ * bf16 with dk = dv in {64, 128} (chunk 128 and N >= 128 for the causal form)
+ * runs on the tensor cores for every variant; other shapes on the CUDA cores.
+ * An invalid variant (unknown map, non-finite shift, normalize not 0 or 1)
+ * returns LA_ERR_INVALID_ARG.
+ */
+la_status la_forward_causal_ex(const void *q, const void *k, const void *v, void *o,
+                               const float *gamma, const la_variant *variant, int B, int H,
+                               int N, int dk, int dv, int chunk, float eps, la_dtype dtype,
+                               la_stream_t stream);
+la_status la_forward_noncausal_ex(const void *q, const void *k, const void *v, void *o,
+                                  const la_variant *variant, int B, int H, int N, int dk,
+                                  int dv, float eps, la_dtype dtype, la_stream_t stream);
+la_status la_decode_step_ex(float *S, float *z, const void *q, const void *k, const void *v,
+                            void *o, const float *gamma, const la_variant *variant, int B,
+                            int H, int dk, int dv, float eps, la_dtype dtype,
+                            la_stream_t stream);
+/* The prefix state under a feature map (normalize is ignored: S and z are the
+ * same either way) and an optional decay. */
+la_status la_prefill_state_ex(const void *k, const void *v, const float *gamma,
+                              const la_variant *variant, float *S, float *z, int B, int H,
+                              int N, int dk, int dv, la_dtype dtype, la_stream_t stream);
+
 /* Human-readable name of a status code (static string, never NULL). */
 const char *la_status_string(la_status s);
 

@@ -36,7 +36,8 @@ def test_exports_every_declared_symbol(lib):
     names = declared_functions()
     assert set(names) >= {"la_forward_causal", "la_forward_noncausal", "la_decode_step",
                           "la_prefill_state", "la_forward_causal_decay", "la_decode_step_decay",
-                          "la_prefill_state_decay",
+                          "la_prefill_state_decay", "la_forward_causal_ex", "la_forward_noncausal_ex",
+                          "la_decode_step_ex", "la_prefill_state_ex",
                           "la_status_string", "la_last_cuda_error",
                           "la_get_device_status", "la_version"}
     for n in names:
@@ -160,6 +161,31 @@ def test_prefill_decay_validation(lib):
     assert f(A, A, g, M, z, 1, 1, 8, 64, 64, 1, None) == MISALIGNED
     assert f(A, A, g, S, z, 1, 1, 8, 24, 64, 1, None) == UNSUPPORTED
     assert f(None, None, None, None, None, 0, 1, 8, 64, 64, 1, None) == OK
+
+
+def test_variant_validation(lib):
+    """An unknown feature map, a non-finite shift or a normalize flag other than 0/1 is
+    rejected by every _ex entry point before any work; so is a misaligned gamma."""
+    V = la.Variant
+    e = ctypes.c_float(1e-6)
+    q, k, v, o = A, A + 0x100000, A + 0x200000, A + 0x300000
+    S, z, g = A + 0x800000, A + 0x900000, A + 0xA00000
+    bad = [V(7, 0.0, 1), V(-1, 0.0, 1), V(1, float("nan"), 1), V(2, float("inf"), 0), V(1, 0.0, 2)]
+    for var in bad:
+        r = ctypes.byref(var)
+        assert lib.la_forward_causal_ex(q, k, v, o, None, r, 1, 2, 16, 64, 64, 128, e, 1, None) == INVALID
+        assert lib.la_forward_noncausal_ex(q, k, v, o, r, 1, 2, 16, 64, 64, e, 1, None) == INVALID
+        assert lib.la_decode_step_ex(S, z, q, k, v, o, None, r, 1, 2, 64, 64, e, 1, None) == INVALID
+        assert lib.la_prefill_state_ex(k, v, None, r, S, z, 1, 2, 16, 64, 64, 1, None) == INVALID
+    ok = ctypes.byref(V(1, 0.5, 0))
+    assert lib.la_forward_causal_ex(q, k, v, o, g + 2, ok, 1, 2, 16, 64, 64, 128, e, 1, None) == MISALIGNED
+    assert lib.la_forward_causal_ex(q, k, v, M, None, ok, 1, 2, 16, 64, 64, 128, e, 1, None) == MISALIGNED
+    assert lib.la_forward_causal_ex(q, k, v, o, None, ok, 1, 2, 16, 48, 64, 128, e, 1, None) == UNSUPPORTED
+    assert lib.la_decode_step_ex(S, z, q, k, v, o, g + 1, ok, 1, 2, 64, 64, e, 1, None) == MISALIGNED
+    assert lib.la_prefill_state_ex(k, v, g + 2, ok, S, z, 1, 2, 16, 64, 64, 1, None) == MISALIGNED
+    # empty problems are a no-op with any valid variant
+    assert lib.la_forward_causal_ex(None, None, None, None, None, ok, 1, 2, 0, 64, 64, 128, e, 1, None) == OK
+    assert lib.la_forward_noncausal_ex(None, None, None, None, ok, 0, 2, 16, 64, 64, e, 1, None) == OK
 
 
 def test_binding_raises_without_cuda_tensors():
