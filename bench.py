@@ -520,6 +520,56 @@ def bench_path_prefill_decay(torch, la, reps, peaks, src):
             "l2": "k, v 1.07 GB > L2"}
 
 
+def bench_path_causal_variant(torch, la, reps, peaks, src, tag, decay, fmap, shift, normalize):
+    """la_forward_causal_ex on the headline causal shape (B=4 H=8 N=2048 d=64, chunk
+    128, bf16) with a feature map, normaliser choice and optional per-head decay."""
+    w = workloads.CAUSAL_BF16
+    q, k, v = workloads.forward_inputs(w)
+    nbytes = forward_bytes(w.BH, w.N, w.dk, w.dv, 2)
+    R = n_rotations(nbytes)
+    base = [dev_copy(torch, x, "bf16") for x in (q, k, v)]
+    sets = [[t.clone() for t in base] + [torch.empty_like(base[2])] for _ in range(R)]
+    g = torch.from_numpy(workloads.decay_gammas(w.H)).cuda() if decay else None
+
+    def step(i):
+        s = sets[i % R]
+        la.la_forward_causal_ex(s[0], s[1], s[2], s[3], gamma=g, feature_map=fmap, shift=shift,
+                                normalize=normalize, chunk=w.chunk, eps=w.eps)
+
+    secs, launches, _ = time_graph_steps(torch, la, step, reps, 3, Dist())
+    t = secs / reps
+    fl = causal_flops(w.BH, w.N, w.dk, w.dv, w.chunk)
+    return {"workload": w.name + "_" + tag, "value": round(w.B * w.N / t, 1), "unit": "tokens/s",
+            "ms_per_step": round(t * 1e3, 4), "launches_per_step": launches / reps,
+            "variant": {"feature_map": fmap, "shift": shift, "normalize": normalize, "decay": decay},
+            "roofline": roofline(fl, nbytes, t, peaks, src, ncu_traffic("causal_" + tag)),
+            "l2": "%d rotating buffer sets" % R}
+
+
+def bench_path_noncausal_variant(torch, la, reps, peaks, src, tag, fmap, shift, normalize):
+    """la_forward_noncausal_ex on the non-causal workload (B=8 H=12 N=4096 d=64, bf16)."""
+    w = workloads.NONCAUSAL_BF16
+    q, k, v = workloads.forward_inputs(w)
+    nbytes = forward_bytes(w.BH, w.N, w.dk, w.dv, 2)
+    R = n_rotations(nbytes)
+    base = [dev_copy(torch, x, "bf16") for x in (q, k, v)]
+    sets = [[t.clone() for t in base] + [torch.empty_like(base[2])] for _ in range(R)]
+
+    def step(i):
+        s = sets[i % R]
+        la.la_forward_noncausal_ex(s[0], s[1], s[2], s[3], feature_map=fmap, shift=shift, normalize=normalize,
+                                   eps=w.eps)
+
+    secs, launches, _ = time_graph_steps(torch, la, step, reps, 3, Dist())
+    t = secs / reps
+    fl = noncausal_flops(w.BH, w.N, w.dk, w.dv)
+    return {"workload": w.name + "_" + tag, "value": round(w.B * w.N / t, 1), "unit": "tokens/s",
+            "ms_per_step": round(t * 1e3, 4), "launches_per_step": launches / reps,
+            "variant": {"feature_map": fmap, "shift": shift, "normalize": normalize},
+            "roofline": roofline(fl, nbytes, t, peaks, src, ncu_traffic("noncausal_" + tag)),
+            "l2": "%d rotating buffer sets" % R}
+
+
 def bench_path_decode_decay(torch, la, steps, peaks, src):
     """la_decode_step_decay on the decode workload (4096 heads, d = 128, fp32 state)."""
     w = workloads.DECODE_BF16
@@ -642,6 +692,12 @@ def run_gpu(args, dist):
         paths["causal_decay"] = bench_path_causal_decay(torch, la, max(args.path_reps, 20), peaks, src)
         paths["decode_decay"] = bench_path_decode_decay(torch, la, 1024, peaks, src)
         paths["prefill_state_decay"] = bench_path_prefill_decay(torch, la, max(args.path_reps, 20), peaks, src)
+        reps = max(args.path_reps, 20)
+        paths["causal_relu"] = bench_path_causal_variant(torch, la, reps, peaks, src, "relu", False, "relu", 0.0, True)
+        paths["causal_retention"] = bench_path_causal_variant(torch, la, reps, peaks, src, "retention", True,
+                                                              "identity", 0.0, False)
+        paths["noncausal_relu_nonorm"] = bench_path_noncausal_variant(torch, la, reps, peaks, src, "relu_nonorm",
+                                                                      "relu", 0.0, False)
         if s2:
             paths["clocks"] = s2.stop(window=(t_paths, time.time()))
 
@@ -676,7 +732,8 @@ def run_gpu(args, dist):
 
 
 PROFILE_CASES = ("headline", "causal_long", "causal_long_quarter", "noncausal", "decode", "prefill_state_quarter",
-                 "causal_decay", "decode_decay", "prefill_state_decay_quarter")
+                 "causal_decay", "decode_decay", "prefill_state_decay_quarter", "causal_relu", "causal_retention",
+                 "noncausal_relu_nonorm")
 
 
 def run_profile_case(name: str, launches: int) -> int:
@@ -691,7 +748,22 @@ def run_profile_case(name: str, launches: int) -> int:
     from causal_kernelized_attention_gb300 import build as la_build
     la_build.build()
     la.load_library()
-    if name == "causal_decay":
+    if name in ("causal_relu", "causal_retention"):
+        w = workloads.CAUSAL_BF16
+        q, k, v = workloads.device_forward_inputs(w)
+        o = torch.empty_like(v)
+        retention = name == "causal_retention"
+        g = torch.from_numpy(workloads.decay_gammas(w.H)).cuda() if retention else None
+        for _ in range(launches):
+            la.la_forward_causal_ex(q, k, v, o, gamma=g, feature_map="identity" if retention else "relu",
+                                    normalize=not retention, chunk=w.chunk, eps=w.eps)
+    elif name == "noncausal_relu_nonorm":
+        w = workloads.NONCAUSAL_BF16
+        q, k, v = workloads.device_forward_inputs(w)
+        o = torch.empty_like(v)
+        for _ in range(launches):
+            la.la_forward_noncausal_ex(q, k, v, o, feature_map="relu", normalize=False, eps=w.eps)
+    elif name == "causal_decay":
         w = workloads.CAUSAL_BF16
         q, k, v = workloads.device_forward_inputs(w)
         o = torch.empty_like(v)

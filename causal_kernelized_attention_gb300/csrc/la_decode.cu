@@ -55,7 +55,7 @@ __device__ __forceinline__ void st_stream(float4 *p, float4 v)
 
 // Grid: one CTA per head (blockIdx.x = b*H + h).  kDecay: gamma[(b*H + h) % H]
 // scales the old S and z.
-template <typename T, int DK, int DV, bool kDecay>
+template <typename T, int DK, int DV, bool kDecay, bool kVar>
 __global__ void __launch_bounds__(kDecodeThreads)
 decode_kernel(float *__restrict__ S, float *__restrict__ z, const T *__restrict__ q,
               const T *__restrict__ k, const T *__restrict__ v, T *__restrict__ o, float eps,
@@ -81,8 +81,13 @@ decode_kernel(float *__restrict__ S, float *__restrict__ z, const T *__restrict_
     const float g = kDecay ? gamma[head % H] : 1.f;
 
     for (int r = tid; r < DK; r += kDecodeThreads) {
-        fq[r] = phi_variant<T>(Elem<T>::to_f32(q[head * DK + r]), var);
-        fk[r] = phi_variant<T>(Elem<T>::to_f32(k[head * DK + r]), var);
+        if (kVar) {
+            fq[r] = phi_variant<T>(Elem<T>::to_f32(q[head * DK + r]), var);
+            fk[r] = phi_variant<T>(Elem<T>::to_f32(k[head * DK + r]), var);
+        } else {
+            fq[r] = Elem<T>::phi(Elem<T>::to_f32(q[head * DK + r]));
+            fk[r] = Elem<T>::phi(Elem<T>::to_f32(k[head * DK + r]));
+        }
     }
     float vc[4];
     load4<T>(v + head * DV + 4 * cg, vc);
@@ -117,7 +122,7 @@ decode_kernel(float *__restrict__ S, float *__restrict__ z, const T *__restrict_
     float den = 0.f;
 #pragma unroll
     for (int w = 0; w < kDecodeThreads / 32; ++w) den += red[w];
-    const float inv = var.normalize ? 1.f / fmaxf(den, eps) : 1.f;
+    const float inv = (kVar && !var.normalize) ? 1.f : 1.f / fmaxf(den, eps);
 
     // Column sums of the row-group partials: thread t < DV produces o[t].
     if (tid < DV) {
@@ -148,12 +153,10 @@ template <typename T, int DK, int DV>
 la_status launch(const DecodeArgs &a)
 {
     count_launches();
-    if (a.gamma)
-        decode_kernel<T, DK, DV, true><<<a.BH, kDecodeThreads, 0, a.stream>>>(
-            a.S, a.z, (const T *)a.q, (const T *)a.k, (const T *)a.v, (T *)a.o, a.eps, a.gamma, a.H, a.var);
-    else
-        decode_kernel<T, DK, DV, false><<<a.BH, kDecodeThreads, 0, a.stream>>>(
-            a.S, a.z, (const T *)a.q, (const T *)a.k, (const T *)a.v, (T *)a.o, a.eps, nullptr, 1, a.var);
+    auto kern = a.gamma ? (a.var.is_default() ? decode_kernel<T, DK, DV, true, false> : decode_kernel<T, DK, DV, true, true>)
+                        : (a.var.is_default() ? decode_kernel<T, DK, DV, false, false> : decode_kernel<T, DK, DV, false, true>);
+    kern<<<a.BH, kDecodeThreads, 0, a.stream>>>(a.S, a.z, (const T *)a.q, (const T *)a.k, (const T *)a.v, (T *)a.o,
+                                                 a.eps, a.gamma, a.gamma ? a.H : 1, a.var);
     return cuda_status(cudaGetLastError());
 }
 

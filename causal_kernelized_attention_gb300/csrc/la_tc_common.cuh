@@ -83,16 +83,16 @@ __device__ __forceinline__ uint32_t phi2(uint32_t w)
 }
 
 // Feature-map variants on a pair of bf16 values (map LA_PHI_RELU: max(x, 0) + c,
-// LA_PHI_IDENTITY: x + c; LA_PHI_ELU1: phi2), in fp32 with one rounding to bf16.
-__device__ __forceinline__ uint32_t phi2_variant(uint32_t w, int map, float c)
+// LA_PHI_IDENTITY: x + c; LA_PHI_ELU1: phi2), in packed bf16: the max is exact and
+// the add rounds once; c2 is the shift rounded to bf16 (2^-9 relative, the size of
+// the operand's own rounding).
+__device__ __forceinline__ uint32_t phi2_variant(uint32_t w, int map, uint32_t c2)
 {
     if (map == LA_PHI_ELU1) return phi2(w);
-    float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w));
-    if (map == LA_PHI_RELU) {
-        f.x = fmaxf(f.x, 0.f);
-        f.y = fmaxf(f.y, 0.f);
-    }
-    return pack_bf16(f.x + c, f.y + c);
+    __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162 *>(&w);
+    if (map == LA_PHI_RELU) x = __hmax2(x, __float2bfloat162_rn(0.f));
+    const __nv_bfloat162 r = __hadd2(x, *reinterpret_cast<const __nv_bfloat162 *>(&c2));
+    return *reinterpret_cast<const uint32_t *>(&r);
 }
 
 // Decayed state: gamma^e for an integer e >= 0 from lg = log2(gamma) (gamma^0 = 1
@@ -144,6 +144,7 @@ __device__ __forceinline__ void phi_tile(uint8_t *tile, int t, int valid, float 
 {
     constexpr int kUnits = 128 * (D / 32);
     constexpr int NU = (kUnits + NT - 1) / NT;
+    const uint32_t c2 = kVar ? pack_bf16(c, c) : 0u;
     uint4 buf[NU][4];
 #pragma unroll
     for (int m = 0; m < NU; ++m) {
@@ -163,8 +164,8 @@ __device__ __forceinline__ void phi_tile(uint8_t *tile, int t, int valid, float 
         for (int k = 0; k < 4; ++k) {
             uint4 &x = buf[m][k];
             if (kVar)
-                x = row < valid ? make_uint4(phi2_variant(x.x, map, c), phi2_variant(x.y, map, c),
-                                             phi2_variant(x.z, map, c), phi2_variant(x.w, map, c))
+                x = row < valid ? make_uint4(phi2_variant(x.x, map, c2), phi2_variant(x.y, map, c2),
+                                             phi2_variant(x.z, map, c2), phi2_variant(x.w, map, c2))
                                 : make_uint4(0u, 0u, 0u, 0u);
             else
                 x = row < valid ? make_uint4(phi2(x.x), phi2(x.y), phi2(x.z), phi2(x.w)) : make_uint4(0u, 0u, 0u, 0u);

@@ -154,18 +154,20 @@ __device__ __forceinline__ float phi_map_f32(float x, int map, float c)
 {
     return map == LA_PHI_RELU ? fmaxf(x, 0.f) + c : map == LA_PHI_IDENTITY ? x + c : (x > 0.f ? x + 1.f : __expf(x));
 }
+template <bool kVar>
 __device__ __forceinline__ uint32_t phi2_split_w(uint32_t w, float wt, uint32_t *lo, int map, float c)
 {
     const __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162 *>(&w);
     const float a = __bfloat162float(x.x), b = __bfloat162float(x.y);
-    const float pa = phi_map_f32(a, map, c) * wt, pb = phi_map_f32(b, map, c) * wt;
+    const float pa = (kVar ? phi_map_f32(a, map, c) : (a > 0.f ? a + 1.f : __expf(a))) * wt;
+    const float pb = (kVar ? phi_map_f32(b, map, c) : (b > 0.f ? b + 1.f : __expf(b))) * wt;
     const __nv_bfloat16 ha = __float2bfloat16_rn(pa), hb = __float2bfloat16_rn(pb);
     const __nv_bfloat162 l = __floats2bfloat162_rn(pa - __bfloat162float(ha), pb - __bfloat162float(hb));
     *lo = *reinterpret_cast<const uint32_t *>(&l);
     const __nv_bfloat162 h = __halves2bfloat162(ha, hb);
     return *reinterpret_cast<const uint32_t *>(&h);
 }
-template <int D, int NT>
+template <int D, int NT, bool kVar>
 __device__ __forceinline__ void phi_tile_split_w(uint8_t *tile, uint8_t *lo, int t, int valid, float lg, int ebase,
                                                  int map, float c)
 {
@@ -185,10 +187,10 @@ __device__ __forceinline__ void phi_tile_split_w(uint8_t *tile, uint8_t *lo, int
         for (int k = 0; k < 4; ++k) {
             uint4 h = make_uint4(0u, 0u, 0u, 0u), l = make_uint4(0u, 0u, 0u, 0u);
             if (row < valid) {
-                h.x = phi2_split_w(x[k].x, wt, &l.x, map, c);
-                h.y = phi2_split_w(x[k].y, wt, &l.y, map, c);
-                h.z = phi2_split_w(x[k].z, wt, &l.z, map, c);
-                h.w = phi2_split_w(x[k].w, wt, &l.w, map, c);
+                h.x = phi2_split_w<kVar>(x[k].x, wt, &l.x, map, c);
+                h.y = phi2_split_w<kVar>(x[k].y, wt, &l.y, map, c);
+                h.z = phi2_split_w<kVar>(x[k].z, wt, &l.z, map, c);
+                h.w = phi2_split_w<kVar>(x[k].w, wt, &l.w, map, c);
             }
             *reinterpret_cast<uint4 *>(tile + off + ((rot + k) & 7) * 16) = h;
             *reinterpret_cast<uint4 *>(lo + off + ((rot + k) & 7) * 16) = l;
@@ -428,7 +430,7 @@ noncausal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
                     const int b = j & 1, n = j >> 1;
                     if (n > 0 && !(ok = wait_bar_warp(abort_flag, &sm.lo_free[b], (n - 1) & 1))) break;
                     if (kVar || prm.gamma)
-                        phi_tile_split_w<D, kPhiThreads>(sm.stage[s], b ? sm.lo1 : sm.aux + CF::kImg0, t, valid,
+                        phi_tile_split_w<D, kPhiThreads, kVar>(sm.stage[s], b ? sm.lo1 : sm.aux + CF::kImg0, t, valid,
                                                          prm.gamma ? log2f(__ldg(prm.gamma + item.bh % prm.H)) : 0.f,
                                                          prm.N - 1 - (item.c0 + c) * kC, prm.map, prm.shift);
                     else
