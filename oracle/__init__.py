@@ -69,6 +69,7 @@ def _declare(lib):
         "la_oracle_prefill_state_general": ([P, P, I, P, I, D, P, P, I, I, I, I], None),
         "la_oracle_noncausal_general": ([P, P, P, I, I, D, I, P, I, I, I, I, D], None),
         "la_oracle_decode_step_general": ([P, P, P, P, P, I, P, I, D, I, P, I, I, I, D], None),
+        "la_oracle_causal_backward": ([P, P, P, P, I, P, P, P, I, I, I, I, D], None),
         "la_oracle_num_threads": ([], I),
     }
     for name, (args, res) in sigs.items():
@@ -310,6 +311,24 @@ class Oracle:
                                                    self.FMAPS[fmap], float(shift), int(bool(normalize)),
                                                    _ptr(o), BH, dk, dv, float(eps))
         return o
+
+    # ---------------------------------------------------------------- backward pass
+    def causal_backward(self, q, k, v, dout, eps=1e-6):
+        """Gradients (dq, dk, dv) of sum(dout * o) for the causal form (elu + 1, normalised)."""
+        (q, k, v, dout), t = _prep(q, k, v, dout)
+        N, dk = q.shape[-2], q.shape[-1]
+        dv = v.shape[-1]
+        lead = q.shape[:-2]
+        if k.shape != q.shape or v.shape[:-1] != q.shape[:-1] or dout.shape != v.shape:
+            raise ValueError("shape mismatch")
+        BH = int(np.prod(lead)) if lead else 1
+        gq = np.zeros(q.shape, dtype=np.float64)
+        gk = np.zeros(k.shape, dtype=np.float64)
+        gv = np.zeros(v.shape, dtype=np.float64)
+        if BH and N:
+            self.lib.la_oracle_causal_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), t, _ptr(gq), _ptr(gk), _ptr(gv),
+                                               BH, N, dk, dv, float(eps))
+        return gq, gk, gv
 
 
 _default = None

@@ -713,6 +713,103 @@ void la_oracle_decode_step_general(double *S, double *z, const void *q, const vo
     }
 }
 
+/* ---------------------------------------------------------------------------
+ * Backward pass of the causal form (elu + 1, with the normaliser): given dO,
+ * the gradients dq, dk, dv of L = sum_i dO_i . o_i.  The pages give no
+ * gradient ("Linear Attention -- Math + Variants", Chunkwise parallelism:
+ * training runs the parallel form); this is the chain rule applied to the
+ * recurrence's definition, with n_i = phi(q_i)^T S_i, d_i = max(phi(q_i)^T z_i, eps),
+ * o_i = n_i / d_i:
+ *   dn_i = dO_i / d_i,  dd_i = -(dO_i . o_i) / d_i  (0 where the clamp binds),
+ *   dphi(q_i) = S_i dn_i + dd_i z_i                    (S_i, z_i inclusive),
+ *   dphi(k_j) = R_j v_j + r_j,  dv_j = R_j^T phi(k_j),
+ *   R_j = sum_{i>=j} phi(q_i) dn_i^T,  r_j = sum_{i>=j} dd_i phi(q_i),
+ *   dq = dphi(q) * phi'(q),  dk = dphi(k) * phi'(k),  phi'(x) = 1 (x > 0), exp(x).
+ * Two passes per sequence: forward (S, z: o, d, dn, dd, dq) and backward (R, r:
+ * dk, dv).  dO has the layout of v; dq, dk of q; dv of v (all double).
+ * ------------------------------------------------------------------------- */
+static double phi_prime(double x)
+{
+    return x > 0.0 ? 1.0 : exp(x);
+}
+
+void la_oracle_causal_backward(const void *q, const void *k, const void *v, const void *dout, int type,
+                               double *dq, double *dk, double *dv, int BH, int N, int dkd, int dvd, double eps)
+{
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int bh = 0; bh < BH; ++bh) {
+        const int64_t qb = (int64_t)bh * N * dkd, vb = (int64_t)bh * N * dvd;
+        double *S = calloc((size_t)dkd * dvd, sizeof(double));
+        double *z = calloc((size_t)dkd, sizeof(double));
+        double *fq = malloc(sizeof(double) * dkd);
+        double *fk = malloc(sizeof(double) * dkd);
+        double *vt = malloc(sizeof(double) * dvd);
+        double *dn = malloc(sizeof(double) * (size_t)N * dvd);  /* dn_i for the second pass */
+        double *dd = malloc(sizeof(double) * (size_t)N);
+        /* pass 1: t = 0 .. N-1 */
+        for (int t = 0; t < N; ++t) {
+            phi_row(q, type, qb, t, dkd, fq);
+            phi_row(k, type, qb, t, dkd, fk);
+            for (int c = 0; c < dvd; ++c)
+                vt[c] = load(v, type, vb + (int64_t)t * dvd + c);
+            for (int r = 0; r < dkd; ++r) {
+                double *Sr = S + (size_t)r * dvd;
+                for (int c = 0; c < dvd; ++c)
+                    Sr[c] += fk[r] * vt[c];
+                z[r] += fk[r];
+            }
+            double den = 0.0;
+            for (int r = 0; r < dkd; ++r)
+                den += fq[r] * z[r];
+            const int clamped = !(den > eps);
+            const double d = clamp_den(den, eps);
+            double g = 0.0; /* dO_t . o_t */
+            for (int c = 0; c < dvd; ++c) {
+                double n = 0.0;
+                for (int r = 0; r < dkd; ++r)
+                    n += fq[r] * S[(size_t)r * dvd + c];
+                const double go = load(dout, type, vb + (int64_t)t * dvd + c);
+                g += go * (n / d);
+                dn[(size_t)t * dvd + c] = go / d;
+            }
+            dd[t] = clamped ? 0.0 : -g / d;
+            for (int r = 0; r < dkd; ++r) {
+                double s = dd[t] * z[r];
+                for (int c = 0; c < dvd; ++c)
+                    s += S[(size_t)r * dvd + c] * dn[(size_t)t * dvd + c];
+                dq[qb + (int64_t)t * dkd + r] = s * phi_prime(load(q, type, qb + (int64_t)t * dkd + r));
+            }
+        }
+        /* pass 2: t = N-1 .. 0, R and r accumulate phi(q_i) dn_i^T and dd_i phi(q_i) for i >= t */
+        double *R = S, *rr = z;
+        memset(R, 0, sizeof(double) * (size_t)dkd * dvd);
+        memset(rr, 0, sizeof(double) * (size_t)dkd);
+        for (int t = N - 1; t >= 0; --t) {
+            phi_row(q, type, qb, t, dkd, fq);
+            phi_row(k, type, qb, t, dkd, fk);
+            for (int r = 0; r < dkd; ++r) {
+                double *Rr = R + (size_t)r * dvd;
+                for (int c = 0; c < dvd; ++c)
+                    Rr[c] += fq[r] * dn[(size_t)t * dvd + c];
+                rr[r] += dd[t] * fq[r];
+            }
+            for (int r = 0; r < dkd; ++r) {
+                double s = rr[r];
+                for (int c = 0; c < dvd; ++c)
+                    s += R[(size_t)r * dvd + c] * load(v, type, vb + (int64_t)t * dvd + c);
+                dk[qb + (int64_t)t * dkd + r] = s * phi_prime(load(k, type, qb + (int64_t)t * dkd + r));
+            }
+            for (int c = 0; c < dvd; ++c) {
+                double s = 0.0;
+                for (int r = 0; r < dkd; ++r)
+                    s += R[(size_t)r * dvd + c] * fk[r];
+                dv[vb + (int64_t)t * dvd + c] = s;
+            }
+        }
+        free(S); free(z); free(fq); free(fk); free(vt); free(dn); free(dd);
+    }
+}
+
 /* Threads OpenMP will use (reported beside CPU timings). */
 int la_oracle_num_threads(void)
 {

@@ -517,4 +517,81 @@ def pin_general_decode_continues_causal(orc):
             assert _rel_err(o, full[:, t]) < 1e-12, (fmap, t)
 
 
+# ----------------------------------------------------------------------------
+# backward pass of the causal form: gradients of L = sum(dO * o).  The pages give
+# none; the oracle's chain-rule scans are pinned to finite differences of the
+# (already pinned) forward oracle and to closed forms.
+# ----------------------------------------------------------------------------
+def _finite_difference(orc, q, k, v, dout, h=1e-6):
+    def loss(qq, kk, vv):
+        return float(np.sum(orc.causal_recurrent(qq, kk, vv, EPS) * dout))
+    grads = []
+    for which in range(3):
+        xs = [q, k, v]
+        x = xs[which]
+        gx = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += h
+            xm[idx] -= h
+            args_p = list(xs); args_p[which] = xp
+            args_m = list(xs); args_m[which] = xm
+            gx[idx] = (loss(*args_p) - loss(*args_m)) / (2 * h)
+        grads.append(gx)
+    return grads
+
+
+def pin_backward_equals_finite_differences(orc):
+    """Central differences of the forward oracle (h = 1e-6, float64) within 1e-7."""
+    rng = np.random.default_rng(3000)
+    BH, N, dk, dv = 2, 9, 4, 3
+    q, k, v, dout = (rng.standard_normal((BH, N, d)) for d in (dk, dk, dv, dv))
+    for got, ref in zip(orc.causal_backward(q, k, v, dout), _finite_difference(orc, q, k, v, dout)):
+        assert _rel_err(got, ref) < 1e-7
+
+
+def pin_backward_dv_dense_form(orc):
+    """dv_j = sum_{i>=j} s_ij dO_i / d_i with s = phi(Q) phi(K)^T (dense numpy)."""
+    q, k, v = _rand(3010, 3, 30, 5, 4)
+    dout = _rand(3011, 3, 30, 5, 4)[2]
+    _, _, gv = orc.causal_backward(q, k, v, dout)
+    for s_ in range(3):
+        fq, fk = phi_np(q[s_]), phi_np(k[s_])
+        sc = np.tril(fq @ fk.T)
+        d = np.maximum(sc.sum(-1), EPS)
+        ref = sc.T @ (dout[s_] / d[:, None])
+        assert _rel_err(gv[s_], ref) < 1e-12
+
+
+def pin_backward_first_output_only(orc):
+    """o_0 = v_0 whatever q, k: a loss on position 0 alone gives dq = dk = 0 and
+    dv = dO at position 0 only."""
+    q, k, v = _rand(3020, 2, 12, 4, 3)
+    dout = np.zeros_like(v)
+    dout[:, 0] = _rand(3021, 2, 1, 4, 3)[2][:, 0]
+    gq, gk, gv = orc.causal_backward(q, k, v, dout)
+    assert np.max(np.abs(gq)) < 1e-14 and np.max(np.abs(gk)) < 1e-14
+    assert _rel_err(gv[:, 0], dout[:, 0]) < 1e-14 and np.max(np.abs(gv[:, 1:])) < 1e-14
+
+
+def pin_backward_constant_v(orc):
+    """With every v_j equal, o_i = v for all i: no gradient reaches q or k, and dv
+    sums to sum_i dO_i (the weights of each row sum to one)."""
+    q, k, _ = _rand(3030, 2, 20, 5, 3)
+    v = np.broadcast_to(np.array([0.5, -1.0, 2.0]), (2, 20, 3)).copy()
+    dout = _rand(3031, 2, 20, 5, 3)[2]
+    gq, gk, gv = orc.causal_backward(q, k, v, dout)
+    assert np.max(np.abs(gq)) < 1e-12 and np.max(np.abs(gk)) < 1e-12
+    assert _rel_err(gv.sum(1), dout.sum(1)) < 1e-12
+
+
+def pin_backward_linear_in_dout(orc):
+    q, k, v = _rand(3040, 2, 15, 4, 3)
+    d1, d2 = _rand(3041, 2, 15, 4, 3)[2], _rand(3042, 2, 15, 4, 3)[2]
+    a = orc.causal_backward(q, k, v, 2.0 * d1 - 3.0 * d2)
+    b1, b2 = orc.causal_backward(q, k, v, d1), orc.causal_backward(q, k, v, d2)
+    for x, y1, y2 in zip(a, b1, b2):
+        assert _rel_err(x, 2.0 * y1 - 3.0 * y2) < 1e-12
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -60,6 +60,12 @@ MUTANTS = {
     "prefill_general_undecayed": ("Sb[(size_t)r * dv + c] = g * Sb[(size_t)r * dv + c] +\n", "Sb[(size_t)r * dv + c] = Sb[(size_t)r * dv + c] +\n"),
     "noncausal_general_default_map": ("la_oracle_prefill_state_general(k, v, type, NULL, map, shift, S, z, BH, N, dk, dv);", "la_oracle_prefill_state_general(k, v, type, NULL, 0, shift, S, z, BH, N, dk, dv);"),
     "decode_general_key_from_query": ("fk[r] = phi_map(load(k, type, (int64_t)bh * dk + r), map, shift);", "fk[r] = phi_map(load(q, type, (int64_t)bh * dk + r), map, shift);"),
+    # backward pass
+    "backward_drops_denominator_term": ("dd[t] = clamped ? 0.0 : -g / d;", "dd[t] = 0.0;"),
+    "backward_reverse_state_from_k": ("Rr[c] += fq[r] * dn[(size_t)t * dvd + c];", "Rr[c] += fk[r] * dn[(size_t)t * dvd + c];"),
+    "backward_phi_prime_constant": ("    return x > 0.0 ? 1.0 : exp(x);", "    return 1.0;"),
+    "backward_dv_from_q": ("s += R[(size_t)r * dvd + c] * fk[r];", "s += R[(size_t)r * dvd + c] * fq[r];"),
+    "backward_dq_sign": ("double s = dd[t] * z[r];", "double s = -dd[t] * z[r];"),
 }
 
 
