@@ -100,6 +100,33 @@ def roofline(flops, nbytes, seconds, peaks, source, traffic=None, burst=True):
     return r
 
 
+# fp32 CUDA-core peak for the paths that run fp32 FMAs (no tensor cores): 152 SMs x 128
+# FP32 lanes x 2 flop per FMA x the 2070 MHz maximum SM clock.
+FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.070e9 / 1e12
+
+
+def roofline_alu(flops, nbytes, seconds, peaks, source, traffic=None):
+    """Roofline of an fp32 CUDA-core path: the slower of flops at the fp32 ALU peak
+    and bytes at the measured HBM bandwidth."""
+    t_mem = nbytes / (peaks["hbm_gbs"] * 1e9)
+    t_alu = flops / (FP32_ALU_TFLOPS * 1e12)
+    if t_mem >= t_alu:
+        achieved = nbytes / seconds / 1e9
+        r = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+             "frac": round(achieved / peaks["hbm_gbs"], 4)}
+    else:
+        achieved = flops / seconds / 1e12
+        r = {"bound": "alu", "achieved": round(achieved, 2), "peak": round(FP32_ALU_TFLOPS, 1), "unit": "TFLOP/s",
+             "frac": round(achieved / FP32_ALU_TFLOPS, 4)}
+    r["traffic"] = traffic
+    r["peak_source"] = ("derived fp32 ALU peak (152 SMs x 128 lanes x 2 x 2.07 GHz)" if r["bound"] == "alu" else
+                        "%s (%s)" % (source, "MEASURED_PEAKS.json" if source == "measured" else "recipe fallback"))
+    r["algorithmic_bytes"] = int(nbytes)
+    r["algorithmic_flop"] = flops
+    r["tflops"] = round(flops / seconds / 1e12, 3)
+    return r
+
+
 def ncu_traffic(kernel_tag):
     """DRAM bytes per launch from a committed ncu summary, if it still matches the
     kernel source (profiles/<tag>.md holds `traffic_bytes_per_launch:`,
@@ -570,6 +597,31 @@ def bench_path_noncausal_variant(torch, la, reps, peaks, src, tag, fmap, shift, 
             "l2": "%d rotating buffer sets" % R}
 
 
+def bench_path_backward(torch, la, reps, peaks, src):
+    """la_backward_causal on the headline causal shape (B=4 H=8 N=2048 d=64, bf16):
+    read q, k, v, dO and write dq, dk, dv once; fp32 arithmetic on the CUDA cores."""
+    w = workloads.CAUSAL_BF16
+    q, k, v = workloads.forward_inputs(w)
+    dout = workloads.random_inputs(w.seed + 100, w.B, w.H, w.N, w.dv, w.dv, "bf16")[2]
+    nbytes = w.BH * w.N * (4 * w.dk + 3 * w.dv) * 2
+    R = n_rotations(nbytes)
+    base = [dev_copy(torch, x, "bf16") for x in (q, k, v, dout)]
+    sets = [[t.clone() for t in base] + [torch.empty_like(base[0]), torch.empty_like(base[1]),
+                                         torch.empty_like(base[2])] for _ in range(R)]
+
+    def step(i):
+        s = sets[i % R]
+        la.la_backward_causal(s[0], s[1], s[2], s[3], s[4], s[5], s[6], eps=w.eps)
+
+    secs, launches, _ = time_graph_steps(torch, la, step, reps, 3, Dist())
+    t = secs / reps
+    fl = 3.0 * causal_flops(w.BH, w.N, w.dk, w.dv, 64)
+    return {"workload": w.name + "_backward", "value": round(w.B * w.N / t, 1), "unit": "tokens/s",
+            "ms_per_step": round(t * 1e3, 4), "launches_per_step": launches / reps,
+            "roofline": roofline_alu(fl, nbytes, t, peaks, src, ncu_traffic("backward")),
+            "l2": "%d rotating buffer sets" % R}
+
+
 def bench_path_decode_decay(torch, la, steps, peaks, src):
     """la_decode_step_decay on the decode workload (4096 heads, d = 128, fp32 state)."""
     w = workloads.DECODE_BF16
@@ -698,6 +750,7 @@ def run_gpu(args, dist):
                                                               "identity", 0.0, False)
         paths["noncausal_relu_nonorm"] = bench_path_noncausal_variant(torch, la, reps, peaks, src, "relu_nonorm",
                                                                       "relu", 0.0, False)
+        paths["backward"] = bench_path_backward(torch, la, reps, peaks, src)
         if s2:
             paths["clocks"] = s2.stop(window=(t_paths, time.time()))
 
@@ -733,7 +786,7 @@ def run_gpu(args, dist):
 
 PROFILE_CASES = ("headline", "causal_long", "causal_long_quarter", "noncausal", "decode", "prefill_state_quarter",
                  "causal_decay", "decode_decay", "prefill_state_decay_quarter", "causal_relu", "causal_retention",
-                 "noncausal_relu_nonorm")
+                 "noncausal_relu_nonorm", "backward")
 
 
 def run_profile_case(name: str, launches: int) -> int:
@@ -748,7 +801,14 @@ def run_profile_case(name: str, launches: int) -> int:
     from causal_kernelized_attention_gb300 import build as la_build
     la_build.build()
     la.load_library()
-    if name in ("causal_relu", "causal_retention"):
+    if name == "backward":
+        w = workloads.CAUSAL_BF16
+        q, k, v = workloads.device_forward_inputs(w)
+        dout = torch.randn(v.shape, device="cuda").to(torch.bfloat16)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        for _ in range(launches):
+            la.la_backward_causal(q, k, v, dout, dq, dk, dv, eps=w.eps)
+    elif name in ("causal_relu", "causal_retention"):
         w = workloads.CAUSAL_BF16
         q, k, v = workloads.device_forward_inputs(w)
         o = torch.empty_like(v)

@@ -64,6 +64,7 @@ def _declare(lib):
         "la_forward_noncausal_ex": [P, P, P, P, P, I, I, I, I, I, F, I, P],
         "la_decode_step_ex": [P, P, P, P, P, P, P, P, I, I, I, I, F, I, P],
         "la_prefill_state_ex": [P, P, P, P, P, P, I, I, I, I, I, I, P],
+        "la_backward_causal": [P, P, P, P, P, P, P, I, I, I, I, I, F, I, P],
         "la_get_device_status": [P],
     }
     for name, args in sigs.items():
@@ -385,6 +386,26 @@ def la_prefill_state_ex(k, v, S=None, z=None, gamma=None, feature_map="elu1", sh
                                             B, H, N, dk, dv, _dtype_code(k), _stream_ptr(stream))
     _check("la_prefill_state_ex", st)
     return S, z
+
+
+def la_backward_causal(q, k, v, dout, dq=None, dk=None, dv=None, eps: float = 1e-6, stream=None):
+    """Gradients (dq, dk, dv) of sum(dout * o) for the causal forward (elu + 1, normalised)."""
+    import torch
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    _need_cuda(q, k, v, dout, dq, dk, dv)
+    _same_dtype(q, k, v, dout, dq, dk, dv)
+    B, H, N, d_k = q.shape
+    d_v = v.shape[-1]
+    if tuple(k.shape) != (B, H, N, d_k) or tuple(v.shape[:-1]) != (B, H, N) or tuple(dout.shape) != tuple(v.shape) \
+            or tuple(dq.shape) != tuple(q.shape) or tuple(dk.shape) != tuple(k.shape) or tuple(dv.shape) != tuple(v.shape):
+        raise ValueError("shape mismatch")
+    st = load_library().la_backward_causal(q.data_ptr(), k.data_ptr(), v.data_ptr(), dout.data_ptr(), dq.data_ptr(),
+                                           dk.data_ptr(), dv.data_ptr(), B, H, N, d_k, d_v, float(eps),
+                                           _dtype_code(q), _stream_ptr(stream))
+    _check("la_backward_causal", st)
+    return dq, dk, dv
 
 
 def la_get_device_status(stream=None) -> int:

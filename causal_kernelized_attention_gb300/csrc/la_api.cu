@@ -354,6 +354,30 @@ la_status la_prefill_state_decay(const void *k, const void *v, const float *gamm
     return la_prefill_state_ex(k, v, gamma, nullptr, S, z, B, H, N, dk, dv, dtype, stream);
 }
 
+la_status la_backward_causal(const void *q, const void *k, const void *v, const void *dout, void *dq, void *dk,
+                             void *dv, int B, int H, int N, int d_k, int d_v, float eps, la_dtype dtype,
+                             la_stream_t stream)
+{
+    if (B < 0 || H < 0 || N < 0 || d_k < 0 || d_v < 0) return LA_ERR_INVALID_ARG;
+    if (!(eps >= 0.f) || !isfinite(eps)) return LA_ERR_INVALID_ARG;
+    if (dtype != LA_F32 && dtype != LA_BF16) return LA_ERR_INVALID_ARG;
+    if ((long long)B * H > 65535) return LA_ERR_UNSUPPORTED;
+    if (B == 0 || H == 0 || N == 0 || d_k == 0 || d_v == 0) return LA_OK;
+    if (!q || !k || !v || !dout || !dq || !dk || !dv) return LA_ERR_INVALID_ARG;
+    const void *all[7] = {q, k, v, dout, dq, dk, dv};
+    for (const void *x : all)
+        if (!aligned16(x)) return LA_ERR_MISALIGNED;
+    if (!supported_dim(d_k) || !supported_dim(d_v)) return LA_ERR_UNSUPPORTED;
+    const size_t es = elem_size(dtype);
+    const size_t nk = (size_t)B * H * N * d_k * es, nv = (size_t)B * H * N * d_v * es;
+    const size_t sizes[7] = {nk, nk, nv, nv, nk, nk, nv};
+    for (int o = 4; o < 7; ++o)  // an output overlaps no input and no other output
+        for (int x = 0; x < 7; ++x)
+            if (x != o && overlaps(all[o], sizes[o], all[x], sizes[x])) return LA_ERR_INVALID_ARG;
+    const BackwardProblem p{q, k, v, dout, dq, dk, dv, B * H, N, d_k, d_v, eps, dtype, (cudaStream_t)stream};
+    return causal_backward(p);
+}
+
 const char *la_status_string(la_status s)
 {
     switch (s) {

@@ -44,6 +44,18 @@ struct Problem {
     Variant var;
 };
 
+// Backward pass of the causal form (la_backward.cu): inputs q, k, v, dout; outputs
+// dq, dk (layout of q) and dv (layout of v); fp32 arithmetic on the CUDA cores.
+struct BackwardProblem {
+    const void *q, *k, *v, *dout;
+    void *dq, *dk, *dv;
+    int BH, N, dkd, dvd;
+    float eps;
+    la_dtype dtype;
+    cudaStream_t stream;
+};
+la_status causal_backward(const BackwardProblem &p);
+
 // SIMT kernels (la_simt.cu): fp32 CUDA-core arithmetic, any supported dtype.
 la_status causal_simt(const Problem &p);
 la_status noncausal_simt(const Problem &p);

@@ -281,6 +281,29 @@ la_status la_prefill_state_ex(const void *k, const void *v, const float *gamma,
                               const la_variant *variant, float *S, float *z, int B, int H,
                               int N, int dk, int dv, la_dtype dtype, la_stream_t stream);
 
+/*
+ * Backward pass of the causal forward (elu + 1, with the normaliser): given
+ * dout = dL/do, writes dq = dL/dq, dk = dL/dk, dv = dL/dv for L = sum dout . o.
+ * The pages give no gradient ("Linear Attention -- Math + Variants", Chunkwise
+ * parallelism: training runs the chunked form); it is the chain rule through
+ * the recurrence: a forward scan of S, z for dq and a reverse scan of
+ * R_j = sum_{i>=j} phi(q_i) dn_i^T, r_j = sum_{i>=j} dd_i phi(q_i) for dk, dv,
+ * with dn_i = dout_i / d_i, dd_i = -(dout_i . o_i) / d_i and d_i the clamped
+ * denominator (no gradient flows through the clamp where it binds).
+ *
+ *   q, k, dq, dk : [B, H, N, d_k]   v, dout, dv : [B, H, N, d_v]   (element type `dtype`)
+ *
+ * Outputs must not overlap any input or each other.  Recomputes the forward
+ * quantities it needs (no saved activations).  fp32 arithmetic on the CUDA
+ * cores, chunk-parallel (chunk states, scans over chunks, per-chunk
+ * gradients); per-call scratch of B*H*ceil(N/C)*d_k*(d_v+1) + B*H*N*(d_v+1)
+ * floats (C = 64, or 32 when d_k or d_v is 128), stream-ordered.
+ * Supported: d_k, d_v in {32, 64, 128}.
+ */
+la_status la_backward_causal(const void *q, const void *k, const void *v, const void *dout,
+                             void *dq, void *dk, void *dv, int B, int H, int N, int d_k, int d_v,
+                             float eps, la_dtype dtype, la_stream_t stream);
+
 /* Human-readable name of a status code (static string, never NULL). */
 const char *la_status_string(la_status s);
 

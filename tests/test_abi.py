@@ -37,7 +37,7 @@ def test_exports_every_declared_symbol(lib):
     assert set(names) >= {"la_forward_causal", "la_forward_noncausal", "la_decode_step",
                           "la_prefill_state", "la_forward_causal_decay", "la_decode_step_decay",
                           "la_prefill_state_decay", "la_forward_causal_ex", "la_forward_noncausal_ex",
-                          "la_decode_step_ex", "la_prefill_state_ex",
+                          "la_decode_step_ex", "la_prefill_state_ex", "la_backward_causal",
                           "la_status_string", "la_last_cuda_error",
                           "la_get_device_status", "la_version"}
     for n in names:
@@ -186,6 +186,25 @@ def test_variant_validation(lib):
     # empty problems are a no-op with any valid variant
     assert lib.la_forward_causal_ex(None, None, None, None, None, ok, 1, 2, 0, 64, 64, 128, e, 1, None) == OK
     assert lib.la_forward_noncausal_ex(None, None, None, None, ok, 0, 2, 16, 64, 64, e, 1, None) == OK
+
+
+def test_backward_validation(lib):
+    f = lib.la_backward_causal
+    e = ctypes.c_float(1e-6)
+    q, k, v, do, dq, dk, dv = (A + i * 0x100000 for i in range(7))
+
+    def call(q=q, k=k, v=v, do=do, dq=dq, dk=dk, dv=dv, B=1, H=2, N=16, d_k=64, d_v=64, eps=e, dtype=1):
+        return f(q, k, v, do, dq, dk, dv, B, H, N, d_k, d_v, eps, dtype, None)
+
+    assert call(do=None) == INVALID
+    assert call(dq=None) == INVALID
+    assert call(dk=M) == MISALIGNED
+    assert call(d_k=48) == UNSUPPORTED
+    assert call(B=-1) == INVALID
+    assert call(eps=ctypes.c_float(float("nan"))) == INVALID
+    assert call(dq=k + 64) == INVALID      # an output over an input
+    assert call(dv=dq) == INVALID          # two outputs on one buffer
+    assert call(N=0, q=None, k=None, v=None, do=None, dq=None, dk=None, dv=None) == OK
 
 
 def test_binding_raises_without_cuda_tensors():
