@@ -70,6 +70,7 @@ def _declare(lib):
         "la_oracle_noncausal_general": ([P, P, P, I, I, D, I, P, I, I, I, I, D], None),
         "la_oracle_decode_step_general": ([P, P, P, P, P, I, P, I, D, I, P, I, I, I, D], None),
         "la_oracle_causal_backward": ([P, P, P, P, I, P, P, P, I, I, I, I, D], None),
+        "la_oracle_favor_features": ([P, I, P, P, ctypes.c_longlong, I, I], None),
         "la_oracle_num_threads": ([], I),
     }
     for name, (args, res) in sigs.items():
@@ -329,6 +330,31 @@ class Oracle:
             self.lib.la_oracle_causal_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), t, _ptr(gq), _ptr(gk), _ptr(gv),
                                                BH, N, dk, dv, float(eps))
         return gq, gk, gv
+
+    # ---------------------------------------------------------------- FAVOR+ features
+    def favor_features(self, x, W):
+        """phi(x)_r = exp(w_r . x - |x|^2 / 2) / sqrt(m) for x [..., d], W [m, d]; returns [..., m]."""
+        (x,), t = _prep(x)
+        W = np.ascontiguousarray(W, dtype=np.float64)
+        m, d = W.shape
+        if x.shape[-1] != d:
+            raise ValueError("shape mismatch")
+        rows = int(np.prod(x.shape[:-1])) if x.ndim > 1 else 1
+        out = np.empty(x.shape[:-1] + (m,), dtype=np.float64)
+        if rows:
+            self.lib.la_oracle_favor_features(_ptr(x), t, _ptr(W), _ptr(out), rows, d, m)
+        return out
+
+    def causal_favor(self, q, k, v, W, eps=1e-6):
+        """Causal linear attention on FAVOR+ features (the identity map on phi(q), phi(k))."""
+        return self.causal_general(self.favor_features(q, W), self.favor_features(k, W), np.asarray(v, np.float64)
+                                   if np.asarray(v).dtype != np.uint16 else _widen_bf16(v), fmap="identity",
+                                   shift=0.0, normalize=True, eps=eps)
+
+
+def _widen_bf16(bits):
+    b = np.ascontiguousarray(bits, dtype=np.uint16).astype(np.uint32) << 16
+    return b.view(np.float32).astype(np.float64)
 
 
 _default = None

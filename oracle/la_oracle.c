@@ -810,6 +810,31 @@ void la_oracle_causal_backward(const void *q, const void *k, const void *v, cons
     }
 }
 
+/* ---------------------------------------------------------------------------
+ * Performer FAVOR+ positive random features ("Linear Attention -- Math +
+ * Variants", Performer: unbiased softmax by positive random features):
+ *   phi(x)_r = exp(w_r . x - |x|^2 / 2) / sqrt(m),  r = 0 .. m-1,
+ * with E[phi(q) . phi(k)] = exp(q . k) for w_r ~ N(0, I).  x [rows, d] (any input
+ * type), W [m, d] double (the random features are an input), out [rows, m] double.
+ * ------------------------------------------------------------------------- */
+void la_oracle_favor_features(const void *x, int type, const double *W, double *out, long long rows, int d, int m)
+{
+#pragma omp parallel for schedule(static)
+    for (long long i = 0; i < rows; ++i) {
+        double nrm = 0.0;
+        for (int c = 0; c < d; ++c) {
+            const double xc = load(x, type, i * d + c);
+            nrm += xc * xc;
+        }
+        for (int r = 0; r < m; ++r) {
+            double dot = 0.0;
+            for (int c = 0; c < d; ++c)
+                dot += W[(size_t)r * d + c] * load(x, type, i * d + c);
+            out[i * m + r] = exp(dot - 0.5 * nrm) / sqrt((double)m);
+        }
+    }
+}
+
 /* Threads OpenMP will use (reported beside CPU timings). */
 int la_oracle_num_threads(void)
 {

@@ -594,4 +594,47 @@ def pin_backward_linear_in_dout(orc):
         assert _rel_err(x, 2.0 * y1 - 3.0 * y2) < 1e-12
 
 
+# ----------------------------------------------------------------------------
+# Performer FAVOR+ features ("Linear Attention -- Math + Variants", Performer):
+# phi(x)_r = exp(w_r . x - |x|^2 / 2) / sqrt(m), E[phi(q) . phi(k)] = exp(q . k)
+# ----------------------------------------------------------------------------
+def pin_favor_unbiased_estimate(orc):
+    """With m = 40000 Gaussian w_r the estimate phi(q) . phi(k) is within 5 standard
+    errors of exp(q . k) (the standard error estimated from the same samples)."""
+    rng = np.random.default_rng(4000)
+    d, m = 8, 40000
+    W = rng.standard_normal((m, d))
+    for _ in range(3):
+        q, k = rng.standard_normal(d) * 0.4, rng.standard_normal(d) * 0.4
+        fq, fk = orc.favor_features(q[None], W)[0], orc.favor_features(k[None], W)[0]
+        terms = fq * fk * m  # each term's mean is exp(q . k)
+        est, se = terms.mean(), terms.std() / np.sqrt(m)
+        assert abs(est - math.exp(float(q @ k))) < 5 * se, (est, math.exp(float(q @ k)), se)
+
+
+def pin_favor_zero_projection(orc):
+    """W = 0: every feature is exp(-|x|^2 / 2) / sqrt(m)."""
+    x = np.array([[0.5, -1.0, 2.0], [0.0, 0.0, 0.0]])
+    out = orc.favor_features(x, np.zeros((4, 3)))
+    ref = np.exp(-0.5 * (x ** 2).sum(-1))[:, None] / 2.0 * np.ones((1, 4))
+    assert _rel_err(out, ref) < 1e-15
+
+
+def pin_favor_unit_projection(orc):
+    """m = 1, w = e_1: phi(x) = exp(x_1 - |x|^2 / 2), with the library's exp."""
+    x = np.array([[0.3, -0.2, 0.7, 1.1]])
+    got = orc.favor_features(x, np.array([[1.0, 0.0, 0.0, 0.0]]))[0, 0]
+    assert abs(got - math.exp(0.3 - 0.5 * (0.09 + 0.04 + 0.49 + 1.21))) < 1e-15
+
+
+def pin_favor_positive_and_scale(orc):
+    """Features are positive, and scaling m by 4 with repeated rows divides each by 2."""
+    rng = np.random.default_rng(4010)
+    x = rng.standard_normal((5, 6))
+    W = rng.standard_normal((3, 6))
+    a = orc.favor_features(x, W)
+    b = orc.favor_features(x, np.tile(W, (4, 1)))
+    assert np.all(a > 0) and _rel_err(b[:, :3], a / 2.0) < 1e-15
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -66,6 +66,10 @@ MUTANTS = {
     "backward_phi_prime_constant": ("    return x > 0.0 ? 1.0 : exp(x);", "    return 1.0;"),
     "backward_dv_from_q": ("s += R[(size_t)r * dvd + c] * fk[r];", "s += R[(size_t)r * dvd + c] * fq[r];"),
     "backward_dq_sign": ("double s = dd[t] * z[r];", "double s = -dd[t] * z[r];"),
+    # FAVOR+ features
+    "favor_drops_norm_term": ("out[i * m + r] = exp(dot - 0.5 * nrm) / sqrt((double)m);", "out[i * m + r] = exp(dot) / sqrt((double)m);"),
+    "favor_norm_sign": ("out[i * m + r] = exp(dot - 0.5 * nrm) / sqrt((double)m);", "out[i * m + r] = exp(dot + 0.5 * nrm) / sqrt((double)m);"),
+    "favor_no_sqrt_m": ("out[i * m + r] = exp(dot - 0.5 * nrm) / sqrt((double)m);", "out[i * m + r] = exp(dot - 0.5 * nrm) / (double)m;"),
 }
 
 
