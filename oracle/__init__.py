@@ -352,6 +352,12 @@ class Oracle:
                                    shift=0.0, normalize=True, eps=eps)
 
 
+    def noncausal_favor(self, q, k, v, W, eps=1e-6):
+        """Non-causal linear attention on FAVOR+ features (the identity map on phi(q), phi(k))."""
+        return self.noncausal_general(self.favor_features(q, W), self.favor_features(k, W),
+                                      np.asarray(v, np.float64) if np.asarray(v).dtype != np.uint16
+                                      else _widen_bf16(v), fmap="identity", shift=0.0, normalize=True, eps=eps)
+
 def _widen_bf16(bits):
     b = np.ascontiguousarray(bits, dtype=np.uint16).astype(np.uint32) << 16
     return b.view(np.float32).astype(np.float64)

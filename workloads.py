@@ -133,6 +133,29 @@ def random_inputs(seed: int, B: int, H: int, N: int, dk: int, dv: int,
     return draw_qkv(seed, (B, H, N, dk), (B, H, N, dv), sigma, dtype)
 
 
+def favor_projection(seed: int, m: int, d: int, dtype: str = "f32", orthogonal: bool = True) -> np.ndarray:
+    """Random projections W [m, d] for FAVOR+ features (an input to both sides).
+
+    The Performer draw ("Linear Attention -- Math + Variants", Performer: Gaussian
+    rows w_r, made orthogonal to reduce the estimator's variance): blocks of d
+    Gaussian rows orthonormalised by a QR factorisation, each row then scaled to
+    the length of an independent Gaussian d-vector, so that every row keeps the
+    N(0, I) marginal; ceil(m / d) blocks, the first m rows kept.  With
+    orthogonal=False the rows are plain N(0, I) draws.  float32, or bf16 bit
+    patterns for dtype "bf16" (the rounded values are what both sides use).
+    """
+    rng = np.random.default_rng(seed)
+    if not orthogonal:
+        return _finish(rng.standard_normal((m, d)).astype(np.float32), dtype)
+    blocks = []
+    for _ in range((m + d - 1) // d):
+        g = rng.standard_normal((d, d))
+        qm, _ = np.linalg.qr(g)
+        lengths = np.linalg.norm(rng.standard_normal((d, d)), axis=1)
+        blocks.append(qm.T * lengths[:, None])
+    return _finish(np.concatenate(blocks, axis=0)[:m].astype(np.float32), dtype)
+
+
 class DecodeInputs:
     """Decode workload: a causal prefill of ``w.N`` tokens, then ``w.steps`` steps.
 
