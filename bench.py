@@ -622,6 +622,93 @@ def bench_path_backward(torch, la, reps, peaks, src):
             "l2": "%d rotating buffer sets" % R}
 
 
+FAVOR_SIGMA = 0.5  # inputs of the FAVOR+ paths: N(0, 0.25), about the Performer's d^(-1/4) input scale at d = 64
+
+
+def favor_flops(rows, d, m):
+    """Projection flop of FAVOR+ features for `rows` input rows (2 per MAC)."""
+    return 2.0 * rows * d * m
+
+
+def bench_path_causal_favor(torch, la, reps, peaks, src):
+    """la_forward_causal_favor on the headline causal shape (B=4 H=8 N=2048 d=64, chunk 128,
+    bf16) with m = 64 orthogonal random features: features of q and k (one launch), then the
+    causal forward on them.  Algorithmic bytes: q, k, v, w read and o written once (the
+    features' round trip through HBM is this design's, not the method's)."""
+    w = workloads.CAUSAL_BF16
+    m = 64
+    q, k, v = workloads.random_inputs(w.seed, w.B, w.H, w.N, w.dk, w.dv, "bf16", sigma=FAVOR_SIGMA)
+    wp = dev_copy(torch, workloads.favor_projection(w.seed + 1, m, w.dk, "bf16"), "bf16")
+    nbytes = forward_bytes(w.BH, w.N, w.dk, w.dv, 2) + m * w.dk * 2
+    R = n_rotations(nbytes + 2 * w.BH * w.N * m * 2)
+    base = [dev_copy(torch, x, "bf16") for x in (q, k, v)]
+    sets = [[t.clone() for t in base] + [torch.empty_like(base[2])] for _ in range(R)]
+
+    def step(i):
+        s = sets[i % R]
+        la.la_forward_causal_favor(s[0], s[1], s[2], wp, s[3], chunk=w.chunk, eps=w.eps)
+
+    secs, launches, _ = time_graph_steps(torch, la, step, reps, 3, Dist())
+    t = secs / reps
+    fl = favor_flops(2 * w.BH * w.N, w.dk, m) + causal_flops(w.BH, w.N, m, w.dv, w.chunk)
+    return {"workload": w.name + "_favor_m%d" % m, "value": round(w.B * w.N / t, 1), "unit": "tokens/s",
+            "ms_per_step": round(t * 1e3, 4), "launches_per_step": launches / reps, "m": m,
+            "sigma": FAVOR_SIGMA,
+            "roofline": roofline(fl, nbytes, t, peaks, src, None),
+            "l2": "%d rotating buffer sets" % R}
+
+
+def bench_path_favor_features(torch, la, reps, peaks, src):
+    """la_favor_features alone over the rows of the headline shape's q and k together
+    (x [8, 8, 2048, 64] bf16, m = 64): read x and w, write phi once."""
+    w = workloads.CAUSAL_BF16
+    m = 64
+    x = workloads.random_inputs(w.seed, 2 * w.B, w.H, w.N, w.dk, w.dv, "bf16", sigma=FAVOR_SIGMA)[0]
+    wp = dev_copy(torch, workloads.favor_projection(w.seed + 1, m, w.dk, "bf16"), "bf16")
+    rows = 2 * w.BH * w.N
+    nbytes = rows * (w.dk + m) * 2 + m * w.dk * 2
+    R = n_rotations(nbytes)
+    base = dev_copy(torch, x, "bf16")
+    sets = [(base.clone(), torch.empty(base.shape[:-1] + (m,), dtype=base.dtype, device=base.device))
+            for _ in range(R)]
+
+    def step(i):
+        s = sets[i % R]
+        la.la_favor_features(s[0], wp, s[1])
+
+    secs, launches, _ = time_graph_steps(torch, la, step, reps, 3, Dist())
+    t = secs / reps
+    return {"workload": "favor_features_rows%d_d%d_m%d" % (rows, w.dk, m), "value": round(rows / t, 1),
+            "unit": "rows/s", "ms_per_step": round(t * 1e3, 4), "launches_per_step": launches / reps,
+            "roofline": roofline(favor_flops(rows, w.dk, m), nbytes, t, peaks, src, ncu_traffic("favor_features")),
+            "l2": "%d rotating buffer sets" % R}
+
+
+def bench_path_noncausal_favor(torch, la, reps, peaks, src):
+    """la_forward_noncausal_favor on the non-causal workload (B=8 H=12 N=4096 d=64, bf16), m = 64."""
+    w = workloads.NONCAUSAL_BF16
+    m = 64
+    q, k, v = workloads.random_inputs(w.seed, w.B, w.H, w.N, w.dk, w.dv, "bf16", sigma=FAVOR_SIGMA)
+    wp = dev_copy(torch, workloads.favor_projection(w.seed + 1, m, w.dk, "bf16"), "bf16")
+    nbytes = forward_bytes(w.BH, w.N, w.dk, w.dv, 2) + m * w.dk * 2
+    R = n_rotations(nbytes + 2 * w.BH * w.N * m * 2)
+    base = [dev_copy(torch, x, "bf16") for x in (q, k, v)]
+    sets = [[t.clone() for t in base] + [torch.empty_like(base[2])] for _ in range(R)]
+
+    def step(i):
+        s = sets[i % R]
+        la.la_forward_noncausal_favor(s[0], s[1], s[2], wp, s[3], eps=w.eps)
+
+    secs, launches, _ = time_graph_steps(torch, la, step, reps, 3, Dist())
+    t = secs / reps
+    fl = favor_flops(2 * w.BH * w.N, w.dk, m) + noncausal_flops(w.BH, w.N, m, w.dv)
+    return {"workload": w.name + "_favor_m%d" % m, "value": round(w.B * w.N / t, 1), "unit": "tokens/s",
+            "ms_per_step": round(t * 1e3, 4), "launches_per_step": launches / reps, "m": m,
+            "sigma": FAVOR_SIGMA,
+            "roofline": roofline(fl, nbytes, t, peaks, src, None),
+            "l2": "%d rotating buffer sets" % R}
+
+
 def bench_path_decode_decay(torch, la, steps, peaks, src):
     """la_decode_step_decay on the decode workload (4096 heads, d = 128, fp32 state)."""
     w = workloads.DECODE_BF16
@@ -751,6 +838,9 @@ def run_gpu(args, dist):
         paths["noncausal_relu_nonorm"] = bench_path_noncausal_variant(torch, la, reps, peaks, src, "relu_nonorm",
                                                                       "relu", 0.0, False)
         paths["backward"] = bench_path_backward(torch, la, reps, peaks, src)
+        paths["favor_features"] = bench_path_favor_features(torch, la, reps, peaks, src)
+        paths["causal_favor"] = bench_path_causal_favor(torch, la, reps, peaks, src)
+        paths["noncausal_favor"] = bench_path_noncausal_favor(torch, la, reps, peaks, src)
         if s2:
             paths["clocks"] = s2.stop(window=(t_paths, time.time()))
 
@@ -786,7 +876,7 @@ def run_gpu(args, dist):
 
 PROFILE_CASES = ("headline", "causal_long", "causal_long_quarter", "noncausal", "decode", "prefill_state_quarter",
                  "causal_decay", "decode_decay", "prefill_state_decay_quarter", "causal_relu", "causal_retention",
-                 "noncausal_relu_nonorm", "backward")
+                 "noncausal_relu_nonorm", "backward", "favor_features", "causal_favor")
 
 
 def run_profile_case(name: str, launches: int) -> int:
@@ -801,7 +891,25 @@ def run_profile_case(name: str, launches: int) -> int:
     from causal_kernelized_attention_gb300 import build as la_build
     la_build.build()
     la.load_library()
-    if name == "backward":
+    if name in ("favor_features", "causal_favor"):
+        # favor_features: x [64, 8, 2048, 64] bf16 (268 MB of x and phi, above L2), m = 64;
+        # causal_favor: the headline causal shape through la_forward_causal_favor, m = 64
+        w = workloads.CAUSAL_BF16
+        g = torch.Generator(device="cuda").manual_seed(w.seed)
+        wp = torch.from_numpy(workloads.favor_projection(w.seed + 1, 64, w.dk, "bf16").view(np.int16)).cuda()
+        wp = wp.view(torch.bfloat16)
+        if name == "favor_features":
+            x = (torch.randn((64, w.H, w.N, w.dk), generator=g, device="cuda") * 0.5).to(torch.bfloat16)
+            phi = torch.empty((64, w.H, w.N, 64), dtype=torch.bfloat16, device="cuda")
+            for _ in range(launches):
+                la.la_favor_features(x, wp, phi)
+        else:
+            q, k, v = ((torch.randn((w.B, w.H, w.N, w.dk), generator=g, device="cuda") * 0.5).to(torch.bfloat16)
+                       for _ in range(3))
+            o = torch.empty_like(v)
+            for _ in range(launches):
+                la.la_forward_causal_favor(q, k, v, wp, o, chunk=w.chunk, eps=w.eps)
+    elif name == "backward":
         w = workloads.CAUSAL_BF16
         q, k, v = workloads.device_forward_inputs(w)
         dout = torch.randn(v.shape, device="cuda").to(torch.bfloat16)

@@ -65,6 +65,9 @@ def _declare(lib):
         "la_decode_step_ex": [P, P, P, P, P, P, P, P, I, I, I, I, F, I, P],
         "la_prefill_state_ex": [P, P, P, P, P, P, I, I, I, I, I, I, P],
         "la_backward_causal": [P, P, P, P, P, P, P, I, I, I, I, I, F, I, P],
+        "la_favor_features": [P, P, P, I, I, I, I, I, I, P],
+        "la_forward_causal_favor": [P, P, P, P, P, I, I, I, I, I, I, I, F, I, P],
+        "la_forward_noncausal_favor": [P, P, P, P, P, I, I, I, I, I, I, F, I, P],
         "la_get_device_status": [P],
     }
     for name, args in sigs.items():
@@ -406,6 +409,67 @@ def la_backward_causal(q, k, v, dout, dq=None, dk=None, dv=None, eps: float = 1e
                                            _dtype_code(q), _stream_ptr(stream))
     _check("la_backward_causal", st)
     return dq, dk, dv
+
+
+def _favor_w(w, x, d):
+    _need_cuda(w)
+    if w.dim() != 2 or w.shape[1] != d or w.dtype != x.dtype:
+        raise ValueError("w must be [m, d] with the dtype of the inputs")
+    return w.shape[0]
+
+
+def la_favor_features(x, w, phi=None, stream=None):
+    """FAVOR+ features phi(x)_r = exp(w_r . x - |x|^2 / 2) / sqrt(m); x [B,H,N,d], w [m,d];
+    returns phi [B,H,N,m] in the dtype of x."""
+    import torch
+    B, H, N, d = x.shape
+    m = _favor_w(w, x, d)
+    if phi is None:
+        phi = torch.empty((B, H, N, m), dtype=x.dtype, device=x.device)
+    _need_cuda(x, phi)
+    _same_dtype(x, w, phi)
+    if tuple(phi.shape) != (B, H, N, m):
+        raise ValueError("shape mismatch")
+    st = load_library().la_favor_features(x.data_ptr(), w.data_ptr(), phi.data_ptr(), B, H, N, d, m,
+                                          _dtype_code(x), _stream_ptr(stream))
+    _check("la_favor_features", st)
+    return phi
+
+
+def _favor_shapes(q, k, v, o, w):
+    _need_cuda(q, k, v, o)
+    _same_dtype(q, k, v, o)
+    B, H, N, d = q.shape
+    dv = v.shape[-1]
+    if tuple(k.shape) != (B, H, N, d) or tuple(v.shape[:-1]) != (B, H, N) or tuple(o.shape) != (B, H, N, dv):
+        raise ValueError("shape mismatch")
+    return B, H, N, d, dv, _favor_w(w, q, d)
+
+
+def la_forward_causal_favor(q, k, v, w, o=None, chunk: int = 128, eps: float = 1e-6, stream=None):
+    """Causal linear attention on FAVOR+ features of q and k (projections w [m, d])."""
+    import torch
+    if o is None:
+        o = torch.empty(q.shape[:-1] + (v.shape[-1],), dtype=q.dtype, device=q.device)
+    B, H, N, d, dv, m = _favor_shapes(q, k, v, o, w)
+    st = load_library().la_forward_causal_favor(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                                w.data_ptr(), B, H, N, d, dv, m, int(chunk), float(eps),
+                                                _dtype_code(q), _stream_ptr(stream))
+    _check("la_forward_causal_favor", st)
+    return o
+
+
+def la_forward_noncausal_favor(q, k, v, w, o=None, eps: float = 1e-6, stream=None):
+    """Non-causal linear attention on FAVOR+ features of q and k (projections w [m, d])."""
+    import torch
+    if o is None:
+        o = torch.empty(q.shape[:-1] + (v.shape[-1],), dtype=q.dtype, device=q.device)
+    B, H, N, d, dv, m = _favor_shapes(q, k, v, o, w)
+    st = load_library().la_forward_noncausal_favor(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                                   w.data_ptr(), B, H, N, d, dv, m, float(eps), _dtype_code(q),
+                                                   _stream_ptr(stream))
+    _check("la_forward_noncausal_favor", st)
+    return o
 
 
 def la_get_device_status(stream=None) -> int:

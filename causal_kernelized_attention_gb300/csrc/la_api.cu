@@ -378,6 +378,93 @@ la_status la_backward_causal(const void *q, const void *k, const void *v, const 
     return causal_backward(p);
 }
 
+la_status la_favor_features(const void *x, const void *w, void *phi, int B, int H, int N, int d, int m,
+                            la_dtype dtype, la_stream_t stream)
+{
+    if (B < 0 || H < 0 || N < 0 || d < 0 || m < 0) return LA_ERR_INVALID_ARG;
+    if (dtype != LA_F32 && dtype != LA_BF16) return LA_ERR_INVALID_ARG;
+    if ((long long)B * H > 65535) return LA_ERR_UNSUPPORTED;
+    if (B == 0 || H == 0 || N == 0 || d == 0 || m == 0) return LA_OK;
+    if (!x || !w || !phi) return LA_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(w) || !aligned16(phi)) return LA_ERR_MISALIGNED;
+    if (!supported_dim(d) || !supported_dim(m)) return LA_ERR_UNSUPPORTED;
+    const size_t es = elem_size(dtype), rows = (size_t)B * H * N;
+    if (overlaps(phi, rows * m * es, x, rows * d * es) || overlaps(phi, rows * m * es, w, (size_t)m * d * es))
+        return LA_ERR_INVALID_ARG;
+    return favor_features(x, nullptr, w, phi, nullptr, B * H, N, d, m, dtype, (cudaStream_t)stream);
+}
+
+// Shared steps of the FAVOR+ forwards: checks, then phi(q) and phi(k) into
+// stream-ordered scratch (*fq, *fk; [B, H, N, m] each, freed with *s).
+static la_status favor_prologue(const void *q, const void *k, const void *v, const void *o, const void *w, int B,
+                                int H, int N, int d, int dv, int m, float eps, la_dtype dtype, cudaStream_t stream,
+                                Scratch *s, void **fq, void **fk, bool *empty)
+{
+    if (m < 0) return LA_ERR_INVALID_ARG;
+    la_status st = check_forward(q, k, v, o, B, H, N, d, dv, eps, dtype, empty);
+    if (st != LA_OK || *empty) return st;
+    if (!w) return LA_ERR_INVALID_ARG;
+    if (!aligned16(w)) return LA_ERR_MISALIGNED;
+    if (!supported_dim(d) || !supported_dim(dv) || !supported_dim(m)) return LA_ERR_UNSUPPORTED;
+    const size_t es = elem_size(dtype);
+    if (overlaps(o, (size_t)B * H * N * dv * es, w, (size_t)m * d * es)) return LA_ERR_INVALID_ARG;
+    const size_t bytes = (size_t)B * H * N * m * es;  // a multiple of 64: both halves stay 16-byte aligned
+    if ((st = s->alloc(2 * bytes, stream)) != LA_OK) return st;
+    *fq = s->ptr;
+    *fk = (char *)s->ptr + bytes;
+    return favor_features(q, k, w, *fq, *fk, B * H, N, d, m, dtype, stream);
+}
+
+// The attention half of the FAVOR+ forwards: phi is already applied, so the
+// feature map is the identity (shift 0), with the normaliser.
+static Variant favor_attention_variant()
+{
+    Variant v;
+    v.map = LA_PHI_IDENTITY;
+    v.shift = 0.f;
+    v.normalize = 1;
+    return v;
+}
+
+la_status la_forward_causal_favor(const void *q, const void *k, const void *v, void *o, const void *w, int B, int H,
+                                  int N, int d, int dv, int m, int chunk, float eps, la_dtype dtype,
+                                  la_stream_t stream)
+{
+    if (chunk != 64 && chunk != 128) return LA_ERR_UNSUPPORTED;
+    Scratch s;
+    void *fq = nullptr, *fk = nullptr;
+    bool empty;
+    la_status st = favor_prologue(q, k, v, o, w, B, H, N, d, dv, m, eps, dtype, (cudaStream_t)stream, &s, &fq, &fk,
+                                  &empty);
+    if (st != LA_OK || empty) return st;
+    Problem p{fq, fk, v, o, B * H, N, m, dv, chunk, eps, dtype, (cudaStream_t)stream, nullptr, H,
+              favor_attention_variant()};
+    if (dtype == LA_BF16) {
+        st = causal_tc(p);
+        if (st != LA_ERR_UNSUPPORTED) return st;
+    }
+    return causal_simt(p);
+}
+
+la_status la_forward_noncausal_favor(const void *q, const void *k, const void *v, void *o, const void *w, int B,
+                                     int H, int N, int d, int dv, int m, float eps, la_dtype dtype,
+                                     la_stream_t stream)
+{
+    Scratch s;
+    void *fq = nullptr, *fk = nullptr;
+    bool empty;
+    la_status st = favor_prologue(q, k, v, o, w, B, H, N, d, dv, m, eps, dtype, (cudaStream_t)stream, &s, &fq, &fk,
+                                  &empty);
+    if (st != LA_OK || empty) return st;
+    Problem p{fq, fk, v, o, B * H, N, m, dv, 0, eps, dtype, (cudaStream_t)stream, nullptr, H,
+              favor_attention_variant()};
+    if (dtype == LA_BF16) {
+        st = noncausal_tc(p);
+        if (st != LA_ERR_UNSUPPORTED) return st;
+    }
+    return noncausal_simt(p);
+}
+
 const char *la_status_string(la_status s)
 {
     switch (s) {
@@ -397,12 +484,14 @@ la_status la_get_device_status(la_stream_t stream)
 {
     la_status st = cuda_status(cudaStreamSynchronize((cudaStream_t)stream));
     if (st != LA_OK) return st;
-    unsigned bits = 0, nc_bits = 0;
+    unsigned bits = 0, nc_bits = 0, fv_bits = 0;
     st = tc_causal_read_status((cudaStream_t)stream, &bits);
     if (st != LA_OK) return st;
     st = tc_noncausal_read_status((cudaStream_t)stream, &nc_bits);
     if (st != LA_OK) return st;
-    return ((bits | nc_bits) & kStatusTimeout) ? LA_ERR_TIMEOUT : LA_OK;
+    st = favor_read_status((cudaStream_t)stream, &fv_bits);
+    if (st != LA_OK) return st;
+    return ((bits | nc_bits | fv_bits) & kStatusTimeout) ? LA_ERR_TIMEOUT : LA_OK;
 }
 
 int la_version(void) { return 100; }

@@ -89,6 +89,15 @@ la_status noncausal_tc_state(const void *k, const void *v, float *S, float *z, i
 // Device status words of translation units that run bounded waits: read and clear.
 la_status tc_causal_read_status(cudaStream_t s, unsigned *bits);
 la_status tc_noncausal_read_status(cudaStream_t s, unsigned *bits);
+la_status favor_read_status(cudaStream_t s, unsigned *bits);
+
+// FAVOR+ features (la_favor.cu): oq = phi(xq) and, when xk is not null, ok =
+// phi(xk), with phi(x)_r = exp(w_r . x - |x|^2 / 2) / sqrt(m); x [BH, N, d],
+// W [m, d] and the outputs [BH, N, m], all of element type dtype.  bf16 with d,
+// m in {64, 128} and N >= 128 on the tensor cores, everything else on the CUDA
+// cores in fp32.
+la_status favor_features(const void *xq, const void *xk, const void *W, void *oq, void *ok, int BH, int N, int d,
+                         int m, la_dtype dtype, cudaStream_t stream);
 
 bool supported_dim(int d);
 

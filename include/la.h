@@ -304,6 +304,48 @@ la_status la_backward_causal(const void *q, const void *k, const void *v, const 
                              void *dq, void *dk, void *dv, int B, int H, int N, int d_k, int d_v,
                              float eps, la_dtype dtype, la_stream_t stream);
 
+/*
+ * FAVOR+ positive random features ("Linear Attention -- Math + Variants",
+ * Performer: features whose inner products estimate the softmax kernel,
+ * E[phi(q) . phi(k)] = exp(q . k) over Gaussian projections w_r):
+ *
+ *   phi(x)_r = exp(w_r . x - |x|^2 / 2) / sqrt(m),   r = 0 .. m-1
+ *
+ *   x : [B, H, N, d]   w : [m, d] (row r is w_r)   phi : [B, H, N, m]
+ *
+ * All three of element type `dtype`.  The projections are the caller's: plain
+ * Gaussian rows, or orthogonal blocks rescaled to Gaussian norms (the page's
+ * variance reduction) -- the library only applies them.  No 1/sqrt(d) or other
+ * scaling is applied to x.  phi must not overlap x or w.  Supported: d, m in
+ * {32, 64, 128}.  bf16 with d, m in {64, 128} and N >= 128 runs on the tensor cores (x w^T
+ * accumulated in fp32, the exponential in fp32, phi rounded to bf16 once);
+ * other shapes and fp32 on the CUDA cores in fp32.  m = 0 is an empty output.
+ */
+la_status la_favor_features(const void *x, const void *w, void *phi, int B, int H, int N, int d, int m,
+                            la_dtype dtype, la_stream_t stream);
+
+/*
+ * Causal and non-causal linear attention on FAVOR+ features (same page): the
+ * forwards of la_forward_causal / la_forward_noncausal with phi(q), phi(k) of
+ * la_favor_features in place of elu + 1, normalised by max(phi(q)^T z, eps):
+ *
+ *   q, k : [B, H, N, d]   v, o : [B, H, N, dv]   w : [m, d]   (element type `dtype`)
+ *
+ * The state has m rows (S is m x dv).  phi(q) and phi(k) are written to
+ * per-call stream-ordered scratch (2 * B*H*N*m elements of `dtype`) and then
+ * attended with the identity map, so each call is two launches or more.
+ * w must not overlap o.  Supported: d, dv, m in {32, 64, 128}; the attention
+ * step runs on the tensor cores for bf16 with m = dv in {64, 128} (and, causal,
+ * chunk 128 and N >= 128), on the CUDA cores otherwise.  m outside the
+ * supported set (0 included) gives LA_ERR_UNSUPPORTED.
+ */
+la_status la_forward_causal_favor(const void *q, const void *k, const void *v, void *o, const void *w, int B,
+                                  int H, int N, int d, int dv, int m, int chunk, float eps, la_dtype dtype,
+                                  la_stream_t stream);
+la_status la_forward_noncausal_favor(const void *q, const void *k, const void *v, void *o, const void *w, int B,
+                                     int H, int N, int d, int dv, int m, float eps, la_dtype dtype,
+                                     la_stream_t stream);
+
 /* Human-readable name of a status code (static string, never NULL). */
 const char *la_status_string(la_status s);
 

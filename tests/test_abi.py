@@ -207,6 +207,38 @@ def test_backward_validation(lib):
     assert call(N=0, q=None, k=None, v=None, do=None, dq=None, dk=None, dv=None) == OK
 
 
+def test_favor_validation(lib):
+    e = ctypes.c_float(1e-6)
+    x, w, phi = A, A + 0x100000, A + 0x200000
+    ff = lib.la_favor_features
+    assert ff(None, w, phi, 1, 2, 16, 64, 64, 1, None) == INVALID
+    assert ff(x, None, phi, 1, 2, 16, 64, 64, 1, None) == INVALID
+    assert ff(x, w, M, 1, 2, 16, 64, 64, 1, None) == MISALIGNED
+    assert ff(x, w, phi, 1, 2, 16, 48, 64, 1, None) == UNSUPPORTED
+    assert ff(x, w, phi, 1, 2, 16, 64, 256, 1, None) == UNSUPPORTED
+    assert ff(x, w, phi, 1, 2, 16, 64, -1, 1, None) == INVALID
+    assert ff(x, w, phi, 1, 2, 16, 64, 64, 5, None) == INVALID
+    assert ff(x, w, x + 64, 1, 2, 16, 64, 64, 1, None) == INVALID    # phi over x
+    assert ff(x, w, w - 64, 1, 2, 16, 64, 64, 1, None) == INVALID    # phi over w
+    assert ff(None, None, None, 1, 2, 0, 64, 64, 1, None) == OK     # empty
+    assert ff(None, None, None, 1, 2, 16, 64, 0, 1, None) == OK     # no features
+    q, k, v, o, w = (A + i * 0x100000 for i in range(5))
+    fc, fn = lib.la_forward_causal_favor, lib.la_forward_noncausal_favor
+    assert fc(q, k, v, o, None, 1, 2, 16, 64, 64, 64, 128, e, 1, None) == INVALID
+    assert fc(q, k, v, o, M, 1, 2, 16, 64, 64, 64, 128, e, 1, None) == MISALIGNED
+    assert fc(q, k, v, o, w, 1, 2, 16, 64, 64, 48, 128, e, 1, None) == UNSUPPORTED
+    assert fc(q, k, v, o, w, 1, 2, 16, 64, 64, 0, 128, e, 1, None) == UNSUPPORTED
+    assert fc(q, k, v, o, w, 1, 2, 16, 64, 64, -2, 128, e, 1, None) == INVALID
+    assert fc(q, k, v, o, w, 1, 2, 16, 64, 64, 64, 96, e, 1, None) == UNSUPPORTED
+    assert fc(q, k, v, o, o + 64, 1, 2, 16, 64, 64, 64, 128, e, 1, None) == INVALID   # w over o
+    assert fc(q, k, v, o, w, 1, 2, 16, 64, 64, 64, 128, ctypes.c_float(-1.0), 1, None) == INVALID
+    assert fc(None, None, None, None, None, 1, 2, 0, 64, 64, 64, 128, e, 1, None) == OK
+    assert fn(q, k, v, o, None, 1, 2, 16, 64, 64, 64, e, 1, None) == INVALID
+    assert fn(q, k, v, o, w, 1, 2, 16, 64, 32, 256, e, 1, None) == UNSUPPORTED
+    assert fn(q, k, v, q + 64, w, 1, 2, 16, 64, 64, 64, e, 1, None) == INVALID      # o over q
+    assert fn(None, None, None, None, None, 0, 2, 16, 64, 64, 64, e, 1, None) == OK
+
+
 def test_binding_raises_without_cuda_tensors():
     torch = pytest.importorskip("torch")
     q = torch.zeros(1, 1, 4, 64)
