@@ -348,7 +348,10 @@ la_status launch_simt(const void *xq, const void *xk, const void *W, void *oq, v
                       int m, cudaStream_t stream)
 {
     const int smem = (int)sizeof(float) * (m * (d + 1) + kSimtRows * d + kSimtRows);
-    la_status st = ensure_smem((const void *)favor_simt_kernel<T>, smem);
+    // The attribute is set once, to the size of the largest shape (d = m = 128), so
+    // that launches of every size fit it whatever order they come in.
+    constexpr int kMaxSmem = (int)sizeof(float) * (128 * 129 + kSimtRows * 128 + kSimtRows);
+    la_status st = ensure_smem((const void *)favor_simt_kernel<T>, kMaxSmem);
     if (st != LA_OK) return st;
     const int tensors = xk ? 2 : 1;
     const long long total = (rows + kSimtRows - 1) / kSimtRows * tensors;
