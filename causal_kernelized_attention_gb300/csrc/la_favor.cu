@@ -5,11 +5,13 @@
 // blocks or plain Gaussian rows alike).
 //
 // x W^T is a dense contraction, so for bf16 with d, m in {64, 128} it runs on
-// the tensor cores: a persistent kernel with W resident in shared memory, 128-row
-// tiles of x brought in by TMA, one tcgen05.mma group per tile into a TMEM
-// accumulator (two buffers), and an epilogue that adds the norm term, takes the
-// exponential with the 1/sqrt(m) scale folded into its exponent and stores bf16
-// rows by TMA.  Other shapes and fp32 run on the CUDA cores in fp32.
+// the tensor cores: a persistent kernel with W resident in shared memory (loaded
+// by TMA with the first tile), 128-row tiles of x brought in by TMA, one
+// tcgen05.mma group per tile into a TMEM accumulator (two buffers), and two sets
+// of epilogue warps, one per accumulator, that take alternate tiles: each adds the
+// norm term, takes the exponential with the 1/sqrt(m) scale folded into its
+// exponent and stores bf16 rows by TMA.  Other shapes and fp32 run on the CUDA
+// cores in fp32.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <math.h>
@@ -28,7 +30,9 @@ using namespace tc;
 static __device__ unsigned g_favor_status;
 
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr int kFavorThreads = 192;  // warp 0: TMA loads, warp 1: MMA issue, warps 2-5: epilogue
+// warp 0: TMA loads, warp 1: MMA issue, warps 2-5: epilogue set 0 (even tiles,
+// accumulator 0), warps 6-9: epilogue set 1 (odd tiles, accumulator 1)
+constexpr int kFavorThreads = 320;
 constexpr uint32_t kOutRows = 32;                 // rows per epilogue warp and per TMA store box
 constexpr uint32_t kOutBox = kOutRows * 128;      // [32 rows x 64 bf16] swizzled: 4 KB
 constexpr uint64_t kDrainLimitNs = 100000000ull;  // 0.1 s for copies still in flight after an abort
@@ -37,10 +41,11 @@ template <int D, int M>
 struct FavorCfg {
     static constexpr int kStages = D == 128 ? 3 : 4;
     static constexpr uint32_t kXTile = (D / 64) * kBox;          // one 128-row tile of x
-    static constexpr uint32_t kWarpOut = (M / 64) * kOutBox;     // 32 rows of phi, one buffer
+    static constexpr uint32_t kWarpOut = (M / 64) * kOutBox;     // 32 rows of phi: one warp's buffer
+    static constexpr uint32_t kWBytes = (D / 64) * M * 128;      // W as D/64 boxes of M rows
     static constexpr uint32_t kOffW = kStages * kXTile;          // W: D/64 boxes of up to 128 rows
-    static constexpr uint32_t kOffOut = kOffW + (D / 64) * kBox;  // 4 warps x 2 buffers
-    static constexpr uint32_t kOffBar = kOffOut + 4 * 2 * kWarpOut;
+    static constexpr uint32_t kOffOut = kOffW + (D / 64) * kBox;  // 8 epilogue warps x 1 buffer
+    static constexpr uint32_t kOffBar = kOffOut + 8 * kWarpOut;
     static constexpr uint32_t kSmem = kOffBar + 256;
     static constexpr uint32_t kTmemCols = 2 * M;                 // two accumulators of M columns
     // exponent offset of the 1/sqrt(m) scale: -log2(m) / 2
@@ -58,7 +63,6 @@ struct FavorParams {
     int BH, N, nch;
     int T1;     // tiles of one tensor: BH * nch
     int total;  // tiles of the launch: T1 or 2 * T1 (q and k)
-    const __nv_bfloat16 *W;
 };
 
 __device__ __forceinline__ bool fwait(int *abort_flag, uint64_t *bar, uint32_t parity)
@@ -83,7 +87,7 @@ template <int D, int M>
 __global__ void __launch_bounds__(kFavorThreads, 1)
 favor_tc_kernel(const __grid_constant__ CUtensorMap map_xq, const __grid_constant__ CUtensorMap map_xk,
                 const __grid_constant__ CUtensorMap map_oq, const __grid_constant__ CUtensorMap map_ok,
-                const FavorParams prm)
+                const __grid_constant__ CUtensorMap map_w, const FavorParams prm)
 {
     using CF = FavorCfg<D, M>;
     constexpr int S = CF::kStages;
@@ -115,14 +119,6 @@ favor_tc_kernel(const __grid_constant__ CUtensorMap map_xq, const __grid_constan
         tmem_relinquish();
     }
     griddep_wait();  // W and x may be written by the launch before this one
-    // W [M, D] into the K-major swizzled layout of the B operand: row r of box
-    // c / 64 holds W[r, 64 * (c / 64) ...], 16-byte chunk u at position u ^ (r % 8).
-    for (int ch = tid; ch < M * D / 8; ch += kFavorThreads) {
-        const int r = ch / (D / 8), c8 = ch - r * (D / 8);
-        const uint4 val = *reinterpret_cast<const uint4 *>(prm.W + (size_t)r * D + c8 * 8);
-        *reinterpret_cast<uint4 *>(ws + (c8 >> 3) * kBox + r * 128 + (((c8 & 7) ^ (r & 7)) << 4)) = val;
-    }
-    fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -141,7 +137,16 @@ favor_tc_kernel(const __grid_constant__ CUtensorMap map_xq, const __grid_constan
                 if (j >= S && !fwait(abort_flag, &bars.empty[s], ((j / S) - 1) & 1)) break;
                 int which, bh, c;
                 tile_coords(prm, (int)blockIdx.x + j * (int)gridDim.x, which, bh, c);
-                mbar_arrive_expect_tx(&bars.full[s], CF::kXTile);
+                if (j == 0) {
+                    // W [M, D] rides on the first tile's barrier: K-major swizzled B operand,
+                    // box b holding columns 64b .. 64b + 63 of all M rows
+                    mbar_arrive_expect_tx(&bars.full[0], CF::kXTile + CF::kWBytes);
+#pragma unroll
+                    for (int bx = 0; bx < D / 64; ++bx)
+                        tma_load_3d(ws + bx * kBox, &map_w, &bars.full[0], 64 * bx, 0, 0);
+                } else {
+                    mbar_arrive_expect_tx(&bars.full[s], CF::kXTile);
+                }
 #pragma unroll
                 for (int bx = 0; bx < D / 64; ++bx)
                     tma_load_3d_hint(xs + s * CF::kXTile + bx * kBox, which ? &map_xk : &map_xq, &bars.full[s],
@@ -175,11 +180,12 @@ favor_tc_kernel(const __grid_constant__ CUtensorMap map_xq, const __grid_constan
     } else {
         // ---------------------------------------------------------------- epilogue
         const int qw = warp & 3;             // TMEM lane quarter this warp may access
+        const int set = (warp - 2) >> 2;     // tiles j with j % 2 == set, accumulator `set`
         const int i = qw * 32 + lane;        // row of the tile
         const uint32_t tl = tmem + ((uint32_t)(qw * 32) << 16);
-        uint8_t *obase = smem_raw + CF::kOffOut + qw * 2 * CF::kWarpOut;
+        uint8_t *ob = smem_raw + CF::kOffOut + (warp - 2) * CF::kWarpOut;
         const uint64_t pol = l2_policy_evict_first();
-        for (int j = 0; j < ntiles; ++j) {
+        for (int j = set; j < ntiles; j += 2) {
             const int s = j % S, b = j & 1;
             int which, bh, c;
             tile_coords(prm, (int)blockIdx.x + j * (int)gridDim.x, which, bh, c);
@@ -208,9 +214,8 @@ favor_tc_kernel(const __grid_constant__ CUtensorMap map_xq, const __grid_constan
             if (lane == 0) mbar_arrive(&bars.empty[s]);  // the MMAs and this warp are done with x
             // phi = 2^(acc log2(e) - |x|^2 log2(e) / 2 - log2(m) / 2)
             const float cexp = fmaf(-0.5f * kLog2e, nrm, CF::kScaleExp);
-            uint8_t *ob = obase + (j & 1) * CF::kWarpOut;
-            // the store issued from this buffer two tiles ago has finished reading it
-            if (lane == 0) tma_store_wait_read<1>();
+            // this warp's store of two tiles ago has finished reading the buffer
+            if (lane == 0) tma_store_wait_read_all();
             __syncwarp();
 #pragma unroll 1
             for (int cc = 0; cc < M / 64; ++cc) {
@@ -275,23 +280,23 @@ la_status launch_tc(const void *xq, const void *xk, const void *W, void *oq, voi
                     cudaStream_t stream)
 {
     using CF = FavorCfg<D, M>;
-    CUtensorMap mxq, mxk, moq, mok;
+    CUtensorMap mxq, mxk, moq, mok, mw;
     la_status st;
     if ((st = make_map_rows(&mxq, xq, BH, N, D, 128)) != LA_OK) return st;
     if ((st = make_map_rows(&mxk, xk ? xk : xq, BH, N, D, 128)) != LA_OK) return st;
     if ((st = make_map_rows(&moq, oq, BH, N, M, (int)kOutRows)) != LA_OK) return st;
     if ((st = make_map_rows(&mok, ok ? ok : oq, BH, N, M, (int)kOutRows)) != LA_OK) return st;
+    if ((st = make_map_rows(&mw, W, 1, M, D, M)) != LA_OK) return st;
     FavorParams prm;
     prm.BH = BH;
     prm.N = N;
     prm.nch = ceil_div(N, 128);
     prm.T1 = BH * prm.nch;
     prm.total = xk ? 2 * prm.T1 : prm.T1;
-    prm.W = (const __nv_bfloat16 *)W;
     if ((st = ensure_smem((const void *)favor_tc_kernel<D, M>, (int)CF::kSmem)) != LA_OK) return st;
     const int grid = prm.total < sm_count() ? prm.total : sm_count();
     st = launch_dependent(favor_tc_kernel<D, M>, (unsigned)grid, kFavorThreads, (int)CF::kSmem, stream, mxq, mxk,
-                          moq, mok, prm);
+                          moq, mok, mw, prm);
     count_launches();
     return st;
 }
