@@ -18,7 +18,8 @@ Tensors are PyTorch CUDA tensors (PyTorch supplies device memory and streams):
 from __future__ import annotations
 
 from ._binding import (LA_BF16, LA_F32, LA_PHI_ELU1, LA_PHI_IDENTITY, LA_PHI_RELU, LAError, Variant, lib_path,
-                       la_backward_causal, la_favor_features, la_forward_causal_favor, la_forward_noncausal_favor, la_decode_step, la_decode_step_decay, la_decode_step_ex, la_forward_causal,
+                       la_backward_causal, la_favor_features, la_forward_causal_favor, la_forward_noncausal_favor,
+                       la_prefill_state_favor, la_decode_step_favor, la_decode_step, la_decode_step_decay, la_decode_step_ex, la_forward_causal,
                        la_forward_causal_decay, la_forward_causal_ex, la_forward_noncausal, la_forward_noncausal_ex,
                        la_prefill_state_ex, la_forward_noncausal_noalloc, la_get_device_status, la_kernel_launches, la_last_cuda_error,
                        la_prefill_state, la_prefill_state_decay, la_status_string, la_version, load_library)
@@ -26,6 +27,7 @@ from ._binding import (LA_BF16, LA_F32, LA_PHI_ELU1, LA_PHI_IDENTITY, LA_PHI_REL
 __all__ = [
     "LA_BF16", "LA_F32", "LA_PHI_ELU1", "LA_PHI_IDENTITY", "LA_PHI_RELU", "LAError", "Variant", "lib_path",
     "la_backward_causal", "la_favor_features", "la_forward_causal_favor", "la_forward_noncausal_favor",
+    "la_prefill_state_favor", "la_decode_step_favor",
     "la_decode_step", "la_decode_step_decay", "la_decode_step_ex", "la_forward_causal", "la_forward_causal_decay",
     "la_forward_causal_ex", "la_forward_noncausal_ex", "la_prefill_state_ex",
     "la_forward_noncausal", "la_forward_noncausal_noalloc", "la_get_device_status", "la_kernel_launches", "la_last_cuda_error", "la_prefill_state",

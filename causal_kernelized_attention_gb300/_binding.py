@@ -68,6 +68,8 @@ def _declare(lib):
         "la_favor_features": [P, P, P, I, I, I, I, I, I, P],
         "la_forward_causal_favor": [P, P, P, P, P, I, I, I, I, I, I, I, F, I, P],
         "la_forward_noncausal_favor": [P, P, P, P, P, I, I, I, I, I, I, F, I, P],
+        "la_prefill_state_favor": [P, P, P, P, P, I, I, I, I, I, I, I, P],
+        "la_decode_step_favor": [P, P, P, P, P, P, P, I, I, I, I, I, F, I, P],
         "la_get_device_status": [P],
     }
     for name, args in sigs.items():
@@ -469,6 +471,48 @@ def la_forward_noncausal_favor(q, k, v, w, o=None, eps: float = 1e-6, stream=Non
                                                    w.data_ptr(), B, H, N, d, dv, m, float(eps), _dtype_code(q),
                                                    _stream_ptr(stream))
     _check("la_forward_noncausal_favor", st)
+    return o
+
+
+def la_prefill_state_favor(k, v, w, S=None, z=None, stream=None):
+    """Prefix state on FAVOR+ features of k (projections w [m, d]); returns (S [B,H,m,dv], z [B,H,m]) fp32."""
+    import torch
+    B, H, N, d = k.shape
+    dv = v.shape[-1]
+    m = _favor_w(w, k, d)
+    if S is None:
+        S = torch.empty((B, H, m, dv), dtype=torch.float32, device=k.device)
+    if z is None:
+        z = torch.empty((B, H, m), dtype=torch.float32, device=k.device)
+    _need_cuda(k, v, S, z)
+    _same_dtype(k, v)
+    if tuple(v.shape[:-1]) != (B, H, N) or tuple(S.shape) != (B, H, m, dv) or tuple(z.shape) != (B, H, m):
+        raise ValueError("shape mismatch")
+    st = load_library().la_prefill_state_favor(k.data_ptr(), v.data_ptr(), w.data_ptr(), S.data_ptr(), z.data_ptr(),
+                                               B, H, N, d, dv, m, _dtype_code(k), _stream_ptr(stream))
+    _check("la_prefill_state_favor", st)
+    return S, z
+
+
+def la_decode_step_favor(S, z, q, k, v, w, o=None, eps: float = 1e-6, stream=None):
+    """One decode step on FAVOR+ features of q and k; S [B,H,m,dv], z [B,H,m] fp32 updated in place."""
+    import torch
+    if o is None:
+        o = torch.empty(q.shape[:-1] + (v.shape[-1],), dtype=q.dtype, device=q.device)
+    _need_cuda(S, z, q, k, v, o)
+    _same_dtype(q, k, v, o)
+    if S.dtype != torch.float32 or z.dtype != torch.float32:
+        raise TypeError("S and z must be float32")
+    B, H, d = q.shape
+    dv = v.shape[-1]
+    m = _favor_w(w, q, d)
+    if tuple(S.shape) != (B, H, m, dv) or tuple(z.shape) != (B, H, m) or tuple(k.shape) != (B, H, d) \
+            or tuple(v.shape) != (B, H, dv) or tuple(o.shape) != (B, H, dv):
+        raise ValueError("shape mismatch")
+    st = load_library().la_decode_step_favor(S.data_ptr(), z.data_ptr(), q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                             o.data_ptr(), w.data_ptr(), B, H, d, dv, m, float(eps), _dtype_code(q),
+                                             _stream_ptr(stream))
+    _check("la_decode_step_favor", st)
     return o
 
 

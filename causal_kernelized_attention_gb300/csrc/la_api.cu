@@ -465,6 +465,63 @@ la_status la_forward_noncausal_favor(const void *q, const void *k, const void *v
     return noncausal_simt(p);
 }
 
+la_status la_prefill_state_favor(const void *k, const void *v, const void *w, float *S, float *z, int B, int H,
+                                 int N, int d, int dv, int m, la_dtype dtype, la_stream_t stream)
+{
+    if (B < 0 || H < 0 || N < 0 || d < 0 || dv < 0 || m < 0) return LA_ERR_INVALID_ARG;
+    if (dtype != LA_F32 && dtype != LA_BF16) return LA_ERR_INVALID_ARG;
+    if ((long long)B * H > 65535) return LA_ERR_UNSUPPORTED;
+    if (B == 0 || H == 0 || dv == 0) return LA_OK;
+    if (!supported_dim(m) || !supported_dim(d)) return LA_ERR_UNSUPPORTED;
+    const la_variant identity = {LA_PHI_IDENTITY, 0.f, 1};
+    if (N == 0)  // no tokens: S and z are zero
+        return la_prefill_state_ex(nullptr, nullptr, nullptr, &identity, S, z, B, H, 0, m, dv, dtype, stream);
+    if (!k || !v || !w || !S || !z) return LA_ERR_INVALID_ARG;
+    if (!aligned16(k) || !aligned16(w)) return LA_ERR_MISALIGNED;
+    const size_t BH = (size_t)B * H, es = elem_size(dtype), nw = (size_t)m * d * es;
+    if (overlaps(S, BH * m * dv * 4, w, nw) || overlaps(z, BH * m * 4, w, nw) ||
+        overlaps(S, BH * m * dv * 4, k, BH * N * d * es) || overlaps(z, BH * m * 4, k, BH * N * d * es))
+        return LA_ERR_INVALID_ARG;
+    const size_t bytes = BH * N * m * es;
+    Scratch s;
+    la_status st = s.alloc(bytes, (cudaStream_t)stream);
+    if (st != LA_OK) return st;
+    if ((st = favor_features(k, nullptr, w, s.ptr, nullptr, (int)BH, N, d, m, dtype, (cudaStream_t)stream)) != LA_OK)
+        return st;
+    return la_prefill_state_ex(s.ptr, v, nullptr, &identity, S, z, B, H, N, m, dv, dtype, stream);
+}
+
+la_status la_decode_step_favor(float *S, float *z, const void *q, const void *k, const void *v, void *o,
+                               const void *w, int B, int H, int d, int dv, int m, float eps, la_dtype dtype,
+                               la_stream_t stream)
+{
+    if (B < 0 || H < 0 || d < 0 || dv < 0 || m < 0) return LA_ERR_INVALID_ARG;
+    if (!(eps >= 0.f) || !isfinite(eps)) return LA_ERR_INVALID_ARG;
+    if (dtype != LA_F32 && dtype != LA_BF16) return LA_ERR_INVALID_ARG;
+    if (B == 0 || H == 0 || dv == 0) return LA_OK;
+    if (!supported_dim(m) || !supported_dim(d)) return LA_ERR_UNSUPPORTED;
+    if (!q || !k || !w || !o || !S || !z) return LA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(w)) return LA_ERR_MISALIGNED;
+    const long long BHl = (long long)B * H;
+    if (BHl > 0x7fffffff) return LA_ERR_UNSUPPORTED;
+    const size_t BH = (size_t)BHl, es = elem_size(dtype), nw = (size_t)m * d * es;
+    if (overlaps(S, BH * m * dv * 4, w, nw) || overlaps(z, BH * m * 4, w, nw) || overlaps(o, BH * dv * es, w, nw) ||
+        overlaps(S, BH * m * dv * 4, q, BH * d * es) || overlaps(S, BH * m * dv * 4, k, BH * d * es) ||
+        overlaps(z, BH * m * 4, q, BH * d * es) || overlaps(z, BH * m * 4, k, BH * d * es) ||
+        overlaps(o, BH * dv * es, q, BH * d * es) || overlaps(o, BH * dv * es, k, BH * d * es))
+        return LA_ERR_INVALID_ARG;
+    // phi(q) and phi(k) of every head: the rows are independent, so the batch is one
+    // sequence of B*H rows (the tensor-core features kernel takes it from 128 rows)
+    const size_t bytes = BH * m * es;  // a multiple of 64: both halves stay 16-byte aligned
+    Scratch s;
+    la_status st = s.alloc(2 * bytes, (cudaStream_t)stream);
+    if (st != LA_OK) return st;
+    void *fq = s.ptr, *fk = (char *)s.ptr + bytes;
+    if ((st = favor_features(q, k, w, fq, fk, 1, (int)BH, d, m, dtype, (cudaStream_t)stream)) != LA_OK) return st;
+    const la_variant identity = {LA_PHI_IDENTITY, 0.f, 1};
+    return la_decode_step_ex(S, z, fq, fk, v, o, nullptr, &identity, B, H, m, dv, eps, dtype, stream);
+}
+
 const char *la_status_string(la_status s)
 {
     switch (s) {

@@ -346,6 +346,30 @@ la_status la_forward_noncausal_favor(const void *q, const void *k, const void *v
                                      int H, int N, int d, int dv, int m, float eps, la_dtype dtype,
                                      la_stream_t stream);
 
+/*
+ * The prefix state and the decode step on FAVOR+ features (same page; the
+ * recurrent form that every kernelized variant keeps): la_prefill_state and
+ * la_decode_step with phi(k), phi(q) of la_favor_features in place of elu + 1.
+ *
+ *   prefill: k : [B, H, N, d]   v : [B, H, N, dv]   w : [m, d]
+ *            S : [B, H, m, dv] fp32, z : [B, H, m] fp32 (OVERWRITTEN; N = 0 writes zeros)
+ *   decode:  q, k : [B, H, d]   v, o : [B, H, dv]   w : [m, d]
+ *            S : [B, H, m, dv], z : [B, H, m] fp32, read and updated in place:
+ *            S += phi(k) v^T;  z += phi(k);  o = phi(q)^T S / max(phi(q)^T z, eps)
+ *
+ * The features go to per-call stream-ordered scratch (prefill: B*H*N*m
+ * elements; decode: 2*B*H*m), then the identity-map forms run on them.  In the
+ * decode step the B*H rows of q and k are featurised as one batch (the tensor-core
+ * features kernel takes it from 128 rows).  w must not overlap S, z or o; S and
+ * z must not overlap k (or q).  Supported: d, dv, m in {32, 64, 128} (B, H or
+ * dv = 0 is an empty problem; another d or m gives LA_ERR_UNSUPPORTED).
+ */
+la_status la_prefill_state_favor(const void *k, const void *v, const void *w, float *S, float *z, int B, int H,
+                                 int N, int d, int dv, int m, la_dtype dtype, la_stream_t stream);
+la_status la_decode_step_favor(float *S, float *z, const void *q, const void *k, const void *v, void *o,
+                               const void *w, int B, int H, int d, int dv, int m, float eps, la_dtype dtype,
+                               la_stream_t stream);
+
 /* Human-readable name of a status code (static string, never NULL). */
 const char *la_status_string(la_status s);
 

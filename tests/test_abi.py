@@ -237,6 +237,22 @@ def test_favor_validation(lib):
     assert fn(q, k, v, o, w, 1, 2, 16, 64, 32, 256, e, 1, None) == UNSUPPORTED
     assert fn(q, k, v, q + 64, w, 1, 2, 16, 64, 64, 64, e, 1, None) == INVALID      # o over q
     assert fn(None, None, None, None, None, 0, 2, 16, 64, 64, 64, e, 1, None) == OK
+    fp, fd = lib.la_prefill_state_favor, lib.la_decode_step_favor
+    S, z = A + 0x500000, A + 0x600000
+    assert fp(k, v, None, S, z, 1, 2, 16, 64, 64, 64, 1, None) == INVALID
+    assert fp(k, v, M, S, z, 1, 2, 16, 64, 64, 64, 1, None) == MISALIGNED
+    assert fp(k, v, w, S, z, 1, 2, 16, 64, 64, 48, 1, None) == UNSUPPORTED
+    assert fp(k, v, w, S, z, 1, 2, 16, 0, 64, 64, 1, None) == UNSUPPORTED
+    assert fp(k, v, S + 64, S, z, 1, 2, 16, 64, 64, 64, 1, None) == INVALID        # w over S
+    assert fp(k, v, w, S, z, 1, 2, 16, 64, 64, 64, 7, None) == INVALID
+    assert fp(None, None, None, S, z, 0, 2, 16, 64, 64, 64, 1, None) == OK         # empty
+    assert fd(S, z, q, k, v, o, None, 1, 2, 64, 64, 64, e, 1, None) == INVALID
+    assert fd(S, z, q, k, v, o, M, 1, 2, 64, 64, 64, e, 1, None) == MISALIGNED
+    assert fd(S, z, q, k, v, o, w, 1, 2, 64, 64, 256, e, 1, None) == UNSUPPORTED
+    assert fd(S, z, q, k, v, o, o + 64, 1, 2, 64, 64, 64, e, 1, None) == INVALID   # w over o
+    assert fd(S, z, q, k, v, q + 64, w, 1, 2, 64, 64, 64, e, 1, None) == INVALID   # o over q
+    assert fd(S, z, q, k, v, o, w, 1, 2, 64, 64, 64, ctypes.c_float(float("nan")), 1, None) == INVALID
+    assert fd(None, None, None, None, None, None, None, 1, 0, 64, 64, 64, e, 1, None) == OK
 
 
 def test_binding_raises_without_cuda_tensors():

@@ -50,8 +50,9 @@ def la():
     return m
 
 
-def widen(w, dtype):
-    return workloads.bf16_bits_to_f32(w).astype(np.float64) if dtype == "bf16" else w.astype(np.float64)
+def widen(x, dtype):
+    """The values an array holds (bf16 bit patterns or fp32), as float64."""
+    return workloads.bf16_bits_to_f32(x).astype(np.float64) if dtype == "bf16" else np.asarray(x, np.float64)
 
 
 def inputs(seed, B, H, N, d, dv, m, dtype):
@@ -111,6 +112,71 @@ def test_noncausal_favor(orc, dtype, B, H, N, d, dv, m):
     assert la().la_get_device_status() == 0
     ref = orc.noncausal_favor(q, k, v, widen(w, dtype))
     assert_parity(from_dev(o), ref, dtype, ("noncausal_favor", N, d, dv, m))
+
+
+def normwise(got, ref):
+    return float(np.max(np.abs(got - ref)) / np.max(np.abs(ref)))
+
+
+# States (normwise): the unnormalised sums keep the features' own error, which the
+# features test bounds elementwise -- fp32: the exponent's rounding, a few 1e-6 relative
+# on the largest features that dominate S (bound 1e-4, the features' bound); bf16: the
+# features' single rounding, 2^-9 relative (bound 1e-2).
+STATE_TOL = {"f32": 1e-4, "bf16": 1e-2}
+
+
+@pytest.mark.parametrize("dtype,B,H,N,d,dv,m", [
+    ("bf16", 2, 3, 300, 64, 64, 64), ("bf16", 1, 4, 1000, 128, 128, 128), ("bf16", 2, 3, 257, 64, 32, 128),
+    ("bf16", 2, 2, 100, 128, 64, 64), ("f32", 2, 3, 300, 64, 64, 64), ("f32", 1, 2, 129, 32, 128, 32),
+])
+def test_prefill_state_favor(orc, dtype, B, H, N, d, dv, m):
+    """S = sum_t phi(k_t) v_t^T, z = sum_t phi(k_t) on FAVOR+ features: tensor-core state
+    (bf16, m = dv in {64, 128}, N >= 128) and CUDA-core shapes."""
+    _, k, v, w = inputs(25000 + N + d + dv + m, B, H, N, d, dv, m, dtype)
+    S, z = la().la_prefill_state_favor(to_dev(k, dtype), to_dev(v, dtype), to_dev(w, dtype))
+    torch.cuda.synchronize()
+    assert la().la_get_device_status() == 0
+    Sr, zr = orc.prefill_state_general(orc.favor_features(k, widen(w, dtype)), widen(v, dtype), fmap="identity",
+                                       shift=0.0)
+    assert normwise(from_dev(S), Sr) <= STATE_TOL[dtype], ("S", dtype, N, d, dv, m)
+    assert normwise(from_dev(z), zr) <= STATE_TOL[dtype], ("z", dtype, N, d, dv, m)
+
+
+def test_prefill_state_favor_empty_sequence_writes_zeros():
+    kd = torch.empty((2, 3, 0, 64), dtype=torch.bfloat16, device="cuda")
+    w = to_dev(workloads.favor_projection(25900, 64, 64, "bf16"), "bf16")
+    S = torch.full((2, 3, 64, 64), 7.0, device="cuda")
+    z = torch.full((2, 3, 64), 7.0, device="cuda")
+    la().la_prefill_state_favor(kd, kd, w, S, z)
+    torch.cuda.synchronize()
+    assert torch.all(S == 0) and torch.all(z == 0)
+
+
+@pytest.mark.parametrize("dtype,B,H,d,dv,m", [
+    ("bf16", 32, 4, 64, 64, 64), ("bf16", 16, 8, 128, 128, 128), ("bf16", 2, 3, 64, 32, 128),
+    ("f32", 2, 3, 64, 64, 64), ("f32", 32, 4, 32, 64, 32),
+])
+def test_decode_step_favor(orc, dtype, B, H, d, dv, m):
+    """A 64-token FAVOR+ prefill, then 4 decode steps: each step's o and the final S, z
+    against the oracle's decode steps on the oracle's features (B*H >= 128 rows take the
+    tensor-core features kernel for bf16 with d, m in {64, 128})."""
+    N, steps = 64, 4
+    _, kp, vp, w = inputs(26000 + d + dv + m + B, B, H, N, d, dv, m, dtype)
+    q, k, v = workloads.random_inputs(26500 + d + m + B, steps, B, H, d, dv, dtype, sigma=SIGMA)
+    wd = to_dev(w, dtype)
+    S, z = la().la_prefill_state_favor(to_dev(kp, dtype), to_dev(vp, dtype), wd)
+    wr = widen(w, dtype)
+    Sr, zr = orc.prefill_state_general(orc.favor_features(kp, wr), widen(vp, dtype), fmap="identity", shift=0.0)
+    Sr, zr = np.ascontiguousarray(Sr), np.ascontiguousarray(zr)
+    for t in range(steps):
+        o = la().la_decode_step_favor(S, z, to_dev(q[t], dtype), to_dev(k[t], dtype), to_dev(v[t], dtype), wd)
+        torch.cuda.synchronize()
+        ref = orc.decode_step_general(Sr, zr, orc.favor_features(q[t], wr), orc.favor_features(k[t], wr),
+                                      widen(v[t], dtype), fmap="identity", shift=0.0, normalize=True)
+        assert_parity(from_dev(o), ref, dtype, ("decode_favor", t, d, dv, m))
+    assert la().la_get_device_status() == 0
+    assert normwise(from_dev(S), Sr) <= STATE_TOL[dtype]
+    assert normwise(from_dev(z), zr) <= STATE_TOL[dtype]
 
 
 def test_causal_favor_first_row_and_graph_replay(orc):
