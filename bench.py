@@ -709,6 +709,37 @@ def bench_path_noncausal_favor(torch, la, reps, peaks, src):
             "l2": "%d rotating buffer sets" % R}
 
 
+def bench_path_decode_favor(torch, la, steps, peaks, src):
+    """la_decode_step_favor on the decode workload (128 x 32 heads, d = 128, fp32 state) with
+    m = 128 features: the features of the step's q and k (8192 rows, one launch) and the
+    decode step on them.  The prefill state comes from la_prefill_state_favor.  Inputs are
+    scaled to sigma = 0.5 (the FAVOR+ input scale)."""
+    w = workloads.DECODE_BF16
+    m = 128
+    (qp, kp, vp), (qd, kd, vd) = workloads.device_decode_inputs(w)
+    for t in (qd, kd):
+        t.mul_(FAVOR_SIGMA)
+    kp.mul_(FAVOR_SIGMA)
+    wp = dev_copy(torch, workloads.favor_projection(w.seed + 1, m, w.dk, "bf16"), "bf16")
+    S, z = la.la_prefill_state_favor(kp, vp, wp)
+    del qp, kp, vp
+    o = torch.empty((w.B, w.H, w.dv), dtype=torch.bfloat16, device="cuda")
+
+    def step(i):
+        la.la_decode_step_favor(S, z, qd[i], kd[i], vd[i], wp, o, eps=w.eps)
+
+    n = min(steps, w.steps)
+    secs, launches, _ = time_graph_steps(torch, la, step, n, 3, Dist())
+    t = secs / n
+    nbytes = decode_bytes_per_step(w.BH, m, w.dv, 2) + m * w.dk * 2
+    fl = decode_flops_per_step(w.BH, m, w.dv) + favor_flops(2 * w.BH, w.dk, m)
+    return {"workload": w.name + "_favor_m%d" % m, "value": round(w.B / t, 1), "unit": "tokens/s",
+            "head_steps_per_s": round(w.BH / t, 1), "ms_per_step": round(t * 1e3, 5), "steps": n,
+            "launches_per_step": launches / n, "m": m, "sigma": FAVOR_SIGMA,
+            "roofline": roofline(fl, nbytes, t, peaks, src, None),
+            "l2": "state 270 MB > L2"}
+
+
 def bench_path_decode_decay(torch, la, steps, peaks, src):
     """la_decode_step_decay on the decode workload (4096 heads, d = 128, fp32 state)."""
     w = workloads.DECODE_BF16
@@ -841,6 +872,7 @@ def run_gpu(args, dist):
         paths["favor_features"] = bench_path_favor_features(torch, la, reps, peaks, src)
         paths["causal_favor"] = bench_path_causal_favor(torch, la, reps, peaks, src)
         paths["noncausal_favor"] = bench_path_noncausal_favor(torch, la, reps, peaks, src)
+        paths["decode_favor"] = bench_path_decode_favor(torch, la, 256, peaks, src)
         if s2:
             paths["clocks"] = s2.stop(window=(t_paths, time.time()))
 
