@@ -11,7 +11,9 @@
 //   R_j = sum_{i>=j} phi(q_i) dn_i^T,   r_j = sum_{i>=j} dd_i phi(q_i)
 //   dq = dphi(q) * phi'(q),  phi'(x) = 1 (x > 0), exp(x) (x <= 0) = min(1, phi(x)).
 //
-// Chunk-parallel, five launches over (b,h, chunk of C tokens):
+// Chunk-parallel, five launches over (b,h, chunk of C tokens); within a chunk every
+// product is a block matrix product over the chunk's shared-memory tiles (a 16 x 16
+// thread grid, each thread a register tile of the output):
 //   1. chunk states    A_c = phi(K_c)^T [V_c | 1]                       -> buf[c]
 //   2. forward scan    buf[c] = sum_{c' < c} A_c'   (exclusive prefix: S, z before c)
 //   3. dq              per chunk: o, d, dn, dd, dq from the prefix and the intra-chunk
@@ -25,8 +27,7 @@
 namespace la {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kWarps = kThreads / 32;
+constexpr int kThreads = 256;  // a 16 x 16 thread grid over every output tile
 
 template <int DK, int DV>
 struct Chunk {
@@ -34,38 +35,155 @@ struct Chunk {
     static constexpr int E = DK * (DV + 1);                    // floats per chunk state
 };
 
+// Shared-memory tiles of one chunk, fp32, rows padded by one float: with row strides
+// of 1 (mod 32) words, the accesses of the products below -- 16 consecutive columns
+// of a row, or 16 consecutive rows of a column -- fall in distinct banks.
+template <int DK, int DV>
+struct Tiles {
+    static constexpr int C = Chunk<DK, DV>::C;
+    static constexpr int LQ = DK + 1, LV = DV + 1, LT = C + 1;
+    static constexpr int kFq = 0;                 // phi(Q_c)        [C][LQ]
+    static constexpr int kFk = kFq + C * LQ;      // phi(K_c)        [C][LQ]
+    static constexpr int kV = kFk + C * LQ;       // V_c             [C][LV]
+    static constexpr int kDn = kV + C * LV;       // [dN_c | dd_c]   [C][LV]
+    static constexpr int kSt = kDn + C * LV;      // [S | z] or [R | r] of the chunk boundary  [DK][LV]
+    static constexpr int kT = kSt + DK * LV;      // scores T, then U  [C][LT]
+    static constexpr int kDen = kT + C * LT;      // denominators      [C]
+    static constexpr int kFloats = kDen + C;
+    static constexpr size_t kBytes = sizeof(float) * kFloats;
+};
+
+// acc[i][j] += sum_k a(ty + 16 i, k) * b(k, tx + 16 j) for an M x N output on the
+// 16 x 16 thread grid (tx = thread % 16, ty = thread / 16).
+template <int M, int N, int K, typename FA, typename FB>
+__device__ __forceinline__ void gemm(float (&acc)[M / 16][N / 16], FA a, FB b)
+{
+    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+#pragma unroll 4
+    for (int k = 0; k < K; ++k) {
+        float av[M / 16], bv[N / 16];
+#pragma unroll
+        for (int i = 0; i < M / 16; ++i) av[i] = a(ty + 16 * i, k);
+#pragma unroll
+        for (int j = 0; j < N / 16; ++j) bv[j] = b(k, tx + 16 * j);
+#pragma unroll
+        for (int i = 0; i < M / 16; ++i)
+#pragma unroll
+            for (int j = 0; j < N / 16; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+    }
+}
+
+template <int M, int N>
+__device__ __forceinline__ void zero(float (&acc)[M][N])
+{
+#pragma unroll
+    for (int i = 0; i < M; ++i)
+#pragma unroll
+        for (int j = 0; j < N; ++j) acc[i][j] = 0.f;
+}
+
 // phi'(x) for elu + 1 from phi(x): 1 where x > 0 (phi > 1), exp(x) = phi(x) otherwise.
 __device__ __forceinline__ float dphi_from_phi(float f) { return fminf(f, 1.f); }
 
-// 1. A_c = phi(K_c)^T [V_c | 1].  Grid (nC, BH).
+// phi(Q_c), phi(K_c), V_c into their tiles (rows past the sequence zero).
+template <typename T, int DK, int DV>
+__device__ __forceinline__ void load_qkv(float *sm, const T *q, const T *k, const T *v, size_t qk0, size_t v0,
+                                         int len)
+{
+    using L = Tiles<DK, DV>;
+    for (int e = threadIdx.x; e < L::C * DK; e += kThreads) {
+        const int j = e / DK, r = e % DK;
+        sm[L::kFq + j * L::LQ + r] = j < len ? Elem<T>::phi(Elem<T>::to_f32(q[qk0 + (size_t)j * DK + r])) : 0.f;
+        sm[L::kFk + j * L::LQ + r] = j < len ? Elem<T>::phi(Elem<T>::to_f32(k[qk0 + (size_t)j * DK + r])) : 0.f;
+    }
+    for (int e = threadIdx.x; e < L::C * DV; e += kThreads) {
+        const int j = e / DV, cc = e % DV;
+        sm[L::kV + j * L::LV + cc] = j < len ? Elem<T>::to_f32(v[v0 + (size_t)j * DV + cc]) : 0.f;
+    }
+}
+
+// T = phi(Q_c) phi(K_c)^T with the causal mask (key <= query < len) into the T tile.
+template <int DK, int DV>
+__device__ __forceinline__ void scores(float *sm, int len)
+{
+    using L = Tiles<DK, DV>;
+    constexpr int C = L::C;
+    const float *fq = sm + L::kFq, *fk = sm + L::kFk;
+    float *ts = sm + L::kT;
+    float acc[C / 16][C / 16];
+    zero(acc);
+    gemm<C, C, DK>(acc, [&](int m, int kk) { return fq[m * L::LQ + kk]; },
+                   [&](int kk, int n) { return fk[n * L::LQ + kk]; });
+    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+#pragma unroll
+    for (int i = 0; i < C / 16; ++i)
+#pragma unroll
+        for (int j = 0; j < C / 16; ++j) {
+            const int m = ty + 16 * i, n = tx + 16 * j;
+            ts[m * L::LT + n] = (n <= m && m < len) ? acc[i][j] : 0.f;
+        }
+}
+
+// U = (dN_c V_c^T + dd_c 1^T) with the causal mask into the T tile.
+template <int DK, int DV>
+__device__ __forceinline__ void weights_u(float *sm, int len)
+{
+    using L = Tiles<DK, DV>;
+    constexpr int C = L::C;
+    const float *dn = sm + L::kDn, *vs = sm + L::kV;
+    float *ts = sm + L::kT;
+    float acc[C / 16][C / 16];
+    zero(acc);
+    gemm<C, C, DV>(acc, [&](int m, int kk) { return dn[m * L::LV + kk]; },
+                   [&](int kk, int n) { return vs[n * L::LV + kk]; });
+    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+#pragma unroll
+    for (int i = 0; i < C / 16; ++i) {
+        const int m = ty + 16 * i;
+        const float dd = dn[m * L::LV + DV];
+#pragma unroll
+        for (int j = 0; j < C / 16; ++j) {
+            const int n = tx + 16 * j;
+            ts[m * L::LT + n] = (n <= m && m < len) ? acc[i][j] + dd : 0.f;
+        }
+    }
+}
+
+// 1. A_c = phi(K_c)^T [V_c | 1] -> buf[c].  Grid (nC, BH).
 template <typename T, int DK, int DV>
 __global__ void __launch_bounds__(kThreads)
 bwd_chunk_state(const T *__restrict__ k, const T *__restrict__ v, float *__restrict__ buf, int N)
 {
-    using CH = Chunk<DK, DV>;
-    constexpr int C = CH::C;
-    __shared__ float fk[C][DK];
-    __shared__ float vs[C][DV + 1];
+    using L = Tiles<DK, DV>;
+    constexpr int C = L::C;
+    extern __shared__ __align__(16) float sm[];
     const int c = blockIdx.x, bh = blockIdx.y, tid = threadIdx.x;
     const int t0 = c * C, len = min(C, N - t0);
-    const T *kh = k + ((size_t)bh * N + t0) * DK;
-    const T *vh = v + ((size_t)bh * N + t0) * DV;
+    const size_t qk0 = ((size_t)bh * N + t0) * DK, v0 = ((size_t)bh * N + t0) * DV;
+    float *fk = sm + L::kFk, *vs = sm + L::kV;
     for (int e = tid; e < C * DK; e += kThreads) {
         const int j = e / DK, r = e % DK;
-        fk[j][r] = j < len ? Elem<T>::phi(Elem<T>::to_f32(kh[(size_t)j * DK + r])) : 0.f;
+        fk[j * L::LQ + r] = j < len ? Elem<T>::phi(Elem<T>::to_f32(k[qk0 + (size_t)j * DK + r])) : 0.f;
     }
-    for (int e = tid; e < C * (DV + 1); e += kThreads) {
-        const int j = e / (DV + 1), cc = e % (DV + 1);
-        vs[j][cc] = j < len ? (cc < DV ? Elem<T>::to_f32(vh[(size_t)j * DV + cc]) : 1.f) : 0.f;
+    for (int e = tid; e < C * DV; e += kThreads) {
+        const int j = e / DV, cc = e % DV;
+        vs[j * L::LV + cc] = j < len ? Elem<T>::to_f32(v[v0 + (size_t)j * DV + cc]) : 0.f;
     }
     __syncthreads();
-    float *out = buf + ((size_t)bh * gridDim.x + c) * CH::E;
-    for (int e = tid; e < CH::E; e += kThreads) {
-        const int r = e / (DV + 1), cc = e % (DV + 1);
-        float acc = 0.f;
-#pragma unroll 8
-        for (int j = 0; j < C; ++j) acc += fk[j][r] * vs[j][cc];
-        out[e] = acc;
+    float *out = buf + ((size_t)bh * gridDim.x + c) * Chunk<DK, DV>::E;
+    float acc[DK / 16][DV / 16];
+    zero(acc);
+    gemm<DK, DV, C>(acc, [&](int m, int kk) { return fk[kk * L::LQ + m]; },
+                    [&](int kk, int n) { return vs[kk * L::LV + n]; });
+    const int tx = tid & 15, ty = tid >> 4;
+#pragma unroll
+    for (int i = 0; i < DK / 16; ++i)
+#pragma unroll
+        for (int j = 0; j < DV / 16; ++j) out[(ty + 16 * i) * (DV + 1) + tx + 16 * j] = acc[i][j];
+    if (tid < DK) {  // z column: the column sums of phi(K_c)
+        float s = 0.f;
+        for (int kk = 0; kk < C; ++kk) s += fk[kk * L::LQ + tid];
+        out[tid * (DV + 1) + DV] = s;
     }
 }
 
@@ -100,186 +218,169 @@ bwd_scan(float *__restrict__ buf, int nC, int E, long long total, int reverse)
     }
 }
 
-template <int DK, int DV>
-struct DqSmem {
-    static constexpr int C = Chunk<DK, DV>::C;
-    float P[DK][DV + 1];    // prefix state before the chunk: S, z in column DV
-    float fq[C][DK + 1];
-    float fk[C][DK + 1];
-    float vs[C][DV + 1];
-    float dn[C][DV + 1];    // dn, dd in column DV
-};
-
-// 3. dq, dn, dd and the reverse chunk state.  Grid (nC, BH), one warp per query row.
+// 3. Per chunk: o and the clamped denominator d, dN = dO / d and dd = -(dO . o) / d
+// (0 where the clamp binds) to dnbuf, dq, and the reverse chunk state
+// B_c = phi(Q_c)^T [dN_c | dd_c] over the chunk's own slot.  Grid (nC, BH).
+//   T   = tril(phi(Q) phi(K)^T)          den = rowsum T + phi(Q) z
+//   num = T V + phi(Q) S                 U   = tril(dN V^T + dd 1^T)
+//   dphi(Q) = U phi(K) + dN S^T + dd z^T
 template <typename T, int DK, int DV>
 __global__ void __launch_bounds__(kThreads)
 bwd_dq(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v, const T *__restrict__ dout,
        T *__restrict__ dq, float *__restrict__ buf, float *__restrict__ dnbuf, int N, float eps)
 {
-    using CH = Chunk<DK, DV>;
-    constexpr int C = CH::C;
-    extern __shared__ __align__(16) unsigned char smem_raw[];
-    auto &sm = *reinterpret_cast<DqSmem<DK, DV> *>(smem_raw);
-    const int c = blockIdx.x, bh = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    using L = Tiles<DK, DV>;
+    constexpr int C = L::C;
+    extern __shared__ __align__(16) float sm[];
+    const int c = blockIdx.x, bh = blockIdx.y, tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
     const int t0 = c * C, len = min(C, N - t0);
     const size_t qk0 = ((size_t)bh * N + t0) * DK, v0 = ((size_t)bh * N + t0) * DV;
-    float *slot = buf + ((size_t)bh * gridDim.x + c) * CH::E;
-    for (int e = tid; e < CH::E; e += kThreads) sm.P[e / (DV + 1)][e % (DV + 1)] = slot[e];
-    for (int e = tid; e < C * DK; e += kThreads) {
-        const int j = e / DK, r = e % DK;
-        sm.fq[j][r] = j < len ? Elem<T>::phi(Elem<T>::to_f32(q[qk0 + (size_t)j * DK + r])) : 0.f;
-        sm.fk[j][r] = j < len ? Elem<T>::phi(Elem<T>::to_f32(k[qk0 + (size_t)j * DK + r])) : 0.f;
-    }
-    for (int e = tid; e < C * DV; e += kThreads) {
-        const int j = e / DV, cc = e % DV;
-        sm.vs[j][cc] = j < len ? Elem<T>::to_f32(v[v0 + (size_t)j * DV + cc]) : 0.f;
+    const float *fq = sm + L::kFq, *fk = sm + L::kFk, *vs = sm + L::kV, *st = sm + L::kSt, *ts = sm + L::kT;
+    float *dn = sm + L::kDn, *den = sm + L::kDen;
+    float *slot = buf + ((size_t)bh * gridDim.x + c) * Chunk<DK, DV>::E;
+    for (int e = tid; e < Chunk<DK, DV>::E; e += kThreads) sm[L::kSt + e] = slot[e];  // [S | z] before the chunk
+    load_qkv<T, DK, DV>(sm, q, k, v, qk0, v0, len);
+    __syncthreads();
+    scores<DK, DV>(sm, len);
+    __syncthreads();
+    if (tid < C) {
+        float s = 0.f;
+        for (int n = 0; n < C; ++n) s += ts[tid * L::LT + n];
+        for (int r = 0; r < DK; ++r) s += fq[tid * L::LQ + r] * st[r * L::LV + DV];
+        den[tid] = s;
     }
     __syncthreads();
-
-    constexpr int KB = C / 32;   // key blocks of 32 in the chunk
-    for (int a = warp; a < len; a += kWarps) {
-        // intra-chunk scores s_ab, b <= a (lane b of block m holds key 32m + lane)
-        float s[KB];
-        float den = 0.f;
+    {
+        float acc[C / 16][DV / 16];
+        zero(acc);
+        gemm<C, DV, C>(acc, [&](int m, int kk) { return ts[m * L::LT + kk]; },
+                       [&](int kk, int n) { return vs[kk * L::LV + n]; });
+        gemm<C, DV, DK>(acc, [&](int m, int kk) { return fq[m * L::LQ + kk]; },
+                        [&](int kk, int n) { return st[kk * L::LV + n]; });
 #pragma unroll
-        for (int m = 0; m < KB; ++m) {
-            const int b = 32 * m + lane;
-            float acc = 0.f;
-#pragma unroll 8
-            for (int r = 0; r < DK; ++r) acc += sm.fq[a][r] * sm.fk[b][r];
-            s[m] = b <= a ? acc : 0.f;
-            den += s[m];
-        }
-        for (int r = lane; r < DK; r += 32) den += sm.fq[a][r] * sm.P[r][DV];
+        for (int i = 0; i < C / 16; ++i) {
+            const int m = ty + 16 * i;
+            const float inv = 1.f / fmaxf(den[m], eps);
+            float go[DV / 16], g = 0.f;
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
-        const bool clamped = !(den > eps);
-        const float d = fmaxf(den, eps), inv = 1.f / d;
-        // numerator columns, lanes over columns: n = phi(q_a) P + sum_b s_ab v_b
-        float g = 0.f;
-        for (int cc = lane; cc < DV; cc += 32) {
-            float n = 0.f;
-#pragma unroll 8
-            for (int r = 0; r < DK; ++r) n += sm.fq[a][r] * sm.P[r][cc];
-#pragma unroll
-            for (int m = 0; m < KB; ++m) {
-                const int bmax = min(32, a + 1 - 32 * m);
-                for (int bb = 0; bb < bmax; ++bb) n += __shfl_sync(0xffffffffu, s[m], bb) * sm.vs[32 * m + bb][cc];
+            for (int j = 0; j < DV / 16; ++j) {
+                go[j] = m < len ? Elem<T>::to_f32(dout[v0 + (size_t)m * DV + tx + 16 * j]) : 0.f;
+                g += go[j] * (acc[i][j] * inv);
             }
-            const float go = Elem<T>::to_f32(dout[v0 + (size_t)a * DV + cc]);
-            g += go * (n * inv);
-            sm.dn[a][cc] = go * inv;
-        }
+            // g = dO_m . o_m over the 16 threads of this row (lanes of one half-warp)
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) g += __shfl_xor_sync(0xffffffffu, g, off);
-        const float dd = clamped ? 0.f : -g * inv;
-        if (lane == 0) sm.dn[a][DV] = dd;
-        __syncwarp();
-        // t_b = v_b . dn_a + dd for the keys b <= a
-        float tb[KB];
+            for (int off = 8; off > 0; off >>= 1) g += __shfl_xor_sync(0xffffffffu, g, off);
 #pragma unroll
-        for (int m = 0; m < KB; ++m) {
-            const int b = 32 * m + lane;
-            float acc = dd;
-#pragma unroll 8
-            for (int cc = 0; cc < DV; ++cc) acc += sm.vs[b][cc] * sm.dn[a][cc];
-            tb[m] = b <= a ? acc : 0.f;
+            for (int j = 0; j < DV / 16; ++j) dn[m * L::LV + tx + 16 * j] = go[j] * inv;
+            if (tx == 0) dn[m * L::LV + DV] = den[m] > eps ? -g * inv : 0.f;
         }
-        // dphi(q_a)[r] = P[r][:] . dn_a + dd z[r] + sum_b t_b phi(k_b)[r]
-        for (int r = lane; r < DK; r += 32) {
-            float acc = dd * sm.P[r][DV];
-#pragma unroll 8
-            for (int cc = 0; cc < DV; ++cc) acc += sm.P[r][cc] * sm.dn[a][cc];
-#pragma unroll
-            for (int m = 0; m < KB; ++m) {
-                const int bmax = min(32, a + 1 - 32 * m);
-                for (int bb = 0; bb < bmax; ++bb) acc += __shfl_sync(0xffffffffu, tb[m], bb) * sm.fk[32 * m + bb][r];
-            }
-            dq[qk0 + (size_t)a * DK + r] = Elem<T>::from_f32(acc * dphi_from_phi(sm.fq[a][r]));
-        }
-        float *dnrow = dnbuf + ((size_t)bh * N + t0 + a) * (DV + 1);
-        for (int cc = lane; cc <= DV; cc += 32) dnrow[cc] = sm.dn[a][cc];
     }
-    // rows past the end of the sequence contribute nothing to the reverse state
-    for (int e = tid; e < (C - len) * (DV + 1); e += kThreads) sm.dn[len + e / (DV + 1)][e % (DV + 1)] = 0.f;
     __syncthreads();
-    // B_c = phi(Q_c)^T [dN_c | dd_c] into this chunk's slot (the prefix was read above)
-    for (int e = tid; e < CH::E; e += kThreads) {
-        const int r = e / (DV + 1), cc = e % (DV + 1);
-        float acc = 0.f;
-#pragma unroll 8
-        for (int a = 0; a < C; ++a) acc += sm.fq[a][r] * sm.dn[a][cc];
-        slot[e] = acc;
+    {
+        float *dst = dnbuf + ((size_t)bh * N + t0) * L::LV;
+        for (int e = tid; e < len * L::LV; e += kThreads) dst[e] = dn[e];
+    }
+    weights_u<DK, DV>(sm, len);
+    __syncthreads();
+    {
+        float acc[C / 16][DK / 16];
+        zero(acc);
+        gemm<C, DK, C>(acc, [&](int m, int kk) { return ts[m * L::LT + kk]; },
+                       [&](int kk, int n) { return fk[kk * L::LQ + n]; });
+        gemm<C, DK, DV>(acc, [&](int m, int kk) { return dn[m * L::LV + kk]; },
+                        [&](int kk, int n) { return st[n * L::LV + kk]; });
+#pragma unroll
+        for (int i = 0; i < C / 16; ++i) {
+            const int m = ty + 16 * i;
+            if (m >= len) continue;
+            const float dd = dn[m * L::LV + DV];
+#pragma unroll
+            for (int j = 0; j < DK / 16; ++j) {
+                const int n = tx + 16 * j;
+                const float g = acc[i][j] + dd * st[n * L::LV + DV];
+                dq[qk0 + (size_t)m * DK + n] = Elem<T>::from_f32(g * dphi_from_phi(fq[m * L::LQ + n]));
+            }
+        }
+    }
+    {
+        // B_c (the slot's prefix was read into shared memory at the start)
+        float acc[DK / 16][DV / 16];
+        zero(acc);
+        gemm<DK, DV, C>(acc, [&](int m, int kk) { return fq[kk * L::LQ + m]; },
+                        [&](int kk, int n) { return dn[kk * L::LV + n]; });
+#pragma unroll
+        for (int i = 0; i < DK / 16; ++i)
+#pragma unroll
+            for (int j = 0; j < DV / 16; ++j) slot[(ty + 16 * i) * (DV + 1) + tx + 16 * j] = acc[i][j];
+        if (tid < DK) {
+            float s = 0.f;
+            for (int kk = 0; kk < C; ++kk) s += fq[kk * L::LQ + tid] * dn[kk * L::LV + DV];
+            slot[tid * (DV + 1) + DV] = s;
+        }
     }
 }
 
-// 5. dk, dv.  Grid (nC, BH), one warp per key row.  Reuses the dq kernel's shared layout:
-// P holds the suffix state [R | r] after the chunk.
+// 5. dk, dv per chunk from the suffix [R | r] after it.  Grid (nC, BH).
+//   dV      = T^T dN + phi(K) R
+//   dphi(K) = U^T phi(Q) + V R^T + 1 r^T
 template <typename T, int DK, int DV>
 __global__ void __launch_bounds__(kThreads)
 bwd_dkdv(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v, T *__restrict__ dk,
          T *__restrict__ dv, const float *__restrict__ buf, const float *__restrict__ dnbuf, int N)
 {
-    using CH = Chunk<DK, DV>;
-    constexpr int C = CH::C;
-    extern __shared__ __align__(16) unsigned char smem_raw[];
-    auto &sm = *reinterpret_cast<DqSmem<DK, DV> *>(smem_raw);
-    const int c = blockIdx.x, bh = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    using L = Tiles<DK, DV>;
+    constexpr int C = L::C;
+    extern __shared__ __align__(16) float sm[];
+    const int c = blockIdx.x, bh = blockIdx.y, tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
     const int t0 = c * C, len = min(C, N - t0);
     const size_t qk0 = ((size_t)bh * N + t0) * DK, v0 = ((size_t)bh * N + t0) * DV;
-    const float *slot = buf + ((size_t)bh * gridDim.x + c) * CH::E;
-    for (int e = tid; e < CH::E; e += kThreads) sm.P[e / (DV + 1)][e % (DV + 1)] = slot[e];
-    for (int e = tid; e < C * DK; e += kThreads) {
-        const int j = e / DK, r = e % DK;
-        sm.fq[j][r] = j < len ? Elem<T>::phi(Elem<T>::to_f32(q[qk0 + (size_t)j * DK + r])) : 0.f;
-        sm.fk[j][r] = j < len ? Elem<T>::phi(Elem<T>::to_f32(k[qk0 + (size_t)j * DK + r])) : 0.f;
-    }
-    for (int e = tid; e < C * DV; e += kThreads) {
-        const int j = e / DV, cc = e % DV;
-        sm.vs[j][cc] = j < len ? Elem<T>::to_f32(v[v0 + (size_t)j * DV + cc]) : 0.f;
-    }
-    const float *dnc = dnbuf + ((size_t)bh * N + t0) * (DV + 1);
-    for (int e = tid; e < C * (DV + 1); e += kThreads) {
-        const int j = e / (DV + 1), cc = e % (DV + 1);
-        sm.dn[j][cc] = j < len ? dnc[(size_t)j * (DV + 1) + cc] : 0.f;
+    const float *fq = sm + L::kFq, *fk = sm + L::kFk, *vs = sm + L::kV, *dn = sm + L::kDn, *st = sm + L::kSt,
+                *ts = sm + L::kT;
+    const float *slot = buf + ((size_t)bh * gridDim.x + c) * Chunk<DK, DV>::E;
+    for (int e = tid; e < Chunk<DK, DV>::E; e += kThreads) sm[L::kSt + e] = slot[e];  // [R | r] after the chunk
+    load_qkv<T, DK, DV>(sm, q, k, v, qk0, v0, len);
+    {
+        const float *src = dnbuf + ((size_t)bh * N + t0) * L::LV;
+        for (int e = tid; e < C * L::LV; e += kThreads) sm[L::kDn + e] = e < len * L::LV ? src[e] : 0.f;
     }
     __syncthreads();
-
-    constexpr int KB = C / 32;
-    for (int j = warp; j < len; j += kWarps) {
-        // for the queries a >= j: u_a = dn_a . v_j + dd_a, w_a = phi(q_a) . phi(k_j)
-        float u[KB], w[KB];
+    scores<DK, DV>(sm, len);
+    __syncthreads();
+    {
+        float acc[C / 16][DV / 16];
+        zero(acc);
+        gemm<C, DV, C>(acc, [&](int m, int kk) { return ts[kk * L::LT + m]; },
+                       [&](int kk, int n) { return dn[kk * L::LV + n]; });
+        gemm<C, DV, DK>(acc, [&](int m, int kk) { return fk[m * L::LQ + kk]; },
+                        [&](int kk, int n) { return st[kk * L::LV + n]; });
 #pragma unroll
-        for (int m = 0; m < KB; ++m) {
-            const int a = 32 * m + lane;
-            float au = sm.dn[a][DV], aw = 0.f;
-#pragma unroll 8
-            for (int cc = 0; cc < DV; ++cc) au += sm.dn[a][cc] * sm.vs[j][cc];
-#pragma unroll 8
-            for (int r = 0; r < DK; ++r) aw += sm.fq[a][r] * sm.fk[j][r];
-            const bool in = a >= j && a < len;
-            u[m] = in ? au : 0.f;
-            w[m] = in ? aw : 0.f;
+        for (int i = 0; i < C / 16; ++i) {
+            const int m = ty + 16 * i;
+            if (m >= len) continue;
+#pragma unroll
+            for (int j = 0; j < DV / 16; ++j) dv[v0 + (size_t)m * DV + tx + 16 * j] = Elem<T>::from_f32(acc[i][j]);
         }
-        // dphi(k_j)[r] = R[r][:] . v_j + r[r] + sum_a u_a phi(q_a)[r]
-        for (int r = lane; r < DK; r += 32) {
-            float acc = sm.P[r][DV];
-#pragma unroll 8
-            for (int cc = 0; cc < DV; ++cc) acc += sm.P[r][cc] * sm.vs[j][cc];
+    }
+    __syncthreads();  // the T tile is read; U replaces it
+    weights_u<DK, DV>(sm, len);
+    __syncthreads();
+    {
+        float acc[C / 16][DK / 16];
+        zero(acc);
+        gemm<C, DK, C>(acc, [&](int m, int kk) { return ts[kk * L::LT + m]; },
+                       [&](int kk, int n) { return fq[kk * L::LQ + n]; });
+        gemm<C, DK, DV>(acc, [&](int m, int kk) { return vs[m * L::LV + kk]; },
+                        [&](int kk, int n) { return st[n * L::LV + kk]; });
 #pragma unroll
-            for (int m = 0; m < KB; ++m)
-                for (int aa = 0; aa < 32; ++aa) acc += __shfl_sync(0xffffffffu, u[m], aa) * sm.fq[32 * m + aa][r];
-            dk[qk0 + (size_t)j * DK + r] = Elem<T>::from_f32(acc * dphi_from_phi(sm.fk[j][r]));
-        }
-        // dv_j[cc] = R[:][cc] . phi(k_j) + sum_a w_a dn_a[cc]
-        for (int cc = lane; cc < DV; cc += 32) {
-            float acc = 0.f;
-#pragma unroll 8
-            for (int r = 0; r < DK; ++r) acc += sm.P[r][cc] * sm.fk[j][r];
+        for (int i = 0; i < C / 16; ++i) {
+            const int m = ty + 16 * i;
+            if (m >= len) continue;
 #pragma unroll
-            for (int m = 0; m < KB; ++m)
-                for (int aa = 0; aa < 32; ++aa) acc += __shfl_sync(0xffffffffu, w[m], aa) * sm.dn[32 * m + aa][cc];
-            dv[v0 + (size_t)j * DV + cc] = Elem<T>::from_f32(acc);
+            for (int j = 0; j < DK / 16; ++j) {
+                const int n = tx + 16 * j;
+                const float g = acc[i][j] + st[n * L::LV + DV];
+                dk[qk0 + (size_t)m * DK + n] = Elem<T>::from_f32(g * dphi_from_phi(fk[m * L::LQ + n]));
+            }
         }
     }
 }
@@ -288,6 +389,7 @@ template <typename T, int DK, int DV>
 la_status launch_backward(const BackwardProblem &p)
 {
     using CH = Chunk<DK, DV>;
+    using L = Tiles<DK, DV>;
     const int nC = ceil_div(p.N, CH::C);
     const size_t state_floats = (size_t)p.BH * nC * CH::E;
     const size_t dn_floats = (size_t)p.BH * p.N * (DV + 1);
@@ -295,15 +397,16 @@ la_status launch_backward(const BackwardProblem &p)
     la_status st = scratch.alloc(sizeof(float) * (state_floats + dn_floats), p.stream);
     if (st != LA_OK) return st;
     float *buf = (float *)scratch.ptr, *dnbuf = buf + state_floats;
-    const size_t smem = sizeof(DqSmem<DK, DV>);
-    st = ensure_smem((const void *)bwd_dq<T, DK, DV>, (int)smem);
-    if (st == LA_OK) st = ensure_smem((const void *)bwd_dkdv<T, DK, DV>, (int)smem);
+    const int smem = (int)L::kBytes;
+    st = ensure_smem((const void *)bwd_chunk_state<T, DK, DV>, smem);
+    if (st == LA_OK) st = ensure_smem((const void *)bwd_dq<T, DK, DV>, smem);
+    if (st == LA_OK) st = ensure_smem((const void *)bwd_dkdv<T, DK, DV>, smem);
     if (st != LA_OK) return st;
     const dim3 grid(nC, p.BH);
     const long long total = (long long)p.BH * CH::E;
     const unsigned scan_blocks = (unsigned)((total + kThreads - 1) / kThreads);
     count_launches(5);
-    bwd_chunk_state<T, DK, DV><<<grid, kThreads, 0, p.stream>>>((const T *)p.k, (const T *)p.v, buf, p.N);
+    bwd_chunk_state<T, DK, DV><<<grid, kThreads, smem, p.stream>>>((const T *)p.k, (const T *)p.v, buf, p.N);
     bwd_scan<<<scan_blocks, kThreads, 0, p.stream>>>(buf, nC, CH::E, total, 0);
     bwd_dq<T, DK, DV><<<grid, kThreads, smem, p.stream>>>((const T *)p.q, (const T *)p.k, (const T *)p.v,
                                                           (const T *)p.dout, (T *)p.dq, buf, dnbuf, p.N, p.eps);
