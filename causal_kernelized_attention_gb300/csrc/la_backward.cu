@@ -50,6 +50,7 @@ struct Tiles {
     static constexpr int kT = kSt + DK * LV;      // scores T, then U  [C][LT]
     static constexpr int kDen = kT + C * LT;      // denominators      [C]
     static constexpr int kFloats = kDen + C;
+    static_assert(kSt % 4 == 0 && (DK * (DV + 1)) % 4 == 0, "st tile and chunk states on 16-byte boundaries");
     static constexpr size_t kBytes = sizeof(float) * kFloats;
 };
 
@@ -85,21 +86,85 @@ __device__ __forceinline__ void zero(float (&acc)[M][N])
 // phi'(x) for elu + 1 from phi(x): 1 where x > 0 (phi > 1), exp(x) = phi(x) otherwise.
 __device__ __forceinline__ float dphi_from_phi(float f) { return fminf(f, 1.f); }
 
+// Rows [0, len) of a contiguous [rows x W] block of T elements into shared-memory rows
+// of stride LD as fp32, through f (rows past len are zero).  Every 16-byte load of a
+// thread is issued before any is used, so a tile costs one memory latency, not one
+// per element.
+template <typename T, int C, int W, typename F>
+__device__ __forceinline__ void load_tile(float *dst, int LD, const T *src, int len, F f)
+{
+    constexpr int VE = 16 / (int)sizeof(T);  // elements per 16-byte vector
+    constexpr int VR = W / VE;                // vectors per row
+    constexpr int NV = C * VR;
+    constexpr int IT = (NV + kThreads - 1) / kThreads;
+    uint4 buf[IT];
+#pragma unroll
+    for (int it = 0; it < IT; ++it) {
+        const int vi = threadIdx.x + it * kThreads;
+        buf[it] = (vi < NV && vi / VR < len) ? __ldg(reinterpret_cast<const uint4 *>(src) + vi)
+                                              : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int it = 0; it < IT; ++it) {
+        const int vi = threadIdx.x + it * kThreads;
+        if (vi >= NV) break;
+        const int row = vi / VR, col = (vi % VR) * VE;
+        const T *e = reinterpret_cast<const T *>(&buf[it]);
+#pragma unroll
+        for (int u = 0; u < VE; ++u) dst[row * LD + col + u] = row < len ? f(Elem<T>::to_f32(e[u])) : 0.f;
+    }
+}
+
+// n floats from global to shared memory, all loads of a thread issued first (scalar:
+// the source need not be 16-byte aligned); elements at or past `valid` read as zero.
+template <int NMAX>
+__device__ __forceinline__ void load_floats(float *dst, const float *src, int n, int valid)
+{
+    constexpr int IT = (NMAX + kThreads - 1) / kThreads;
+    float buf[IT];
+#pragma unroll
+    for (int it = 0; it < IT; ++it) {
+        const int e = threadIdx.x + it * kThreads;
+        buf[it] = (e < n && e < valid) ? __ldg(src + e) : 0.f;
+    }
+#pragma unroll
+    for (int it = 0; it < IT; ++it) {
+        const int e = threadIdx.x + it * kThreads;
+        if (e < n) dst[e] = buf[it];
+    }
+}
+
+// NF floats (a multiple of 4, both addresses 16-byte aligned) from global to shared
+// memory in 16-byte vectors, all loads of a thread issued first.
+template <int NF>
+__device__ __forceinline__ void load_flat(float *dst, const float *src)
+{
+    static_assert(NF % 4 == 0, "whole vectors");
+    constexpr int NV = NF / 4, IT = (NV + kThreads - 1) / kThreads;
+    float4 buf[IT];
+#pragma unroll
+    for (int it = 0; it < IT; ++it) {
+        const int vi = threadIdx.x + it * kThreads;
+        if (vi < NV) buf[it] = __ldg(reinterpret_cast<const float4 *>(src) + vi);
+    }
+#pragma unroll
+    for (int it = 0; it < IT; ++it) {
+        const int vi = threadIdx.x + it * kThreads;
+        if (vi < NV) reinterpret_cast<float4 *>(dst)[vi] = buf[it];
+    }
+}
+
 // phi(Q_c), phi(K_c), V_c into their tiles (rows past the sequence zero).
 template <typename T, int DK, int DV>
 __device__ __forceinline__ void load_qkv(float *sm, const T *q, const T *k, const T *v, size_t qk0, size_t v0,
                                          int len)
 {
     using L = Tiles<DK, DV>;
-    for (int e = threadIdx.x; e < L::C * DK; e += kThreads) {
-        const int j = e / DK, r = e % DK;
-        sm[L::kFq + j * L::LQ + r] = j < len ? Elem<T>::phi(Elem<T>::to_f32(q[qk0 + (size_t)j * DK + r])) : 0.f;
-        sm[L::kFk + j * L::LQ + r] = j < len ? Elem<T>::phi(Elem<T>::to_f32(k[qk0 + (size_t)j * DK + r])) : 0.f;
-    }
-    for (int e = threadIdx.x; e < L::C * DV; e += kThreads) {
-        const int j = e / DV, cc = e % DV;
-        sm[L::kV + j * L::LV + cc] = j < len ? Elem<T>::to_f32(v[v0 + (size_t)j * DV + cc]) : 0.f;
-    }
+    auto phi = [](float x) { return Elem<T>::phi(x); };
+    auto id = [](float x) { return x; };
+    load_tile<T, L::C, DK>(sm + L::kFq, L::LQ, q + qk0, len, phi);
+    load_tile<T, L::C, DK>(sm + L::kFk, L::LQ, k + qk0, len, phi);
+    load_tile<T, L::C, DV>(sm + L::kV, L::LV, v + v0, len, id);
 }
 
 // T = phi(Q_c) phi(K_c)^T with the causal mask (key <= query < len) into the T tile.
@@ -161,14 +226,8 @@ bwd_chunk_state(const T *__restrict__ k, const T *__restrict__ v, float *__restr
     const int t0 = c * C, len = min(C, N - t0);
     const size_t qk0 = ((size_t)bh * N + t0) * DK, v0 = ((size_t)bh * N + t0) * DV;
     float *fk = sm + L::kFk, *vs = sm + L::kV;
-    for (int e = tid; e < C * DK; e += kThreads) {
-        const int j = e / DK, r = e % DK;
-        fk[j * L::LQ + r] = j < len ? Elem<T>::phi(Elem<T>::to_f32(k[qk0 + (size_t)j * DK + r])) : 0.f;
-    }
-    for (int e = tid; e < C * DV; e += kThreads) {
-        const int j = e / DV, cc = e % DV;
-        vs[j * L::LV + cc] = j < len ? Elem<T>::to_f32(v[v0 + (size_t)j * DV + cc]) : 0.f;
-    }
+    load_tile<T, C, DK>(fk, L::LQ, k + qk0, len, [](float x) { return Elem<T>::phi(x); });
+    load_tile<T, C, DV>(vs, L::LV, v + v0, len, [](float x) { return x; });
     __syncthreads();
     float *out = buf + ((size_t)bh * gridDim.x + c) * Chunk<DK, DV>::E;
     float acc[DK / 16][DV / 16];
@@ -238,8 +297,19 @@ bwd_dq(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v
     const float *fq = sm + L::kFq, *fk = sm + L::kFk, *vs = sm + L::kV, *st = sm + L::kSt, *ts = sm + L::kT;
     float *dn = sm + L::kDn, *den = sm + L::kDen;
     float *slot = buf + ((size_t)bh * gridDim.x + c) * Chunk<DK, DV>::E;
-    for (int e = tid; e < Chunk<DK, DV>::E; e += kThreads) sm[L::kSt + e] = slot[e];  // [S | z] before the chunk
+    // [S | z] before the chunk, in the layout of the st tile ([DK][DV + 1]); slot and
+    // tile start on 16-byte boundaries (E and the tile offset are multiples of 4 floats)
+    load_flat<Chunk<DK, DV>::E>(sm + L::kSt, slot);
     load_qkv<T, DK, DV>(sm, q, k, v, qk0, v0, len);
+    // this thread's dO elements, in flight while the scores are formed
+    float go[C / 16][DV / 16];
+#pragma unroll
+    for (int i = 0; i < C / 16; ++i)
+#pragma unroll
+        for (int j = 0; j < DV / 16; ++j) {
+            const int m = ty + 16 * i;
+            go[i][j] = m < len ? Elem<T>::to_f32(dout[v0 + (size_t)m * DV + tx + 16 * j]) : 0.f;
+        }
     __syncthreads();
     scores<DK, DV>(sm, len);
     __syncthreads();
@@ -261,17 +331,14 @@ bwd_dq(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v
         for (int i = 0; i < C / 16; ++i) {
             const int m = ty + 16 * i;
             const float inv = 1.f / fmaxf(den[m], eps);
-            float go[DV / 16], g = 0.f;
+            float g = 0.f;
 #pragma unroll
-            for (int j = 0; j < DV / 16; ++j) {
-                go[j] = m < len ? Elem<T>::to_f32(dout[v0 + (size_t)m * DV + tx + 16 * j]) : 0.f;
-                g += go[j] * (acc[i][j] * inv);
-            }
+            for (int j = 0; j < DV / 16; ++j) g += go[i][j] * (acc[i][j] * inv);
             // g = dO_m . o_m over the 16 threads of this row (lanes of one half-warp)
 #pragma unroll
             for (int off = 8; off > 0; off >>= 1) g += __shfl_xor_sync(0xffffffffu, g, off);
 #pragma unroll
-            for (int j = 0; j < DV / 16; ++j) dn[m * L::LV + tx + 16 * j] = go[j] * inv;
+            for (int j = 0; j < DV / 16; ++j) dn[m * L::LV + tx + 16 * j] = go[i][j] * inv;
             if (tx == 0) dn[m * L::LV + DV] = den[m] > eps ? -g * inv : 0.f;
         }
     }
@@ -337,12 +404,10 @@ bwd_dkdv(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__
     const float *fq = sm + L::kFq, *fk = sm + L::kFk, *vs = sm + L::kV, *dn = sm + L::kDn, *st = sm + L::kSt,
                 *ts = sm + L::kT;
     const float *slot = buf + ((size_t)bh * gridDim.x + c) * Chunk<DK, DV>::E;
-    for (int e = tid; e < Chunk<DK, DV>::E; e += kThreads) sm[L::kSt + e] = slot[e];  // [R | r] after the chunk
+    // [R | r] after the chunk, in the layout of the st tile (16-byte aligned as in bwd_dq)
+    load_flat<Chunk<DK, DV>::E>(sm + L::kSt, slot);
     load_qkv<T, DK, DV>(sm, q, k, v, qk0, v0, len);
-    {
-        const float *src = dnbuf + ((size_t)bh * N + t0) * L::LV;
-        for (int e = tid; e < C * L::LV; e += kThreads) sm[L::kDn + e] = e < len * L::LV ? src[e] : 0.f;
-    }
+    load_floats<C * L::LV>(sm + L::kDn, dnbuf + ((size_t)bh * N + t0) * L::LV, C * L::LV, len * L::LV);
     __syncthreads();
     scores<DK, DV>(sm, len);
     __syncthreads();
