@@ -35,13 +35,14 @@ struct Chunk {
     static constexpr int E = DK * (DV + 1);                    // floats per chunk state
 };
 
-// Shared-memory tiles of one chunk, fp32, rows padded by one float: with row strides
-// of 1 (mod 32) words, the accesses of the products below -- 16 consecutive columns
-// of a row, or 16 consecutive rows of a column -- fall in distinct banks.
+// Shared-memory tiles of one chunk, fp32, rows padded by four floats: every row starts
+// on a 16-byte boundary, and with row strides of 4 (mod 32) words the products' accesses
+// -- 16 consecutive elements of a row, one address per half-warp, or one 16-byte vector
+// from each of 8 consecutive rows per quarter-warp -- fall in distinct banks.
 template <int DK, int DV>
 struct Tiles {
     static constexpr int C = Chunk<DK, DV>::C;
-    static constexpr int LQ = DK + 1, LV = DV + 1, LT = C + 1;
+    static constexpr int LQ = DK + 4, LV = DV + 4, LT = C + 4;
     static constexpr int kFq = 0;                 // phi(Q_c)        [C][LQ]
     static constexpr int kFk = kFq + C * LQ;      // phi(K_c)        [C][LQ]
     static constexpr int kV = kFk + C * LQ;       // V_c             [C][LV]
@@ -50,27 +51,55 @@ struct Tiles {
     static constexpr int kT = kSt + DK * LV;      // scores T, then U  [C][LT]
     static constexpr int kDen = kT + C * LT;      // denominators      [C]
     static constexpr int kFloats = kDen + C;
-    static_assert(kSt % 4 == 0 && (DK * (DV + 1)) % 4 == 0, "st tile and chunk states on 16-byte boundaries");
     static constexpr size_t kBytes = sizeof(float) * kFloats;
+    // the chunk-state kernel needs phi(K_c) and V_c only: [C][LQ] then [C][LV]
+    static constexpr size_t kStateBytes = sizeof(float) * C * (LQ + LV);
 };
 
-// acc[i][j] += sum_k a(ty + 16 i, k) * b(k, tx + 16 j) for an M x N output on the
-// 16 x 16 thread grid (tx = thread % 16, ty = thread / 16).
-template <int M, int N, int K, typename FA, typename FB>
-__device__ __forceinline__ void gemm(float (&acc)[M / 16][N / 16], FA a, FB b)
+// Operands of the products, element (r, k) of an R x K matrix in shared memory:
+// KRow: k contiguous, at p[r * ld + k] (four consecutive k in one 16-byte load);
+// KCol: r contiguous, at p[k * ld + r].
+struct KRow {
+    const float *p;
+    int ld;
+    __device__ __forceinline__ float4 load4(int r, int k) const
+    {
+        return *reinterpret_cast<const float4 *>(p + r * ld + k);
+    }
+};
+struct KCol {
+    const float *p;
+    int ld;
+    __device__ __forceinline__ float4 load4(int r, int k) const
+    {
+        return make_float4(p[k * ld + r], p[(k + 1) * ld + r], p[(k + 2) * ld + r], p[(k + 3) * ld + r]);
+    }
+};
+
+// acc[i][j] += sum_k A(ty + 16 i, k) * B(tx + 16 j, k) for an M x N output on the 16 x 16
+// thread grid (tx = thread % 16, ty = thread / 16); A is M x K and B is N x K (B(n, k) is
+// element (k, n) of the right-hand factor), taken four k at a time.
+template <int M, int N, int K, typename OA, typename OB>
+__device__ __forceinline__ void gemm(float (&acc)[M / 16][N / 16], OA a, OB b)
 {
+    static_assert(K % 4 == 0, "K in steps of 4");
     const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
-#pragma unroll 4
-    for (int k = 0; k < K; ++k) {
-        float av[M / 16], bv[N / 16];
+#pragma unroll 2
+    for (int k = 0; k < K; k += 4) {
+        float4 av[M / 16], bv[N / 16];
 #pragma unroll
-        for (int i = 0; i < M / 16; ++i) av[i] = a(ty + 16 * i, k);
+        for (int i = 0; i < M / 16; ++i) av[i] = a.load4(ty + 16 * i, k);
 #pragma unroll
-        for (int j = 0; j < N / 16; ++j) bv[j] = b(k, tx + 16 * j);
+        for (int j = 0; j < N / 16; ++j) bv[j] = b.load4(tx + 16 * j, k);
 #pragma unroll
         for (int i = 0; i < M / 16; ++i)
 #pragma unroll
-            for (int j = 0; j < N / 16; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+            for (int j = 0; j < N / 16; ++j) {
+                acc[i][j] = fmaf(av[i].x, bv[j].x, acc[i][j]);
+                acc[i][j] = fmaf(av[i].y, bv[j].y, acc[i][j]);
+                acc[i][j] = fmaf(av[i].z, bv[j].z, acc[i][j]);
+                acc[i][j] = fmaf(av[i].w, bv[j].w, acc[i][j]);
+            }
     }
 }
 
@@ -115,42 +144,25 @@ __device__ __forceinline__ void load_tile(float *dst, int LD, const T *src, int 
     }
 }
 
-// n floats from global to shared memory, all loads of a thread issued first (scalar:
-// the source need not be 16-byte aligned); elements at or past `valid` read as zero.
-template <int NMAX>
-__device__ __forceinline__ void load_floats(float *dst, const float *src, int n, int valid)
+// Rows [0, rows) of W floats each, contiguous in global memory (any alignment), into
+// shared-memory rows of stride LD; rows at or past `valid` read as zero.  Loads go in
+// batches of 8 per thread, all issued before their stores.
+template <int W>
+__device__ __forceinline__ void load_rows(float *dst, int LD, const float *src, int rows, int valid)
 {
-    constexpr int IT = (NMAX + kThreads - 1) / kThreads;
-    float buf[IT];
+    const int n = rows * W;
+    for (int base = 0; base < n; base += 8 * kThreads) {
+        float buf[8];
 #pragma unroll
-    for (int it = 0; it < IT; ++it) {
-        const int e = threadIdx.x + it * kThreads;
-        buf[it] = (e < n && e < valid) ? __ldg(src + e) : 0.f;
-    }
+        for (int u = 0; u < 8; ++u) {
+            const int e = base + (int)threadIdx.x + u * kThreads;
+            buf[u] = (e < n && e / W < valid) ? __ldg(src + e) : 0.f;
+        }
 #pragma unroll
-    for (int it = 0; it < IT; ++it) {
-        const int e = threadIdx.x + it * kThreads;
-        if (e < n) dst[e] = buf[it];
-    }
-}
-
-// NF floats (a multiple of 4, both addresses 16-byte aligned) from global to shared
-// memory in 16-byte vectors, all loads of a thread issued first.
-template <int NF>
-__device__ __forceinline__ void load_flat(float *dst, const float *src)
-{
-    static_assert(NF % 4 == 0, "whole vectors");
-    constexpr int NV = NF / 4, IT = (NV + kThreads - 1) / kThreads;
-    float4 buf[IT];
-#pragma unroll
-    for (int it = 0; it < IT; ++it) {
-        const int vi = threadIdx.x + it * kThreads;
-        if (vi < NV) buf[it] = __ldg(reinterpret_cast<const float4 *>(src) + vi);
-    }
-#pragma unroll
-    for (int it = 0; it < IT; ++it) {
-        const int vi = threadIdx.x + it * kThreads;
-        if (vi < NV) reinterpret_cast<float4 *>(dst)[vi] = buf[it];
+        for (int u = 0; u < 8; ++u) {
+            const int e = base + (int)threadIdx.x + u * kThreads;
+            if (e < n) dst[(e / W) * LD + e % W] = buf[u];
+        }
     }
 }
 
@@ -177,8 +189,7 @@ __device__ __forceinline__ void scores(float *sm, int len)
     float *ts = sm + L::kT;
     float acc[C / 16][C / 16];
     zero(acc);
-    gemm<C, C, DK>(acc, [&](int m, int kk) { return fq[m * L::LQ + kk]; },
-                   [&](int kk, int n) { return fk[n * L::LQ + kk]; });
+    gemm<C, C, DK>(acc, KRow{fq, L::LQ}, KRow{fk, L::LQ});
     const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
 #pragma unroll
     for (int i = 0; i < C / 16; ++i)
@@ -199,8 +210,7 @@ __device__ __forceinline__ void weights_u(float *sm, int len)
     float *ts = sm + L::kT;
     float acc[C / 16][C / 16];
     zero(acc);
-    gemm<C, C, DV>(acc, [&](int m, int kk) { return dn[m * L::LV + kk]; },
-                   [&](int kk, int n) { return vs[n * L::LV + kk]; });
+    gemm<C, C, DV>(acc, KRow{dn, L::LV}, KRow{vs, L::LV});
     const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
 #pragma unroll
     for (int i = 0; i < C / 16; ++i) {
@@ -225,15 +235,14 @@ bwd_chunk_state(const T *__restrict__ k, const T *__restrict__ v, float *__restr
     const int c = blockIdx.x, bh = blockIdx.y, tid = threadIdx.x;
     const int t0 = c * C, len = min(C, N - t0);
     const size_t qk0 = ((size_t)bh * N + t0) * DK, v0 = ((size_t)bh * N + t0) * DV;
-    float *fk = sm + L::kFk, *vs = sm + L::kV;
+    float *fk = sm, *vs = sm + C * L::LQ;  // the kStateBytes layout
     load_tile<T, C, DK>(fk, L::LQ, k + qk0, len, [](float x) { return Elem<T>::phi(x); });
     load_tile<T, C, DV>(vs, L::LV, v + v0, len, [](float x) { return x; });
     __syncthreads();
     float *out = buf + ((size_t)bh * gridDim.x + c) * Chunk<DK, DV>::E;
     float acc[DK / 16][DV / 16];
     zero(acc);
-    gemm<DK, DV, C>(acc, [&](int m, int kk) { return fk[kk * L::LQ + m]; },
-                    [&](int kk, int n) { return vs[kk * L::LV + n]; });
+    gemm<DK, DV, C>(acc, KCol{fk, L::LQ}, KCol{vs, L::LV});
     const int tx = tid & 15, ty = tid >> 4;
 #pragma unroll
     for (int i = 0; i < DK / 16; ++i)
@@ -256,18 +265,19 @@ bwd_scan(float *__restrict__ buf, int nC, int E, long long total, int reverse)
     const long long bh = g / E, e = g % E;
     float *p = buf + bh * (long long)nC * E + e;
     float run = 0.f;
-    for (int i = 0; i < nC; i += 8) {
-        float x[8];
-        const int m = min(8, nC - i);
+    // 32 chunks per round trip: every load of a round is issued before the first store
+    for (int i = 0; i < nC; i += 32) {
+        float x[32];
+        const int m = min(32, nC - i);
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
+        for (int u = 0; u < 32; ++u) {
             if (u < m) {
                 const int c = reverse ? nC - 1 - (i + u) : i + u;
                 x[u] = p[(long long)c * E];
             }
         }
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
+        for (int u = 0; u < 32; ++u) {
             if (u < m) {
                 const int c = reverse ? nC - 1 - (i + u) : i + u;
                 p[(long long)c * E] = run;
@@ -297,9 +307,7 @@ bwd_dq(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v
     const float *fq = sm + L::kFq, *fk = sm + L::kFk, *vs = sm + L::kV, *st = sm + L::kSt, *ts = sm + L::kT;
     float *dn = sm + L::kDn, *den = sm + L::kDen;
     float *slot = buf + ((size_t)bh * gridDim.x + c) * Chunk<DK, DV>::E;
-    // [S | z] before the chunk, in the layout of the st tile ([DK][DV + 1]); slot and
-    // tile start on 16-byte boundaries (E and the tile offset are multiples of 4 floats)
-    load_flat<Chunk<DK, DV>::E>(sm + L::kSt, slot);
+    load_rows<DV + 1>(sm + L::kSt, L::LV, slot, DK, DK);  // [S | z] before the chunk
     load_qkv<T, DK, DV>(sm, q, k, v, qk0, v0, len);
     // this thread's dO elements, in flight while the scores are formed
     float go[C / 16][DV / 16];
@@ -323,10 +331,8 @@ bwd_dq(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v
     {
         float acc[C / 16][DV / 16];
         zero(acc);
-        gemm<C, DV, C>(acc, [&](int m, int kk) { return ts[m * L::LT + kk]; },
-                       [&](int kk, int n) { return vs[kk * L::LV + n]; });
-        gemm<C, DV, DK>(acc, [&](int m, int kk) { return fq[m * L::LQ + kk]; },
-                        [&](int kk, int n) { return st[kk * L::LV + n]; });
+        gemm<C, DV, C>(acc, KRow{ts, L::LT}, KCol{vs, L::LV});
+        gemm<C, DV, DK>(acc, KRow{fq, L::LQ}, KCol{st, L::LV});
 #pragma unroll
         for (int i = 0; i < C / 16; ++i) {
             const int m = ty + 16 * i;
@@ -344,18 +350,16 @@ bwd_dq(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v
     }
     __syncthreads();
     {
-        float *dst = dnbuf + ((size_t)bh * N + t0) * L::LV;
-        for (int e = tid; e < len * L::LV; e += kThreads) dst[e] = dn[e];
+        float *dst = dnbuf + ((size_t)bh * N + t0) * (DV + 1);
+        for (int e = tid; e < len * (DV + 1); e += kThreads) dst[e] = dn[(e / (DV + 1)) * L::LV + e % (DV + 1)];
     }
     weights_u<DK, DV>(sm, len);
     __syncthreads();
     {
         float acc[C / 16][DK / 16];
         zero(acc);
-        gemm<C, DK, C>(acc, [&](int m, int kk) { return ts[m * L::LT + kk]; },
-                       [&](int kk, int n) { return fk[kk * L::LQ + n]; });
-        gemm<C, DK, DV>(acc, [&](int m, int kk) { return dn[m * L::LV + kk]; },
-                        [&](int kk, int n) { return st[n * L::LV + kk]; });
+        gemm<C, DK, C>(acc, KRow{ts, L::LT}, KCol{fk, L::LQ});
+        gemm<C, DK, DV>(acc, KRow{dn, L::LV}, KRow{st, L::LV});
 #pragma unroll
         for (int i = 0; i < C / 16; ++i) {
             const int m = ty + 16 * i;
@@ -373,8 +377,7 @@ bwd_dq(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v
         // B_c (the slot's prefix was read into shared memory at the start)
         float acc[DK / 16][DV / 16];
         zero(acc);
-        gemm<DK, DV, C>(acc, [&](int m, int kk) { return fq[kk * L::LQ + m]; },
-                        [&](int kk, int n) { return dn[kk * L::LV + n]; });
+        gemm<DK, DV, C>(acc, KCol{fq, L::LQ}, KCol{dn, L::LV});
 #pragma unroll
         for (int i = 0; i < DK / 16; ++i)
 #pragma unroll
@@ -404,20 +407,17 @@ bwd_dkdv(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__
     const float *fq = sm + L::kFq, *fk = sm + L::kFk, *vs = sm + L::kV, *dn = sm + L::kDn, *st = sm + L::kSt,
                 *ts = sm + L::kT;
     const float *slot = buf + ((size_t)bh * gridDim.x + c) * Chunk<DK, DV>::E;
-    // [R | r] after the chunk, in the layout of the st tile (16-byte aligned as in bwd_dq)
-    load_flat<Chunk<DK, DV>::E>(sm + L::kSt, slot);
+    load_rows<DV + 1>(sm + L::kSt, L::LV, slot, DK, DK);  // [R | r] after the chunk
     load_qkv<T, DK, DV>(sm, q, k, v, qk0, v0, len);
-    load_floats<C * L::LV>(sm + L::kDn, dnbuf + ((size_t)bh * N + t0) * L::LV, C * L::LV, len * L::LV);
+    load_rows<DV + 1>(sm + L::kDn, L::LV, dnbuf + ((size_t)bh * N + t0) * (DV + 1), C, len);
     __syncthreads();
     scores<DK, DV>(sm, len);
     __syncthreads();
     {
         float acc[C / 16][DV / 16];
         zero(acc);
-        gemm<C, DV, C>(acc, [&](int m, int kk) { return ts[kk * L::LT + m]; },
-                       [&](int kk, int n) { return dn[kk * L::LV + n]; });
-        gemm<C, DV, DK>(acc, [&](int m, int kk) { return fk[m * L::LQ + kk]; },
-                        [&](int kk, int n) { return st[kk * L::LV + n]; });
+        gemm<C, DV, C>(acc, KCol{ts, L::LT}, KCol{dn, L::LV});
+        gemm<C, DV, DK>(acc, KRow{fk, L::LQ}, KCol{st, L::LV});
 #pragma unroll
         for (int i = 0; i < C / 16; ++i) {
             const int m = ty + 16 * i;
@@ -432,10 +432,8 @@ bwd_dkdv(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__
     {
         float acc[C / 16][DK / 16];
         zero(acc);
-        gemm<C, DK, C>(acc, [&](int m, int kk) { return ts[kk * L::LT + m]; },
-                       [&](int kk, int n) { return fq[kk * L::LQ + n]; });
-        gemm<C, DK, DV>(acc, [&](int m, int kk) { return vs[m * L::LV + kk]; },
-                        [&](int kk, int n) { return st[n * L::LV + kk]; });
+        gemm<C, DK, C>(acc, KCol{ts, L::LT}, KCol{fq, L::LQ});
+        gemm<C, DK, DV>(acc, KRow{vs, L::LV}, KRow{st, L::LV});
 #pragma unroll
         for (int i = 0; i < C / 16; ++i) {
             const int m = ty + 16 * i;
@@ -463,7 +461,7 @@ la_status launch_backward(const BackwardProblem &p)
     if (st != LA_OK) return st;
     float *buf = (float *)scratch.ptr, *dnbuf = buf + state_floats;
     const int smem = (int)L::kBytes;
-    st = ensure_smem((const void *)bwd_chunk_state<T, DK, DV>, smem);
+    st = ensure_smem((const void *)bwd_chunk_state<T, DK, DV>, (int)L::kStateBytes);
     if (st == LA_OK) st = ensure_smem((const void *)bwd_dq<T, DK, DV>, smem);
     if (st == LA_OK) st = ensure_smem((const void *)bwd_dkdv<T, DK, DV>, smem);
     if (st != LA_OK) return st;
@@ -471,7 +469,8 @@ la_status launch_backward(const BackwardProblem &p)
     const long long total = (long long)p.BH * CH::E;
     const unsigned scan_blocks = (unsigned)((total + kThreads - 1) / kThreads);
     count_launches(5);
-    bwd_chunk_state<T, DK, DV><<<grid, kThreads, smem, p.stream>>>((const T *)p.k, (const T *)p.v, buf, p.N);
+    bwd_chunk_state<T, DK, DV><<<grid, kThreads, L::kStateBytes, p.stream>>>((const T *)p.k, (const T *)p.v, buf,
+                                                                             p.N);
     bwd_scan<<<scan_blocks, kThreads, 0, p.stream>>>(buf, nC, CH::E, total, 0);
     bwd_dq<T, DK, DV><<<grid, kThreads, smem, p.stream>>>((const T *)p.q, (const T *)p.k, (const T *)p.v,
                                                           (const T *)p.dout, (T *)p.dq, buf, dnbuf, p.N, p.eps);
