@@ -637,4 +637,19 @@ def pin_favor_positive_and_scale(orc):
     assert np.all(a > 0) and _rel_err(b[:, :3], a / 2.0) < 1e-15
 
 
+def pin_favor_attention_zero_projection(orc):
+    """W = 0: phi(q) . phi(k) = exp(-|q|^2 / 2) exp(-|k|^2 / 2), so the query factor cancels
+    and the FAVOR+ forms are the key-weighted averages o_i = sum_j a_j v_j / sum_j a_j with
+    a_j = exp(-|k_j|^2 / 2), over j <= i (causal) or all j (non-causal)."""
+    rng = np.random.default_rng(4020)
+    N, d, dv, m = 9, 3, 2, 4
+    q, k, v = rng.standard_normal((N, d)) * 0.5, rng.standard_normal((N, d)) * 0.5, rng.standard_normal((N, dv))
+    W = np.zeros((m, d))
+    a = np.exp(-0.5 * (k ** 2).sum(-1))
+    causal = np.cumsum(a[:, None] * v, 0) / np.cumsum(a)[:, None]
+    full = np.broadcast_to((a[:, None] * v).sum(0) / a.sum(), (N, dv))
+    assert _rel_err(orc.causal_favor(q, k, v, W), causal) < 1e-14
+    assert _rel_err(orc.noncausal_favor(q, k, v, W), full) < 1e-14
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]
