@@ -9,8 +9,10 @@ output buffer sets are rotated (537 MB > 4x the 129 MB L2) so every step reads
 q, k, v from HBM.
 
 Also reported ("paths"): the long causal forward (B=1 H=32 N=65536 d=128),
-the non-causal forward (B=8 H=12 N=4096 d=64) and the decode step (128 x 32
-heads, d=128, fp32 state), each with its roofline fraction.
+the non-causal forward (B=8 H=12 N=4096 d=64), the decode step (128 x 32
+heads, d=128, fp32 state) and its prefill state, the decayed-state and
+feature-map variants, the backward pass, and FAVOR+ (features alone, causal,
+non-causal and decode), each with its roofline fraction.
 
 `--impl reference` times the float64 CPU oracle (the only reference this
 method has) on a bounded sample of the same workload, on the host cores.
