@@ -104,6 +104,7 @@ def test_causal_favor(orc, dtype, B, H, N, d, dv, m, chunk):
 @pytest.mark.parametrize("dtype,B,H,N,d,dv,m", [
     ("bf16", 2, 3, 1000, 64, 64, 64), ("bf16", 1, 4, 3000, 128, 128, 128), ("bf16", 2, 2, 500, 64, 128, 128),
     ("bf16", 2, 3, 300, 64, 32, 128), ("f32", 2, 3, 300, 64, 64, 64),
+    ("bf16", 8, 12, 4096, 64, 64, 64),  # the benchmark's FAVOR+ non-causal workload
 ])
 def test_noncausal_favor(orc, dtype, B, H, N, d, dv, m):
     q, k, v, w = inputs(23000 + N + d + dv + m, B, H, N, d, dv, m, dtype)
