@@ -627,6 +627,18 @@ def pin_favor_unit_projection(orc):
     assert abs(got - math.exp(0.3 - 0.5 * (0.09 + 0.04 + 0.49 + 1.21))) < 1e-15
 
 
+def pin_favor_coordinate_projections(orc):
+    """Rows of W that pick single coordinates, in a non-square order (m = 2, d = 3):
+    phi(x)_0 = exp(x_2 - |x|^2 / 2) / sqrt(2), phi(x)_1 = exp(-x_0 - |x|^2 / 2) / sqrt(2)."""
+    x = np.array([[0.4, -0.3, 1.2], [-0.8, 0.5, 0.1]])
+    W = np.array([[0.0, 0.0, 1.0], [-1.0, 0.0, 0.0]])
+    got = orc.favor_features(x, W)
+    for i in range(2):
+        h = 0.5 * float(x[i] @ x[i])
+        assert abs(got[i, 0] - math.exp(x[i, 2] - h) / math.sqrt(2.0)) < 1e-15
+        assert abs(got[i, 1] - math.exp(-x[i, 0] - h) / math.sqrt(2.0)) < 1e-15
+
+
 def pin_favor_positive_and_scale(orc):
     """Features are positive, and scaling m by 4 with repeated rows divides each by 2."""
     rng = np.random.default_rng(4010)

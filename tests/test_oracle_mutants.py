@@ -70,6 +70,9 @@ MUTANTS = {
     "favor_drops_norm_term": ("out[i * m + r] = exp(dot - 0.5 * nrm) / sqrt((double)m);", "out[i * m + r] = exp(dot) / sqrt((double)m);"),
     "favor_norm_sign": ("out[i * m + r] = exp(dot - 0.5 * nrm) / sqrt((double)m);", "out[i * m + r] = exp(dot + 0.5 * nrm) / sqrt((double)m);"),
     "favor_no_sqrt_m": ("out[i * m + r] = exp(dot - 0.5 * nrm) / sqrt((double)m);", "out[i * m + r] = exp(dot - 0.5 * nrm) / (double)m;"),
+    # W [m, d] read as if stored [d, m] (a transposed operand)
+    "favor_transposed_projection": ("dot += W[(size_t)r * d + c] * load(x, type, i * d + c);",
+                                    "dot += W[(size_t)c * m + r] * load(x, type, i * d + c);"),
 }
 
 
