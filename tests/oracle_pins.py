@@ -664,4 +664,112 @@ def pin_favor_attention_zero_projection(orc):
     assert _rel_err(orc.noncausal_favor(q, k, v, W), full) < 1e-14
 
 
+# ----------------------------------------------------------------------------
+# Identities and special cases that reach the decode, prefix-state and backward
+# forms from a second direction
+# ----------------------------------------------------------------------------
+def _phi_elu1(x):
+    return np.where(x > 0, x + 1.0, np.exp(np.minimum(x, 0.0)))
+
+
+def pin_backward_homogeneity(orc):
+    """Where the clamp does not bind, o_i does not change when phi(q_i) is scaled, nor when
+    every phi(k_j) is scaled by one factor, and o is linear in V.  By Euler's theorem on
+    homogeneous functions: sum_r dphi(q_i)_r phi(q_i)_r = 0 for each i,
+    sum_{j,r} dphi(k_j)_r phi(k_j)_r = 0, and sum_j v_j . dv_j = sum_i dO_i . o_i.  With
+    dq = dphi(q) phi'(q), phi / phi' is x + 1 for x > 0 and 1 for x <= 0."""
+    rng = np.random.default_rng(4030)
+    N, dk, dv = 40, 5, 3
+    q, k = rng.standard_normal((N, dk)), rng.standard_normal((N, dk))
+    v, dout = rng.standard_normal((N, dv)), rng.standard_normal((N, dv))
+    gq, gk, gv = orc.causal_backward(q, k, v, dout)
+
+    def ratio(x):
+        return np.where(x > 0, x + 1.0, 1.0)
+
+    tq, tk = gq * ratio(q), gk * ratio(k)
+    assert np.max(np.abs(tq.sum(-1))) <= 1e-12 * np.max(np.abs(tq).sum(-1))
+    assert abs(tk.sum()) <= 1e-12 * np.abs(tk).sum()
+    lhs, rhs = float((v * gv).sum()), float((dout * orc.causal_recurrent(q, k, v)).sum())
+    assert abs(lhs - rhs) <= 1e-12 * max(abs(rhs), 1.0)
+
+
+def pin_decode_from_zero_state_returns_v(orc):
+    """From a zero state a step sees its own key only, so o = v for any q (the first-row case
+    o_0 = v_0): the plain step, the decayed step for any gamma, and the general step."""
+    rng = np.random.default_rng(4040)
+    H, dk, dv = 3, 4, 2
+    q, k, v = rng.standard_normal((H, dk)) * 0.5, rng.standard_normal((H, dk)) * 0.5, rng.standard_normal((H, dv))
+    steps = [lambda S, z: orc.decode_step(S, z, q, k, v),
+             lambda S, z: orc.decode_step_decay(S, z, q, k, v, np.array([0.0, 0.5, 1.0])),
+             lambda S, z: orc.decode_step_general(S, z, q, k, v, fmap="relu", shift=0.5),
+             lambda S, z: orc.decode_step_general(S, z, q, k, v, gamma=np.array([0.9, 0.5, 0.1]))]
+    for step in steps:
+        S, z = np.zeros((H, dk, dv)), np.zeros((H, dk))
+        assert _rel_err(step(S, z), v) < 1e-14
+
+
+def pin_decode_decay_zero_wipes_state(orc):
+    """gamma = 0 forgets the state before the token: o = v from any state, decayed and general."""
+    rng = np.random.default_rng(4050)
+    H, dk, dv = 2, 3, 4
+    q, k, v = rng.standard_normal((H, dk)) * 0.5, rng.standard_normal((H, dk)) * 0.5, rng.standard_normal((H, dv))
+    for general in (False, True):
+        S = np.ascontiguousarray(rng.standard_normal((H, dk, dv)))
+        z = np.ascontiguousarray(np.abs(rng.standard_normal((H, dk))) + 1.0)
+        o = (orc.decode_step_general(S, z, q, k, v, gamma=np.zeros(H)) if general
+             else orc.decode_step_decay(S, z, q, k, v, np.zeros(H)))
+        assert _rel_err(o, v) < 1e-14
+
+
+def pin_decode_two_tokens_bruteforce(orc):
+    """Two steps from a zero state against the two weights written out:
+    o_1 = (g a_0 v_0 + a_1 v_1) / (g a_0 + a_1), a_j = phi(q_1) . phi(k_j), for elu + 1 (g = 1),
+    ReLU + 1/4 and a decay g = 0.6."""
+    rng = np.random.default_rng(4060)
+    dk, dv = 3, 2
+    q, k, v = rng.standard_normal((2, dk)), rng.standard_normal((2, dk)), rng.standard_normal((2, dv))
+    cases = [("elu1", 0.0, None), ("relu", 0.25, None), ("elu1", 0.0, 0.6)]
+    for fmap, shift, g in cases:
+        phi = _phi_elu1 if fmap == "elu1" else (lambda x: np.maximum(x, 0.0) + shift)
+        a = [float(phi(q[1]) @ phi(k[j])) for j in range(2)]
+        w0 = a[0] * (1.0 if g is None else g)
+        ref = (w0 * v[0] + a[1] * v[1]) / (w0 + a[1])
+        S, z = np.zeros((1, dk, dv)), np.zeros((1, dk))
+        gam = None if g is None else np.array([g])
+        for t in range(2):
+            o = orc.decode_step_general(S, z, q[t][None], k[t][None], v[t][None], gamma=gam, fmap=fmap,
+                                        shift=shift)
+        assert _rel_err(o[0], ref) < 1e-13, (fmap, g)
+
+
+def pin_prefill_decay_zero_keeps_last_token(orc):
+    """gamma = 0: after N tokens the state holds the last token only, S = phi(k)v^T, z = phi(k)."""
+    rng = np.random.default_rng(4070)
+    H, N, dk, dv = 2, 5, 3, 4
+    k, v = rng.standard_normal((H, N, dk)), rng.standard_normal((H, N, dv))
+    S, z = orc.prefill_state_general(k, v, gamma=np.zeros(H))
+    fk = _phi_elu1(k[:, -1])
+    assert _rel_err(S, fk[:, :, None] * v[:, -1][:, None, :]) < 1e-15
+    assert _rel_err(z, fk) < 1e-15
+
+
+def pin_bf16_known_values_first_row(orc):
+    """bf16 bit patterns of known values reach the output unchanged through o_0 = v_0:
+    0x3FC0 = 1.5, 0xC000 = -2.0, 0x3E20 = 0.15625, 0xBF80 = -1.0."""
+    v = np.array([[[0x3FC0, 0xC000], [0x3E20, 0xBF80]]], dtype=np.uint16)  # [1, N=2, dv=2]
+    qk = np.array([[[0x3F80], [0x3F00]]], dtype=np.uint16)                 # 1.0 and 0.5, dk = 1
+    o = orc.causal_recurrent(qk, qk, v, EPS)
+    assert o[0, 0, 0] == 1.5 and o[0, 0, 1] == -2.0
+
+
+def pin_decay_quadratic_forms(orc):
+    """The decayed quadratic companion form: gamma = 0 keeps only the current token
+    (o = v), and for gamma in (0, 1) it agrees with the decayed recurrence."""
+    q, k, v = _rand(1080, 2, 25, 3, 2)
+    assert _rel_err(orc.causal_decay_quadratic(q, k, v, np.zeros(2), EPS), v) < 1e-14
+    g = np.array([0.7, 0.95])
+    assert _rel_err(orc.causal_decay_quadratic(q, k, v, g, EPS), orc.causal_decay_recurrent(q, k, v, g, EPS)) < 1e-12
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]
