@@ -32,7 +32,9 @@
  *    for give LA_ERR_UNSUPPORTED (see each function).
  *  - o must not overlap q, k or v.
  *  - Scratch memory.  The bf16 tensor-core forward paths keep two workspaces
- *    per (device, stream): 64 KB of work tickets and flags, zeroed once and
+ *    per (device, stream) -- the per-thread default stream
+ *    (cudaStreamPerThread) of each host thread has its own -- : 64 KB of work
+ *    tickets and flags, zeroed once and
  *    left zeroed by every launch, and a data buffer (split partials,
  *    published states) grown to the largest problem seen on that stream.
  *    Both are created or grown only outside stream capture, with cudaMalloc,
@@ -122,14 +124,23 @@ la_status la_forward_noncausal(const void *q, const void *k, const void *v, void
  *
  * Its scratch (the per-head S and z sums, B*H*dk*(dv+1) floats) lives in one
  * array of LA_NOALLOC_SCRATCH_BYTES bytes compiled into the library; every GPU
- * that loads the library holds that array until the process exits.  Problems
+ * on which this part of the library has been loaded (see below) holds that
+ * array until the process exits.  Problems
  * needing more than LA_NOALLOC_SCRATCH_BYTES bytes of scratch are rejected
  * with LA_ERR_UNSUPPORTED before any work is enqueued.
  *
- * The first call on a device looks up the array's device address
- * (cudaGetSymbolAddress, with that device current) and caches it; make that
- * first call before any stream capture.  All calls share the one array, and
- * each call clears the part it uses before accumulating into it, so calls
+ * The first call on a device that has work to do sets up: it looks up the
+ * array's device address (cudaGetSymbolAddress, with that device current) and
+ * caches it.  Under CUDA's lazy module loading (the default) the first calls
+ * also load this part of the library onto the device -- the array when its
+ * address is looked up, and each kernel when it is first launched (one pair
+ * of kernels per dtype and dk) -- and loading is a device allocation.  So,
+ * on each device, make one call of every dtype and dk you will use before
+ * reserving the rest of device memory for a pool and before any stream
+ * capture; later calls allocate nothing.  (A process may instead set
+ * CUDA_MODULE_LOADING=EAGER, which loads everything when its CUDA context is
+ * created.)  All calls share the one
+ * array, and each call clears the part it uses before accumulating into it, so calls
  * whose work may overlap on the GPU (different streams, different host
  * threads) race with each other and must be serialised by the caller.
  */
@@ -382,6 +393,28 @@ int la_last_cuda_error(void);
  * wait since the last call, LA_OK otherwise (LA_ERR_CUDA if the read failed).
  */
 la_status la_get_device_status(la_stream_t stream);
+
+/*
+ * Hooks for the library's own failure-detection tests -- not for production use.
+ * They act on the chunk-parallel causal kernel (bf16, dk = dv = 64, chunk 128,
+ * elu + 1 with the normaliser, no decay, 16 or more heads in total), whose work
+ * items publish per-chunk states that later items wait for.  Both settings are
+ * process-wide and apply to launches made after the call.
+ *
+ * la_test_set_wait_limit_ns(ns): every bounded wait of that kernel gives up after
+ * ns nanoseconds instead of 2 s (0 restores 2 s).  A wait that gives up records
+ * LA_ERR_TIMEOUT for la_get_device_status() and raises the launch's abort word, so
+ * every CTA of the launch stops taking work, drains its copies and tensor-core
+ * operations in flight, frees its tensor memory and exits; the outputs of that
+ * launch are then undefined, and the next launch starts clean.
+ *
+ * la_test_drop_publication(t): the work item with ticket t (ticket t is chunk
+ * t / (B*H) of sequence t % (B*H)) computes as usual but never publishes its
+ * chunk state, so the later chunks of its sequence wait until their limit runs
+ * out -- a lost message, made on purpose.  -1 turns it off.
+ */
+void la_test_set_wait_limit_ns(unsigned long long ns);
+void la_test_drop_publication(long long ticket);
 
 /* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
 int la_version(void);
