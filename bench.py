@@ -853,6 +853,18 @@ def run_gpu(args, dist):
     e2e_steps = max(10, min(args.steps, 200))
     e2e_value = whole_job_throughput(dist.world, w.B * w.N, e2e_steps, dist.max(e2e_secs))
 
+    # The headline again over a window of >= 200 ms (the same graphs replayed), so
+    # that the clock record has samples inside the timed region.
+    window = None
+    if not args.headline_only and args.window_steps > 0:
+        s3 = ClockSampler(gpu_index=torch.cuda.current_device()) if dist.rank == 0 else None
+        wsecs, _, _, _, wclocks = bench_causal_headline(torch, la, w, args.window_steps, args.warmup, dist, peaks,
+                                                        src, s3)
+        wt = dist.max(wsecs) / args.window_steps
+        window = {"steps": args.window_steps, "seconds": round(dist.max(wsecs), 4), "ms_per_step": round(wt * 1e3, 5),
+                  "value": round(whole_job_throughput(dist.world, w.B * w.N, args.window_steps, dist.max(wsecs)), 1),
+                  "frac": roofline(fl, nbytes, wt, peaks, src)["frac"], "clocks": wclocks}
+
     paths = {}
     if not args.headline_only:
         s2 = ClockSampler(gpu_index=torch.cuda.current_device(), period_ms=100).start() if dist.rank == 0 else None
@@ -896,16 +908,45 @@ def run_gpu(args, dist):
                 "d2h_bytes_per_step": int(d2h), "steps": e2e_steps,
                 "overlap": "2 device buffer sets; step i's copies in, step i-1's compute and step i-2's "
                            "copy out on three streams (pinned host buffers)"},
-        "paths": paths,
     }
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
         val, cores, desc, el = oracle_causal_sample(w, target_s=args.cpu_seconds)
         line["cpu_baseline"] = {"value": round(val, 1), "unit": "tokens/s", "cores": cores, "kind": "oracle",
                                 "sample": desc}
+    if window is not None:
+        line["headline_window"] = window
+    # Every secondary path in compact form, the gated ones (long causal, decode) last,
+    # then the three gate fractions: the end of the line is what a truncated log keeps.
+    if paths:
+        order = [n for n in paths if n not in ("causal_long", "decode", "clocks")] + ["causal_long", "decode"]
+        line["paths"] = {n: compact_path(paths[n], peaks) for n in order if n in paths}
+        if "clocks" in paths:
+            line["paths_clocks"] = paths["clocks"]
+        line["gates"] = {"causal_headline_frac": roof["frac"],
+                         "causal_long_frac": paths["causal_long"]["roofline"]["frac"],
+                         "decode_hbm_frac": paths["decode"]["roofline"]["frac"],
+                         "decode_dram_frac": compact_path(paths["decode"], peaks).get("dram_frac")}
+    if args.details and dist.rank == 0:
+        with open(args.details, "w") as f:
+            json.dump({"headline_roofline": roof, "paths": paths, "headline_window": window}, f, indent=1)
     if dist.rank == 0:
         print(json.dumps(line), flush=True)
     dist.close()
     return 0
+
+
+def compact_path(p, peaks):
+    """One secondary path in a few keys: throughput, time per step, roofline
+    fraction (of algorithmic bytes or flop) and, where an ncu capture of the
+    current kernel gives its DRAM bytes per launch, the fraction of the copy
+    bandwidth those bytes reach (`dram_frac`)."""
+    r = p["roofline"]
+    c = {"workload": p["workload"], "value": p["value"], "unit": p["unit"], "ms": p["ms_per_step"],
+         "bound": r["bound"], "frac": r["frac"]}
+    if r.get("traffic"):
+        secs = p["ms_per_step"] / 1e3
+        c["dram_frac"] = round(r["traffic"] / secs / 1e9 / peaks["hbm_gbs"], 4)
+    return c
 
 
 PROFILE_CASES = ("headline", "causal_long", "causal_long_quarter", "noncausal", "decode", "prefill_state_quarter",
@@ -1034,6 +1075,9 @@ def main():
     ap.add_argument("--path-reps", type=int, default=20, help="timed steps of the long causal path")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--window-steps", type=int, default=16384,
+                    help="steps of the second, long-window headline timing (0: skip)")
+    ap.add_argument("--details", default=None, help="write every path's full record (JSON) to this file")
     ap.add_argument("--profile-case", choices=PROFILE_CASES, default=None,
                     help="run a few plain launches of one workload (for ncu) instead of the benchmark")
     ap.add_argument("--profile-launches", type=int, default=3)
