@@ -71,6 +71,10 @@ def _declare(lib):
         "la_oracle_decode_step_general": ([P, P, P, P, P, I, P, I, D, I, P, I, I, I, D], None),
         "la_oracle_causal_backward": ([P, P, P, P, I, P, P, P, I, I, I, I, D], None),
         "la_oracle_favor_features": ([P, I, P, P, ctypes.c_longlong, I, I], None),
+        "la_oracle_causal_gated_recurrent": ([P, P, P, I, P, P, I, I, I, I, D], None),
+        "la_oracle_causal_gated_quadratic": ([P, P, P, I, P, P, I, I, I, I, D], None),
+        "la_oracle_decode_step_gated": ([P, P, P, P, P, I, P, P, I, I, I, D], None),
+        "la_oracle_prefill_state_gated": ([P, P, I, P, P, P, I, I, I, I], None),
         "la_oracle_num_threads": ([], I),
     }
     for name, (args, res) in sigs.items():
@@ -312,6 +316,68 @@ class Oracle:
                                                    self.FMAPS[fmap], float(shift), int(bool(normalize)),
                                                    _ptr(o), BH, dk, dv, float(eps))
         return o
+
+    # ---------------------------------------------------------------- gated state
+    # alpha: the per-key gate, one value in [0, 1] per (token, key feature), shaped
+    # like k ([..., N, dk]; [..., dk] for a decode step).
+    @staticmethod
+    def _alpha(alpha, shape):
+        a = np.ascontiguousarray(np.broadcast_to(np.asarray(alpha, dtype=np.float64), shape))
+        if np.any(a < 0) or np.any(a > 1) or not np.all(np.isfinite(a)):
+            raise ValueError("alpha must lie in [0, 1]")
+        return a
+
+    def _fwd_gated(self, fname, q, k, v, alpha, eps):
+        (q, k, v), t = _prep(q, k, v)
+        N, dk = q.shape[-2], q.shape[-1]
+        dv = v.shape[-1]
+        lead = q.shape[:-2]
+        if k.shape != q.shape or v.shape[:-1] != q.shape[:-1]:
+            raise ValueError("shape mismatch")
+        a = self._alpha(alpha, k.shape)
+        BH = int(np.prod(lead)) if lead else 1
+        o = np.empty(lead + (N, dv), dtype=np.float64)
+        if BH and N and dv:
+            getattr(self.lib, fname)(_ptr(q), _ptr(k), _ptr(v), t, _ptr(a), _ptr(o), BH, N, dk, dv, float(eps))
+        return o
+
+    def causal_gated_recurrent(self, q, k, v, alpha, eps=1e-6):
+        """Gated causal form: S_t = Diag(alpha_t) S_{t-1} + phi(k_t) v_t^T, z likewise."""
+        return self._fwd_gated("la_oracle_causal_gated_recurrent", q, k, v, alpha, eps)
+
+    def causal_gated_quadratic(self, q, k, v, alpha, eps=1e-6):
+        return self._fwd_gated("la_oracle_causal_gated_quadratic", q, k, v, alpha, eps)
+
+    def decode_step_gated(self, S, z, q, k, v, alpha, eps=1e-6):
+        """One gated step for every head, S and z (float64) updated in place; alpha [..., dk]."""
+        if S.dtype != np.float64 or z.dtype != np.float64 or not S.flags.c_contiguous \
+                or not z.flags.c_contiguous:
+            raise TypeError("S and z must be C-contiguous float64 (updated in place)")
+        (q, k, v), t = _prep(q, k, v)
+        dk, dv = q.shape[-1], v.shape[-1]
+        lead = q.shape[:-1]
+        BH = int(np.prod(lead)) if lead else 1
+        if S.shape != lead + (dk, dv) or z.shape != lead + (dk,):
+            raise ValueError("state shape mismatch")
+        a = self._alpha(alpha, k.shape)
+        o = np.empty(lead + (dv,), dtype=np.float64)
+        if BH:
+            self.lib.la_oracle_decode_step_gated(_ptr(S), _ptr(z), _ptr(q), _ptr(k), _ptr(v), t, _ptr(a),
+                                                 _ptr(o), BH, dk, dv, float(eps))
+        return o
+
+    def prefill_state_gated(self, k, v, alpha):
+        """S [..., dk, dv], z [..., dk] after the gated recurrence over all N tokens."""
+        (k, v), t = _prep(k, v)
+        N, dk, dv = k.shape[-2], k.shape[-1], v.shape[-1]
+        lead = k.shape[:-2]
+        BH = int(np.prod(lead)) if lead else 1
+        a = self._alpha(alpha, k.shape)
+        S = np.zeros(lead + (dk, dv), dtype=np.float64)
+        z = np.zeros(lead + (dk,), dtype=np.float64)
+        if BH:
+            self.lib.la_oracle_prefill_state_gated(_ptr(k), _ptr(v), t, _ptr(a), _ptr(S), _ptr(z), BH, N, dk, dv)
+        return S, z
 
     # ---------------------------------------------------------------- backward pass
     def causal_backward(self, q, k, v, dout, eps=1e-6):

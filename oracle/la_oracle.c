@@ -836,6 +836,173 @@ void la_oracle_favor_features(const void *x, int type, const double *W, double *
 }
 
 /* Threads OpenMP will use (reported beside CPU timings). */
+/* ---------------------------------------------------------------------------
+ * Gated state, one gate per key feature ([wiki] "What is actually lost": gated
+ * variants insert a decay, S_t = G_t (.) S_{t-1} + phi(k_t) v_t^T; [math] "RetNet
+ * and gated linear attention": S_i = Diag(alpha_i) S_{i-1} + k_i v_i^T, the decay
+ * computed from the token itself).
+ * Readings: the gate values are an input, alpha [BH, N, dk] in [0, 1] (the
+ * projection that makes them from the token is a trained layer, the caller's);
+ * G_t = alpha_t 1^T, i.e. row r of S (key feature r) is scaled by alpha_t[r];
+ * phi is applied to k as everywhere else; the normaliser z decays with the same
+ * gate (the reading taken for the scalar decay above, which this reduces to when
+ * every alpha_t[r] = gamma):
+ *   S_t = Diag(alpha_t) S_{t-1} + phi(k_t) v_t^T,  z_t = alpha_t (.) z_{t-1} + phi(k_t),
+ *   o_t = phi(q_t)^T S_t / max(phi(q_t)^T z_t, eps).
+ * ------------------------------------------------------------------------- */
+void la_oracle_causal_gated_recurrent(const void *q, const void *k, const void *v, int type,
+                                      const double *alpha, double *o, int BH, int N, int dk,
+                                      int dv, double eps)
+{
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int bh = 0; bh < BH; ++bh) {
+        double *S = calloc((size_t)dk * dv, sizeof(double));
+        double *z = calloc((size_t)dk, sizeof(double));
+        double *fq = malloc(sizeof(double) * dk);
+        double *fk = malloc(sizeof(double) * dk);
+        double *vt = malloc(sizeof(double) * dv);
+        const int64_t qb = (int64_t)bh * N * dk, vb = (int64_t)bh * N * dv;
+        for (int t = 0; t < N; ++t) {
+            phi_row(q, type, qb, t, dk, fq);
+            phi_row(k, type, qb, t, dk, fk);
+            const double *at = alpha + qb + (int64_t)t * dk;
+            for (int c = 0; c < dv; ++c)
+                vt[c] = load(v, type, vb + (int64_t)t * dv + c);
+            /* S = Diag(alpha_t) S + phi(k_t) v_t^T ; z = alpha_t (.) z + phi(k_t) */
+            for (int r = 0; r < dk; ++r) {
+                double *Sr = S + (size_t)r * dv;
+                for (int c = 0; c < dv; ++c)
+                    Sr[c] = at[r] * Sr[c] + fk[r] * vt[c];
+                z[r] = at[r] * z[r] + fk[r];
+            }
+            double den = 0.0;
+            for (int r = 0; r < dk; ++r)
+                den += fq[r] * z[r];
+            double *ot = o + vb + (int64_t)t * dv;
+            for (int c = 0; c < dv; ++c)
+                ot[c] = 0.0;
+            for (int r = 0; r < dk; ++r) {
+                const double *Sr = S + (size_t)r * dv;
+                for (int c = 0; c < dv; ++c)
+                    ot[c] += fq[r] * Sr[c];
+            }
+            den = clamp_den(den, eps);
+            for (int c = 0; c < dv; ++c)
+                ot[c] /= den;
+        }
+        free(S); free(z); free(fq); free(fk); free(vt);
+    }
+}
+
+/* The weighted pairwise form the gated recurrence unrolls to: key j reaches query
+ * i >= j through feature r with weight prod_{s=j+1..i} alpha_s[r], so
+ *   w_ij = sum_r phi(q_i)[r] phi(k_j)[r] prod_{s=j+1..i} alpha_s[r],
+ *   o_i = sum_{j<=i} w_ij v_j / max(sum_{j<=i} w_ij, eps).
+ * The products are built going back from j = i (empty product 1).  O(N^2 dk):
+ * cross-check only. */
+void la_oracle_causal_gated_quadratic(const void *q, const void *k, const void *v, int type,
+                                      const double *alpha, double *o, int BH, int N, int dk,
+                                      int dv, double eps)
+{
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int bh = 0; bh < BH; ++bh) {
+        double *fq = malloc(sizeof(double) * dk);
+        double *fk = malloc(sizeof(double) * dk);
+        double *prod = malloc(sizeof(double) * dk);
+        const int64_t qb = (int64_t)bh * N * dk, vb = (int64_t)bh * N * dv;
+        for (int i = 0; i < N; ++i) {
+            phi_row(q, type, qb, i, dk, fq);
+            double *oi = o + vb + (int64_t)i * dv;
+            for (int c = 0; c < dv; ++c)
+                oi[c] = 0.0;
+            for (int r = 0; r < dk; ++r)
+                prod[r] = 1.0;
+            double rowsum = 0.0;
+            for (int j = i; j >= 0; --j) {
+                if (j < i)
+                    for (int r = 0; r < dk; ++r)
+                        prod[r] *= alpha[qb + (int64_t)(j + 1) * dk + r];
+                phi_row(k, type, qb, j, dk, fk);
+                double w = 0.0;
+                for (int r = 0; r < dk; ++r)
+                    w += fq[r] * fk[r] * prod[r];
+                rowsum += w;
+                for (int c = 0; c < dv; ++c)
+                    oi[c] += w * load(v, type, vb + (int64_t)j * dv + c);
+            }
+            rowsum = clamp_den(rowsum, eps);
+            for (int c = 0; c < dv; ++c)
+                oi[c] /= rowsum;
+        }
+        free(fq); free(fk); free(prod);
+    }
+}
+
+/* One gated decode step, state in place: S = Diag(alpha) S + phi(k) v^T,
+ * z = alpha (.) z + phi(k), then o = phi(q)^T S / max(phi(q)^T z, eps).
+ * alpha [BH, dk]. */
+void la_oracle_decode_step_gated(double *S, double *z, const void *q, const void *k,
+                                 const void *v, int type, const double *alpha, double *o, int BH,
+                                 int dk, int dv, double eps)
+{
+#pragma omp parallel for schedule(static)
+    for (int bh = 0; bh < BH; ++bh) {
+        double *Sb = S + (size_t)bh * dk * dv;
+        double *zb = z + (size_t)bh * dk;
+        double *ob = o + (size_t)bh * dv;
+        const double *ab = alpha + (size_t)bh * dk;
+        double *fq = malloc(sizeof(double) * dk);
+        double *fk = malloc(sizeof(double) * dk);
+        for (int r = 0; r < dk; ++r) {
+            fq[r] = la_oracle_phi(load(q, type, (int64_t)bh * dk + r));
+            fk[r] = la_oracle_phi(load(k, type, (int64_t)bh * dk + r));
+        }
+        for (int r = 0; r < dk; ++r) {
+            for (int c = 0; c < dv; ++c)
+                Sb[(size_t)r * dv + c] = ab[r] * Sb[(size_t)r * dv + c] + fk[r] * load(v, type, (int64_t)bh * dv + c);
+            zb[r] = ab[r] * zb[r] + fk[r];
+        }
+        double den = 0.0;
+        for (int r = 0; r < dk; ++r)
+            den += fq[r] * zb[r];
+        den = clamp_den(den, eps);
+        for (int c = 0; c < dv; ++c) {
+            double s = 0.0;
+            for (int r = 0; r < dk; ++r)
+                s += fq[r] * Sb[(size_t)r * dv + c];
+            ob[c] = s / den;
+        }
+        free(fq); free(fk);
+    }
+}
+
+/* State after N tokens of the gated recurrence from a zero state (a prefill):
+ * S = sum_t Diag(prod_{s=t+1..N-1} alpha_s) phi(k_t) v_t^T, z likewise, written as
+ * the recurrence itself.  S [BH, dk, dv] and z [BH, dk] are overwritten. */
+void la_oracle_prefill_state_gated(const void *k, const void *v, int type, const double *alpha,
+                                   double *S, double *z, int BH, int N, int dk, int dv)
+{
+#pragma omp parallel for schedule(static)
+    for (int bh = 0; bh < BH; ++bh) {
+        double *Sb = S + (size_t)bh * dk * dv;
+        double *zb = z + (size_t)bh * dk;
+        double *fk = malloc(sizeof(double) * dk);
+        const int64_t kb = (int64_t)bh * N * dk, vb = (int64_t)bh * N * dv;
+        memset(Sb, 0, sizeof(double) * dk * dv);
+        memset(zb, 0, sizeof(double) * dk);
+        for (int t = 0; t < N; ++t) {
+            phi_row(k, type, kb, t, dk, fk);
+            const double *at = alpha + kb + (int64_t)t * dk;
+            for (int r = 0; r < dk; ++r) {
+                for (int c = 0; c < dv; ++c)
+                    Sb[(size_t)r * dv + c] = at[r] * Sb[(size_t)r * dv + c] + fk[r] * load(v, type, vb + (int64_t)t * dv + c);
+                zb[r] = at[r] * zb[r] + fk[r];
+            }
+        }
+        free(fk);
+    }
+}
+
 int la_oracle_num_threads(void)
 {
 #ifdef _OPENMP

@@ -772,4 +772,139 @@ def pin_decay_quadratic_forms(orc):
     assert _rel_err(orc.causal_decay_quadratic(q, k, v, g, EPS), orc.causal_decay_recurrent(q, k, v, g, EPS)) < 1e-12
 
 
+# ----------------------------------------------------------------------------
+# gated state, one gate per key feature ("Linear Attention", What is actually lost:
+# S_t = G_t (.) S_{t-1} + phi(k_t) v_t^T; "Linear Attention -- Math + Variants",
+# RetNet and gated linear attention: S_i = Diag(alpha_i) S_{i-1} + k_i v_i^T)
+# ----------------------------------------------------------------------------
+def gated_pairwise_np(q, k, v, alpha, eps=EPS):
+    """w_ij = sum_r phi(q_i)[r] phi(k_j)[r] prod_{s=j+1..i} alpha_s[r] for j <= i, by
+    cumulative sums of log(alpha) in numpy (a gate of 0 handled by counting zeros),
+    o_i = sum_j w_ij v_j / max(sum_j w_ij, eps).  Dense, float64."""
+    fq, fk = phi_np(q), phi_np(k)
+    a = np.asarray(alpha, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    zero = (a == 0.0)
+    la = np.log(np.where(zero, 1.0, a))
+    L = np.cumsum(la, axis=-2)                      # L_i = sum_{s<=i} log alpha_s
+    Z = np.cumsum(zero, axis=-2)                    # zeros among alpha_0..alpha_i
+    N = q.shape[-2]
+    out = np.empty(q.shape[:-1] + (v.shape[-1],))
+    for i in range(N):
+        # prod_{s=j+1..i} alpha_s = exp(L_i - L_j), zero if a gate in (j, i] is zero
+        dec = np.exp(L[..., i:i + 1, :] - L[..., :i + 1, :])
+        dec = np.where((Z[..., i:i + 1, :] - Z[..., :i + 1, :]) > 0, 0.0, dec)
+        w = np.einsum("...r,...jr->...j", fq[..., i, :], fk[..., :i + 1, :] * dec)
+        den = np.maximum(w.sum(-1, keepdims=True), eps)
+        out[..., i, :] = np.einsum("...j,...jc->...c", w, v[..., :i + 1, :]) / den
+    return out
+
+
+def _gate(seed, shape, lo=0.3):
+    return np.random.default_rng(seed).uniform(lo, 1.0, size=shape)
+
+
+def pin_gated_equals_numpy_pairwise(orc):
+    """The gated recurrence and the oracle's own pairwise form equal the numpy form
+    above (dk != dv; gates in [0.3, 1), a few exactly 0 and 1)."""
+    q, k, v = _rand(1100, 3, 40, 5, 3)
+    a = _gate(1101, k.shape)
+    a[0, 7, :] = 0.0
+    a[1, 3, 2] = 0.0
+    a[2, :, 4] = 1.0
+    ref = gated_pairwise_np(q, k, v, a)
+    assert _rel_err(orc.causal_gated_recurrent(q, k, v, a, EPS), ref) < 1e-12
+    assert _rel_err(orc.causal_gated_quadratic(q, k, v, a, EPS), ref) < 1e-12
+
+
+def pin_gated_constant_gate_is_scalar_decay(orc):
+    """alpha_t[r] = gamma for every token and feature reduces to the (pinned) scalar
+    decay of each head."""
+    q, k, v = _rand(1110, 4, 30, 4, 6)
+    g = np.array([1.0, 0.9, 0.5, 0.0])
+    a = np.broadcast_to(g[:, None, None], k.shape)
+    assert _rel_err(orc.causal_gated_recurrent(q, k, v, a, EPS), orc.causal_decay_recurrent(q, k, v, g, EPS)) < 1e-13
+
+
+def pin_gated_one_is_undecayed_and_zero_returns_v(orc):
+    q, k, v = _rand(1120, 2, 25, 5, 4)
+    assert _rel_err(orc.causal_gated_recurrent(q, k, v, np.ones(k.shape), EPS),
+                    pairwise_bruteforce(q, k, v, causal=True)) < 1e-12
+    assert _rel_err(orc.causal_gated_recurrent(q, k, v, np.zeros(k.shape), EPS), v) < 1e-14
+
+
+def pin_gated_exact_rational(orc):
+    """Tiny inputs with q, k > 0 (phi = x + 1 exact) and gates in {1/4, 1/2, 3/4, 1},
+    one per (token, feature), against exact rational arithmetic of the unrolled form."""
+    rng = np.random.default_rng(1130)
+    N, dk, dv = 6, 3, 2
+    qv = rng.integers(1, 8, size=(N, dk)) / 8.0
+    kv = rng.integers(1, 8, size=(N, dk)) / 8.0
+    vv = rng.integers(-8, 9, size=(N, dv)) / 4.0
+    av = rng.integers(1, 5, size=(N, dk)) / 4.0
+    got = orc.causal_gated_recurrent(qv[None], kv[None], vv[None], av[None], 0.0)[0]
+    fr = lambda x: Fraction(x).limit_denominator(64)
+    fq = [[fr(x) + 1 for x in row] for row in qv]
+    fk = [[fr(x) + 1 for x in row] for row in kv]
+    vf = [[fr(x) for x in row] for row in vv]
+    af = [[fr(x) for x in row] for row in av]
+    for i in range(N):
+        num = [Fraction(0)] * dv
+        den = Fraction(0)
+        for j in range(i + 1):
+            w = Fraction(0)
+            for r in range(dk):
+                p = Fraction(1)
+                for s_ in range(j + 1, i + 1):
+                    p *= af[s_][r]
+                w += fq[i][r] * fk[j][r] * p
+            den += w
+            for c in range(dv):
+                num[c] += w * vf[j][c]
+        for c in range(dv):
+            assert abs(got[i, c] - float(num[c] / den)) <= 1e-14 * max(1.0, abs(float(num[c] / den)))
+
+
+def pin_gated_gate_acts_per_key_feature(orc):
+    """A gate that closes feature 0 only (alpha[:, 0] = 0, the rest 1) leaves the
+    other features' history untouched: the output equals the ungated form computed
+    with feature 0 of every earlier key removed from the weights."""
+    q, k, v = _rand(1140, 2, 20, 4, 3)
+    a = np.ones(k.shape)
+    a[..., 0] = 0.0
+    fq, fk = phi_np(q), phi_np(k)
+    N = q.shape[-2]
+    ref = np.empty(v.shape)
+    for i in range(N):
+        w = np.einsum("br,bjr->bj", fq[:, i, 1:], fk[:, :i + 1, 1:])
+        w[:, i] += fq[:, i, 0] * fk[:, i, 0]           # feature 0 of the current key only
+        ref[:, i] = np.einsum("bj,bjc->bc", w, v[:, :i + 1]) / np.maximum(w.sum(-1), EPS)[:, None]
+    assert _rel_err(orc.causal_gated_recurrent(q, k, v, a, EPS), ref) < 1e-12
+
+
+def pin_gated_decode_and_prefill_continue_causal(orc):
+    """Gated decode steps from a zero state reproduce the gated causal forward at
+    every position; the gated prefill state over a prefix, continued by decode
+    steps, does too; and the prefill state equals the numpy sum of its terms."""
+    BH, N, P, dk, dv = 3, 18, 7, 5, 4
+    q, k, v = _rand(1150, BH, N, dk, dv)
+    a = _gate(1151, k.shape)
+    full = gated_pairwise_np(q, k, v, a)
+    S = np.zeros((BH, dk, dv))
+    z = np.zeros((BH, dk))
+    for t in range(N):
+        o = orc.decode_step_gated(S, z, q[:, t], k[:, t], v[:, t], a[:, t], EPS)
+        assert _rel_err(o, full[:, t]) < 1e-12, t
+    S, z = orc.prefill_state_gated(k[:, :P], v[:, :P], a[:, :P])
+    fk = phi_np(k[:, :P])
+    dec = np.ones((BH, P, dk))
+    for t in range(P):
+        dec[:, t] = np.prod(a[:, t + 1:P], axis=1)
+    assert _rel_err(S, np.einsum("btr,btc->brc", fk * dec, v[:, :P])) < 1e-12
+    assert _rel_err(z, (fk * dec).sum(1)) < 1e-12
+    for t in range(P, N):
+        o = orc.decode_step_gated(S, z, q[:, t], k[:, t], v[:, t], a[:, t], EPS)
+        assert _rel_err(o, full[:, t]) < 1e-12, t
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

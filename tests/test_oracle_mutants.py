@@ -66,6 +66,17 @@ MUTANTS = {
     "backward_phi_prime_constant": ("    return x > 0.0 ? 1.0 : exp(x);", "    return 1.0;"),
     "backward_dv_from_q": ("s += R[(size_t)r * dvd + c] * fk[r];", "s += R[(size_t)r * dvd + c] * fq[r];"),
     "backward_dq_sign": ("double s = dd[t] * z[r];", "double s = -dd[t] * z[r];"),
+    # gated state (one gate per key feature)
+    "gated_z_ungated": ("z[r] = at[r] * z[r] + fk[r];", "z[r] = z[r] + fk[r];"),
+    "gated_gate_after_update": ("Sr[c] = at[r] * Sr[c] + fk[r] * vt[c];", "Sr[c] = at[r] * (Sr[c] + fk[r] * vt[c]);"),
+    "gated_gate_of_previous_token": ("const double *at = alpha + qb + (int64_t)t * dk;",
+                                     "const double *at = alpha + qb + (int64_t)(t > 0 ? t - 1 : 0) * dk;"),
+    "gated_gate_on_value_axis": ("Sr[c] = at[r] * Sr[c] + fk[r] * vt[c];", "Sr[c] = at[c % dk] * Sr[c] + fk[r] * vt[c];"),
+    "gated_quadratic_gate_index_off": ("prod[r] *= alpha[qb + (int64_t)(j + 1) * dk + r];",
+                                       "prod[r] *= alpha[qb + (int64_t)j * dk + r];"),
+    "gated_decode_z_uses_q": ("zb[r] = ab[r] * zb[r] + fk[r];", "zb[r] = ab[r] * zb[r] + fq[r];"),
+    "gated_prefill_ungated": ("Sb[(size_t)r * dv + c] = at[r] * Sb[(size_t)r * dv + c] + fk[r]",
+                              "Sb[(size_t)r * dv + c] = Sb[(size_t)r * dv + c] + fk[r]"),
     # FAVOR+ features
     "favor_drops_norm_term": ("out[i * m + r] = exp(dot - 0.5 * nrm) / sqrt((double)m);", "out[i * m + r] = exp(dot) / sqrt((double)m);"),
     "favor_norm_sign": ("out[i * m + r] = exp(dot - 0.5 * nrm) / sqrt((double)m);", "out[i * m + r] = exp(dot + 0.5 * nrm) / sqrt((double)m);"),
