@@ -84,6 +84,10 @@ def _declare(lib):
     lib.la_version.restype = ctypes.c_int
     lib.la_kernel_launches.argtypes = []
     lib.la_kernel_launches.restype = ctypes.c_ulonglong
+    lib.la_test_set_wait_limit_ns.argtypes = [ctypes.c_ulonglong]
+    lib.la_test_set_wait_limit_ns.restype = None
+    lib.la_test_drop_publication.argtypes = [ctypes.c_longlong]
+    lib.la_test_drop_publication.restype = None
     return lib
 
 

@@ -7,6 +7,7 @@
 #include <map>
 #include <mutex>
 #include <set>
+#include <thread>
 #include <tuple>
 #include <utility>
 
@@ -60,24 +61,38 @@ la_status ensure_smem(const void *kernel, int bytes)
     return LA_OK;
 }
 
+// Key of a stream's workspaces: the device, the stream handle and, for the
+// per-thread default stream, the host thread.  cudaStreamPerThread is one handle
+// value in every host thread but a different stream in each, so two threads
+// must not share its workspaces.  (The stream's unique id would tell streams
+// apart too, but querying it is not permitted while a stream is being captured.)
+typedef std::tuple<int, cudaStream_t, std::thread::id> StreamKey;
+static la_status stream_key(cudaStream_t s, StreamKey *key)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_status(e);
+    *key = std::make_tuple(dev, s, s == cudaStreamPerThread ? std::this_thread::get_id() : std::thread::id());
+    return LA_OK;
+}
+
 la_status flag_workspace(cudaStream_t s, size_t bytes, void **out)
 {
     *out = nullptr;
     if (bytes > kFlagWorkspaceBytes) return LA_ERR_UNSUPPORTED;
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return cuda_status(e);
+    StreamKey key;
+    la_status st = stream_key(s, &key);
+    if (st != LA_OK) return st;
     static std::mutex mu;
-    static std::map<std::pair<int, cudaStream_t>, void *> spaces;  // kept until the process exits
+    static std::map<StreamKey, void *> spaces;  // kept until the process exits
     std::lock_guard<std::mutex> lock(mu);
-    const auto key = std::make_pair(dev, s);
     auto it = spaces.find(key);
     if (it != spaces.end()) {
         *out = it->second;
         return LA_OK;
     }
     cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
-    e = cudaStreamIsCapturing(s, &cs);
+    cudaError_t e = cudaStreamIsCapturing(s, &cs);
     if (e != cudaSuccess) return cuda_status(e);
     if (cs != cudaStreamCaptureStatusNone) return LA_ERR_UNSUPPORTED;
     void *p = nullptr;
@@ -98,20 +113,19 @@ la_status data_workspace(cudaStream_t s, size_t bytes, void **out)
 {
     *out = nullptr;
     if (bytes == 0) return LA_OK;
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return cuda_status(e);
+    StreamKey key;
+    la_status st = stream_key(s, &key);
+    if (st != LA_OK) return st;
     static std::mutex mu;
-    static std::map<std::pair<int, cudaStream_t>, std::pair<void *, size_t>> spaces;
+    static std::map<StreamKey, std::pair<void *, size_t>> spaces;
     std::lock_guard<std::mutex> lock(mu);
-    const auto key = std::make_pair(dev, s);
     auto it = spaces.find(key);
     if (it != spaces.end() && it->second.second >= bytes) {
         *out = it->second.first;
         return LA_OK;
     }
     cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
-    e = cudaStreamIsCapturing(s, &cs);
+    cudaError_t e = cudaStreamIsCapturing(s, &cs);
     if (e != cudaSuccess) return cuda_status(e);
     if (cs != cudaStreamCaptureStatusNone) return LA_ERR_UNSUPPORTED;
     size_t size = it != spaces.end() ? std::max(bytes, 2 * it->second.second) : bytes;
@@ -125,6 +139,17 @@ la_status data_workspace(cudaStream_t s, size_t bytes, void **out)
     *out = p;
     return LA_OK;
 }
+
+static std::atomic<unsigned long long> g_test_wait_ns{0};
+static std::atomic<long long> g_test_drop{-1};
+constexpr unsigned long long kDefaultWaitNs = 2000000000ull;  // 2 s: far beyond any healthy wait
+
+unsigned long long test_wait_limit_ns()
+{
+    const unsigned long long v = g_test_wait_ns.load(std::memory_order_relaxed);
+    return v ? v : kDefaultWaitNs;
+}
+long long test_drop_ticket() { return g_test_drop.load(std::memory_order_relaxed); }
 
 static bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
@@ -548,10 +573,17 @@ la_status la_get_device_status(la_stream_t stream)
     if (st != LA_OK) return st;
     st = favor_read_status((cudaStream_t)stream, &fv_bits);
     if (st != LA_OK) return st;
-    return ((bits | nc_bits | fv_bits) & kStatusTimeout) ? LA_ERR_TIMEOUT : LA_OK;
+    unsigned cc_bits = 0;
+    st = tc_chunks_read_status((cudaStream_t)stream, &cc_bits);
+    if (st != LA_OK) return st;
+    return ((bits | nc_bits | fv_bits | cc_bits) & kStatusTimeout) ? LA_ERR_TIMEOUT : LA_OK;
 }
 
 int la_version(void) { return 100; }
+
+void la_test_set_wait_limit_ns(unsigned long long ns) { g_test_wait_ns.store(ns, std::memory_order_relaxed); }
+
+void la_test_drop_publication(long long ticket) { g_test_drop.store(ticket, std::memory_order_relaxed); }
 
 unsigned long long la_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
 

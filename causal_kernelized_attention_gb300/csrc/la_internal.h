@@ -77,6 +77,9 @@ la_status decode_step(float *S, float *z, const void *q, const void *k, const vo
 // Tensor-core (tcgen05) paths (la_tc_causal.cu); return LA_ERR_UNSUPPORTED when
 // the problem is outside the shapes they are built for.
 la_status causal_tc(const Problem &p);
+// Chunk-parallel causal kernel (la_tc_causal_chunks.cu): bf16, dk = dv = 64, chunk
+// 128, N >= 128, elu + 1 with the normaliser, no decay.
+la_status causal_chunks_tc(const Problem &p);
 // (la_tc_noncausal.cu)
 la_status noncausal_tc(const Problem &p);
 // S, z (fp32, [BH,D,D], [BH,D]) = sums over N tokens on the tensor cores (bf16
@@ -90,6 +93,13 @@ la_status noncausal_tc_state(const void *k, const void *v, float *S, float *z, i
 la_status tc_causal_read_status(cudaStream_t s, unsigned *bits);
 la_status tc_noncausal_read_status(cudaStream_t s, unsigned *bits);
 la_status favor_read_status(cudaStream_t s, unsigned *bits);
+la_status tc_chunks_read_status(cudaStream_t s, unsigned *bits);
+
+// Failure-detection test hooks (la_test_set_wait_limit_ns, la_test_drop_publication):
+// the limit of the chunk-parallel causal kernel's bounded waits (2 s unless a test
+// set another) and the ticket whose state that kernel does not publish (-1: none).
+unsigned long long test_wait_limit_ns();
+long long test_drop_ticket();
 
 // FAVOR+ features (la_favor.cu): oq = phi(xq) and, when xk is not null, ok =
 // phi(xk), with phi(x)_r = exp(w_r . x - |x|^2 / 2) / sqrt(m); x [BH, N, d],

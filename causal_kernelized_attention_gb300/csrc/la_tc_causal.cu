@@ -57,6 +57,7 @@ constexpr int kTmaWarp = 8, kMmaWarp = 9, kEpiPWarp0 = 10, kEpiOWarp0 = 14;
 // kPoison or more marks a segment whose CTA gave up.
 constexpr uint32_t kPublished = 8, kPoison = 1u << 20;
 constexpr int kMaxShortSegs = 32;  // segments per head in short-sequence mode
+constexpr int kChunkKernelMinHeads = 16;  // B*H from which d = 64 runs the chunk-parallel kernel
 
 // Row sums and z ride on the tensor cores in one of two ways:
 //  * fused (D = 64): the B operand of P V and of the state update is [V | 1] and
@@ -1158,6 +1159,10 @@ la_status causal_tc(const Problem &p)
         return p.dk == 128 ? launch<128, true, false>(p) : launch<64, true, false>(p);
     }
     if (var) return p.dk == 128 ? launch<128, false, true>(p) : launch<64, false, true>(p);
+    // d = 64 with enough heads: the chunk-parallel kernel (la_tc_causal_chunks.cu),
+    // whose look-back needs the chunks of one head in flight at a time (about twice
+    // the SM count divided by the heads) to fit its 32-chunk window.
+    if (p.dk == 64 && p.BH >= kChunkKernelMinHeads) return causal_chunks_tc(p);
     return p.dk == 128 ? launch<128, false, false>(p) : launch<64, false, false>(p);
 }
 

@@ -79,6 +79,39 @@ def test_causal_tensor_core_shapes(orc, B, H, N, d):
     assert e["normwise"] < 2e-2, e
 
 
+# Shapes of the chunk-parallel kernel (bf16, dk = dv = 64, chunk 128, 16 or more
+# heads in total): one chunk per head, ragged tails, fewer items than SMs, several
+# items per CTA, many one-chunk heads, and long sequences whose look-back runs
+# across many chunks of the same head in flight at once.
+@pytest.mark.parametrize("B,H,N", [
+    (2, 8, 128), (2, 8, 129), (2, 8, 1000), (1, 16, 5000), (8, 16, 300), (3, 7, 4173), (16, 16, 130),
+    (1, 16, 65536), (4, 8, 2048), (1, 17, 12345),
+])
+def test_causal_chunk_parallel_shapes(orc, B, H, N):
+    q, k, v = workloads.random_inputs(6000 + N + B * H, B, H, N, 64, 64, "bf16")
+    got = run_causal(q, k, v, "bf16", 128)
+    ref = orc.causal_recurrent(q, k, v)
+    e = assert_parity(got, ref, "bf16", (B, H, N))
+    assert e["normwise"] < 2e-2, e
+    # the late rows of long sequences are small: not a near-zero wrong answer there
+    tail = errors(got[:, :, -128:], ref[:, :, -128:])
+    assert tail["normwise"] < 2e-2, tail
+
+
+def test_causal_chunk_parallel_repeatable(orc):
+    """Which published prefix a look-back finds nearest depends on timing, so the
+    order of the fp32 additions may differ between calls: repeated calls all match
+    the oracle."""
+    q, k, v = workloads.random_inputs(6123, 4, 8, 2048, 64, 64, "bf16")
+    ref = orc.causal_recurrent(q, k, v)
+    dq, dk_, dv_ = to_dev(q, "bf16"), to_dev(k, "bf16"), to_dev(v, "bf16")
+    outs = [la().la_forward_causal(dq, dk_, dv_) for _ in range(6)]
+    torch.cuda.synchronize()
+    assert la().la_get_device_status() == 0
+    for o in outs:
+        assert_parity(from_dev(o), ref, "bf16", "repeat")
+
+
 def test_causal_output0_is_v0(orc):
     # "26. Linear (Kernelized) Attention", Step-by-Step step 6: o_0 = v_0 for any q_0.
     q, k, v = workloads.random_inputs(77, 2, 4, 130, 64, 64, "f32")
@@ -341,7 +374,8 @@ def test_flag_workspace_reused_across_shapes_and_paths(orc):
     workspace per stream, which every launch leaves cleared for the next: calls
     of different shapes and paths in a row all match the oracle, twice over."""
     cases = [("causal", 2, 3, 1000, 64), ("noncausal", 4, 40, 4173, 64), ("causal", 1, 4, 8192, 128),
-             ("noncausal", 1, 1, 128, 128), ("causal", 3, 5, 300, 64), ("noncausal", 2, 3, 9000, 128)]
+             ("noncausal", 1, 1, 128, 128), ("causal", 3, 5, 300, 64), ("noncausal", 2, 3, 9000, 128),
+             ("causal", 4, 8, 2048, 64), ("causal", 2, 9, 700, 64)]
     refs = {}
     for rep in range(2):
         for kind, B, H, N, d in cases:
@@ -358,7 +392,7 @@ def test_ticketed_kernels_under_graph_capture(orc, warm):
     """Captured and replayed calls on a fresh stream.  warm: the stream's flag
     workspace exists before capture (the graph reuses it, and each launch clears
     it for the next); cold: capture falls back to per-call flags and a memset."""
-    q, k, v = workloads.random_inputs(4242, 2, 4, 1500, 64, 64, "bf16")
+    q, k, v = workloads.random_inputs(4242, 4, 8, 1500, 64, 64, "bf16")
     qn, kn, vn = workloads.random_inputs(4343, 3, 4, 2048, 64, 64, "bf16")
     ref_c, ref_n = orc.causal_recurrent(q, k, v), orc.noncausal(qn, kn, vn)
     dev = [to_dev(x, "bf16") for x in (q, k, v, qn, kn, vn)]
