@@ -10,8 +10,8 @@ q, k, v from HBM.
 
 Also reported ("paths"): the long causal forward (B=1 H=32 N=65536 d=128),
 the non-causal forward (B=8 H=12 N=4096 d=64), the decode step (128 x 32
-heads, d=128, fp32 state) and its prefill state, the decayed-state and
-feature-map variants, the backward pass, and FAVOR+ (features alone, causal,
+heads, d=128, fp32 state) and its prefill state, the decayed-state, gated-state
+and feature-map variants, the backward pass, and FAVOR+ (features alone, causal,
 non-causal and decode), each with its roofline fraction.
 
 `--impl reference` times the float64 CPU oracle (the only reference this
@@ -525,6 +525,32 @@ def bench_path_causal_decay(torch, la, reps, peaks, src):
             "l2": "%d rotating buffer sets" % R}
 
 
+def bench_path_causal_gated(torch, la, reps, peaks, src):
+    """la_forward_causal_gated on the headline causal shape (B=4 H=8 N=2048 d=64, bf16)
+    with one gate per (token, key feature) drawn uniformly in [0.8, 1); the gates are a
+    third input stream (fp32, the size of q and k together): bytes read q, k, v, alpha,
+    written o.  CUDA cores, fp32 recurrence."""
+    w = workloads.CAUSAL_BF16
+    q, k, v = workloads.forward_inputs(w)
+    alpha = np.random.default_rng(w.seed + 7).uniform(0.8, 1.0, size=(w.B, w.H, w.N, w.dk)).astype(np.float32)
+    nbytes = forward_bytes(w.BH, w.N, w.dk, w.dv, 2) + alpha.nbytes
+    R = n_rotations(nbytes)
+    base = [dev_copy(torch, x, "bf16") for x in (q, k, v)] + [torch.from_numpy(alpha).cuda()]
+    sets = [[t.clone() for t in base] + [torch.empty_like(base[2])] for _ in range(R)]
+
+    def step(i):
+        s = sets[i % R]
+        la.la_forward_causal_gated(s[0], s[1], s[2], s[3], s[4], eps=w.eps)
+
+    secs, launches, _ = time_graph_steps(torch, la, step, reps, 3, Dist())
+    t = secs / reps
+    fl = float(w.BH) * w.N * (6 * w.dk * w.dv + 4 * w.dk)  # per token: gate, update, read (2 flop per MAC)
+    return {"workload": w.name + "_gated", "value": round(w.B * w.N / t, 1), "unit": "tokens/s",
+            "ms_per_step": round(t * 1e3, 4), "launches_per_step": launches / reps,
+            "roofline": roofline_alu(fl, nbytes, t, peaks, src, None),
+            "l2": "%d rotating buffer sets" % R}
+
+
 def bench_path_prefill_decay(torch, la, reps, peaks, src):
     """la_prefill_state_decay on the decode workload's prefill (4096 heads x 512
     tokens, d = 128, per-head decays 0.9 .. 0.999)."""
@@ -876,6 +902,7 @@ def run_gpu(args, dist):
         paths["causal_decay"] = bench_path_causal_decay(torch, la, max(args.path_reps, 20), peaks, src)
         paths["decode_decay"] = bench_path_decode_decay(torch, la, 1024, peaks, src)
         paths["prefill_state_decay"] = bench_path_prefill_decay(torch, la, max(args.path_reps, 20), peaks, src)
+        paths["causal_gated"] = bench_path_causal_gated(torch, la, max(args.path_reps, 20), peaks, src)
         reps = max(args.path_reps, 20)
         paths["causal_relu"] = bench_path_causal_variant(torch, la, reps, peaks, src, "relu", False, "relu", 0.0, True)
         paths["causal_retention"] = bench_path_causal_variant(torch, la, reps, peaks, src, "retention", True,

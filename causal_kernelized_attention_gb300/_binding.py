@@ -70,6 +70,9 @@ def _declare(lib):
         "la_forward_noncausal_favor": [P, P, P, P, P, I, I, I, I, I, I, F, I, P],
         "la_prefill_state_favor": [P, P, P, P, P, I, I, I, I, I, I, I, P],
         "la_decode_step_favor": [P, P, P, P, P, P, P, I, I, I, I, I, F, I, P],
+        "la_forward_causal_gated": [P, P, P, P, P, I, I, I, I, I, F, I, P],
+        "la_prefill_state_gated": [P, P, P, P, P, I, I, I, I, I, I, P],
+        "la_decode_step_gated": [P, P, P, P, P, P, P, I, I, I, I, F, I, P],
         "la_get_device_status": [P],
     }
     for name, args in sigs.items():
@@ -306,6 +309,73 @@ def la_prefill_state_decay(k, v, gamma, S=None, z=None, stream=None):
                                                z.data_ptr(), B, H, N, dk, dv, _dtype_code(k), _stream_ptr(stream))
     _check("la_prefill_state_decay", st)
     return S, z
+
+
+def _alpha_tensor(alpha, shape):
+    import torch
+    if not isinstance(alpha, torch.Tensor) or alpha.dtype != torch.float32 or not alpha.is_cuda \
+            or not alpha.is_contiguous() or tuple(alpha.shape) != tuple(shape):
+        raise ValueError("alpha must be a contiguous float32 CUDA tensor of shape %s" % (tuple(shape),))
+
+
+def la_forward_causal_gated(q, k, v, alpha, o=None, eps: float = 1e-6, stream=None):
+    """Causal forward with a gated state, one gate per key feature: alpha [B,H,N,dk]
+    fp32 (S_t = Diag(alpha_t) S_{t-1} + phi(k_t) v_t^T, z alike); returns o [B,H,N,dv]."""
+    import torch
+    if o is None:
+        o = torch.empty(q.shape[:-1] + (v.shape[-1],), dtype=q.dtype, device=q.device)
+    _need_cuda(q, k, v, o)
+    _same_dtype(q, k, v, o)
+    B, H, N, dk = q.shape
+    dv = v.shape[-1]
+    if tuple(k.shape) != (B, H, N, dk) or tuple(v.shape[:-1]) != (B, H, N) or tuple(o.shape) != (B, H, N, dv):
+        raise ValueError("shape mismatch")
+    _alpha_tensor(alpha, k.shape)
+    st = load_library().la_forward_causal_gated(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                                alpha.data_ptr(), B, H, N, dk, dv, float(eps), _dtype_code(q),
+                                                _stream_ptr(stream))
+    _check("la_forward_causal_gated", st)
+    return o
+
+
+def la_prefill_state_gated(k, v, alpha, S=None, z=None, stream=None):
+    """State after the gated recurrence over N tokens from zero; returns (S, z) fp32."""
+    import torch
+    B, H, N, dk = k.shape
+    dv = v.shape[-1]
+    if S is None:
+        S = torch.empty((B, H, dk, dv), dtype=torch.float32, device=k.device)
+    if z is None:
+        z = torch.empty((B, H, dk), dtype=torch.float32, device=k.device)
+    _need_cuda(k, v, S, z)
+    _same_dtype(k, v)
+    if tuple(v.shape[:-1]) != (B, H, N) or tuple(S.shape) != (B, H, dk, dv) or tuple(z.shape) != (B, H, dk):
+        raise ValueError("shape mismatch")
+    _alpha_tensor(alpha, k.shape)
+    st = load_library().la_prefill_state_gated(k.data_ptr(), v.data_ptr(), alpha.data_ptr(), S.data_ptr(),
+                                               z.data_ptr(), B, H, N, dk, dv, _dtype_code(k), _stream_ptr(stream))
+    _check("la_prefill_state_gated", st)
+    return S, z
+
+
+def la_decode_step_gated(S, z, q, k, v, alpha, o=None, eps: float = 1e-6, stream=None):
+    """One gated decode step in place; q, k, alpha [B,H,dk], v [B,H,dv]; returns o [B,H,dv]."""
+    import torch
+    if o is None:
+        o = torch.empty(v.shape, dtype=q.dtype, device=q.device)
+    _need_cuda(S, z, q, k, v, o)
+    _same_dtype(q, k, v, o)
+    B, H, dk = q.shape
+    dv = v.shape[-1]
+    if tuple(k.shape) != (B, H, dk) or tuple(v.shape) != (B, H, dv) or tuple(S.shape) != (B, H, dk, dv) \
+            or tuple(z.shape) != (B, H, dk):
+        raise ValueError("shape mismatch")
+    _alpha_tensor(alpha, k.shape)
+    st = load_library().la_decode_step_gated(S.data_ptr(), z.data_ptr(), q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                             o.data_ptr(), alpha.data_ptr(), B, H, dk, dv, float(eps),
+                                             _dtype_code(q), _stream_ptr(stream))
+    _check("la_decode_step_gated", st)
+    return o
 
 
 def _gamma_ptr(gamma, H):

@@ -379,6 +379,76 @@ la_status la_prefill_state_decay(const void *k, const void *v, const float *gamm
     return la_prefill_state_ex(k, v, gamma, nullptr, S, z, B, H, N, dk, dv, dtype, stream);
 }
 
+// ---------------------------------------------------------------- gated state
+la_status la_forward_causal_gated(const void *q, const void *k, const void *v, void *o, const float *alpha, int B,
+                                  int H, int N, int dk, int dv, float eps, la_dtype dtype, la_stream_t stream)
+{
+    bool empty;
+    la_status st = check_forward(q, k, v, o, B, H, N, dk, dv, eps, dtype, &empty);
+    if (st != LA_OK || empty) return st;
+    if (!alpha) return LA_ERR_INVALID_ARG;
+    if (!aligned16(alpha)) return LA_ERR_MISALIGNED;
+    const size_t na = (size_t)B * H * N * dk * 4, no = (size_t)B * H * N * dv * elem_size(dtype);
+    if (overlaps(alpha, na, o, no)) return LA_ERR_INVALID_ARG;
+    if (!supported_dim(dk) || !supported_dim(dv)) return LA_ERR_UNSUPPORTED;
+    return causal_gated(q, k, v, alpha, o, B * H, N, dk, dv, eps, dtype, (cudaStream_t)stream);
+}
+
+la_status la_prefill_state_gated(const void *k, const void *v, const float *alpha, float *S, float *z, int B, int H,
+                                 int N, int dk, int dv, la_dtype dtype, la_stream_t stream)
+{
+    if (B < 0 || H < 0 || N < 0 || dk < 0 || dv < 0) return LA_ERR_INVALID_ARG;
+    if (dtype != LA_F32 && dtype != LA_BF16) return LA_ERR_INVALID_ARG;
+    if ((long long)B * H > 65535) return LA_ERR_UNSUPPORTED;
+    if (B == 0 || H == 0 || dk == 0 || dv == 0) return LA_OK;
+    if (!S || !z) return LA_ERR_INVALID_ARG;
+    if (!aligned16(S) || !aligned16(z)) return LA_ERR_MISALIGNED;
+    if (!supported_dim(dk) || !supported_dim(dv)) return LA_ERR_UNSUPPORTED;
+    const size_t BH = (size_t)B * H;
+    if (overlaps(S, BH * dk * dv * 4, z, BH * dk * 4)) return LA_ERR_INVALID_ARG;
+    if (N > 0) {
+        if (!k || !v || !alpha) return LA_ERR_INVALID_ARG;
+        if (!aligned16(k) || !aligned16(v) || !aligned16(alpha)) return LA_ERR_MISALIGNED;
+        const size_t es = elem_size(dtype), nk = BH * N * dk * es, nv = BH * N * dv * es, na = BH * N * dk * 4;
+        const void *in[3] = {k, v, alpha};
+        const size_t ins[3] = {nk, nv, na};
+        for (int x = 0; x < 3; ++x)
+            if (overlaps(S, BH * dk * dv * 4, in[x], ins[x]) || overlaps(z, BH * dk * 4, in[x], ins[x]))
+                return LA_ERR_INVALID_ARG;
+    }
+    if (N == 0) {  // the empty prefix: zero state
+        cudaError_t e = cudaMemsetAsync(S, 0, BH * dk * dv * 4, (cudaStream_t)stream);
+        if (e == cudaSuccess) e = cudaMemsetAsync(z, 0, BH * dk * 4, (cudaStream_t)stream);
+        count_launches(2);
+        return cuda_status(e);
+    }
+    return state_gated(k, v, alpha, S, z, (int)BH, N, dk, dv, dtype, (cudaStream_t)stream);
+}
+
+la_status la_decode_step_gated(float *S, float *z, const void *q, const void *k, const void *v, void *o,
+                               const float *alpha, int B, int H, int dk, int dv, float eps, la_dtype dtype,
+                               la_stream_t stream)
+{
+    if (B < 0 || H < 0 || dk < 0 || dv < 0) return LA_ERR_INVALID_ARG;
+    if (!(eps >= 0.f) || !isfinite(eps)) return LA_ERR_INVALID_ARG;
+    if (dtype != LA_F32 && dtype != LA_BF16) return LA_ERR_INVALID_ARG;
+    if ((long long)B * H > 65535) return LA_ERR_UNSUPPORTED;
+    if (B == 0 || H == 0 || dk == 0 || dv == 0) return LA_OK;
+    if (!S || !z || !q || !k || !v || !o || !alpha) return LA_ERR_INVALID_ARG;
+    const void *all[7] = {S, z, q, k, v, o, alpha};
+    for (const void *x : all)
+        if (!aligned16(x)) return LA_ERR_MISALIGNED;
+    if (!supported_dim(dk) || !supported_dim(dv)) return LA_ERR_UNSUPPORTED;
+    const size_t BH = (size_t)B * H, es = elem_size(dtype);
+    const size_t sizes[7] = {BH * dk * dv * 4, BH * dk * 4, BH * dk * es, BH * dk * es, BH * dv * es, BH * dv * es,
+                             BH * dk * 4};
+    const int outs[3] = {0, 1, 5};  // S, z and o are written: they overlap nothing else
+    for (int oi : outs)
+        for (int x = 0; x < 7; ++x)
+            if (x != oi && overlaps(all[oi], sizes[oi], all[x], sizes[x])) return LA_ERR_INVALID_ARG;
+    return decode_step_gated(S, z, q, k, v, o, alpha, (int)BH, dk, dv, eps, dtype, (cudaStream_t)stream);
+}
+
 la_status la_backward_causal(const void *q, const void *k, const void *v, const void *dout, void *dq, void *dk,
                              void *dv, int B, int H, int N, int d_k, int d_v, float eps, la_dtype dtype,
                              la_stream_t stream)
@@ -573,10 +643,12 @@ la_status la_get_device_status(la_stream_t stream)
     if (st != LA_OK) return st;
     st = favor_read_status((cudaStream_t)stream, &fv_bits);
     if (st != LA_OK) return st;
-    unsigned cc_bits = 0;
+    unsigned cc_bits = 0, cl_bits = 0;
     st = tc_chunks_read_status((cudaStream_t)stream, &cc_bits);
     if (st != LA_OK) return st;
-    return ((bits | nc_bits | fv_bits | cc_bits) & kStatusTimeout) ? LA_ERR_TIMEOUT : LA_OK;
+    st = tc_cluster_read_status((cudaStream_t)stream, &cl_bits);
+    if (st != LA_OK) return st;
+    return ((bits | nc_bits | fv_bits | cc_bits | cl_bits) & kStatusTimeout) ? LA_ERR_TIMEOUT : LA_OK;
 }
 
 int la_version(void) { return 100; }

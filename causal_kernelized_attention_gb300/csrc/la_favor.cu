@@ -264,6 +264,7 @@ la_status make_map_rows(CUtensorMap *m, const void *ptr, int BH, int N, int D, i
 {
     EncodeTiledFn enc;
     la_status st = encode_fn(&enc);
+    if (st == LA_OK) st = bind_thread_context();
     if (st != LA_OK) return st;
     const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)N, (cuuint64_t)BH};
     const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)N * D * 2};

@@ -67,6 +67,16 @@ la_status state_simt(const void *k, const void *v, float *S, float *z, int BH, i
                      int dv, la_dtype dtype, cudaStream_t stream, const float *gamma = nullptr,
                      int H = 1, const Variant &var = Variant());
 
+// Gated state with one gate per key feature (la_gated.cu), fp32 on the CUDA cores:
+// alpha [BH, N, dk] (decode: [BH, dk]) fp32 in device memory.
+la_status causal_gated(const void *q, const void *k, const void *v, const float *alpha, void *o, int BH, int N,
+                       int dk, int dv, float eps, la_dtype dtype, cudaStream_t stream);
+la_status state_gated(const void *k, const void *v, const float *alpha, float *S, float *z, int BH, int N, int dk,
+                      int dv, la_dtype dtype, cudaStream_t stream);
+la_status decode_step_gated(float *S, float *z, const void *q, const void *k, const void *v, void *o,
+                            const float *alpha, int BH, int dk, int dv, float eps, la_dtype dtype,
+                            cudaStream_t stream);
+
 // Decode step (la_decode.cu).
 // gamma (device, [H], head = bh % H): the decayed step S = g S + phi(k) v^T,
 // z = g z + phi(k); null for the undecayed step.
@@ -80,6 +90,9 @@ la_status causal_tc(const Problem &p);
 // Chunk-parallel causal kernel (la_tc_causal_chunks.cu): bf16, dk = dv = 64, chunk
 // 128, N >= 128, elu + 1 with the normaliser, no decay.
 la_status causal_chunks_tc(const Problem &p);
+// Cluster kernel (la_tc_causal_cluster.cu): bf16, dk = dv = 64, chunk 128,
+// 128 <= N <= 2048, elu + 1 with the normaliser, no decay.
+la_status causal_cluster_tc(const Problem &p);
 // (la_tc_noncausal.cu)
 la_status noncausal_tc(const Problem &p);
 // S, z (fp32, [BH,D,D], [BH,D]) = sums over N tokens on the tensor cores (bf16
@@ -94,6 +107,7 @@ la_status tc_causal_read_status(cudaStream_t s, unsigned *bits);
 la_status tc_noncausal_read_status(cudaStream_t s, unsigned *bits);
 la_status favor_read_status(cudaStream_t s, unsigned *bits);
 la_status tc_chunks_read_status(cudaStream_t s, unsigned *bits);
+la_status tc_cluster_read_status(cudaStream_t s, unsigned *bits);
 
 // Failure-detection test hooks (la_test_set_wait_limit_ns, la_test_drop_publication):
 // the limit of the chunk-parallel causal kernel's bounded waits (2 s unless a test

@@ -58,6 +58,7 @@ constexpr int kTmaWarp = 8, kMmaWarp = 9, kEpiPWarp0 = 10, kEpiOWarp0 = 14;
 constexpr uint32_t kPublished = 8, kPoison = 1u << 20;
 constexpr int kMaxShortSegs = 32;  // segments per head in short-sequence mode
 constexpr int kChunkKernelMinHeads = 16;  // B*H from which d = 64 runs the chunk-parallel kernel
+constexpr int kClusterKernelMaxN = 2048;  // sequences up to which d = 64 runs the cluster kernel
 
 // Row sums and z ride on the tensor cores in one of two ways:
 //  * fused (D = 64): the B operand of P V and of the state update is [V | 1] and
@@ -1149,9 +1150,15 @@ la_status launch(const Problem &p)
 
 }  // namespace
 
-la_status causal_tc(const Problem &p)
+la_status causal_tc(const Problem &p_in)
 {
-    if (p.dtype != LA_BF16 || p.dk != p.dv || (p.dk != 64 && p.dk != 128) || p.chunk != kC || p.N < kC)
+    // The chunked form computes the same function for every chunk length (only the
+    // order of the roundings differs), so a request for chunks of 64 runs here too,
+    // with the tensor-core kernels' 128-token tiles.
+    if (p_in.chunk != 64 && p_in.chunk != kC) return LA_ERR_UNSUPPORTED;
+    Problem p = p_in;
+    p.chunk = kC;
+    if (p.dtype != LA_BF16 || p.dk != p.dv || (p.dk != 64 && p.dk != 128) || p.N < kC)
         return LA_ERR_UNSUPPORTED;
     const bool var = !p.var.is_default();
     if (p.gamma) {
@@ -1159,9 +1166,12 @@ la_status causal_tc(const Problem &p)
         return p.dk == 128 ? launch<128, true, false>(p) : launch<64, true, false>(p);
     }
     if (var) return p.dk == 128 ? launch<128, false, true>(p) : launch<64, false, true>(p);
-    // d = 64 with enough heads: the chunk-parallel kernel (la_tc_causal_chunks.cu),
-    // whose look-back needs the chunks of one head in flight at a time (about twice
-    // the SM count divided by the heads) to fit its 32-chunk window.
+    // d = 64: up to 16 chunks per head, one thread-block cluster per head
+    // (la_tc_causal_cluster.cu); longer sequences with enough heads, the
+    // chunk-parallel kernel (la_tc_causal_chunks.cu), whose look-back needs the
+    // chunks of one head in flight at a time (about twice the SM count divided by
+    // the heads) to fit its 32-chunk window.
+    if (p.dk == 64 && p.N <= kClusterKernelMaxN) return causal_cluster_tc(p);
     if (p.dk == 64 && p.BH >= kChunkKernelMinHeads) return causal_chunks_tc(p);
     return p.dk == 128 ? launch<128, false, false>(p) : launch<64, false, false>(p);
 }

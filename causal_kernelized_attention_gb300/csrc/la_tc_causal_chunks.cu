@@ -24,10 +24,10 @@
 //  * The MMA thread runs one item ahead: A and T of item n + 1 go to the tensor
 //    pipe before the output MMAs of item n, which wait for item n's look-back.
 //
-// Warp roles (640 threads): warps 0-3 turn T into P (TMEM lane quadrant = warp);
+// Warp roles (800 threads): warps 0-3 turn T into P (TMEM lane quadrant = warp);
 // 4-7 normalise O and store it; 8-9 read A_c back and publish it; 10 tickets and
-// TMA loads; 11 MMA issue and TMEM; 12-15 look-back and the state image; 16-19
-// phi.  Every wait is bounded (Params::wait_ns); on expiry the CTA records
+// TMA loads; 11 the T, P V and output MMAs, and TMEM; 12-19 look-back and the
+// state image; 20-23 phi (K first, then Q); 24 the chunk-state MMAs.  Every wait is bounded (Params::wait_ns); on expiry the CTA records
 // LA_ERR_TIMEOUT in this file's status word and raises the launch's abort word,
 // so that every CTA winds down: each drains its copies and MMAs in flight and
 // frees its TMEM before it exits.
@@ -47,18 +47,19 @@ using namespace tc;
 static __device__ unsigned g_cc_status;
 
 constexpr int D = 64;
-constexpr int kThreads = 640;
+constexpr int kThreads = 800;
 constexpr int kS = 4;                    // stages: Q, K and V of one chunk each
 constexpr int kR = 8;                    // item ring
 constexpr uint32_t kTile = kC * D * 2;   // one [128 x 64] bf16 tile: 16 KB
 constexpr uint32_t kSbBytes = D * D * 2; // bf16 state image, MN-major for phi(Q) E
 constexpr int kOWarp0 = 4, kAggWarp0 = 8, kTmaWarp = 10, kMmaWarp = 11, kLbWarp0 = 12,
-              kPhiWarp0 = 16;
-constexpr int kPhiThreads = 128, kLbThreads = 128, kAggThreads = 64;
+              kPhiWarp0 = 20, kAWarp = 24;
+constexpr int kPhiThreads = 128, kLbThreads = 256, kAggThreads = 64;
 // Readers of a ring entry: 4 T->P warps, 4 O warps, 2 publishing warps, the MMA
-// thread, 4 look-back warps, 4 phi warps (one arrival per warp).
-constexpr uint32_t kRingReaders = 4 + 4 + 2 + 1 + 4 + 4;
-constexpr uint32_t kPublished = 4;       // a published state's counter value
+// thread, 8 look-back warps, 4 phi warps, the chunk-state MMA thread (one arrival
+// per warp).
+constexpr uint32_t kRingReaders = 4 + 4 + 2 + 1 + 8 + 4 + 1;
+constexpr uint32_t kPublished = 8;       // a published state's counter value
 constexpr size_t kStateFloats = (size_t)D * D + D;  // S (thread-major, see add_state), then z
 // TMEM columns: T (and P over it) in two buffers of 128, O = [P V | rowsum] +
 // phi(Q) [E | z] in two buffers of 80, A_c = [S | z] in 80.
@@ -77,9 +78,9 @@ struct alignas(1024) Smem {
     uint8_t v[kS][kTile];
     uint8_t img[2][kSbBytes];  // state images E_c (bf16, MN-major), one per item parity
     uint8_t ones[kC * 128];    // column 0 = 1; columns 16(b+1), 16(b+1)+1 = z_hi, z_lo of image b
-    uint64_t full[kS], phi_done[kS], empty[kS];
+    uint64_t full[kS], k_ready[kS], phi_done[kS], empty[kS];
     uint64_t item_full[kR], item_empty[kR];
-    uint64_t a_full, a_free, drain;
+    uint64_t a_full, a_free, drain, drain_a;
     uint64_t t_full[2], p_full[2], pv_done[2], o_full[2], o_free[2], o_staged[2], s_ready[2];
     uint64_t lb_sync;  // the look-back warps' barrier (bounded, unlike bar.sync)
     Item items[kR];
@@ -163,6 +164,35 @@ __device__ __forceinline__ void put_z_pair(uint8_t *ones, int i, float zv, int b
     *reinterpret_cast<__nv_bfloat162 *>(ones + sw128_offset(i, 16 * (b + 1))) = __halves2bfloat162(hi, lo);
 }
 
+// Row i, columns [16 h, 16 h + 16) of a published state (thread-major layout: the
+// float4 of columns 4c..4c+3 of row i at float4 index c * D + i), and z_i for h = 0.
+__device__ __forceinline__ void load_part(const float *st, int i, int h, float4 (&x)[4], float &zv)
+{
+    const float4 *s4 = reinterpret_cast<const float4 *>(st);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) x[e] = __ldcg(s4 + (size_t)(4 * h + e) * D + i);
+    zv = h == 0 ? __ldcg(st + (size_t)D * D + i) : 0.f;
+}
+__device__ __forceinline__ void add_part(float (&acc)[16], float &zacc, const float4 (&x)[4], float zv)
+{
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        acc[4 * e] += x[e].x; acc[4 * e + 1] += x[e].y; acc[4 * e + 2] += x[e].z; acc[4 * e + 3] += x[e].w;
+    }
+    zacc += zv;
+}
+// Row i, columns [col0, col0 + 16) of the bf16 state image (MN-major, 128-byte swizzled, D = 64).
+__device__ __forceinline__ void put_sb16(uint8_t *sb, int i, int col0, const float (&x)[16])
+{
+#pragma unroll
+    for (int c8 = 0; c8 < 16; c8 += 8) {
+        const int col = col0 + c8;
+        *reinterpret_cast<uint4 *>(sb + i * 128 + (((col >> 3) ^ (i & 7)) << 4)) =
+            make_uint4(pack_bf16(x[c8], x[c8 + 1]), pack_bf16(x[c8 + 2], x[c8 + 3]), pack_bf16(x[c8 + 4], x[c8 + 5]),
+                       pack_bf16(x[c8 + 6], x[c8 + 7]));
+    }
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
 causal_chunks_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                      const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_o,
@@ -204,8 +234,10 @@ causal_chunks_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
     if (tid == 0) {
         for (int s = 0; s < kS; ++s) {
             mbar_init(&sm.full[s], 1);
+            mbar_init(&sm.k_ready[s], kPhiThreads);
             mbar_init(&sm.phi_done[s], kPhiThreads);
-            mbar_init(&sm.empty[s], 1);
+            // released by the output store and by the read-back of the chunk state
+            mbar_init(&sm.empty[s], 2);
         }
         for (int r = 0; r < kR; ++r) {
             mbar_init(&sm.item_full[r], 1);
@@ -214,6 +246,7 @@ causal_chunks_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
         mbar_init(&sm.a_full, 1);
         mbar_init(&sm.a_free, kAggThreads);
         mbar_init(&sm.drain, 1);
+        mbar_init(&sm.drain_a, 1);
         for (int b = 0; b < 2; ++b) {
             mbar_init(&sm.t_full[b], 1);
             mbar_init(&sm.p_full[b], 128);
@@ -240,7 +273,7 @@ causal_chunks_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
     const uint32_t tmem = sm.tmem_base;
     int *abort_flag = &sm.abort;
 
-    if (warp >= kPhiWarp0) {
+    if (warp >= kPhiWarp0 && warp < kAWarp) {
         // ---------------------------------------------------------------- phi warps
         const int t = tid - kPhiWarp0 * 32;
         for (int it = 0;; ++it) {
@@ -250,9 +283,41 @@ causal_chunks_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
             if (!wait_bar_warp(prm, abort_flag, &sm.full[s], (it / kS) & 1)) break;
             const int valid = prm.N - item.c * kC;  // rows past the sequence become zeros
             phi_tile<D, kPhiThreads>(sm.k[s], t, valid);
+            fence_proxy_async_smem();
+            mbar_arrive(&sm.k_ready[s]);  // the chunk-state MMA needs phi(K) only
             phi_tile<D, kPhiThreads>(sm.q[s], t, valid);
             fence_proxy_async_smem();
             mbar_arrive(&sm.phi_done[s]);
+        }
+    } else if (warp == kAWarp) {
+        // ---------------------------------------------------------------- chunk-state MMA
+        // A_c = phi(K_c)^T [V_c | 1] as soon as phi(K_c) is done and the publishing
+        // warps have read A of the item before: no look-back delays a publication.
+        if (lane == 0) {
+            const uint32_t id_KV = idesc_bf16_f32(128, D + 16, true, true);  // phi(K)^T [V | 1]
+            const uint32_t ones = smem_u32(sm.ones);
+            for (int it = 0;; ++it) {
+                const int r = it % kR;
+                if (!wait_bar(prm, abort_flag, &sm.item_full[r], (it / kR) & 1)) break;
+                const Item item = sm.items[r];
+                mbar_arrive(&sm.item_empty[r]);
+                if (item.c < 0) break;
+                const int s = it % kS;
+                if (!wait_bar(prm, abort_flag, &sm.k_ready[s], (it / kS) & 1)) break;
+                if (it >= 1 && !wait_bar(prm, abort_flag, &sm.a_free, (it - 1) & 1)) break;
+                tc_fence_after();
+                const uint32_t ka = smem_u32(sm.k[s]), va = smem_u32(sm.v[s]);
+                // phi(K)^T is MN-major; its second 64-row block (one tile on) feeds rows
+                // 64..127 of A, which nothing reads.
+                const uint64_t dkt = mnmajor(ka, 0, kBox), dv = mnmajor(va, 0, ones - va);
+#pragma unroll
+                for (int kk = 0; kk < kC / 16; ++kk)
+                    mma_ss(tmem + tA, dkt + 128 * kk, dv + 128 * kk, id_KV, kk > 0 ? 1u : 0u);
+                mma_commit(&sm.a_full);
+            }
+            // its MMAs complete before TMEM is freed
+            mma_commit(&sm.drain_a);
+            drain_bar(&sm.drain_a, 0);
         }
     } else if (warp == kTmaWarp) {
         // ---------------------------------------------------------------- tickets + TMA
@@ -296,24 +361,13 @@ causal_chunks_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
             const uint32_t id_T = idesc_bf16_f32(128, 128, false, false);   // phi(Q) phi(K)^T
             const uint32_t id_PV = idesc_bf16_f32(128, D + 16, false, true); // P [V | 1] (P in TMEM)
             const uint32_t id_QS = idesc_bf16_f32(128, D + 16, false, true); // phi(Q) [E | z]
-            const uint32_t id_KV = idesc_bf16_f32(128, D + 16, true, true);  // phi(K)^T [V | 1]
             const uint32_t ones = smem_u32(sm.ones);
-            // A and T of item n (stage n % kS): A into the single A buffer once the
-            // publishing warps have read A of item n - 1; T into buffer n % 2 once
-            // P V of item n - 2, which read P from it, is done.
-            auto issue_AT = [&](int n) -> bool {
+            // T of item n (stage n % kS) into buffer n % 2 once P V of item n - 2, which
+            // read P from it, is done.  (The chunk state A is issued by its own thread.)
+            auto issue_T = [&](int n) -> bool {
                 const int s = n % kS, b = n & 1;
                 if (!wait_bar(prm, abort_flag, &sm.phi_done[s], (n / kS) & 1)) return false;
-                if (n >= 1 && !wait_bar(prm, abort_flag, &sm.a_free, (n - 1) & 1)) return false;
-                tc_fence_after();
-                const uint32_t qa = smem_u32(sm.q[s]), ka = smem_u32(sm.k[s]), va = smem_u32(sm.v[s]);
-                // phi(K)^T is MN-major; its second 64-row block (one tile on) feeds rows
-                // 64..127 of A, which nothing reads.
-                const uint64_t dkt = mnmajor(ka, 0, kBox), dv = mnmajor(va, 0, ones - va);
-#pragma unroll
-                for (int kk = 0; kk < kC / 16; ++kk)
-                    mma_ss(tmem + tA, dkt + 128 * kk, dv + 128 * kk, id_KV, kk > 0 ? 1u : 0u);
-                mma_commit(&sm.a_full);
+                const uint32_t qa = smem_u32(sm.q[s]), ka = smem_u32(sm.k[s]);
                 if (n >= 2 && !wait_bar(prm, abort_flag, &sm.pv_done[b], ((n - 2) >> 1) & 1)) return false;
                 tc_fence_after();
                 const uint64_t dq = kmajor(qa, 0), dk = kmajor(ka, 0);
@@ -328,14 +382,14 @@ causal_chunks_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
             if (ok) {
                 cur = sm.items[0];
                 mbar_arrive(&sm.item_empty[0]);
-                ok = cur.c >= 0 && issue_AT(0);
+                ok = cur.c >= 0 && issue_T(0);
             }
             for (int n = 0; ok; ++n) {
                 const int n1 = n + 1, r1 = n1 % kR;
                 if (!(ok = wait_bar(prm, abort_flag, &sm.item_full[r1], (n1 / kR) & 1))) break;
                 const Item nx = sm.items[r1];
                 mbar_arrive(&sm.item_empty[r1]);
-                if (nx.c >= 0 && !(ok = issue_AT(n1))) break;
+                if (nx.c >= 0 && !(ok = issue_T(n1))) break;
                 // outputs of item n: P V into O buffer n % 2 (free once item n - 2's O
                 // has been read), then phi(Q) [E | z] once the look-back is done
                 const int s = n % kS, b = n & 1;
@@ -501,19 +555,21 @@ causal_chunks_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
             if (publish) dst[(size_t)D * D + i] = zv;
             tc_fence_before();
             mbar_arrive(&sm.a_free);
+            // A_c complete implies its reads of K and V are done: the stage's second release
+            if (warp == kAggWarp0 && lane == 0) mbar_arrive(&sm.empty[it % kS]);
             if (publish) {
-                // the warp's stores before lane 0's release (two warps: kPublished = 4)
+                // the warp's stores before lane 0's release (two warps, half of kPublished each)
                 __syncwarp();
-                if (lane == 0) red_release_add_gpu((item.c == 0 ? prm.incl_cnt : prm.agg_cnt) + idx, 2u);
+                if (lane == 0) red_release_add_gpu((item.c == 0 ? prm.incl_cnt : prm.agg_cnt) + idx, kPublished / 2);
             }
         }
-    } else if (warp >= kLbWarp0) {
+    } else if (warp >= kLbWarp0 && warp < kPhiWarp0) {
         // ---------------------------------------------------------------- look-back (warps 12-15)
-        // Thread lt owns state row i = lt % 64 and columns [32 h, 32 h + 32), h = lt / 64
+        // Thread lt owns state row i = lt % 64 and columns [16 h, 16 h + 16), h = lt / 64
         // (h = 0 also z_i).  The group's first warp finds, among the 32 chunks before
         // c, the nearest published inclusive prefix I_j with every aggregate after it
         // published; all four warps then add them.
-        const int lt = tid - kLbWarp0 * 32, i = lt & 63, h = lt >> 6;
+        const int lt = tid - kLbWarp0 * 32, i = lt & 63, h = lt >> 6;  // h: columns 16 h .. 16 h + 15
         uint32_t syncs = 0;  // completed uses of lb_sync
         for (int it = 0;; ++it) {
             Item item;
@@ -566,37 +622,43 @@ causal_chunks_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
                 ++syncs;
                 const int base = synced ? sm.lb_base[b] : -1;
                 if (base < 0) break;  // gave up
-                float acc[32];
+                // States of the look-back: I_base, then A_{base+1} .. A_{c-1} (their sum is
+                // E_c), then A_c (for I_c).  Two states' loads are in flight per round trip.
+                auto st_ptr = [&](int j) -> const float * {
+                    return (j == base ? prm.incl : prm.agg) + (head0 + j) * kStateFloats;
+                };
+                float acc[16];
 #pragma unroll
-                for (int e = 0; e < 32; ++e) acc[e] = 0.f;
+                for (int e = 0; e < 16; ++e) acc[e] = 0.f;
                 float zacc = 0.f;
-                const int cg0 = 8 * h;
-                {
-                    const float *st = prm.incl + (head0 + base) * kStateFloats;
-                    const float zv = h == 0 ? __ldcg(st + (size_t)D * D + i) : 0.f;
-                    add_state<D>(acc, st, cg0, i);
-                    zacc += zv;
+                int j = base;
+                for (; j + 1 < item.c; j += 2) {
+                    float4 x0[4], x1[4];
+                    float z0, z1;
+                    load_part(st_ptr(j), i, h, x0, z0);
+                    load_part(st_ptr(j + 1), i, h, x1, z1);
+                    add_part(acc, zacc, x0, z0);
+                    add_part(acc, zacc, x1, z1);
                 }
-                for (int jj = base + 1; jj < item.c; ++jj) {
-                    const float *st = prm.agg + (head0 + jj) * kStateFloats;
-                    const float zv = h == 0 ? __ldcg(st + (size_t)D * D + i) : 0.f;
-                    add_state<D>(acc, st, cg0, i);
-                    zacc += zv;
-                }
-                put_sb<D>(sm.img[b], i, 32 * h, acc);
+                // the last state of E_c (if any) and A_c in the same round trip
+                float4 xe[4], xo[4];
+                float ze = 0.f, zo = 0.f;
+                const bool e_left = j < item.c;
+                if (e_left) load_part(st_ptr(j), i, h, xe, ze);
+                if (!last) load_part(prm.agg + (head0 + item.c) * kStateFloats, i, h, xo, zo);
+                if (e_left) add_part(acc, zacc, xe, ze);
+                put_sb16(sm.img[b], i, 16 * h, acc);
                 if (h == 0) put_z_pair(sm.ones, i, zacc, b);
                 fence_proxy_async_smem();
                 if (!last) {  // I_c = E_c + A_c for the chunks after this one
-                    const float *own = prm.agg + (head0 + item.c) * kStateFloats;
+                    add_part(acc, zacc, xo, zo);
                     float *dst = prm.incl + (head0 + item.c) * kStateFloats;
-                    const float zo = h == 0 ? __ldcg(own + (size_t)D * D + i) : 0.f;
-                    add_state<D>(acc, own, cg0, i);
                     float4 *d4 = reinterpret_cast<float4 *>(dst);
 #pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        d4[(size_t)(cg0 + e) * D + i] = make_float4(acc[4 * e], acc[4 * e + 1], acc[4 * e + 2],
-                                                                    acc[4 * e + 3]);
-                    if (h == 0) dst[(size_t)D * D + i] = zacc + zo;
+                    for (int e = 0; e < 4; ++e)
+                        d4[(size_t)(4 * h + e) * D + i] = make_float4(acc[4 * e], acc[4 * e + 1], acc[4 * e + 2],
+                                                                      acc[4 * e + 3]);
+                    if (h == 0) dst[(size_t)D * D + i] = zacc;
                 }
             }
             mbar_arrive(&sm.s_ready[b]);

@@ -317,11 +317,49 @@ inline la_status encode_fn(EncodeTiledFn *out)
     return LA_OK;
 }
 
+// The tensor-map encoder is a driver call: it needs a current context in the
+// calling thread, which the runtime binds only when that thread makes its first
+// runtime call that uses the device.  A host thread whose first CUDA work is this
+// library has none yet: bind the runtime's primary context of the current device
+// (once per thread; a thread without a context cannot be capturing a stream).
+inline la_status bind_thread_context()
+{
+    typedef CUresult (*CtxGetFn)(CUcontext *);
+    static std::mutex mu;
+    static CtxGetFn get = nullptr;
+    static thread_local bool bound = false;
+    if (bound) return LA_OK;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (!get) {
+            cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+            cudaError_t e = cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", (void **)&get, 12000,
+                                                             cudaEnableDefault, &q);
+            if (e != cudaSuccess) return cuda_status(e);
+            if (q != cudaDriverEntryPointSuccess || !get) {
+                get = nullptr;
+                return cuda_status(cudaErrorNotSupported);
+            }
+        }
+    }
+    CUcontext ctx = nullptr;
+    if (get(&ctx) != CUDA_SUCCESS) return cuda_status(cudaErrorInvalidValue);
+    if (!ctx) {
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e == cudaSuccess) e = cudaSetDevice(dev);
+        if (e != cudaSuccess) return cuda_status(e);
+    }
+    bound = true;
+    return LA_OK;
+}
+
 // [BH, N, D] bf16 as a 3-D tensor (D, N, BH); box = 64 columns x 128 rows, 128-byte swizzle.
 inline la_status make_map(CUtensorMap *m, const void *ptr, int BH, int N, int D)
 {
     EncodeTiledFn enc;
     la_status st = encode_fn(&enc);
+    if (st == LA_OK) st = bind_thread_context();
     if (st != LA_OK) return st;
     const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)N, (cuuint64_t)BH};
     const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)N * D * 2};
@@ -331,6 +369,15 @@ inline la_status make_map(CUtensorMap *m, const void *ptr, int BH, int N, int D)
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? LA_OK : cuda_status(cudaErrorInvalidValue);
+}
+
+// Programmatic stream serialization is requested only on streams the caller
+// created: the default streams (legacy, per-thread) synchronise implicitly with
+// other work, and there the kernels launch plainly (their griddepcontrol
+// instructions are then no-ops).
+inline bool dependent_launch_allowed(cudaStream_t s)
+{
+    return s != nullptr && s != cudaStreamLegacy && s != cudaStreamPerThread;
 }
 
 // Launches a tensor-core kernel with programmatic stream serialization: its CTAs
@@ -350,7 +397,7 @@ inline la_status launch_dependent(void (*kern)(Params...), unsigned grid, int th
     at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     at[0].val.programmaticStreamSerializationAllowed = 1;
     lc.attrs = at;
-    lc.numAttrs = 1;
+    lc.numAttrs = dependent_launch_allowed(s) ? 1 : 0;
     return cuda_status(cudaLaunchKernelEx(&lc, kern, args...));
 }
 

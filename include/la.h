@@ -89,6 +89,10 @@ typedef struct CUstream_st *la_stream_t;
  * `chunk`; the last chunk is then shorter.  `chunk` must be 64 or 128.
  * Supported: dk, dv in {32, 64, 128} for fp32; for bf16 dk == dv in
  * {64, 128} on the tensor-core path, and dk, dv in {32, 64, 128} otherwise.
+ * The tensor-core path (bf16, dk == dv in {64, 128}, N >= 128) computes with
+ * chunks of 128 tokens whether `chunk` is 64 or 128: the chunked form is the
+ * same function for every chunk length, only the order of the roundings
+ * differs.  The CUDA-core path (fp32, other shapes) uses `chunk` as given.
  */
 la_status la_forward_causal(const void *q, const void *k, const void *v, void *o,
                             int B, int H, int N, int dk, int dv, int chunk, float eps,
@@ -182,8 +186,8 @@ la_status la_decode_step(float *S, float *z, const void *q, const void *k, const
  * Head h of every batch entry uses gamma[h].  gamma must be 4-byte aligned and
  * must not overlap o; its values are read by the kernel and not checked (the
  * method takes them in [0, 1]).  `chunk` (64 or 128) is the length of the
- * intra-chunk quadratic blocks.  bf16 with dk = dv in {64, 128}, chunk 128 and
- * N >= 128 runs on the tensor cores (the kernel of la_forward_causal with the
+ * intra-chunk quadratic blocks on the CUDA cores.  bf16 with dk = dv in
+ * {64, 128} and N >= 128 runs on the tensor cores (128-token chunks) (the kernel of la_forward_causal with the
  * decay weights in the intra-chunk mask, on the rows of phi(Q) and phi(K), on
  * the running state and in the scan across segments); other shapes run on the
  * CUDA cores in fp32.  Supported: dk, dv in {32, 64, 128}.
@@ -240,6 +244,45 @@ la_status la_prefill_state_decay(const void *k, const void *v, const float *gamm
                                  la_stream_t stream);
 
 /*
+ * Gated state with one gate per key feature ("Linear Attention",
+ * aiwiki.thehackersbrain.dev, What is actually lost: gated variants insert a
+ * decay, S_t = G_t (.) S_{t-1} + phi(k_t) v_t^T; "Linear Attention -- Math +
+ * Variants", RetNet and gated linear attention: S_i = Diag(alpha_i) S_{i-1} +
+ * k_i v_i^T, the decay computed from the token itself):
+ *
+ *   S_t = Diag(alpha_t) S_{t-1} + phi(k_t) v_t^T,   z_t = alpha_t (.) z_{t-1} + phi(k_t),
+ *   o_t = phi(q_t)^T S_t / max(phi(q_t)^T z_t, eps)
+ *
+ * i.e. key j reaches query i >= j through feature r with weight
+ * prod_{s=j+1..i} alpha_s[r], in the numerator and the normaliser alike.  The
+ * gate values are the caller's (the layer that computes them from the token has
+ * trained weights): alpha is fp32 DEVICE memory shaped like k, [B, H, N, dk]
+ * ([B, H, dk] for a decode step), 16-byte aligned; its values are read as given
+ * (the method takes them in [0, 1]).  Every alpha = gamma[h] reproduces
+ * la_forward_causal_decay; every alpha = 1 reproduces la_forward_causal.
+ *
+ * la_forward_causal_gated: q, k : [B, H, N, dk]   v, o : [B, H, N, dv].  o must not
+ *   overlap q, k, v or alpha.
+ * la_prefill_state_gated: the state after N tokens from a zero state
+ *   (S [B, H, dk, dv], z [B, H, dk] fp32, OVERWRITTEN; N = 0 writes zeros), so
+ *   that la_decode_step_gated continues the sequence.
+ * la_decode_step_gated: S, z read and updated in place; q, k : [B, H, dk],
+ *   v, o : [B, H, dv], alpha : [B, H, dk].  S, z and o overlap nothing else.
+ *
+ * fp32 arithmetic on the CUDA cores: the recurrence itself, split over value
+ * columns (each column of S evolves on its own).  Supported: dk, dv in
+ * {32, 64, 128}.
+ */
+la_status la_forward_causal_gated(const void *q, const void *k, const void *v, void *o, const float *alpha,
+                                  int B, int H, int N, int dk, int dv, float eps, la_dtype dtype,
+                                  la_stream_t stream);
+la_status la_prefill_state_gated(const void *k, const void *v, const float *alpha, float *S, float *z, int B,
+                                 int H, int N, int dk, int dv, la_dtype dtype, la_stream_t stream);
+la_status la_decode_step_gated(float *S, float *z, const void *q, const void *k, const void *v, void *o,
+                               const float *alpha, int B, int H, int dk, int dv, float eps, la_dtype dtype,
+                               la_stream_t stream);
+
+/*
  * Variants of the feature map and of the normaliser.
  *
  * Feature maps ("Linear attention", learn.pranaymahendrakar.com, What the
@@ -270,7 +313,7 @@ typedef struct {
  * and results as the specialised entry points, which they reduce to:
  *   la_forward_causal_ex(..., NULL, NULL, ...)   = la_forward_causal
  *   la_forward_causal_ex(..., gamma, NULL, ...)  = la_forward_causal_decay
- * bf16 with dk = dv in {64, 128} (chunk 128 and N >= 128 for the causal form)
+ * bf16 with dk = dv in {64, 128} (and N >= 128 for the causal form)
  * runs on the tensor cores for every variant; other shapes on the CUDA cores.
  * An invalid variant (unknown map, non-finite shift, normalize not 0 or 1)
  * returns LA_ERR_INVALID_ARG.
@@ -347,7 +390,7 @@ la_status la_favor_features(const void *x, const void *w, void *phi, int B, int 
  * attended with the identity map, so each call is two launches or more.
  * w must not overlap o.  Supported: d, dv, m in {32, 64, 128}; the attention
  * step runs on the tensor cores for bf16 with m = dv in {64, 128} (and, causal,
- * chunk 128 and N >= 128), on the CUDA cores otherwise.  m outside the
+ * N >= 128), on the CUDA cores otherwise.  m outside the
  * supported set (0 included) gives LA_ERR_UNSUPPORTED.
  */
 la_status la_forward_causal_favor(const void *q, const void *k, const void *v, void *o, const void *w, int B,
@@ -396,12 +439,13 @@ la_status la_get_device_status(la_stream_t stream);
 
 /*
  * Hooks for the library's own failure-detection tests -- not for production use.
- * They act on the chunk-parallel causal kernel (bf16, dk = dv = 64, chunk 128,
- * elu + 1 with the normaliser, no decay, 16 or more heads in total), whose work
- * items publish per-chunk states that later items wait for.  Both settings are
- * process-wide and apply to launches made after the call.
+ * They act on the causal forward for bf16 with dk = dv = 64 (elu + 1 with the
+ * normaliser, no decay): its chunk-parallel kernel (N > 2048 and 16 or more heads
+ * in total), whose work items publish per-chunk states that later items wait
+ * for, and -- the wait limit only -- its cluster kernel (N <= 2048).  Both
+ * settings are process-wide and apply to launches made after the call.
  *
- * la_test_set_wait_limit_ns(ns): every bounded wait of that kernel gives up after
+ * la_test_set_wait_limit_ns(ns): every bounded wait of those kernels gives up after
  * ns nanoseconds instead of 2 s (0 restores 2 s).  A wait that gives up records
  * LA_ERR_TIMEOUT for la_get_device_status() and raises the launch's abort word, so
  * every CTA of the launch stops taking work, drains its copies and tensor-core

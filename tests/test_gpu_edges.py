@@ -353,3 +353,49 @@ def test_more_output_guard_canaries(path):
         assert untouched(b), path
         assert bool(torch.isfinite(o.float()).all()), path
 
+
+
+# ------------------------------------------------------------------ per-thread default streams
+def test_per_thread_default_streams_get_their_own_workspaces(orc):
+    """Two host threads, one after the other, call the bf16 tensor-core forwards on
+    cudaStreamPerThread (each thread's own stream, whose workspaces are keyed by the
+    thread as well as the handle) while the main thread's work on another stream is
+    still queued: every result matches the oracle.  The threads make no CUDA call of
+    their own before the library's (it binds the primary context to a thread that
+    has none)."""
+    import ctypes
+    import threading
+    lib = la().load_library()
+    per_thread = ctypes.c_void_p(2)  # cudaStreamPerThread
+    cases = [workloads.random_inputs(44000 + t, 4, 8, 4096, 64, 64, "bf16") for t in range(2)]
+    refs = [(orc.causal_recurrent(*c), orc.noncausal(*c)) for c in cases]
+    devs = [dev(*c, dtype="bf16") for c in cases]
+    reps = 3
+    outs = [[[torch.empty_like(d[2]) for _ in range(2)] for _ in range(reps)] for d in devs]
+    torch.cuda.synchronize()
+    status = [[], []]
+
+    def worker(t):
+        q, k, v = devs[t]
+        B, H, N, d = q.shape
+        for r in range(reps):
+            status[t].append(lib.la_forward_causal(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                                   outs[t][r][0].data_ptr(), B, H, N, d, d, 128, ctypes.c_float(1e-6),
+                                                   1, per_thread))
+            status[t].append(lib.la_forward_noncausal(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                                      outs[t][r][1].data_ptr(), B, H, N, d, d, ctypes.c_float(1e-6),
+                                                      1, per_thread))
+        status[t].append(int(torch.cuda.synchronize() is None))
+
+    for t in range(2):  # one thread after the other
+        th = threading.Thread(target=worker, args=(t,))
+        th.start()
+        th.join(timeout=120)
+        assert not th.is_alive()
+    torch.cuda.synchronize()
+    assert la().la_get_device_status() == 0
+    for t in range(2):
+        assert all(st == 0 for st in status[t][:-1]), status[t]
+        for r in range(reps):
+            check(from_dev(outs[t][r][0]), refs[t][0], "bf16", ("per-thread causal", t, r))
+            check(from_dev(outs[t][r][1]), refs[t][1], "bf16", ("per-thread noncausal", t, r))

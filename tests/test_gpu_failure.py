@@ -37,11 +37,11 @@ def la():
 
 @pytest.mark.parametrize("ticket", [40, 0, 33])
 def test_lost_publication_times_out_and_the_next_call_is_clean(orc, ticket):
-    """B4 H8 N2048 d64 (32 heads x 16 chunks; ticket t is chunk t // 32 of head
-    t % 32): ticket 40 is chunk 1 of head 8, 0 is chunk 0 of head 0 (its inclusive
-    prefix is lost), 33 is chunk 1 of head 1."""
+    """B4 H8 N4096 d64 (32 heads x 32 chunks, the chunk-parallel kernel; ticket t is
+    chunk t // 32 of head t % 32): ticket 40 is chunk 1 of head 8, 0 is chunk 0 of
+    head 0 (its inclusive prefix is lost), 33 is chunk 1 of head 1."""
     lib = la().load_library()
-    q, k, v = workloads.random_inputs(51000 + ticket, 4, 8, 2048, 64, 64, "bf16")
+    q, k, v = workloads.random_inputs(51000 + ticket, 4, 8, 4096, 64, 64, "bf16")
     dq, dk_, dv_ = to_dev(q, "bf16"), to_dev(k, "bf16"), to_dev(v, "bf16")
     assert la().la_get_device_status() == 0
     lib.la_test_set_wait_limit_ns(2_000_000)
@@ -69,9 +69,15 @@ def test_lost_publication_times_out_and_the_next_call_is_clean(orc, ticket):
 
 
 def test_short_wait_limit_alone_does_not_fire(orc):
-    """With every publication made, a 50 ms limit never runs out on the headline shape."""
+    """With every publication made, a 50 ms limit never runs out (the chunk-parallel
+    kernel at B4 H8 N4096 and the cluster kernel at the headline shape B4 H8 N2048)."""
     lib = la().load_library()
-    q, k, v = workloads.random_inputs(53000, 4, 8, 2048, 64, 64, "bf16")
+    for N in (4096, 2048):
+        q, k, v = workloads.random_inputs(53000 + N, 4, 8, N, 64, 64, "bf16")
+        _short_limit_case(lib, orc, q, k, v)
+
+
+def _short_limit_case(lib, orc, q, k, v):
     dq, dk_, dv_ = to_dev(q, "bf16"), to_dev(k, "bf16"), to_dev(v, "bf16")
     lib.la_test_set_wait_limit_ns(50_000_000)
     try:

@@ -98,6 +98,16 @@ def test_causal_chunk_parallel_shapes(orc, B, H, N):
     assert tail["normwise"] < 2e-2, tail
 
 
+@pytest.mark.parametrize("B,H,N,d", [(2, 3, 1000, 64), (1, 2, 3000, 128), (4, 8, 2048, 64)])
+def test_causal_chunk64_runs_on_the_tensor_cores(orc, B, H, N, d):
+    """bf16 with chunk = 64 takes the tensor-core path (128-token tiles: the chunked form
+    is the same function for any chunk length) and matches the oracle."""
+    q, k, v = workloads.random_inputs(6200 + N + d, B, H, N, d, d, "bf16")
+    got = run_causal(q, k, v, "bf16", 64)
+    e = assert_parity(got, orc.causal_recurrent(q, k, v), "bf16", (B, H, N, d, "chunk 64"))
+    assert e["normwise"] < 2e-2, e
+
+
 def test_causal_chunk_parallel_repeatable(orc):
     """Which published prefix a look-back finds nearest depends on timing, so the
     order of the fp32 additions may differ between calls: repeated calls all match
