@@ -11,29 +11,40 @@
 //  * CTA r of a head's cluster holds the head's chunks [r L, (r+1) L),
 //    L = ceil(n_c / 4) <= 4, all of them in shared memory at once (Q, K and V
 //    loaded by TMA at the start; O is later staged in each chunk's Q tile).
-//  * Phase A, on the tensor cores: the chunk states accumulate in tensor memory,
-//    A = sum_{p' <= p} phi(K_p')^T [V_p' | 1] after chunk p; the scan warps read
-//    each running sum back (its rows repeated in the upper lanes, so that every
-//    lane quadrant sees all 64 key features).
+//  * Phase A, on the tensor cores: the state of chunk p, phi(K_p)^T [V_p | 1], in
+//    its own TMEM columns (its rows repeated in the upper lanes, so that every lane
+//    quadrant sees all 64 key features); the scan threads read the four back once
+//    and form the running sums after each chunk in registers.
 //  * Scan: each CTA puts its segment total (fp32) in its shared memory, and the
 //    CTAs of higher rank add up the totals of the lower ranks straight from their
 //    shared memory (ld.shared::cluster), synchronised by remote mbarrier arrivals
 //    with release / acquire at cluster scope: E_r, the state before the segment.
 //  * Output, on the tensor cores, for chunk p of the segment with image
-//    bf16(E_r + A up to chunk p - 1) (and z as a bf16 high + low pair):
+//    bf16(E_r + running sum up to chunk p - 1) (and z as a bf16 high + low pair):
 //      T = phi(Q_p) phi(K_p)^T,  P = bf16(tril T) over T in TMEM,
 //      O = P [V_p | 1] + phi(Q_p) [image | z],  o = O / max(rowsum + phi(q) z, eps).
-//    T, P and P V of every chunk run before the scan; only phi(Q) [image | z]
-//    waits for it.  The images of all chunks are written right after the scan,
-//    each into its chunk's K tile (no MMA reads K by then), so no chunk waits on
-//    the chunk before it.
+//    Only phi(Q) [image | z] waits for the scan.  The images go into each chunk's
+//    K tile once T of that chunk (and of its pair) has completed, two chunks at a
+//    time, so no chunk waits on the chunk before it.
 //
-// Warp roles (512 threads): warps 0-3 turn T into P, warps 4-7 normalise and store
-// O, and both groups (256 threads) do the scan and write the images; warp 8 TMA;
-// warp 9 MMA and TMEM; warps 10-15 phi.  Every wait is bounded (Params::wait_ns);
-// on expiry the CTA records LA_ERR_TIMEOUT in this file's status word and winds
-// down.  No CTA returns early: every one reaches the final cluster barrier, so none
-// leaves while a peer may still read its shared memory or arrive on its barriers.
+// Warp roles (512 threads): warps 0-3 and 4-7 are two groups that each cover the
+// four TMEM lane quadrants.  Together (256 threads) they apply phi to every K tile
+// as it lands, read the chunk states, do the scan and write the images; group g
+// turns T into P and normalises and stores O for the chunks p with p % 2 == g.
+// Warp 8: TMA.  Warp 9: MMA issue and TMEM.  Warps 10-12, 14, 15: phi of the Q
+// tiles (warp 13, on the MMA warp's sub-partition, idles).  The order within the
+// groups was set by a %globaltimer trace of the launch: phi of K first (the
+// groups are otherwise idle while the loads land), the segment total published
+// right after phase A, T -> P of the group's first chunk before the cross-CTA sum
+// (the sum's distributed-shared-memory reads take about 0.6 us for the highest
+// rank), and T -> P of the second chunk after the first images.  In the tail the
+// MMA issue thread is the limit: each group of 4 or 8 MMAs takes 400-600 cycles
+// from the first issue to the commit.
+//
+// Every wait is bounded (Params::wait_ns); on expiry the CTA records LA_ERR_TIMEOUT
+// in this file's status word and winds down.  No CTA returns early: every one
+// reaches the final cluster barrier, so none leaves while a peer may still read its
+// shared memory or arrive on its barriers.
 #include "la_common.cuh"
 #include "la_internal.h"
 #include "la_sm100.cuh"
@@ -56,10 +67,26 @@ constexpr int kLmax = 4;                 // chunks per CTA
 constexpr int kThreads = 512;
 constexpr uint32_t kTile = kC * D * 2;   // 16 KB
 constexpr uint32_t kSbBytes = D * D * 2; // 8 KB bf16 image
-constexpr int kOWarp0 = 4, kTmaWarp = 8, kMmaWarp = 9, kPhiWarp0 = 10;
-constexpr int kScanThreads = 256, kPhiThreads = 192;
-constexpr uint32_t tO = 256, kOStride = 80, tA = 416;  // TMEM: T/P buffers at 0 and 128
-static_assert(tO + 2 * kOStride <= tA && tA + 80 <= 512, "TMEM column groups overlap");
+constexpr int kTmaWarp = 8, kMmaWarp = 9, kPhiWarp0 = 10;
+constexpr int kScanThreads = 256, kPhiThreads = 160;
+// The phi warps are 10, 11, 12, 14 and 15: warp 13 would share a sub-partition (warp
+// index mod 4) with the MMA warp, whose issue rate drops severalfold while another
+// warp of its sub-partition has work; it stays idle.
+constexpr int kIdleWarp = 13;
+static_assert(kIdleWarp % 4 == kMmaWarp % 4, "the idle warp shares the MMA warp's sub-partition");
+
+// TMEM columns.  T / P buffers at 0 and 128; O buffers at 256, 336 and 416 (chunk
+// 2; chunk 3 reuses chunk 1's).  Phase A puts chunk p's state in its own group of 80
+// columns, the first three in the T / P area and the fourth at 416; all are read
+// before the first T is issued.  (Keeping the T / P buffers clear, so that T(0) need
+// not wait for the read, measured 0.4 us slower per launch.)
+constexpr uint32_t tO0 = 256, tO1 = 336, tA3 = 416;
+__host__ __device__ constexpr uint32_t a_col(int p) { return p < 3 ? 80u * (uint32_t)p : tA3; }
+// O buffer of chunk p (0: chunk 0, 1: chunks 1 and 3, 2: chunk 2) and its column
+__host__ __device__ constexpr int o_buf(int p) { return p == 0 ? 0 : p == 2 ? 2 : 1; }
+__host__ __device__ constexpr uint32_t o_col(int b) { return b == 0 ? tO0 : b == 1 ? tO1 : tA3; }
+static_assert(a_col(2) + 80 <= tO0 && tO0 + 80 <= tO1 && tO1 + 80 <= tA3 && tA3 + 80 <= 512,
+              "TMEM column groups overlap");
 constexpr uint32_t kDrainNs = 100000000u;
 
 struct alignas(1024) Smem {
@@ -73,9 +100,11 @@ struct alignas(1024) Smem {
     alignas(1024) uint8_t ones[kC * 128];
     float xz[D];
     uint64_t kv_full[kLmax], q_full[kLmax], k_ready[kLmax], q_ready[kLmax];
-    uint64_t a_full, a_free, drain;
-    uint64_t t_full[2], p_full[2], pv_done[2], o_full[2], o_free[2], o_staged[2];
-    uint64_t img_ready;  // the images of every chunk are in place
+    uint64_t a_full, a_read, drain;  // phase A done (one-shot); its states read (one-shot)
+    uint64_t t_full[2], p_full[2], pv_done[2];
+    uint64_t o_full[3], o_staged[3], o_free;  // per O buffer; o_free: buffer 1 read (chunk 1)
+    uint64_t t_done[2];     // T of chunks 2 j, 2 j + 1 completed (one-shot, from the MMA warp)
+    uint64_t img_ready[2];  // the images of chunks 2 j, 2 j + 1 are in place (one-shot)
     uint64_t scan_sync;  // the scan threads' barrier (bounded)
     uint64_t agg_ready;  // the lower ranks' totals are readable (their remote arrivals)
     uint32_t tmem_base;
@@ -181,21 +210,26 @@ causal_cluster_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_co
         for (int p = 0; p < kLmax; ++p) {
             mbar_init(&sm.kv_full[p], 1);
             mbar_init(&sm.q_full[p], 1);
-            mbar_init(&sm.k_ready[p], kPhiThreads);
+            mbar_init(&sm.k_ready[p], kScanThreads);
             mbar_init(&sm.q_ready[p], kPhiThreads);
         }
         mbar_init(&sm.a_full, 1);
-        mbar_init(&sm.a_free, kScanThreads);
+        mbar_init(&sm.a_read, kScanThreads);
+        mbar_init(&sm.o_free, 128);
+        for (int b = 0; b < 3; ++b) {
+            mbar_init(&sm.o_full[b], 1);
+            mbar_init(&sm.o_staged[b], 128);
+        }
         mbar_init(&sm.drain, 1);
         for (int b = 0; b < 2; ++b) {
             mbar_init(&sm.t_full[b], 1);
             mbar_init(&sm.p_full[b], 128);
             mbar_init(&sm.pv_done[b], 1);
-            mbar_init(&sm.o_full[b], 1);
-            mbar_init(&sm.o_free[b], 128);
-            mbar_init(&sm.o_staged[b], 128);
         }
-        mbar_init(&sm.img_ready, kScanThreads);
+        for (int j = 0; j < 2; ++j) {
+            mbar_init(&sm.t_done[j], 1);
+            mbar_init(&sm.img_ready[j], kScanThreads);
+        }
         mbar_init(&sm.scan_sync, kScanThreads);
         mbar_init(&sm.agg_ready, max(rank, 1));  // one arrival per lower rank
         sm.abort = layout_ok ? 0 : 1;
@@ -215,19 +249,17 @@ causal_cluster_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_co
     const uint32_t tmem = sm.tmem_base;
     int *abort_flag = &sm.abort;
 
-    if (warp >= kPhiWarp0) {
-        // ---------------------------------------------------------------- phi warps: K first, then Q
-        const int t = tid - kPhiWarp0 * 32;
+    if (warp == kIdleWarp) {
+        // nothing: see kIdleWarp
+    } else if (warp >= kPhiWarp0) {
+        // ---------------------------------------------------------------- phi warps: every Q tile
+        // (warps 0-7 take every K tile as it lands)
+        const int t = (warp - kPhiWarp0 - (warp > kIdleWarp ? 1 : 0)) * 32 + lane;
         bool ok = true;
-        for (int p = 0; p < nch && ok; ++p) {
-            if (!(ok = wait_bar_warp(prm, abort_flag, &sm.kv_full[p], 0))) break;
-            phi_tile<D, kPhiThreads>(sm.k[p], t, prm.N - (c0 + p) * kC);
-            fence_proxy_async_smem();
-            mbar_arrive(&sm.k_ready[p]);
-        }
+#pragma unroll 1
         for (int p = 0; p < nch && ok; ++p) {
             if (!(ok = wait_bar_warp(prm, abort_flag, &sm.q_full[p], 0))) break;
-            phi_tile<D, kPhiThreads>(sm.q[p], t, prm.N - (c0 + p) * kC);
+            phi_tile_rolled<D>(sm.q[p], t, kPhiThreads, prm.N - (c0 + p) * kC);
             fence_proxy_async_smem();
             mbar_arrive(&sm.q_ready[p]);
         }
@@ -263,19 +295,20 @@ causal_cluster_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_co
             const uint32_t id_KV = idesc_bf16_f32(128, D + 16, true, true);  // phi(K)^T [V | 1]
             const uint32_t ones = smem_u32(sm.ones);
             bool ok = true;
-            // Phase A: running sums of the chunk states.  phi(K)^T is MN-major; its second
-            // 64-row block has offset 0 (LBO = 0), so rows 64..127 of A repeat rows 0..63.
+            // Phase A: the state of each chunk in its own columns.  phi(K)^T is MN-major;
+            // its second 64-row block has offset 0 (LBO = 0), so rows 64..127 of each
+            // state repeat rows 0..63.
+#pragma unroll 1
             for (int p = 0; p < nch && ok; ++p) {
                 if (!(ok = wait_bar(prm, abort_flag, &sm.k_ready[p], 0))) break;
-                if (p > 0 && !(ok = wait_bar(prm, abort_flag, &sm.a_free, (p - 1) & 1))) break;
                 tc_fence_after();
                 const uint32_t ka = smem_u32(sm.k[p]), va = smem_u32(sm.v[p]);
                 const uint64_t dkt = mnmajor(ka, 0, 0), dv = mnmajor(va, 0, ones - va);
 #pragma unroll
                 for (int kk = 0; kk < kC / 16; ++kk)
-                    mma_ss(tmem + tA, dkt + 128 * kk, dv + 128 * kk, id_KV, (p > 0 || kk > 0) ? 1u : 0u);
-                mma_commit(&sm.a_full);
+                    mma_ss(tmem + a_col(p), dkt + 128 * kk, dv + 128 * kk, id_KV, kk > 0 ? 1u : 0u);
             }
+            if (ok && nch > 0) mma_commit(&sm.a_full);
             auto issue_T = [&](int p) -> bool {
                 if (!wait_bar(prm, abort_flag, &sm.q_ready[p], 0)) return false;
                 if (p >= 2 && !wait_bar(prm, abort_flag, &sm.pv_done[p & 1], ((p - 2) >> 1) & 1)) return false;
@@ -289,14 +322,14 @@ causal_cluster_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_co
             };
             auto issue_PV = [&](int p) -> bool {
                 if (!wait_bar(prm, abort_flag, &sm.p_full[p & 1], (p >> 1) & 1)) return false;
-                if (p >= 2 && !wait_bar(prm, abort_flag, &sm.o_free[p & 1], ((p - 2) >> 1) & 1)) return false;
+                if (p == 3 && !wait_bar(prm, abort_flag, &sm.o_free, 0)) return false;  // chunk 1's O read
                 tc_fence_after();
                 const uint32_t va = smem_u32(sm.v[p]);
                 const uint64_t dv = mnmajor(va, 0, ones - va);
-                const uint32_t dO = tmem + tO + (p & 1) * kOStride, dP = tmem + (p & 1) * 128;
+                const uint32_t dO = tmem + o_col(o_buf(p)), dP = tmem + (p & 1) * 128;
 #pragma unroll
                 for (int kk = 0; kk < kC / 16; ++kk) mma_ts(dO, dP + kk * 8, dv + 128 * kk, id_PV, kk > 0 ? 1u : 0u);
-                mma_commit(&sm.pv_done[p & 1]);
+                if (p < 2) mma_commit(&sm.pv_done[p & 1]);  // only T(p + 2) waits for it
                 return true;
             };
             auto issue_QS = [&](int p) -> bool {
@@ -306,24 +339,28 @@ causal_cluster_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_co
                     // z block in the second half (an LBO of 8 KB)
                     const uint64_t dsb = mnmajor(smem_u32(sm.k[p]), 0, kSbBytes);
                     const uint64_t dq = kmajor(smem_u32(sm.q[p]), 0);
-                    const uint32_t dO = tmem + tO + (p & 1) * kOStride;
+                    const uint32_t dO = tmem + o_col(o_buf(p));
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) mma_ss(dO, dq + 2 * kk, dsb + 128 * kk, id_QS, 1u);
                 }
-                mma_commit(&sm.o_full[p & 1]);
+                mma_commit(&sm.o_full[o_buf(p)]);
                 return true;
             };
             // Before the scan: T of every chunk and P V of the first two (their O buffers
             // are free); T of chunk p >= 2 needs P V of chunk p - 2 done with its buffer.
             const int pre = min(2, nch);
+            if (ok && nch > 0) ok = wait_bar(prm, abort_flag, &sm.a_read, 0);
             for (int p = 0; p < pre && ok; ++p) ok = issue_T(p);
+            if (ok) mma_commit(&sm.t_done[0]);
             for (int p = 0; p < pre && ok; ++p) ok = issue_PV(p);
             for (int p = 2; p < nch && ok; ++p) ok = issue_T(p);
-            // After the scan: the state term of each chunk (and P V of chunks 2, 3, whose O
-            // buffers free up as the first outputs are written).
-            if (ok && nch > 0) ok = wait_bar(prm, abort_flag, &sm.img_ready, 0);
+            if (ok) mma_commit(&sm.t_done[1]);
+            // After the scan: the state term of each chunk once its pair's images are in
+            // place (and P V of chunks 2, 3, whose O buffers free up as the first
+            // outputs are written).
             for (int p = 0; p < nch && ok; ++p) {
                 if (p >= 2 && !(ok = issue_PV(p))) break;
+                if ((p & 1) == 0 && !(ok = wait_bar(prm, abort_flag, &sm.img_ready[p >> 1], 0))) break;
                 ok = issue_QS(p);
             }
             // all issued MMAs complete before TMEM is freed
@@ -337,134 +374,151 @@ causal_cluster_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_co
         // h = 2 (warp / 4) + q / 2; h = 0 also owns z_i.
         const int q = warp & 3;
         const int i = 32 * (q & 1) + lane, h = 2 * (warp >> 2) + (q >> 1);
-        const bool is_o = warp >= kOWarp0;
         const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16);
         uint32_t syncs = 0;
         bool ok = true;
-        // ---- phase A: the running sums after each chunk.  The images need those after
-        // chunks 0 .. L-2 (kept in registers); the one after the last chunk is the
-        // segment total, which goes straight to the exchange buffer for the peers.
+        // ---- phase A: the chunk states, read once all are in place; the running sums
+        // after chunks 0 .. L-2 stay in registers for the images, the one after the
+        // last chunk is the segment total, which goes to the exchange buffer.
         float cum[kLmax - 1][16], cz[kLmax - 1];
         float4 *xb = sm.xch;
+        // ---- phi of every K tile as it lands (phase A of a chunk follows at once)
+#pragma unroll 1
+        for (int p = 0; p < nch && ok; ++p) {
+            if (!(ok = wait_bar_warp(prm, abort_flag, &sm.kv_full[p], 0))) break;
+            phi_tile_rolled<D>(sm.k[p], tid, kScanThreads, prm.N - (c0 + p) * kC);
+            fence_proxy_async_smem();
+            mbar_arrive(&sm.k_ready[p]);
+        }
+        // ---- T -> P of chunk p, by group g = warp / 4 for the chunks p with p % 2 == g
+        // (T, P and O buffer g): row 32 q + lane of T; key block kb is visible for
+        // kb < q, masked on the diagonal for kb == q, zero for kb > q; 16 keys at a time,
+        // P half-block hb of key block kb over columns 16 kb + 8 hb .., i.e. over T
+        // columns 32 kb + 16 hb .. already read
+        const int g = warp >> 2;
+        auto t_to_p = [&](int p) -> bool {
+            if (!wait_bar_warp(prm, abort_flag, &sm.t_full[g], (p >> 1) & 1)) return false;
+            tc_fence_after();
+            const uint32_t tb = tl + g * 128;
 #pragma unroll
-        for (int p = 0; p < kLmax; ++p) {
-            if (p < kLmax - 1) {
+            for (int kb = 0; kb < 4; ++kb) {
 #pragma unroll
-                for (int e = 0; e < 16; ++e) cum[p][e] = 0.f;
-                cz[p] = 0.f;
-            }
-            if (p < nch && ok) {
-                ok = wait_bar_warp(prm, abort_flag, &sm.a_full, p & 1);
-                if (ok) {
-                    tc_fence_after();
-                    uint32_t a[16];
-                    tmem_ld16(tl + tA + 16 * h, a);
-                    const uint32_t zr = tmem_ld1(tl + tA + D);
-                    tmem_ld_wait();
-                    tc_fence_before();
-                    mbar_arrive(&sm.a_free);
-                    if (p == nch - 1) {
+                for (int hb = 0; hb < 2; ++hb) {
+                    uint32_t pk[8];
+                    if (kb <= q) {
+                        uint32_t t[16];
+                        tmem_ld16(tb + kb * 32 + 16 * hb, t);
+                        tmem_ld_wait();
 #pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            xb[(4 * h + e) * D + i] = make_float4(__uint_as_float(a[4 * e]), __uint_as_float(a[4 * e + 1]),
-                                                                  __uint_as_float(a[4 * e + 2]), __uint_as_float(a[4 * e + 3]));
-                        if (h == 0) sm.xz[i] = __uint_as_float(zr);
-                    } else if (p < kLmax - 1) {
+                        for (int e = 0; e < 8; ++e) {
+                            const int jk = 16 * hb + 2 * e;  // key offset within the block
+                            pk[e] = (kb < q) ? pack_bf16(__uint_as_float(t[2 * e]), __uint_as_float(t[2 * e + 1]))
+                                             : pack_bf16(jk <= lane ? __uint_as_float(t[2 * e]) : 0.f,
+                                                         jk + 1 <= lane ? __uint_as_float(t[2 * e + 1]) : 0.f);
+                        }
+                    } else {
 #pragma unroll
-                        for (int e = 0; e < 16; ++e) cum[p][e] = __uint_as_float(a[e]);
-                        cz[p] = h == 0 ? __uint_as_float(zr) : 0.f;
+                        for (int e = 0; e < 8; ++e) pk[e] = 0u;
                     }
+                    tmem_st8(tb + kb * 16 + 8 * hb, pk);
                 }
             }
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(&sm.p_full[g]);
+            return true;
+        };
+        if (ok && nch > 0) {
+            ok = wait_bar_warp(prm, abort_flag, &sm.a_full, 0);
+            if (ok) tc_fence_after();
+        }
+        {
+            float run[16], rz = 0.f;
+#pragma unroll
+            for (int e = 0; e < 16; ++e) run[e] = 0.f;
+#pragma unroll
+            for (int p = 0; p < kLmax; ++p) {
+                if (p < nch && ok) {
+                    uint32_t a[16];
+                    tmem_ld16(tl + a_col(p) + 16 * h, a);
+                    const uint32_t zr = tmem_ld1(tl + a_col(p) + D);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) run[e] += __uint_as_float(a[e]);
+                    rz += h == 0 ? __uint_as_float(zr) : 0.f;
+                }
+                if (p < kLmax - 1) {
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) cum[p][e] = run[e];
+                    cz[p] = rz;
+                }
+                if (p == nch - 1 && ok) {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        xb[(4 * h + e) * D + i] = make_float4(run[4 * e], run[4 * e + 1], run[4 * e + 2], run[4 * e + 3]);
+                    if (h == 0) sm.xz[i] = rz;
+                }
+            }
+        }
+        if (ok && nch > 0) {
+            tc_fence_before();
+            mbar_arrive(&sm.a_read);
         }
         if (ok && nch == 0) {  // no chunks: a zero total
 #pragma unroll
             for (int e = 0; e < 4; ++e) xb[(4 * h + e) * D + i] = make_float4(0.f, 0.f, 0.f, 0.f);
             if (h == 0) sm.xz[i] = 0.f;
         }
-        // ---- T -> P (warps 0-3): row 32 q + lane of T; key block kb is visible for
-        // kb < q, masked on the diagonal for kb == q, zero for kb > q; P block kb over
-        // columns 16 kb .. 16 kb + 15 of the buffer (T blocks already read or unused)
-        if (!is_o) {
-            for (int p = 0; p < nch && ok; ++p) {
-                if (!(ok = wait_bar_warp(prm, abort_flag, &sm.t_full[p & 1], (p >> 1) & 1))) break;
-                tc_fence_after();
-                const uint32_t tb = tl + (p & 1) * 128;
-                // (16 keys at a time: P half-block hb of key block kb goes to columns
-                // 16 kb + 8 hb .., over T columns 32 kb + 16 hb .. already read)
-#pragma unroll
-                for (int kb = 0; kb < 4; ++kb) {
-#pragma unroll
-                    for (int hb = 0; hb < 2; ++hb) {
-                        uint32_t pk[8];
-                        if (kb <= q) {
-                            uint32_t t[16];
-                            tmem_ld16(tb + kb * 32 + 16 * hb, t);
-                            tmem_ld_wait();
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) {
-                                const int jk = 16 * hb + 2 * e;  // key offset within the block
-                                pk[e] = (kb < q) ? pack_bf16(__uint_as_float(t[2 * e]), __uint_as_float(t[2 * e + 1]))
-                                                 : pack_bf16(jk <= lane ? __uint_as_float(t[2 * e]) : 0.f,
-                                                             jk + 1 <= lane ? __uint_as_float(t[2 * e + 1]) : 0.f);
-                            }
-                        } else {
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) pk[e] = 0u;
-                        }
-                        tmem_st8(tb + kb * 16 + 8 * hb, pk);
-                    }
-                }
-                tmem_st_wait();
-                tc_fence_before();
-                mbar_arrive(&sm.p_full[p & 1]);
-            }
-        }
-        // ---- scan across the cluster: E = the sum of the lower ranks' segment totals
-        float E[16], ez = 0.f;
-#pragma unroll
-        for (int e = 0; e < 16; ++e) E[e] = 0.f;
+        // ---- publish the total to the higher ranks right after phase A
         if (ok) {
             ok = scan_barrier(prm, sm, abort_flag, syncs);  // every thread's part is written
             if (ok && tid == 0)
                 for (int r2 = rank + 1; r2 < kG; ++r2) mbar_arrive_remote_release(mapa_shared(smem_u32(&sm.agg_ready), r2));
-            if (ok && rank > 0) ok = wait_bar_warp(prm, abort_flag, &sm.agg_ready, 0, true);
-            if (ok) {  // two peers' loads in flight at a time
+        }
+        if (ok && g < nch) ok = t_to_p(g);
+        // ---- scan across the cluster: E = the sum of the lower ranks' segment totals
+        float E[16], ez = 0.f;
 #pragma unroll
-                for (int r0 = 0; r0 < kG - 1; r0 += 2) {
-                    float4 x[2][4];
-                    float zx[2] = {0.f, 0.f};
+        for (int e = 0; e < 16; ++e) E[e] = 0.f;
+        if (ok && rank > 0) ok = wait_bar_warp(prm, abort_flag, &sm.agg_ready, 0, true);
+        if (ok) {  // two peers' loads in flight at a time
 #pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const int r2 = r0 + u;
-                        if (r2 < rank) {
+            for (int r0 = 0; r0 < kG - 1; r0 += 2) {
+                float4 x[2][4];
+                float zx[2] = {0.f, 0.f};
 #pragma unroll
-                            for (int e = 0; e < 4; ++e)
-                                x[u][e] = ld_dsmem_f4(mapa_shared(smem_u32(xb + (4 * h + e) * D + i), r2));
-                            if (h == 0) zx[u] = ld_dsmem_f32(mapa_shared(smem_u32(&sm.xz[i]), r2));
-                        }
+                for (int u = 0; u < 2; ++u) {
+                    const int r2 = r0 + u;
+                    if (r2 < rank) {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            x[u][e] = ld_dsmem_f4(mapa_shared(smem_u32(xb + (4 * h + e) * D + i), r2));
+                        if (h == 0) zx[u] = ld_dsmem_f32(mapa_shared(smem_u32(&sm.xz[i]), r2));
                     }
+                }
 #pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        if (r0 + u < rank) {
+                for (int u = 0; u < 2; ++u) {
+                    if (r0 + u < rank) {
 #pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                E[4 * e] += x[u][e].x; E[4 * e + 1] += x[u][e].y;
-                                E[4 * e + 2] += x[u][e].z; E[4 * e + 3] += x[u][e].w;
-                            }
-                            ez += zx[u];
+                        for (int e = 0; e < 4; ++e) {
+                            E[4 * e] += x[u][e].x; E[4 * e + 1] += x[u][e].y;
+                            E[4 * e + 2] += x[u][e].z; E[4 * e + 3] += x[u][e].w;
                         }
+                        ez += zx[u];
                     }
                 }
             }
         }
         // ---- images: chunk p sees E + (running sum after chunk p - 1), written as bf16
-        // into the first half of the chunk's K tile and z into the second half.  The
-        // K tiles are free: every T and A MMA completed before the scan (the T -> P
-        // warps saw t_full of every chunk, the scan threads a_full).
-        if (ok) {
+        // into the first half of the chunk's K tile and z into the second half, once
+        // no MMA reads that K tile any more: phase A is over (the scan read every
+        // running sum) and T of chunks 2 j, 2 j + 1 completed (t_done[j], a one-shot
+        // barrier).  Pair j then releases the state terms of its chunks (img_ready[j]).
+        auto images = [&](int j) -> bool {
+            if (!wait_bar_warp(prm, abort_flag, &sm.t_done[j], 0)) return false;
 #pragma unroll
-            for (int p = 0; p < kLmax; ++p) {
+            for (int u = 0; u < 2; ++u) {
+                const int p = 2 * j + u;
                 if (p < nch) {
                     float x[16];
                     float zv = ez;
@@ -476,19 +530,24 @@ causal_cluster_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_co
                 }
             }
             fence_proxy_async_smem();
-            mbar_arrive(&sm.img_ready);
-        }
-        if (is_o) {
-            // ---- O out (warps 4-7): o = O / max(den, eps) as bf16, staged in the chunk's Q
-            // tile (no MMA reads it once O is final), written by a TMA store.
+            mbar_arrive(&sm.img_ready[j]);
+            return true;
+        };
+        if (ok && nch > 0) ok = images(0);
+        if (ok && g + 2 < nch) ok = t_to_p(g + 2);
+        if (ok && nch > 2) ok = images(1);
+        {
+            // ---- O out (this group's chunks): o = O / max(den, eps) as bf16, staged in
+            // the chunk's Q tile (no MMA reads it once O is final), written by a TMA store.
             const int row = q * 32 + lane;
-            const bool leader = warp == kOWarp0 && lane == 0;
+            const bool leader = (warp & 3) == 0 && lane == 0;
             const uint64_t pol = l2_policy_evict_first();
-            for (int p = 0; p < nch && ok; ++p) {
-                const int b = p & 1;
-                if (!(ok = wait_bar_warp(prm, abort_flag, &sm.o_full[b], (p >> 1) & 1))) break;
+            for (int p = g; p < nch && ok; p += 2) {
+                const int b = o_buf(p);
+                const uint32_t ph = p == 3 ? 1u : 0u;  // buffer 1 holds chunk 1, then chunk 3
+                if (!(ok = wait_bar_warp(prm, abort_flag, &sm.o_full[b], ph))) break;
                 tc_fence_after();
-                const uint32_t to = tl + tO + b * kOStride;
+                const uint32_t to = tl + o_col(b);
                 const float den = __uint_as_float(tmem_ld1(to + D)) + __uint_as_float(tmem_ld1(to + D + 1));
                 tmem_ld_wait();
                 const float inv = 1.f / fmaxf(den, prm.eps);
@@ -511,10 +570,12 @@ causal_cluster_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_co
                 }
                 fence_proxy_async_smem();
                 mbar_arrive(&sm.o_staged[b]);
-                tc_fence_before();
-                mbar_arrive(&sm.o_free[b]);
+                if (p == 1) {
+                    tc_fence_before();
+                    mbar_arrive(&sm.o_free);
+                }
                 bool st_ok = true;
-                if (leader && (st_ok = wait_bar(prm, abort_flag, &sm.o_staged[b], (p >> 1) & 1))) {
+                if (leader && (st_ok = wait_bar(prm, abort_flag, &sm.o_staged[b], ph))) {
                     tma_store_3d_hint(&map_o, sm.q[p], 0, (c0 + p) * kC, bh, pol);
                     tma_store_commit();
                 }

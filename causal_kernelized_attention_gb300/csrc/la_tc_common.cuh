@@ -191,6 +191,32 @@ __device__ __forceinline__ void phi_tile(uint8_t *tile, int t, int valid, float 
     }
 }
 
+// phi_tile (elu + 1, no weights) as a loop that is not unrolled, for nt threads
+// given at run time: one unit (16 independent packed phi pairs) per trip.  The
+// code is a few hundred bytes, so a kernel that runs it a few times per launch
+// fetches it once; the unrolled form is several kilobytes per call site, each
+// run from a cold instruction cache.
+template <int D>
+__device__ __forceinline__ void phi_tile_rolled(uint8_t *tile, int t, int nt, int valid)
+{
+    constexpr int kUnits = 128 * (D / 32);
+#pragma unroll 1
+    for (int u = t; u < kUnits; u += nt) {
+        const int row = u & 127, hb = u >> 7;
+        uint8_t *rp = tile + (hb >> 1) * kBox + row * 128;
+        const int rot = row + (hb & 1) * 4;
+        uint4 x[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) x[k] = *reinterpret_cast<const uint4 *>(rp + ((rot + k) & 7) * 16);
+        const bool live = row < valid;
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            x[k] = live ? make_uint4(phi2(x[k].x), phi2(x[k].y), phi2(x[k].z), phi2(x[k].w)) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) *reinterpret_cast<uint4 *>(rp + ((rot + k) & 7) * 16) = x[k];
+    }
+}
+
 // phi of two bf16 values in fp32, split into bf16 high parts (returned) and the
 // bf16 rounding of the remainders (*lo): hi + lo carries phi to about 2^-17.
 __device__ __forceinline__ uint32_t phi2_split(uint32_t w, uint32_t *lo)
