@@ -643,12 +643,14 @@ la_status la_get_device_status(la_stream_t stream)
     if (st != LA_OK) return st;
     st = favor_read_status((cudaStream_t)stream, &fv_bits);
     if (st != LA_OK) return st;
-    unsigned cc_bits = 0, cl_bits = 0;
+    unsigned cc_bits = 0, cl_bits = 0, bw_bits = 0;
     st = tc_chunks_read_status((cudaStream_t)stream, &cc_bits);
     if (st != LA_OK) return st;
     st = tc_cluster_read_status((cudaStream_t)stream, &cl_bits);
     if (st != LA_OK) return st;
-    return ((bits | nc_bits | fv_bits | cc_bits | cl_bits) & kStatusTimeout) ? LA_ERR_TIMEOUT : LA_OK;
+    st = tc_backward_read_status((cudaStream_t)stream, &bw_bits);
+    if (st != LA_OK) return st;
+    return ((bits | nc_bits | fv_bits | cc_bits | cl_bits | bw_bits) & kStatusTimeout) ? LA_ERR_TIMEOUT : LA_OK;
 }
 
 int la_version(void) { return 100; }

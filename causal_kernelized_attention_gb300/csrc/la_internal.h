@@ -55,6 +55,12 @@ struct BackwardProblem {
     cudaStream_t stream;
 };
 la_status causal_backward(const BackwardProblem &p);
+// Tensor-core backward (la_tc_backward.cu): bf16, dk = dv = 64, N >= 128.
+bool backward_tc_eligible(const BackwardProblem &p);
+la_status causal_backward_tc(const BackwardProblem &p);
+// Exclusive scan over the nC chunk states (E floats each) of every head, in place:
+// prefix (forward) or suffix (reverse).
+la_status backward_scan(float *buf, int BH, int nC, int E, bool reverse, cudaStream_t s);
 
 // SIMT kernels (la_simt.cu): fp32 CUDA-core arithmetic, any supported dtype.
 la_status causal_simt(const Problem &p);
@@ -108,6 +114,7 @@ la_status tc_noncausal_read_status(cudaStream_t s, unsigned *bits);
 la_status favor_read_status(cudaStream_t s, unsigned *bits);
 la_status tc_chunks_read_status(cudaStream_t s, unsigned *bits);
 la_status tc_cluster_read_status(cudaStream_t s, unsigned *bits);
+la_status tc_backward_read_status(cudaStream_t s, unsigned *bits);
 
 // Failure-detection test hooks (la_test_set_wait_limit_ns, la_test_drop_publication):
 // the limit of the chunk-parallel causal kernel's bounded waits (2 s unless a test

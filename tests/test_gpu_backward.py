@@ -54,6 +54,8 @@ def run_backward(q, k, v, dout, dtype, eps=1e-6):
     (1, 1, 1, 32, 32), (2, 3, 63, 64, 64), (2, 3, 64, 64, 64), (1, 2, 65, 64, 64), (2, 2, 130, 128, 128),
     (1, 3, 300, 64, 128), (2, 2, 257, 128, 64), (1, 2, 1000, 32, 64), (2, 4, 2048, 64, 64),
     (4, 8, 2048, 64, 64),  # the benchmark's backward workload
+    # bf16 d = 64 from 128 tokens runs on the tensor cores: one chunk, ragged tails
+    (1, 2, 128, 64, 64), (2, 3, 200, 64, 64), (1, 2, 255, 64, 64), (2, 2, 1000, 64, 64), (1, 1, 1500, 64, 64),
 ])
 def test_backward_matches_oracle(orc, dtype, B, H, N, dk, dv):
     """One and many chunks, ragged tails, dk != dv, every supported width."""
