@@ -626,8 +626,11 @@ def bench_path_noncausal_variant(torch, la, reps, peaks, src, tag, fmap, shift, 
 
 
 def bench_path_backward(torch, la, reps, peaks, src):
-    """la_backward_causal on the headline causal shape (B=4 H=8 N=2048 d=64, bf16):
-    read q, k, v, dO and write dq, dk, dv once; fp32 arithmetic on the CUDA cores."""
+    """la_backward_causal on the headline causal shape (B=4 H=8 N=2048 d=64, bf16): read
+    q, k, v, dO and write dq, dk, dv once; bf16 operands on the tensor cores with fp32
+    accumulation.  Algorithmic flop: three times the forward's at chunk 128 (the
+    masked half of each intra-chunk tile); the bound is the slower of those flop at
+    the bf16 peak and the bytes at HBM bandwidth."""
     w = workloads.CAUSAL_BF16
     q, k, v = workloads.forward_inputs(w)
     dout = workloads.random_inputs(w.seed + 100, w.B, w.H, w.N, w.dv, w.dv, "bf16")[2]
@@ -643,10 +646,10 @@ def bench_path_backward(torch, la, reps, peaks, src):
 
     secs, launches, _ = time_graph_steps(torch, la, step, reps, 3, Dist())
     t = secs / reps
-    fl = 3.0 * causal_flops(w.BH, w.N, w.dk, w.dv, 64)
+    fl = 3.0 * causal_flops(w.BH, w.N, w.dk, w.dv, 128)
     return {"workload": w.name + "_backward", "value": round(w.B * w.N / t, 1), "unit": "tokens/s",
             "ms_per_step": round(t * 1e3, 4), "launches_per_step": launches / reps,
-            "roofline": roofline_alu(fl, nbytes, t, peaks, src, ncu_traffic("backward")),
+            "roofline": roofline(fl, nbytes, t, peaks, src, ncu_traffic("backward")),
             "l2": "%d rotating buffer sets" % R}
 
 

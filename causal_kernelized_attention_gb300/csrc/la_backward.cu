@@ -504,15 +504,6 @@ la_status backward_by_dk(const BackwardProblem &p)
 
 }  // namespace
 
-la_status backward_scan(float *buf, int BH, int nC, int E, bool reverse, cudaStream_t s)
-{
-    const long long total = (long long)BH * E;
-    const unsigned blocks = (unsigned)((total + kThreads - 1) / kThreads);
-    count_launches();
-    bwd_scan<<<blocks, kThreads, 0, s>>>(buf, nC, E, total, reverse ? 1 : 0);
-    return cuda_status(cudaGetLastError());
-}
-
 la_status causal_backward(const BackwardProblem &p)
 {
     if (!supported_dim(p.dkd) || !supported_dim(p.dvd)) return LA_ERR_UNSUPPORTED;

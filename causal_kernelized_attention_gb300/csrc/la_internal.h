@@ -58,9 +58,6 @@ la_status causal_backward(const BackwardProblem &p);
 // Tensor-core backward (la_tc_backward.cu): bf16, dk = dv = 64, N >= 128.
 bool backward_tc_eligible(const BackwardProblem &p);
 la_status causal_backward_tc(const BackwardProblem &p);
-// Exclusive scan over the nC chunk states (E floats each) of every head, in place:
-// prefix (forward) or suffix (reverse).
-la_status backward_scan(float *buf, int BH, int nC, int E, bool reverse, cudaStream_t s);
 
 // SIMT kernels (la_simt.cu): fp32 CUDA-core arithmetic, any supported dtype.
 la_status causal_simt(const Problem &p);

@@ -5,7 +5,7 @@
 // C = 128 tokens, with every block product a tcgen05 MMA:
 //
 //   1. chunk states     A_c = phi(K_c)^T [V_c | 1]                        -> buf[c]
-//   2. forward scan     buf[c] = sum_{c' < c} A_c' = [S | z] before chunk c  (la_backward.cu)
+//   2. forward scan     buf[c] = sum_{c' < c} A_c' = [S | z] before chunk c
 //   3. dq, per chunk    T = phi(Q) phi(K)^T, P = bf16(tril T)             (TMEM)
 //                       [num | den] = P [V | 1] + phi(Q) [S | z]
 //                       d = max(den, eps), dN = dO / d, dd = -(dO . num / d) / d (0 if clamped)
@@ -13,7 +13,7 @@
 //                       dphi(Q) = U' phi(K) + dN S^T (+ dd z^T, fp32)  ->  dq = dphi(Q) phi'(q)
 //                       B_c = phi(Q)^T [dN | dd]                          -> buf[c]
 //                       dN (bf16) and dd (fp32) to scratch for step 5
-//   4. reverse scan     buf[c] = sum_{c' > c} B_c' = [R | r] after chunk c  (la_backward.cu)
+//   4. reverse scan     buf[c] = sum_{c' > c} B_c' = [R | r] after chunk c
 //   5. dk, dv per chunk T^T = phi(K) phi(Q)^T, P^T = bf16(triu T^T)       (TMEM)
 //                       U^T = V dN^T, U'^T = bf16(triu(U^T + 1 dd^T))     (TMEM)
 //                       dV = P^T dN + phi(K) R
@@ -170,6 +170,51 @@ __device__ __forceinline__ void tmem_mask_bf16(uint32_t tb, int q, int lane, Bia
     tmem_st_wait();
 }
 
+// As tmem_mask_bf16 (lower mask), split between two groups of warps on the same
+// rows: group g converts key blocks 2g, 2g + 1; every thread reads its blocks into
+// registers before either group writes (the packed output of blocks 2, 3 lands on
+// block 1's columns), with one barrier of both groups (bar_id, 256 threads) between.
+// Every thread of both groups calls it; with live == false it only takes part in the
+// barrier (so that a CTA winding down after a failed wait cannot stall there).
+template <typename Bias>
+__device__ __forceinline__ void tmem_tril_bf16_split(bool live, uint32_t tb, int q, int lane, int g, uint32_t bar_id,
+                                                     Bias bias)
+{
+    uint32_t pk[2][2][8];
+#pragma unroll
+    for (int b = 0; b < 2; ++b) {
+        const int kb = 2 * g + b;
+#pragma unroll
+        for (int hb = 0; hb < 2; ++hb) {
+            if (live && kb <= q) {
+                uint32_t t[16];
+                tmem_ld16(tb + kb * 32 + 16 * hb, t);
+                tmem_ld_wait();
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int j = 16 * hb + 2 * e;
+                    const int c = kb * 32 + j;
+                    const bool k0 = kb != q || j <= lane, k1 = kb != q || j + 1 <= lane;
+                    pk[b][hb][e] = pack_bf16(k0 ? __uint_as_float(t[2 * e]) + bias(c) : 0.f,
+                                             k1 ? __uint_as_float(t[2 * e + 1]) + bias(c + 1) : 0.f);
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) pk[b][hb][e] = 0u;
+            }
+        }
+    }
+    named_bar_sync(bar_id, 256);
+    if (!live) return;
+#pragma unroll
+    for (int b = 0; b < 2; ++b) {
+        const int kb = 2 * g + b;
+#pragma unroll
+        for (int hb = 0; hb < 2; ++hb) tmem_st8(tb + kb * 16 + 8 * hb, pk[b][hb]);
+    }
+    tmem_st_wait();
+}
+
 // 16 bf16 values of row r, columns [c0, c0 + 16), of a 128-byte swizzled tile.
 __device__ __forceinline__ void ld_row16(const uint8_t *tile, int r, int c0, float (&x)[16])
 {
@@ -211,7 +256,9 @@ struct StateSmem {
     int abort;
 };
 
-__global__ void __launch_bounds__(128)
+constexpr int kStateThreads = 256;
+
+__global__ void __launch_bounds__(kStateThreads)
 bwd_tc_state(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v, float *buf,
              const Params prm)
 {
@@ -231,7 +278,7 @@ bwd_tc_state(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ 
         tmem_alloc(&sm.tmem_base, 128);
         tmem_relinquish();
     }
-    init_extra(sm.extra, tid, 128);
+    init_extra(sm.extra, tid, kStateThreads);
     if (tid < kC) put_extra(sm.extra, tid, kDdOff, 0u);  // no dd or z here
     if (tid < kC) put_extra(sm.extra, tid, kZOff, 0u);
     griddep_wait();
@@ -250,7 +297,7 @@ bwd_tc_state(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ 
     }
     bool ok = !aborted(abort_flag) && wait_w(abort_flag, &sm.full);
     if (ok) {
-        phi_tile_rolled<D>(sm.k, tid, 128, prm.N - c * kC);
+        phi_tile_rolled<D>(sm.k, tid, kStateThreads, prm.N - c * kC);
         fence_proxy_async_smem();
     }
     __syncthreads();
@@ -296,17 +343,49 @@ bwd_tc_state(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ 
     if (warp == 0) tmem_dealloc(tmem, 128);
 }
 
+// ---------------------------------------------------------------------- 2., 4. scans
+// Exclusive scan over the nC chunk states of every head, in place: prefix (forward)
+// or suffix (reverse).  Thread = (head, float4 of the state); every load of a round
+// of 16 chunks is issued before the first store.
+constexpr int kScanThreads = 256;
+__global__ void __launch_bounds__(kScanThreads)
+bwd_tc_scan(float *buf, int nC, int BH, int reverse)
+{
+    griddep_launch_dependents();
+    constexpr int E4 = kE / 4;
+    const long long gidx = (long long)blockIdx.x * kScanThreads + threadIdx.x;
+    griddep_wait();
+    if (gidx >= (long long)BH * E4) return;
+    const long long bh = gidx / E4, e = gidx % E4;
+    float4 *p = reinterpret_cast<float4 *>(buf) + bh * (long long)nC * E4 + e;
+    float4 run = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int i = 0; i < nC; i += 16) {
+        float4 x[16];
+        const int m = min(16, nC - i);
+#pragma unroll
+        for (int u = 0; u < 16; ++u)
+            if (u < m) x[u] = __ldcg(p + (long long)(reverse ? nC - 1 - (i + u) : i + u) * E4);
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+            if (u < m) {
+                __stcg(p + (long long)(reverse ? nC - 1 - (i + u) : i + u) * E4, run);
+                run.x += x[u].x; run.y += x[u].y; run.z += x[u].z; run.w += x[u].w;
+            }
+        }
+    }
+}
+
 // ---------------------------------------------------------------------- 3. dq
 struct DqSmem {
-    uint8_t q[kTile];   // phi(Q), then dq staged
+    uint8_t q[kTile];   // phi(Q)
     uint8_t k[kTile];   // phi(K)
     uint8_t v[kTile];
-    uint8_t go[kTile];  // dO
+    uint8_t go[kTile];  // dO, then dq staged
     uint8_t dn[kTile];  // dN (bf16), also stored to scratch
     uint8_t simg[kImg]; // bf16 S before the chunk, [f][v]
     uint8_t extra[kC * 128];
     float zf[D];        // z before the chunk (fp32)
-    float dd[kC];       // dd per row (fp32)
+    float gpart[2][kC]; // each group's half of dO . o per row
     uint64_t full, ready, t_full, p_full, o_full, dn_ready, u_full, bc_full, up_full, g_full, dq_staged, drain;
     uint32_t tmem_base;
     int abort;
@@ -335,10 +414,10 @@ bwd_tc_dq(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUt
         uint64_t *bars[] = {&sm.full, &sm.t_full, &sm.o_full, &sm.u_full, &sm.bc_full, &sm.g_full, &sm.drain};
         for (uint64_t *b : bars) mbar_init(b, 1);
         mbar_init(&sm.ready, kWork);
-        mbar_init(&sm.p_full, 128);
-        mbar_init(&sm.dn_ready, 128);
-        mbar_init(&sm.up_full, 128);
-        mbar_init(&sm.dq_staged, 128);
+        mbar_init(&sm.p_full, kWork);
+        mbar_init(&sm.dn_ready, kWork);
+        mbar_init(&sm.up_full, kWork);
+        mbar_init(&sm.dq_staged, kWork);
         sm.abort = (smem_u32(smem_raw) & 1023u) == 0 ? 0 : 1;
         if (sm.abort) atomicOr(&g_bw_status, kStatusTimeout);
         fence_mbar_init();
@@ -397,7 +476,8 @@ bwd_tc_dq(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUt
                         mma_ss(tmem + tT, kmajor(dna, kk), kmajor(va, kk), id, kk > 0);
                     mma_commit(&sm.u_full);
                 }
-                {  // B_c = phi(Q)^T [dN | dd]: rows 64..127 repeat rows 0..63 (LBO 0)
+                {  // B_c = phi(Q)^T [dN | dd]: rows 64..127 repeat rows 0..63 (LBO 0); it runs
+                   // while the epilogue warps form U'
                     const uint32_t id = idesc_bf16_f32(128, D + 16, true, true);
 #pragma unroll
                     for (int kk = 0; kk < kC / 16; ++kk)
@@ -431,104 +511,116 @@ bwd_tc_dq(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUt
         fence_proxy_async_smem();
         named_bar_sync(1, kWork);  // zf[] complete before any thread of either group reads it
         if (ok) mbar_arrive(&sm.ready);
-        if (g == 0) {
-            // ---- group 0: P, the output epilogue (dN, dd), dq
-            if (ok && (ok = wait_w(abort_flag, &sm.t_full))) {
-                tc_fence_after();
-                tmem_mask_bf16<true>(tl + tT, q, lane, [](int) { return 0.f; });
-                tc_fence_before();
-                mbar_arrive(&sm.p_full);
-            }
-            float ddr = 0.f;
-            if (ok && (ok = wait_w(abort_flag, &sm.o_full))) {
-                tc_fence_after();
-                const float den = __uint_as_float(tmem_ld1(tl + tO + D)) + __uint_as_float(tmem_ld1(tl + tO + D + 1));
+        // Both groups share every step: the conversions split by key blocks, the
+        // epilogues by value columns [32 g, 32 g + 32) (named barrier 2 for the halves
+        // of dO . o, 3 and 4 inside the conversions).
+        const int c0 = 32 * g;
+        if (ok) ok = wait_w(abort_flag, &sm.t_full);  // P = bf16(tril T)
+        tc_fence_after();
+        tmem_tril_bf16_split(ok, tl + tT, q, lane, g, 3, [](int) { return 0.f; });
+        if (ok) {
+            tc_fence_before();
+            mbar_arrive(&sm.p_full);
+        }
+        float ddr = 0.f;
+        if (ok && (ok = wait_w(abort_flag, &sm.o_full))) {
+            // o = num / d, dN = dO / d (bf16 into the dN tile), dd = -(dO . o) / d
+            tc_fence_after();
+            const float den = __uint_as_float(tmem_ld1(tl + tO + D)) + __uint_as_float(tmem_ld1(tl + tO + D + 1));
+            tmem_ld_wait();
+            const float inv = 1.f / fmaxf(den, prm.eps);
+            float gsum = 0.f;
+#pragma unroll
+            for (int blk = 0; blk < 2; ++blk) {
+                uint32_t a[16];
+                tmem_ld16(tl + tO + c0 + 16 * blk, a);
+                float go[16];
+                ld_row16(sm.go, r, c0 + 16 * blk, go);
                 tmem_ld_wait();
-                const float inv = 1.f / fmaxf(den, prm.eps);
-                float gsum = 0.f;
+                float dnv[16];
 #pragma unroll
-                for (int blk = 0; blk < 4; ++blk) {
-                    uint32_t a[16];
-                    tmem_ld16(tl + tO + 16 * blk, a);
-                    float go[16];
-                    ld_row16(sm.go, r, 16 * blk, go);
-                    tmem_ld_wait();
-                    float dnv[16];
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        gsum += go[e] * (__uint_as_float(a[e]) * inv);
-                        dnv[e] = go[e] * inv;
-                    }
-                    st_row16(sm.dn, r, 16 * blk, dnv);
+                for (int e = 0; e < 16; ++e) {
+                    gsum += go[e] * (__uint_as_float(a[e]) * inv);
+                    dnv[e] = go[e] * inv;
                 }
-                ddr = den > prm.eps ? -gsum * inv : 0.f;
-                sm.dd[r] = ddr;
+                st_row16(sm.dn, r, c0 + 16 * blk, dnv);
+            }
+            sm.gpart[g][r] = gsum;
+        }
+        named_bar_sync(2, kWork);
+        if (ok) {
+            const float den = __uint_as_float(tmem_ld1(tl + tO + D)) + __uint_as_float(tmem_ld1(tl + tO + D + 1));
+            tmem_ld_wait();
+            const float inv = 1.f / fmaxf(den, prm.eps);
+            ddr = den > prm.eps ? -(sm.gpart[0][r] + sm.gpart[1][r]) * inv : 0.f;
+            if (g == 0) {
                 put_extra(sm.extra, r, kDdOff, pack_bf16(ddr, 0.f));
                 if (r < len) ddbuf[(size_t)bh * prm.N + c * kC + r] = ddr;
-                fence_proxy_async_smem();
-                tc_fence_before();
-                mbar_arrive(&sm.dn_ready);
             }
-            if (ok && warp == 0 && lane == 0 && (ok = wait_b(abort_flag, &sm.dn_ready))) {
-                tma_store_3d_hint(&map_dn, sm.dn, 0, c * kC, bh, l2_policy_evict_last());
-                tma_store_commit();
-            }
-            ok = __all_sync(0xffffffffu, ok);
-            if (ok && (ok = wait_w(abort_flag, &sm.g_full))) {
-                // dq = (dphi(Q) + dd z^T) phi'(q), staged over phi(Q) (no MMA reads it now)
-                tc_fence_after();
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(&sm.dn_ready);
+        }
+        if (ok && tid == 0 && (ok = wait_b(abort_flag, &sm.dn_ready))) {
+            tma_store_3d_hint(&map_dn, sm.dn, 0, c * kC, bh, l2_policy_evict_last());
+            tma_store_commit();
+        }
+        ok = __all_sync(0xffffffffu, ok);
+        if (ok) ok = wait_w(abort_flag, &sm.u_full);  // U' = bf16(tril(U + dd 1^T))
+        tc_fence_after();
+        tmem_tril_bf16_split(ok, tl + tT, q, lane, g, 4, [ddr](int) { return ddr; });
+        if (ok) {
+            tc_fence_before();
+            mbar_arrive(&sm.up_full);
+        }
+        if (ok && (ok = wait_w(abort_flag, &sm.bc_full)) && q < 2) {
+            // B_c rows 0..63 (64..127 repeat them), value columns [c0, c0 + 32) and, for
+            // group 0, the r column
+            tc_fence_after();
+            const int f = r;
+            float4 *out = reinterpret_cast<float4 *>(slot);
 #pragma unroll
-                for (int blk = 0; blk < 4; ++blk) {
-                    uint32_t a[16];
-                    tmem_ld16(tl + tG + 16 * blk, a);
-                    float fq[16];
-                    ld_row16(sm.q, r, 16 * blk, fq);
-                    tmem_ld_wait();
-                    float x[16];
+            for (int blk = 0; blk < 2; ++blk) {
+                uint32_t a[16];
+                tmem_ld16(tl + tO + c0 + 16 * blk, a);
+                tmem_ld_wait();
 #pragma unroll
-                    for (int e = 0; e < 16; ++e)
-                        x[e] = (__uint_as_float(a[e]) + ddr * sm.zf[16 * blk + e]) * dphi(fq[e]);
-                    st_row16(sm.q, r, 16 * blk, x);
-                }
-                fence_proxy_async_smem();
-                mbar_arrive(&sm.dq_staged);
+                for (int e = 0; e < 4; ++e)
+                    out[((c0 + 16 * blk) / 4 + e) * D + f] = make_float4(
+                        __uint_as_float(a[4 * e]), __uint_as_float(a[4 * e + 1]), __uint_as_float(a[4 * e + 2]),
+                        __uint_as_float(a[4 * e + 3]));
             }
-            if (warp == 0 && lane == 0) {
-                if (ok && wait_b(abort_flag, &sm.dq_staged)) {
-                    tma_store_3d_hint(&map_dq, sm.q, 0, c * kC, bh, l2_policy_evict_first());
-                    tma_store_commit();
-                }
-                tma_store_wait_all();
-            }
-        } else {
-            // ---- group 1: U', the reverse chunk state B_c
-            // dd[] is written by group 0 before it arrives on dn_ready
-            if (ok && (ok = wait_w(abort_flag, &sm.dn_ready)) && (ok = wait_w(abort_flag, &sm.u_full))) {
-                tc_fence_after();
-                const float ddr = sm.dd[r];
-                tmem_mask_bf16<true>(tl + tT, q, lane, [ddr](int) { return ddr; });
-                tc_fence_before();
-                mbar_arrive(&sm.up_full);
-            }
-            if (ok && (ok = wait_w(abort_flag, &sm.bc_full)) && q < 2) {
-                tc_fence_after();
-                const int f = r;  // rows 0..63 (64..127 repeat them)
-                float4 *out = reinterpret_cast<float4 *>(slot);
-#pragma unroll
-                for (int blk = 0; blk < 4; ++blk) {
-                    uint32_t a[16];
-                    tmem_ld16(tl + tO + 16 * blk, a);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        out[(4 * blk + e) * D + f] = make_float4(__uint_as_float(a[4 * e]), __uint_as_float(a[4 * e + 1]),
-                                                                 __uint_as_float(a[4 * e + 2]),
-                                                                 __uint_as_float(a[4 * e + 3]));
-                }
+            if (g == 0) {
                 slot[D * D + f] = __uint_as_float(tmem_ld1(tl + tO + D));
                 tmem_ld_wait();
             }
         }
+        ok = __all_sync(0xffffffffu, ok);
+        if (ok && (ok = wait_w(abort_flag, &sm.g_full))) {
+            // dq = (dphi(Q) + dd z^T) phi'(q), staged in the dO tile (read only by the
+            // output epilogue, long done)
+            tc_fence_after();
+#pragma unroll
+            for (int blk = 0; blk < 2; ++blk) {
+                uint32_t a[16];
+                tmem_ld16(tl + tG + c0 + 16 * blk, a);
+                float fq[16];
+                ld_row16(sm.q, r, c0 + 16 * blk, fq);
+                tmem_ld_wait();
+                float x[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    x[e] = (__uint_as_float(a[e]) + ddr * sm.zf[c0 + 16 * blk + e]) * dphi(fq[e]);
+                st_row16(sm.go, r, c0 + 16 * blk, x);
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(&sm.dq_staged);
+        }
+        if (tid == 0 && ok && wait_b(abort_flag, &sm.dq_staged)) {
+            tma_store_3d_hint(&map_dq, sm.go, 0, c * kC, bh, l2_policy_evict_first());
+            tma_store_commit();
+        }
+        if (tid == 0) tma_store_wait_all();
     }
     tc_fence_before();
     __syncthreads();
@@ -767,13 +859,14 @@ la_status causal_backward_tc(const BackwardProblem &p)
     if (st != LA_OK) return st;
     Params prm{p.N, p.BH, nC, p.eps};
     const unsigned grid = (unsigned)(p.BH * nC);
-    count_launches(3);
-    st = launch_dependent(bwd_tc_state, grid, 128, (int)sizeof(StateSmem), p.stream, mk, mv, buf, prm);
-    if (st == LA_OK) st = backward_scan(buf, p.BH, nC, kE, false, p.stream);
+    const unsigned scan_grid = (unsigned)(((long long)p.BH * (kE / 4) + kScanThreads - 1) / kScanThreads);
+    count_launches(5);
+    st = launch_dependent(bwd_tc_state, grid, kStateThreads, (int)sizeof(StateSmem), p.stream, mk, mv, buf, prm);
+    if (st == LA_OK) st = launch_dependent(bwd_tc_scan, scan_grid, kScanThreads, 0, p.stream, buf, nC, p.BH, 0);
     if (st == LA_OK)
         st = launch_dependent(bwd_tc_dq, grid, kThreads, (int)sizeof(DqSmem), p.stream, mq, mk, mv, mdo, mdn, mdq, buf,
                               ddbuf, prm);
-    if (st == LA_OK) st = backward_scan(buf, p.BH, nC, kE, true, p.stream);
+    if (st == LA_OK) st = launch_dependent(bwd_tc_scan, scan_grid, kScanThreads, 0, p.stream, buf, nC, p.BH, 1);
     if (st == LA_OK)
         st = launch_dependent(bwd_tc_dkdv, grid, kThreads, (int)sizeof(DkSmem), p.stream, mq, mk, mv, mdn, mdk, mdv, buf,
                               ddbuf, prm);
