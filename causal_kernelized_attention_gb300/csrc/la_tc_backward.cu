@@ -107,22 +107,27 @@ __device__ __forceinline__ void init_extra(uint8_t *blk, int t, int nt)
         *reinterpret_cast<uint4 *>(blk + r * 128 + ch * 16) = make_uint4(x, 0u, 0u, 0u);
     }
 }
-// A chunk state from buf (thread t of 256: row f = t % 64, columns 16 (t / 64) ..) into
-// a bf16 image; the fp32 last column to zf[] and, if zblk, as a hi + lo pair into the
-// extra-column block (rows 0..63).
-__device__ __forceinline__ void state_to_image(const float *slot, uint8_t *img, float *zf, uint8_t *zblk, int t)
+// A chunk state from buf into a bf16 image, in two steps so that the loads are in
+// flight while the thread does other work: load_state (thread t of 256: row f = t % 64,
+// columns 16 (t / 64) .. and, for t < 64, the last column) and put_state (the image
+// row part; the fp32 last column to zf[] and, if zblk, as a hi + lo pair into the
+// extra-column block, rows 0..63).
+__device__ __forceinline__ void load_state(const float *slot, int t, float (&x)[16], float &z)
 {
     const int f = t & 63, cg = t >> 6;
     const float4 *s4 = reinterpret_cast<const float4 *>(slot);
-    float x[16];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
         const float4 a = __ldcg(s4 + (size_t)(4 * cg + e) * D + f);
         x[4 * e] = a.x; x[4 * e + 1] = a.y; x[4 * e + 2] = a.z; x[4 * e + 3] = a.w;
     }
+    z = cg == 0 ? __ldcg(slot + D * D + f) : 0.f;
+}
+__device__ __forceinline__ void put_state(uint8_t *img, float *zf, uint8_t *zblk, int t, const float (&x)[16], float z)
+{
+    const int f = t & 63, cg = t >> 6;
     put_img16(img, f, 16 * cg, x);
     if (cg == 0) {
-        const float z = __ldcg(slot + D * D + f);
         zf[f] = z;
         if (zblk) {
             const __nv_bfloat16 hi = __float2bfloat16_rn(z);
@@ -251,7 +256,7 @@ struct StateSmem {
     uint8_t k[kTile];
     uint8_t v[kTile];
     uint8_t extra[kC * 128];
-    uint64_t full, mma;
+    uint64_t k_full, full, mma;  // k_full: K landed; full: V landed
     uint32_t tmem_base;
     int abort;
 };
@@ -268,6 +273,7 @@ bwd_tc_state(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ 
     const int bh = (int)blockIdx.x / prm.nC, c = (int)blockIdx.x % prm.nC;
     griddep_launch_dependents();
     if (tid == 0) {
+        mbar_init(&sm.k_full, 1);
         mbar_init(&sm.full, 1);
         mbar_init(&sm.mma, 1);
         sm.abort = (smem_u32(smem_raw) & 1023u) == 0 ? 0 : 1;
@@ -289,16 +295,18 @@ bwd_tc_state(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ 
     int *abort_flag = &sm.abort;
     bool loaded = false;
     if (tid == 0 && !aborted(abort_flag)) {
-        mbar_arrive_expect_tx(&sm.full, 2 * kTile);
         const uint64_t pol = l2_policy_evict_last();  // read again by the dq and dk, dv kernels
-        tma_load_3d_hint(sm.k, &map_k, &sm.full, 0, c * kC, bh, pol);
+        mbar_arrive_expect_tx(&sm.k_full, kTile);
+        tma_load_3d_hint(sm.k, &map_k, &sm.k_full, 0, c * kC, bh, pol);
+        mbar_arrive_expect_tx(&sm.full, kTile);
         tma_load_3d_hint(sm.v, &map_v, &sm.full, 0, c * kC, bh, pol);
         loaded = true;
     }
-    bool ok = !aborted(abort_flag) && wait_w(abort_flag, &sm.full);
+    bool ok = !aborted(abort_flag) && wait_w(abort_flag, &sm.k_full);
     if (ok) {
         phi_tile_rolled<D>(sm.k, tid, kStateThreads, prm.N - c * kC);
         fence_proxy_async_smem();
+        ok = wait_w(abort_flag, &sm.full);
     }
     __syncthreads();
     ok = ok && !aborted(abort_flag);
@@ -335,7 +343,10 @@ bwd_tc_state(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ 
             tmem_ld_wait();
         }
     }
-    if (tid == 0 && loaded) drain(&sm.full);
+    if (tid == 0 && loaded) {
+        drain(&sm.k_full);
+        drain(&sm.full);
+    }
     if (issued) drain(&sm.mma);  // the committed group completes before TMEM is freed
     tc_fence_before();
     __syncthreads();
@@ -386,7 +397,8 @@ struct DqSmem {
     uint8_t extra[kC * 128];
     float zf[D];        // z before the chunk (fp32)
     float gpart[2][kC]; // each group's half of dO . o per row
-    uint64_t full, ready, t_full, p_full, o_full, dn_ready, u_full, bc_full, up_full, g_full, dq_staged, drain;
+    // qk_full: Q, K landed; full: V, dO landed
+    uint64_t qk_full, full, ready, t_full, p_full, o_full, dn_ready, u_full, bc_full, up_full, g_full, dq_staged, drain;
     uint32_t tmem_base;
     int abort;
 };
@@ -411,7 +423,7 @@ bwd_tc_dq(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUt
     float *slot = buf + ((size_t)bh * prm.nC + c) * kE;
     griddep_launch_dependents();
     if (tid == 0) {
-        uint64_t *bars[] = {&sm.full, &sm.t_full, &sm.o_full, &sm.u_full, &sm.bc_full, &sm.g_full, &sm.drain};
+        uint64_t *bars[] = {&sm.qk_full, &sm.full, &sm.t_full, &sm.o_full, &sm.u_full, &sm.bc_full, &sm.g_full, &sm.drain};
         for (uint64_t *b : bars) mbar_init(b, 1);
         mbar_init(&sm.ready, kWork);
         mbar_init(&sm.p_full, kWork);
@@ -436,13 +448,15 @@ bwd_tc_dq(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUt
 
     if (warp == kTmaWarp) {
         if (lane == 0 && !aborted(abort_flag)) {
-            mbar_arrive_expect_tx(&sm.full, 4 * kTile);
             const uint64_t pol = l2_policy_evict_first();
-            tma_load_3d_hint(sm.q, &map_q, &sm.full, 0, c * kC, bh, pol);
-            tma_load_3d_hint(sm.k, &map_k, &sm.full, 0, c * kC, bh, l2_policy_evict_last());
+            mbar_arrive_expect_tx(&sm.qk_full, 2 * kTile);  // phi starts on these
+            tma_load_3d_hint(sm.q, &map_q, &sm.qk_full, 0, c * kC, bh, pol);
+            tma_load_3d_hint(sm.k, &map_k, &sm.qk_full, 0, c * kC, bh, l2_policy_evict_last());
+            mbar_arrive_expect_tx(&sm.full, 2 * kTile);
             tma_load_3d_hint(sm.v, &map_v, &sm.full, 0, c * kC, bh, l2_policy_evict_last());
             tma_load_3d_hint(sm.go, &map_do, &sm.full, 0, c * kC, bh, pol);
-            drain(&sm.full);  // no copy may still be writing shared memory when the CTA exits
+            drain(&sm.qk_full);  // no copy may still be writing shared memory when the CTA exits
+            drain(&sm.full);
         }
     } else if (warp == kMmaWarp) {
         if (lane == 0) {
@@ -456,7 +470,8 @@ bwd_tc_dq(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUt
                 for (int kk = 0; kk < D / 16; ++kk) mma_ss(tmem + tT, kmajor(qa, kk), kmajor(ka, kk), id, kk > 0);
                 mma_commit(&sm.t_full);
             }
-            if (ok && (ok = wait_b(abort_flag, &sm.p_full))) {  // [num | den] = P [V | 1] + phi(Q) [S | z]
+            if (ok && (ok = wait_b(abort_flag, &sm.p_full)) && (ok = wait_b(abort_flag, &sm.full))) {
+                // [num | den] = P [V | 1] + phi(Q) [S | z]
                 tc_fence_after();
                 const uint32_t id = idesc_bf16_f32(128, D + 16, false, true);
 #pragma unroll
@@ -503,11 +518,13 @@ bwd_tc_dq(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUt
         const int q = warp & 3, g = warp >> 2, r = 32 * q + lane;  // TMEM lane quadrant, group, row
         const uint32_t tl = tmem + ((uint32_t)(32 * q) << 16);
         bool ok = !aborted(abort_flag);
-        if (ok) state_to_image(slot, sm.simg, sm.zf, sm.extra, tid);
-        if (ok && (ok = wait_w(abort_flag, &sm.full))) {
+        float sx[16], sz = 0.f;
+        if (ok) load_state(slot, tid, sx, sz);  // in flight during phi
+        if (ok && (ok = wait_w(abort_flag, &sm.qk_full))) {
             phi_tile_rolled<D>(sm.q, tid, kWork, len);
             phi_tile_rolled<D>(sm.k, tid, kWork, len);
         }
+        if (ok) put_state(sm.simg, sm.zf, sm.extra, tid, sx, sz);
         fence_proxy_async_smem();
         named_bar_sync(1, kWork);  // zf[] complete before any thread of either group reads it
         if (ok) mbar_arrive(&sm.ready);
@@ -523,7 +540,7 @@ bwd_tc_dq(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUt
             mbar_arrive(&sm.p_full);
         }
         float ddr = 0.f;
-        if (ok && (ok = wait_w(abort_flag, &sm.o_full))) {
+        if (ok && (ok = wait_w(abort_flag, &sm.full)) && (ok = wait_w(abort_flag, &sm.o_full))) {
             // o = num / d, dN = dO / d (bf16 into the dN tile), dd = -(dO . o) / d
             tc_fence_after();
             const float den = __uint_as_float(tmem_ld1(tl + tO + D)) + __uint_as_float(tmem_ld1(tl + tO + D + 1));
@@ -637,7 +654,8 @@ struct DkSmem {
     uint8_t rimg[kImg]; // bf16 R after the chunk, [f][v]
     float rf[D];        // r after the chunk (fp32)
     float dd[kC];
-    uint64_t full, ready, tt_full, ut_full, pt_full, upt_full, dv_full, dk_full, dv_staged, dk_staged, drain;
+    // qk_full: Q, K landed; full: V, dN landed
+    uint64_t qk_full, full, ready, tt_full, ut_full, pt_full, upt_full, dv_full, dk_full, dv_staged, dk_staged, drain;
     uint32_t tmem_base;
     int abort;
 };
@@ -661,7 +679,7 @@ bwd_tc_dkdv(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
     const float *slot = buf + ((size_t)bh * prm.nC + c) * kE;
     griddep_launch_dependents();
     if (tid == 0) {
-        uint64_t *bars[] = {&sm.full, &sm.tt_full, &sm.ut_full, &sm.dv_full, &sm.dk_full, &sm.drain};
+        uint64_t *bars[] = {&sm.qk_full, &sm.full, &sm.tt_full, &sm.ut_full, &sm.dv_full, &sm.dk_full, &sm.drain};
         for (uint64_t *b : bars) mbar_init(b, 1);
         mbar_init(&sm.ready, kWork);
         mbar_init(&sm.pt_full, 128);
@@ -685,12 +703,14 @@ bwd_tc_dkdv(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
 
     if (warp == kTmaWarp) {
         if (lane == 0 && !aborted(abort_flag)) {
-            mbar_arrive_expect_tx(&sm.full, 4 * kTile);
             const uint64_t pol = l2_policy_evict_first();
-            tma_load_3d_hint(sm.q, &map_q, &sm.full, 0, c * kC, bh, pol);
-            tma_load_3d_hint(sm.k, &map_k, &sm.full, 0, c * kC, bh, pol);
+            mbar_arrive_expect_tx(&sm.qk_full, 2 * kTile);  // phi starts on these
+            tma_load_3d_hint(sm.q, &map_q, &sm.qk_full, 0, c * kC, bh, pol);
+            tma_load_3d_hint(sm.k, &map_k, &sm.qk_full, 0, c * kC, bh, pol);
+            mbar_arrive_expect_tx(&sm.full, 2 * kTile);
             tma_load_3d_hint(sm.v, &map_v, &sm.full, 0, c * kC, bh, pol);
             tma_load_3d_hint(sm.dn, &map_dn, &sm.full, 0, c * kC, bh, pol);
+            drain(&sm.qk_full);
             drain(&sm.full);
         }
     } else if (warp == kMmaWarp) {
@@ -704,6 +724,11 @@ bwd_tc_dkdv(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) mma_ss(tmem + tTT, kmajor(ka, kk), kmajor(qa, kk), id, kk > 0);
                 mma_commit(&sm.tt_full);  // T^T = phi(K) phi(Q)^T
+                ok = wait_b(abort_flag, &sm.full);  // V, dN
+            }
+            if (ok) {
+                tc_fence_after();
+                const uint32_t id = idesc_bf16_f32(128, 128, false, false);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) mma_ss(tmem + tUT, kmajor(va, kk), kmajor(dna, kk), id, kk > 0);
                 mma_commit(&sm.ut_full);  // U^T = V dN^T
@@ -735,13 +760,18 @@ bwd_tc_dkdv(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
         const int q = warp & 3, g = warp >> 2, r = 32 * q + lane;
         const uint32_t tl = tmem + ((uint32_t)(32 * q) << 16);
         bool ok = !aborted(abort_flag);
+        float sx[16], sz = 0.f, ddv = 0.f;
         if (ok) {
-            state_to_image(slot, sm.rimg, sm.rf, nullptr, tid);
-            if (tid < kC) sm.dd[tid] = tid < len ? __ldcg(ddbuf + (size_t)bh * prm.N + c * kC + tid) : 0.f;
+            load_state(slot, tid, sx, sz);  // in flight during phi
+            if (tid < kC && tid < len) ddv = __ldcg(ddbuf + (size_t)bh * prm.N + c * kC + tid);
         }
-        if (ok && (ok = wait_w(abort_flag, &sm.full))) {
+        if (ok && (ok = wait_w(abort_flag, &sm.qk_full))) {
             phi_tile_rolled<D>(sm.q, tid, kWork, len);
             phi_tile_rolled<D>(sm.k, tid, kWork, len);
+        }
+        if (ok) {
+            put_state(sm.rimg, sm.rf, nullptr, tid, sx, sz);
+            if (tid < kC) sm.dd[tid] = ddv;
         }
         fence_proxy_async_smem();
         __syncwarp();

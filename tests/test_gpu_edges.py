@@ -197,17 +197,32 @@ def test_variant_clamp_binds(orc, eps, dtype, N, d):
 def test_backward_clamp_binds(orc, dtype):
     """eps = 1e4: the clamp binds on the early rows only; no gradient flows into
     the denominator there.  Gradient errors scaled by the largest reference
-    gradient: <= 1e-5 (fp32), <= 1e-2 (bf16)."""
+    gradient: <= 1e-5 (fp32), <= 1e-2 (bf16).  The decision den > eps is taken in
+    each side's own precision; in bf16 (the tensor-core path sums the bf16-rounded
+    scores) a row whose float64 denominator lies within 1% of eps may fall on the
+    other side, which changes that row's dq by about dd * z: those rows (checked
+    to be few) are left out of the dq comparison, dk and dv are compared in full."""
     B, H, N, d = 2, 3, 300, 64
+    eps = 1e4
     q, k, v = workloads.random_inputs(38000, B, H, N, d, d, dtype)
     dout = workloads.random_inputs(38001, B, H, N, d, d, dtype)[2]
-    got = la().la_backward_causal(*dev(q, k, v, dout, dtype=dtype), eps=1e4)
+    got = la().la_backward_causal(*dev(q, k, v, dout, dtype=dtype), eps=eps)
     torch.cuda.synchronize()
-    ref = orc.causal_backward(q, k, v, dout, 1e4)
+    ref = orc.causal_backward(q, k, v, dout, eps)
     scale = max(float(np.max(np.abs(r))) for r in ref)
     tol = 1e-5 if dtype == "f32" else 1e-2
+    keep = np.ones((B, H, N), bool)
+    if dtype == "bf16":
+        phi = lambda x: np.where(x > 0, x + 1.0, np.exp(np.minimum(x, 0.0)))
+        fq = phi(workloads.bf16_bits_to_f32(q).astype(np.float64))  # q, k: bf16 bit patterns
+        fk = phi(workloads.bf16_bits_to_f32(k).astype(np.float64))
+        den = np.einsum("bhnd,bhnd->bhn", fq, np.cumsum(fk, axis=2))
+        keep = np.abs(den / eps - 1.0) > 1e-2
+        assert keep.mean() > 0.95, float(keep.mean())
     for name, g, r in zip(("dq", "dk", "dv"), got, ref):
         d_ = np.abs(from_dev(g) - r)
+        if name == "dq":
+            d_ = d_[keep]
         assert d_.max() <= tol * scale, (name, float(d_.max()), scale)
 
 
