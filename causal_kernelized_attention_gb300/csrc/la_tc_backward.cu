@@ -287,6 +287,10 @@ bwd_tc_state(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ 
     init_extra(sm.extra, tid, kStateThreads);
     if (tid < kC) put_extra(sm.extra, tid, kDdOff, 0u);  // no dd or z here
     if (tid < kC) put_extra(sm.extra, tid, kZOff, 0u);
+    if (tid == 32) {  // into L2 while an earlier kernel on the stream finishes (the L2 is coherent)
+        tma_prefetch_3d(&map_k, 0, c * kC, bh);
+        tma_prefetch_3d(&map_v, 0, c * kC, bh);
+    }
     griddep_wait();
     tc_fence_before();
     __syncthreads();
@@ -439,6 +443,12 @@ bwd_tc_dq(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUt
         tmem_relinquish();
     }
     if (tid < kWork) init_extra(sm.extra, tid, kWork);
+    if (warp == kTmaWarp && lane == 0) {  // into L2 while the scan before this kernel runs
+        tma_prefetch_3d(&map_q, 0, c * kC, bh);
+        tma_prefetch_3d(&map_k, 0, c * kC, bh);
+        tma_prefetch_3d(&map_v, 0, c * kC, bh);
+        tma_prefetch_3d(&map_do, 0, c * kC, bh);
+    }
     griddep_wait();
     tc_fence_before();
     __syncthreads();
@@ -693,6 +703,12 @@ bwd_tc_dkdv(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
     if (warp == kMmaWarp) {
         tmem_alloc(&sm.tmem_base, kTmemCols);
         tmem_relinquish();
+    }
+    if (warp == kTmaWarp && lane == 0) {  // into L2 while the scan before this kernel runs
+        tma_prefetch_3d(&map_q, 0, c * kC, bh);
+        tma_prefetch_3d(&map_k, 0, c * kC, bh);
+        tma_prefetch_3d(&map_v, 0, c * kC, bh);
+        tma_prefetch_3d(&map_dn, 0, c * kC, bh);
     }
     griddep_wait();
     tc_fence_before();

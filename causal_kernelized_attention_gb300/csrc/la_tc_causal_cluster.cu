@@ -240,6 +240,19 @@ causal_cluster_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_co
         tmem_alloc(&sm.tmem_base, 512);
         tmem_relinquish();
     }
+    if (warp == kTmaWarp && lane == 0) {
+        // the tensor maps are launch parameters and the L2 is coherent: both prefetches
+        // may run while an earlier kernel on the stream still writes the inputs
+        tma_prefetch_map(&map_q);
+        tma_prefetch_map(&map_k);
+        tma_prefetch_map(&map_v);
+        tma_prefetch_map(&map_o);
+        for (int p = 0; p < nch; ++p) {
+            tma_prefetch_3d(&map_k, 0, (c0 + p) * kC, bh);
+            tma_prefetch_3d(&map_v, 0, (c0 + p) * kC, bh);
+        }
+        for (int p = 0; p < nch; ++p) tma_prefetch_3d(&map_q, 0, (c0 + p) * kC, bh);
+    }
     griddep_wait();
     tc_fence_before();
     __syncthreads();
