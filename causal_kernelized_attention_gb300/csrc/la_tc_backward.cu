@@ -881,14 +881,21 @@ la_status causal_backward_tc(const BackwardProblem &p)
     const size_t state_floats = (size_t)p.BH * nC * kE;
     const size_t dd_floats = (size_t)p.BH * p.N;
     const size_t dn_bytes = (size_t)p.BH * p.N * D * 2;
-    Scratch scratch;
     // states, dd, then dN (16-byte aligned: the states and dd are multiples of 4 floats
-    // only when N is; round the offset up)
+    // only when N is; round the offset up).  The stream's data workspace when it can
+    // serve the call (no allocation per call, none inside a captured graph), else
+    // stream-ordered scratch.
     const size_t dn_off = ((sizeof(float) * (state_floats + dd_floats)) + 255) & ~(size_t)255;
-    la_status st = scratch.alloc(dn_off + dn_bytes, p.stream);
-    if (st != LA_OK) return st;
-    float *buf = (float *)scratch.ptr, *ddbuf = buf + state_floats;
-    void *dn = (uint8_t *)scratch.ptr + dn_off;
+    Scratch scratch;
+    void *base = nullptr;
+    la_status st = data_workspace(p.stream, dn_off + dn_bytes, &base);
+    if (st != LA_OK) {
+        st = scratch.alloc(dn_off + dn_bytes, p.stream);
+        if (st != LA_OK) return st;
+        base = scratch.ptr;
+    }
+    float *buf = (float *)base, *ddbuf = buf + state_floats;
+    void *dn = (uint8_t *)base + dn_off;
     CUtensorMap mq, mk, mv, mdo, mdn, mdq, mdk, mdv;
     st = make_map(&mq, p.q, p.BH, p.N, D);
     if (st == LA_OK) st = make_map(&mk, p.k, p.BH, p.N, D);
