@@ -303,6 +303,14 @@ la_status decode_by_dk(float *S, float *z, const void *q, const void *k, const v
 la_status causal_gated(const void *q, const void *k, const void *v, const float *alpha, void *o, int BH, int N,
                        int dk, int dv, float eps, la_dtype dtype, cudaStream_t stream)
 {
+    // the chunked form (la_gated_chunk.cu); the token-by-token recurrence below serves
+    // the prefix state and stays available as a reference for it
+    return causal_gated_chunked(q, k, v, alpha, o, BH, N, dk, dv, eps, dtype, stream);
+}
+
+la_status causal_gated_recurrent(const void *q, const void *k, const void *v, const float *alpha, void *o, int BH,
+                                 int N, int dk, int dv, float eps, la_dtype dtype, cudaStream_t stream)
+{
     if (!supported_dim(dk) || !supported_dim(dv)) return LA_ERR_UNSUPPORTED;
     return dtype == LA_F32 ? gated_by_dk<float, false>(q, k, v, alpha, o, nullptr, nullptr, BH, N, dk, dv, eps, stream)
                            : gated_by_dk<__nv_bfloat16, false>(q, k, v, alpha, o, nullptr, nullptr, BH, N, dk, dv, eps,

@@ -74,6 +74,12 @@ la_status state_simt(const void *k, const void *v, float *S, float *z, int BH, i
 // alpha [BH, N, dk] (decode: [BH, dk]) fp32 in device memory.
 la_status causal_gated(const void *q, const void *k, const void *v, const float *alpha, void *o, int BH, int N,
                        int dk, int dv, float eps, la_dtype dtype, cudaStream_t stream);
+// The chunked form of the gated causal forward (la_gated_chunk.cu), and the
+// token-by-token recurrence it replaced for the forward (la_gated.cu).
+la_status causal_gated_chunked(const void *q, const void *k, const void *v, const float *alpha, void *o, int BH,
+                               int N, int dk, int dv, float eps, la_dtype dtype, cudaStream_t stream);
+la_status causal_gated_recurrent(const void *q, const void *k, const void *v, const float *alpha, void *o, int BH,
+                                 int N, int dk, int dv, float eps, la_dtype dtype, cudaStream_t stream);
 la_status state_gated(const void *k, const void *v, const float *alpha, float *S, float *z, int BH, int N, int dk,
                       int dv, la_dtype dtype, cudaStream_t stream);
 la_status decode_step_gated(float *S, float *z, const void *q, const void *k, const void *v, void *o,
