@@ -529,7 +529,7 @@ def bench_path_causal_gated(torch, la, reps, peaks, src):
     """la_forward_causal_gated on the headline causal shape (B=4 H=8 N=2048 d=64, bf16)
     with one gate per (token, key feature) drawn uniformly in [0.8, 1); the gates are a
     third input stream (fp32, the size of q and k together): bytes read q, k, v, alpha,
-    written o.  CUDA cores, fp32 recurrence."""
+    written o.  CUDA cores, fp32, in chunks of 32 tokens."""
     w = workloads.CAUSAL_BF16
     q, k, v = workloads.forward_inputs(w)
     alpha = np.random.default_rng(w.seed + 7).uniform(0.8, 1.0, size=(w.B, w.H, w.N, w.dk)).astype(np.float32)

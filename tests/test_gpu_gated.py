@@ -59,6 +59,18 @@ def test_gated_causal_matches_oracle(orc, dtype, B, H, N, dk, dv):
     assert_parity(from_dev(o), ref, dtype, (B, H, N, dk, dv))
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_gated_small_gates(orc, dtype):
+    """Gates drawn from [0, 1): products over a few tokens underflow; the chunked form
+    never divides by a product of gates, so it matches the recurrence."""
+    B, H, N, d = 2, 3, 1000, 64
+    q, k, v = workloads.random_inputs(60500, B, H, N, d, d, dtype)
+    a = gates(60501, (B, H, N, d), lo=0.0)
+    o = la().la_forward_causal_gated(to_dev(q, dtype), to_dev(k, dtype), to_dev(v, dtype), dev_f32(a))
+    torch.cuda.synchronize()
+    assert_parity(from_dev(o), orc.causal_gated_recurrent(q, k, v, a.astype(np.float64)), dtype, "small gates")
+
+
 def test_gated_special_gates(orc):
     """Gates of 1 give la_forward_causal; gates of gamma[h] give the decayed form;
     gates of 0 give o = v; closing one feature keeps the others' history."""
