@@ -1165,13 +1165,13 @@ la_status causal_tc(const Problem &p_in)
         if (var) return p.dk == 128 ? launch<128, true, true>(p) : launch<64, true, true>(p);
         return p.dk == 128 ? launch<128, true, false>(p) : launch<64, true, false>(p);
     }
-    if (var) return p.dk == 128 ? launch<128, false, true>(p) : launch<64, false, true>(p);
     // d = 64: up to 16 chunks per head, one thread-block cluster per head
-    // (la_tc_causal_cluster.cu); longer sequences with enough heads, the
-    // chunk-parallel kernel (la_tc_causal_chunks.cu), whose look-back needs the
-    // chunks of one head in flight at a time (about twice the SM count divided by
-    // the heads) to fit its 32-chunk window.
+    // (la_tc_causal_cluster.cu; any map and normaliser); longer sequences with enough
+    // heads (elu + 1 with the normaliser), the chunk-parallel kernel
+    // (la_tc_causal_chunks.cu), whose look-back needs the chunks of one head in flight
+    // at a time (about twice the SM count divided by the heads) to fit its 32-chunk window.
     if (p.dk == 64 && p.N <= kClusterKernelMaxN) return causal_cluster_tc(p);
+    if (var) return p.dk == 128 ? launch<128, false, true>(p) : launch<64, false, true>(p);
     if (p.dk == 64 && p.BH >= kChunkKernelMinHeads) return causal_chunks_tc(p);
     return p.dk == 128 ? launch<128, false, false>(p) : launch<64, false, false>(p);
 }

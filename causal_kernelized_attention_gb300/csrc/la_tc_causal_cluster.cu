@@ -119,7 +119,40 @@ struct Params {
     int N, BH, n_c, L;
     float eps;
     unsigned long long wait_ns;
+    // Feature-map variant (kVar): LA_PHI_* map with the shift as a bf16 pair; normalize 0:
+    // o = phi(q)^T S without the denominator.
+    int map, normalize;
+    uint32_t shift2;
 };
+
+// phi (elu + 1, or with kVar the map `map` with shift c2) in place on one tile, as a
+// loop that is not unrolled (its code is fetched once per launch), by nt threads.
+template <bool kVar>
+__device__ __forceinline__ void phi_tile_cluster(uint8_t *tile, int t, int nt, int valid, const Params &prm)
+{
+    if (!kVar) {
+        phi_tile_rolled<D>(tile, t, nt, valid);
+        return;
+    }
+    constexpr int kUnits = 128 * (D / 32);
+#pragma unroll 1
+    for (int u = t; u < kUnits; u += nt) {
+        const int row = u & 127, hb = u >> 7;
+        uint8_t *rp = tile + (hb >> 1) * kBox + row * 128;
+        const int rot = row + (hb & 1) * 4;
+        uint4 x[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) x[k] = *reinterpret_cast<const uint4 *>(rp + ((rot + k) & 7) * 16);
+        const bool live = row < valid;
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            x[k] = live ? make_uint4(phi2_variant(x[k].x, prm.map, prm.shift2), phi2_variant(x[k].y, prm.map, prm.shift2),
+                                     phi2_variant(x[k].z, prm.map, prm.shift2), phi2_variant(x[k].w, prm.map, prm.shift2))
+                        : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) *reinterpret_cast<uint4 *>(rp + ((rot + k) & 7) * 16) = x[k];
+    }
+}
 
 __device__ __forceinline__ bool wait_bar(const Params &prm, int *abort_flag, uint64_t *bar, uint32_t parity,
                                          bool cluster_acquire = false)
@@ -183,6 +216,7 @@ __device__ __forceinline__ void put_img16(uint8_t *sb, int i, int col0, const fl
 }
 
 
+template <bool kVar>
 __global__ void __launch_bounds__(kThreads, 1)
 causal_cluster_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                       const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_o,
@@ -272,7 +306,7 @@ causal_cluster_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_co
 #pragma unroll 1
         for (int p = 0; p < nch && ok; ++p) {
             if (!(ok = wait_bar_warp(prm, abort_flag, &sm.q_full[p], 0))) break;
-            phi_tile_rolled<D>(sm.q[p], t, kPhiThreads, prm.N - (c0 + p) * kC);
+            phi_tile_cluster<kVar>(sm.q[p], t, kPhiThreads, prm.N - (c0 + p) * kC, prm);
             fence_proxy_async_smem();
             mbar_arrive(&sm.q_ready[p]);
         }
@@ -399,7 +433,7 @@ causal_cluster_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_co
 #pragma unroll 1
         for (int p = 0; p < nch && ok; ++p) {
             if (!(ok = wait_bar_warp(prm, abort_flag, &sm.kv_full[p], 0))) break;
-            phi_tile_rolled<D>(sm.k[p], tid, kScanThreads, prm.N - (c0 + p) * kC);
+            phi_tile_cluster<kVar>(sm.k[p], tid, kScanThreads, prm.N - (c0 + p) * kC, prm);
             fence_proxy_async_smem();
             mbar_arrive(&sm.k_ready[p]);
         }
@@ -563,7 +597,7 @@ causal_cluster_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_co
                 const uint32_t to = tl + o_col(b);
                 const float den = __uint_as_float(tmem_ld1(to + D)) + __uint_as_float(tmem_ld1(to + D + 1));
                 tmem_ld_wait();
-                const float inv = 1.f / fmaxf(den, prm.eps);
+                const float inv = (kVar && !prm.normalize) ? 1.f : 1.f / fmaxf(den, prm.eps);
                 uint8_t *rowp = sm.q[p] + row * 128;
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
@@ -608,13 +642,14 @@ causal_cluster_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_co
 
 }  // namespace
 
-// bf16, dk = dv = 64, chunk 128, 128 <= N <= 2048 (at most 16 chunks per head), elu + 1
-// with the normaliser, no decay.
+// bf16, dk = dv = 64, chunk 128, 128 <= N <= 2048 (at most 16 chunks per head), no
+// decay; elu + 1 with the normaliser, or a feature-map / normaliser variant.
 la_status causal_cluster_tc(const Problem &p)
 {
     if (p.dtype != LA_BF16 || p.dk != D || p.dv != D || p.chunk != kC || p.N < kC || p.N > kG * kLmax * kC ||
-        p.gamma || !p.var.is_default())
+        p.gamma)
         return LA_ERR_UNSUPPORTED;
+    const bool var = !p.var.is_default();
     if ((long long)p.BH * kG > 0x7fffffffLL) return LA_ERR_UNSUPPORTED;
     CUtensorMap mq, mk, mv, mo;
     la_status st = make_map(&mq, p.q, p.BH, p.N, D);
@@ -629,8 +664,16 @@ la_status causal_cluster_tc(const Problem &p)
     prm.L = ceil_div(prm.n_c, kG);
     prm.eps = p.eps;
     prm.wait_ns = test_wait_limit_ns();
+    prm.map = p.var.map;
+    prm.normalize = p.var.normalize;
+    {
+        const __nv_bfloat16 c = __float2bfloat16_rn(p.var.shift);
+        const uint16_t b = *reinterpret_cast<const uint16_t *>(&c);
+        prm.shift2 = (uint32_t)b | ((uint32_t)b << 16);
+    }
+    auto kern = var ? causal_cluster_kernel<true> : causal_cluster_kernel<false>;
     const int smem = (int)sizeof(Smem);
-    st = ensure_smem((const void *)causal_cluster_kernel, smem);
+    st = ensure_smem((const void *)kern, smem);
     if (st != LA_OK) return st;
     cudaLaunchConfig_t lc = {};
     lc.gridDim = dim3((unsigned)(p.BH * kG));
@@ -647,7 +690,7 @@ la_status causal_cluster_tc(const Problem &p)
     lc.attrs = at;
     lc.numAttrs = dependent_launch_allowed(p.stream) ? 2 : 1;
     count_launches();
-    return cuda_status(cudaLaunchKernelEx(&lc, causal_cluster_kernel, mq, mk, mv, mo, prm));
+    return cuda_status(cudaLaunchKernelEx(&lc, kern, mq, mk, mv, mo, prm));
 }
 
 la_status tc_cluster_read_status(cudaStream_t s, unsigned *bits)
