@@ -107,21 +107,21 @@ __device__ __forceinline__ void init_extra(uint8_t *blk, int t, int nt)
         *reinterpret_cast<uint4 *>(blk + r * 128 + ch * 16) = make_uint4(x, 0u, 0u, 0u);
     }
 }
-// A chunk state from buf into a bf16 image, in two steps so that the loads are in
-// flight while the thread does other work: load_state (thread t of 256: row f = t % 64,
-// columns 16 (t / 64) .. and, for t < 64, the last column) and put_state (the image
-// row part; the fp32 last column to zf[] and, if zblk, as a hi + lo pair into the
-// extra-column block, rows 0..63).
-__device__ __forceinline__ void load_state(const float *slot, int t, float (&x)[16], float &z)
+// A chunk state, copied from buf into shared memory (the S part at st in buf's layout,
+// the last column at zs), into a bf16 image: load_state (thread t of 256: row f =
+// t % 64, columns 16 (t / 64) .. and, for t < 64, the last column) and put_state (the
+// image row part; the fp32 last column to zf[] and, if zblk, as a hi + lo pair into
+// the extra-column block, rows 0..63).
+__device__ __forceinline__ void load_state(const float *st, const float *zs, int t, float (&x)[16], float &z)
 {
     const int f = t & 63, cg = t >> 6;
-    const float4 *s4 = reinterpret_cast<const float4 *>(slot);
+    const float4 *s4 = reinterpret_cast<const float4 *>(st);
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-        const float4 a = __ldcg(s4 + (size_t)(4 * cg + e) * D + f);
+        const float4 a = s4[(4 * cg + e) * D + f];
         x[4 * e] = a.x; x[4 * e + 1] = a.y; x[4 * e + 2] = a.z; x[4 * e + 3] = a.w;
     }
-    z = cg == 0 ? __ldcg(slot + D * D + f) : 0.f;
+    z = cg == 0 ? zs[f] : 0.f;
 }
 __device__ __forceinline__ void put_state(uint8_t *img, float *zf, uint8_t *zblk, int t, const float (&x)[16], float z)
 {
@@ -271,7 +271,6 @@ bwd_tc_state(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ 
     StateSmem &sm = *reinterpret_cast<StateSmem *>(smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int bh = (int)blockIdx.x / prm.nC, c = (int)blockIdx.x % prm.nC;
-    griddep_launch_dependents();
     if (tid == 0) {
         mbar_init(&sm.k_full, 1);
         mbar_init(&sm.full, 1);
@@ -292,6 +291,7 @@ bwd_tc_state(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ 
         tma_prefetch_3d(&map_v, 0, c * kC, bh);
     }
     griddep_wait();
+    griddep_launch_dependents();  // after the wait: see the dq kernel
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -366,10 +366,10 @@ constexpr int kScanThreads = 256;
 __global__ void __launch_bounds__(kScanThreads)
 bwd_tc_scan(float *buf, int nC, int BH, int reverse)
 {
-    griddep_launch_dependents();
     constexpr int E4 = kE / 4;
     const long long gidx = (long long)blockIdx.x * kScanThreads + threadIdx.x;
     griddep_wait();
+    griddep_launch_dependents();  // after the wait: see the dq kernel
     if (gidx >= (long long)BH * E4) return;
     const long long bh = gidx / E4, e = gidx % E4;
     float4 *p = reinterpret_cast<float4 *>(buf) + bh * (long long)nC * E4 + e;
@@ -396,17 +396,18 @@ struct DqSmem {
     uint8_t k[kTile];   // phi(K)
     uint8_t v[kTile];
     uint8_t go[kTile];  // dO, then dq staged
-    uint8_t dn[kTile];  // dN (bf16), also stored to scratch
+    uint8_t dn[kTile];  // the fp32 state S before the chunk as copied, then dN (bf16), also stored to scratch
     uint8_t simg[kImg]; // bf16 S before the chunk, [f][v]
     uint8_t extra[kC * 128];
     float zf[D];        // z before the chunk (fp32)
     float gpart[2][kC]; // each group's half of dO . o per row
-    // qk_full: Q, K landed; full: V, dO landed
-    uint64_t qk_full, full, ready, t_full, p_full, o_full, dn_ready, u_full, bc_full, up_full, g_full, dq_staged, drain;
+    // qk_full: Q, K landed; full: V, dO landed; st_full: the state landed
+    uint64_t qk_full, full, st_full, ready, t_full, p_full, o_full, dn_ready, u_full, bc_full, up_full, g_full, dq_staged, drain;
     uint32_t tmem_base;
     int abort;
 };
 static_assert(sizeof(DqSmem) + 1024 <= 232448 / 2, "two dq CTAs per SM");
+static_assert(kTile == D * D * sizeof(float), "the state's fp32 copy fits the dN tile");
 
 // TMEM of the dq kernel: T at 0 (then P over its first 64 columns), [num | den] at
 // 128 (80 columns); after the output epilogue has read them, U at 0 (then U' over
@@ -425,9 +426,8 @@ bwd_tc_dq(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUt
     const int bh = (int)blockIdx.x / prm.nC, c = (int)blockIdx.x % prm.nC;
     const int len = min(kC, prm.N - c * kC);
     float *slot = buf + ((size_t)bh * prm.nC + c) * kE;
-    griddep_launch_dependents();
     if (tid == 0) {
-        uint64_t *bars[] = {&sm.qk_full, &sm.full, &sm.t_full, &sm.o_full, &sm.u_full, &sm.bc_full, &sm.g_full, &sm.drain};
+        uint64_t *bars[] = {&sm.qk_full, &sm.full, &sm.st_full, &sm.t_full, &sm.o_full, &sm.u_full, &sm.bc_full, &sm.g_full, &sm.drain};
         for (uint64_t *b : bars) mbar_init(b, 1);
         mbar_init(&sm.ready, kWork);
         mbar_init(&sm.p_full, kWork);
@@ -443,21 +443,20 @@ bwd_tc_dq(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUt
         tmem_relinquish();
     }
     if (tid < kWork) init_extra(sm.extra, tid, kWork);
-    if (warp == kTmaWarp && lane == 0) {  // into L2 while the scan before this kernel runs
-        tma_prefetch_3d(&map_q, 0, c * kC, bh);
-        tma_prefetch_3d(&map_k, 0, c * kC, bh);
-        tma_prefetch_3d(&map_v, 0, c * kC, bh);
-        tma_prefetch_3d(&map_do, 0, c * kC, bh);
-    }
-    griddep_wait();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = sm.tmem_base;
     int *abort_flag = &sm.abort;
 
+    // Dependent launch.  Every kernel of this backward triggers its dependents only
+    // after its own griddep_wait() has returned, so when this grid starts, every grid
+    // before the scan that precedes it has completed: q, k, v and dO (none of which
+    // the scan writes) are read and phi applied while the scan may still run.  Only
+    // the chunk state, which the scan writes, is read after the wait.
     if (warp == kTmaWarp) {
-        if (lane == 0 && !aborted(abort_flag)) {
+        const bool go = lane == 0 && !aborted(abort_flag);
+        if (go) {
             const uint64_t pol = l2_policy_evict_first();
             mbar_arrive_expect_tx(&sm.qk_full, 2 * kTile);  // phi starts on these
             tma_load_3d_hint(sm.q, &map_q, &sm.qk_full, 0, c * kC, bh, pol);
@@ -465,10 +464,20 @@ bwd_tc_dq(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUt
             mbar_arrive_expect_tx(&sm.full, 2 * kTile);
             tma_load_3d_hint(sm.v, &map_v, &sm.full, 0, c * kC, bh, l2_policy_evict_last());
             tma_load_3d_hint(sm.go, &map_do, &sm.full, 0, c * kC, bh, pol);
+        }
+        griddep_wait();
+        griddep_launch_dependents();
+        if (go) {
+            mbar_arrive_expect_tx(&sm.st_full, (D * D + D) * sizeof(float));
+            bulk_load(sm.dn, slot, D * D * sizeof(float), &sm.st_full);
+            bulk_load(sm.zf, slot + D * D, D * sizeof(float), &sm.st_full);
             drain(&sm.qk_full);  // no copy may still be writing shared memory when the CTA exits
             drain(&sm.full);
+            drain(&sm.st_full);
         }
     } else if (warp == kMmaWarp) {
+        griddep_wait();
+        griddep_launch_dependents();
         if (lane == 0) {
             const uint32_t qa = smem_u32(sm.q), ka = smem_u32(sm.k), va = smem_u32(sm.v), dna = smem_u32(sm.dn);
             const uint32_t sa = smem_u32(sm.simg), ex = smem_u32(sm.extra);
@@ -529,12 +538,16 @@ bwd_tc_dq(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUt
         const uint32_t tl = tmem + ((uint32_t)(32 * q) << 16);
         bool ok = !aborted(abort_flag);
         float sx[16], sz = 0.f;
-        if (ok) load_state(slot, tid, sx, sz);  // in flight during phi
         if (ok && (ok = wait_w(abort_flag, &sm.qk_full))) {
             phi_tile_rolled<D>(sm.q, tid, kWork, len);
             phi_tile_rolled<D>(sm.k, tid, kWork, len);
         }
-        if (ok) put_state(sm.simg, sm.zf, sm.extra, tid, sx, sz);
+        griddep_wait();
+        griddep_launch_dependents();
+        if (ok && (ok = wait_w(abort_flag, &sm.st_full))) {
+            load_state(reinterpret_cast<const float *>(sm.dn), sm.zf, tid, sx, sz);
+            put_state(sm.simg, sm.zf, sm.extra, tid, sx, sz);
+        }
         fence_proxy_async_smem();
         named_bar_sync(1, kWork);  // zf[] complete before any thread of either group reads it
         if (ok) mbar_arrive(&sm.ready);
@@ -662,10 +675,11 @@ struct DkSmem {
     uint8_t v[kTile];
     uint8_t dn[kTile];  // dN, then dv staged
     uint8_t rimg[kImg]; // bf16 R after the chunk, [f][v]
+    float rst[D * D];   // the fp32 R as copied
     float rf[D];        // r after the chunk (fp32)
     float dd[kC];
-    // qk_full: Q, K landed; full: V, dN landed
-    uint64_t qk_full, full, ready, tt_full, ut_full, pt_full, upt_full, dv_full, dk_full, dv_staged, dk_staged, drain;
+    // qk_full: Q, K landed; full: V, dN landed; st_full: the state landed
+    uint64_t qk_full, full, st_full, ready, tt_full, ut_full, pt_full, upt_full, dv_full, dk_full, dv_staged, dk_staged, drain;
     uint32_t tmem_base;
     int abort;
 };
@@ -687,9 +701,8 @@ bwd_tc_dkdv(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
     const int bh = (int)blockIdx.x / prm.nC, c = (int)blockIdx.x % prm.nC;
     const int len = min(kC, prm.N - c * kC);
     const float *slot = buf + ((size_t)bh * prm.nC + c) * kE;
-    griddep_launch_dependents();
     if (tid == 0) {
-        uint64_t *bars[] = {&sm.qk_full, &sm.full, &sm.tt_full, &sm.ut_full, &sm.dv_full, &sm.dk_full, &sm.drain};
+        uint64_t *bars[] = {&sm.qk_full, &sm.full, &sm.st_full, &sm.tt_full, &sm.ut_full, &sm.dv_full, &sm.dk_full, &sm.drain};
         for (uint64_t *b : bars) mbar_init(b, 1);
         mbar_init(&sm.ready, kWork);
         mbar_init(&sm.pt_full, 128);
@@ -704,21 +717,18 @@ bwd_tc_dkdv(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
         tmem_alloc(&sm.tmem_base, kTmemCols);
         tmem_relinquish();
     }
-    if (warp == kTmaWarp && lane == 0) {  // into L2 while the scan before this kernel runs
-        tma_prefetch_3d(&map_q, 0, c * kC, bh);
-        tma_prefetch_3d(&map_k, 0, c * kC, bh);
-        tma_prefetch_3d(&map_v, 0, c * kC, bh);
-        tma_prefetch_3d(&map_dn, 0, c * kC, bh);
-    }
-    griddep_wait();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = sm.tmem_base;
     int *abort_flag = &sm.abort;
 
+    // As in the dq kernel: q, k, v, and dN and dd (the dq kernel's, which completed
+    // before the scan preceding this grid passed its wait) are read before the wait;
+    // the state R, which that scan writes, after it.
     if (warp == kTmaWarp) {
-        if (lane == 0 && !aborted(abort_flag)) {
+        const bool go = lane == 0 && !aborted(abort_flag);
+        if (go) {
             const uint64_t pol = l2_policy_evict_first();
             mbar_arrive_expect_tx(&sm.qk_full, 2 * kTile);  // phi starts on these
             tma_load_3d_hint(sm.q, &map_q, &sm.qk_full, 0, c * kC, bh, pol);
@@ -726,10 +736,20 @@ bwd_tc_dkdv(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
             mbar_arrive_expect_tx(&sm.full, 2 * kTile);
             tma_load_3d_hint(sm.v, &map_v, &sm.full, 0, c * kC, bh, pol);
             tma_load_3d_hint(sm.dn, &map_dn, &sm.full, 0, c * kC, bh, pol);
+        }
+        griddep_wait();
+        griddep_launch_dependents();
+        if (go) {
+            mbar_arrive_expect_tx(&sm.st_full, (D * D + D) * sizeof(float));
+            bulk_load(sm.rst, slot, D * D * sizeof(float), &sm.st_full);
+            bulk_load(sm.rf, slot + D * D, D * sizeof(float), &sm.st_full);
             drain(&sm.qk_full);
             drain(&sm.full);
+            drain(&sm.st_full);
         }
     } else if (warp == kMmaWarp) {
+        griddep_wait();
+        griddep_launch_dependents();
         if (lane == 0) {
             const uint32_t qa = smem_u32(sm.q), ka = smem_u32(sm.k), va = smem_u32(sm.v), dna = smem_u32(sm.dn);
             const uint32_t ra = smem_u32(sm.rimg);
@@ -777,15 +797,15 @@ bwd_tc_dkdv(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
         const uint32_t tl = tmem + ((uint32_t)(32 * q) << 16);
         bool ok = !aborted(abort_flag);
         float sx[16], sz = 0.f, ddv = 0.f;
-        if (ok) {
-            load_state(slot, tid, sx, sz);  // in flight during phi
-            if (tid < kC && tid < len) ddv = __ldcg(ddbuf + (size_t)bh * prm.N + c * kC + tid);
-        }
+        if (ok && tid < kC && tid < len) ddv = __ldcg(ddbuf + (size_t)bh * prm.N + c * kC + tid);  // in flight during phi
         if (ok && (ok = wait_w(abort_flag, &sm.qk_full))) {
             phi_tile_rolled<D>(sm.q, tid, kWork, len);
             phi_tile_rolled<D>(sm.k, tid, kWork, len);
         }
-        if (ok) {
+        griddep_wait();
+        griddep_launch_dependents();
+        if (ok && (ok = wait_w(abort_flag, &sm.st_full))) {
+            load_state(sm.rst, sm.rf, tid, sx, sz);
             put_state(sm.rimg, sm.rf, nullptr, tid, sx, sz);
             if (tid < kC) sm.dd[tid] = ddv;
         }
