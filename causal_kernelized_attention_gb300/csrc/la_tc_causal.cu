@@ -34,6 +34,7 @@
 #include "la_internal.h"
 #include "la_sm100.cuh"
 #include "la_tc_common.cuh"
+#include "la_tc_pad.cuh"
 
 #include <algorithm>
 #include <mutex>
@@ -143,6 +144,9 @@ struct Params {
     int map;
     float shift;
     int normalize;
+    // Feature widths (multiples of 8, at most D): q, k carry dk columns, v, o dv;
+    // the tiles' columns past them are zero (see zero_cols).
+    int dk, dv;
 };
 
 __device__ __forceinline__ bool wait_bar(int *abort_flag, uint64_t *bar, uint32_t parity)
@@ -391,10 +395,12 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
         for (int x = 0; x < min(ps.nA + ps.nch, S); ++x) {
             const int row0 = job_chunk(x, ps.nA, ps.a0, ps.c0) * kC;
 #pragma unroll
-            for (int b = 0; b < D / 64; ++b) {
-                if (x >= ps.nA) tma_prefetch_3d(&map_q, 64 * b, row0, ps.bh);
-                tma_prefetch_3d(&map_k, 64 * b, row0, ps.bh);
-                tma_prefetch_3d(&map_v, 64 * b, row0, ps.bh);
+            for (int b = 0; b < D / 64; ++b) {  // (boxes past a width hold no data)
+                if (64 * b < prm.dk) {
+                    if (x >= ps.nA) tma_prefetch_3d(&map_q, 64 * b, row0, ps.bh);
+                    tma_prefetch_3d(&map_k, 64 * b, row0, ps.bh);
+                }
+                if (64 * b < prm.dv) tma_prefetch_3d(&map_v, 64 * b, row0, ps.bh);
             }
         }
     }
@@ -468,9 +474,11 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
             const int valid = prm.N - chunk * kC;
             if (isC) {
                 phi_tile<D, kPhiThreads, false, kVar>(sm.k[s], tid, valid, 0.f, 0, prm.map, prm.shift);
+                if (prm.dk < D) zero_cols<D>(sm.k[s], tid, kPhiThreads, prm.dk);
                 phi_tile<D, kPhiThreads, false, kVar>(sm.q[s], tid, valid, 0.f, 0, prm.map, prm.shift);
             } else {  // the other half: epilogue warps
                 phi_tile<D, 2 * kPhiThreads, kDecay, kVar>(sm.k[s], tid, valid, lg, eA - chunk * kC, prm.map, prm.shift);
+                if (prm.dk < D) zero_cols<D>(sm.k[s], tid, 2 * kPhiThreads, prm.dk);
             }
             fence_proxy_async_smem();
             if (isC)
@@ -679,6 +687,7 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
             const int chunk = job_chunk(j, nA, a0, c0);
             phi_tile<D, 2 * kPhiThreads, kDecay, kVar>(sm.k[s], kPhiThreads + gtid, prm.N - chunk * kC, lg,
                                                       eA - chunk * kC, prm.map, prm.shift);
+            if (prm.dk < D) zero_cols<D>(sm.k[s], kPhiThreads + gtid, 2 * kPhiThreads, prm.dk);
             fence_proxy_async_smem();
             mbar_arrive(&sm.phi_done[s]);
         }
@@ -976,7 +985,7 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
                 }
                 const float inv = (kVar && !prm.normalize) ? 1.f : 1.f / fmaxf(den, prm.eps);
 #pragma unroll 1
-                for (int cc = 0; cc < D / 64; ++cc) {
+                for (int cc = 0; cc < D / 64 && 64 * cc < prm.dv; ++cc) {  // (columns past dv are not stored)
                     uint32_t a[64];
                     if constexpr (CF::kFused) {
 #pragma unroll
@@ -1008,7 +1017,8 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
                     const uint64_t pol_once = l2_policy_evict_first();
 #pragma unroll
                     for (int cc = 0; cc < D / 64; ++cc)
-                        tma_store_3d_hint(&map_o, sm.q[s] + cc * kBox, 64 * cc, (c0 + cj) * kC, bh, pol_once);
+                        if (64 * cc < prm.dv)
+                            tma_store_3d_hint(&map_o, sm.q[s] + cc * kBox, 64 * cc, (c0 + cj) * kC, bh, pol_once);
                     tma_store_commit();
                 }
                 if (!CF::kFused && cj < nch - 1 && !refresh_state<D, kDecay>(sm, abort_flag, tl, i, row_ok, cj, gC))
@@ -1048,10 +1058,10 @@ template <int D, bool kDecay, bool kVar>
 la_status launch(const Problem &p)
 {
     CUtensorMap mq, mk, mv, mo;
-    la_status st = make_map(&mq, p.q, p.BH, p.N, D);
-    if (st == LA_OK) st = make_map(&mk, p.k, p.BH, p.N, D);
-    if (st == LA_OK) st = make_map(&mv, p.v, p.BH, p.N, D);
-    if (st == LA_OK) st = make_map(&mo, p.o, p.BH, p.N, D);
+    la_status st = make_map(&mq, p.q, p.BH, p.N, p.dk);
+    if (st == LA_OK) st = make_map(&mk, p.k, p.BH, p.N, p.dk);
+    if (st == LA_OK) st = make_map(&mv, p.v, p.BH, p.N, p.dv);
+    if (st == LA_OK) st = make_map(&mo, p.o, p.BH, p.N, p.dv);
     if (st != LA_OK) return st;
 
     const int n_chunks = ceil_div(p.N, kC);
@@ -1139,6 +1149,8 @@ la_status launch(const Problem &p)
     prm.map = p.var.map;
     prm.shift = p.var.shift;
     prm.normalize = p.var.normalize;
+    prm.dk = p.dk;
+    prm.dv = p.dv;
 
     const int smem = (int)sizeof(Smem<D>);
     auto kern = causal_tc_kernel<D, kDecay, kVar>;
@@ -1158,9 +1170,20 @@ la_status causal_tc(const Problem &p_in)
     if (p_in.chunk != 64 && p_in.chunk != kC) return LA_ERR_UNSUPPORTED;
     Problem p = p_in;
     p.chunk = kC;
-    if (p.dtype != LA_BF16 || p.dk != p.dv || (p.dk != 64 && p.dk != 128) || p.N < kC)
-        return LA_ERR_UNSUPPORTED;
+    if (p.dtype != LA_BF16 || p.N < kC) return LA_ERR_UNSUPPORTED;
     const bool var = !p.var.is_default();
+    if (p.dk != p.dv || (p.dk != 64 && p.dk != 128)) {
+        // Other widths (multiples of 8 up to 128, dk and dv apart): the general kernel
+        // for the next tile width, the columns past each width zero.
+        if (!padded_widths_ok(p.dk, p.dv)) return LA_ERR_UNSUPPORTED;
+        const bool wide = std::max(p.dk, p.dv) > 64;
+        if (p.gamma) {
+            if (var) return wide ? launch<128, true, true>(p) : launch<64, true, true>(p);
+            return wide ? launch<128, true, false>(p) : launch<64, true, false>(p);
+        }
+        if (var) return wide ? launch<128, false, true>(p) : launch<64, false, true>(p);
+        return wide ? launch<128, false, false>(p) : launch<64, false, false>(p);
+    }
     if (p.gamma) {
         if (var) return p.dk == 128 ? launch<128, true, true>(p) : launch<64, true, true>(p);
         return p.dk == 128 ? launch<128, true, false>(p) : launch<64, true, false>(p);

@@ -40,6 +40,7 @@
 #include "la_internal.h"
 #include "la_sm100.cuh"
 #include "la_tc_common.cuh"
+#include "la_tc_pad.cuh"
 
 #include <algorithm>
 
@@ -145,6 +146,9 @@ struct Params {
     int map;
     float shift;
     int normalize;
+    // Feature widths (multiples of 8, at most D; output mode): q, k carry dk
+    // columns, v, o dv; the tiles' columns past them are zero (see zero_cols).
+    int dk, dv;
 };
 
 // State mode, decayed state or another feature map: the map (elu + 1, max(x, 0) + c
@@ -437,6 +441,7 @@ noncausal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
                         phi_tile_split<D, kPhiThreads>(sm.stage[s], b ? sm.lo1 : sm.aux + CF::kImg0, t, valid);
                 } else {
                     phi_tile<D, kPhiThreads, false, kVar>(sm.stage[s], t, valid, 0.f, 0, prm.map, prm.shift);
+                    if (prm.dk < D && item.kind == kSum) zero_cols<D>(sm.stage[s], t, kPhiThreads, prm.dk);
                 }
                 fence_proxy_async_smem();
                 mbar_arrive(&sm.phi_done[s]);
@@ -739,7 +744,7 @@ noncausal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
                     }
                     uint8_t *ost = sm.stage[s] + kTile;  // the second tile of the stage stages O
 #pragma unroll 1
-                    for (int cc = 0; cc < D / 64; ++cc) {
+                    for (int cc = 0; cc < D / 64 && 64 * cc < prm.dv; ++cc) {  // (columns past dv are not stored)
                         uint32_t v[64];
                         tmem_ld32(ta + cc * 64, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
                         tmem_ld32(ta + cc * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
@@ -763,7 +768,8 @@ noncausal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
                         const uint64_t pol_once = l2_policy_evict_first();
 #pragma unroll
                         for (int cc = 0; cc < D / 64; ++cc)
-                            tma_store_3d_hint(&map_o, ost + cc * kBox, 64 * cc, (item.c0 + c) * kC, item.bh, pol_once);
+                            if (64 * cc < prm.dv)
+                                tma_store_3d_hint(&map_o, ost + cc * kBox, 64 * cc, (item.c0 + c) * kC, item.bh, pol_once);
                         tma_store_commit();
                         // The previous tile's store has read its staged O: that stage may be refilled.
                         tma_store_wait_read<1>();
@@ -810,10 +816,10 @@ la_status launch(const Problem &p, float *S_out = nullptr, float *z_out = nullpt
     // and are built on k.
     const bool state = S_out != nullptr;
     CUtensorMap mq, mk, mv, mo;
-    la_status st = make_map(&mq, state ? p.k : p.q, p.BH, p.N, D);
-    if (st == LA_OK) st = make_map(&mk, p.k, p.BH, p.N, D);
-    if (st == LA_OK) st = make_map(&mv, p.v, p.BH, p.N, D);
-    if (st == LA_OK) st = make_map(&mo, state ? p.k : p.o, p.BH, p.N, D);
+    la_status st = make_map(&mq, state ? p.k : p.q, p.BH, p.N, p.dk);
+    if (st == LA_OK) st = make_map(&mk, p.k, p.BH, p.N, p.dk);
+    if (st == LA_OK) st = make_map(&mv, p.v, p.BH, p.N, p.dv);
+    if (st == LA_OK) st = make_map(&mo, state ? p.k : p.o, p.BH, p.N, state ? p.dk : p.dv);
     if (st != LA_OK) return st;
 
     const int n_chunks = ceil_div(p.N, kC);
@@ -884,6 +890,8 @@ la_status launch(const Problem &p, float *S_out = nullptr, float *z_out = nullpt
     prm.map = p.var.map;
     prm.shift = p.var.shift;
     prm.normalize = p.var.normalize;
+    prm.dk = p.dk;
+    prm.dv = p.dv;
 
     const int smem = (int)sizeof(Smem<D>);
     auto kern = noncausal_tc_kernel<D, kVar>;
@@ -898,10 +906,12 @@ la_status launch(const Problem &p, float *S_out = nullptr, float *z_out = nullpt
 
 la_status noncausal_tc(const Problem &p)
 {
-    if (p.dtype != LA_BF16 || p.dk != p.dv || (p.dk != 64 && p.dk != 128) || p.N < kC)
-        return LA_ERR_UNSUPPORTED;
-    if (!p.var.is_default()) return p.dk == 128 ? launch<128, true>(p) : launch<64, true>(p);
-    return p.dk == 128 ? launch<128, false>(p) : launch<64, false>(p);
+    if (p.dtype != LA_BF16 || p.N < kC || !padded_widths_ok(p.dk, p.dv)) return LA_ERR_UNSUPPORTED;
+    // dk = dv = 64 or 128, or other widths on the next tile width (columns past each
+    // width zero)
+    const bool wide = std::max(p.dk, p.dv) > 64;
+    if (!p.var.is_default()) return wide ? launch<128, true>(p) : launch<64, true>(p);
+    return wide ? launch<128, false>(p) : launch<64, false>(p);
 }
 
 la_status noncausal_tc_state(const void *k, const void *v, float *S, float *z, int BH, int N, int D,

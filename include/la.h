@@ -87,12 +87,13 @@ typedef struct CUstream_st *la_stream_t;
  * o[b,h,i,:] = phi(q_i)^T S_i / max(phi(q_i)^T z_i, eps) with the sums over
  * j <= i of the same (b,h) (inclusive of i).  N need not be a multiple of
  * `chunk`; the last chunk is then shorter.  `chunk` must be 64 or 128.
- * Supported: dk, dv in {32, 64, 128} for fp32; for bf16 dk == dv in
- * {64, 128} on the tensor-core path, and dk, dv in {32, 64, 128} otherwise.
- * The tensor-core path (bf16, dk == dv in {64, 128}, N >= 128) computes with
- * chunks of 128 tokens whether `chunk` is 64 or 128: the chunked form is the
- * same function for every chunk length, only the order of the roundings
- * differs.  The CUDA-core path (fp32, other shapes) uses `chunk` as given.
+ * Supported: dk, dv in {32, 64, 128}.  bf16 with N >= 128 runs on the
+ * tensor cores, any dk and dv (with dk != dv, or 32, on tiles of the next
+ * width, 64 or 128, whose extra columns are zero and drop out of every
+ * product); it computes with chunks of 128 tokens whether `chunk` is 64 or
+ * 128: the chunked form is the same function for every chunk length, only the
+ * order of the roundings differs.  The CUDA-core path (fp32, N < 128) uses
+ * `chunk` as given.
  */
 la_status la_forward_causal(const void *q, const void *k, const void *v, void *o,
                             int B, int H, int N, int dk, int dv, int chunk, float eps,
@@ -107,7 +108,10 @@ la_status la_forward_causal(const void *q, const void *k, const void *v, void *o
  *
  * o_i = phi(q_i)^T S / max(phi(q_i)^T z, eps), S = sum_j phi(k_j) v_j^T,
  * z = sum_j phi(k_j), j over all N positions of the same (b,h).
- * Supported: dk, dv in {32, 64, 128}.
+ * Supported: dk, dv in {32, 64, 128}.  bf16 with N >= 128 runs on the
+ * tensor cores for every dk and dv (widths other than dk = dv in {64, 128}
+ * on tiles of the next width, the extra columns zero); fp32 and shorter
+ * sequences on the CUDA cores.
  */
 la_status la_forward_noncausal(const void *q, const void *k, const void *v, void *o,
                                int B, int H, int N, int dk, int dv, float eps,
@@ -186,8 +190,8 @@ la_status la_decode_step(float *S, float *z, const void *q, const void *k, const
  * Head h of every batch entry uses gamma[h].  gamma must be 4-byte aligned and
  * must not overlap o; its values are read by the kernel and not checked (the
  * method takes them in [0, 1]).  `chunk` (64 or 128) is the length of the
- * intra-chunk quadratic blocks on the CUDA cores.  bf16 with dk = dv in
- * {64, 128} and N >= 128 runs on the tensor cores (128-token chunks) (the kernel of la_forward_causal with the
+ * intra-chunk quadratic blocks on the CUDA cores.  bf16 with N >= 128 runs on
+ * the tensor cores (128-token chunks, any dk, dv as la_forward_causal) (the kernel of la_forward_causal with the
  * decay weights in the intra-chunk mask, on the rows of phi(Q) and phi(K), on
  * the running state and in the scan across segments); other shapes run on the
  * CUDA cores in fp32.  Supported: dk, dv in {32, 64, 128}.
@@ -313,8 +317,8 @@ typedef struct {
  * and results as the specialised entry points, which they reduce to:
  *   la_forward_causal_ex(..., NULL, NULL, ...)   = la_forward_causal
  *   la_forward_causal_ex(..., gamma, NULL, ...)  = la_forward_causal_decay
- * bf16 with dk = dv in {64, 128} (and N >= 128 for the causal form)
- * runs on the tensor cores for every variant; other shapes on the CUDA cores.
+ * bf16 with N >= 128 runs on the tensor cores for every variant and every
+ * dk, dv; fp32 and shorter sequences on the CUDA cores.
  * An invalid variant (unknown map, non-finite shift, normalize not 0 or 1)
  * returns LA_ERR_INVALID_ARG.
  */
