@@ -357,10 +357,10 @@ la_status la_prefill_state_ex(const void *k, const void *v, const float *gamma, 
         (overlaps(gamma, (size_t)H * 4, S, BH * dk * dv * 4) || overlaps(gamma, (size_t)H * 4, z, BH * dk * 4)))
         return LA_ERR_INVALID_ARG;
     if (N == 0) gamma = nullptr;
-    // bf16 with dk = dv in {64, 128}: the summary phase of the tensor-core non-causal
-    // kernel (the final causal state is the non-causal state of the prefix).
-    if (dtype == LA_BF16 && dk == dv && (dk == 64 || dk == 128) && N >= 128) {
-        st = noncausal_tc_state(k, v, S, z, (int)BH, N, dk, (cudaStream_t)stream, gamma, H, var);
+    // bf16: the summary phase of the tensor-core non-causal kernel (the final causal
+    // state is the non-causal state of the prefix).
+    if (dtype == LA_BF16 && N >= 128) {
+        st = noncausal_tc_state(k, v, S, z, (int)BH, N, dk, dv, (cudaStream_t)stream, gamma, H, var);
         if (st != LA_ERR_UNSUPPORTED) return st;
     }
     return state_simt(k, v, S, z, (int)BH, N, dk, dv, dtype, (cudaStream_t)stream, gamma, H, var);

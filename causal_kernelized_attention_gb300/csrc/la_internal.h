@@ -104,10 +104,11 @@ la_status causal_chunks_tc(const Problem &p);
 la_status causal_cluster_tc(const Problem &p);
 // (la_tc_noncausal.cu)
 la_status noncausal_tc(const Problem &p);
-// S, z (fp32, [BH,D,D], [BH,D]) = sums over N tokens on the tensor cores (bf16
-// k, v; D in {64, 128}, N >= 128); overwrites S and z.  gamma (device, [H]): token
-// t weighted by gamma[bh % H]^(N-1-t); null: unweighted.
-la_status noncausal_tc_state(const void *k, const void *v, float *S, float *z, int BH, int N, int D,
+// S, z (fp32, [BH,dk,dv], [BH,dk]) = sums over N tokens on the tensor cores (bf16
+// k, v; dk, dv multiples of 8 up to 128 (on tiles of 64 or 128 columns), N >= 128);
+// overwrites S and z.  gamma (device, [H]): token t weighted by gamma[bh % H]^(N-1-t);
+// null: unweighted.
+la_status noncausal_tc_state(const void *k, const void *v, float *S, float *z, int BH, int N, int dk, int dv,
                              cudaStream_t stream, const float *gamma = nullptr, int H = 1,
                              const Variant &var = Variant());
 

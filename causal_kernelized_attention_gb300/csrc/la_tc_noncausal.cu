@@ -135,8 +135,9 @@ struct Params {
     int P, L1;           // splits per head, key chunks per split
     int T, L2;           // output items per head, query chunks per item
     float eps;
-    // State mode (T = 0, no output items): the sums are written to S_out [BH, D, D]
-    // (row = key feature) and z_out [BH, D], fp32, row-major; null otherwise.
+    // State mode (T = 0, no output items): the sums are written to S_out [BH, dk, dv]
+    // (row = key feature) and z_out [BH, dk], fp32, row-major; null otherwise.  (Rows
+    // past dk, fed by phi(0) of the zero-filled columns, are not written.)
     float *S_out, *z_out;
     // State mode, decayed state: token t of head bh weighted by gamma[bh % H]^(N-1-t)
     // (the decayed recurrence unrolled over the prefix); null otherwise.
@@ -293,7 +294,7 @@ __device__ __forceinline__ void build_image(const Params &prm, int bh, int t)
 }
 
 // State mode: sums the head's P partials in split order and writes S (fp32,
-// [D, D] row-major, row = key feature) and z (fp32, [D]).  Run by the 128
+// [dk, dv] row-major, row = key feature) and z (fp32, [dk]).  Run by the 128
 // epilogue threads; thread t takes row t % D and a column range.
 template <int D>
 __device__ __forceinline__ void write_state(const Params &prm, int bh, int t)
@@ -308,20 +309,21 @@ __device__ __forceinline__ void write_state(const Params &prm, int bh, int t)
 #pragma unroll
         for (int e = 0; e < 32; ++e) acc[e] = 0.f;
         const int col0 = grp * kCols + cc;
+        if (i >= prm.dk || col0 >= prm.dv) continue;
         int p = 0;
         for (; p + 1 < prm.P; p += 2) {
             add_state<D>(acc, part + p * seg, col0 >> 2, i);
             add_state<D>(acc, part + (p + 1) * seg, col0 >> 2, i);
         }
         if (p < prm.P) add_state<D>(acc, part + p * seg, col0 >> 2, i);
-        float4 *dst = reinterpret_cast<float4 *>(prm.S_out + ((size_t)bh * D + i) * D + col0);
+        float4 *dst = reinterpret_cast<float4 *>(prm.S_out + ((size_t)bh * prm.dk + i) * prm.dv + col0);
 #pragma unroll
         for (int e = 0; e < 8; ++e) dst[e] = make_float4(acc[4 * e], acc[4 * e + 1], acc[4 * e + 2], acc[4 * e + 3]);
     }
-    if (t < D) {
+    if (t < prm.dk) {
         float zk = 0.f;
         for (int q = 0; q < prm.P; ++q) zk += __ldcg(part + q * seg + (size_t)D * D + t);
-        prm.z_out[(size_t)bh * D + t] = zk;
+        prm.z_out[(size_t)bh * prm.dk + t] = zk;
     }
 }
 
@@ -678,7 +680,8 @@ noncausal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
                     tmem_ld32(ta + cc, v);
                     tmem_ld_wait();
                     if (i < D && state_now) {
-                        float4 *d4 = reinterpret_cast<float4 *>(prm.S_out + ((size_t)item.bh * D + i) * D + cc);
+                        if (i >= prm.dk || cc >= prm.dv) continue;  // (after the warp-wide tmem_ld32)
+                        float4 *d4 = reinterpret_cast<float4 *>(prm.S_out + ((size_t)item.bh * prm.dk + i) * prm.dv + cc);
 #pragma unroll
                         for (int e = 0; e < 8; ++e)
                             d4[e] = make_float4(__uint_as_float(v[4 * e]), __uint_as_float(v[4 * e + 1]),
@@ -695,9 +698,9 @@ noncausal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
                 const float zs = __uint_as_float(tmem_ld1(ta + D));
                 tmem_ld_wait();
                 if (i < D) {
-                    if (state_now)
-                        prm.z_out[(size_t)item.bh * D + i] = zs;
-                    else
+                    if (state_now) {
+                        if (i < prm.dk) prm.z_out[(size_t)item.bh * prm.dk + i] = zs;
+                    } else
                         dst[(size_t)D * D + i] = zs;
                 }
                 tc_fence_before();
@@ -914,10 +917,11 @@ la_status noncausal_tc(const Problem &p)
     return wide ? launch<128, false>(p) : launch<64, false>(p);
 }
 
-la_status noncausal_tc_state(const void *k, const void *v, float *S, float *z, int BH, int N, int D,
+la_status noncausal_tc_state(const void *k, const void *v, float *S, float *z, int BH, int N, int dk, int dv,
                              cudaStream_t stream, const float *gamma, int H, const Variant &var)
 {
-    if ((D != 64 && D != 128) || N < kC) return LA_ERR_UNSUPPORTED;
+    if (N < kC || !padded_widths_ok(dk, dv)) return LA_ERR_UNSUPPORTED;
+    const int D = std::max(dk, dv) > 64 ? 128 : 64;
     Problem p{};
     p.q = k;
     p.k = k;
@@ -925,7 +929,8 @@ la_status noncausal_tc_state(const void *k, const void *v, float *S, float *z, i
     p.o = nullptr;
     p.BH = BH;
     p.N = N;
-    p.dk = p.dv = D;
+    p.dk = dk;
+    p.dv = dv;
     p.chunk = kC;
     p.eps = 0.f;
     p.dtype = LA_BF16;

@@ -220,8 +220,9 @@ la_status la_decode_step_decay(float *S, float *z, const void *q, const void *k,
  *   k : [B, H, N, dk]   v : [B, H, N, dv]   S : [B, H, dk, dv] fp32   z : [B, H, dk] fp32
  *
  * S and z are OVERWRITTEN (not accumulated).  N = 0 writes zeros.
- * Supported: dk, dv in {32, 64, 128}.  bf16 with dk = dv in {64, 128} and
- * N >= 128 runs on the tensor cores: phi(k) is evaluated in fp32 and split into
+ * Supported: dk, dv in {32, 64, 128}.  bf16 with N >= 128 runs on the tensor
+ * cores (any dk, dv; other than dk = dv in {64, 128} on tiles of the next
+ * width): phi(k) is evaluated in fp32 and split into
  * a bf16 high part and a bf16 low part (together accurate to about 2^-17), both
  * multiplied by v with fp32 accumulation; other shapes use fp32 CUDA-core
  * arithmetic.
@@ -239,9 +240,9 @@ la_status la_prefill_state(const void *k, const void *v, float *S, float *z,
  * so that la_decode_step_decay continues the sequence.  Layouts as
  * la_prefill_state; gamma as la_forward_causal_decay (DEVICE memory, [H] fp32,
  * 4-byte aligned, not overlapping S or z; may be NULL when N = 0).  S and z are
- * OVERWRITTEN; N = 0 writes zeros.  bf16 with dk = dv in {64, 128} and N >= 128
- * runs on the tensor cores as la_prefill_state does (phi(k) times its weight in
- * fp32, split into bf16 high and low parts); other shapes on the CUDA cores in fp32.
+ * OVERWRITTEN; N = 0 writes zeros.  bf16 with N >= 128 runs on the tensor cores
+ * as la_prefill_state does, for the same widths (phi(k) times its weight in fp32,
+ * split into bf16 high and low parts); fp32 and shorter prefixes on the CUDA cores.
  */
 la_status la_prefill_state_decay(const void *k, const void *v, const float *gamma, float *S,
                                  float *z, int B, int H, int N, int dk, int dv, la_dtype dtype,

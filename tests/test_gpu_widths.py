@@ -149,3 +149,27 @@ def test_widths_run_on_the_tensor_cores(path, dk, dv):
     want = "causal_tc_kernel" if path == "causal" else "noncausal_tc_kernel"
     assert any(want in n for n in names), names
     assert not any("simt" in n for n in names), names
+
+
+@pytest.mark.parametrize("B,H,N,dk,dv", [
+    (2, 3, 700, 32, 32), (1, 4, 2000, 64, 128), (2, 2, 300, 128, 32), (16, 20, 130, 32, 64),
+    (1, 2, 65536, 32, 128),
+])
+@pytest.mark.parametrize("fmap,shift,decay", [("elu1", 0.0, False), ("elu1", 0.0, True), ("relu", 0.3, False)])
+def test_prefill_state_widths(orc, B, H, N, dk, dv, fmap, shift, decay):
+    """The prefix state [dk, dv] and z [dk] from the D-wide sums: one key split per
+    head (written by the split itself: 16 x 20 heads of one chunk) and many (summed
+    by the CTA that completes the last); the state rows past dk, fed by phi(0), are
+    not written."""
+    _, k, v = workloads.random_inputs(35000 + N + dk + dv, B, H, N, dk, dv, "bf16")
+    gamma = workloads.decay_gammas(H) if decay else None
+    S, z = la().la_prefill_state_ex(to_dev(k, "bf16"), to_dev(v, "bf16"),
+                                    gamma=None if gamma is None else torch.from_numpy(gamma).cuda(),
+                                    feature_map=fmap, shift=shift)
+    torch.cuda.synchronize()
+    assert la().la_get_device_status() == 0
+    assert S.shape == (B, H, dk, dv) and z.shape == (B, H, dk)
+    Sr, zr = orc.prefill_state_general(k, v, gamma=None if gamma is None else gamma.astype(np.float64),
+                                       fmap=fmap, shift=shift)
+    es, ez = errors(from_dev(S), Sr), errors(from_dev(z), zr)
+    assert es["normwise"] < 1e-5 and ez["normwise"] < 1e-5, (es, ez)
