@@ -55,7 +55,7 @@ struct BackwardProblem {
     cudaStream_t stream;
 };
 la_status causal_backward(const BackwardProblem &p);
-// Tensor-core backward (la_tc_backward.cu): bf16, dk = dv = 64, N >= 128.
+// Tensor-core backward (la_tc_backward.cu): bf16, dk, dv <= 64 (64-column tiles), N >= 128.
 bool backward_tc_eligible(const BackwardProblem &p);
 la_status causal_backward_tc(const BackwardProblem &p);
 

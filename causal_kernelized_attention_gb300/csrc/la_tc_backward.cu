@@ -1,5 +1,5 @@
-// Backward pass of the causal form on the tensor cores: bf16 q, k, v, dO, dk = dv = 64,
-// N >= 128; fp32 accumulation, bf16 gradients.  The same chain rule as the CUDA-core
+// Backward pass of the causal form on the tensor cores: bf16 q, k, v, dO, dk = dv = 64
+// (narrower widths on the same tiles: see backward_tc_eligible), N >= 128; fp32 accumulation, bf16 gradients.  The same chain rule as the CUDA-core
 // backward in la_backward.cu (the pages give no gradient; "Linear Attention -- Math +
 // Variants", Chunkwise parallelism: training runs the chunked form), over chunks of
 // C = 128 tokens, with every block product a tcgen05 MMA:
@@ -39,6 +39,7 @@
 #include "la_internal.h"
 #include "la_sm100.cuh"
 #include "la_tc_common.cuh"
+#include "la_tc_pad.cuh"
 
 namespace la {
 namespace {
@@ -249,6 +250,7 @@ __device__ __forceinline__ float dphi(float phi) { return fminf(phi, 1.f); }
 struct Params {
     int N, BH, nC;
     float eps;
+    int dk;  // q, k, dq, dk width (at most D; columns past it are zero in phi(K), clipped from the stores)
 };
 
 // ---------------------------------------------------------------------- 1. chunk states
@@ -309,6 +311,7 @@ bwd_tc_state(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ 
     bool ok = !aborted(abort_flag) && wait_w(abort_flag, &sm.k_full);
     if (ok) {
         phi_tile_rolled<D>(sm.k, tid, kStateThreads, prm.N - c * kC);
+        if (prm.dk < D) zero_cols<D>(sm.k, tid, kStateThreads, prm.dk);
         fence_proxy_async_smem();
         ok = wait_w(abort_flag, &sm.full);
     }
@@ -541,6 +544,7 @@ bwd_tc_dq(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUt
         if (ok && (ok = wait_w(abort_flag, &sm.qk_full))) {
             phi_tile_rolled<D>(sm.q, tid, kWork, len);
             phi_tile_rolled<D>(sm.k, tid, kWork, len);
+            if (prm.dk < D) zero_cols<D>(sm.k, tid, kWork, prm.dk);
         }
         griddep_wait();
         griddep_launch_dependents();
@@ -801,6 +805,7 @@ bwd_tc_dkdv(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
         if (ok && (ok = wait_w(abort_flag, &sm.qk_full))) {
             phi_tile_rolled<D>(sm.q, tid, kWork, len);
             phi_tile_rolled<D>(sm.k, tid, kWork, len);
+            if (prm.dk < D) zero_cols<D>(sm.k, tid, kWork, prm.dk);
         }
         griddep_wait();
         griddep_launch_dependents();
@@ -888,9 +893,13 @@ bwd_tc_dkdv(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
 
 }  // namespace
 
+// dk = dv = 64, or narrower widths (multiples of 8) on the same 64-column tiles: the
+// zero-filled columns of q, k, v and dO enter phi(K) as 0 (zero_cols), so the forward
+// quantities are exact; the terms phi(Q)'s extra columns feed (rows of R, columns of
+// dphi(Q) and dphi(K)) land only in output columns past the widths, which the stores clip.
 bool backward_tc_eligible(const BackwardProblem &p)
 {
-    return p.dtype == LA_BF16 && p.dkd == D && p.dvd == D && p.N >= kC;
+    return p.dtype == LA_BF16 && padded_widths_ok(p.dkd, p.dvd) && p.dkd <= D && p.dvd <= D && p.N >= kC;
 }
 
 la_status causal_backward_tc(const BackwardProblem &p)
@@ -917,20 +926,20 @@ la_status causal_backward_tc(const BackwardProblem &p)
     float *buf = (float *)base, *ddbuf = buf + state_floats;
     void *dn = (uint8_t *)base + dn_off;
     CUtensorMap mq, mk, mv, mdo, mdn, mdq, mdk, mdv;
-    st = make_map(&mq, p.q, p.BH, p.N, D);
-    if (st == LA_OK) st = make_map(&mk, p.k, p.BH, p.N, D);
-    if (st == LA_OK) st = make_map(&mv, p.v, p.BH, p.N, D);
-    if (st == LA_OK) st = make_map(&mdo, p.dout, p.BH, p.N, D);
+    st = make_map(&mq, p.q, p.BH, p.N, p.dkd);
+    if (st == LA_OK) st = make_map(&mk, p.k, p.BH, p.N, p.dkd);
+    if (st == LA_OK) st = make_map(&mv, p.v, p.BH, p.N, p.dvd);
+    if (st == LA_OK) st = make_map(&mdo, p.dout, p.BH, p.N, p.dvd);
     if (st == LA_OK) st = make_map(&mdn, dn, p.BH, p.N, D);
-    if (st == LA_OK) st = make_map(&mdq, p.dq, p.BH, p.N, D);
-    if (st == LA_OK) st = make_map(&mdk, p.dk, p.BH, p.N, D);
-    if (st == LA_OK) st = make_map(&mdv, p.dv, p.BH, p.N, D);
+    if (st == LA_OK) st = make_map(&mdq, p.dq, p.BH, p.N, p.dkd);
+    if (st == LA_OK) st = make_map(&mdk, p.dk, p.BH, p.N, p.dkd);
+    if (st == LA_OK) st = make_map(&mdv, p.dv, p.BH, p.N, p.dvd);
     if (st != LA_OK) return st;
     if (st == LA_OK) st = ensure_smem((const void *)bwd_tc_state, (int)sizeof(StateSmem));
     if (st == LA_OK) st = ensure_smem((const void *)bwd_tc_dq, (int)sizeof(DqSmem));
     if (st == LA_OK) st = ensure_smem((const void *)bwd_tc_dkdv, (int)sizeof(DkSmem));
     if (st != LA_OK) return st;
-    Params prm{p.N, p.BH, nC, p.eps};
+    Params prm{p.N, p.BH, nC, p.eps, p.dkd};
     const unsigned grid = (unsigned)(p.BH * nC);
     const unsigned scan_grid = (unsigned)(((long long)p.BH * (kE / 4) + kScanThreads - 1) / kScanThreads);
     count_launches(5);

@@ -353,11 +353,14 @@ la_status la_prefill_state_ex(const void *k, const void *v, const float *gamma,
  *   q, k, dq, dk : [B, H, N, d_k]   v, dout, dv : [B, H, N, d_v]   (element type `dtype`)
  *
  * Outputs must not overlap any input or each other.  Recomputes the forward
- * quantities it needs (no saved activations).  fp32 arithmetic on the CUDA
- * cores, chunk-parallel (chunk states, scans over chunks, per-chunk
- * gradients); per-call scratch of B*H*ceil(N/C)*d_k*(d_v+1) + B*H*N*(d_v+1)
- * floats (C = 64, or 32 when d_k or d_v is 128), stream-ordered.
- * Supported: d_k, d_v in {32, 64, 128}.
+ * quantities it needs (no saved activations).  bf16 with d_k, d_v in {32, 64}
+ * and N >= 128 runs on the tensor cores: five launches over chunks of 128
+ * tokens (chunk states, a forward scan, dq, a reverse scan, dk and dv), bf16
+ * operands with fp32 accumulation, scratch from the stream's workspace.  Other
+ * shapes and fp32: fp32 arithmetic on the CUDA cores, chunk-parallel (chunk
+ * states, scans over chunks, per-chunk gradients); per-call scratch of
+ * B*H*ceil(N/C)*d_k*(d_v+1) + B*H*N*(d_v+1) floats (C = 64, or 32 when d_k or
+ * d_v is 128), stream-ordered.  Supported: d_k, d_v in {32, 64, 128}.
  */
 la_status la_backward_causal(const void *q, const void *k, const void *v, const void *dout,
                              void *dq, void *dk, void *dv, int B, int H, int N, int d_k, int d_v,

@@ -56,6 +56,8 @@ def run_backward(q, k, v, dout, dtype, eps=1e-6):
     (4, 8, 2048, 64, 64),  # the benchmark's backward workload
     # bf16 d = 64 from 128 tokens runs on the tensor cores: one chunk, ragged tails
     (1, 2, 128, 64, 64), (2, 3, 200, 64, 64), (1, 2, 255, 64, 64), (2, 2, 1000, 64, 64), (1, 1, 1500, 64, 64),
+    # and the narrower widths on the same 64-column tiles
+    (2, 3, 300, 32, 32), (1, 2, 1000, 64, 32), (2, 2, 129, 32, 64), (4, 8, 2048, 32, 32),
 ])
 def test_backward_matches_oracle(orc, dtype, B, H, N, dk, dv):
     """One and many chunks, ragged tails, dk != dv, every supported width."""

@@ -173,3 +173,20 @@ def test_prefill_state_widths(orc, B, H, N, dk, dv, fmap, shift, decay):
                                        fmap=fmap, shift=shift)
     es, ez = errors(from_dev(S), Sr), errors(from_dev(z), zr)
     assert es["normwise"] < 1e-5 and ez["normwise"] < 1e-5, (es, ez)
+
+
+@pytest.mark.parametrize("dk,dv", [(32, 32), (32, 64), (64, 32)])
+def test_backward_widths_run_on_the_tensor_cores(dk, dv):
+    """The backward at widths up to 64 runs the five tensor-core launches (its parity
+    against the oracle is in test_gpu_backward.py)."""
+    B, H, N = 2, 3, 1000
+    gen = torch.Generator(device="cuda").manual_seed(dk * dv)
+    q, k = (torch.randn((B, H, N, dk), device="cuda", generator=gen).to(torch.bfloat16) for _ in range(2))
+    v, do = (torch.randn((B, H, N, dv), device="cuda", generator=gen).to(torch.bfloat16) for _ in range(2))
+    call = lambda: la().la_backward_causal(q, k, v, do)
+    call()
+    torch.cuda.synchronize()
+    names = kernels_of(call)
+    if not names:
+        pytest.skip("the profiler recorded no kernels")
+    assert sum("bwd_tc" in n for n in names) == 5, names
