@@ -491,9 +491,8 @@ la_status la_favor_features(const void *x, const void *w, void *phi, int B, int 
 
 // Shared steps of the FAVOR+ forwards: checks, then phi(q) and phi(k) into
 // stream-ordered scratch (*fq, *fk; [B, H, N, m] each, freed with *s).
-static la_status favor_prologue(const void *q, const void *k, const void *v, const void *o, const void *w, int B,
-                                int H, int N, int d, int dv, int m, float eps, la_dtype dtype, cudaStream_t stream,
-                                Scratch *s, void **fq, void **fk, bool *empty)
+static la_status favor_check(const void *q, const void *k, const void *v, const void *o, const void *w, int B,
+                             int H, int N, int d, int dv, int m, float eps, la_dtype dtype, bool *empty)
 {
     if (m < 0) return LA_ERR_INVALID_ARG;
     la_status st = check_forward(q, k, v, o, B, H, N, d, dv, eps, dtype, empty);
@@ -503,6 +502,16 @@ static la_status favor_prologue(const void *q, const void *k, const void *v, con
     if (!supported_dim(d) || !supported_dim(dv) || !supported_dim(m)) return LA_ERR_UNSUPPORTED;
     const size_t es = elem_size(dtype);
     if (overlaps(o, (size_t)B * H * N * dv * es, w, (size_t)m * d * es)) return LA_ERR_INVALID_ARG;
+    return LA_OK;
+}
+
+static la_status favor_prologue(const void *q, const void *k, const void *v, const void *o, const void *w, int B,
+                                int H, int N, int d, int dv, int m, float eps, la_dtype dtype, cudaStream_t stream,
+                                Scratch *s, void **fq, void **fk, bool *empty)
+{
+    la_status st = favor_check(q, k, v, o, w, B, H, N, d, dv, m, eps, dtype, empty);
+    if (st != LA_OK || *empty) return st;
+    const size_t es = elem_size(dtype);
     const size_t bytes = (size_t)B * H * N * m * es;  // a multiple of 64: both halves stay 16-byte aligned
     if ((st = s->alloc(2 * bytes, stream)) != LA_OK) return st;
     *fq = s->ptr;
@@ -545,6 +554,14 @@ la_status la_forward_noncausal_favor(const void *q, const void *k, const void *v
                                      int H, int N, int d, int dv, int m, float eps, la_dtype dtype,
                                      la_stream_t stream)
 {
+    if (dtype == LA_BF16 && d == 64 && m == 64) {  // the features inside the attention kernel
+        bool empty;
+        la_status st = favor_check(q, k, v, o, w, B, H, N, d, dv, m, eps, dtype, &empty);
+        if (st != LA_OK || empty) return st;
+        Problem p{q, k, v, o, B * H, N, d, dv, 0, eps, dtype, (cudaStream_t)stream, nullptr, H, Variant()};
+        st = noncausal_tc_favor(p, w);
+        if (st != LA_ERR_UNSUPPORTED) return st;
+    }
     Scratch s;
     void *fq = nullptr, *fk = nullptr;
     bool empty;

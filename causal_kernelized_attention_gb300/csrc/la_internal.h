@@ -104,6 +104,10 @@ la_status causal_chunks_tc(const Problem &p);
 la_status causal_cluster_tc(const Problem &p);
 // (la_tc_noncausal.cu)
 la_status noncausal_tc(const Problem &p);
+// The non-causal FAVOR+ form with the features computed in the kernel
+// (la_tc_noncausal.cu): bf16, q, k [.., 64] and W [64, 64] (m = d = 64, device,
+// 16-byte aligned), dv <= 64, N >= 128; LA_ERR_UNSUPPORTED otherwise.
+la_status noncausal_tc_favor(const Problem &p, const void *w);
 // S, z (fp32, [BH,dk,dv], [BH,dk]) = sums over N tokens on the tensor cores (bf16
 // k, v; dk, dv multiples of 8 up to 128 (on tiles of 64 or 128 columns), N >= 128);
 // overwrites S and z.  gamma (device, [H]): token t weighted by gamma[bh % H]^(N-1-t);

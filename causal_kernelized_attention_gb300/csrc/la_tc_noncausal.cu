@@ -30,9 +30,19 @@
 //    by [V | 1] (or V and W), so the state is accurate to about 2^-17 relative
 //    to fp32 phi rather than to bf16 rounding.
 //
+// FAVOR+ ("Linear Attention -- Math + Variants", Performer) with d = m = 64 runs
+// inside this kernel (kFavor): phi(x) = exp(x W^T - |x|^2 / 2) / sqrt(m) of every Q
+// and K tile replaces the tile in place.  Warp 7 issues x W^T (two N = 32 MMAs, W
+// resident in shared memory) into the unused columns of the accumulators (80..111
+// and 208..239, or 336..367 and 464..495: two buffers); the phi warps take
+// alternate tiles, warps 8-11 the even ones and 12-15 the odd ones, one thread per
+// row: the row's squared norm from shared memory, its 64 projections from TMEM,
+// the exponentials written over the row.
+//
 // Warp roles (512 threads): warps 0-3 epilogue (TMEM lane quadrant = warp),
 // warp 4 scheduler and TMA producer, warp 5 MMA issuer and TMEM owner, warp 6
-// state-image loader, warp 7 idle, warps 8-15 apply phi in shared memory.  Each
+// state-image loader, warp 7 idle (FAVOR+: the projection MMAs), warps 8-15 apply
+// phi in shared memory.  Each
 // item is published to the other roles through a small ring in shared memory.
 // Every wait is bounded (mbarriers and the ready flag alike); on expiry the CTA
 // records LA_ERR_TIMEOUT in this file's status word and winds down.
@@ -56,6 +66,7 @@ constexpr int kThreads = 512;
 constexpr int kEpiThreads = 128;  // warps 0-3
 constexpr int kTmaWarp = 4, kMmaWarp = 5, kImgWarp = 6, kPhiWarp0 = 8;
 constexpr int kPhiThreads = 256;  // warps 8-15
+constexpr int kFavorWarp = 7;     // FAVOR+: the projection MMAs
 constexpr int kRing = 4;          // item ring entries
 // Readers of each ring entry: 8 phi warps, the MMA thread, the loader, 4 epilogue warps.
 constexpr uint32_t kRingReaders = 8 + 1 + 1 + 4;
@@ -112,6 +123,7 @@ struct alignas(1024) Smem {
     uint64_t img_full[Cfg<D>::kImgs], img_empty[Cfg<D>::kImgs];
     uint64_t epi_sync, drain;
     uint64_t lo_free[2];  // state mode: the MMAs have read low-part buffer b
+    uint64_t f_full[2], f_free[2], f_drain;  // FAVOR+: projection buffer b written / read
     Item items[kRing];
     uint32_t tmem_base;
     int abort;
@@ -150,7 +162,36 @@ struct Params {
     // Feature widths (multiples of 8, at most D; output mode): q, k carry dk
     // columns, v, o dv; the tiles' columns past them are zero (see zero_cols).
     int dk, dv;
+    // FAVOR+ (kFavor): the projection W [64, 64] bf16, row r = w_r, device memory.
+    const uint16_t *favor_w;
 };
+
+// FAVOR+ projection buffers (D = 64): the columns of the accumulators past their 80
+// (S or O, then z or qz), features 0..31 and 32..63 of buffer b.
+__host__ __device__ constexpr uint32_t favor_lo(int b) { return b ? 336u : 80u; }
+__host__ __device__ constexpr uint32_t favor_hi(int b) { return b ? 464u : 208u; }
+static_assert(Cfg<64>::kAccStride == 128 && favor_lo(0) >= 64 + 16 && favor_lo(0) + 32 <= 128 &&
+                  favor_hi(0) == 128 + favor_lo(0) && favor_lo(1) == 256 + favor_lo(0) && favor_hi(1) + 32 <= 512,
+              "FAVOR+ projection buffers inside the accumulators' unused columns");
+constexpr float kFavorLog2e = 1.4426950408889634f;
+
+// phi of features [32 h, 32 h + 32) of row `row` of a [128 x 64] tile (128-byte
+// swizzled) from their projections f: 2^((f - |x|^2 / 2) log2(e) - 3), the factor
+// 1/sqrt(64) folded into the exponent; zero past the end of the sequence.
+__device__ __forceinline__ void favor_half(uint8_t *tile, int row, int h, bool live, const uint32_t (&f)[32],
+                                           float nrm)
+{
+    uint8_t *rp = tile + row * 128;
+    const float cexp = fmaf(-0.5f * kFavorLog2e, nrm, -3.0f);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        float x[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] = live ? exp2f(fmaf(__uint_as_float(f[8 * u + e]), kFavorLog2e, cexp)) : 0.f;
+        *reinterpret_cast<uint4 *>(rp + (((4 * h + u) ^ (row & 7)) << 4)) =
+            make_uint4(pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]), pack_bf16(x[4], x[5]), pack_bf16(x[6], x[7]));
+    }
+}
 
 // State mode, decayed state or another feature map: the map (elu + 1, max(x, 0) + c
 // or x + c) in fp32, times the row's weight gamma^(ebase - row) (lg = log2 gamma; 0
@@ -338,7 +379,7 @@ __device__ __forceinline__ bool epi_barrier(int *abort_flag, uint64_t *bar, uint
     return ok;
 }
 
-template <int D, bool kVar>
+template <int D, bool kVar, bool kFavor = false>
 __global__ void __launch_bounds__(512, 1)
 noncausal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                     const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_o,
@@ -381,7 +422,7 @@ noncausal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
         }
         for (int r = 0; r < kRing; ++r) {
             mbar_init(&sm.item_full[r], 1);
-            mbar_init(&sm.item_empty[r], kRingReaders);
+            mbar_init(&sm.item_empty[r], kRingReaders + (kFavor ? 1 : 0));
         }
         for (int a = 0; a < CF::kAcc; ++a) {
             mbar_init(&sm.acc_full[a], 1);
@@ -396,6 +437,11 @@ noncausal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
         mbar_init(&sm.lo_free[0], 1);
         mbar_init(&sm.lo_free[1], 1);
         mbar_init(&sm.drain, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&sm.f_full[b], 1);
+            mbar_init(&sm.f_free[b], 128);
+        }
+        mbar_init(&sm.f_drain, 1);
         sm.abort = 0;
         fence_mbar_init();
     }
@@ -406,6 +452,19 @@ noncausal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
     // Global memory only after the grids this one depends on are done (the launch
     // before may still be clearing the flags or reading the workspace).
     griddep_wait();
+    if constexpr (kFavor) {
+        static_assert(D == 64, "FAVOR+ in the kernel: d = m = 64");
+        // W into lo1 (unused outside state mode), K-major and 128-byte swizzled: the B
+        // operand of x W^T, rows 0..31 for features 0..31 and rows 32..63 (4 KB on)
+        if (tid < 128) {
+            const uint4 *w4 = reinterpret_cast<const uint4 *>(prm.favor_w);
+            for (int u = tid; u < 64 * 8; u += 128) {
+                const int row = u >> 3, ch = u & 7;
+                *reinterpret_cast<uint4 *>(sm.lo1 + row * 128 + ((ch ^ (row & 7)) << 4)) = __ldg(w4 + u);
+            }
+            fence_proxy_async_smem();
+        }
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -441,6 +500,37 @@ noncausal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
                                                          prm.N - 1 - (item.c0 + c) * kC, prm.map, prm.shift);
                     else
                         phi_tile_split<D, kPhiThreads>(sm.stage[s], b ? sm.lo1 : sm.aux + CF::kImg0, t, valid);
+                } else if constexpr (kFavor) {
+                    // tile j: warps 8-11 if j is even, 12-15 if odd; buffer j % 2
+                    const int b = j & 1, n = j >> 1;
+                    if (((warp - kPhiWarp0) >> 2) == b) {
+                        const int row = 32 * (warp & 3) + lane;
+                        const uint8_t *rp = sm.stage[s] + row * 128;
+                        float nrm = 0.f;
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) {  // any chunk order covers the row
+                            const uint4 w4 = *reinterpret_cast<const uint4 *>(rp + (((u + row) & 7) << 4));
+                            const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&wv[e]));
+                                nrm = fmaf(f.x, f.x, nrm);
+                                nrm = fmaf(f.y, f.y, nrm);
+                            }
+                        }
+                        if (!(ok = wait_bar_warp(abort_flag, &sm.f_full[b], n & 1))) break;
+                        tc_fence_after();
+                        const uint32_t tq = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+#pragma unroll 1
+                        for (int h = 0; h < 2; ++h) {
+                            uint32_t f[32];
+                            tmem_ld32(tq + (h ? favor_hi(b) : favor_lo(b)), f);
+                            tmem_ld_wait();
+                            favor_half(sm.stage[s], row, h, row < valid, f, nrm);
+                        }
+                        tc_fence_before();
+                        mbar_arrive(&sm.f_free[b]);  // both halves read from TMEM
+                    }
                 } else {
                     phi_tile<D, kPhiThreads, false, kVar>(sm.stage[s], t, valid, 0.f, 0, prm.map, prm.shift);
                     if (prm.dk < D && item.kind == kSum) zero_cols<D>(sm.stage[s], t, kPhiThreads, prm.dk);
@@ -586,6 +676,42 @@ noncausal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
             mma_commit(&sm.drain);
             const uint64_t t0 = globaltimer_ns();
             while (!mbar_try_wait(&sm.drain, 0) && globaltimer_ns() - t0 < kWaitLimitNs) {
+            }
+        }
+    } else if (kFavor && warp == kFavorWarp) {
+        // ---------------------------------------------------------------- FAVOR+ projections
+        if (lane == 0) {
+            const uint32_t wa = smem_u32(sm.lo1);
+            const uint32_t id = idesc_bf16_f32(128, 32, false, false);  // x W^T, 32 features a group
+            int j = 0;
+            bool ok = true, issued = false;
+            for (int it = 0; ok; ++it) {
+                const int r = it % kRing;
+                if (!(ok = wait_bar(abort_flag, &sm.item_full[r], (it / kRing) & 1))) break;
+                const Item item = sm.items[r];
+                mbar_arrive(&sm.item_empty[r]);
+                if (item.kind == kEnd) break;
+                for (int c = 0; c < item.nch; ++c, ++j) {
+                    const int s = j % S, b = j & 1, n = j >> 1;
+                    if (!(ok = wait_bar(abort_flag, &sm.full[s], (j / S) & 1))) break;
+                    if (n > 0 && !(ok = wait_bar(abort_flag, &sm.f_free[b], (n - 1) & 1))) break;
+                    tc_fence_after();
+                    const uint32_t xa = smem_u32(sm.stage[s]);
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk)
+                        mma_ss(tmem + favor_lo(b), kmajor(xa, kk), kmajor(wa, kk), id, kk > 0 ? 1u : 0u);
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk)
+                        mma_ss(tmem + favor_hi(b), kmajor(xa, kk), kmajor(wa + 32 * 128, kk), id, kk > 0 ? 1u : 0u);
+                    mma_commit(&sm.f_full[b]);
+                    issued = true;
+                }
+            }
+            if (issued) {  // every projection issued completes before TMEM is freed
+                mma_commit(&sm.f_drain);
+                const uint64_t t0 = globaltimer_ns();
+                while (!mbar_try_wait(&sm.f_drain, 0) && globaltimer_ns() - t0 < kWaitLimitNs) {
+                }
             }
         }
     } else if (warp == kImgWarp) {
@@ -738,7 +864,10 @@ noncausal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
                         // phi(q) z_hi and phi(q) z_lo: fused in columns D, D + 1; separate
                         // in columns D + 1, D + 2 (W rows 1 and 2)
                         uint32_t qz[32];
-                        tmem_ld32(ta + D, qz);
+                        if constexpr (kFavor)  // columns 80.. hold projections being written
+                            tmem_ld16(ta + D, *reinterpret_cast<uint32_t(*)[16]>(&qz[0]));
+                        else
+                            tmem_ld32(ta + D, qz);
                         tmem_ld_wait();
                         constexpr int zc = CF::kFused ? 0 : 1;
                         inv = (kVar && !prm.normalize)
@@ -811,8 +940,8 @@ noncausal_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
 }
 
 // ------------------------------------------------------------------ host side
-template <int D, bool kVar>
-la_status launch(const Problem &p, float *S_out = nullptr, float *z_out = nullptr)
+template <int D, bool kVar, bool kFavor = false>
+la_status launch(const Problem &p, float *S_out = nullptr, float *z_out = nullptr, const void *favor_w = nullptr)
 {
     using CF = Cfg<D>;
     // State mode (S_out given): summary items only; the q and o maps are never used
@@ -895,9 +1024,10 @@ la_status launch(const Problem &p, float *S_out = nullptr, float *z_out = nullpt
     prm.normalize = p.var.normalize;
     prm.dk = p.dk;
     prm.dv = p.dv;
+    prm.favor_w = (const uint16_t *)favor_w;
 
     const int smem = (int)sizeof(Smem<D>);
-    auto kern = noncausal_tc_kernel<D, kVar>;
+    auto kern = noncausal_tc_kernel<D, kVar, kFavor>;
     st = ensure_smem((const void *)kern, smem);
     if (st != LA_OK) return st;
     const unsigned grid = (unsigned)std::min<long long>(items, n_sm);
@@ -915,6 +1045,18 @@ la_status noncausal_tc(const Problem &p)
     const bool wide = std::max(p.dk, p.dv) > 64;
     if (!p.var.is_default()) return wide ? launch<128, true>(p) : launch<64, true>(p);
     return wide ? launch<128, false>(p) : launch<64, false>(p);
+}
+
+la_status noncausal_tc_favor(const Problem &p, const void *w)
+{
+    // FAVOR+ features in the kernel: d = m = 64 (the features replace the tiles in
+    // place), dv up to 64, the identity map on the features with the normaliser.
+    if (p.dtype != LA_BF16 || p.N < kC || p.dk != 64 || p.dv > 64 || !padded_widths_ok(p.dk, p.dv) || !w ||
+        ((uintptr_t)w & 15u) != 0)
+        return LA_ERR_UNSUPPORTED;
+    Problem q = p;
+    q.var = Variant();
+    return launch<64, false, true>(q, nullptr, nullptr, w);
 }
 
 la_status noncausal_tc_state(const void *k, const void *v, float *S, float *z, int BH, int N, int dk, int dv,

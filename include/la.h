@@ -395,7 +395,9 @@ la_status la_favor_features(const void *x, const void *w, void *phi, int B, int 
  *
  * The state has m rows (S is m x dv).  phi(q) and phi(k) are written to
  * per-call stream-ordered scratch (2 * B*H*N*m elements of `dtype`) and then
- * attended with the identity map, so each call is two launches or more.
+ * attended with the identity map, so each call is two launches or more;
+ * except the non-causal form for bf16 with d = m = 64, dv <= 64 and N >= 128,
+ * which computes the features inside its one attention launch (no scratch).
  * w must not overlap o.  Supported: d, dv, m in {32, 64, 128}; the attention
  * step runs on the tensor cores for bf16 with m = dv in {64, 128} (and, causal,
  * N >= 128), on the CUDA cores otherwise.  m outside the

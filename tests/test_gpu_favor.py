@@ -105,6 +105,10 @@ def test_causal_favor(orc, dtype, B, H, N, d, dv, m, chunk):
     ("bf16", 2, 3, 1000, 64, 64, 64), ("bf16", 1, 4, 3000, 128, 128, 128), ("bf16", 2, 2, 500, 64, 128, 128),
     ("bf16", 2, 3, 300, 64, 32, 128), ("f32", 2, 3, 300, 64, 64, 64),
     ("bf16", 8, 12, 4096, 64, 64, 64),  # the benchmark's FAVOR+ non-causal workload
+    # d = m = 64 computes the features inside the attention kernel: one chunk, ragged
+    # tails, many one-chunk heads, several key splits per head, dv = 32
+    ("bf16", 2, 3, 128, 64, 64, 64), ("bf16", 2, 3, 129, 64, 64, 64), ("bf16", 64, 16, 128, 64, 64, 64),
+    ("bf16", 4, 40, 4173, 64, 64, 64), ("bf16", 2, 3, 1000, 64, 32, 64), ("bf16", 1, 2, 20000, 64, 64, 64),
 ])
 def test_noncausal_favor(orc, dtype, B, H, N, d, dv, m):
     q, k, v, w = inputs(23000 + N + d + dv + m, B, H, N, d, dv, m, dtype)
@@ -203,3 +207,28 @@ def test_causal_favor_first_row_and_graph_replay(orc):
     torch.cuda.synchronize()
     assert la().la_get_device_status() == 0
     assert torch.equal(out, eager)
+
+
+def test_noncausal_favor_features_in_the_attention_kernel():
+    """bf16 with d = m = 64: one launch of the non-causal kernel, no separate
+    features kernel (a profiler pass over one call)."""
+    from torch.profiler import ProfilerActivity, profile
+    B, H, N, d = 2, 3, 1000, 64
+    gen = torch.Generator(device="cuda").manual_seed(3)
+    q, k, v = [(0.5 * torch.randn((B, H, N, d), device="cuda", generator=gen)).to(torch.bfloat16) for _ in range(3)]
+    w = torch.randn((d, d), device="cuda", generator=gen).to(torch.bfloat16)
+    call = lambda: la().la_forward_noncausal_favor(q, k, v, w)
+    call()
+    torch.cuda.synchronize()
+    names = []
+    for _ in range(2):  # a first profiler session can come back empty
+        with profile(activities=[ProfilerActivity.CUDA]) as prof:
+            call()
+            torch.cuda.synchronize()
+        names = [e.name for e in prof.events() if e.device_type == torch.autograd.DeviceType.CUDA]
+        if names:
+            break
+    if not names:
+        pytest.skip("the profiler recorded no kernels")
+    assert any("noncausal_tc_kernel" in n for n in names), names
+    assert not any("favor_tc_kernel" in n for n in names), names
