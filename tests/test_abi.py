@@ -234,6 +234,10 @@ def test_favor_validation(lib):
     assert fc(q, k, v, o, w, 1, 2, 16, 64, 64, 64, 128, ctypes.c_float(-1.0), 1, None) == INVALID
     assert fc(None, None, None, None, None, 1, 2, 0, 64, 64, 64, 128, e, 1, None) == OK
     assert fn(q, k, v, o, None, 1, 2, 16, 64, 64, 64, e, 1, None) == INVALID
+    # bf16 with d = m = 64 takes the in-kernel features path: the same checks first
+    assert fn(q, k, v, o, M, 1, 2, 16, 64, 64, 64, e, 1, None) == MISALIGNED
+    assert fn(q, k, v, o, o + 64, 1, 2, 16, 64, 64, 64, e, 1, None) == INVALID     # w over o
+    assert fn(q, k, v, o, w, 1, 2, 16, 64, 64, 64, ctypes.c_float(-1.0), 1, None) == INVALID
     assert fn(q, k, v, o, w, 1, 2, 16, 64, 32, 256, e, 1, None) == UNSUPPORTED
     assert fn(q, k, v, q + 64, w, 1, 2, 16, 64, 64, 64, e, 1, None) == INVALID      # o over q
     assert fn(None, None, None, None, None, 0, 2, 16, 64, 64, 64, e, 1, None) == OK
