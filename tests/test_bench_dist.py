@@ -1,6 +1,7 @@
 """Host logic of bench.py on CPU: the multi-rank timed region (gloo, world size
 2: max-over-ranks reduction and barrier), the whole-job throughput, the
-reference arm printing on rank 0 only, and the clock record's sample selection."""
+reference arm printing on rank 0 only, the clock record's sample selection, and
+the guard that keeps a profile's DRAM traffic only while its sources match."""
 import os
 import socket
 import subprocess
@@ -83,3 +84,24 @@ def test_clock_sampler_uses_samples_inside_the_timed_window():
     # no sample inside the window: the median of all samples
     c = bench.ClockSampler.summarise(text, (0.0, 1.0), 20)
     assert c["samples_in_timed_region"] == 0 and c["sm_mhz"] == (1800 + 2055) / 2
+
+
+def test_profile_traffic_only_while_the_source_matches(tmp_path, monkeypatch):
+    """roofline.traffic comes from a committed ncu summary only while the SHA-256 of
+    the kernel sources it names still matches: a changed source gives None."""
+    import hashlib
+    sys.path.insert(0, ROOT)
+    import bench
+    (tmp_path / "profiles").mkdir()
+    (tmp_path / "k").mkdir()
+    src_a, src_b = tmp_path / "k" / "a.cu", tmp_path / "k" / "b.cuh"
+    src_a.write_bytes(b"kernel a\n")
+    src_b.write_bytes(b"header b\n")
+    sha = hashlib.sha256(src_a.read_bytes() + src_b.read_bytes()).hexdigest()
+    (tmp_path / "profiles" / "demo.md").write_text(
+        "# demo\n\ntraffic_bytes_per_launch: 12345\nsource_file: k/a.cu, k/b.cuh\nsource_sha256: %s\n" % sha)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.ncu_traffic("demo") == 12345
+    assert bench.ncu_traffic("missing") is None
+    src_b.write_bytes(b"header b, changed\n")
+    assert bench.ncu_traffic("demo") is None
